@@ -1,0 +1,162 @@
+/*
+ * conv_oracle.c -- plain CPU oracle for INT8 2-D convolution forward
+ * propagation with integer accumulation.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link or
+ * call this file; only the tests, the package smoke check and the CPU-baseline
+ * leg of the benchmark use it.  It shares no code, header or table with the
+ * CUDA library.
+ *
+ * What it computes (cuDNN documentation, "Convolutions", section
+ * "Convolution Fprop": response = image * filter, with the argument list of its
+ * "Python API" subsection: pre_padding, post_padding, stride, dilation,
+ * convolution_mode, compute_data_type), written out as the definition:
+ *
+ *   for n < N, k < K, p < P, q < Q:
+ *     acc = sum over c < C, r < R, s < S of X[n,c,h,w] * W[k,c,r',s']
+ *       h = p*stride_h - pre_h + r*dil_h,  w = q*stride_w - pre_w + s*dil_w
+ *       terms whose (h, w) lies outside [0,H) x [0,W) are zero (zero padding)
+ *       (r', s') = (r, s) in CROSS_CORRELATION, (R-1-r, S-1-s) in CONVOLUTION
+ *     Y[n,k,p,q] = acc, then + bias[k] (two's-complement int32 wrap-around),
+ *                  then max(0, .) if ReLU is requested.
+ *
+ *   P = floor((H + pre_h + post_h - dil_h*(R-1) - 1) / stride_h) + 1, and Q
+ *   likewise.  This size rule is not printed on the pages; it is the reading
+ *   that reproduces both worked shapes they give (5x5 image, 3x3 filter ->
+ *   3x3 output in the forum thread "INT8 convolution using cuDNN Python
+ *   Frontend"; 32x32 -> 30x30 in "Building a From-Scratch INT8 Strided
+ *   Convolution Kernel", section "Correctness Testing").
+ *
+ * The accumulator is int64 and the loop order is n, k, p, q, c, r, s: the
+ * seven-loop shape of the naive loop in "Building a From-Scratch INT8 Strided
+ * Convolution Kernel", section "Step 2: Implement the Naive Strided Loop",
+ * without that listing's slips (it indexes the filter's output channel with
+ * the channel stride, has no padding or dilation, and clamps to int8).  Every
+ * element address is sum(index_i * stride_i) over the tensor's own strides,
+ * so every layout goes through the same code.
+ *
+ * An accumulator outside int32 is reported (return value 2) instead of being
+ * wrapped: the int32 output type of the compute_data_type=INT32 reading
+ * cannot hold it.
+ */
+#include <stdint.h>
+#include <stddef.h>
+
+#define ORACLE_OK 0
+#define ORACLE_BAD_ARGS 1
+#define ORACLE_ACC_OUT_OF_INT32 2
+
+typedef struct {
+    int64_t pre[2], post[2], stride[2], dil[2];
+    int32_t mode;   /* 0 cross-correlation, 1 convolution */
+    int32_t relu;   /* 1: max(0, .) after the bias */
+} oracle_params;
+
+int64_t oracle_out_extent(int64_t in, int64_t pre, int64_t post, int64_t taps,
+                          int64_t dil, int64_t stride) {
+    int64_t span = in + pre + post - dil * (taps - 1) - 1;
+    if (stride < 1 || span < 0) return 0;
+    return span / stride + 1;
+}
+
+/* One output element, straight from the definition above. */
+static int one_output(const int8_t *x, const int64_t *xd, const int64_t *xs,
+                      const int8_t *w, const int64_t *wd, const int64_t *ws,
+                      const int32_t *bias, const oracle_params *pp,
+                      int64_t n, int64_t k, int64_t p, int64_t q, int32_t *out) {
+    const int64_t C = xd[1], H = xd[2], W = xd[3];
+    const int64_t R = wd[2], S = wd[3];
+    int64_t acc = 0;
+    for (int64_t c = 0; c < C; ++c) {
+        for (int64_t r = 0; r < R; ++r) {
+            for (int64_t s = 0; s < S; ++s) {
+                int64_t h = p * pp->stride[0] - pp->pre[0] + r * pp->dil[0];
+                int64_t ww = q * pp->stride[1] - pp->pre[1] + s * pp->dil[1];
+                if (h < 0 || h >= H || ww < 0 || ww >= W) continue; /* zero padding */
+                int64_t rf = pp->mode ? (R - 1 - r) : r;
+                int64_t sf = pp->mode ? (S - 1 - s) : s;
+                int64_t xv = x[n * xs[0] + c * xs[1] + h * xs[2] + ww * xs[3]];
+                int64_t wv = w[k * ws[0] + c * ws[1] + rf * ws[2] + sf * ws[3]];
+                acc += xv * wv;
+            }
+        }
+    }
+    if (acc > INT32_MAX || acc < INT32_MIN) return ORACLE_ACC_OUT_OF_INT32;
+    int32_t v = (int32_t)acc;
+    if (bias) v = (int32_t)((uint32_t)v + (uint32_t)bias[k]);
+    if (pp->relu && v < 0) v = 0;
+    *out = v;
+    return ORACLE_OK;
+}
+
+static int check_args(const int64_t *xd, const int64_t *wd, const int64_t *yd,
+                      const oracle_params *pp) {
+    if (xd[1] != wd[1]) return ORACLE_BAD_ARGS;
+    if (yd[0] != xd[0] || yd[1] != wd[0]) return ORACLE_BAD_ARGS;
+    for (int i = 0; i < 2; ++i)
+        if (pp->stride[i] < 1 || pp->dil[i] < 1 || pp->pre[i] < 0 || pp->post[i] < 0)
+            return ORACLE_BAD_ARGS;
+    if (yd[2] != oracle_out_extent(xd[2], pp->pre[0], pp->post[0], wd[2], pp->dil[0], pp->stride[0]))
+        return ORACLE_BAD_ARGS;
+    if (yd[3] != oracle_out_extent(xd[3], pp->pre[1], pp->post[1], wd[3], pp->dil[1], pp->stride[1]))
+        return ORACLE_BAD_ARGS;
+    return ORACLE_OK;
+}
+
+/* Full output.  x: logical [N,C,H,W]; w: [K,C,R,S]; y: [N,K,P,Q]; strides in
+ * elements.  bias may be NULL.  The (n, k) pairs are independent, so they are
+ * shared out over OpenMP threads when the build enables it. */
+int oracle_conv_fprop(const int8_t *x, const int64_t *xd, const int64_t *xs,
+                      const int8_t *w, const int64_t *wd, const int64_t *ws,
+                      int32_t *y, const int64_t *yd, const int64_t *ys,
+                      const int32_t *bias, const oracle_params *pp) {
+    int rc = check_args(xd, wd, yd, pp);
+    if (rc) return rc;
+    const int64_t N = yd[0], K = yd[1], P = yd[2], Q = yd[3];
+    int bad = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic) reduction(| : bad)
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t k = 0; k < K; ++k) {
+            for (int64_t p = 0; p < P; ++p) {
+                for (int64_t q = 0; q < Q; ++q) {
+                    int32_t v = 0;
+                    if (one_output(x, xd, xs, w, wd, ws, bias, pp, n, k, p, q, &v)) bad = 1;
+                    y[n * ys[0] + k * ys[1] + p * ys[2] + q * ys[3]] = v;
+                }
+            }
+        }
+    }
+    return bad ? ORACLE_ACC_OUT_OF_INT32 : ORACLE_OK;
+}
+
+/* Selected outputs only: idx holds count rows of (n, k, p, q); out[i] gets
+ * Y at row i.  Used at sizes where the full output is too slow on the CPU. */
+int oracle_conv_fprop_points(const int8_t *x, const int64_t *xd, const int64_t *xs,
+                             const int8_t *w, const int64_t *wd, const int64_t *ws,
+                             const int64_t *yd, const int32_t *bias,
+                             const oracle_params *pp, const int64_t *idx,
+                             int64_t count, int32_t *out) {
+    int rc = check_args(xd, wd, yd, pp);
+    if (rc) return rc;
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (int64_t i = 0; i < count; ++i) {
+        const int64_t *t = idx + 4 * i;
+        if (t[0] < 0 || t[0] >= yd[0] || t[1] < 0 || t[1] >= yd[1] ||
+            t[2] < 0 || t[2] >= yd[2] || t[3] < 0 || t[3] >= yd[3]) {
+            bad |= 1;
+            continue;
+        }
+        if (one_output(x, xd, xs, w, wd, ws, bias, pp, t[0], t[1], t[2], t[3], out + i)) bad |= 2;
+    }
+    if (bad & 1) return ORACLE_BAD_ARGS;
+    return bad ? ORACLE_ACC_OUT_OF_INT32 : ORACLE_OK;
+}
+
+/* Number of threads the OpenMP runtime would use (1 without OpenMP). */
+#ifdef _OPENMP
+#include <omp.h>
+int oracle_num_threads(void) { return omp_get_max_threads(); }
+#else
+int oracle_num_threads(void) { return 1; }
+#endif
