@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Throughput of INT8 conv2d forward propagation (int32 results) on GB300.
+
+One step = one full conv_fprop of the workload (filter repack kernel + the
+tcgen05 implicit-GEMM kernel, which computes the output with bias/ReLU fused
+when the workload asks for them).  Default workload: N=32, C=256, 56x56 image,
+K=256, 3x3 filter, stride 1, padding 1, NHWC image / KRSC filter / NHWC output.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Throughput is 2*N*K*P*Q*C*R*S / time in
+TOPS.  Inputs stay resident in HBM; successive steps rotate over several
+input/output sets whose total exceeds the 129 MB L2, so every step starts
+with cold caches.  Under torchrun each rank runs its own copy of the workload
+(weak scaling, no collective on the data path); the elapsed time is the max
+over ranks.  ``--impl reference`` times the CPU oracle on the host cores
+instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "INT8 conv fprop TOPS (2NKPQCRS/s) and % of GB300 dense INT8 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DOMINANT_KERNEL_SRC = os.path.join(ROOT, "int8_conv2d_fprop_gb300", "csrc", "igemm.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "igemm_traffic.json")
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c3_3x3_large", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------- ranks
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (a host-side timing reduction only)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------- peaks, clocks
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            return d, "measured"
+        except (OSError, ValueError):
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _peak_value(peaks: dict, keys):
+    for k in keys:
+        v = peaks.get(k)
+        if isinstance(v, (int, float)) and v > 0:
+            return float(v)
+        if isinstance(v, dict):
+            for kk in ("value", "tflops", "gbs"):
+                if isinstance(v.get(kk), (int, float)):
+                    return float(v[kk])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str, period_ms: int = 50):
+        self.gpu_id, self.period_ms = gpu_id, period_ms
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms", str(self.period_ms)], stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        with open(self.tmp.name) as f:
+            lines = [ln.strip() for ln in f if ln.strip()]
+        os.unlink(self.tmp.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------- oracle timing
+def time_oracle_sample(cfg, seconds: float, x, w, b):
+    """Time the CPU oracle on a random sample of output points sized to take
+    about ``seconds``; returns (TOPS, threads, description)."""
+    import oracle
+    oracle.build()
+    xf, xs = synth.place(x, cfg.x_layout)
+    wf, ws = synth.place(w, cfg.w_layout)
+    rng = np.random.default_rng(1)
+
+    def pts(n):
+        return np.stack([rng.integers(0, d, n) for d in cfg.y_dims], axis=1)
+
+    red = cfg.C * cfg.R * cfg.S
+    probe = pts(max(64, int(2e7 // red)))
+    t0 = time.perf_counter()
+    oracle.conv_fprop_points(xf, cfg.x_dims, xs, wf, cfg.w_dims, ws, probe, cfg.pre, cfg.post, cfg.stride,
+                             cfg.dilation, cfg.mode, b, cfg.relu)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    n = max(256, int(len(probe) * seconds / dt))
+    n = min(n, int(np.prod(cfg.y_dims)))
+    sample = pts(n)
+    t0 = time.perf_counter()
+    oracle.conv_fprop_points(xf, cfg.x_dims, xs, wf, cfg.w_dims, ws, sample, cfg.pre, cfg.post, cfg.stride,
+                             cfg.dilation, cfg.mode, b, cfg.relu)
+    dt = time.perf_counter() - t0
+    tops = 2.0 * n * red / dt / 1e12
+    desc = (f"{n} randomly drawn output elements of the workload ({n * red * 2 / 1e9:.2f} G ops, "
+            f"{100.0 * n / np.prod(cfg.y_dims):.3f}% of the outputs), seven-loop oracle, {dt:.1f} s")
+    return tops, oracle.num_threads(), desc, n
+
+
+# ---------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+
+    import int8_conv2d_fprop_gb300 as ic
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    cfg = synth.CONFIGS[args.workload]
+    x, w, b = synth.make_inputs(cfg)
+    xf, xs = synth.place(x, cfg.x_layout)
+    wf, ws = synth.place(w, cfg.w_layout)
+    ystr = synth.packed_strides(cfg.y_dims, cfg.y_layout)
+    ysz = int(np.prod(cfg.y_dims))
+    set_bytes = xf.size + ysz * 4
+    nsets = max(2, int(np.ceil(3 * L2_BYTES / set_bytes)) + 1)
+    xs_dev = [torch.from_numpy(xf).to(dev) for _ in range(nsets)]
+    ys_dev = [torch.empty(ysz, dtype=torch.int32, device=dev) for _ in range(nsets)]
+    w_dev = torch.from_numpy(wf).to(dev)
+    b_dev = torch.from_numpy(b).to(dev) if b is not None else None
+    xd = ic.TensorDesc.make(ic.CONV_INT8, cfg.x_dims, xs, xf.size)
+    wd = ic.TensorDesc.make(ic.CONV_INT8, cfg.w_dims, ws, wf.size)
+    yd = ic.TensorDesc.make(ic.CONV_INT32, cfg.y_dims, ystr, ysz * 4)
+    p = ic.Params.make(cfg.pre, cfg.post, cfg.stride, cfg.dilation, cfg.mode, cfg.bias, cfg.relu)
+    algo = ic.plan(xd, wd, yd, p)
+    ws_bytes = ic.workspace_size(xd, wd, yd, p)
+    work = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    bias_ptr = b_dev.data_ptr() if b_dev is not None else 0
+
+    def step(i, ev_a=None, ev_b=None):
+        s = i % nsets
+        st = ic.pack_filter_raw(xd, wd, w_dev.data_ptr(), yd, p, work.data_ptr(), ws_bytes, sh)
+        if st:
+            raise ic.ConvError(st, "pack filter")
+        if ev_a is not None:
+            ev_a.record(stream)
+        st = ic.conv_fprop_prepacked_raw(xd, xs_dev[s].data_ptr(), wd, w_dev.data_ptr(), yd, ys_dev[s].data_ptr(),
+                                         bias_ptr, p, work.data_ptr(), ws_bytes, sh)
+        if st:
+            raise ic.ConvError(st, "conv")
+        if ev_b is not None:
+            ev_b.record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    status = ic.device_status(sh)
+    if status:
+        raise ic.ConvError(status, "warm-up")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = str(local)
+    sampler = ClockSampler(uuid)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.15)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i, *evs[i])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    barrier(world)
+    elapsed_ms = e0.elapsed_time(e1)
+    main_ms = [a.elapsed_time(bb) for a, bb in evs]
+    status = ic.device_status(sh)
+    if status:
+        raise ic.ConvError(status, "timed region")
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+    kernel_ms = statistics.mean(main_ms)
+
+    # end to end through the public API: pinned host inputs copied in, result read back
+    e2e = None
+    if args.e2e_steps > 0:
+        xh = torch.from_numpy(xf).pin_memory()
+        wh = torch.from_numpy(wf).pin_memory()
+        bh = torch.from_numpy(b).pin_memory() if b is not None else None
+        yh = torch.empty(ysz, dtype=torch.int32).pin_memory()
+        xdv = torch.as_strided(xs_dev[0], cfg.x_dims, xs)
+        wdv = torch.as_strided(w_dev, cfg.w_dims, ws)
+        ydv = torch.as_strided(ys_dev[0], cfg.y_dims, ystr)
+
+        def e2e_step():
+            xs_dev[0].copy_(xh, non_blocking=True)
+            w_dev.copy_(wh, non_blocking=True)
+            if b_dev is not None:
+                b_dev.copy_(bh, non_blocking=True)
+            ic.conv_fprop(xdv, wdv, b_dev, pre_padding=cfg.pre, post_padding=cfg.post, stride=cfg.stride,
+                          dilation=cfg.dilation, mode=cfg.mode, relu=cfg.relu, out=ydv, workspace=work)
+            yh.copy_(ys_dev[0], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        f1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, dev) / args.e2e_steps
+        status = ic.device_status(sh)
+        if status:
+            raise ic.ConvError(status, "end-to-end")
+        h2d = xf.size + wf.size + (b.size * 4 if b is not None else 0)
+        e2e = {"value": round(world * cfg.ops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TOPS",
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(ysz * 4),
+               "api": "int8_conv2d_fprop_gb300.conv_fprop (pinned host -> device copies, D2H of the output)"}
+
+    ms_per_step = elapsed_ms / args.steps
+    value = world * cfg.ops / (ms_per_step * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    bf16 = _peak_value(peaks, ("bf16_tflops", "bf16_dense_tflops"))
+    if bf16 is None:
+        bf16, peak_src = FALLBACK_PEAKS["bf16_tflops"], "fallback"
+    achieved = cfg.ops / (kernel_ms * 1e-3) / 1e12
+    traffic = None
+    if os.path.exists(TRAFFIC_FILE):
+        try:
+            with open(TRAFFIC_FILE) as f:
+                tr = json.load(f)
+            src_sha = hashlib.sha256(open(DOMINANT_KERNEL_SRC, "rb").read()).hexdigest()
+            if tr.get("kernel_src_sha256") == src_sha and tr.get("workload") == args.workload:
+                traffic = tr.get("dram_bytes_per_launch")
+        except (OSError, ValueError):
+            traffic = None
+    roofline = {
+        "bound": "tensor",
+        "kernel": "igemm_conv_kernel" if algo == ic.ALGO_IMPLICIT_GEMM else ic.ALGO_NAMES.get(algo),
+        "achieved": round(achieved, 2), "peak": bf16, "unit": "TFLOP/s",
+        "frac": round(achieved / bf16, 4), "traffic": traffic,
+        "peak_source": f"{peak_src} bf16 dense (f16 operands run at the bf16 rate; sm_103a has no integer tensor MMA)",
+        "kernel_ms": round(kernel_ms, 5),
+        "algorithmic_bytes": cfg.algorithmic_bytes(),
+        "hbm_floor_ms": round(cfg.algorithmic_bytes() / (_peak_value(peaks, ("hbm_gbs",)) or 6800.0) / 1e6, 5),
+    }
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tops, threads, desc, _ = time_oracle_sample(cfg, args.cpu_seconds, x, w, b)
+        cpu = {"value": round(tops, 6), "unit": "TOPS", "cores": threads, "kind": "oracle", "sample": desc}
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8 x int8 -> int32 (exact, f16 tensor MMA)",
+        "data": "synthetic (splitmix64 seeded int8 uniform[-128,127])",
+        "config": {"workload": f"{cfg.name}: N={cfg.N} C={cfg.C} H={cfg.H} W={cfg.W} K={cfg.K} R={cfg.R} "
+                               f"S={cfg.S} stride={cfg.stride} pad={cfg.pre}/{cfg.post} dil={cfg.dilation} "
+                               f"mode={'conv' if cfg.mode else 'xcorr'} x={cfg.x_layout} w={cfg.w_layout} "
+                               f"y={cfg.y_layout} bias={cfg.bias} relu={cfg.relu}",
+                   "ops_per_step": cfg.ops, "algo": ic.ALGO_NAMES.get(algo),
+                   "l2": f"rotating {nsets} resident input/output sets ({nsets * set_bytes / 1e6:.0f} MB > 129 MB L2)",
+                   "parallelism": f"replicas x{world}, no data-path collective"},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps if algo == ic.ALGO_IMPLICIT_GEMM else args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------- reference arm
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    cfg = synth.CONFIGS[args.workload]
+    x, w, b = synth.make_inputs(cfg)
+    import oracle
+    oracle.build()
+    xf, xs = synth.place(x, cfg.x_layout)
+    wf, ws = synth.place(w, cfg.w_layout)
+    # size each step so that warm-up + timed steps take about 90 s in total
+    per_step_s = max(0.05, min(2.0, 90.0 / max(1, args.steps + args.warmup)))
+    _, threads, _, npts = time_oracle_sample(cfg, per_step_s, x, w, b)
+    rng = np.random.default_rng(2)
+    sample = np.stack([rng.integers(0, d, npts) for d in cfg.y_dims], axis=1)
+
+    def step():
+        oracle.conv_fprop_points(xf, cfg.x_dims, xs, wf, cfg.w_dims, ws, sample, cfg.pre, cfg.post, cfg.stride,
+                                 cfg.dilation, cfg.mode, b, cfg.relu)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    red = cfg.C * cfg.R * cfg.S
+    value = 2.0 * npts * red * args.steps / dt / 1e12
+    desc = (f"each step: {npts} randomly drawn output elements of the workload "
+            f"({2 * npts * red / 1e9:.3f} G ops) by the seven-loop CPU oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8 x int8 -> int64 -> int32",
+        "data": "synthetic (splitmix64 seeded int8 uniform[-128,127])",
+        "config": {"workload": cfg.name, "ops_per_step_sampled": int(2 * npts * red)},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TOPS", "kind": "oracle", "cores": threads,
+                         "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,215 @@
+/*
+ * int8conv.h -- C ABI of the GB300 (sm_103a) INT8 2-D convolution forward
+ * propagation library, libint8conv.so.
+ *
+ * The operation is conv_fprop as defined in the cuDNN documentation page
+ * "Convolutions", section "Convolution Fprop" (response = image * filter),
+ * with the arguments of its "Python API" list: image, weight, pre_padding,
+ * post_padding, stride, dilation, convolution_mode, compute_data_type; the
+ * "symmetric-padding overload" (padding in place of pre/post) is
+ * conv_params_set_symmetric_padding below.  Tensors are described as in the
+ * forum thread "INT8 convolution using cuDNN Python Frontend": logical dims
+ * plus one element stride per logical dim.
+ *
+ * Semantics (integer arithmetic throughout, exact):
+ *   Y[n,k,p,q] = sum_{c,r,s} X[n,c,h,w] * W[k,c,r',s']   (+ bias[k]) (ReLU)
+ *     h = p*stride[0] - pre_padding[0] + r*dilation[0]
+ *     w = q*stride[1] - pre_padding[1] + s*dilation[1]
+ *     taps outside the image contribute 0 (zero padding)
+ *     (r',s') = (r,s) for CONV_CROSS_CORRELATION,
+ *               (R-1-r, S-1-s) for CONV_CONVOLUTION (the filter flipped in
+ *               both spatial axes; channels are not flipped)
+ *     P = floor((H + pre[0] + post[0] - dilation[0]*(R-1) - 1) / stride[0]) + 1
+ *     Q likewise with index 1.
+ *   The accumulator is exact: the validator rejects shapes for which
+ *   C*R*S*2^14 could exceed 2^31-1.  The bias is added with two's-complement
+ *   int32 wrap-around, then ReLU is max(0, .).
+ *
+ * Ownership: the caller owns every buffer and the stream.  conv_fprop never
+ * allocates and never synchronises; all work is queued on `stream`.  The
+ * library keeps one small device status word per device (see
+ * conv_device_status) and nothing else between calls.
+ *
+ * Errors: every entry point returns a conv_status; nothing is thrown across
+ * the ABI.  Descriptors are validated on every call before anything is
+ * launched.  Kernel launch failures give CONV_ERR_CUDA.  A kernel whose
+ * internal wait runs out of time records CONV_ERR_DEVICE_TIMEOUT in the
+ * device status word and returns early; conv_device_status reports it.
+ *
+ * Thread safety: all entry points are reentrant; concurrent calls on
+ * different streams are independent (they share only the status word).
+ */
+#ifndef INT8CONV_H
+#define INT8CONV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CONV_OK = 0,
+    CONV_ERR_NULL_PTR = 1,            /* a required pointer is NULL */
+    CONV_ERR_RANK = 2,                /* a descriptor's rank is not 4 */
+    CONV_ERR_DTYPE = 3,               /* image/filter not INT8, output not INT32 */
+    CONV_ERR_SHAPE_MISMATCH = 4,      /* C, K, N or the output dims disagree */
+    CONV_ERR_BAD_STRIDES = 5,         /* non-positive stride of a dim > 1, or elements alias */
+    CONV_ERR_BUFFER_TOO_SMALL = 6,    /* descriptor's capacity_bytes below its extent */
+    CONV_ERR_BAD_PARAM = 7,           /* stride/dilation < 1, padding < 0, empty output, bad mode */
+    CONV_ERR_OVERFLOW_RISK = 8,       /* C*R*S*2^14 > 2^31-1: int32 could overflow */
+    CONV_ERR_UNSUPPORTED_COMPUTE = 9, /* compute_dtype other than CONV_INT32 */
+    CONV_ERR_ALIGNMENT = 10,          /* a forced algorithm cannot take these pointers/strides */
+    CONV_ERR_CUDA = 11,               /* a CUDA runtime call failed */
+    CONV_ERR_DEVICE_TIMEOUT = 12,     /* a kernel gave up waiting (see conv_device_status) */
+    CONV_ERR_WORKSPACE = 13,          /* workspace NULL or smaller than conv_fprop_workspace_size */
+    CONV_ERR_UNSUPPORTED_DEVICE = 14, /* the current device is not sm_103 */
+    CONV_ERR_OVERLAP = 15,            /* output bytes overlap an input or the workspace */
+    CONV_ERR_TOO_LARGE = 16           /* an extent or offset exceeds the library's index range */
+} conv_status;
+
+typedef enum { CONV_INT8 = 1, CONV_INT32 = 2 } conv_dtype;
+
+typedef enum { CONV_CROSS_CORRELATION = 0, CONV_CONVOLUTION = 1 } conv_mode;
+
+/* Algorithm selection; CONV_ALGO_AUTO lets the planner choose. */
+typedef enum {
+    CONV_ALGO_AUTO = 0,
+    CONV_ALGO_IMPLICIT_GEMM = 1, /* tcgen05 tensor-core implicit GEMM */
+    CONV_ALGO_DIRECT_DP4A = 2,   /* CUDA-core direct kernel, 4-way int8 dot products */
+    CONV_ALGO_DIRECT_GENERIC = 3 /* CUDA-core direct kernel, any strides */
+} conv_algo;
+
+/* Epilogue flags (bit set). */
+#define CONV_EPILOGUE_BIAS 1u /* add int32 bias[k] */
+#define CONV_EPILOGUE_RELU 2u /* max(0, .) after the bias */
+
+/*
+ * Tensor descriptor.  dims and strides are in LOGICAL order: [N,C,H,W] for
+ * the image and output ([N,K,P,Q]), [K,C,R,S] for the filter.  strides are in
+ * elements (not bytes), one per logical dim, as in the forum thread's
+ * graph.tensor(dim=..., stride=...).  The stride of a dim of extent 1 is
+ * never multiplied by a non-zero index and is ignored.  capacity_bytes is the
+ * size of the buffer behind the pointer; the largest addressed element must
+ * lie inside it.
+ */
+typedef struct {
+    int32_t dtype;          /* conv_dtype */
+    int32_t rank;           /* must be 4 */
+    int64_t dims[4];
+    int64_t strides[4];
+    uint64_t capacity_bytes;
+} conv_tensor_desc;
+
+/* conv_fprop attributes (cuDNN "Convolutions": Conv_fprop_attributes setters
+ * and the Python argument list).  Index 0 is the H axis, index 1 the W axis. */
+typedef struct {
+    int64_t pre_padding[2];
+    int64_t post_padding[2];
+    int64_t stride[2];
+    int64_t dilation[2];
+    int32_t mode;          /* conv_mode */
+    int32_t compute_dtype; /* must be CONV_INT32 */
+    uint32_t epilogue;     /* CONV_EPILOGUE_* bits */
+    int32_t algo;          /* conv_algo */
+} conv_fprop_params;
+
+/* Fill *p with: no padding, stride 1, dilation 1, cross-correlation,
+ * compute INT32, no epilogue, automatic algorithm. */
+void conv_params_init(conv_fprop_params *p);
+
+/* The symmetric-padding overload: pre_padding = post_padding = pad. */
+void conv_params_set_symmetric_padding(conv_fprop_params *p, const int64_t pad[2]);
+
+/* Stride calculator: fill d for a packed tensor.  layout is one of "NCHW",
+ * "NHWC" (image/output) or "KCRS", "KRSC" (filter); dims are logical.
+ * capacity_bytes is set to the packed size.  Returns CONV_ERR_BAD_PARAM for
+ * an unknown layout or a non-positive dim. */
+conv_status conv_tensor_desc_packed(conv_tensor_desc *d, int32_t dtype, const int64_t dims[4],
+                                    const char *layout);
+
+/* Output dims [N,K,P,Q] for image x, filter w and params p. */
+conv_status conv_fprop_output_dims(const conv_tensor_desc *x, const conv_tensor_desc *w,
+                                   const conv_fprop_params *p, int64_t out_dims[4]);
+
+/* Full host-side validation of a call (no device work).  bias_elems is the
+ * number of int32 elements behind the bias pointer (ignored unless the bias
+ * flag is set; must be >= K when it is). */
+conv_status conv_fprop_validate(const conv_tensor_desc *x, const conv_tensor_desc *w,
+                                const conv_tensor_desc *y, const conv_fprop_params *p,
+                                int64_t bias_elems);
+
+/* Algorithm the planner would run for this call (after validation). */
+conv_status conv_fprop_plan(const conv_tensor_desc *x, const conv_tensor_desc *w,
+                            const conv_tensor_desc *y, const conv_fprop_params *p,
+                            int32_t *algo_out);
+
+/* Bytes of device workspace conv_fprop needs for this call (0 for the direct
+ * kernels; the repacked half-precision filter, plus a channels-last copy of
+ * the image when its strides do not allow direct loads, for the implicit
+ * GEMM).  The caller allocates it, 256-byte aligned.  The size assumes a
+ * 16-byte-aligned image pointer (as every cudaMalloc or PyTorch allocation
+ * is); with a misaligned one the image needs the copy too, and conv_fprop
+ * returns CONV_ERR_WORKSPACE if the workspace cannot hold it. */
+conv_status conv_fprop_workspace_size(const conv_tensor_desc *x, const conv_tensor_desc *w,
+                                      const conv_tensor_desc *y, const conv_fprop_params *p,
+                                      size_t *bytes);
+
+/*
+ * Y = conv_fprop(X, W) on `stream` (a cudaStream_t; NULL = legacy default).
+ * x_dev, w_dev, y_dev, bias_dev and workspace are device pointers on the
+ * current device.  bias_dev holds K int32 values and is read only when
+ * p->epilogue has CONV_EPILOGUE_BIAS.  The output must not overlap the
+ * inputs or the workspace.  Asynchronous: returns after queuing the kernels.
+ */
+conv_status conv_fprop(const conv_tensor_desc *x, const int8_t *x_dev,
+                       const conv_tensor_desc *w, const int8_t *w_dev,
+                       const conv_tensor_desc *y, int32_t *y_dev,
+                       const int32_t *bias_dev, const conv_fprop_params *p,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * conv_fprop in two halves, for callers that reuse one filter across many
+ * images (the filter repack then runs once):
+ *   conv_fprop_pack_filter writes the repacked filter into the workspace
+ *   (nothing to do for the direct kernels);
+ *   conv_fprop_prepacked runs the convolution from that workspace.
+ * Both take the same descriptors and params as conv_fprop and validate them
+ * the same way; conv_fprop_prepacked still needs w_dev (the direct kernels
+ * read the filter itself).  The workspace contents must come from a
+ * conv_fprop_pack_filter call with the same filter, descriptors and params;
+ * the library cannot check that.  Calling the two in order on one stream is
+ * conv_fprop.
+ */
+conv_status conv_fprop_pack_filter(const conv_tensor_desc *x, const conv_tensor_desc *w, const int8_t *w_dev,
+                                   const conv_tensor_desc *y, const conv_fprop_params *p, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
+conv_status conv_fprop_prepacked(const conv_tensor_desc *x, const int8_t *x_dev,
+                                 const conv_tensor_desc *w, const int8_t *w_dev,
+                                 const conv_tensor_desc *y, int32_t *y_dev,
+                                 const int32_t *bias_dev, const conv_fprop_params *p,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronise `stream`, then read and clear the current device's status
+ * word: CONV_OK, or CONV_ERR_DEVICE_TIMEOUT if a kernel gave up waiting
+ * since the last call. */
+conv_status conv_device_status(void *stream);
+
+/* Self-test of the timeout path: launches one kernel that waits on a barrier
+ * nobody signals, with a limit of `limit_us` microseconds, so that it records
+ * CONV_ERR_DEVICE_TIMEOUT and exits.  Returns the launch status. */
+conv_status conv_selftest_wait_timeout(uint32_t limit_us, void *stream);
+
+/* Human-readable name of a status. */
+const char *conv_status_string(conv_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t conv_library_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* INT8CONV_H */

@@ -1,0 +1,80 @@
+// internal.h -- declarations shared by the translation units of libint8conv.
+// Not part of the public ABI (that is include/int8conv.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "int8conv.h"
+
+namespace i8c {
+
+// Geometry of one validated call, flattened for the launchers.
+struct ConvGeom {
+    int64_t N, C, H, W;        // image
+    int64_t K, R, S;           // filter
+    int64_t P, Q;              // output
+    int64_t xs[4], ws[4], ys[4];  // element strides (logical order)
+    int64_t pad_h, pad_w;      // pre-padding (post padding only changes P, Q)
+    int64_t str_h, str_w;
+    int64_t dil_h, dil_w;
+    int32_t mode;              // 0 cross-correlation, 1 convolution
+    bool bias, relu;
+};
+
+// Fill g from validated descriptors.
+void make_geom(const conv_tensor_desc *x, const conv_tensor_desc *w, const conv_tensor_desc *y,
+               const conv_fprop_params *p, ConvGeom *g);
+
+// Largest addressed element offset + 1 of a descriptor (0 if a dim is 0).
+int64_t desc_extent_elems(const conv_tensor_desc *d);
+
+// ---------------------------------------------------------------- igemm
+// Tile shape of the tensor-core kernel: 128 output pixels x kIgemmNTile
+// output channels, reduction consumed 64 channels (one 128-byte row of f16)
+// at a time.
+constexpr int kIgemmMTile = 128;
+constexpr int kIgemmNTile = 128;
+constexpr int kIgemmKStep = 64;
+
+struct IgemmPlan {
+    bool pack_x;            // image must be copied to channels-last first
+    int64_t c16;            // channel count rounded up to 16 (valid load width)
+    int64_t c_steps;        // ceil(C / 64)
+    int64_t k_steps;        // R * S * c_steps
+    int64_t n_tiles;        // ceil(K / kIgemmNTile)
+    int64_t m_tiles;        // ceil(N*P*Q / kIgemmMTile)
+    size_t wpack_bytes;     // repacked filter
+    size_t xpack_bytes;     // channels-last image copy (0 if not needed)
+    size_t workspace_bytes; // total, each part 256-byte aligned
+};
+
+bool igemm_supported(const ConvGeom &g);
+void igemm_plan(const ConvGeom &g, const void *x_dev, IgemmPlan *pl);
+// Repacks the filter into the first pl.wpack_bytes of the workspace.
+conv_status igemm_pack_filter_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *w, void *workspace,
+                                     void *stream);
+// Runs the convolution from a workspace whose filter part is already packed
+// (copies the image to channels-last first when pl.pack_x).
+conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, int32_t *y,
+                              const int32_t *bias, void *workspace, void *stream);
+
+// ---------------------------------------------------------------- direct
+bool dp4a_supported(const ConvGeom &g);
+conv_status dp4a_launch(const ConvGeom &g, const int8_t *x, const int8_t *w, int32_t *y,
+                        const int32_t *bias, void *stream);
+conv_status generic_launch(const ConvGeom &g, const int8_t *x, const int8_t *w, int32_t *y,
+                           const int32_t *bias, void *stream);
+
+// ---------------------------------------------------------------- device
+// Current device is an sm_103 part (cached per device).
+conv_status check_device();
+// Time limit, in nanoseconds, of every wait inside a kernel.
+uint64_t wait_limit_ns();
+// Number of SMs of the current device.
+int device_sm_count();
+// Device address of the current device's status word (kernels record
+// CONV_ERR_DEVICE_TIMEOUT there); nullptr if it cannot be obtained.
+int *device_status_word();
+
+}  // namespace i8c

@@ -1,0 +1,218 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle,
+element by element, bit-exact (integer work: tolerance 0).
+
+Full outputs are compared at sizes the oracle finishes in seconds; the two
+largest workloads are compared in full at reduced batch (same tiling, same
+code path) and on sampled outputs at full size, in the launch configuration
+the benchmark times."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def ic():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import int8_conv2d_fprop_gb300 as m
+    torch.cuda.set_device(0)
+    return m
+
+
+def _to_dev(flat, dims, strides):
+    return torch.as_strided(torch.from_numpy(np.ascontiguousarray(flat)).cuda(), tuple(dims), tuple(strides))
+
+
+def _run_both(ic, cfg, algo=0, x=None, w=None, b=None, x_pad=0, w_pad=0, y_layout=None, points=None):
+    if x is None:
+        x, w, b = synth.make_inputs(cfg)
+    xf, xs = synth.place(x, cfg.x_layout, pad_elems=x_pad)
+    wf, ws = synth.place(w, cfg.w_layout, pad_elems=w_pad)
+    xt, wt = _to_dev(xf, cfg.x_dims, xs), _to_dev(wf, cfg.w_dims, ws)
+    bt = torch.from_numpy(b).cuda() if b is not None else None
+    yl = y_layout or cfg.y_layout
+    fmt = torch.channels_last if yl == "NHWC" else torch.contiguous_format
+    # canaries around the output: 64 guard words on each side
+    P, Q = cfg.P, cfg.Q
+    ysz = cfg.N * cfg.K * P * Q
+    guard = torch.full((ysz + 128,), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
+    ystr = synth.packed_strides(cfg.y_dims, yl)
+    yt = torch.as_strided(guard[64:64 + ysz], cfg.y_dims, ystr)
+    y = ic.conv_fprop(xt, wt, bt, pre_padding=cfg.pre, post_padding=cfg.post, stride=cfg.stride,
+                      dilation=cfg.dilation, mode=cfg.mode, relu=cfg.relu, algo=algo, out=yt)
+    torch.cuda.synchronize()
+    assert ic.device_status() == 0
+    g = guard.cpu().numpy()
+    assert np.all(g[:64] == 0x5A5A5A5A) and np.all(g[64 + ysz:] == 0x5A5A5A5A), "write outside the output"
+    got = y.cpu().numpy()
+    if points is not None:
+        pts = points(cfg)
+        ref = oracle.conv_fprop_points(xf, cfg.x_dims, xs, wf, cfg.w_dims, ws, pts, cfg.pre, cfg.post,
+                                       cfg.stride, cfg.dilation, cfg.mode, b, cfg.relu)
+        return got[tuple(pts.T)], ref
+    ref = oracle.conv_fprop(xf, cfg.x_dims, xs, wf, cfg.w_dims, ws, cfg.pre, cfg.post, cfg.stride,
+                            cfg.dilation, cfg.mode, b, cfg.relu)
+    return got, ref
+
+
+def _assert_equal(got, ref, what):
+    if not np.array_equal(got, ref):
+        idx = np.argwhere(got != ref)
+        first = tuple(idx[0])
+        raise AssertionError(f"{what}: {len(idx)} of {ref.size} outputs differ; first at {first}: "
+                             f"got {got[first]} expected {ref[first]}")
+
+
+def _sample_points(count, seed=0):
+    def f(cfg):
+        rng = np.random.default_rng(seed)
+        pts = np.stack([rng.integers(0, d, count) for d in cfg.y_dims], axis=1)
+        # always include the four corners of the first and last image/channel
+        corners = [(n, k, p, q) for n in (0, cfg.N - 1) for k in (0, cfg.K - 1)
+                   for p in (0, cfg.P - 1) for q in (0, cfg.Q - 1)]
+        return np.concatenate([pts, np.array(corners, dtype=np.int64)])
+    return f
+
+
+# ------------------------------------------------------------------ workloads
+@pytest.mark.parametrize("name", ["c1_tiny_nchw", "p4_shape", "c2_s2_nhwc", "c4_1x1_bias_relu"])
+def test_workload_full(ic, name):
+    cfg = synth.CONFIGS[name]
+    got, ref = _run_both(ic, cfg)
+    _assert_equal(got, ref, name)
+
+
+@pytest.mark.parametrize("name,batch", [("c3_3x3_large", 2), ("c5_7x1_dilated_conv", 2)])
+def test_workload_reduced_batch_full(ic, name, batch):
+    import dataclasses
+    cfg = dataclasses.replace(synth.CONFIGS[name], N=batch)
+    got, ref = _run_both(ic, cfg)
+    _assert_equal(got, ref, f"{name} N={batch}")
+
+
+@pytest.mark.parametrize("name", ["c3_3x3_large", "c5_7x1_dilated_conv"])
+def test_workload_full_size_sampled(ic, name):
+    cfg = synth.CONFIGS[name]
+    got, ref = _run_both(ic, cfg, points=_sample_points(6000, seed=3))
+    _assert_equal(got, ref, name)
+
+
+# ------------------------------------------------------------------ every algorithm
+ALGOS = [1, 2, 3]  # implicit GEMM, dp4a, generic
+
+
+def _shape_cases():
+    C = synth.ConvConfig
+    return [
+        C("ragged_m_k", 3, 64, 13, 11, 200, 3, 3, pre=(1, 1), post=(1, 1), seed=11),
+        C("c80_masked", 2, 80, 9, 9, 72, 3, 2, stride=(2, 1), pre=(1, 0), post=(0, 1), seed=12),
+        C("c48_single_step", 2, 48, 10, 7, 40, 2, 2, dilation=(2, 3), pre=(2, 2), post=(1, 3), seed=13),
+        C("c24_repacked", 2, 24, 8, 8, 36, 3, 3, pre=(1, 1), post=(1, 1), mode=1, bias=True, relu=True, seed=14),
+        C("nchw_conv_mode", 2, 32, 11, 12, 20, 4, 2, stride=(1, 2), dilation=(2, 1), pre=(3, 0), post=(2, 1),
+          mode=1, x_layout="NCHW", w_layout="KCRS", y_layout="NCHW", seed=15),
+        C("one_by_one_strided", 2, 128, 15, 15, 130, 1, 1, stride=(2, 2), bias=True, seed=16),
+        C("tiny_c3", 1, 3, 12, 9, 10, 3, 3, pre=(1, 1), post=(1, 1), x_layout="NCHW", w_layout="KCRS",
+          y_layout="NCHW", seed=17),
+    ]
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("case", _shape_cases(), ids=lambda c: c.name)
+def test_algorithms_agree_with_oracle(ic, case, algo):
+    if algo == 2 and case.C * case.R * case.S > 1024:
+        pytest.skip("dp4a takes C*R*S <= 1024")
+    got, ref = _run_both(ic, case, algo=algo)
+    _assert_equal(got, ref, f"{case.name} algo {algo}")
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_padded_strides_and_output_layouts(ic, algo):
+    cfg = synth.ConvConfig("strided", 2, 32, 9, 10, 24, 3, 3, pre=(1, 2), post=(0, 1), seed=21)
+    for yl in ("NCHW", "NHWC"):
+        got, ref = _run_both(ic, cfg, algo=algo, x_pad=16, w_pad=3, y_layout=yl)
+        _assert_equal(got, ref, f"padded strides algo {algo} y {yl}")
+
+
+# ------------------------------------------------------------------ exactness
+def test_extreme_values_exceed_f32_integer_range(ic):
+    """All -128 operands: interior sums C*R*S*2^14 = 37,748,736 > 2^24, so
+    the f16 tensor path is exact only through its int32 group sums."""
+    cfg = synth.ConvConfig("all_min", 1, 256, 6, 6, 130, 3, 3, pre=(1, 1), post=(1, 1))
+    x = np.full(cfg.x_dims, -128, dtype=np.int8)
+    w = np.full(cfg.w_dims, -128, dtype=np.int8)
+    got, ref = _run_both(ic, cfg, algo=1, x=x, w=w, b=None)
+    assert ref[0, 0, 2, 2] == 256 * 9 * 16384
+    _assert_equal(got, ref, "all -128")
+
+
+def test_group_sum_reaches_two_to_24(ic):
+    """One group of 1024 products of 2^14 sums to exactly 2^24; mixed signs
+    and magnitudes near the extremes around it."""
+    cfg = synth.ConvConfig("g24", 1, 2048, 3, 3, 16, 1, 1)
+    x = np.full(cfg.x_dims, -128, dtype=np.int8)
+    w = np.full(cfg.w_dims, -128, dtype=np.int8)
+    w[1, 1024:] = 127      # second half of the reduction flips sign
+    w[2, ::2] = 127        # alternating
+    w[3, :] = -127
+    x[0, ::3, 1, 1] = 127
+    got, ref = _run_both(ic, cfg, algo=1, x=x, w=w, b=None)
+    assert ref[0, 0, 0, 0] == 2048 * 16384
+    _assert_equal(got, ref, "2^24 groups")
+
+
+def test_random_extremes_full_reduction(ic):
+    cfg = synth.ConvConfig("ext", 2, 512, 7, 7, 64, 3, 3, pre=(1, 1), post=(1, 1), extremes=0.5, seed=31)
+    got, ref = _run_both(ic, cfg, algo=1)
+    _assert_equal(got, ref, "random extremes")
+
+
+# ------------------------------------------------------------------ edge cases and status
+def test_empty_batch_is_a_no_op(ic):
+    x = torch.zeros((0, 64, 8, 8), dtype=torch.int8, device="cuda").to(memory_format=torch.channels_last)
+    w = torch.zeros((16, 64, 3, 3), dtype=torch.int8, device="cuda").to(memory_format=torch.channels_last)
+    y = ic.conv_fprop(x, w, padding=(1, 1))
+    assert tuple(y.shape) == (0, 16, 8, 8)
+
+
+def test_single_pixel_output(ic):
+    cfg = synth.ConvConfig("one_pixel", 1, 64, 3, 3, 8, 3, 3, seed=41)
+    for algo in ALGOS:
+        got, ref = _run_both(ic, cfg, algo=algo)
+        _assert_equal(got, ref, f"1x1 output algo {algo}")
+
+
+def test_timeout_is_reported_and_cleared(ic):
+    assert ic.device_status() == 0
+    assert ic.selftest_wait_timeout(2000) == 0
+    assert ic.device_status() == ic.STATUS_CODE["CONV_ERR_DEVICE_TIMEOUT"]
+    assert ic.device_status() == 0
+    # the context still works afterwards
+    got, ref = _run_both(ic, synth.CONFIGS["c1_tiny_nchw"])
+    _assert_equal(got, ref, "after timeout")
+
+
+def test_workspace_too_small_is_refused(ic):
+    cfg = synth.CONFIGS["c2_s2_nhwc"]
+    xd = ic.TensorDesc.packed(ic.CONV_INT8, cfg.x_dims, cfg.x_layout)
+    wd = ic.TensorDesc.packed(ic.CONV_INT8, cfg.w_dims, cfg.w_layout)
+    yd = ic.TensorDesc.packed(ic.CONV_INT32, cfg.y_dims, cfg.y_layout)
+    p = ic.Params.make(cfg.pre, cfg.post, cfg.stride)
+    need = ic.workspace_size(xd, wd, yd, p)
+    x = torch.zeros(xd.capacity_bytes, dtype=torch.int8, device="cuda")
+    w = torch.zeros(wd.capacity_bytes, dtype=torch.int8, device="cuda")
+    y = torch.zeros(yd.capacity_bytes // 4, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    assert ic.conv_fprop_raw(xd, x.data_ptr(), wd, w.data_ptr(), yd, y.data_ptr(), 0, p, ws.data_ptr(),
+                             need - 256, s) == ic.STATUS_CODE["CONV_ERR_WORKSPACE"]
+    assert ic.conv_fprop_raw(xd, x.data_ptr(), wd, w.data_ptr(), yd, y.data_ptr(), 0, p, ws.data_ptr(),
+                             need, s) == 0
+    torch.cuda.synchronize()

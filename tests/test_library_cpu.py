@@ -1,0 +1,247 @@
+"""Host-side checks of libint8conv.so that need no GPU: the library loads and
+exports every entry point of include/int8conv.h, the stride calculator, the
+output-size rule and every rejection rule of the validator (including the two
+descriptor sets of the forum thread "INT8 convolution using cuDNN Python
+Frontend"), the planner's choices and workspace sizes, and the argument checks
+conv_fprop makes before it touches a device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import oracle
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ic():
+    import __graft_entry__
+    __graft_entry__.build_library()
+    import int8_conv2d_fprop_gb300 as m
+    m.lib()
+    return m
+
+
+def _descs(ic, cfg, y_layout=None):
+    xd = ic.TensorDesc.packed(ic.CONV_INT8, cfg.x_dims, cfg.x_layout)
+    wd = ic.TensorDesc.packed(ic.CONV_INT8, cfg.w_dims, cfg.w_layout)
+    yd = ic.TensorDesc.packed(ic.CONV_INT32, cfg.y_dims, y_layout or cfg.y_layout)
+    p = ic.Params.make(cfg.pre, cfg.post, cfg.stride, cfg.dilation, cfg.mode, cfg.bias, cfg.relu)
+    return xd, wd, yd, p
+
+
+def test_exports_every_declared_entry_point(ic):
+    header = open(os.path.join(ROOT, "include", "int8conv.h")).read()
+    declared = set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(conv_[a-z_0-9]+)\s*\(", header, re.M))
+    assert declared == set(ic.EXPORTED_SYMBOLS)
+    out = subprocess.run(["nm", "-D", "--defined-only", ic._LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (conv_[a-z_0-9]+)$", out, re.M))
+    assert declared <= exported
+    for name in declared:
+        assert hasattr(ic.lib(), name)
+
+
+def test_status_strings_cover_every_code(ic):
+    for code, name in ic.STATUS.items():
+        assert ic.status_string(code).startswith(name)
+    assert ic.lib().conv_library_version() >= 100
+
+
+def test_params_defaults_and_symmetric_padding(ic):
+    p = ic.Params()
+    ic.lib().conv_params_init(ctypes.byref(p))
+    assert tuple(p.stride) == (1, 1) and tuple(p.dilation) == (1, 1)
+    assert tuple(p.pre_padding) == (0, 0) and tuple(p.post_padding) == (0, 0)
+    assert p.mode == ic.CROSS_CORRELATION and p.compute_dtype == ic.CONV_INT32 and p.algo == 0
+    q = ic.Params.make(padding=(3, 2))
+    assert tuple(q.pre_padding) == (3, 2) and tuple(q.post_padding) == (3, 2)
+
+
+@pytest.mark.parametrize("layout", ["NCHW", "NHWC", "KCRS", "KRSC"])
+def test_stride_calculator_matches_packed_layouts(ic, layout):
+    dims = (2, 3, 5, 7)
+    d = ic.TensorDesc.packed(ic.CONV_INT8, dims, layout)
+    assert d.strides_t == synth.packed_strides(dims, layout)
+    assert d.capacity_bytes == 2 * 3 * 5 * 7
+    d32 = ic.TensorDesc.packed(ic.CONV_INT32, dims, layout)
+    assert d32.capacity_bytes == 4 * 2 * 3 * 5 * 7
+    with pytest.raises(ic.ConvError):
+        ic.TensorDesc.packed(ic.CONV_INT8, dims, "NWHC")
+
+
+@pytest.mark.parametrize("name", sorted(synth.CONFIGS))
+def test_output_dims_and_validation_of_workloads(ic, name):
+    cfg = synth.CONFIGS[name]
+    xd, wd, yd, p = _descs(ic, cfg)
+    assert ic.output_dims(xd, wd, p) == cfg.y_dims
+    assert ic.output_dims(xd, wd, p) == oracle.out_dims(cfg.x_dims, cfg.w_dims, cfg.pre, cfg.post,
+                                                        cfg.stride, cfg.dilation)
+    assert ic.validate(xd, wd, yd, p, cfg.K if cfg.bias else 0) == 0
+
+
+def test_forum_descriptors_are_both_valid(ic):
+    """Both stride sets of the forum thread describe the same bytes (C = 1)."""
+    p = ic.Params.make(padding=(0, 0))
+    for xs, ws in (((25, 1, 5, 1), (9, 1, 3, 1)), ((25, 25, 5, 1), (9, 9, 3, 1))):
+        xd = ic.TensorDesc.make(ic.CONV_INT8, (1, 1, 5, 5), xs, 25)
+        wd = ic.TensorDesc.make(ic.CONV_INT8, (1, 1, 3, 3), ws, 9)
+        yd = ic.TensorDesc.make(ic.CONV_INT32, (1, 1, 3, 3), (9, 9, 3, 1), 36)
+        assert ic.validate(xd, wd, yd, p) == 0
+
+
+def test_forum_failure_output_typed_int8_is_rejected(ic):
+    """The forum thread's output was left to default to the int8 I/O type; an
+    output descriptor that is not INT32 is refused."""
+    p = ic.Params.make()
+    xd = ic.TensorDesc.make(ic.CONV_INT8, (1, 1, 5, 5), (25, 25, 5, 1), 25)
+    wd = ic.TensorDesc.make(ic.CONV_INT8, (1, 1, 3, 3), (9, 9, 3, 1), 9)
+    yd = ic.TensorDesc.make(ic.CONV_INT8, (1, 1, 3, 3), (9, 9, 3, 1), 36)
+    assert ic.validate(xd, wd, yd, p) == ic.STATUS_CODE["CONV_ERR_DTYPE"]
+    wd32 = ic.TensorDesc.make(ic.CONV_INT32, (1, 1, 3, 3), (9, 9, 3, 1), 36)
+    yd32 = ic.TensorDesc.make(ic.CONV_INT32, (1, 1, 3, 3), (9, 9, 3, 1), 36)
+    assert ic.validate(xd, wd32, yd32, p) == ic.STATUS_CODE["CONV_ERR_DTYPE"]
+
+
+def _base(ic):
+    cfg = synth.CONFIGS["c2_s2_nhwc"]
+    return cfg, _descs(ic, cfg)
+
+
+def _code(ic, name):
+    return ic.STATUS_CODE[name]
+
+
+def test_validator_rejections(ic):
+    cfg, (xd, wd, yd, p) = _base(ic)
+    assert ic.validate(xd, wd, yd, p) == 0
+
+    def mod(desc, **kw):
+        d = ic.TensorDesc.make(desc.dtype, desc.dims_t, desc.strides_t, desc.capacity_bytes)
+        for k, v in kw.items():
+            if k in ("dims", "strides"):
+                for i in range(4):
+                    getattr(d, k)[i] = v[i]
+            else:
+                setattr(d, k, v)
+        return d
+
+    # aliasing strides (two dims map onto the same bytes)
+    bad = mod(xd, strides=(xd.strides[0], 1, xd.strides[2], 32))
+    assert ic.validate(bad, wd, yd, p) == _code(ic, "CONV_ERR_BAD_STRIDES")
+    # zero and negative strides of a dim larger than one
+    assert ic.validate(mod(xd, strides=(xd.strides[0], 1, 0, 64)), wd, yd, p) == _code(ic, "CONV_ERR_BAD_STRIDES")
+    assert ic.validate(mod(xd, strides=(xd.strides[0], 1, -3584, 64)), wd, yd, p) == _code(ic, "CONV_ERR_BAD_STRIDES")
+    # buffer smaller than the extent
+    assert ic.validate(xd, wd, mod(yd, capacity_bytes=yd.capacity_bytes - 4), p) == _code(ic, "CONV_ERR_BUFFER_TOO_SMALL")
+    assert ic.validate(mod(xd, capacity_bytes=xd.capacity_bytes - 1), wd, yd, p) == _code(ic, "CONV_ERR_BUFFER_TOO_SMALL")
+    # rank and dtype
+    assert ic.validate(mod(xd, rank=3), wd, yd, p) == _code(ic, "CONV_ERR_RANK")
+    assert ic.validate(mod(xd, dtype=ic.CONV_INT32), wd, yd, p) == _code(ic, "CONV_ERR_DTYPE")
+    # channel mismatch between image and filter
+    wbad = ic.TensorDesc.packed(ic.CONV_INT8, (64, 32, 3, 3), "KRSC")
+    assert ic.validate(xd, wbad, yd, p) == _code(ic, "CONV_ERR_SHAPE_MISMATCH")
+    # output dims that are not the computed P, Q
+    ybad = ic.TensorDesc.packed(ic.CONV_INT32, (8, 64, 27, 28), "NHWC")
+    assert ic.validate(xd, wd, ybad, p) == _code(ic, "CONV_ERR_SHAPE_MISMATCH")
+    ybad = ic.TensorDesc.packed(ic.CONV_INT32, (8, 32, 28, 28), "NHWC")
+    assert ic.validate(xd, wd, ybad, p) == _code(ic, "CONV_ERR_SHAPE_MISMATCH")
+    # parameters
+    for kw in (dict(stride=(0, 1)), dict(dilation=(1, 0)), dict(pre_padding=(-1, 0), post_padding=(1, 1))):
+        args = dict(pre_padding=(1, 1), post_padding=(1, 1), stride=(2, 2))
+        args.update(kw)
+        assert ic.validate(xd, wd, yd, ic.Params.make(**args)) == _code(ic, "CONV_ERR_BAD_PARAM")
+    pm = ic.Params.make((1, 1), (1, 1), (2, 2), mode=2)
+    assert ic.validate(xd, wd, yd, pm) == _code(ic, "CONV_ERR_BAD_PARAM")
+    pc = ic.Params.make((1, 1), (1, 1), (2, 2), compute_dtype=ic.CONV_INT8)
+    assert ic.validate(xd, wd, yd, pc) == _code(ic, "CONV_ERR_UNSUPPORTED_COMPUTE")
+    # bias requested but too short
+    pb = ic.Params.make((1, 1), (1, 1), (2, 2), bias=True)
+    assert ic.validate(xd, wd, yd, pb, 63) == _code(ic, "CONV_ERR_BUFFER_TOO_SMALL")
+    assert ic.validate(xd, wd, yd, pb, 64) == 0
+    # empty output (filter wider than the padded image)
+    xs = ic.TensorDesc.packed(ic.CONV_INT8, (1, 4, 2, 2), "NHWC")
+    ws = ic.TensorDesc.packed(ic.CONV_INT8, (4, 4, 3, 3), "KRSC")
+    out = (ctypes.c_int64 * 4)()
+    assert ic.lib().conv_fprop_output_dims(ctypes.byref(xs), ctypes.byref(ws), ctypes.byref(ic.Params.make()),
+                                           out) == _code(ic, "CONV_ERR_BAD_PARAM")
+
+
+def test_overflow_bound(ic):
+    """C*R*S*2^14 must fit int32: 131071 taps pass, 131072 are refused."""
+    p = ic.Params.make()
+    for crs, ok in ((131071, True), (131072, False)):
+        xd = ic.TensorDesc.packed(ic.CONV_INT8, (1, crs, 1, 1), "NHWC")
+        wd = ic.TensorDesc.packed(ic.CONV_INT8, (1, crs, 1, 1), "KRSC")
+        yd = ic.TensorDesc.packed(ic.CONV_INT32, (1, 1, 1, 1), "NHWC")
+        st = ic.validate(xd, wd, yd, p)
+        assert (st == 0) == ok
+        if not ok:
+            assert st == _code(ic, "CONV_ERR_OVERFLOW_RISK")
+    assert oracle.worst_case_abs(131071, 1, 1) <= 2 ** 31 - 1 < oracle.worst_case_abs(131072, 1, 1)
+
+
+def test_unit_dim_strides_are_ignored(ic):
+    p = ic.Params.make()
+    xd = ic.TensorDesc.make(ic.CONV_INT8, (1, 1, 5, 5), (0, -7, 5, 1), 25)
+    wd = ic.TensorDesc.make(ic.CONV_INT8, (1, 1, 3, 3), (123, 0, 3, 1), 9)
+    yd = ic.TensorDesc.make(ic.CONV_INT32, (1, 1, 3, 3), (0, 0, 3, 1), 36)
+    assert ic.validate(xd, wd, yd, p) == 0
+
+
+def test_planner_choices_and_workspace(ic):
+    algo = {}
+    ws = {}
+    for name, cfg in synth.CONFIGS.items():
+        xd, wd, yd, p = _descs(ic, cfg)
+        algo[name] = ic.plan(xd, wd, yd, p)
+        ws[name] = ic.workspace_size(xd, wd, yd, p)
+    assert algo["c1_tiny_nchw"] == ic.ALGO_DIRECT_DP4A
+    assert algo["p4_shape"] == ic.ALGO_DIRECT_DP4A
+    for name in ("c2_s2_nhwc", "c3_3x3_large", "c4_1x1_bias_relu", "c5_7x1_dilated_conv"):
+        assert algo[name] == ic.ALGO_IMPLICIT_GEMM
+    assert ws["c1_tiny_nchw"] == 0 and ws["p4_shape"] == 0
+    # C3: 2 n-tiles x 36 k-steps x 16 KB of f16 filter blocks, no image copy
+    assert ws["c3_3x3_large"] == 2 * 36 * 16384
+    # C5 has an NCHW image: the channels-last copy is added
+    c5 = synth.CONFIGS["c5_7x1_dilated_conv"]
+    assert ws["c5_7x1_dilated_conv"] == 2 * 14 * 16384 + c5.N * c5.H * c5.W * c5.C
+    # forced algorithms are honoured
+    xd, wd, yd, p = _descs(ic, synth.CONFIGS["c2_s2_nhwc"])
+    for a in (ic.ALGO_DIRECT_GENERIC, ic.ALGO_DIRECT_DP4A, ic.ALGO_IMPLICIT_GEMM):
+        p.algo = a
+        assert ic.plan(xd, wd, yd, p) == a
+        assert (ic.workspace_size(xd, wd, yd, p) > 0) == (a == ic.ALGO_IMPLICIT_GEMM)
+
+
+def test_dp4a_refuses_long_reductions(ic):
+    cfg = synth.CONFIGS["c3_3x3_large"]
+    xd, wd, yd, p = _descs(ic, cfg)
+    p.algo = ic.ALGO_DIRECT_DP4A
+    with pytest.raises(ic.ConvError) as e:
+        ic.plan(xd, wd, yd, p)
+    assert e.value.name == "CONV_ERR_ALIGNMENT"
+
+
+def test_call_checks_before_any_device_work(ic):
+    cfg = synth.CONFIGS["c2_s2_nhwc"]
+    xd, wd, yd, p = _descs(ic, cfg)
+    code = ic.conv_fprop_raw(xd, 0, wd, 0x10000, yd, 0x20000000, 0, p, 0x40000000, 1 << 30, 0)
+    assert code == _code(ic, "CONV_ERR_NULL_PTR")
+    # output overlapping the image
+    x = 0x10000000
+    code = ic.conv_fprop_raw(xd, x, wd, 0x30000000, yd, x + 1024, 0, p, 0x40000000, 1 << 30, 0)
+    assert code == _code(ic, "CONV_ERR_OVERLAP")
+    # bias requested but no pointer
+    pb = ic.Params.make(cfg.pre, cfg.post, cfg.stride, bias=True)
+    code = ic.conv_fprop_raw(xd, x, wd, 0x30000000, yd, 0x50000000, 0, pb, 0x40000000, 1 << 30, 0)
+    assert code == _code(ic, "CONV_ERR_NULL_PTR")
+    # empty batch: nothing to do, nothing launched
+    xe = ic.TensorDesc.packed(ic.CONV_INT8, (1, 64, 56, 56), "NHWC")
+    xe.dims[0] = 0
+    ye = ic.TensorDesc.packed(ic.CONV_INT32, (1, 64, 28, 28), "NHWC")
+    ye.dims[0] = 0
+    assert ic.conv_fprop_raw(xe, 0, wd, 0, ye, 0, 0, p, 0, 0, 0) == 0
