@@ -15,18 +15,23 @@
 // memory slot, converted to int32 by the epilogue warps and summed in int32
 // registers.  The result is bit-identical to integer arithmetic.
 //
-// Persistent, warp-specialised CTA (one per SM), tile 128 pixels x 128
-// channels:
-//   warps 0-3  producers: each thread owns one pixel row of the A tile; it
-//              gathers 64 channels of one tap with 16-byte loads (the im2col
-//              address formed on the fly from stride, padding and dilation),
-//              converts int8 -> f16 in registers and writes the row into the
-//              128-byte-swizzled shared-memory stage.  Thread 0 also brings the
-//              matching pre-swizzled f16 filter block with one bulk async copy.
-//   warp 4     allocates tensor memory; lane 0 issues tcgen05.mma (M=128,
-//              N=128, K=16 per instruction) into one of two accumulator slots.
-//   warps 5-8  epilogue: tcgen05.ld each finished slot, f32 -> int32, sum the
-//              groups, add bias, ReLU, store int32 rows.
+// Persistent, warp-specialised CTA (one per SM), 512 threads, tile 128 pixels
+// x NT output channels (NT = 128 or 256):
+//   warpgroup 0  producers: each thread owns one pixel row of the A tile; it
+//                gathers 64 channels of one tap with 16-byte loads (the im2col
+//                address formed on the fly from stride, padding and
+//                dilation), two items ahead of the one it stores, converts
+//                int8 -> f16 in registers and writes the row into the
+//                128-byte-swizzled shared-memory stage.  Thread 0 also brings
+//                the matching pre-swizzled f16 filter block with one bulk
+//                async copy.
+//   warpgroup 1  warp 4 allocates tensor memory; its lane 0 issues
+//                tcgen05.mma (M=128, N=NT, K=16 per instruction) into one of
+//                two accumulator slots.  Warps 5-7 have no role.
+//   warpgroups 2-3  epilogue, two warps per tensor-memory lane quadrant, each
+//                owning NT/2 columns: tcgen05.ld each finished slot,
+//                f32 -> int32, sum the groups, add bias, ReLU, store int32.
+// Registers are moved from warpgroups 0-1 to the epilogue with setmaxnreg.
 // Every wait is bounded in time; on expiry the CTA records
 // CONV_ERR_DEVICE_TIMEOUT, stops, lets issued copies and MMAs finish and frees
 // its tensor memory.
@@ -41,19 +46,28 @@ namespace i8c {
 namespace {
 
 constexpr int MT = kIgemmMTile;  // 128
-constexpr int NT = kIgemmNTile;  // 128
 constexpr int KS = kIgemmKStep;  // 64 channels = 128 bytes of f16 per row
-constexpr int STAGES = 6;
 constexpr int NSLOT = 2;
-constexpr int TMEM_COLS = NSLOT * NT;  // 256
 constexpr int MAX_GROUP_STEPS = 1024 / KS;  // 16 k-steps: at most 1024 products per f32 sum
-constexpr int A_BYTES = MT * KS * 2;  // 16 KB
-constexpr int B_BYTES = NT * KS * 2;  // 16 KB
-constexpr int NUM_PRODUCER_WARPS = 4;
+constexpr int A_BYTES = MT * KS * 2;       // 16 KB
+constexpr int THREADS = 512;
 constexpr int MMA_WARP = 4;
-constexpr int NUM_EPI_WARPS = 4;
-constexpr int THREADS = 32 * (NUM_PRODUCER_WARPS + 1 + NUM_EPI_WARPS);  // 288
-constexpr int SMEM_BYTES = 1024 /*align slack*/ + STAGES * (A_BYTES + B_BYTES) + 256 /*barriers*/;
+constexpr int FIRST_EPI_WARP = 8;
+constexpr int NUM_EPI_THREADS = 256;
+constexpr int PRODUCER_REGS = 80;
+constexpr int EPILOGUE_REGS = 176;
+static_assert(2 * 128 * PRODUCER_REGS + 2 * 128 * EPILOGUE_REGS <= 65536, "register split exceeds the launch");
+constexpr int PREFETCH = 2;  // items in flight ahead of the one being stored
+
+template <int NT>
+struct TileCfg {
+    static constexpr int B_BYTES = NT * KS * 2;
+    static constexpr int STAGES = NT == 256 ? 4 : 6;
+    static constexpr int TMEM_COLS = NSLOT * NT;
+    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + STAGES * (A_BYTES + B_BYTES) + 256 /*barriers*/;
+    static_assert(TMEM_COLS <= 512, "tensor memory has 512 columns");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+};
 
 struct IgemmArgs {
     const int8_t *x;     // channels-last image
@@ -72,6 +86,7 @@ struct IgemmArgs {
     int *status;         // device status word
 };
 
+template <int STAGES>
 struct SharedCtl {
     uint64_t a_full[STAGES];
     uint64_t b_full[STAGES];
@@ -82,7 +97,7 @@ struct SharedCtl {
     uint32_t tmem_base;
     int32_t abort_flag;
 };
-static_assert(sizeof(SharedCtl) <= 256, "control block too large");
+static_assert(sizeof(SharedCtl<6>) <= 256, "control block too large");
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting or
 // the time limit passed (then the CTA is marked aborting and the device status
@@ -192,14 +207,19 @@ __device__ __forceinline__ void cursor_advance(LoadCursor &c, const IgemmArgs &a
     }
 }
 
+template <int NT>
 __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_constant__ IgemmArgs a) {
+    using Cfg = TileCfg<NT>;
+    constexpr int STAGES = Cfg::STAGES;
+    constexpr int B_BYTES = Cfg::B_BYTES;
+    constexpr int HALF = NT / 2;  // columns per epilogue thread
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t *const base_ptr = smem_raw + (base - raw_addr);
     const uint32_t a_smem = base;
     const uint32_t b_smem = base + STAGES * A_BYTES;
-    SharedCtl *ctl = reinterpret_cast<SharedCtl *>(base_ptr + STAGES * (A_BYTES + B_BYTES));
+    SharedCtl<STAGES> *ctl = reinterpret_cast<SharedCtl<STAGES> *>(base_ptr + STAGES * (A_BYTES + B_BYTES));
     volatile int32_t *abort_flag = &ctl->abort_flag;
 
     const int warp = threadIdx.x >> 5;
@@ -207,20 +227,20 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            ptx::mbar_init(ptx::smem_addr(&ctl->a_full[i]), 32 * NUM_PRODUCER_WARPS);
+            ptx::mbar_init(ptx::smem_addr(&ctl->a_full[i]), 128);
             ptx::mbar_init(ptx::smem_addr(&ctl->b_full[i]), 1);
             ptx::mbar_init(ptx::smem_addr(&ctl->empty[i]), 1);
         }
         for (int i = 0; i < NSLOT; ++i) {
             ptx::mbar_init(ptx::smem_addr(&ctl->acc_full[i]), 1);
-            ptx::mbar_init(ptx::smem_addr(&ctl->acc_empty[i]), 32 * NUM_EPI_WARPS);
+            ptx::mbar_init(ptx::smem_addr(&ctl->acc_empty[i]), NUM_EPI_THREADS);
         }
         ptx::mbar_init(ptx::smem_addr(&ctl->mma_done), 1);
         ctl->abort_flag = 0;
         ptx::fence_mbar_init();
     }
     if (warp == MMA_WARP) {
-        ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), TMEM_COLS);
+        ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), Cfg::TMEM_COLS);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
@@ -229,51 +249,70 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
     const uint32_t tmem_base = ctl->tmem_base;
     const uint64_t limit = a.wait_limit_ns;
 
-    if (warp < NUM_PRODUCER_WARPS) {
+    if (warp < 4) {
         // ------------------------------------------------------------ producers
+        ptx::setmaxnreg_dec<PRODUCER_REGS>();
         const int row = threadIdx.x;  // 0..127
         const uint32_t row_off = (uint32_t)row * 128u;
         const uint32_t swz = (uint32_t)(row & 7);
+        const int my_tiles = blockIdx.x < a.num_tiles ? (a.num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+        const int total = my_tiles * a.k_steps;
         LoadCursor cur;
         cursor_set_tile(cur, a, blockIdx.x, row);
-        uint4 nxt[4];
-        if (cur.tile < a.num_tiles) cursor_load(cur, a, nxt);
+        uint4 pf[PREFETCH][4];
+#pragma unroll
+        for (int d = 0; d < PREFETCH; ++d) {
+            if (cur.tile < a.num_tiles) {
+                cursor_load(cur, a, pf[d]);
+                cursor_advance(cur, a, row);
+            }
+        }
         int stage = 0;
         uint32_t phase = 0;
         int b_tile = blockIdx.x, b_j = 0;  // filter block cursor (thread 0 only)
         int64_t b_issued = 0;
-        while (cur.tile < a.num_tiles) {
-            uint4 v[4];
+        bool ok = true;
+        for (int it = 0; it < total && ok; it += PREFETCH) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) v[i] = nxt[i];
-            cursor_advance(cur, a, row);
-            if (cur.tile < a.num_tiles) cursor_load(cur, a, nxt);  // next item in flight
-            if (!wait_phase(ptx::smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, limit, a.status)) break;
-            if (threadIdx.x == 0) {
-                const uint32_t bar = ptx::smem_addr(&ctl->b_full[stage]);
-                ptx::mbar_arrive_expect_tx(bar, B_BYTES);
-                const int nt = b_tile % a.n_tiles;
-                const uint8_t *src = a.wp + ((size_t)nt * a.k_steps + b_j) * (size_t)B_BYTES;
-                ptx::bulk_copy_g2s(b_smem + stage * B_BYTES, src, B_BYTES, bar);
-                ++b_issued;
-                if (++b_j == a.k_steps) {
-                    b_j = 0;
-                    b_tile += gridDim.x;
+            for (int d = 0; d < PREFETCH; ++d) {
+                if (it + d >= total) break;
+                uint4 v[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) v[i] = pf[d][i];
+                if (cur.tile < a.num_tiles) {  // keep PREFETCH items in flight
+                    cursor_load(cur, a, pf[d]);
+                    cursor_advance(cur, a, row);
                 }
-            }
-            const uint32_t dst = a_smem + stage * A_BYTES + row_off;
+                if (!wait_phase(ptx::smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, limit, a.status)) {
+                    ok = false;
+                    break;
+                }
+                if (threadIdx.x == 0) {
+                    const uint32_t bar = ptx::smem_addr(&ctl->b_full[stage]);
+                    ptx::mbar_arrive_expect_tx(bar, B_BYTES);
+                    const int nt = b_tile % a.n_tiles;
+                    const uint8_t *src = a.wp + ((size_t)nt * a.k_steps + b_j) * (size_t)B_BYTES;
+                    ptx::bulk_copy_g2s(b_smem + stage * B_BYTES, src, B_BYTES, bar);
+                    ++b_issued;
+                    if (++b_j == a.k_steps) {
+                        b_j = 0;
+                        b_tile += gridDim.x;
+                    }
+                }
+                const uint32_t dst = a_smem + stage * A_BYTES + row_off;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                uint4 lo, hi;
-                cvt16(v[i], lo, hi);
-                ptx::st_shared_v4(dst + ((((uint32_t)(2 * i)) ^ swz) << 4), lo);
-                ptx::st_shared_v4(dst + ((((uint32_t)(2 * i + 1)) ^ swz) << 4), hi);
-            }
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(ptx::smem_addr(&ctl->a_full[stage]));
-            if (++stage == STAGES) {
-                stage = 0;
-                phase ^= 1u;
+                for (int i = 0; i < 4; ++i) {
+                    uint4 lo, hi;
+                    cvt16(v[i], lo, hi);
+                    ptx::st_shared_v4(dst + ((((uint32_t)(2 * i)) ^ swz) << 4), lo);
+                    ptx::st_shared_v4(dst + ((((uint32_t)(2 * i + 1)) ^ swz) << 4), hi);
+                }
+                ptx::fence_proxy_async_smem();
+                ptx::mbar_arrive(ptx::smem_addr(&ctl->a_full[stage]));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
         }
         if (threadIdx.x == 0 && *abort_flag) {
@@ -282,12 +321,14 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
             // (copies into s) - 1 of b_full[s], and phases complete in order
             for (int s = 0; s < STAGES; ++s) {
                 const int64_t n_s = b_issued / STAGES + (s < b_issued % STAGES ? 1 : 0);
-                if (n_s > 0) (void)drain_phase(ptx::smem_addr(&ctl->b_full[s]), (uint32_t)((n_s - 1) & 1), limit, a.status);
+                if (n_s > 0)
+                    (void)drain_phase(ptx::smem_addr(&ctl->b_full[s]), (uint32_t)((n_s - 1) & 1), limit, a.status);
             }
         }
-    } else if (warp == MMA_WARP) {
+    } else if (warp < FIRST_EPI_WARP) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        ptx::setmaxnreg_dec<PRODUCER_REGS>();
+        if (warp == MMA_WARP && lane == 0) {
             constexpr uint32_t idesc = ptx::idesc_f16_f32(MT, NT);
             int stage = 0;
             uint32_t phase = 0;
@@ -338,9 +379,11 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        const int quad = warp & 3;  // tensor-memory lanes this warp may access
+        ptx::setmaxnreg_inc<EPILOGUE_REGS>();
+        const int quad = warp & 3;                      // tensor-memory lanes this warp may access
+        const int col0 = ((warp - FIRST_EPI_WARP) >> 2) * HALF;  // this warp's half of the columns
         const int row = quad * 32 + lane;
-        const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
+        const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)col0;
         uint32_t gi = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
@@ -357,9 +400,9 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 const int q = rem - p * a.Q;
                 yoff = (int64_t)n * a.ys_n + (int64_t)p * a.ys_p + (int64_t)q * a.ys_q;
             }
-            int32_t acc[NT];
+            int32_t acc[HALF];
 #pragma unroll
-            for (int i = 0; i < NT; ++i) acc[i] = 0;
+            for (int i = 0; i < HALF; ++i) acc[i] = 0;
             for (int g = 0; g < a.groups; ++g) {
                 const uint32_t slot = gi % NSLOT;
                 const uint32_t aph = (gi / NSLOT) & 1u;
@@ -371,7 +414,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 }
                 ptx::tc_fence_after();
 #pragma unroll
-                for (int cc = 0; cc < NT / 32; ++cc) {
+                for (int cc = 0; cc < HALF / 32; ++cc) {
                     uint32_t v[32];
                     ptx::tmem_ld_32x32b_x32(lane_base + slot * NT + cc * 32, v);
                     ptx::tmem_ld_wait();
@@ -384,10 +427,10 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
             }
             if (!ok) break;
             if (valid) {
-                const int k0 = nt * NT;
+                const int k0 = nt * NT + col0;
                 int32_t *yrow = a.y + yoff;
 #pragma unroll
-                for (int c4 = 0; c4 < NT / 4; ++c4) {
+                for (int c4 = 0; c4 < HALF / 4; ++c4) {
                     const int k = k0 + c4 * 4;
                     int32_t o[4];
 #pragma unroll
@@ -412,7 +455,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    if (warp == MMA_WARP) ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    if (warp == MMA_WARP) ptx::tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
 // ---------------------------------------------------------------- filter repack
@@ -421,18 +464,18 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
 // CONVOLUTION), each row's 16-byte chunk i stored at chunk position
 // i ^ (row % 8): the image of the shared-memory stage, copied as one block.
 __global__ void igemm_pack_filter_kernel(const int8_t *w, int64_t ws0, int64_t ws1, int64_t ws2, int64_t ws3,
-                                         int32_t K, int32_t C, int32_t R, int32_t S, int32_t mode,
-                                         int32_t c_steps, int32_t k_steps, int32_t n_tiles, uint8_t *wp) {
-    const int64_t total = (int64_t)n_tiles * k_steps * NT * 8;
+                                         int32_t K, int32_t C, int32_t R, int32_t S, int32_t mode, int32_t c_steps,
+                                         int32_t k_steps, int32_t n_tiles, int32_t nt_rows, uint8_t *wp) {
+    const int64_t total = (int64_t)n_tiles * k_steps * nt_rows * 8;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
         const int chunk = (int)(idx & 7);
         const int64_t t = idx >> 3;
-        const int nl = (int)(t % NT);
-        const int64_t t2 = t / NT;
+        const int nl = (int)(t % nt_rows);
+        const int64_t t2 = t / nt_rows;
         const int j = (int)(t2 % k_steps);
         const int nt = (int)(t2 / k_steps);
-        const int k = nt * NT + nl;
+        const int k = nt * nt_rows + nl;
         const int tap = j / c_steps;
         const int cb = j - tap * c_steps;
         const int r = tap / S;
@@ -448,12 +491,13 @@ __global__ void igemm_pack_filter_kernel(const int8_t *w, int64_t ws0, int64_t w
             for (int b = 0; b < 2; ++b) {
                 const int c = c0 + 2 * e + b;
                 int v = 0;
-                if (k < K && c < C) v = w[(int64_t)k * ws0 + (int64_t)c * ws1 + (int64_t)rf * ws2 + (int64_t)sf * ws3];
+                if (k < K && c < C)
+                    v = w[(int64_t)k * ws0 + (int64_t)c * ws1 + (int64_t)rf * ws2 + (int64_t)sf * ws3];
                 hv[b] = __half_as_ushort(__int2half_rn(v));
             }
             words[e] = (uint32_t)hv[0] | ((uint32_t)hv[1] << 16);
         }
-        uint8_t *dst = wp + ((t2 * NT + nl) * 128) + (((chunk ^ (nl & 7))) << 4);
+        uint8_t *dst = wp + ((t2 * nt_rows + nl) * 128) + (((chunk ^ (nl & 7))) << 4);
         *reinterpret_cast<uint4 *>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
     }
 }
@@ -494,6 +538,22 @@ __global__ void igemm_pack_image_kernel(const int8_t *x, int64_t xs0, int64_t xs
 
 inline int64_t align256(int64_t v) { return (v + 255) & ~255LL; }
 
+template <int NT>
+conv_status launch_conv(const IgemmArgs &a, int grid, cudaStream_t st) {
+    using Cfg = TileCfg<NT>;
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        if (cudaFuncSetAttribute(igemm_conv_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::SMEM_BYTES) != cudaSuccess)
+            return CONV_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    igemm_conv_kernel<NT><<<grid, THREADS, Cfg::SMEM_BYTES, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}
+
 }  // namespace
 
 bool igemm_supported(const ConvGeom &g) {
@@ -513,12 +573,13 @@ void igemm_plan(const ConvGeom &g, const void *x_dev, IgemmPlan *pl) {
     const bool direct = g.xs[1] == 1 && (g.C % 16) == 0 && (g.xs[0] % 16) == 0 && (g.xs[2] % 16) == 0 &&
                         (g.xs[3] % 16) == 0 && (x_dev == nullptr || ((uintptr_t)x_dev % 16) == 0);
     pl->pack_x = !direct;
+    pl->n_tile = g.K > 128 ? 256 : 128;
     pl->c16 = (g.C + 15) / 16 * 16;
     pl->c_steps = (g.C + KS - 1) / KS;
     pl->k_steps = g.R * g.S * pl->c_steps;
-    pl->n_tiles = (g.K + NT - 1) / NT;
+    pl->n_tiles = (g.K + pl->n_tile - 1) / pl->n_tile;
     pl->m_tiles = (g.N * g.P * g.Q + MT - 1) / MT;
-    pl->wpack_bytes = (size_t)align256(pl->n_tiles * pl->k_steps * (int64_t)B_BYTES);
+    pl->wpack_bytes = (size_t)align256(pl->n_tiles * pl->k_steps * pl->n_tile * (int64_t)(KS * 2));
     pl->xpack_bytes = pl->pack_x ? (size_t)align256(g.N * g.H * g.W * pl->c16) : 0;
     pl->workspace_bytes = pl->wpack_bytes + pl->xpack_bytes;
 }
@@ -528,13 +589,13 @@ conv_status igemm_pack_filter_launch(const ConvGeom &g, const IgemmPlan &pl, con
     cudaStream_t st = (cudaStream_t)stream;
     const int sms = device_sm_count();
     uint8_t *wp = static_cast<uint8_t *>(workspace);
-    const int64_t total = pl.n_tiles * pl.k_steps * NT * 8;
+    const int64_t total = pl.n_tiles * pl.k_steps * pl.n_tile * 8;
     int64_t blocks = (total + 255) / 256;
     if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
     if (blocks == 0) return CONV_OK;
     igemm_pack_filter_kernel<<<(unsigned)blocks, 256, 0, st>>>(
         w, g.ws[0], g.ws[1], g.ws[2], g.ws[3], (int32_t)g.K, (int32_t)g.C, (int32_t)g.R, (int32_t)g.S, g.mode,
-        (int32_t)pl.c_steps, (int32_t)pl.k_steps, (int32_t)pl.n_tiles, wp);
+        (int32_t)pl.c_steps, (int32_t)pl.k_steps, (int32_t)pl.n_tiles, (int32_t)pl.n_tile, wp);
     return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
@@ -588,19 +649,8 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
     a.status = device_status_word();
     if (!a.status) return CONV_ERR_CUDA;
     if (a.num_tiles == 0) return CONV_OK;
-
-    static bool attr_set[64] = {false};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(igemm_conv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-            cudaSuccess)
-            return CONV_ERR_CUDA;
-        attr_set[dev] = true;
-    }
     const int grid = a.num_tiles < sms ? a.num_tiles : sms;
-    igemm_conv_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(a);
-    return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+    return pl.n_tile == 256 ? launch_conv<256>(a, grid, st) : launch_conv<128>(a, grid, st);
 }
 
 }  // namespace i8c

@@ -30,15 +30,15 @@ void make_geom(const conv_tensor_desc *x, const conv_tensor_desc *w, const conv_
 int64_t desc_extent_elems(const conv_tensor_desc *d);
 
 // ---------------------------------------------------------------- igemm
-// Tile shape of the tensor-core kernel: 128 output pixels x kIgemmNTile
-// output channels, reduction consumed 64 channels (one 128-byte row of f16)
-// at a time.
+// Tile shape of the tensor-core kernel: 128 output pixels x n_tile (128 or
+// 256) output channels, reduction consumed 64 channels (one 128-byte row of
+// f16) at a time.
 constexpr int kIgemmMTile = 128;
-constexpr int kIgemmNTile = 128;
 constexpr int kIgemmKStep = 64;
 
 struct IgemmPlan {
     bool pack_x;            // image must be copied to channels-last first
+    int64_t n_tile;         // output channels per tile (128 or 256)
     int64_t c16;            // channel count rounded up to 16 (valid load width)
     int64_t c_steps;        // ceil(C / 64)
     int64_t k_steps;        // R * S * c_steps
