@@ -66,7 +66,8 @@ typedef enum {
     CONV_ERR_WORKSPACE = 13,          /* workspace NULL or smaller than conv_fprop_workspace_size */
     CONV_ERR_UNSUPPORTED_DEVICE = 14, /* the current device is not sm_103 */
     CONV_ERR_OVERLAP = 15,            /* output bytes overlap an input or the workspace */
-    CONV_ERR_TOO_LARGE = 16           /* an extent or offset exceeds the library's index range */
+    CONV_ERR_TOO_LARGE = 16,          /* an extent or offset exceeds the library's index range */
+    CONV_ERR_STATIC_WORKSPACE_LIMIT = 17 /* call needs more scratch than CONV_STATIC_WORKSPACE_BYTES */
 } conv_status;
 
 typedef enum { CONV_INT8 = 1, CONV_INT32 = 2 } conv_dtype;
@@ -191,6 +192,37 @@ conv_status conv_fprop_prepacked(const conv_tensor_desc *x, const int8_t *x_dev,
                                  const conv_tensor_desc *y, int32_t *y_dev,
                                  const int32_t *bias_dev, const conv_fprop_params *p,
                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * conv_fprop without a caller-provided workspace.  (The pages have no
+ * counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory: a plugin whose host framework owns all device
+ * allocations and hands none to it, or a latency-critical loop that must not
+ * call cudaMalloc, which may synchronise the device.)
+ *
+ * Same arguments and results as conv_fprop, minus the workspace: the scratch
+ * (the repacked filter and, when the image strides need it, a channels-last
+ * image copy) lives in a device array of CONV_STATIC_WORKSPACE_BYTES that is
+ * part of the library, so every GPU that loads the library holds that much
+ * memory until the process exits.  Calls needing more scratch than that
+ * return CONV_ERR_STATIC_WORKSPACE_LIMIT and launch nothing
+ * (conv_fprop_workspace_size tells the need in advance).  It allocates
+ * nothing: no cudaMalloc, cudaFree or allocating library routine.
+ *
+ * The first call on a device looks up that device's copy of the array (one
+ * cudaGetSymbolAddress with the device current), so make that first call
+ * before any stream capture.  Every call shares the one array and the
+ * kernels overwrite all scratch they read, so nothing needs clearing between
+ * calls; but calls whose work overlaps on the GPU (different streams, or
+ * different host threads) race on the array: order them on one stream.
+ */
+#define CONV_STATIC_WORKSPACE_BYTES (32u << 20)
+
+conv_status conv_fprop_static_workspace(const conv_tensor_desc *x, const int8_t *x_dev,
+                                        const conv_tensor_desc *w, const int8_t *w_dev,
+                                        const conv_tensor_desc *y, int32_t *y_dev,
+                                        const int32_t *bias_dev, const conv_fprop_params *p,
+                                        void *stream);
 
 /* Synchronise `stream`, then read and clear the current device's status
  * word: CONV_OK, or CONV_ERR_DEVICE_TIMEOUT if a kernel gave up waiting

@@ -37,14 +37,15 @@ STATUS = {
     7: "CONV_ERR_BAD_PARAM", 8: "CONV_ERR_OVERFLOW_RISK", 9: "CONV_ERR_UNSUPPORTED_COMPUTE",
     10: "CONV_ERR_ALIGNMENT", 11: "CONV_ERR_CUDA", 12: "CONV_ERR_DEVICE_TIMEOUT",
     13: "CONV_ERR_WORKSPACE", 14: "CONV_ERR_UNSUPPORTED_DEVICE", 15: "CONV_ERR_OVERLAP",
-    16: "CONV_ERR_TOO_LARGE",
+    16: "CONV_ERR_TOO_LARGE", 17: "CONV_ERR_STATIC_WORKSPACE_LIMIT",
 }
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 
 EXPORTED_SYMBOLS = (
     "conv_params_init", "conv_params_set_symmetric_padding", "conv_tensor_desc_packed",
     "conv_fprop_output_dims", "conv_fprop_validate", "conv_fprop_plan", "conv_fprop_workspace_size",
-    "conv_fprop", "conv_fprop_pack_filter", "conv_fprop_prepacked", "conv_device_status",
+    "conv_fprop", "conv_fprop_pack_filter", "conv_fprop_prepacked", "conv_fprop_static_workspace",
+    "conv_device_status",
     "conv_selftest_wait_timeout", "conv_status_string", "conv_library_version",
 )
 
@@ -145,6 +146,8 @@ def lib():
         L.conv_fprop_pack_filter.argtypes = [D, D, ctypes.c_void_p, D, P, ctypes.c_void_p, ctypes.c_size_t,
                                              ctypes.c_void_p]
         L.conv_fprop_prepacked.argtypes = list(L.conv_fprop.argtypes)
+        L.conv_fprop_static_workspace.argtypes = [D, ctypes.c_void_p, D, ctypes.c_void_p, D, ctypes.c_void_p,
+                                                  ctypes.c_void_p, P, ctypes.c_void_p]
         L.conv_device_status.argtypes = [ctypes.c_void_p]
         L.conv_selftest_wait_timeout.argtypes = [ctypes.c_uint32, ctypes.c_void_p]
         L.conv_status_string.argtypes = [ctypes.c_int]
@@ -152,7 +155,8 @@ def lib():
         L.conv_library_version.restype = ctypes.c_int32
         for name in ("conv_tensor_desc_packed", "conv_fprop_output_dims", "conv_fprop_validate",
                      "conv_fprop_plan", "conv_fprop_workspace_size", "conv_fprop", "conv_fprop_pack_filter",
-                     "conv_fprop_prepacked", "conv_device_status", "conv_selftest_wait_timeout"):
+                     "conv_fprop_prepacked", "conv_fprop_static_workspace", "conv_device_status",
+                     "conv_selftest_wait_timeout"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -215,6 +219,14 @@ def conv_fprop_prepacked_raw(xd: TensorDesc, x_ptr: int, wd: TensorDesc, w_ptr: 
     return int(lib().conv_fprop_prepacked(ctypes.byref(xd), x_ptr, ctypes.byref(wd), w_ptr, ctypes.byref(yd),
                                           y_ptr, bias_ptr or None, ctypes.byref(p), workspace_ptr or None,
                                           int(workspace_bytes), stream or None))
+
+
+def conv_fprop_static_workspace_raw(xd: TensorDesc, x_ptr: int, wd: TensorDesc, w_ptr: int, yd: TensorDesc,
+                                    y_ptr: int, bias_ptr: int, p: Params, stream: int) -> int:
+    """conv_fprop with the library's own static scratch array instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    return int(lib().conv_fprop_static_workspace(ctypes.byref(xd), x_ptr, ctypes.byref(wd), w_ptr, ctypes.byref(yd),
+                                                 y_ptr, bias_ptr or None, ctypes.byref(p), stream or None))
 
 
 def device_status(stream: int = 0) -> int:

@@ -126,6 +126,19 @@ __global__ void selftest_wait_kernel(uint64_t limit_ns, int *status) {
 }
 
 }  // namespace
+
+conv_status conv_fprop_workspace_size_for(const conv_tensor_desc *x, const void *x_dev, const conv_tensor_desc *w,
+                                          const conv_tensor_desc *y, const conv_fprop_params *p, size_t *bytes) {
+    if (!bytes) return CONV_ERR_NULL_PTR;
+    ConvGeom g;
+    IgemmPlan pl;
+    int algo = 0;
+    conv_status st = plan_call(x, w, y, p, x_dev, &g, &algo, &pl);
+    if (st) return st;
+    *bytes = (algo == CONV_ALGO_IMPLICIT_GEMM && g.N > 0 && g.K > 0) ? pl.workspace_bytes : 0;
+    return CONV_OK;
+}
+
 }  // namespace i8c
 
 using namespace i8c;

@@ -241,6 +241,8 @@ const char *conv_status_string(conv_status s) {
         case CONV_ERR_UNSUPPORTED_DEVICE: return "CONV_ERR_UNSUPPORTED_DEVICE: current device is not sm_103";
         case CONV_ERR_OVERLAP: return "CONV_ERR_OVERLAP: output overlaps an input or the workspace";
         case CONV_ERR_TOO_LARGE: return "CONV_ERR_TOO_LARGE: extent beyond the library's index range";
+        case CONV_ERR_STATIC_WORKSPACE_LIMIT:
+            return "CONV_ERR_STATIC_WORKSPACE_LIMIT: the call needs more scratch than the library's static array";
     }
     return "unknown conv_status";
 }

@@ -66,6 +66,11 @@ conv_status dp4a_launch(const ConvGeom &g, const int8_t *x, const int8_t *w, int
 conv_status generic_launch(const ConvGeom &g, const int8_t *x, const int8_t *w, int32_t *y,
                            const int32_t *bias, void *stream);
 
+// Workspace bytes a call needs given the actual image pointer (a misaligned
+// pointer needs the channels-last image copy too).
+conv_status conv_fprop_workspace_size_for(const conv_tensor_desc *x, const void *x_dev, const conv_tensor_desc *w,
+                                          const conv_tensor_desc *y, const conv_fprop_params *p, size_t *bytes);
+
 // ---------------------------------------------------------------- device
 // Current device is an sm_103 part (cached per device).
 conv_status check_device();
