@@ -79,7 +79,12 @@ typedef enum {
     CONV_ALGO_AUTO = 0,
     CONV_ALGO_IMPLICIT_GEMM = 1, /* tcgen05 tensor-core implicit GEMM */
     CONV_ALGO_DIRECT_DP4A = 2,   /* CUDA-core direct kernel, 4-way int8 dot products */
-    CONV_ALGO_DIRECT_GENERIC = 3 /* CUDA-core direct kernel, any strides */
+    CONV_ALGO_DIRECT_GENERIC = 3, /* CUDA-core direct kernel, any strides */
+    /* the tensor-core kernel with the image gathered by per-thread global
+       loads instead of TMA im2col tiles (what CONV_ALGO_IMPLICIT_GEMM falls
+       back to when a TMA im2col map cannot express the call: stride > 8,
+       padding or reach beyond the map's corner range) */
+    CONV_ALGO_IMPLICIT_GEMM_GLOBAL_LOADS = 4
 } conv_algo;
 
 /* Epilogue flags (bit set). */

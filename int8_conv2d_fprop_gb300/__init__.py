@@ -27,9 +27,11 @@ _lib = None
 CONV_INT8, CONV_INT32 = 1, 2
 CROSS_CORRELATION, CONVOLUTION = 0, 1
 ALGO_AUTO, ALGO_IMPLICIT_GEMM, ALGO_DIRECT_DP4A, ALGO_DIRECT_GENERIC = 0, 1, 2, 3
+ALGO_IMPLICIT_GEMM_GLOBAL_LOADS = 4
 EPILOGUE_BIAS, EPILOGUE_RELU = 1, 2
 ALGO_NAMES = {ALGO_IMPLICIT_GEMM: "implicit_gemm", ALGO_DIRECT_DP4A: "direct_dp4a",
-              ALGO_DIRECT_GENERIC: "direct_generic"}
+              ALGO_DIRECT_GENERIC: "direct_generic",
+              ALGO_IMPLICIT_GEMM_GLOBAL_LOADS: "implicit_gemm_global_loads"}
 
 STATUS = {
     0: "CONV_OK", 1: "CONV_ERR_NULL_PTR", 2: "CONV_ERR_RANK", 3: "CONV_ERR_DTYPE",

@@ -94,10 +94,14 @@ conv_status plan_call(const conv_tensor_desc *x, const conv_tensor_desc *w, cons
     conv_status st = conv_fprop_validate(x, w, y, p, bias_elems);
     if (st) return st;
     make_geom(x, w, y, p, g);
-    *algo = choose_algo(*g, p->algo);
+    const bool global_loads = p->algo == CONV_ALGO_IMPLICIT_GEMM_GLOBAL_LOADS;
+    *algo = choose_algo(*g, global_loads ? CONV_ALGO_IMPLICIT_GEMM : p->algo);
     if (*algo == CONV_ALGO_IMPLICIT_GEMM && !igemm_supported(*g)) return CONV_ERR_ALIGNMENT;
     if (*algo == CONV_ALGO_DIRECT_DP4A && !dp4a_supported(*g)) return CONV_ERR_ALIGNMENT;
-    if (*algo == CONV_ALGO_IMPLICIT_GEMM) igemm_plan(*g, x_dev, pl);
+    if (*algo == CONV_ALGO_IMPLICIT_GEMM) {
+        igemm_plan(*g, x_dev, pl);
+        pl->register_loads = global_loads;
+    }
     return CONV_OK;
 }
 
@@ -153,7 +157,7 @@ conv_status conv_fprop_plan(const conv_tensor_desc *x, const conv_tensor_desc *w
     int algo = 0;
     conv_status st = plan_call(x, w, y, p, nullptr, &g, &algo, &pl);
     if (st) return st;
-    *algo_out = algo;
+    *algo_out = (algo == CONV_ALGO_IMPLICIT_GEMM && pl.register_loads) ? CONV_ALGO_IMPLICIT_GEMM_GLOBAL_LOADS : algo;
     return CONV_OK;
 }
 

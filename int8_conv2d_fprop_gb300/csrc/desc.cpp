@@ -95,7 +95,7 @@ static conv_status check_params(const conv_fprop_params *p) {
     }
     if (p->mode != CONV_CROSS_CORRELATION && p->mode != CONV_CONVOLUTION) return CONV_ERR_BAD_PARAM;
     if (p->epilogue & ~(CONV_EPILOGUE_BIAS | CONV_EPILOGUE_RELU)) return CONV_ERR_BAD_PARAM;
-    if (p->algo < CONV_ALGO_AUTO || p->algo > CONV_ALGO_DIRECT_GENERIC) return CONV_ERR_BAD_PARAM;
+    if (p->algo < CONV_ALGO_AUTO || p->algo > CONV_ALGO_IMPLICIT_GEMM_GLOBAL_LOADS) return CONV_ERR_BAD_PARAM;
     return CONV_OK;
 }
 

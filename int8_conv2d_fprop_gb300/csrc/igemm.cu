@@ -16,18 +16,19 @@
 // registers.  The result is bit-identical to integer arithmetic.
 //
 // Persistent, warp-specialised CTA (one per SM), 512 threads, tile 128 pixels
-// x NT output channels (NT = 128 or 256):
-//   warpgroup 0  producers: each thread owns one pixel row of the A tile; it
-//                gathers 64 channels of one tap with 16-byte loads (the im2col
-//                address formed on the fly from stride, padding and
-//                dilation), two items ahead of the one it stores, converts
-//                int8 -> f16 in registers and writes the row into the
-//                128-byte-swizzled shared-memory stage.  Thread 0 also brings
-//                the matching pre-swizzled f16 filter block with one bulk
-//                async copy.
-//   warpgroup 1  warp 4 allocates tensor memory; its lane 0 issues
-//                tcgen05.mma (M=128, N=NT, K=16 per instruction) into one of
-//                two accumulator slots.  Warps 5-7 have no role.
+// x NT output channels (NT = 128 or 256).  Two ways to stage the image tile:
+//  * TMA (default): warp 5 lane 0 issues one TMA im2col load per k-step (128
+//    output pixels x 64 channels of one tap, zero outside the image) into an
+//    8-deep int8 staging ring; warpgroup 0 converts each staged tile to f16
+//    into the 128-byte-swizzled A stage; warp 6 lane 0 brings the matching
+//    pre-swizzled f16 filter block with one bulk async copy.
+//  * global loads (fallback when an im2col map cannot express the call):
+//    warpgroup 0 threads each own one pixel row, gather 64 channels of one tap
+//    with 16-byte loads two items ahead (address formed from stride, padding
+//    and dilation), convert in registers and write the row; thread 0 also
+//    issues the filter block copies.
+// In both, warp 4 allocates tensor memory and its lane 0 issues tcgen05.mma
+// (M=128, N=NT, K=16 per instruction) into one of two accumulator slots:
 //   warpgroups 2-3  epilogue, two warps per tensor-memory lane quadrant, each
 //                owning NT/2 columns: tcgen05.ld each finished slot,
 //                f32 -> int32, sum the groups, add bias, ReLU, store int32.
@@ -35,8 +36,12 @@
 // Every wait is bounded in time; on expiry the CTA records
 // CONV_ERR_DEVICE_TIMEOUT, stops, lets issued copies and MMAs finish and frees
 // its tensor memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
 
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -57,19 +62,28 @@ constexpr int NUM_EPI_THREADS = 256;
 constexpr int PRODUCER_REGS = 80;
 constexpr int EPILOGUE_REGS = 176;
 static_assert(2 * 128 * PRODUCER_REGS + 2 * 128 * EPILOGUE_REGS <= 65536, "register split exceeds the launch");
-constexpr int PREFETCH = 2;  // items in flight ahead of the one being stored
+constexpr int PREFETCH = 2;  // register path: items in flight ahead of the one being stored
+constexpr int STG_BYTES = MT * KS;  // one int8 im2col tile: 128 pixels x 64 channels
+constexpr int A_ISSUER_WARP = 5;    // TMA path: issues the im2col loads
+constexpr int B_ISSUER_WARP = 6;    // TMA path: issues the filter block copies
 
-template <int NT>
+// kTma: the int8 image tile arrives by TMA (im2col mode) in a ring of
+// STG_STAGES staging buffers and the producer warps convert it shared ->
+// shared; otherwise the producer warps gather it with global loads.
+template <int NT, bool kTma>
 struct TileCfg {
     static constexpr int B_BYTES = NT * KS * 2;
-    static constexpr int STAGES = NT == 256 ? 4 : 6;
+    static constexpr int STAGES = kTma ? (NT == 256 ? 3 : 4) : (NT == 256 ? 4 : 6);
+    static constexpr int STG_STAGES = kTma ? 8 : 0;
     static constexpr int TMEM_COLS = NSLOT * NT;
-    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + STAGES * (A_BYTES + B_BYTES) + 256 /*barriers*/;
+    static constexpr int SMEM_BYTES =
+        1024 /*align slack*/ + STAGES * (A_BYTES + B_BYTES) + STG_STAGES * STG_BYTES + 512 /*barriers*/;
     static_assert(TMEM_COLS <= 512, "tensor memory has 512 columns");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
 struct IgemmArgs {
+    CUtensorMap tmap_x;  // im2col map of the channels-last image (TMA path only)
     const int8_t *x;     // channels-last image
     const uint8_t *wp;   // repacked f16 filter blocks
     int32_t *y;
@@ -91,13 +105,15 @@ struct SharedCtl {
     uint64_t a_full[STAGES];
     uint64_t b_full[STAGES];
     uint64_t empty[STAGES];
+    uint64_t stg_full[8];   // TMA path: im2col tile landed
+    uint64_t stg_empty[8];  // TMA path: im2col tile converted
     uint64_t acc_full[NSLOT];
     uint64_t acc_empty[NSLOT];
     uint64_t mma_done;
     uint32_t tmem_base;
     int32_t abort_flag;
 };
-static_assert(sizeof(SharedCtl<6>) <= 256, "control block too large");
+static_assert(sizeof(SharedCtl<6>) <= 512, "control block too large");
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting or
 // the time limit passed (then the CTA is marked aborting and the device status
@@ -207,10 +223,21 @@ __device__ __forceinline__ void cursor_advance(LoadCursor &c, const IgemmArgs &a
     }
 }
 
-template <int NT>
+// Lets every copy issued into a ring of `depth` slots land: the newest copy
+// into slot s completes phase (copies into s) - 1, and phases complete in
+// order.
+__device__ __forceinline__ void drain_ring(uint64_t *bars, int depth, int64_t issued, uint64_t limit, int *status) {
+    for (int s = 0; s < depth; ++s) {
+        const int64_t n_s = issued / depth + (s < issued % depth ? 1 : 0);
+        if (n_s > 0) (void)drain_phase(ptx::smem_addr(&bars[s]), (uint32_t)((n_s - 1) & 1), limit, status);
+    }
+}
+
+template <int NT, bool kTma>
 __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_constant__ IgemmArgs a) {
-    using Cfg = TileCfg<NT>;
+    using Cfg = TileCfg<NT, kTma>;
     constexpr int STAGES = Cfg::STAGES;
+    constexpr int STG = Cfg::STG_STAGES;
     constexpr int B_BYTES = Cfg::B_BYTES;
     constexpr int HALF = NT / 2;  // columns per epilogue thread
     extern __shared__ uint8_t smem_raw[];
@@ -219,11 +246,15 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
     uint8_t *const base_ptr = smem_raw + (base - raw_addr);
     const uint32_t a_smem = base;
     const uint32_t b_smem = base + STAGES * A_BYTES;
-    SharedCtl<STAGES> *ctl = reinterpret_cast<SharedCtl<STAGES> *>(base_ptr + STAGES * (A_BYTES + B_BYTES));
+    const uint32_t stg_smem = base + STAGES * (A_BYTES + B_BYTES);
+    SharedCtl<STAGES> *ctl =
+        reinterpret_cast<SharedCtl<STAGES> *>(base_ptr + STAGES * (A_BYTES + B_BYTES) + STG * STG_BYTES);
     volatile int32_t *abort_flag = &ctl->abort_flag;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int my_tiles = blockIdx.x < a.num_tiles ? (a.num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int total = my_tiles * a.k_steps;  // (tile, k-step) items of this CTA
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
@@ -231,6 +262,11 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
             ptx::mbar_init(ptx::smem_addr(&ctl->b_full[i]), 1);
             ptx::mbar_init(ptx::smem_addr(&ctl->empty[i]), 1);
         }
+        for (int i = 0; i < STG; ++i) {
+            ptx::mbar_init(ptx::smem_addr(&ctl->stg_full[i]), 1);
+            ptx::mbar_init(ptx::smem_addr(&ctl->stg_empty[i]), 128);
+        }
+        if (kTma) ptx::prefetch_tensormap(&a.tmap_x);
         for (int i = 0; i < NSLOT; ++i) {
             ptx::mbar_init(ptx::smem_addr(&ctl->acc_full[i]), 1);
             ptx::mbar_init(ptx::smem_addr(&ctl->acc_empty[i]), NUM_EPI_THREADS);
@@ -249,14 +285,51 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
     const uint32_t tmem_base = ctl->tmem_base;
     const uint64_t limit = a.wait_limit_ns;
 
-    if (warp < 4) {
+    if (warp < 4 && kTma) {
+        // ------------------------------------------------------------ converters
+        // The im2col tile in staging holds pixel row i at i*64 bytes.  Four
+        // neighbouring lanes take the four 16-byte chunks of one row, so a
+        // warp reads 8 whole rows per instruction and writes them to the
+        // swizzled f16 stage without bank conflicts.
+        ptx::setmaxnreg_dec<PRODUCER_REGS>();
+        const uint32_t chunk = threadIdx.x & 3;
+        const int row0 = (warp << 5) + (lane >> 2);
+        int stage = 0, s8 = 0;
+        uint32_t phase = 0, ph8 = 0;
+        for (int it = 0; it < total; ++it) {
+            if (!wait_phase(ptx::smem_addr(&ctl->stg_full[s8]), ph8, abort_flag, limit, a.status)) break;
+            if (!wait_phase(ptx::smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, limit, a.status)) break;
+            const uint32_t src = stg_smem + s8 * STG_BYTES + chunk * 16u;
+            const uint32_t dst = a_smem + stage * A_BYTES;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t row = (uint32_t)(row0 + 8 * i);
+                const uint4 v = ptx::ld_shared_v4(src + row * 64u);
+                uint4 lo, hi;
+                cvt16(v, lo, hi);
+                const uint32_t rdst = dst + row * 128u;
+                const uint32_t swz = row & 7u;
+                ptx::st_shared_v4(rdst + (((2u * chunk) ^ swz) << 4), lo);
+                ptx::st_shared_v4(rdst + (((2u * chunk + 1u) ^ swz) << 4), hi);
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(ptx::smem_addr(&ctl->stg_empty[s8]));
+            ptx::mbar_arrive(ptx::smem_addr(&ctl->a_full[stage]));
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+            if (++s8 == STG) {
+                s8 = 0;
+                ph8 ^= 1u;
+            }
+        }
+    } else if (warp < 4) {
         // ------------------------------------------------------------ producers
         ptx::setmaxnreg_dec<PRODUCER_REGS>();
         const int row = threadIdx.x;  // 0..127
         const uint32_t row_off = (uint32_t)row * 128u;
         const uint32_t swz = (uint32_t)(row & 7);
-        const int my_tiles = blockIdx.x < a.num_tiles ? (a.num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-        const int total = my_tiles * a.k_steps;
         LoadCursor cur;
         cursor_set_tile(cur, a, blockIdx.x, row);
         uint4 pf[PREFETCH][4];
@@ -315,16 +388,8 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 }
             }
         }
-        if (threadIdx.x == 0 && *abort_flag) {
-            // let every filter copy this thread issued land before the CTA
-            // exits: the newest copy into stage s completes phase
-            // (copies into s) - 1 of b_full[s], and phases complete in order
-            for (int s = 0; s < STAGES; ++s) {
-                const int64_t n_s = b_issued / STAGES + (s < b_issued % STAGES ? 1 : 0);
-                if (n_s > 0)
-                    (void)drain_phase(ptx::smem_addr(&ctl->b_full[s]), (uint32_t)((n_s - 1) & 1), limit, a.status);
-            }
-        }
+        // let every filter copy this thread issued land before the CTA exits
+        if (threadIdx.x == 0 && *abort_flag) drain_ring(ctl->b_full, STAGES, b_issued, limit, a.status);
     } else if (warp < FIRST_EPI_WARP) {
         // ------------------------------------------------------------ MMA issuer
         ptx::setmaxnreg_dec<PRODUCER_REGS>();
@@ -375,6 +440,74 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
             // all MMAs issued by this thread complete before tensor memory is freed
             ptx::mma_commit(ptx::smem_addr(&ctl->mma_done));
             (void)drain_phase(ptx::smem_addr(&ctl->mma_done), 0, limit, a.status);
+        } else if (kTma && warp == A_ISSUER_WARP && lane == 0) {
+            // im2col tiles: 128 consecutive output pixels x 64 channels of one
+            // tap; the map's bounding box turns pixel order into window
+            // origins (stride and pre-padding), the tap enters as the pixel
+            // offset (r*dil_h, s*dil_w), and out-of-image reads are zeros
+            int s8 = 0;
+            uint32_t ph8 = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            const int pq = a.P * a.Q;
+            for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
+                const int m0 = (tile / a.n_tiles) * MT;
+                const int n0 = m0 / pq;
+                const int rem = m0 - n0 * pq;
+                const int p0 = rem / a.Q;
+                const int q0 = rem - p0 * a.Q;
+                const int w0 = q0 * a.str_w - a.pad_w;
+                const int h0 = p0 * a.str_h - a.pad_h;
+                int cb = 0, r = 0, s = 0;
+                for (int j = 0; j < a.k_steps; ++j) {
+                    if (!wait_phase(ptx::smem_addr(&ctl->stg_empty[s8]), ph8 ^ 1u, abort_flag, limit, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bar = ptx::smem_addr(&ctl->stg_full[s8]);
+                    ptx::mbar_arrive_expect_tx(bar, STG_BYTES);
+                    ptx::tma_load_im2col_4d(stg_smem + s8 * STG_BYTES, &a.tmap_x, cb * KS, w0, h0, n0,
+                                            (uint16_t)(s * a.dil_w), (uint16_t)(r * a.dil_h), bar);
+                    ++issued;
+                    if (++s8 == STG) {
+                        s8 = 0;
+                        ph8 ^= 1u;
+                    }
+                    if (++cb == a.c_steps) {
+                        cb = 0;
+                        if (++s == a.S) {
+                            s = 0;
+                            ++r;
+                        }
+                    }
+                }
+            }
+            if (*abort_flag) drain_ring(ctl->stg_full, STG, issued, limit, a.status);
+        } else if (kTma && warp == B_ISSUER_WARP && lane == 0) {
+            // pre-swizzled f16 filter blocks, one bulk copy per k-step
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
+                const int nt = tile % a.n_tiles;
+                const uint8_t *blk = a.wp + (size_t)nt * a.k_steps * (size_t)B_BYTES;
+                for (int j = 0; j < a.k_steps; ++j) {
+                    if (!wait_phase(ptx::smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, limit, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bar = ptx::smem_addr(&ctl->b_full[stage]);
+                    ptx::mbar_arrive_expect_tx(bar, B_BYTES);
+                    ptx::bulk_copy_g2s(b_smem + stage * B_BYTES, blk + (size_t)j * B_BYTES, B_BYTES, bar);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (*abort_flag) drain_ring(ctl->b_full, STAGES, issued, limit, a.status);
         }
         __syncwarp();
     } else {
@@ -538,20 +671,67 @@ __global__ void igemm_pack_image_kernel(const int8_t *x, int64_t xs0, int64_t xs
 
 inline int64_t align256(int64_t v) { return (v + 255) & ~255LL; }
 
-template <int NT>
+template <int NT, bool kTma>
 conv_status launch_conv(const IgemmArgs &a, int grid, cudaStream_t st) {
-    using Cfg = TileCfg<NT>;
-    static bool attr_set[64] = {false};
+    using Cfg = TileCfg<NT, kTma>;
+    static std::atomic<bool> attr_set[64];
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(igemm_conv_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (dev < 0 || dev >= 64 || !attr_set[dev].load()) {
+        if (cudaFuncSetAttribute(igemm_conv_kernel<NT, kTma>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg::SMEM_BYTES) != cudaSuccess)
             return CONV_ERR_CUDA;
-        attr_set[dev] = true;
+        if (dev >= 0 && dev < 64) attr_set[dev].store(true);
     }
-    igemm_conv_kernel<NT><<<grid, THREADS, Cfg::SMEM_BYTES, st>>>(a);
+    igemm_conv_kernel<NT, kTma><<<grid, THREADS, Cfg::SMEM_BYTES, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}
+
+// The driver's im2col tensor-map encoder, looked up once through the runtime
+// (no link against the driver library).
+PFN_cuTensorMapEncodeIm2col_v12000 im2col_encoder() {
+    static std::atomic<void *> fn{nullptr};
+    static std::atomic<bool> tried{false};
+    if (!tried.load()) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn.store(p);
+        tried.store(true);
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeIm2col_v12000>(fn.load());
+}
+
+// im2col map of a channels-last int8 image [N][H][W][C] (byte strides
+// xs_n, xs_h, xs_w): each load brings 128 consecutive output pixels x 64
+// channels.  The bounding box runs from -pre to post - (taps-1)*dil along W
+// and H so that its traversal at the convolution stride visits exactly the
+// P x Q window origins.  Returns false when the map cannot express the call
+// (stride above 8, corner or offset out of range, encoder unavailable).
+bool encode_im2col_map(const ConvGeom &g, const void *x, int64_t xs_n, int64_t xs_h, int64_t xs_w, int64_t c_dim,
+                       CUtensorMap *map) {
+    if (g.str_h > 8 || g.str_w > 8) return false;
+    const int64_t lo_w = -g.pad_w, lo_h = -g.pad_h;
+    const int64_t hi_w = (g.Q - 1) * g.str_w + lo_w - (g.W - 1);  // = post_w - (S-1)*dil_w
+    const int64_t hi_h = (g.P - 1) * g.str_h + lo_h - (g.H - 1);
+    for (int64_t v : {lo_w, lo_h, hi_w, hi_h})
+        if (v < -128 || v > 127) return false;
+    if ((g.R - 1) * g.dil_h > 65535 || (g.S - 1) * g.dil_w > 65535) return false;
+    if (((uintptr_t)x % 16) != 0 || xs_w % 16 || xs_h % 16 || xs_n % 16) return false;
+    auto enc = im2col_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)c_dim, (cuuint64_t)g.W, (cuuint64_t)g.H, (cuuint64_t)g.N};
+    const cuuint64_t strides[3] = {(cuuint64_t)xs_w, (cuuint64_t)xs_h, (cuuint64_t)xs_n};
+    const int lower[2] = {(int)lo_w, (int)lo_h};
+    const int upper[2] = {(int)hi_w, (int)hi_h};
+    const cuuint32_t estr[4] = {1, (cuuint32_t)g.str_w, (cuuint32_t)g.str_h, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(x), dims, strides, lower, upper,
+                           (cuuint32_t)KS, (cuuint32_t)MT, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -573,6 +753,7 @@ void igemm_plan(const ConvGeom &g, const void *x_dev, IgemmPlan *pl) {
     const bool direct = g.xs[1] == 1 && (g.C % 16) == 0 && (g.xs[0] % 16) == 0 && (g.xs[2] % 16) == 0 &&
                         (g.xs[3] % 16) == 0 && (x_dev == nullptr || ((uintptr_t)x_dev % 16) == 0);
     pl->pack_x = !direct;
+    pl->register_loads = false;
     pl->n_tile = g.K > 128 ? 256 : 128;
     pl->c16 = (g.C + 15) / 16 * 16;
     pl->c_steps = (g.C + KS - 1) / KS;
@@ -650,7 +831,10 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
     if (!a.status) return CONV_ERR_CUDA;
     if (a.num_tiles == 0) return CONV_OK;
     const int grid = a.num_tiles < sms ? a.num_tiles : sms;
-    return pl.n_tile == 256 ? launch_conv<256>(a, grid, st) : launch_conv<128>(a, grid, st);
+    const bool tma = !pl.register_loads && encode_im2col_map(g, a.x, a.xs_n, a.xs_h, a.xs_w,
+                                                             pl.pack_x ? pl.c16 : g.C, &a.tmap_x);
+    if (tma) return pl.n_tile == 256 ? launch_conv<256, true>(a, grid, st) : launch_conv<128, true>(a, grid, st);
+    return pl.n_tile == 256 ? launch_conv<256, false>(a, grid, st) : launch_conv<128, false>(a, grid, st);
 }
 
 }  // namespace i8c

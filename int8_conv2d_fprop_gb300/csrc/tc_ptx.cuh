@@ -63,6 +63,32 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
         : "memory");
 }
 
+// Tensor copy global -> shared in im2col mode (4-D NHWC map): loads the
+// map's pixelsPerColumn pixels x channelsPerPixel channels starting at
+// coordinates (c, w, h, n), each pixel displaced by (off_w, off_h); elements
+// outside the tensor read as zero.  Completion counted in bytes on `bar`.
+__device__ __forceinline__ void tma_load_im2col_4d(uint32_t dst, const void *tmap, int32_t c, int32_t w,
+                                                   int32_t h, int32_t n, uint16_t off_w, uint16_t off_h,
+                                                   uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], {%7, %8};" ::"r"(dst),
+        "l"(tmap), "r"(c), "r"(w), "r"(h), "r"(n), "r"(bar), "h"(off_w), "h"(off_h)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
 // ---------------------------------------------------------------- global loads
 __device__ __forceinline__ uint4 ld_nc_v4(const void *p) {
     uint4 v;

@@ -106,7 +106,7 @@ def test_workload_full_size_sampled(ic, name):
 
 
 # ------------------------------------------------------------------ every algorithm
-ALGOS = [1, 2, 3]  # implicit GEMM, dp4a, generic
+ALGOS = [1, 2, 3, 4]  # implicit GEMM (TMA im2col), dp4a, generic, implicit GEMM (global loads)
 
 
 def _shape_cases():

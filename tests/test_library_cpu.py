@@ -211,10 +211,14 @@ def test_planner_choices_and_workspace(ic):
     assert ws["c5_7x1_dilated_conv"] == 2 * 14 * 16384 + c5.N * c5.H * c5.W * c5.C
     # forced algorithms are honoured
     xd, wd, yd, p = _descs(ic, synth.CONFIGS["c2_s2_nhwc"])
-    for a in (ic.ALGO_DIRECT_GENERIC, ic.ALGO_DIRECT_DP4A, ic.ALGO_IMPLICIT_GEMM):
+    for a in (ic.ALGO_DIRECT_GENERIC, ic.ALGO_DIRECT_DP4A, ic.ALGO_IMPLICIT_GEMM,
+              ic.ALGO_IMPLICIT_GEMM_GLOBAL_LOADS):
         p.algo = a
         assert ic.plan(xd, wd, yd, p) == a
-        assert (ic.workspace_size(xd, wd, yd, p) > 0) == (a == ic.ALGO_IMPLICIT_GEMM)
+        tensor_core = a in (ic.ALGO_IMPLICIT_GEMM, ic.ALGO_IMPLICIT_GEMM_GLOBAL_LOADS)
+        assert (ic.workspace_size(xd, wd, yd, p) > 0) == tensor_core
+    p.algo = 5
+    assert ic.validate(xd, wd, yd, p) == _code(ic, "CONV_ERR_BAD_PARAM")
 
 
 def test_dp4a_refuses_long_reductions(ic):
