@@ -199,6 +199,37 @@ conv_status conv_fprop_prepacked(const conv_tensor_desc *x, const int8_t *x_dev,
                                  void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * conv_fprop with the image, filter, bias and output in HOST memory (same
+ * descriptors and semantics as conv_fprop; x_host, w_host, y_host and
+ * bias_host are host pointers, page-locked for the copies to overlap).
+ *
+ * The filter and bias are copied once; the batch is then processed in up to
+ * four chunks of whole images on three library-owned streams, so that the
+ * copy of chunk c to the device, the convolution of chunk c-1 and the copy
+ * of chunk c-2 back to the host run at the same time.  Chunking needs every
+ * image in its own byte range of the buffers (batch outermost in memory, as
+ * in NCHW or NHWC); otherwise the whole batch is one chunk.
+ *
+ * device_buffer (device memory, 256-byte aligned, at least
+ * conv_fprop_host_buffer_size bytes, owned by the caller) holds the filter,
+ * bias, workspace and double-buffered image and output chunks.  The call is
+ * asynchronous: it returns after queueing the work, and `stream` (the
+ * caller's) is made to wait for its completion, so synchronising `stream`
+ * means y_host holds the result.  The streams and events it uses are created
+ * on the first call on each device and live until the process exits; calls
+ * on one device are queued one after the other.
+ */
+conv_status conv_fprop_host_buffer_size(const conv_tensor_desc *x, const conv_tensor_desc *w,
+                                        const conv_tensor_desc *y, const conv_fprop_params *p,
+                                        size_t *bytes);
+
+conv_status conv_fprop_host(const conv_tensor_desc *x, const int8_t *x_host,
+                            const conv_tensor_desc *w, const int8_t *w_host,
+                            const conv_tensor_desc *y, int32_t *y_host,
+                            const int32_t *bias_host, const conv_fprop_params *p,
+                            void *device_buffer, size_t device_buffer_bytes, void *stream);
+
+/*
  * conv_fprop without a caller-provided workspace.  (The pages have no
  * counterpart to this entry point; it exists for callers that cannot
  * allocate device memory: a plugin whose host framework owns all device

@@ -47,7 +47,7 @@ EXPORTED_SYMBOLS = (
     "conv_params_init", "conv_params_set_symmetric_padding", "conv_tensor_desc_packed",
     "conv_fprop_output_dims", "conv_fprop_validate", "conv_fprop_plan", "conv_fprop_workspace_size",
     "conv_fprop", "conv_fprop_pack_filter", "conv_fprop_prepacked", "conv_fprop_static_workspace",
-    "conv_device_status",
+    "conv_fprop_host_buffer_size", "conv_fprop_host", "conv_device_status",
     "conv_selftest_wait_timeout", "conv_status_string", "conv_library_version",
 )
 
@@ -150,6 +150,10 @@ def lib():
         L.conv_fprop_prepacked.argtypes = list(L.conv_fprop.argtypes)
         L.conv_fprop_static_workspace.argtypes = [D, ctypes.c_void_p, D, ctypes.c_void_p, D, ctypes.c_void_p,
                                                   ctypes.c_void_p, P, ctypes.c_void_p]
+        L.conv_fprop_host_buffer_size.argtypes = [D, D, D, P, ctypes.POINTER(ctypes.c_size_t)]
+        L.conv_fprop_host_buffer_size.restype = ctypes.c_int
+        L.conv_fprop_host.argtypes = list(L.conv_fprop.argtypes)
+        L.conv_fprop_host.restype = ctypes.c_int
         L.conv_device_status.argtypes = [ctypes.c_void_p]
         L.conv_selftest_wait_timeout.argtypes = [ctypes.c_uint32, ctypes.c_void_p]
         L.conv_status_string.argtypes = [ctypes.c_int]
@@ -229,6 +233,41 @@ def conv_fprop_static_workspace_raw(xd: TensorDesc, x_ptr: int, wd: TensorDesc, 
     caller workspace (for callers that cannot allocate device memory)."""
     return int(lib().conv_fprop_static_workspace(ctypes.byref(xd), x_ptr, ctypes.byref(wd), w_ptr, ctypes.byref(yd),
                                                  y_ptr, bias_ptr or None, ctypes.byref(p), stream or None))
+
+
+def host_buffer_size(xd: TensorDesc, wd: TensorDesc, yd: TensorDesc, p: Params) -> int:
+    out = ctypes.c_size_t()
+    _check(lib().conv_fprop_host_buffer_size(ctypes.byref(xd), ctypes.byref(wd), ctypes.byref(yd), ctypes.byref(p),
+                                             ctypes.byref(out)), "host buffer size")
+    return int(out.value)
+
+
+def conv_fprop_host_raw(xd: TensorDesc, x_host: int, wd: TensorDesc, w_host: int, yd: TensorDesc, y_host: int,
+                        bias_host: int, p: Params, device_buffer: int, device_buffer_bytes: int, stream: int) -> int:
+    """conv_fprop on host buffers (copies and compute pipelined by the library)."""
+    return int(lib().conv_fprop_host(ctypes.byref(xd), x_host, ctypes.byref(wd), w_host, ctypes.byref(yd), y_host,
+                                     bias_host or None, ctypes.byref(p), device_buffer or None,
+                                     int(device_buffer_bytes), stream or None))
+
+
+def conv_fprop_from_host(x, w, bias=None, *, out, device_buffer=None, stream=None, pre_padding=(0, 0),
+                         post_padding=(0, 0), padding=None, stride=(1, 1), dilation=(1, 1),
+                         mode: int = CROSS_CORRELATION, relu: bool = False, algo: int = ALGO_AUTO):
+    """conv_fprop on CPU tensors (pin them for overlapped copies); ``out`` is
+    a CPU int32 tensor.  Asynchronous on ``stream``; returns ``out``."""
+    import torch
+    p = Params.make(pre_padding, post_padding, stride, dilation, mode, bias is not None, relu, algo, padding)
+    xd, wd, yd = TensorDesc.from_tensor(x), TensorDesc.from_tensor(w), TensorDesc.from_tensor(out)
+    need = host_buffer_size(xd, wd, yd, p)
+    if device_buffer is None or device_buffer.numel() * device_buffer.element_size() < need:
+        device_buffer = torch.empty(max(need, 256), dtype=torch.uint8, device="cuda")
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    st = conv_fprop_host_raw(xd, x.data_ptr(), wd, w.data_ptr(), yd, out.data_ptr(),
+                             bias.data_ptr() if bias is not None else 0, p, device_buffer.data_ptr(),
+                             device_buffer.numel() * device_buffer.element_size(), stream.cuda_stream)
+    _check(st, "conv_fprop_host")
+    return out
 
 
 def device_status(stream: int = 0) -> int:

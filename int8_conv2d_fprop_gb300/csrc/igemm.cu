@@ -66,24 +66,48 @@ constexpr int PREFETCH = 2;  // register path: items in flight ahead of the one 
 constexpr int STG_BYTES = MT * KS;  // one int8 im2col tile: 128 pixels x 64 channels
 constexpr int A_ISSUER_WARP = 5;    // TMA path: issues the im2col loads
 constexpr int B_ISSUER_WARP = 6;    // TMA path: issues the filter block copies
+// Output staging for TMA stores: per epilogue warp two buffers of 32 rows x
+// 16 int32 columns (64-byte rows, 64-byte swizzle).
+constexpr int EPI_COLS = 16;
+constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 4;  // 2 KB
+constexpr int EPI_SMEM_BYTES = 8 * 2 * EPI_BUF_BYTES;  // 32 KB
 
 // kTma: the int8 image tile arrives by TMA (im2col mode) in a ring of
 // STG_STAGES staging buffers and the producer warps convert it shared ->
 // shared; otherwise the producer warps gather it with global loads.
+// The f16 A ring (A_ST stages), the filter ring (B_ST stages) and the int8
+// staging ring (STG stages) advance independently: the filter blocks stream
+// from L2 and need the deepest ring, the conversion into the A ring is short.
 template <int NT, bool kTma>
 struct TileCfg {
     static constexpr int B_BYTES = NT * KS * 2;
-    static constexpr int STAGES = kTma ? (NT == 256 ? 3 : 4) : (NT == 256 ? 4 : 6);
-    static constexpr int STG_STAGES = kTma ? 8 : 0;
+    static constexpr int A_ST = kTma ? (NT == 256 ? 2 : 3) : (NT == 256 ? 4 : 6);
+    static constexpr int B_ST = kTma ? (NT == 256 ? 3 : 4) : A_ST;
+    static constexpr int STG_STAGES = kTma ? (NT == 256 ? 4 : 6) : 0;
     static constexpr int TMEM_COLS = NSLOT * NT;
-    static constexpr int SMEM_BYTES =
-        1024 /*align slack*/ + STAGES * (A_BYTES + B_BYTES) + STG_STAGES * STG_BYTES + 512 /*barriers*/;
+    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + A_ST * A_BYTES + B_ST * B_BYTES +
+                                      STG_STAGES * STG_BYTES + EPI_SMEM_BYTES + 512 /*barriers*/;
     static_assert(TMEM_COLS <= 512, "tensor memory has 512 columns");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+    static_assert(kTma || A_ST == B_ST, "the global-load producers fill A and B stages together");
+};
+
+// Slot index and phase parity of a ring of N mbarrier-guarded buffers.
+template <int N>
+struct Ring {
+    int idx = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void next() {
+        if (++idx == N) {
+            idx = 0;
+            phase ^= 1u;
+        }
+    }
 };
 
 struct IgemmArgs {
     CUtensorMap tmap_x;  // im2col map of the channels-last image (TMA path only)
+    CUtensorMap tmap_y;  // 2-D [pixels][K] int32 map of the output (when y_tma)
     const int8_t *x;     // channels-last image
     const uint8_t *wp;   // repacked f16 filter blocks
     int32_t *y;
@@ -96,24 +120,22 @@ struct IgemmArgs {
     int32_t pad_h, pad_w, str_h, str_w, dil_h, dil_w;
     int32_t m_total, n_tiles, num_tiles;
     int32_t relu, y_vec;
+    int32_t y_tma;       // output pixel-major with contiguous channels: TMA stores
     uint64_t wait_limit_ns;
     int *status;         // device status word
 };
 
-template <int STAGES>
 struct SharedCtl {
-    uint64_t a_full[STAGES];
-    uint64_t b_full[STAGES];
-    uint64_t empty[STAGES];
-    uint64_t stg_full[8];   // TMA path: im2col tile landed
-    uint64_t stg_empty[8];  // TMA path: im2col tile converted
+    uint64_t a_full[8], a_empty[8];      // f16 A ring
+    uint64_t b_full[8], b_empty[8];      // filter ring
+    uint64_t stg_full[8], stg_empty[8];  // TMA path: im2col tile landed / converted
     uint64_t acc_full[NSLOT];
     uint64_t acc_empty[NSLOT];
     uint64_t mma_done;
     uint32_t tmem_base;
     int32_t abort_flag;
 };
-static_assert(sizeof(SharedCtl<6>) <= 512, "control block too large");
+static_assert(sizeof(SharedCtl) <= 512, "control block too large");
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting or
 // the time limit passed (then the CTA is marked aborting and the device status
@@ -236,7 +258,8 @@ __device__ __forceinline__ void drain_ring(uint64_t *bars, int depth, int64_t is
 template <int NT, bool kTma>
 __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_constant__ IgemmArgs a) {
     using Cfg = TileCfg<NT, kTma>;
-    constexpr int STAGES = Cfg::STAGES;
+    constexpr int A_ST = Cfg::A_ST;
+    constexpr int B_ST = Cfg::B_ST;
     constexpr int STG = Cfg::STG_STAGES;
     constexpr int B_BYTES = Cfg::B_BYTES;
     constexpr int HALF = NT / 2;  // columns per epilogue thread
@@ -245,22 +268,30 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t *const base_ptr = smem_raw + (base - raw_addr);
     const uint32_t a_smem = base;
-    const uint32_t b_smem = base + STAGES * A_BYTES;
-    const uint32_t stg_smem = base + STAGES * (A_BYTES + B_BYTES);
-    SharedCtl<STAGES> *ctl =
-        reinterpret_cast<SharedCtl<STAGES> *>(base_ptr + STAGES * (A_BYTES + B_BYTES) + STG * STG_BYTES);
+    const uint32_t b_smem = a_smem + A_ST * A_BYTES;
+    const uint32_t stg_smem = b_smem + B_ST * B_BYTES;
+    const uint32_t epi_smem = stg_smem + STG * STG_BYTES;
+    SharedCtl *ctl = reinterpret_cast<SharedCtl *>(base_ptr + A_ST * A_BYTES + B_ST * B_BYTES + STG * STG_BYTES +
+                                                   EPI_SMEM_BYTES);
     volatile int32_t *abort_flag = &ctl->abort_flag;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int my_tiles = blockIdx.x < a.num_tiles ? (a.num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     const int total = my_tiles * a.k_steps;  // (tile, k-step) items of this CTA
+    // TMA path: each CTA walks the reduction starting at its own k-step, so
+    // the SMs do not all fetch the same filter block at the same moment (any
+    // order is exact: a group is any run of at most 1024 products)
+    const int rot = kTma ? (int)(((int64_t)blockIdx.x * 7) % a.k_steps) : 0;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < STAGES; ++i) {
+        for (int i = 0; i < A_ST; ++i) {
             ptx::mbar_init(ptx::smem_addr(&ctl->a_full[i]), 128);
+            ptx::mbar_init(ptx::smem_addr(&ctl->a_empty[i]), 1);
+        }
+        for (int i = 0; i < B_ST; ++i) {
             ptx::mbar_init(ptx::smem_addr(&ctl->b_full[i]), 1);
-            ptx::mbar_init(ptx::smem_addr(&ctl->empty[i]), 1);
+            ptx::mbar_init(ptx::smem_addr(&ctl->b_empty[i]), 1);
         }
         for (int i = 0; i < STG; ++i) {
             ptx::mbar_init(ptx::smem_addr(&ctl->stg_full[i]), 1);
@@ -294,13 +325,14 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
         ptx::setmaxnreg_dec<PRODUCER_REGS>();
         const uint32_t chunk = threadIdx.x & 3;
         const int row0 = (warp << 5) + (lane >> 2);
-        int stage = 0, s8 = 0;
-        uint32_t phase = 0, ph8 = 0;
+        Ring<A_ST> ra;
+        Ring<STG> rs;
         for (int it = 0; it < total; ++it) {
-            if (!wait_phase(ptx::smem_addr(&ctl->stg_full[s8]), ph8, abort_flag, limit, a.status)) break;
-            if (!wait_phase(ptx::smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, limit, a.status)) break;
-            const uint32_t src = stg_smem + s8 * STG_BYTES + chunk * 16u;
-            const uint32_t dst = a_smem + stage * A_BYTES;
+            if (!wait_phase(ptx::smem_addr(&ctl->stg_full[rs.idx]), rs.phase, abort_flag, limit, a.status)) break;
+            if (!wait_phase(ptx::smem_addr(&ctl->a_empty[ra.idx]), ra.phase ^ 1u, abort_flag, limit, a.status))
+                break;
+            const uint32_t src = stg_smem + rs.idx * STG_BYTES + chunk * 16u;
+            const uint32_t dst = a_smem + ra.idx * A_BYTES;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint32_t row = (uint32_t)(row0 + 8 * i);
@@ -313,16 +345,10 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 ptx::st_shared_v4(rdst + (((2u * chunk + 1u) ^ swz) << 4), hi);
             }
             ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(ptx::smem_addr(&ctl->stg_empty[s8]));
-            ptx::mbar_arrive(ptx::smem_addr(&ctl->a_full[stage]));
-            if (++stage == STAGES) {
-                stage = 0;
-                phase ^= 1u;
-            }
-            if (++s8 == STG) {
-                s8 = 0;
-                ph8 ^= 1u;
-            }
+            ptx::mbar_arrive(ptx::smem_addr(&ctl->stg_empty[rs.idx]));
+            ptx::mbar_arrive(ptx::smem_addr(&ctl->a_full[ra.idx]));
+            ra.next();
+            rs.next();
         }
     } else if (warp < 4) {
         // ------------------------------------------------------------ producers
@@ -340,8 +366,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 cursor_advance(cur, a, row);
             }
         }
-        int stage = 0;
-        uint32_t phase = 0;
+        Ring<A_ST> rg;  // A and B stages advance together on this path
         int b_tile = blockIdx.x, b_j = 0;  // filter block cursor (thread 0 only)
         int64_t b_issued = 0;
         bool ok = true;
@@ -356,23 +381,28 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                     cursor_load(cur, a, pf[d]);
                     cursor_advance(cur, a, row);
                 }
-                if (!wait_phase(ptx::smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, limit, a.status)) {
+                if (!wait_phase(ptx::smem_addr(&ctl->a_empty[rg.idx]), rg.phase ^ 1u, abort_flag, limit, a.status)) {
                     ok = false;
                     break;
                 }
                 if (threadIdx.x == 0) {
-                    const uint32_t bar = ptx::smem_addr(&ctl->b_full[stage]);
+                    if (!wait_phase(ptx::smem_addr(&ctl->b_empty[rg.idx]), rg.phase ^ 1u, abort_flag, limit,
+                                    a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bar = ptx::smem_addr(&ctl->b_full[rg.idx]);
                     ptx::mbar_arrive_expect_tx(bar, B_BYTES);
                     const int nt = b_tile % a.n_tiles;
                     const uint8_t *src = a.wp + ((size_t)nt * a.k_steps + b_j) * (size_t)B_BYTES;
-                    ptx::bulk_copy_g2s(b_smem + stage * B_BYTES, src, B_BYTES, bar);
+                    ptx::bulk_copy_g2s(b_smem + rg.idx * B_BYTES, src, B_BYTES, bar);
                     ++b_issued;
                     if (++b_j == a.k_steps) {
                         b_j = 0;
                         b_tile += gridDim.x;
                     }
                 }
-                const uint32_t dst = a_smem + stage * A_BYTES + row_off;
+                const uint32_t dst = a_smem + rg.idx * A_BYTES + row_off;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     uint4 lo, hi;
@@ -381,22 +411,19 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                     ptx::st_shared_v4(dst + ((((uint32_t)(2 * i + 1)) ^ swz) << 4), hi);
                 }
                 ptx::fence_proxy_async_smem();
-                ptx::mbar_arrive(ptx::smem_addr(&ctl->a_full[stage]));
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
+                ptx::mbar_arrive(ptx::smem_addr(&ctl->a_full[rg.idx]));
+                rg.next();
             }
         }
         // let every filter copy this thread issued land before the CTA exits
-        if (threadIdx.x == 0 && *abort_flag) drain_ring(ctl->b_full, STAGES, b_issued, limit, a.status);
+        if (threadIdx.x == 0 && *abort_flag) drain_ring(ctl->b_full, B_ST, b_issued, limit, a.status);
     } else if (warp < FIRST_EPI_WARP) {
         // ------------------------------------------------------------ MMA issuer
         ptx::setmaxnreg_dec<PRODUCER_REGS>();
         if (warp == MMA_WARP && lane == 0) {
             constexpr uint32_t idesc = ptx::idesc_f16_f32(MT, NT);
-            int stage = 0;
-            uint32_t phase = 0;
+            Ring<A_ST> ra;
+            Ring<B_ST> rb;
             uint32_t gi = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
@@ -412,25 +439,26 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                     ptx::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + slot * NT;
                     for (int j = js; j < je; ++j) {
-                        if (!wait_phase(ptx::smem_addr(&ctl->a_full[stage]), phase, abort_flag, limit, a.status) ||
-                            !wait_phase(ptx::smem_addr(&ctl->b_full[stage]), phase, abort_flag, limit, a.status)) {
+                        if (!wait_phase(ptx::smem_addr(&ctl->a_full[ra.idx]), ra.phase, abort_flag, limit,
+                                        a.status) ||
+                            !wait_phase(ptx::smem_addr(&ctl->b_full[rb.idx]), rb.phase, abort_flag, limit,
+                                        a.status)) {
                             ok = false;
                             break;
                         }
                         ptx::tc_fence_after();
-                        const uint64_t adesc = ptx::smem_desc_sw128(a_smem + stage * A_BYTES);
-                        const uint64_t bdesc = ptx::smem_desc_sw128(b_smem + stage * B_BYTES);
+                        const uint64_t adesc = ptx::smem_desc_sw128(a_smem + ra.idx * A_BYTES);
+                        const uint64_t bdesc = ptx::smem_desc_sw128(b_smem + rb.idx * B_BYTES);
 #pragma unroll
                         for (int kk = 0; kk < KS / 16; ++kk) {
                             // advance 16 f16 = 32 bytes along K inside the swizzled row
                             ptx::mma_f16_ss(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
                                             (j > js || kk > 0) ? 1u : 0u);
                         }
-                        ptx::mma_commit(ptx::smem_addr(&ctl->empty[stage]));
-                        if (++stage == STAGES) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
+                        ptx::mma_commit(ptx::smem_addr(&ctl->a_empty[ra.idx]));
+                        ptx::mma_commit(ptx::smem_addr(&ctl->b_empty[rb.idx]));
+                        ra.next();
+                        rb.next();
                     }
                     if (!ok) break;
                     ptx::mma_commit(ptx::smem_addr(&ctl->acc_full[slot]));
@@ -445,8 +473,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
             // tap; the map's bounding box turns pixel order into window
             // origins (stride and pre-padding), the tap enters as the pixel
             // offset (r*dil_h, s*dil_w), and out-of-image reads are zeros
-            int s8 = 0;
-            uint32_t ph8 = 0;
+            Ring<STG> rs;
             int64_t issued = 0;
             bool ok = true;
             const int pq = a.P * a.Q;
@@ -458,56 +485,52 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 const int q0 = rem - p0 * a.Q;
                 const int w0 = q0 * a.str_w - a.pad_w;
                 const int h0 = p0 * a.str_h - a.pad_h;
-                int cb = 0, r = 0, s = 0;
                 for (int j = 0; j < a.k_steps; ++j) {
-                    if (!wait_phase(ptx::smem_addr(&ctl->stg_empty[s8]), ph8 ^ 1u, abort_flag, limit, a.status)) {
+                    int jr = j + rot;
+                    if (jr >= a.k_steps) jr -= a.k_steps;
+                    const int tap = jr / a.c_steps;
+                    const int cb = jr - tap * a.c_steps;
+                    const int r = tap / a.S;
+                    const int s = tap - r * a.S;
+                    if (!wait_phase(ptx::smem_addr(&ctl->stg_empty[rs.idx]), rs.phase ^ 1u, abort_flag, limit,
+                                    a.status)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t bar = ptx::smem_addr(&ctl->stg_full[s8]);
+                    const uint32_t bar = ptx::smem_addr(&ctl->stg_full[rs.idx]);
                     ptx::mbar_arrive_expect_tx(bar, STG_BYTES);
-                    ptx::tma_load_im2col_4d(stg_smem + s8 * STG_BYTES, &a.tmap_x, cb * KS, w0, h0, n0,
+                    ptx::tma_load_im2col_4d(stg_smem + rs.idx * STG_BYTES, &a.tmap_x, cb * KS, w0, h0, n0,
                                             (uint16_t)(s * a.dil_w), (uint16_t)(r * a.dil_h), bar);
                     ++issued;
-                    if (++s8 == STG) {
-                        s8 = 0;
-                        ph8 ^= 1u;
-                    }
-                    if (++cb == a.c_steps) {
-                        cb = 0;
-                        if (++s == a.S) {
-                            s = 0;
-                            ++r;
-                        }
-                    }
+                    rs.next();
                 }
             }
             if (*abort_flag) drain_ring(ctl->stg_full, STG, issued, limit, a.status);
         } else if (kTma && warp == B_ISSUER_WARP && lane == 0) {
-            // pre-swizzled f16 filter blocks, one bulk copy per k-step
-            int stage = 0;
-            uint32_t phase = 0;
+            // pre-swizzled f16 filter blocks, one bulk copy per k-step, in the
+            // same rotated k-step order as the image tiles
+            Ring<B_ST> rb;
             int64_t issued = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
                 const int nt = tile % a.n_tiles;
                 const uint8_t *blk = a.wp + (size_t)nt * a.k_steps * (size_t)B_BYTES;
                 for (int j = 0; j < a.k_steps; ++j) {
-                    if (!wait_phase(ptx::smem_addr(&ctl->empty[stage]), phase ^ 1u, abort_flag, limit, a.status)) {
+                    int jr = j + rot;
+                    if (jr >= a.k_steps) jr -= a.k_steps;
+                    if (!wait_phase(ptx::smem_addr(&ctl->b_empty[rb.idx]), rb.phase ^ 1u, abort_flag, limit,
+                                    a.status)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t bar = ptx::smem_addr(&ctl->b_full[stage]);
+                    const uint32_t bar = ptx::smem_addr(&ctl->b_full[rb.idx]);
                     ptx::mbar_arrive_expect_tx(bar, B_BYTES);
-                    ptx::bulk_copy_g2s(b_smem + stage * B_BYTES, blk + (size_t)j * B_BYTES, B_BYTES, bar);
+                    ptx::bulk_copy_g2s(b_smem + rb.idx * B_BYTES, blk + (size_t)jr * B_BYTES, B_BYTES, bar);
                     ++issued;
-                    if (++stage == STAGES) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                    rb.next();
                 }
             }
-            if (*abort_flag) drain_ring(ctl->b_full, STAGES, issued, limit, a.status);
+            if (*abort_flag) drain_ring(ctl->b_full, B_ST, issued, limit, a.status);
         }
         __syncwarp();
     } else {
@@ -559,7 +582,46 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 ++gi;
             }
             if (!ok) break;
-            if (valid) {
+            if (a.y_tma) {
+                // Rows of the tile are consecutive pixels with contiguous
+                // channels: each warp stages 32 rows x 16 columns at a time in
+                // shared memory (64-byte rows; 16-byte chunk c of row r at
+                // c ^ ((r >> 1) & 3), the 64-byte swizzle) and one lane writes
+                // them with a TMA store, which also clips rows past the last
+                // pixel and columns past K.  Two buffers per warp alternate.
+                const int k0 = nt * NT + col0;
+                const int m0w = mt * MT + quad * 32;
+                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (2u * EPI_BUF_BYTES);
+                const uint32_t sw = ((uint32_t)lane >> 1) & 3u;
+#pragma unroll
+                for (int ch = 0; ch < HALF / EPI_COLS; ++ch) {
+                    const uint32_t buf = ebase + (uint32_t)(ch & 1) * EPI_BUF_BYTES;
+                    if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store that last read buf is done
+                    __syncwarp();
+                    const uint32_t rowaddr = buf + (uint32_t)lane * 64u;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        int32_t o[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = ch * EPI_COLS + c * 4 + e;
+                            const int k = k0 + i;
+                            int32_t val = acc[i];
+                            if (a.bias && k < a.K) val = (int32_t)((uint32_t)val + (uint32_t)__ldg(a.bias + k));
+                            if (a.relu) val = max(val, 0);
+                            o[e] = val;
+                        }
+                        ptx::st_shared_v4(rowaddr + ((((uint32_t)c) ^ sw) << 4),
+                                          make_uint4((uint32_t)o[0], (uint32_t)o[1], (uint32_t)o[2], (uint32_t)o[3]));
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_2d(&a.tmap_y, k0 + ch * EPI_COLS, m0w, buf);
+                        ptx::bulk_commit_group();
+                    }
+                }
+            } else if (valid) {
                 const int k0 = nt * NT + col0;
                 int32_t *yrow = a.y + yoff;
 #pragma unroll
@@ -583,6 +645,8 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 }
             }
         }
+        // the output stores must finish reading shared memory before the CTA exits
+        if (a.y_tma && lane == 0) ptx::bulk_wait_group_all();
     }
 
     ptx::tc_fence_before();
@@ -617,18 +681,29 @@ __global__ void igemm_pack_filter_kernel(const int8_t *w, int64_t ws0, int64_t w
         const int sf = mode ? S - 1 - s : s;
         const int c0 = cb * KS + chunk * 8;
         uint32_t words[4];
+        const int64_t off = (int64_t)k * ws0 + (int64_t)c0 * ws1 + (int64_t)rf * ws2 + (int64_t)sf * ws3;
+        if (k < K && c0 + 8 <= C && ws1 == 1 && ((uintptr_t)(w + off) & 7) == 0) {
+            // eight channels contiguous in memory: one 8-byte load
+            const uint2 v = *reinterpret_cast<const uint2 *>(w + off);
+            const uint32_t lo = v.x ^ 0x80808080u, hi = v.y ^ 0x80808080u;
+            words[0] = cvt_pair(lo, 0x4140);
+            words[1] = cvt_pair(lo, 0x4342);
+            words[2] = cvt_pair(hi, 0x4140);
+            words[3] = cvt_pair(hi, 0x4342);
+        } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            unsigned short hv[2];
+            for (int e = 0; e < 4; ++e) {
+                unsigned short hv[2];
 #pragma unroll
-            for (int b = 0; b < 2; ++b) {
-                const int c = c0 + 2 * e + b;
-                int v = 0;
-                if (k < K && c < C)
-                    v = w[(int64_t)k * ws0 + (int64_t)c * ws1 + (int64_t)rf * ws2 + (int64_t)sf * ws3];
-                hv[b] = __half_as_ushort(__int2half_rn(v));
+                for (int b = 0; b < 2; ++b) {
+                    const int c = c0 + 2 * e + b;
+                    int v = 0;
+                    if (k < K && c < C)
+                        v = w[(int64_t)k * ws0 + (int64_t)c * ws1 + (int64_t)rf * ws2 + (int64_t)sf * ws3];
+                    hv[b] = __half_as_ushort(__int2half_rn(v));
+                }
+                words[e] = (uint32_t)hv[0] | ((uint32_t)hv[1] << 16);
             }
-            words[e] = (uint32_t)hv[0] | ((uint32_t)hv[1] << 16);
         }
         uint8_t *dst = wp + ((t2 * nt_rows + nl) * 128) + (((chunk ^ (nl & 7))) << 4);
         *reinterpret_cast<uint4 *>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
@@ -734,6 +809,53 @@ bool encode_im2col_map(const ConvGeom &g, const void *x, int64_t xs_n, int64_t x
     return r == CUDA_SUCCESS;
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tiled_encoder() {
+    static std::atomic<void *> fn{nullptr};
+    static std::atomic<bool> tried{false};
+    if (!tried.load()) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn.store(p);
+        tried.store(true);
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn.load());
+}
+
+// 2-D map [N*P*Q pixels][K channels] of an int32 output whose pixels follow
+// one another at a fixed stride with channels contiguous (NHWC, possibly with
+// padded pixel rows): box 32 pixels x 16 channels, 64-byte swizzle.  Returns
+// false for any other layout.
+bool encode_output_map(const ConvGeom &g, const int32_t *y, CUtensorMap *map) {
+    if (g.ys[1] != 1 && g.K > 1) return false;
+    int64_t ps;  // element stride between consecutive pixels
+    if (g.Q > 1) {
+        ps = g.ys[3];
+        if (g.P > 1 && g.ys[2] != g.Q * ps) return false;
+        if (g.N > 1 && g.ys[0] != g.P * g.Q * ps) return false;
+    } else if (g.P > 1) {
+        ps = g.ys[2];
+        if (g.N > 1 && g.ys[0] != g.P * ps) return false;
+    } else {
+        ps = g.N > 1 ? g.ys[0] : g.K;
+    }
+    const int64_t m_total = g.N * g.P * g.Q;
+    if (ps < g.K || (ps * 4) % 16 != 0 || ((uintptr_t)y % 16) != 0) return false;
+    if (m_total > ((int64_t)1 << 32) || (m_total > 1 && ps * 4 >= ((int64_t)1 << 40))) return false;
+    auto enc = tiled_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)g.K, (cuuint64_t)m_total};
+    const cuuint64_t strides[1] = {(cuuint64_t)(ps * 4)};
+    const cuuint32_t box[2] = {(cuuint32_t)EPI_COLS, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<int32_t *>(y), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool igemm_supported(const ConvGeom &g) {
@@ -826,6 +948,7 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
                (g.ys[2] % 4) == 0 && (g.ys[3] % 4) == 0)
                   ? 1
                   : 0;
+    a.y_tma = encode_output_map(g, y, &a.tmap_y) ? 1 : 0;
     a.wait_limit_ns = wait_limit_ns();
     a.status = device_status_word();
     if (!a.status) return CONV_ERR_CUDA;

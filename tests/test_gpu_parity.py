@@ -174,6 +174,46 @@ def test_random_extremes_full_reduction(ic):
     _assert_equal(got, ref, "random extremes")
 
 
+# ------------------------------------------------------------------ host buffers
+@pytest.mark.parametrize("name,batch,pinned", [("c2_s2_nhwc", None, True), ("c4_1x1_bias_relu", None, True),
+                                               ("c5_7x1_dilated_conv", 3, True), ("p4_shape", None, False),
+                                               ("c3_3x3_large", 5, False)])
+def test_host_buffer_pipeline(ic, name, batch, pinned):
+    """conv_fprop_host: tensors in host memory, batch pipelined in chunks."""
+    import dataclasses
+    cfg = synth.CONFIGS[name] if batch is None else dataclasses.replace(synth.CONFIGS[name], N=batch)
+    x, w, b = synth.make_inputs(cfg)
+    xf, xs = synth.place(x, cfg.x_layout)
+    wf, ws = synth.place(w, cfg.w_layout)
+    ystr = synth.packed_strides(cfg.y_dims, cfg.y_layout)
+    ysz = int(np.prod(cfg.y_dims))
+
+    def host(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return t.pin_memory() if pinned else t
+
+    xh, wh = host(xf), host(wf)
+    bh = host(b) if b is not None else None
+    yh = torch.full((ysz,), -3, dtype=torch.int32)
+    yh = yh.pin_memory() if pinned else yh
+    xd = ic.TensorDesc.make(ic.CONV_INT8, cfg.x_dims, xs, xf.size)
+    wd = ic.TensorDesc.make(ic.CONV_INT8, cfg.w_dims, ws, wf.size)
+    yd = ic.TensorDesc.make(ic.CONV_INT32, cfg.y_dims, ystr, ysz * 4)
+    p = ic.Params.make(cfg.pre, cfg.post, cfg.stride, cfg.dilation, cfg.mode, cfg.bias, cfg.relu)
+    need = ic.host_buffer_size(xd, wd, yd, p)
+    buf = torch.empty(need, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream()
+    st = ic.conv_fprop_host_raw(xd, xh.data_ptr(), wd, wh.data_ptr(), yd, yh.data_ptr(),
+                                bh.data_ptr() if bh is not None else 0, p, buf.data_ptr(), need, s.cuda_stream)
+    assert st == 0, ic.STATUS.get(st)
+    s.synchronize()
+    assert ic.device_status() == 0
+    got = synth.gather_logical(yh.numpy(), cfg.y_dims, ystr)
+    ref = oracle.conv_fprop(xf, cfg.x_dims, xs, wf, cfg.w_dims, ws, cfg.pre, cfg.post, cfg.stride,
+                            cfg.dilation, cfg.mode, b, cfg.relu)
+    _assert_equal(got, ref, f"host pipeline {name}")
+
+
 # ------------------------------------------------------------------ edge cases and status
 def test_empty_batch_is_a_no_op(ic):
     x = torch.zeros((0, 64, 8, 8), dtype=torch.int8, device="cuda").to(memory_format=torch.channels_last)

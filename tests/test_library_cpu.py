@@ -221,6 +221,19 @@ def test_planner_choices_and_workspace(ic):
     assert ic.validate(xd, wd, yd, p) == _code(ic, "CONV_ERR_BAD_PARAM")
 
 
+def test_host_buffer_size_covers_chunks(ic):
+    """The host-pipeline device buffer holds the filter, the workspace and two
+    image and two output chunks (a quarter of the batch each for C3)."""
+    cfg = synth.CONFIGS["c3_3x3_large"]
+    xd, wd, yd, p = _descs(ic, cfg)
+    need = ic.host_buffer_size(xd, wd, yd, p)
+    ws = ic.workspace_size(xd, wd, yd, p)
+    x_chunk = 8 * 256 * 56 * 56
+    y_chunk = 8 * 256 * 56 * 56 * 4
+    assert need >= cfg.K * cfg.C * 9 + ws + 2 * x_chunk + 2 * y_chunk
+    assert need < cfg.K * cfg.C * 9 + ws + 2 * x_chunk + 2 * y_chunk + 8 * 256
+
+
 def test_dp4a_refuses_long_reductions(ic):
     cfg = synth.CONFIGS["c3_3x3_large"]
     xd, wd, yd, p = _descs(ic, cfg)
