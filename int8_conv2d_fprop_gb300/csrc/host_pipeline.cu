@@ -79,6 +79,9 @@ conv_status host_plan(const conv_tensor_desc *x, const conv_tensor_desc *w, cons
                                         y->strides[0] >= extent_of_images(y, 1));
     hp->chunks = (!batch_outer || N < 2) ? 1 : (int)(N < kMaxChunks ? N : kMaxChunks);
     hp->per_chunk = N == 0 ? 0 : (N + hp->chunks - 1) / hp->chunks;
+    // rounding the chunk size up can leave fewer non-empty chunks (N = 5 in
+    // chunks of 2 needs 3, not 4)
+    if (N > 0) hp->chunks = (int)((N + hp->per_chunk - 1) / hp->per_chunk);
     hp->x_chunk_elems = hp->chunks == 1 ? desc_extent_elems(x) : extent_of_images(x, hp->per_chunk);
     hp->y_chunk_elems = hp->chunks == 1 ? desc_extent_elems(y) : extent_of_images(y, hp->per_chunk);
     hp->w_elems = desc_extent_elems(w);
@@ -163,6 +166,7 @@ conv_status conv_fprop_host(const conv_tensor_desc *x, const int8_t *x_host, con
         const int bsel = c & 1;
         const int64_t n0 = c * hp.per_chunk;
         const int64_t nb = (N - n0) < hp.per_chunk ? (N - n0) : hp.per_chunk;
+        if (nb <= 0) return CONV_ERR_BAD_PARAM;  // cannot happen: chunks = ceil(N / per_chunk)
         conv_tensor_desc xc = *x, yc = *y;
         xc.dims[0] = yc.dims[0] = nb;
         const int64_t x_elems = hp.chunks == 1 ? desc_extent_elems(x) : extent_of_images(x, nb);

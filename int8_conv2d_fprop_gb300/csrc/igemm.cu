@@ -78,18 +78,39 @@ constexpr int EPI_SMEM_BYTES = 8 * 2 * EPI_BUF_BYTES;  // 32 KB
 // The f16 A ring (A_ST stages), the filter ring (B_ST stages) and the int8
 // staging ring (STG stages) advance independently: the filter blocks stream
 // from L2 and need the deepest ring, the conversion into the A ring is short.
+// Ring depths of the TMA path (tuning knobs; shared memory is the limit).
+#ifndef IGEMM_A_ST_256
+#define IGEMM_A_ST_256 4
+#endif
+#ifndef IGEMM_B_ST_256
+#define IGEMM_B_ST_256 3
+#endif
+#ifndef IGEMM_STG_256
+#define IGEMM_STG_256 3
+#endif
+#ifndef IGEMM_A_ST_128
+#define IGEMM_A_ST_128 4
+#endif
+#ifndef IGEMM_B_ST_128
+#define IGEMM_B_ST_128 5
+#endif
+#ifndef IGEMM_STG_128
+#define IGEMM_STG_128 4
+#endif
+
 template <int NT, bool kTma>
 struct TileCfg {
     static constexpr int B_BYTES = NT * KS * 2;
-    static constexpr int A_ST = kTma ? (NT == 256 ? 2 : 3) : (NT == 256 ? 4 : 6);
-    static constexpr int B_ST = kTma ? (NT == 256 ? 3 : 4) : A_ST;
-    static constexpr int STG_STAGES = kTma ? (NT == 256 ? 4 : 6) : 0;
+    static constexpr int A_ST = kTma ? (NT == 256 ? IGEMM_A_ST_256 : IGEMM_A_ST_128) : (NT == 256 ? 4 : 6);
+    static constexpr int B_ST = kTma ? (NT == 256 ? IGEMM_B_ST_256 : IGEMM_B_ST_128) : A_ST;
+    static constexpr int STG_STAGES = kTma ? (NT == 256 ? IGEMM_STG_256 : IGEMM_STG_128) : 0;
     static constexpr int TMEM_COLS = NSLOT * NT;
     static constexpr int SMEM_BYTES = 1024 /*align slack*/ + A_ST * A_BYTES + B_ST * B_BYTES +
                                       STG_STAGES * STG_BYTES + EPI_SMEM_BYTES + 512 /*barriers*/;
     static_assert(TMEM_COLS <= 512, "tensor memory has 512 columns");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     static_assert(kTma || A_ST == B_ST, "the global-load producers fill A and B stages together");
+    static_assert(A_ST <= 8 && B_ST <= 8 && STG_STAGES <= 8, "the control block has 8 barriers per ring");
 };
 
 // Slot index and phase parity of a ring of N mbarrier-guarded buffers.
