@@ -19,6 +19,7 @@ namespace i8c {
 namespace {
 
 constexpr int kMaxChunks = 4;
+constexpr int64_t kMinChunkBytes = 8 << 20;
 constexpr int kMaxDevices = 64;
 
 struct DeviceRes {
@@ -77,7 +78,12 @@ conv_status host_plan(const conv_tensor_desc *x, const conv_tensor_desc *w, cons
     // whole images in disjoint, ordered byte ranges?
     const bool batch_outer = N <= 1 || (x->strides[0] >= extent_of_images(x, 1) &&
                                         y->strides[0] >= extent_of_images(y, 1));
-    hp->chunks = (!batch_outer || N < 2) ? 1 : (int)(N < kMaxChunks ? N : kMaxChunks);
+    // chunks only pay off when each moves a good amount of data: at least
+    // kMinChunkBytes of output per chunk
+    int64_t max_chunks = N < kMaxChunks ? N : kMaxChunks;
+    const int64_t y_bytes = desc_extent_elems(y) * 4;
+    while (max_chunks > 1 && y_bytes / max_chunks < kMinChunkBytes) --max_chunks;
+    hp->chunks = (!batch_outer || N < 2) ? 1 : (int)max_chunks;
     hp->per_chunk = N == 0 ? 0 : (N + hp->chunks - 1) / hp->chunks;
     // rounding the chunk size up can leave fewer non-empty chunks (N = 5 in
     // chunks of 2 needs 3, not 4)

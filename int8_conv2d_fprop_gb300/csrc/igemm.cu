@@ -75,24 +75,20 @@ constexpr int EPI_SMEM_BYTES = 8 * 2 * EPI_BUF_BYTES;  // 32 KB
 // kTma: the int8 image tile arrives by TMA (im2col mode) in a ring of
 // STG_STAGES staging buffers and the producer warps convert it shared ->
 // shared; otherwise the producer warps gather it with global loads.
-// The f16 A ring (A_ST stages), the filter ring (B_ST stages) and the int8
-// staging ring (STG stages) advance independently: the filter blocks stream
-// from L2 and need the deepest ring, the conversion into the A ring is short.
+// One ring of ST stages holds the f16 A tile and the filter block of a
+// k-step side by side, guarded by one "full" barrier (128 producer arrivals
+// plus the filter copy's bytes) and one "empty" barrier (one MMA commit), so
+// the single MMA-issuing thread waits once and commits once per k-step.  The
+// int8 staging ring of the TMA path (STG stages) runs ahead of it.
 // Ring depths of the TMA path (tuning knobs; shared memory is the limit).
-#ifndef IGEMM_A_ST_256
-#define IGEMM_A_ST_256 4
-#endif
-#ifndef IGEMM_B_ST_256
-#define IGEMM_B_ST_256 3
+#ifndef IGEMM_ST_256
+#define IGEMM_ST_256 3
 #endif
 #ifndef IGEMM_STG_256
-#define IGEMM_STG_256 3
+#define IGEMM_STG_256 6
 #endif
-#ifndef IGEMM_A_ST_128
-#define IGEMM_A_ST_128 4
-#endif
-#ifndef IGEMM_B_ST_128
-#define IGEMM_B_ST_128 5
+#ifndef IGEMM_ST_128
+#define IGEMM_ST_128 5
 #endif
 #ifndef IGEMM_STG_128
 #define IGEMM_STG_128 4
@@ -101,16 +97,14 @@ constexpr int EPI_SMEM_BYTES = 8 * 2 * EPI_BUF_BYTES;  // 32 KB
 template <int NT, bool kTma>
 struct TileCfg {
     static constexpr int B_BYTES = NT * KS * 2;
-    static constexpr int A_ST = kTma ? (NT == 256 ? IGEMM_A_ST_256 : IGEMM_A_ST_128) : (NT == 256 ? 4 : 6);
-    static constexpr int B_ST = kTma ? (NT == 256 ? IGEMM_B_ST_256 : IGEMM_B_ST_128) : A_ST;
+    static constexpr int ST = kTma ? (NT == 256 ? IGEMM_ST_256 : IGEMM_ST_128) : (NT == 256 ? 4 : 6);
     static constexpr int STG_STAGES = kTma ? (NT == 256 ? IGEMM_STG_256 : IGEMM_STG_128) : 0;
     static constexpr int TMEM_COLS = NSLOT * NT;
-    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + A_ST * A_BYTES + B_ST * B_BYTES +
-                                      STG_STAGES * STG_BYTES + EPI_SMEM_BYTES + 512 /*barriers*/;
+    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + ST * (A_BYTES + B_BYTES) + STG_STAGES * STG_BYTES +
+                                      EPI_SMEM_BYTES + 512 /*barriers*/;
     static_assert(TMEM_COLS <= 512, "tensor memory has 512 columns");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
-    static_assert(kTma || A_ST == B_ST, "the global-load producers fill A and B stages together");
-    static_assert(A_ST <= 8 && B_ST <= 8 && STG_STAGES <= 8, "the control block has 8 barriers per ring");
+    static_assert(ST <= 8 && STG_STAGES <= 8, "the control block has 8 barriers per ring");
 };
 
 // Slot index and phase parity of a ring of N mbarrier-guarded buffers.
@@ -147,8 +141,7 @@ struct IgemmArgs {
 };
 
 struct SharedCtl {
-    uint64_t a_full[8], a_empty[8];      // f16 A ring
-    uint64_t b_full[8], b_empty[8];      // filter ring
+    uint64_t full[8], empty[8];          // A + filter ring
     uint64_t stg_full[8], stg_empty[8];  // TMA path: im2col tile landed / converted
     uint64_t acc_full[NSLOT];
     uint64_t acc_empty[NSLOT];
@@ -268,7 +261,11 @@ __device__ __forceinline__ void cursor_advance(LoadCursor &c, const IgemmArgs &a
 
 // Lets every copy issued into a ring of `depth` slots land: the newest copy
 // into slot s completes phase (copies into s) - 1, and phases complete in
-// order.
+// order.  Used only after an abort.  A filter copy shares its "full" barrier
+// with the 128 producer arrivals, which an aborting CTA may never make; the
+// wait is then cut off after DRAIN_LIMIT_NS.  Copies issued before the abort
+// (itself a wait that ran out after the full time limit) have long landed.
+constexpr uint64_t DRAIN_LIMIT_NS = 10000000;  // 10 ms
 __device__ __forceinline__ void drain_ring(uint64_t *bars, int depth, int64_t issued, uint64_t limit, int *status) {
     for (int s = 0; s < depth; ++s) {
         const int64_t n_s = issued / depth + (s < issued % depth ? 1 : 0);
@@ -279,8 +276,7 @@ __device__ __forceinline__ void drain_ring(uint64_t *bars, int depth, int64_t is
 template <int NT, bool kTma>
 __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_constant__ IgemmArgs a) {
     using Cfg = TileCfg<NT, kTma>;
-    constexpr int A_ST = Cfg::A_ST;
-    constexpr int B_ST = Cfg::B_ST;
+    constexpr int ST = Cfg::ST;
     constexpr int STG = Cfg::STG_STAGES;
     constexpr int B_BYTES = Cfg::B_BYTES;
     constexpr int HALF = NT / 2;  // columns per epilogue thread
@@ -289,11 +285,11 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t *const base_ptr = smem_raw + (base - raw_addr);
     const uint32_t a_smem = base;
-    const uint32_t b_smem = a_smem + A_ST * A_BYTES;
-    const uint32_t stg_smem = b_smem + B_ST * B_BYTES;
+    const uint32_t b_smem = a_smem + ST * A_BYTES;
+    const uint32_t stg_smem = b_smem + ST * B_BYTES;
     const uint32_t epi_smem = stg_smem + STG * STG_BYTES;
-    SharedCtl *ctl = reinterpret_cast<SharedCtl *>(base_ptr + A_ST * A_BYTES + B_ST * B_BYTES + STG * STG_BYTES +
-                                                   EPI_SMEM_BYTES);
+    SharedCtl *ctl =
+        reinterpret_cast<SharedCtl *>(base_ptr + ST * (A_BYTES + B_BYTES) + STG * STG_BYTES + EPI_SMEM_BYTES);
     volatile int32_t *abort_flag = &ctl->abort_flag;
 
     const int warp = threadIdx.x >> 5;
@@ -306,13 +302,11 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
     const int rot = kTma ? (int)(((int64_t)blockIdx.x * 7) % a.k_steps) : 0;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < A_ST; ++i) {
-            ptx::mbar_init(ptx::smem_addr(&ctl->a_full[i]), 128);
-            ptx::mbar_init(ptx::smem_addr(&ctl->a_empty[i]), 1);
-        }
-        for (int i = 0; i < B_ST; ++i) {
-            ptx::mbar_init(ptx::smem_addr(&ctl->b_full[i]), 1);
-            ptx::mbar_init(ptx::smem_addr(&ctl->b_empty[i]), 1);
+        for (int i = 0; i < ST; ++i) {
+            // 128 producer arrivals (A tile written) + 1 arrival with the
+            // filter copy's byte count
+            ptx::mbar_init(ptx::smem_addr(&ctl->full[i]), 129);
+            ptx::mbar_init(ptx::smem_addr(&ctl->empty[i]), 1);
         }
         for (int i = 0; i < STG; ++i) {
             ptx::mbar_init(ptx::smem_addr(&ctl->stg_full[i]), 1);
@@ -346,11 +340,11 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
         ptx::setmaxnreg_dec<PRODUCER_REGS>();
         const uint32_t chunk = threadIdx.x & 3;
         const int row0 = (warp << 5) + (lane >> 2);
-        Ring<A_ST> ra;
+        Ring<ST> ra;
         Ring<STG> rs;
         for (int it = 0; it < total; ++it) {
             if (!wait_phase(ptx::smem_addr(&ctl->stg_full[rs.idx]), rs.phase, abort_flag, limit, a.status)) break;
-            if (!wait_phase(ptx::smem_addr(&ctl->a_empty[ra.idx]), ra.phase ^ 1u, abort_flag, limit, a.status))
+            if (!wait_phase(ptx::smem_addr(&ctl->empty[ra.idx]), ra.phase ^ 1u, abort_flag, limit, a.status))
                 break;
             const uint32_t src = stg_smem + rs.idx * STG_BYTES + chunk * 16u;
             const uint32_t dst = a_smem + ra.idx * A_BYTES;
@@ -367,7 +361,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
             }
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(ptx::smem_addr(&ctl->stg_empty[rs.idx]));
-            ptx::mbar_arrive(ptx::smem_addr(&ctl->a_full[ra.idx]));
+            ptx::mbar_arrive(ptx::smem_addr(&ctl->full[ra.idx]));
             ra.next();
             rs.next();
         }
@@ -387,7 +381,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 cursor_advance(cur, a, row);
             }
         }
-        Ring<A_ST> rg;  // A and B stages advance together on this path
+        Ring<ST> rg;
         int b_tile = blockIdx.x, b_j = 0;  // filter block cursor (thread 0 only)
         int64_t b_issued = 0;
         bool ok = true;
@@ -402,17 +396,12 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                     cursor_load(cur, a, pf[d]);
                     cursor_advance(cur, a, row);
                 }
-                if (!wait_phase(ptx::smem_addr(&ctl->a_empty[rg.idx]), rg.phase ^ 1u, abort_flag, limit, a.status)) {
+                if (!wait_phase(ptx::smem_addr(&ctl->empty[rg.idx]), rg.phase ^ 1u, abort_flag, limit, a.status)) {
                     ok = false;
                     break;
                 }
                 if (threadIdx.x == 0) {
-                    if (!wait_phase(ptx::smem_addr(&ctl->b_empty[rg.idx]), rg.phase ^ 1u, abort_flag, limit,
-                                    a.status)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t bar = ptx::smem_addr(&ctl->b_full[rg.idx]);
+                    const uint32_t bar = ptx::smem_addr(&ctl->full[rg.idx]);
                     ptx::mbar_arrive_expect_tx(bar, B_BYTES);
                     const int nt = b_tile % a.n_tiles;
                     const uint8_t *src = a.wp + ((size_t)nt * a.k_steps + b_j) * (size_t)B_BYTES;
@@ -432,19 +421,21 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                     ptx::st_shared_v4(dst + ((((uint32_t)(2 * i + 1)) ^ swz) << 4), hi);
                 }
                 ptx::fence_proxy_async_smem();
-                ptx::mbar_arrive(ptx::smem_addr(&ctl->a_full[rg.idx]));
+                ptx::mbar_arrive(ptx::smem_addr(&ctl->full[rg.idx]));
                 rg.next();
             }
         }
         // let every filter copy this thread issued land before the CTA exits
-        if (threadIdx.x == 0 && *abort_flag) drain_ring(ctl->b_full, B_ST, b_issued, limit, a.status);
+        if (threadIdx.x == 0 && *abort_flag) drain_ring(ctl->full, ST, b_issued, DRAIN_LIMIT_NS, a.status);
     } else if (warp < FIRST_EPI_WARP) {
         // ------------------------------------------------------------ MMA issuer
         ptx::setmaxnreg_dec<PRODUCER_REGS>();
         if (warp == MMA_WARP && lane == 0) {
             constexpr uint32_t idesc = ptx::idesc_f16_f32(MT, NT);
-            Ring<A_ST> ra;
-            Ring<B_ST> rb;
+            // stage s descriptors = stage 0 descriptors + s * (stage bytes >> 4)
+            const uint64_t adesc0 = ptx::smem_desc_sw128(a_smem);
+            const uint64_t bdesc0 = ptx::smem_desc_sw128(b_smem);
+            Ring<ST> rg;
             uint32_t gi = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
@@ -460,26 +451,24 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                     ptx::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + slot * NT;
                     for (int j = js; j < je; ++j) {
-                        if (!wait_phase(ptx::smem_addr(&ctl->a_full[ra.idx]), ra.phase, abort_flag, limit,
-                                        a.status) ||
-                            !wait_phase(ptx::smem_addr(&ctl->b_full[rb.idx]), rb.phase, abort_flag, limit,
-                                        a.status)) {
+                        // the stage's operands were published by TMA (complete_tx) or
+                        // by producer stores followed by fence.proxy.async and the
+                        // barrier arrive; waiting on the barrier orders them before
+                        // the MMAs (no tcgen05 fence: nothing tcgen05-side to order)
+                        if (!wait_phase(ptx::smem_addr(&ctl->full[rg.idx]), rg.phase, abort_flag, limit, a.status)) {
                             ok = false;
                             break;
                         }
-                        ptx::tc_fence_after();
-                        const uint64_t adesc = ptx::smem_desc_sw128(a_smem + ra.idx * A_BYTES);
-                        const uint64_t bdesc = ptx::smem_desc_sw128(b_smem + rb.idx * B_BYTES);
+                        const uint64_t adesc = adesc0 + (uint64_t)(rg.idx * (A_BYTES >> 4));
+                        const uint64_t bdesc = bdesc0 + (uint64_t)(rg.idx * (B_BYTES >> 4));
 #pragma unroll
                         for (int kk = 0; kk < KS / 16; ++kk) {
                             // advance 16 f16 = 32 bytes along K inside the swizzled row
                             ptx::mma_f16_ss(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
                                             (j > js || kk > 0) ? 1u : 0u);
                         }
-                        ptx::mma_commit(ptx::smem_addr(&ctl->a_empty[ra.idx]));
-                        ptx::mma_commit(ptx::smem_addr(&ctl->b_empty[rb.idx]));
-                        ra.next();
-                        rb.next();
+                        ptx::mma_commit(ptx::smem_addr(&ctl->empty[rg.idx]));
+                        rg.next();
                     }
                     if (!ok) break;
                     ptx::mma_commit(ptx::smem_addr(&ctl->acc_full[slot]));
@@ -530,7 +519,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
         } else if (kTma && warp == B_ISSUER_WARP && lane == 0) {
             // pre-swizzled f16 filter blocks, one bulk copy per k-step, in the
             // same rotated k-step order as the image tiles
-            Ring<B_ST> rb;
+            Ring<ST> rb;
             int64_t issued = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
@@ -539,19 +528,19 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 for (int j = 0; j < a.k_steps; ++j) {
                     int jr = j + rot;
                     if (jr >= a.k_steps) jr -= a.k_steps;
-                    if (!wait_phase(ptx::smem_addr(&ctl->b_empty[rb.idx]), rb.phase ^ 1u, abort_flag, limit,
+                    if (!wait_phase(ptx::smem_addr(&ctl->empty[rb.idx]), rb.phase ^ 1u, abort_flag, limit,
                                     a.status)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t bar = ptx::smem_addr(&ctl->b_full[rb.idx]);
+                    const uint32_t bar = ptx::smem_addr(&ctl->full[rb.idx]);
                     ptx::mbar_arrive_expect_tx(bar, B_BYTES);
                     ptx::bulk_copy_g2s(b_smem + rb.idx * B_BYTES, blk + (size_t)jr * B_BYTES, B_BYTES, bar);
                     ++issued;
                     rb.next();
                 }
             }
-            if (*abort_flag) drain_ring(ctl->b_full, B_ST, issued, limit, a.status);
+            if (*abort_flag) drain_ring(ctl->full, ST, issued, DRAIN_LIMIT_NS, a.status);
         }
         __syncwarp();
     } else {
