@@ -71,6 +71,10 @@ def _bind(path: str):
                                              i64p, i64p, ctypes.c_void_p,
                                              ctypes.POINTER(_Params), i64p, ctypes.c_int64,
                                              ctypes.c_void_p]
+    lib.oracle_conv_fprop_i8.restype = ctypes.c_int
+    lib.oracle_conv_fprop_i8.argtypes = [ctypes.c_void_p, i64p, i64p, ctypes.c_void_p, i64p, i64p,
+                                         ctypes.c_void_p, i64p, i64p, ctypes.c_void_p,
+                                         ctypes.POINTER(_Params), ctypes.c_int32]
     lib.oracle_out_extent.restype = ctypes.c_int64
     lib.oracle_out_extent.argtypes = [ctypes.c_int64] * 6
     lib.oracle_num_threads.restype = ctypes.c_int
@@ -124,11 +128,12 @@ def out_dims(x_dims, w_dims, pre=(0, 0), post=(0, 0), stride=(1, 1), dilation=(1
 def conv_fprop(x_flat: np.ndarray, x_dims, x_strides, w_flat: np.ndarray, w_dims, w_strides,
                pre=(0, 0), post=(0, 0), stride=(1, 1), dilation=(1, 1), mode: int = 0,
                bias: Optional[np.ndarray] = None, relu: bool = False,
-               y_strides=None) -> np.ndarray:
+               y_strides=None, out_int8: bool = False, out_shift: int = 0) -> np.ndarray:
     """Full convolution.  Inputs are flat buffers plus logical dims and element
-    strides.  Returns the logical int32 output [N,K,P,Q] (packed NCHW) unless
+    strides.  Returns the logical output [N,K,P,Q] (packed NCHW) unless
     ``y_strides`` is given, in which case the flat buffer in that layout is
-    returned."""
+    returned.  The output is int32, or with ``out_int8`` int8 after the
+    rounding right shift by ``out_shift`` and saturation."""
     lib = _load()
     x_flat = np.ascontiguousarray(x_flat, dtype=np.int8)
     w_flat = np.ascontiguousarray(w_flat, dtype=np.int8)
@@ -136,13 +141,19 @@ def conv_fprop(x_flat: np.ndarray, x_dims, x_strides, w_flat: np.ndarray, w_dims
     if y_strides is None:
         y_strides = (yd[1] * yd[2] * yd[3], yd[2] * yd[3], yd[3], 1)
     ysize = 1 + sum((d - 1) * s for d, s in zip(yd, y_strides)) if min(yd) > 0 else 0
-    y = np.zeros(max(ysize, 1), dtype=np.int32)
+    y = np.zeros(max(ysize, 1), dtype=np.int8 if out_int8 else np.int32)
     b = None if bias is None else np.ascontiguousarray(bias, dtype=np.int32)
     p = _params(pre, post, stride, dilation, mode, relu)
-    rc = lib.oracle_conv_fprop(x_flat.ctypes.data, _i64(x_dims), _i64(x_strides),
-                               w_flat.ctypes.data, _i64(w_dims), _i64(w_strides),
-                               y.ctypes.data, _i64(yd), _i64(y_strides),
-                               None if b is None else b.ctypes.data, ctypes.byref(p))
+    if out_int8:
+        rc = lib.oracle_conv_fprop_i8(x_flat.ctypes.data, _i64(x_dims), _i64(x_strides),
+                                      w_flat.ctypes.data, _i64(w_dims), _i64(w_strides),
+                                      y.ctypes.data, _i64(yd), _i64(y_strides),
+                                      None if b is None else b.ctypes.data, ctypes.byref(p), int(out_shift))
+    else:
+        rc = lib.oracle_conv_fprop(x_flat.ctypes.data, _i64(x_dims), _i64(x_strides),
+                                   w_flat.ctypes.data, _i64(w_dims), _i64(w_strides),
+                                   y.ctypes.data, _i64(yd), _i64(y_strides),
+                                   None if b is None else b.ctypes.data, ctypes.byref(p))
     if rc == 2:
         raise OverflowError("accumulator outside int32")
     if rc != 0:

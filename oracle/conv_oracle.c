@@ -38,6 +38,15 @@
  * An accumulator outside int32 is reported (return value 2) instead of being
  * wrapped: the int32 output type of the compute_data_type=INT32 reading
  * cannot hold it.
+ *
+ * int8 output (oracle_conv_fprop_i8): the int32 value above (after bias and
+ * ReLU) is requantised by an optional rounding arithmetic right shift,
+ *   v' = floor((v + 2^(shift-1)) / 2^shift)   for shift > 0,  v' = v for 0,
+ * then saturated to [-128, 127].  The saturation is the clamp of the naive
+ * loop in "Building a From-Scratch INT8 Strided Convolution Kernel" (section
+ * "Step 2") and what the forum thread's int8-typed output holds (its printed
+ * words are the int32 truth clamped to int8); the shift is the plainest
+ * integer reading of that post's "ReLU and quantization step" roadmap item.
  */
 #include <stdint.h>
 #include <stddef.h>
@@ -122,6 +131,43 @@ int oracle_conv_fprop(const int8_t *x, const int64_t *xd, const int64_t *xs,
                     int32_t v = 0;
                     if (one_output(x, xd, xs, w, wd, ws, bias, pp, n, k, p, q, &v)) bad = 1;
                     y[n * ys[0] + k * ys[1] + p * ys[2] + q * ys[3]] = v;
+                }
+            }
+        }
+    }
+    return bad ? ORACLE_ACC_OUT_OF_INT32 : ORACLE_OK;
+}
+
+/* int8 output: v (int32, after bias and ReLU) -> rounding shift -> clamp. */
+static int8_t requant_i8(int32_t v, int32_t shift) {
+    int64_t t = v;
+    if (shift > 0) {
+        t += (int64_t)1 << (shift - 1);
+        /* floor division by 2^shift, also for negative t */
+        t = (t >= 0) ? (t >> shift) : -((-t + ((int64_t)1 << shift) - 1) >> shift);
+    }
+    if (t > 127) t = 127;
+    if (t < -128) t = -128;
+    return (int8_t)t;
+}
+
+int oracle_conv_fprop_i8(const int8_t *x, const int64_t *xd, const int64_t *xs,
+                         const int8_t *w, const int64_t *wd, const int64_t *ws,
+                         int8_t *y, const int64_t *yd, const int64_t *ys,
+                         const int32_t *bias, const oracle_params *pp, int32_t shift) {
+    int rc = check_args(xd, wd, yd, pp);
+    if (rc) return rc;
+    if (shift < 0 || shift > 31) return ORACLE_BAD_ARGS;
+    const int64_t N = yd[0], K = yd[1], P = yd[2], Q = yd[3];
+    int bad = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic) reduction(| : bad)
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t k = 0; k < K; ++k) {
+            for (int64_t p = 0; p < P; ++p) {
+                for (int64_t q = 0; q < Q; ++q) {
+                    int32_t v = 0;
+                    if (one_output(x, xd, xs, w, wd, ws, bias, pp, n, k, p, q, &v)) bad = 1;
+                    y[n * ys[0] + k * ys[1] + p * ys[2] + q * ys[3]] = requant_i8(v, shift);
                 }
             }
         }

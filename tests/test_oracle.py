@@ -345,6 +345,39 @@ def test_bias_wraps_as_int32():
     assert y[0, 0, 0, 0] == ((127 * 127 + 2 ** 31 - 1 + 2 ** 31) % 2 ** 32) - 2 ** 31
 
 
+@pytest.mark.parametrize("shift", [0, 1, 5, 9, 14, 31])
+def test_int8_output_is_requantised_int32(shift):
+    """int8 output = saturate(floor((y + 2^(shift-1)) / 2^shift)) of the int32
+    result, computed here in numpy int64 from the oracle's int32 output."""
+    x = _rand(110 + shift, (2, 5, 7, 6))
+    w = _rand(111 + shift, (4, 5, 3, 2))
+    b = np.array([-(1 << 20), 77, 0, 1 << 19], dtype=np.int32)
+    kw = dict(pre=(1, 0), post=(0, 1), stride=(1, 2), bias=b, relu=shift % 2 == 1)
+    y32 = _run(x, w, **kw).astype(np.int64)
+    y8 = _run(x, w, out_int8=True, out_shift=shift, **kw)
+    assert y8.dtype == np.int8
+    t = y32 if shift == 0 else np.floor_divide(y32 + (1 << (shift - 1)), 1 << shift)
+    assert np.array_equal(y8, np.clip(t, -128, 127))
+    if shift == 0:
+        assert np.array_equal(y8, oracle.saturate_int8(y32))
+
+
+def test_int8_output_rounding_and_saturation_closed_forms():
+    """A 1x1, one-channel convolution is a product x*w; the rounding right
+    shift rounds halves up (towards +inf) and the result saturates."""
+    xs = np.array([3, -3, 2, -2, 5, -5, 1, -1, 127, -128, 127], dtype=np.int8)
+    ws = np.array([1, 1, 1, 1, 1, 1, 1, 1, 127, 127, -128], dtype=np.int8)
+    expect = {0: [3, -3, 2, -2, 5, -5, 1, -1, 127, -128, -128],
+              1: [2, -1, 1, -1, 3, -2, 1, 0, 127, -128, -128],
+              2: [1, -1, 1, 0, 1, -1, 0, 0, 127, -128, -128],
+              8: [0, 0, 0, 0, 0, 0, 0, 0, 63, -63, -63]}
+    x = xs.reshape(1, 1, 1, -1)
+    for shift, exp in expect.items():
+        got = [int(_run(x[..., i:i + 1], ws[i].reshape(1, 1, 1, 1), out_int8=True, out_shift=shift)[0, 0, 0, 0])
+               for i in range(len(xs))]
+        assert got == exp, (shift, got)
+
+
 def test_points_match_full_output():
     cfg = synth.CONFIGS["p4_shape"]
     x, w, _ = synth.make_inputs(cfg)
@@ -384,6 +417,8 @@ MUTATIONS = {
     "padding_not_zero": ("continue; /* zero padding */", "{ h = h < 0 ? 0 : (h >= H ? H - 1 : h); ww = ww < 0 ? 0 : (ww >= W ? W - 1 : ww); }"),
     "relu_before_bias": ("if (bias) v = (int32_t)((uint32_t)v + (uint32_t)bias[k]);\n    if (pp->relu && v < 0) v = 0;",
                          "if (pp->relu && v < 0) v = 0;\n    if (bias) v = (int32_t)((uint32_t)v + (uint32_t)bias[k]);"),
+    "int8_no_saturation": ("    if (t > 127) t = 127;\n", ""),
+    "int8_truncating_shift": ("        t += (int64_t)1 << (shift - 1);\n", ""),
 }
 
 _PIN_FUNCS = None
@@ -400,6 +435,7 @@ def _pin_suite():
         lambda: [test_constant_inputs_count_inbound_taps(v) for v in (1, -128)],
         test_flip_equivalence_between_modes,
         test_bias_then_relu,
+        test_int8_output_rounding_and_saturation_closed_forms,
     ]
     for f in funcs:
         try:
