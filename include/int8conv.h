@@ -53,7 +53,7 @@ typedef enum {
     CONV_OK = 0,
     CONV_ERR_NULL_PTR = 1,            /* a required pointer is NULL */
     CONV_ERR_RANK = 2,                /* a descriptor's rank is not 4 */
-    CONV_ERR_DTYPE = 3,               /* image/filter not INT8, output not INT32 */
+    CONV_ERR_DTYPE = 3,               /* image/filter not INT8; output not INT32 (INT8 with CONV_EPILOGUE_INT8_OUT) */
     CONV_ERR_SHAPE_MISMATCH = 4,      /* C, K, N or the output dims disagree */
     CONV_ERR_BAD_STRIDES = 5,         /* non-positive stride of a dim > 1, or elements alias */
     CONV_ERR_BUFFER_TOO_SMALL = 6,    /* descriptor's capacity_bytes below its extent */
@@ -90,6 +90,11 @@ typedef enum {
 /* Epilogue flags (bit set). */
 #define CONV_EPILOGUE_BIAS 1u /* add int32 bias[k] */
 #define CONV_EPILOGUE_RELU 2u /* max(0, .) after the bias */
+/* int8 output: after bias and ReLU, v -> floor((v + 2^(s-1)) / 2^s) for
+ * s = out_shift > 0 (a rounding right shift; s = 0 leaves v), then clamped to
+ * [-128, 127].  The output descriptor must then be CONV_INT8 (and must be
+ * CONV_INT32 without this flag: an output type is never inferred). */
+#define CONV_EPILOGUE_INT8_OUT 4u
 
 /*
  * Tensor descriptor.  dims and strides are in LOGICAL order: [N,C,H,W] for
@@ -119,10 +124,12 @@ typedef struct {
     int32_t compute_dtype; /* must be CONV_INT32 */
     uint32_t epilogue;     /* CONV_EPILOGUE_* bits */
     int32_t algo;          /* conv_algo */
+    int32_t out_shift;     /* 0..31, with CONV_EPILOGUE_INT8_OUT only (else 0) */
+    int32_t reserved;      /* must be 0 */
 } conv_fprop_params;
 
 /* Fill *p with: no padding, stride 1, dilation 1, cross-correlation,
- * compute INT32, no epilogue, automatic algorithm. */
+ * compute INT32, no epilogue, automatic algorithm, shift 0. */
 void conv_params_init(conv_fprop_params *p);
 
 /* The symmetric-padding overload: pre_padding = post_padding = pad. */
@@ -166,12 +173,14 @@ conv_status conv_fprop_workspace_size(const conv_tensor_desc *x, const conv_tens
  * Y = conv_fprop(X, W) on `stream` (a cudaStream_t; NULL = legacy default).
  * x_dev, w_dev, y_dev, bias_dev and workspace are device pointers on the
  * current device.  bias_dev holds K int32 values and is read only when
- * p->epilogue has CONV_EPILOGUE_BIAS.  The output must not overlap the
- * inputs or the workspace.  Asynchronous: returns after queuing the kernels.
+ * p->epilogue has CONV_EPILOGUE_BIAS.  y_dev holds int32 elements, or int8
+ * elements with CONV_EPILOGUE_INT8_OUT (as its descriptor says).  The output
+ * must not overlap the inputs or the workspace.  Asynchronous: returns after
+ * queuing the kernels.
  */
 conv_status conv_fprop(const conv_tensor_desc *x, const int8_t *x_dev,
                        const conv_tensor_desc *w, const int8_t *w_dev,
-                       const conv_tensor_desc *y, int32_t *y_dev,
+                       const conv_tensor_desc *y, void *y_dev,
                        const int32_t *bias_dev, const conv_fprop_params *p,
                        void *workspace, size_t workspace_bytes, void *stream);
 
@@ -194,7 +203,7 @@ conv_status conv_fprop_pack_filter(const conv_tensor_desc *x, const conv_tensor_
 
 conv_status conv_fprop_prepacked(const conv_tensor_desc *x, const int8_t *x_dev,
                                  const conv_tensor_desc *w, const int8_t *w_dev,
-                                 const conv_tensor_desc *y, int32_t *y_dev,
+                                 const conv_tensor_desc *y, void *y_dev,
                                  const int32_t *bias_dev, const conv_fprop_params *p,
                                  void *workspace, size_t workspace_bytes, void *stream);
 
@@ -225,7 +234,7 @@ conv_status conv_fprop_host_buffer_size(const conv_tensor_desc *x, const conv_te
 
 conv_status conv_fprop_host(const conv_tensor_desc *x, const int8_t *x_host,
                             const conv_tensor_desc *w, const int8_t *w_host,
-                            const conv_tensor_desc *y, int32_t *y_host,
+                            const conv_tensor_desc *y, void *y_host,
                             const int32_t *bias_host, const conv_fprop_params *p,
                             void *device_buffer, size_t device_buffer_bytes, void *stream);
 
@@ -256,7 +265,7 @@ conv_status conv_fprop_host(const conv_tensor_desc *x, const int8_t *x_host,
 
 conv_status conv_fprop_static_workspace(const conv_tensor_desc *x, const int8_t *x_dev,
                                         const conv_tensor_desc *w, const int8_t *w_dev,
-                                        const conv_tensor_desc *y, int32_t *y_dev,
+                                        const conv_tensor_desc *y, void *y_dev,
                                         const int32_t *bias_dev, const conv_fprop_params *p,
                                         void *stream);
 

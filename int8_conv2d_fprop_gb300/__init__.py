@@ -1,5 +1,5 @@
 """Python binding of libint8conv.so: INT8 2-D convolution forward propagation
-with int32 results on GB300 (sm_103a).
+with int32 results (or int8 after a rounding right shift) on GB300 (sm_103a).
 
 Argument marshalling only: every step of the computation runs in the CUDA
 kernels behind the C ABI declared in ``include/int8conv.h``.  PyTorch provides
@@ -28,7 +28,7 @@ CONV_INT8, CONV_INT32 = 1, 2
 CROSS_CORRELATION, CONVOLUTION = 0, 1
 ALGO_AUTO, ALGO_IMPLICIT_GEMM, ALGO_DIRECT_DP4A, ALGO_DIRECT_GENERIC = 0, 1, 2, 3
 ALGO_IMPLICIT_GEMM_GLOBAL_LOADS = 4
-EPILOGUE_BIAS, EPILOGUE_RELU = 1, 2
+EPILOGUE_BIAS, EPILOGUE_RELU, EPILOGUE_INT8_OUT = 1, 2, 4
 ALGO_NAMES = {ALGO_IMPLICIT_GEMM: "implicit_gemm", ALGO_DIRECT_DP4A: "direct_dp4a",
               ALGO_DIRECT_GENERIC: "direct_generic",
               ALGO_IMPLICIT_GEMM_GLOBAL_LOADS: "implicit_gemm_global_loads"}
@@ -100,13 +100,16 @@ class Params(ctypes.Structure):
     _fields_ = [("pre_padding", ctypes.c_int64 * 2), ("post_padding", ctypes.c_int64 * 2),
                 ("stride", ctypes.c_int64 * 2), ("dilation", ctypes.c_int64 * 2),
                 ("mode", ctypes.c_int32), ("compute_dtype", ctypes.c_int32),
-                ("epilogue", ctypes.c_uint32), ("algo", ctypes.c_int32)]
+                ("epilogue", ctypes.c_uint32), ("algo", ctypes.c_int32),
+                ("out_shift", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
     @classmethod
     def make(cls, pre_padding=(0, 0), post_padding=(0, 0), stride=(1, 1), dilation=(1, 1),
              mode: int = CROSS_CORRELATION, bias: bool = False, relu: bool = False,
              algo: int = ALGO_AUTO, padding: Optional[Sequence[int]] = None,
-             compute_dtype: int = CONV_INT32) -> "Params":
+             compute_dtype: int = CONV_INT32, out_shift: Optional[int] = None) -> "Params":
+        """out_shift=None: int32 output; an integer s in 0..31: int8 output
+        round(v / 2^s) (halves toward +inf) saturated to [-128, 127]."""
         p = cls()
         lib().conv_params_init(ctypes.byref(p))
         if padding is not None:
@@ -120,6 +123,9 @@ class Params(ctypes.Structure):
         p.mode = int(mode)
         p.compute_dtype = int(compute_dtype)
         p.epilogue = (EPILOGUE_BIAS if bias else 0) | (EPILOGUE_RELU if relu else 0)
+        if out_shift is not None:
+            p.epilogue |= EPILOGUE_INT8_OUT
+            p.out_shift = int(out_shift)
         p.algo = int(algo)
         return p
 
@@ -252,11 +258,14 @@ def conv_fprop_host_raw(xd: TensorDesc, x_host: int, wd: TensorDesc, w_host: int
 
 def conv_fprop_from_host(x, w, bias=None, *, out, device_buffer=None, stream=None, pre_padding=(0, 0),
                          post_padding=(0, 0), padding=None, stride=(1, 1), dilation=(1, 1),
-                         mode: int = CROSS_CORRELATION, relu: bool = False, algo: int = ALGO_AUTO):
+                         mode: int = CROSS_CORRELATION, relu: bool = False, algo: int = ALGO_AUTO,
+                         out_shift: Optional[int] = None):
     """conv_fprop on CPU tensors (pin them for overlapped copies); ``out`` is
-    a CPU int32 tensor.  Asynchronous on ``stream``; returns ``out``."""
+    a CPU int32 tensor (int8 when ``out_shift`` is given).  Asynchronous on
+    ``stream``; returns ``out``."""
     import torch
-    p = Params.make(pre_padding, post_padding, stride, dilation, mode, bias is not None, relu, algo, padding)
+    p = Params.make(pre_padding, post_padding, stride, dilation, mode, bias is not None, relu, algo, padding,
+                    out_shift=out_shift)
     xd, wd, yd = TensorDesc.from_tensor(x), TensorDesc.from_tensor(w), TensorDesc.from_tensor(out)
     need = host_buffer_size(xd, wd, yd, p)
     if device_buffer is None or device_buffer.numel() * device_buffer.element_size() < need:
@@ -280,24 +289,28 @@ def selftest_wait_timeout(limit_us: int, stream: int = 0) -> int:
 
 def conv_fprop(x, w, bias=None, *, pre_padding=(0, 0), post_padding=(0, 0), padding=None,
                stride=(1, 1), dilation=(1, 1), mode: int = CROSS_CORRELATION, relu: bool = False,
-               algo: int = ALGO_AUTO, out=None, workspace=None, stream=None):
+               algo: int = ALGO_AUTO, out=None, workspace=None, stream=None, out_shift: Optional[int] = None):
     """Y = conv_fprop(x, w) on the GPU.
 
     x: int8 CUDA tensor [N,C,H,W] with any strides; w: int8 [K,C,R,S]; bias:
     optional int32 [K]; out: optional int32 [N,K,P,Q] (any strides; default:
-    the image's memory format).  Runs on ``stream`` (a torch.cuda.Stream;
-    default the current stream).  Returns ``out``.
+    the image's memory format), int8 when ``out_shift`` is given (the int32
+    result after bias and ReLU, shifted right by out_shift with rounding and
+    saturated).  Runs on ``stream`` (a torch.cuda.Stream; default the current
+    stream).  Returns ``out``.
     """
     import torch
     if not (x.is_cuda and w.is_cuda):
         raise ValueError("x and w must be CUDA tensors")
-    p = Params.make(pre_padding, post_padding, stride, dilation, mode, bias is not None, relu, algo, padding)
+    p = Params.make(pre_padding, post_padding, stride, dilation, mode, bias is not None, relu, algo, padding,
+                    out_shift=out_shift)
     xd, wd = TensorDesc.from_tensor(x), TensorDesc.from_tensor(w)
     od = output_dims(xd, wd, p)
     if out is None:
         cl = x.dim() == 4 and x.is_contiguous(memory_format=torch.channels_last) and not x.is_contiguous()
         fmt = torch.channels_last if cl else torch.contiguous_format
-        out = torch.empty(od, dtype=torch.int32, device=x.device, memory_format=fmt)
+        odt = torch.int32 if out_shift is None else torch.int8
+        out = torch.empty(od, dtype=odt, device=x.device, memory_format=fmt)
     yd = TensorDesc.from_tensor(out)
     ws_bytes = workspace_size(xd, wd, yd, p)
     if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):

@@ -179,7 +179,7 @@ namespace {
 // Validation, planning and pointer checks shared by the three entry points
 // that launch work.  *nothing_to_do is set for an empty output.
 conv_status prepare_call(const conv_tensor_desc *x, const int8_t *x_dev, const conv_tensor_desc *w,
-                         const int8_t *w_dev, const conv_tensor_desc *y, int32_t *y_dev, const int32_t *bias_dev,
+                         const int8_t *w_dev, const conv_tensor_desc *y, void *y_dev, const int32_t *bias_dev,
                          const conv_fprop_params *p, void *workspace, size_t workspace_bytes, ConvGeom *g,
                          int *algo, IgemmPlan *pl, bool *nothing_to_do) {
     conv_status st = plan_call(x, w, y, p, x_dev, g, algo, pl);
@@ -188,7 +188,7 @@ conv_status prepare_call(const conv_tensor_desc *x, const int8_t *x_dev, const c
     if (*nothing_to_do) return CONV_OK;
     if (!x_dev || !w_dev || !y_dev) return CONV_ERR_NULL_PTR;
     if (g->bias && !bias_dev) return CONV_ERR_NULL_PTR;
-    const uint64_t ybytes = (uint64_t)desc_extent_elems(y) * 4;
+    const uint64_t ybytes = (uint64_t)desc_extent_elems(y) * (g->out_int8 ? 1u : 4u);
     if (overlaps(y_dev, ybytes, x_dev, (uint64_t)desc_extent_elems(x)) ||
         overlaps(y_dev, ybytes, w_dev, (uint64_t)desc_extent_elems(w)) ||
         overlaps(y_dev, ybytes, workspace, workspace_bytes) ||
@@ -205,7 +205,7 @@ conv_status prepare_call(const conv_tensor_desc *x, const int8_t *x_dev, const c
 }
 
 conv_status run_main(const ConvGeom &g, int algo, const IgemmPlan &pl, const int8_t *x_dev, const int8_t *w_dev,
-                     int32_t *y_dev, const int32_t *bias_dev, void *workspace, void *stream) {
+                     void *y_dev, const int32_t *bias_dev, void *workspace, void *stream) {
     switch (algo) {
         case CONV_ALGO_IMPLICIT_GEMM:
             return igemm_main_launch(g, pl, x_dev, y_dev, bias_dev, workspace, stream);
@@ -219,7 +219,7 @@ conv_status run_main(const ConvGeom &g, int algo, const IgemmPlan &pl, const int
 }  // namespace
 
 conv_status conv_fprop(const conv_tensor_desc *x, const int8_t *x_dev, const conv_tensor_desc *w,
-                       const int8_t *w_dev, const conv_tensor_desc *y, int32_t *y_dev, const int32_t *bias_dev,
+                       const int8_t *w_dev, const conv_tensor_desc *y, void *y_dev, const int32_t *bias_dev,
                        const conv_fprop_params *p, void *workspace, size_t workspace_bytes, void *stream) {
     ConvGeom g;
     IgemmPlan pl;
@@ -251,7 +251,7 @@ conv_status conv_fprop_pack_filter(const conv_tensor_desc *x, const conv_tensor_
 }
 
 conv_status conv_fprop_prepacked(const conv_tensor_desc *x, const int8_t *x_dev, const conv_tensor_desc *w,
-                                 const int8_t *w_dev, const conv_tensor_desc *y, int32_t *y_dev,
+                                 const int8_t *w_dev, const conv_tensor_desc *y, void *y_dev,
                                  const int32_t *bias_dev, const conv_fprop_params *p, void *workspace,
                                  size_t workspace_bytes, void *stream) {
     ConvGeom g;

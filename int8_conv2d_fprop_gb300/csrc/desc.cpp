@@ -94,7 +94,9 @@ static conv_status check_params(const conv_fprop_params *p) {
             return CONV_ERR_TOO_LARGE;
     }
     if (p->mode != CONV_CROSS_CORRELATION && p->mode != CONV_CONVOLUTION) return CONV_ERR_BAD_PARAM;
-    if (p->epilogue & ~(CONV_EPILOGUE_BIAS | CONV_EPILOGUE_RELU)) return CONV_ERR_BAD_PARAM;
+    if (p->epilogue & ~(CONV_EPILOGUE_BIAS | CONV_EPILOGUE_RELU | CONV_EPILOGUE_INT8_OUT)) return CONV_ERR_BAD_PARAM;
+    if (p->out_shift < 0 || p->out_shift > 31 || p->reserved != 0) return CONV_ERR_BAD_PARAM;
+    if (p->out_shift != 0 && !(p->epilogue & CONV_EPILOGUE_INT8_OUT)) return CONV_ERR_BAD_PARAM;
     if (p->algo < CONV_ALGO_AUTO || p->algo > CONV_ALGO_IMPLICIT_GEMM_GLOBAL_LOADS) return CONV_ERR_BAD_PARAM;
     return CONV_OK;
 }
@@ -117,6 +119,8 @@ void make_geom(const conv_tensor_desc *x, const conv_tensor_desc *w, const conv_
     g->mode = p->mode;
     g->bias = (p->epilogue & CONV_EPILOGUE_BIAS) != 0;
     g->relu = (p->epilogue & CONV_EPILOGUE_RELU) != 0;
+    g->out_int8 = (p->epilogue & CONV_EPILOGUE_INT8_OUT) != 0;
+    g->out_shift = p->out_shift;
 }
 
 }  // namespace i8c
@@ -203,7 +207,9 @@ conv_status conv_fprop_validate(const conv_tensor_desc *x, const conv_tensor_des
     const int64_t out_min[4] = {0, 0, 1, 1};
     if ((st = check_desc(x, CONV_INT8, img_min))) return st;
     if ((st = check_desc(w, CONV_INT8, flt_min))) return st;
-    if ((st = check_desc(y, CONV_INT32, out_min))) return st;
+    // the output type is what the caller asked for, never a default
+    const int32_t y_type = (p->epilogue & CONV_EPILOGUE_INT8_OUT) ? CONV_INT8 : CONV_INT32;
+    if ((st = check_desc(y, y_type, out_min))) return st;
     int64_t od[4];
     if ((st = conv_fprop_output_dims(x, w, p, od))) return st;
     for (int i = 0; i < 4; ++i)
@@ -227,7 +233,8 @@ const char *conv_status_string(conv_status s) {
         case CONV_OK: return "CONV_OK";
         case CONV_ERR_NULL_PTR: return "CONV_ERR_NULL_PTR: a required pointer is NULL";
         case CONV_ERR_RANK: return "CONV_ERR_RANK: descriptor rank is not 4";
-        case CONV_ERR_DTYPE: return "CONV_ERR_DTYPE: image/filter must be INT8 and output INT32";
+        case CONV_ERR_DTYPE:
+            return "CONV_ERR_DTYPE: image/filter must be INT8, output INT32 (INT8 only with CONV_EPILOGUE_INT8_OUT)";
         case CONV_ERR_SHAPE_MISMATCH: return "CONV_ERR_SHAPE_MISMATCH: dims of image, filter and output disagree";
         case CONV_ERR_BAD_STRIDES: return "CONV_ERR_BAD_STRIDES: non-positive or aliasing strides";
         case CONV_ERR_BUFFER_TOO_SMALL: return "CONV_ERR_BUFFER_TOO_SMALL: buffer smaller than the descriptor's extent";

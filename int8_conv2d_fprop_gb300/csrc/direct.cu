@@ -20,7 +20,7 @@ namespace i8c {
 struct DirectArgs {
     const int8_t *x;
     const int8_t *w;
-    int32_t *y;
+    void *y;  // int32 elements, or int8 when out_int8
     const int32_t *bias;
     int64_t N, C, H, W, K, R, S, P, Q;
     int64_t xs0, xs1, xs2, xs3;
@@ -28,12 +28,15 @@ struct DirectArgs {
     int64_t ys0, ys1, ys2, ys3;
     int64_t pad_h, pad_w, str_h, str_w, dil_h, dil_w;
     int32_t mode, relu;
+    int32_t out_int8, out_shift;
 };
 
-static DirectArgs make_args(const ConvGeom &g, const int8_t *x, const int8_t *w, int32_t *y,
+static DirectArgs make_args(const ConvGeom &g, const int8_t *x, const int8_t *w, void *y,
                             const int32_t *bias) {
     DirectArgs a;
     a.x = x; a.w = w; a.y = y; a.bias = g.bias ? bias : nullptr;
+    a.out_int8 = g.out_int8 ? 1 : 0;
+    a.out_shift = g.out_shift;
     a.N = g.N; a.C = g.C; a.H = g.H; a.W = g.W; a.K = g.K; a.R = g.R; a.S = g.S;
     a.P = g.P; a.Q = g.Q;
     a.xs0 = g.xs[0]; a.xs1 = g.xs[1]; a.xs2 = g.xs[2]; a.xs3 = g.xs[3];
@@ -49,6 +52,13 @@ __device__ __forceinline__ int32_t finish(int32_t acc, const int32_t *bias, int6
     if (bias) acc = (int32_t)((uint32_t)acc + (uint32_t)__ldg(bias + k));
     if (relu) acc = max(acc, 0);
     return acc;
+}
+
+__device__ __forceinline__ void store_out(const DirectArgs &a, int64_t off, int32_t v) {
+    if (a.out_int8)
+        static_cast<int8_t *>(a.y)[off] = requant_i8(v, a.out_shift);
+    else
+        static_cast<int32_t *>(a.y)[off] = v;
 }
 
 // ---------------------------------------------------------------- generic
@@ -82,11 +92,11 @@ __global__ void __launch_bounds__(256) conv_direct_generic_kernel(const DirectAr
                     acc += (int32_t)__ldg(xp + c * a.xs1) * (int32_t)__ldg(wp + c * a.ws1);
             }
         }
-        a.y[n * a.ys0 + k * a.ys1 + p * a.ys2 + q * a.ys3] = finish(acc, a.bias, k, a.relu);
+        store_out(a, n * a.ys0 + k * a.ys1 + p * a.ys2 + q * a.ys3, finish(acc, a.bias, k, a.relu));
     }
 }
 
-conv_status generic_launch(const ConvGeom &g, const int8_t *x, const int8_t *w, int32_t *y,
+conv_status generic_launch(const ConvGeom &g, const int8_t *x, const int8_t *w, void *y,
                            const int32_t *bias, void *stream) {
     DirectArgs a = make_args(g, x, w, y, bias);
     const int64_t total = g.N * g.K * g.P * g.Q;
@@ -176,12 +186,12 @@ __global__ void __launch_bounds__(kDp4aThreads) conv_direct_dp4a_kernel(const Di
         for (int kk = 0; kk < kDp4aKB; ++kk) {
             const int64_t k = k0 + kk;
             if (k < a.K)
-                a.y[n * a.ys0 + k * a.ys1 + p * a.ys2 + q * a.ys3] = finish(acc[kk], a.bias, k, a.relu);
+                store_out(a, n * a.ys0 + k * a.ys1 + p * a.ys2 + q * a.ys3, finish(acc[kk], a.bias, k, a.relu));
         }
     }
 }
 
-conv_status dp4a_launch(const ConvGeom &g, const int8_t *x, const int8_t *w, int32_t *y,
+conv_status dp4a_launch(const ConvGeom &g, const int8_t *x, const int8_t *w, void *y,
                         const int32_t *bias, void *stream) {
     if (!dp4a_supported(g)) return CONV_ERR_ALIGNMENT;
     DirectArgs a = make_args(g, x, w, y, bias);

@@ -63,7 +63,8 @@ struct HostPlan {
     int chunks;
     int64_t per_chunk;       // images per chunk (the last may hold fewer)
     int64_t x_chunk_elems;   // device bytes of one image chunk
-    int64_t y_chunk_elems;   // int32 elements of one output chunk
+    int64_t y_chunk_elems;   // output elements of one output chunk
+    int64_t y_esz;           // bytes per output element (4 for int32, 1 for int8)
     int64_t w_elems;
     size_t ws_bytes;         // conv workspace for one chunk
     size_t off_w, off_bias, off_ws, off_x[2], off_y[2], total;
@@ -75,13 +76,14 @@ conv_status host_plan(const conv_tensor_desc *x, const conv_tensor_desc *w, cons
     conv_status st = conv_fprop_validate(x, w, y, p, bias_elems);
     if (st) return st;
     const int64_t N = x->dims[0];
+    hp->y_esz = (p->epilogue & CONV_EPILOGUE_INT8_OUT) ? 1 : 4;
     // whole images in disjoint, ordered byte ranges?
     const bool batch_outer = N <= 1 || (x->strides[0] >= extent_of_images(x, 1) &&
                                         y->strides[0] >= extent_of_images(y, 1));
     // chunks only pay off when each moves a good amount of data: at least
     // kMinChunkBytes of output per chunk
     int64_t max_chunks = N < kMaxChunks ? N : kMaxChunks;
-    const int64_t y_bytes = desc_extent_elems(y) * 4;
+    const int64_t y_bytes = desc_extent_elems(y) * hp->y_esz;
     while (max_chunks > 1 && y_bytes / max_chunks < kMinChunkBytes) --max_chunks;
     hp->chunks = (!batch_outer || N < 2) ? 1 : (int)max_chunks;
     hp->per_chunk = N == 0 ? 0 : (N + hp->chunks - 1) / hp->chunks;
@@ -94,7 +96,7 @@ conv_status host_plan(const conv_tensor_desc *x, const conv_tensor_desc *w, cons
     conv_tensor_desc xc = *x, yc = *y;
     xc.dims[0] = yc.dims[0] = hp->per_chunk;
     xc.capacity_bytes = (uint64_t)hp->x_chunk_elems;
-    yc.capacity_bytes = (uint64_t)hp->y_chunk_elems * 4;
+    yc.capacity_bytes = (uint64_t)(hp->y_chunk_elems * hp->y_esz);
     hp->ws_bytes = 0;
     if (hp->per_chunk > 0 && (st = conv_fprop_workspace_size(&xc, w, &yc, p, &hp->ws_bytes))) return st;
     size_t off = 0;
@@ -110,7 +112,7 @@ conv_status host_plan(const conv_tensor_desc *x, const conv_tensor_desc *w, cons
     }
     for (int b = 0; b < 2; ++b) {
         hp->off_y[b] = off;
-        off = align256(off + (size_t)hp->y_chunk_elems * 4);
+        off = align256(off + (size_t)(hp->y_chunk_elems * hp->y_esz));
     }
     hp->total = off;
     return CONV_OK;
@@ -134,7 +136,7 @@ conv_status conv_fprop_host_buffer_size(const conv_tensor_desc *x, const conv_te
 }
 
 conv_status conv_fprop_host(const conv_tensor_desc *x, const int8_t *x_host, const conv_tensor_desc *w,
-                            const int8_t *w_host, const conv_tensor_desc *y, int32_t *y_host,
+                            const int8_t *w_host, const conv_tensor_desc *y, void *y_host,
                             const int32_t *bias_host, const conv_fprop_params *p, void *device_buffer,
                             size_t device_buffer_bytes, void *stream) {
     HostPlan hp;
@@ -178,9 +180,9 @@ conv_status conv_fprop_host(const conv_tensor_desc *x, const int8_t *x_host, con
         const int64_t x_elems = hp.chunks == 1 ? desc_extent_elems(x) : extent_of_images(x, nb);
         const int64_t y_elems = hp.chunks == 1 ? desc_extent_elems(y) : extent_of_images(y, nb);
         xc.capacity_bytes = (uint64_t)x_elems;
-        yc.capacity_bytes = (uint64_t)y_elems * 4;
+        yc.capacity_bytes = (uint64_t)(y_elems * hp.y_esz);
         int8_t *x_dev = reinterpret_cast<int8_t *>(buf + hp.off_x[bsel]);
-        int32_t *y_dev = reinterpret_cast<int32_t *>(buf + hp.off_y[bsel]);
+        void *y_dev = buf + hp.off_y[bsel];
         // image chunk in; its buffer was last read by the convolution of chunk c-2
         if (c >= 2 && !ok(cudaStreamWaitEvent(r.s_in, r.ev_cmp[c - 2], 0))) return CONV_ERR_CUDA;
         if (!ok(cudaMemcpyAsync(x_dev, x_host + n0 * x->strides[0], (size_t)x_elems, cudaMemcpyHostToDevice,
@@ -196,8 +198,8 @@ conv_status conv_fprop_host(const conv_tensor_desc *x, const int8_t *x_host, con
         if (!ok(cudaEventRecord(r.ev_cmp[c], r.s_cmp))) return CONV_ERR_CUDA;
         // output chunk out
         if (!ok(cudaStreamWaitEvent(r.s_out, r.ev_cmp[c], 0)) ||
-            !ok(cudaMemcpyAsync(y_host + n0 * y->strides[0], y_dev, (size_t)y_elems * 4, cudaMemcpyDeviceToHost,
-                                r.s_out)) ||
+            !ok(cudaMemcpyAsync(static_cast<uint8_t *>(y_host) + n0 * y->strides[0] * hp.y_esz, y_dev,
+                                (size_t)(y_elems * hp.y_esz), cudaMemcpyDeviceToHost, r.s_out)) ||
             !ok(cudaEventRecord(r.ev_out[c], r.s_out)))
             return CONV_ERR_CUDA;
     }

@@ -122,10 +122,11 @@ struct Ring {
 
 struct IgemmArgs {
     CUtensorMap tmap_x;  // im2col map of the channels-last image (TMA path only)
-    CUtensorMap tmap_y;  // 2-D [pixels][K] int32 map of the output (when y_tma)
+    CUtensorMap tmap_y;  // 2-D [pixels][K] map of the output (when y_tma)
     const int8_t *x;     // channels-last image
     const uint8_t *wp;   // repacked f16 filter blocks
-    int32_t *y;
+    void *y;             // int32 output, or int8 when out_int8
+    int32_t out_int8, out_shift;
     const int32_t *bias;
     int64_t xs_n, xs_h, xs_w;  // element (= byte) strides of the channels-last image
     int64_t ys_n, ys_k, ys_p, ys_q;
@@ -608,21 +609,34 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                     const uint32_t buf = ebase + (uint32_t)(ch & 1) * EPI_BUF_BYTES;
                     if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store that last read buf is done
                     __syncwarp();
-                    const uint32_t rowaddr = buf + (uint32_t)lane * 64u;
+                    int32_t o[EPI_COLS];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        int32_t o[4];
+                    for (int e = 0; e < EPI_COLS; ++e) {
+                        const int i = ch * EPI_COLS + e;
+                        const int k = k0 + i;
+                        int32_t val = acc[i];
+                        if (a.bias && k < a.K) val = (int32_t)((uint32_t)val + (uint32_t)__ldg(a.bias + k));
+                        if (a.relu) val = max(val, 0);
+                        o[e] = val;
+                    }
+                    if (a.out_int8) {
+                        // int8 rows of 16 bytes, unswizzled: lane r's row at r * 16
+                        uint32_t wv[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int i = ch * EPI_COLS + c * 4 + e;
-                            const int k = k0 + i;
-                            int32_t val = acc[i];
-                            if (a.bias && k < a.K) val = (int32_t)((uint32_t)val + (uint32_t)__ldg(a.bias + k));
-                            if (a.relu) val = max(val, 0);
-                            o[e] = val;
+                        for (int c = 0; c < 4; ++c) {
+                            wv[c] = 0;
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                wv[c] |= (uint32_t)(uint8_t)requant_i8(o[c * 4 + e], a.out_shift) << (8 * e);
                         }
-                        ptx::st_shared_v4(rowaddr + ((((uint32_t)c) ^ sw) << 4),
-                                          make_uint4((uint32_t)o[0], (uint32_t)o[1], (uint32_t)o[2], (uint32_t)o[3]));
+                        ptx::st_shared_v4(buf + (uint32_t)lane * 16u, make_uint4(wv[0], wv[1], wv[2], wv[3]));
+                    } else {
+                        const uint32_t rowaddr = buf + (uint32_t)lane * 64u;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            ptx::st_shared_v4(rowaddr + ((((uint32_t)c) ^ sw) << 4),
+                                              make_uint4((uint32_t)o[c * 4], (uint32_t)o[c * 4 + 1],
+                                                         (uint32_t)o[c * 4 + 2], (uint32_t)o[c * 4 + 3]));
                     }
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
@@ -631,9 +645,22 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                         ptx::bulk_commit_group();
                     }
                 }
+            } else if (valid && a.out_int8) {
+                const int k0 = nt * NT + col0;
+                int8_t *yrow = static_cast<int8_t *>(a.y) + yoff;
+#pragma unroll
+                for (int i = 0; i < HALF; ++i) {
+                    const int k = k0 + i;
+                    if (k < a.K) {
+                        int32_t val = acc[i];
+                        if (a.bias) val = (int32_t)((uint32_t)val + (uint32_t)__ldg(a.bias + k));
+                        if (a.relu) val = max(val, 0);
+                        yrow[(int64_t)k * a.ys_k] = requant_i8(val, a.out_shift);
+                    }
+                }
             } else if (valid) {
                 const int k0 = nt * NT + col0;
-                int32_t *yrow = a.y + yoff;
+                int32_t *yrow = static_cast<int32_t *>(a.y) + yoff;
 #pragma unroll
                 for (int c4 = 0; c4 < HALF / 4; ++c4) {
                     const int k = k0 + c4 * 4;
@@ -834,11 +861,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tiled_encoder() {
     return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn.load());
 }
 
-// 2-D map [N*P*Q pixels][K channels] of an int32 output whose pixels follow
-// one another at a fixed stride with channels contiguous (NHWC, possibly with
-// padded pixel rows): box 32 pixels x 16 channels, 64-byte swizzle.  Returns
-// false for any other layout.
-bool encode_output_map(const ConvGeom &g, const int32_t *y, CUtensorMap *map) {
+// 2-D map [N*P*Q pixels][K channels] of the output when its pixels follow one
+// another at a fixed stride with channels contiguous (NHWC, possibly with
+// padded pixel rows): box 32 pixels x 16 channels; int32 elements with the
+// 64-byte swizzle, int8 elements (16-byte rows) unswizzled.  Returns false for
+// any other layout.
+bool encode_output_map(const ConvGeom &g, const void *y, CUtensorMap *map) {
+    const int64_t esz = g.out_int8 ? 1 : 4;
     if (g.ys[1] != 1 && g.K > 1) return false;
     int64_t ps;  // element stride between consecutive pixels
     if (g.Q > 1) {
@@ -852,16 +881,17 @@ bool encode_output_map(const ConvGeom &g, const int32_t *y, CUtensorMap *map) {
         ps = g.N > 1 ? g.ys[0] : g.K;
     }
     const int64_t m_total = g.N * g.P * g.Q;
-    if (ps < g.K || (ps * 4) % 16 != 0 || ((uintptr_t)y % 16) != 0) return false;
-    if (m_total > ((int64_t)1 << 32) || (m_total > 1 && ps * 4 >= ((int64_t)1 << 40))) return false;
+    if (ps < g.K || (ps * esz) % 16 != 0 || ((uintptr_t)y % 16) != 0) return false;
+    if (m_total > ((int64_t)1 << 32) || (m_total > 1 && ps * esz >= ((int64_t)1 << 40))) return false;
     auto enc = tiled_encoder();
     if (!enc) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)g.K, (cuuint64_t)m_total};
-    const cuuint64_t strides[1] = {(cuuint64_t)(ps * 4)};
+    const cuuint64_t strides[1] = {(cuuint64_t)(ps * esz)};
     const cuuint32_t box[2] = {(cuuint32_t)EPI_COLS, 32};
     const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<int32_t *>(y), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+    const CUresult r = enc(map, g.out_int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_INT32, 2,
+                           const_cast<void *>(y), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           g.out_int8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_64B,
                            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -912,7 +942,7 @@ conv_status igemm_pack_filter_launch(const ConvGeom &g, const IgemmPlan &pl, con
     return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
-conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, int32_t *y,
+conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *y,
                               const int32_t *bias, void *workspace, void *stream) {
     cudaStream_t st = (cudaStream_t)stream;
     const int sms = device_sm_count();
@@ -939,6 +969,8 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
     }
     a.wp = wp;
     a.y = y;
+    a.out_int8 = g.out_int8 ? 1 : 0;
+    a.out_shift = g.out_shift;
     a.bias = g.bias ? bias : nullptr;
     a.ys_n = g.ys[0]; a.ys_k = g.ys[1]; a.ys_p = g.ys[2]; a.ys_q = g.ys[3];
     a.H = (int32_t)g.H; a.W = (int32_t)g.W; a.P = (int32_t)g.P; a.Q = (int32_t)g.Q;
@@ -954,7 +986,7 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
     a.n_tiles = (int32_t)pl.n_tiles;
     a.num_tiles = (int32_t)(pl.m_tiles * pl.n_tiles);
     a.relu = g.relu ? 1 : 0;
-    a.y_vec = (g.ys[1] == 1 && (g.K % 4) == 0 && ((uintptr_t)y % 16) == 0 && (g.ys[0] % 4) == 0 &&
+    a.y_vec = (!g.out_int8 && g.ys[1] == 1 && (g.K % 4) == 0 && ((uintptr_t)y % 16) == 0 && (g.ys[0] % 4) == 0 &&
                (g.ys[2] % 4) == 0 && (g.ys[3] % 4) == 0)
                   ? 1
                   : 0;

@@ -20,7 +20,21 @@ struct ConvGeom {
     int64_t dil_h, dil_w;
     int32_t mode;              // 0 cross-correlation, 1 convolution
     bool bias, relu;
+    bool out_int8;             // int8 output: rounding right shift then saturation
+    int32_t out_shift;
 };
+
+#ifdef __CUDACC__
+// int8 output of CONV_EPILOGUE_INT8_OUT: floor((v + 2^(shift-1)) / 2^shift)
+// (shift > 0; the arithmetic right shift of a signed value floors), then
+// clamped to [-128, 127].
+__device__ __forceinline__ int8_t requant_i8(int32_t v, int32_t shift) {
+    int64_t t = v;
+    if (shift > 0) t = (t + ((int64_t)1 << (shift - 1))) >> shift;
+    t = t > 127 ? 127 : (t < -128 ? -128 : t);
+    return (int8_t)t;
+}
+#endif
 
 // Fill g from validated descriptors.
 void make_geom(const conv_tensor_desc *x, const conv_tensor_desc *w, const conv_tensor_desc *y,
@@ -57,14 +71,14 @@ conv_status igemm_pack_filter_launch(const ConvGeom &g, const IgemmPlan &pl, con
                                      void *stream);
 // Runs the convolution from a workspace whose filter part is already packed
 // (copies the image to channels-last first when pl.pack_x).
-conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, int32_t *y,
+conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *y,
                               const int32_t *bias, void *workspace, void *stream);
 
 // ---------------------------------------------------------------- direct
 bool dp4a_supported(const ConvGeom &g);
-conv_status dp4a_launch(const ConvGeom &g, const int8_t *x, const int8_t *w, int32_t *y,
+conv_status dp4a_launch(const ConvGeom &g, const int8_t *x, const int8_t *w, void *y,
                         const int32_t *bias, void *stream);
-conv_status generic_launch(const ConvGeom &g, const int8_t *x, const int8_t *w, int32_t *y,
+conv_status generic_launch(const ConvGeom &g, const int8_t *x, const int8_t *w, void *y,
                            const int32_t *bias, void *stream);
 
 // Workspace bytes a call needs given the actual image pointer (a misaligned

@@ -46,7 +46,7 @@ using namespace i8c;
 
 extern "C" conv_status conv_fprop_static_workspace(const conv_tensor_desc *x, const int8_t *x_dev,
                                                    const conv_tensor_desc *w, const int8_t *w_dev,
-                                                   const conv_tensor_desc *y, int32_t *y_dev,
+                                                   const conv_tensor_desc *y, void *y_dev,
                                                    const int32_t *bias_dev, const conv_fprop_params *p,
                                                    void *stream) {
     size_t need = 0;

@@ -199,6 +199,125 @@ int oracle_conv_fprop_points(const int8_t *x, const int64_t *xd, const int64_t *
     return bad ? ORACLE_ACC_OUT_OF_INT32 : ORACLE_OK;
 }
 
+/*
+ * Data gradient (cuDNN "Convolutions", section "Convolution Dgrad": the
+ * gradient with respect to the image during backpropagation, from the loss
+ * gradient dY -- the "loss" argument, logical [N,K,P,Q] -- and the filter).
+ * The fprop above is linear in X, so the data gradient is its transpose
+ * applied to dY: every fprop term X[n,c,h,w] * W[k,c,r',s'] that fed
+ * Y[n,k,p,q] sends dY[n,k,p,q] * W[k,c,r',s'] back to position (h, w):
+ *
+ *   dX[n,c,h,w] = sum over k < K, r < R, s < S of dY[n,k,p,q] * W[k,c,r',s']
+ *     where p = (h + pre_h - r*dil_h) / stride_h and q likewise, counted only
+ *     when the division is exact and 0 <= p < P, 0 <= q < Q;
+ *     (r', s') as in fprop (flipped in CONVOLUTION mode).
+ *
+ * The image size H x W is that of dX's descriptor (with a stride above 1
+ * several H give the same P); dY's P, Q must be the fprop output size of it.
+ * No bias, ReLU or int8 output: the result is the int32 gradient.  The
+ * accumulator is int64 and one outside int32 is reported, as in fprop.
+ */
+static int check_grad_args(const int64_t *xd, const int64_t *wd, const int64_t *yd,
+                           const oracle_params *pp) {
+    if (pp->relu) return ORACLE_BAD_ARGS;
+    return check_args(xd, wd, yd, pp);
+}
+
+int oracle_conv_dgrad(const int8_t *dy, const int64_t *yd, const int64_t *ys,
+                      const int8_t *w, const int64_t *wd, const int64_t *ws,
+                      int32_t *dx, const int64_t *xd, const int64_t *xs,
+                      const oracle_params *pp) {
+    int rc = check_grad_args(xd, wd, yd, pp);
+    if (rc) return rc;
+    const int64_t N = xd[0], C = xd[1], H = xd[2], W = xd[3];
+    const int64_t K = wd[0], R = wd[2], S = wd[3], P = yd[2], Q = yd[3];
+    int bad = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic) reduction(| : bad)
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t c = 0; c < C; ++c) {
+            for (int64_t h = 0; h < H; ++h) {
+                for (int64_t ww = 0; ww < W; ++ww) {
+                    int64_t acc = 0;
+                    for (int64_t k = 0; k < K; ++k) {
+                        for (int64_t r = 0; r < R; ++r) {
+                            int64_t th = h + pp->pre[0] - r * pp->dil[0];
+                            if (th < 0 || th % pp->stride[0]) continue;
+                            int64_t p = th / pp->stride[0];
+                            if (p >= P) continue;
+                            for (int64_t s = 0; s < S; ++s) {
+                                int64_t tw = ww + pp->pre[1] - s * pp->dil[1];
+                                if (tw < 0 || tw % pp->stride[1]) continue;
+                                int64_t q = tw / pp->stride[1];
+                                if (q >= Q) continue;
+                                int64_t rf = pp->mode ? (R - 1 - r) : r;
+                                int64_t sf = pp->mode ? (S - 1 - s) : s;
+                                int64_t gv = dy[n * ys[0] + k * ys[1] + p * ys[2] + q * ys[3]];
+                                int64_t wv = w[k * ws[0] + c * ws[1] + rf * ws[2] + sf * ws[3]];
+                                acc += gv * wv;
+                            }
+                        }
+                    }
+                    if (acc > INT32_MAX || acc < INT32_MIN) bad = 1;
+                    dx[n * xs[0] + c * xs[1] + h * xs[2] + ww * xs[3]] = (int32_t)acc;
+                }
+            }
+        }
+    }
+    return bad ? ORACLE_ACC_OUT_OF_INT32 : ORACLE_OK;
+}
+
+/*
+ * Weight gradient (cuDNN "Convolutions", section "Convolution Wgrad": the
+ * gradient with respect to the filter, from the image and the loss gradient
+ * dY).  fprop is linear in W, and W[k,c,r',s'] multiplies X[n,c,h,w] in the
+ * term feeding Y[n,k,p,q], so:
+ *
+ *   dW[k,c,r',s'] = sum over n < N, p < P, q < Q of dY[n,k,p,q] * X[n,c,h,w]
+ *     h = p*stride_h - pre_h + r*dil_h, w = q*stride_w - pre_w + s*dil_w,
+ *     zero outside the image; (r', s') = (r, s), or (R-1-r, S-1-s) in
+ *     CONVOLUTION mode.
+ *
+ * R x S is that of dW's descriptor.  int64 accumulator, int32 result.
+ */
+int oracle_conv_wgrad(const int8_t *x, const int64_t *xd, const int64_t *xs,
+                      const int8_t *dy, const int64_t *yd, const int64_t *ys,
+                      int32_t *dw, const int64_t *wd, const int64_t *ws,
+                      const oracle_params *pp) {
+    int rc = check_grad_args(xd, wd, yd, pp);
+    if (rc) return rc;
+    const int64_t N = xd[0], C = xd[1], H = xd[2], W = xd[3];
+    const int64_t K = wd[0], R = wd[2], S = wd[3], P = yd[2], Q = yd[3];
+    int bad = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic) reduction(| : bad)
+    for (int64_t k = 0; k < K; ++k) {
+        for (int64_t c = 0; c < C; ++c) {
+            for (int64_t r = 0; r < R; ++r) {
+                for (int64_t s = 0; s < S; ++s) {
+                    int64_t acc = 0;
+                    for (int64_t n = 0; n < N; ++n) {
+                        for (int64_t p = 0; p < P; ++p) {
+                            int64_t h = p * pp->stride[0] - pp->pre[0] + r * pp->dil[0];
+                            if (h < 0 || h >= H) continue;
+                            for (int64_t q = 0; q < Q; ++q) {
+                                int64_t ww = q * pp->stride[1] - pp->pre[1] + s * pp->dil[1];
+                                if (ww < 0 || ww >= W) continue;
+                                int64_t gv = dy[n * ys[0] + k * ys[1] + p * ys[2] + q * ys[3]];
+                                int64_t xv = x[n * xs[0] + c * xs[1] + h * xs[2] + ww * xs[3]];
+                                acc += gv * xv;
+                            }
+                        }
+                    }
+                    int64_t rf = pp->mode ? (R - 1 - r) : r;
+                    int64_t sf = pp->mode ? (S - 1 - s) : s;
+                    if (acc > INT32_MAX || acc < INT32_MIN) bad = 1;
+                    dw[k * ws[0] + c * ws[1] + rf * ws[2] + sf * ws[3]] = (int32_t)acc;
+                }
+            }
+        }
+    }
+    return bad ? ORACLE_ACC_OUT_OF_INT32 : ORACLE_OK;
+}
+
 /* Number of threads the OpenMP runtime would use (1 without OpenMP). */
 #ifdef _OPENMP
 #include <omp.h>

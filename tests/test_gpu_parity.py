@@ -31,7 +31,8 @@ def _to_dev(flat, dims, strides):
     return torch.as_strided(torch.from_numpy(np.ascontiguousarray(flat)).cuda(), tuple(dims), tuple(strides))
 
 
-def _run_both(ic, cfg, algo=0, x=None, w=None, b=None, x_pad=0, w_pad=0, y_layout=None, points=None):
+def _run_both(ic, cfg, algo=0, x=None, w=None, b=None, x_pad=0, w_pad=0, y_layout=None, points=None,
+              out_shift=None):
     if x is None:
         x, w, b = synth.make_inputs(cfg)
     xf, xs = synth.place(x, cfg.x_layout, pad_elems=x_pad)
@@ -43,16 +44,21 @@ def _run_both(ic, cfg, algo=0, x=None, w=None, b=None, x_pad=0, w_pad=0, y_layou
     # canaries around the output: 64 guard words on each side
     P, Q = cfg.P, cfg.Q
     ysz = cfg.N * cfg.K * P * Q
-    guard = torch.full((ysz + 128,), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
+    fill = 0x5A5A5A5A if out_shift is None else 0x5A
+    guard = torch.full((ysz + 128,), fill, dtype=torch.int32 if out_shift is None else torch.int8, device="cuda")
     ystr = synth.packed_strides(cfg.y_dims, yl)
     yt = torch.as_strided(guard[64:64 + ysz], cfg.y_dims, ystr)
     y = ic.conv_fprop(xt, wt, bt, pre_padding=cfg.pre, post_padding=cfg.post, stride=cfg.stride,
-                      dilation=cfg.dilation, mode=cfg.mode, relu=cfg.relu, algo=algo, out=yt)
+                      dilation=cfg.dilation, mode=cfg.mode, relu=cfg.relu, algo=algo, out=yt, out_shift=out_shift)
     torch.cuda.synchronize()
     assert ic.device_status() == 0
     g = guard.cpu().numpy()
-    assert np.all(g[:64] == 0x5A5A5A5A) and np.all(g[64 + ysz:] == 0x5A5A5A5A), "write outside the output"
+    assert np.all(g[:64] == fill) and np.all(g[64 + ysz:] == fill), "write outside the output"
     got = y.cpu().numpy()
+    if out_shift is not None:
+        ref = oracle.conv_fprop(xf, cfg.x_dims, xs, wf, cfg.w_dims, ws, cfg.pre, cfg.post, cfg.stride,
+                                cfg.dilation, cfg.mode, b, cfg.relu, out_int8=True, out_shift=out_shift)
+        return got, ref
     if points is not None:
         pts = points(cfg)
         ref = oracle.conv_fprop_points(xf, cfg.x_dims, xs, wf, cfg.w_dims, ws, pts, cfg.pre, cfg.post,
@@ -131,6 +137,41 @@ def test_algorithms_agree_with_oracle(ic, case, algo):
         pytest.skip("dp4a takes C*R*S <= 1024")
     got, ref = _run_both(ic, case, algo=algo)
     _assert_equal(got, ref, f"{case.name} algo {algo}")
+
+
+def _int8_out_cases():
+    C = synth.ConvConfig
+    return [
+        # NHWC, K % 16 == 0: the tensor-core path writes through TMA tensor stores
+        C("nhwc_k64", 3, 64, 13, 11, 64, 3, 3, pre=(1, 1), post=(1, 1), bias=True, seed=41),
+        # ragged K (not a multiple of 16): plain byte stores
+        C("nhwc_ragged_k", 2, 80, 9, 9, 200, 3, 2, stride=(2, 1), pre=(1, 0), post=(0, 1), relu=True, seed=42),
+        C("nchw_conv_mode", 2, 32, 11, 12, 20, 4, 2, stride=(1, 2), dilation=(2, 1), pre=(3, 0), post=(2, 1),
+          mode=1, bias=True, relu=True, x_layout="NCHW", w_layout="KCRS", y_layout="NCHW", seed=43),
+        C("one_by_one_k256", 2, 128, 15, 15, 256, 1, 1, stride=(2, 2), bias=True, seed=44),
+    ]
+
+
+@pytest.mark.parametrize("shift", [0, 7, 12])
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("case", _int8_out_cases(), ids=lambda c: c.name)
+def test_int8_output_matches_oracle(ic, case, algo, shift):
+    """int8 output (rounding right shift, then saturation) on every algorithm;
+    shift 0 saturates almost every output, 12 leaves most in range."""
+    if algo == 2 and case.C * case.R * case.S > 1024:
+        pytest.skip("dp4a takes C*R*S <= 1024")
+    got, ref = _run_both(ic, case, algo=algo, out_shift=shift)
+    assert got.dtype == np.int8
+    _assert_equal(got, ref, f"{case.name} algo {algo} shift {shift}")
+
+
+def test_int8_output_large_workload_reduced_batch(ic):
+    import dataclasses
+    cfg = dataclasses.replace(synth.CONFIGS["c3_3x3_large"], N=2)
+    got, ref = _run_both(ic, cfg, out_shift=12)
+    _assert_equal(got, ref, "c3 N=2 int8 out")
+    # a shift that leaves most values inside the int8 range exercises the rounding
+    assert np.mean(np.abs(ref.astype(np.int32)) < 127) > 0.5
 
 
 @pytest.mark.parametrize("algo", ALGOS)
@@ -212,6 +253,38 @@ def test_host_buffer_pipeline(ic, name, batch, pinned):
     ref = oracle.conv_fprop(xf, cfg.x_dims, xs, wf, cfg.w_dims, ws, cfg.pre, cfg.post, cfg.stride,
                             cfg.dilation, cfg.mode, b, cfg.relu)
     _assert_equal(got, ref, f"host pipeline {name}")
+
+
+def test_host_buffer_pipeline_int8_output(ic):
+    """conv_fprop_host with int8 output: chunk sizes and copies by the 1-byte
+    element (5 images of the 3x3 workload at full spatial size)."""
+    import dataclasses
+    cfg = dataclasses.replace(synth.CONFIGS["c3_3x3_large"], N=5)
+    x, w, b = synth.make_inputs(cfg)
+    xf, xs = synth.place(x, cfg.x_layout)
+    wf, ws = synth.place(w, cfg.w_layout)
+    ystr = synth.packed_strides(cfg.y_dims, cfg.y_layout)
+    ysz = int(np.prod(cfg.y_dims))
+    xh, wh = torch.from_numpy(xf).pin_memory(), torch.from_numpy(wf).pin_memory()
+    yh = torch.full((ysz + 64,), 0x5A, dtype=torch.int8).pin_memory()
+    xd = ic.TensorDesc.make(ic.CONV_INT8, cfg.x_dims, xs, xf.size)
+    wd = ic.TensorDesc.make(ic.CONV_INT8, cfg.w_dims, ws, wf.size)
+    yd = ic.TensorDesc.make(ic.CONV_INT8, cfg.y_dims, ystr, ysz)
+    p = ic.Params.make(cfg.pre, cfg.post, cfg.stride, cfg.dilation, cfg.mode, cfg.bias, cfg.relu, out_shift=9)
+    need = ic.host_buffer_size(xd, wd, yd, p)
+    buf = torch.empty(need, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream()
+    st = ic.conv_fprop_host_raw(xd, xh.data_ptr(), wd, wh.data_ptr(), yd, yh.data_ptr(), 0, p, buf.data_ptr(),
+                                need, s.cuda_stream)
+    assert st == 0, ic.STATUS.get(st)
+    s.synchronize()
+    assert ic.device_status() == 0
+    yn = yh.numpy()
+    assert np.all(yn[ysz:] == 0x5A), "write past the output"
+    got = synth.gather_logical(yn[:ysz], cfg.y_dims, ystr)
+    ref = oracle.conv_fprop(xf, cfg.x_dims, xs, wf, cfg.w_dims, ws, cfg.pre, cfg.post, cfg.stride,
+                            cfg.dilation, cfg.mode, b, cfg.relu, out_int8=True, out_shift=9)
+    _assert_equal(got, ref, "host pipeline int8 output")
 
 
 # ------------------------------------------------------------------ edge cases and status

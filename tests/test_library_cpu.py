@@ -234,6 +234,48 @@ def test_host_buffer_size_covers_chunks(ic):
     assert need < cfg.K * cfg.C * 9 + ws + 2 * x_chunk + 2 * y_chunk + 8 * 256
 
 
+def test_int8_output_validation(ic):
+    """INT8 output is an epilogue option: the output descriptor must be INT8
+    exactly when CONV_EPILOGUE_INT8_OUT is set, with 0 <= out_shift <= 31;
+    out_shift without the flag and a nonzero reserved word are refused."""
+    cfg = synth.CONFIGS["c2_s2_nhwc"]
+    xd, wd, yd32, p32 = _descs(ic, cfg)
+    yd8 = ic.TensorDesc.packed(ic.CONV_INT8, cfg.y_dims, cfg.y_layout)
+    assert yd8.capacity_bytes * 4 == yd32.capacity_bytes
+    for s in (0, 1, 7, 31):
+        p = ic.Params.make(cfg.pre, cfg.post, cfg.stride, out_shift=s)
+        assert p.epilogue & ic.EPILOGUE_INT8_OUT
+        assert ic.validate(xd, wd, yd8, p) == 0
+        # the flag with an int32 output descriptor, and int8 without the flag
+        assert ic.validate(xd, wd, yd32, p) == _code(ic, "CONV_ERR_DTYPE")
+    assert ic.validate(xd, wd, yd8, ic.Params.make(cfg.pre, cfg.post, cfg.stride)) == _code(ic, "CONV_ERR_DTYPE")
+    for s in (-1, 32, 1000):
+        p = ic.Params.make(cfg.pre, cfg.post, cfg.stride, out_shift=s)
+        assert ic.validate(xd, wd, yd8, p) == _code(ic, "CONV_ERR_BAD_PARAM")
+    p = ic.Params.make(cfg.pre, cfg.post, cfg.stride)
+    p.out_shift = 3
+    assert ic.validate(xd, wd, yd32, p) == _code(ic, "CONV_ERR_BAD_PARAM")
+    p = ic.Params.make(cfg.pre, cfg.post, cfg.stride, out_shift=3)
+    p.reserved = 1
+    assert ic.validate(xd, wd, yd8, p) == _code(ic, "CONV_ERR_BAD_PARAM")
+    p = ic.Params.make(cfg.pre, cfg.post, cfg.stride, out_shift=3)
+    small = ic.TensorDesc.make(ic.CONV_INT8, yd8.dims_t, yd8.strides_t, yd8.capacity_bytes - 1)
+    assert ic.validate(xd, wd, small, p) == _code(ic, "CONV_ERR_BUFFER_TOO_SMALL")
+    # the host pipeline sizes its output chunks by the output element size
+    c3 = synth.CONFIGS["c3_3x3_large"]
+    x3, w3, y3, p3 = _descs(ic, c3)
+    y3_8 = ic.TensorDesc.packed(ic.CONV_INT8, c3.y_dims, c3.y_layout)
+    p3_8 = ic.Params.make(c3.pre, c3.post, c3.stride, out_shift=8)
+    need8 = ic.host_buffer_size(x3, w3, y3_8, p3_8)
+    assert need8 < ic.host_buffer_size(x3, w3, y3, p3)
+    # 25.7 MB of int8 output: three chunks of at least 8 MB, 11 images each
+    per = 11
+    x_chunk = per * c3.C * c3.H * c3.W
+    y_chunk = per * c3.K * c3.P * c3.Q
+    base = c3.K * c3.C * 9 + ic.workspace_size(x3, w3, y3_8, p3_8) + 2 * x_chunk + 2 * y_chunk
+    assert base <= need8 < base + 8 * 256
+
+
 def test_dp4a_refuses_long_reductions(ic):
     cfg = synth.CONFIGS["c3_3x3_large"]
     xd, wd, yd, p = _descs(ic, cfg)
