@@ -1,4 +1,5 @@
-"""CPU oracle for INT8 conv2d forward propagation with int32 results.
+"""CPU oracle for INT8 conv2d forward propagation with int32 results, and for
+the data and weight gradients of the same convolution.
 
 TEST INFRASTRUCTURE ONLY.  The product path (the CUDA library and its Python
 binding) never imports this package; only ``tests/``, the package smoke check
@@ -15,6 +16,12 @@ Contents
 * ``saturate_int8`` / ``pack_int8_words``: the int8-output reading of the
   forum thread "INT8 convolution using cuDNN Python Frontend" (its printed
   cuDNN words are the int32 truth clamped to int8, four bytes to a word).
+* ``conv_fprop(..., out_int8=True, out_shift=s)``: the int8 output (rounding
+  right shift, then saturation).
+* ``conv_dgrad`` / ``conv_wgrad``: the data and weight gradients ("Convolutions",
+  sections "Convolution Dgrad" and "Convolution Wgrad"), written in C as the
+  transposes of the forward sum; ``grads_pyint`` derives both over Python
+  integers by the chain rule applied term by term to the forward definition.
 * ``worst_case_abs``: the accumulator bound |acc| <= C*R*S*2^14.
 
 Parity status: every function here is pinned by tests in
@@ -75,6 +82,11 @@ def _bind(path: str):
     lib.oracle_conv_fprop_i8.argtypes = [ctypes.c_void_p, i64p, i64p, ctypes.c_void_p, i64p, i64p,
                                          ctypes.c_void_p, i64p, i64p, ctypes.c_void_p,
                                          ctypes.POINTER(_Params), ctypes.c_int32]
+    for name in ("oracle_conv_dgrad", "oracle_conv_wgrad"):
+        f = getattr(lib, name)
+        f.restype = ctypes.c_int
+        f.argtypes = [ctypes.c_void_p, i64p, i64p, ctypes.c_void_p, i64p, i64p, ctypes.c_void_p, i64p, i64p,
+                      ctypes.POINTER(_Params)]
     lib.oracle_out_extent.restype = ctypes.c_int64
     lib.oracle_out_extent.argtypes = [ctypes.c_int64] * 6
     lib.oracle_num_threads.restype = ctypes.c_int
@@ -212,6 +224,76 @@ def conv_fprop_pyint(x, w, pre=(0, 0), post=(0, 0), stride=(1, 1), dilation=(1, 
                         acc = max(acc, 0)
                     y[n][k][p][q] = acc
     return np.array(y, dtype=np.int64).reshape(N, K, P, Q)
+
+
+def _packed(dims):
+    return (dims[1] * dims[2] * dims[3], dims[2] * dims[3], dims[3], 1)
+
+
+def conv_dgrad(dy_flat, dy_dims, dy_strides, w_flat, w_dims, w_strides, x_dims,
+               pre=(0, 0), post=(0, 0), stride=(1, 1), dilation=(1, 1), mode: int = 0) -> np.ndarray:
+    """Data gradient dX (logical [N,C,H,W] int32, packed NCHW) of the image of
+    size ``x_dims`` from the loss gradient dY [N,K,P,Q] and the filter."""
+    lib = _load()
+    dy_flat = np.ascontiguousarray(dy_flat, dtype=np.int8)
+    w_flat = np.ascontiguousarray(w_flat, dtype=np.int8)
+    xs = _packed(x_dims)
+    dx = np.zeros(max(int(np.prod(x_dims)), 1), dtype=np.int32)
+    p = _params(pre, post, stride, dilation, mode, False)
+    rc = lib.oracle_conv_dgrad(dy_flat.ctypes.data, _i64(dy_dims), _i64(dy_strides), w_flat.ctypes.data,
+                               _i64(w_dims), _i64(w_strides), dx.ctypes.data, _i64(x_dims), _i64(xs),
+                               ctypes.byref(p))
+    if rc == 2:
+        raise OverflowError("accumulator outside int32")
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (rc={rc})")
+    return dx[: int(np.prod(x_dims))].reshape(x_dims)
+
+
+def conv_wgrad(x_flat, x_dims, x_strides, dy_flat, dy_dims, dy_strides, w_dims,
+               pre=(0, 0), post=(0, 0), stride=(1, 1), dilation=(1, 1), mode: int = 0) -> np.ndarray:
+    """Weight gradient dW (logical [K,C,R,S] int32, packed KCRS) of a filter of
+    size ``w_dims`` from the image and the loss gradient dY [N,K,P,Q]."""
+    lib = _load()
+    x_flat = np.ascontiguousarray(x_flat, dtype=np.int8)
+    dy_flat = np.ascontiguousarray(dy_flat, dtype=np.int8)
+    ws = _packed(w_dims)
+    dw = np.zeros(max(int(np.prod(w_dims)), 1), dtype=np.int32)
+    p = _params(pre, post, stride, dilation, mode, False)
+    rc = lib.oracle_conv_wgrad(x_flat.ctypes.data, _i64(x_dims), _i64(x_strides), dy_flat.ctypes.data,
+                               _i64(dy_dims), _i64(dy_strides), dw.ctypes.data, _i64(w_dims), _i64(ws),
+                               ctypes.byref(p))
+    if rc == 2:
+        raise OverflowError("accumulator outside int32")
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (rc={rc})")
+    return dw[: int(np.prod(w_dims))].reshape(w_dims)
+
+
+def grads_pyint(x, w, dy, pre=(0, 0), post=(0, 0), stride=(1, 1), dilation=(1, 1), mode=0):
+    """dX and dW over Python integers (tiny cases only), by walking every term
+    X[n,c,h,w] * W[k,c,r',s'] of the forward sum and sending dY[n,k,p,q] back
+    along it: the chain rule applied to the definition term by term."""
+    N, C, H, W = x.shape
+    K, _, R, S = w.shape
+    _, _, P, Q = out_dims(x.shape, w.shape, pre, post, stride, dilation)
+    dx = [[[[0] * W for _ in range(H)] for _ in range(C)] for _ in range(N)]
+    dw = [[[[0] * S for _ in range(R)] for _ in range(C)] for _ in range(K)]
+    for n in range(N):
+        for k in range(K):
+            for p in range(P):
+                for q in range(Q):
+                    g = int(dy[n, k, p, q])
+                    for c in range(C):
+                        for r in range(R):
+                            for s in range(S):
+                                h = p * stride[0] - pre[0] + r * dilation[0]
+                                ww = q * stride[1] - pre[1] + s * dilation[1]
+                                if 0 <= h < H and 0 <= ww < W:
+                                    rf, sf = (R - 1 - r, S - 1 - s) if mode else (r, s)
+                                    dx[n][c][h][ww] += g * int(w[k, c, rf, sf])
+                                    dw[k][c][rf][sf] += g * int(x[n, c, h, ww])
+    return np.array(dx, dtype=np.int64), np.array(dw, dtype=np.int64)
 
 
 def worst_case_abs(C: int, R: int, S: int, bias_abs: int = 0) -> int:

@@ -47,6 +47,12 @@
  * "Step 2") and what the forum thread's int8-typed output holds (its printed
  * words are the int32 truth clamped to int8); the shift is the plainest
  * integer reading of that post's "ReLU and quantization step" roadmap item.
+ *
+ * Gradients (oracle_conv_dgrad, oracle_conv_wgrad): the same page's sections
+ * "Convolution Dgrad" and "Convolution Wgrad" name the operations (data and
+ * weight gradient during backpropagation) and their arguments but print no
+ * formula; the reading taken is the plain one, the transpose of the forward
+ * sum with respect to the image and to the filter, written out below.
  */
 #include <stdint.h>
 #include <stddef.h>

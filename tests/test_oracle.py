@@ -407,6 +407,117 @@ def test_generator_is_layout_free_and_seeded():
 # --------------------------------------------------------------------------
 # Planted mistakes: each one must break at least one pin above
 # --------------------------------------------------------------------------
+# ------------------------------------------------------------------ data and weight gradients
+# Pins of oracle_conv_dgrad / oracle_conv_wgrad ("Convolutions", sections
+# "Convolution Dgrad" and "Convolution Wgrad": the gradients of a loss with
+# respect to the image and to the filter, given the loss gradient dY).
+
+
+def _grads(x, w, dy, pre=(0, 0), post=(0, 0), stride=(1, 1), dilation=(1, 1), mode=0, layouts=("NCHW", "KCRS")):
+    xf, xs = synth.place(x, layouts[0])
+    wf, ws = synth.place(w, layouts[1])
+    yf, ys = synth.place(dy, layouts[0])
+    kw = dict(pre=pre, post=post, stride=stride, dilation=dilation, mode=mode)
+    dx = oracle.conv_dgrad(yf, dy.shape, ys, wf, w.shape, ws, x.shape, **kw)
+    dw = oracle.conv_wgrad(xf, x.shape, xs, yf, dy.shape, ys, w.shape, **kw)
+    return dx, dw
+
+
+def _grad_case(c):
+    x = _rand(c["seed"], (c["N"], c["C"], c["H"], c["W"]))
+    w = _rand(c["seed"] + 1000, (c["K"], c["C"], c["R"], c["S"]))
+    kw = dict(pre=c["pre"], post=c["post"], stride=c["stride"], dilation=c["dilation"], mode=c["mode"])
+    yd = oracle.out_dims(x.shape, w.shape, c["pre"], c["post"], c["stride"], c["dilation"])
+    dy = _rand(c["seed"] + 2000, yd)
+    return x, w, dy, kw
+
+
+@pytest.mark.parametrize("case", _small_cases()[:20])
+def test_grads_are_the_adjoints_of_fprop(case):
+    """fprop is bilinear, so for every X, W, dY:
+    <fprop(X, W), dY> = <X, dgrad(dY, W)> = <W, wgrad(X, dY)>  (exact integers).
+    Ties both gradients to the pinned forward oracle."""
+    x, w, dy, kw = _grad_case(case)
+    y = _run(x, w, **kw).astype(np.int64)
+    dx, dw = _grads(x, w, dy, **kw)
+    lhs = int((y * dy.astype(np.int64)).sum())
+    assert lhs == int((x.astype(np.int64) * dx.astype(np.int64)).sum())
+    assert lhs == int((w.astype(np.int64) * dw.astype(np.int64)).sum())
+
+
+@pytest.mark.parametrize("case", _small_cases()[20:32])
+def test_grads_brute_force_chain_rule(case):
+    """Element by element against the chain rule applied term by term to the
+    forward definition (Python integers, scatter order)."""
+    x, w, dy, kw = _grad_case(case)
+    dx, dw = _grads(x, w, dy, **kw)
+    px, pw = oracle.grads_pyint(x, w, dy, **kw)
+    assert np.array_equal(dx, px)
+    assert np.array_equal(dw, pw)
+
+
+@pytest.mark.parametrize("case", _small_cases()[32:40])
+def test_grads_match_float64_autograd(case):
+    """Element by element against PyTorch autograd of a float64 conv2d (exact:
+    every value is an integer far below 2^53); convolution mode flips the
+    filter before the library's cross-correlation."""
+    x, w, dy, kw = _grad_case(case)
+    dx, dw = _grads(x, w, dy, **kw)
+    xt = torch.tensor(x, dtype=torch.float64, requires_grad=True)
+    wt = torch.tensor(w, dtype=torch.float64, requires_grad=True)
+    pre, post = kw["pre"], kw["post"]
+    xp = F.pad(xt, (pre[1], post[1], pre[0], post[0]))
+    weff = torch.flip(wt, [2, 3]) if kw["mode"] else wt
+    y = F.conv2d(xp, weff, stride=kw["stride"], dilation=kw["dilation"])
+    assert tuple(y.shape) == dy.shape
+    (y * torch.tensor(dy, dtype=torch.float64)).sum().backward()
+    assert np.array_equal(dx, xt.grad.numpy().astype(np.int64))
+    assert np.array_equal(dw, wt.grad.numpy().astype(np.int64))
+
+
+def test_grads_one_by_one_are_integer_gemms():
+    """1x1 filter, stride 1, no padding: dX[n,:,h,w] = W^T dY[n,:,h,w] and
+    dW = sum over pixels of dY x X^T (int64 matrix products)."""
+    x = _rand(60, (2, 5, 4, 3))
+    w = _rand(61, (6, 5, 1, 1))
+    dy = _rand(62, (2, 6, 4, 3))
+    dx, dw = _grads(x, w, dy, layouts=("NHWC", "KRSC"))
+    wm = w[:, :, 0, 0].astype(np.int64)                      # K x C
+    ym = dy.transpose(0, 2, 3, 1).reshape(-1, 6).astype(np.int64)  # pixels x K
+    xm = x.transpose(0, 2, 3, 1).reshape(-1, 5).astype(np.int64)   # pixels x C
+    assert np.array_equal(dx.transpose(0, 2, 3, 1).reshape(-1, 5), ym @ wm)
+    assert np.array_equal(dw[:, :, 0, 0], ym.T @ xm)
+
+
+def test_dgrad_stride_two_leaves_unreached_pixels_zero():
+    """Stride 2, 1x1 filter, no padding: only pixels on the stride grid feed the
+    output, so every other row and column of dX is zero and the grid holds
+    W^T dY."""
+    x = np.zeros((1, 2, 6, 6), dtype=np.int8)
+    w = _rand(63, (3, 2, 1, 1))
+    dy = _rand(64, (1, 3, 3, 3))
+    dx, _ = _grads(x, w, dy, stride=(2, 2))
+    assert np.all(dx[:, :, 1::2, :] == 0) and np.all(dx[:, :, :, 1::2] == 0)
+    ref = np.einsum("kc,nkpq->ncpq", w[:, :, 0, 0].astype(np.int64), dy.astype(np.int64))
+    assert np.array_equal(dx[:, :, ::2, ::2], ref)
+
+
+def test_wgrad_accumulator_bound():
+    """dW sums N*P*Q products of two int8 values: an all-(-128) image and loss
+    gradient over 131072 pixels reach 2^31 and are reported, one pixel fewer
+    fits int32."""
+    x = np.full((1, 1, 256, 512), -128, dtype=np.int8)
+    dy = np.full((1, 1, 256, 512), -128, dtype=np.int8)
+    with pytest.raises(OverflowError):
+        oracle.conv_wgrad(x.ravel(), x.shape, (131072, 131072, 512, 1), dy.ravel(), dy.shape,
+                          (131072, 131072, 512, 1), (1, 1, 1, 1))
+    x2 = x.copy()
+    x2[0, 0, 0, 0] = 0
+    dw = oracle.conv_wgrad(x2.ravel(), x.shape, (131072, 131072, 512, 1), dy.ravel(), dy.shape,
+                           (131072, 131072, 512, 1), (1, 1, 1, 1))
+    assert int(dw.ravel()[0]) == 131071 * 16384
+
+
 MUTATIONS = {
     "no_flip": ("int64_t rf = pp->mode ? (R - 1 - r) : r;", "int64_t rf = r;"),
     "pre_post_swapped": ("int64_t h = p * pp->stride[0] - pp->pre[0] + r * pp->dil[0];",
@@ -419,6 +530,14 @@ MUTATIONS = {
                          "if (pp->relu && v < 0) v = 0;\n    if (bias) v = (int32_t)((uint32_t)v + (uint32_t)bias[k]);"),
     "int8_no_saturation": ("    if (t > 127) t = 127;\n", ""),
     "int8_truncating_shift": ("        t += (int64_t)1 << (shift - 1);\n", ""),
+    "dgrad_floor_instead_of_exact_division": ("if (th < 0 || th % pp->stride[0]) continue;", "if (th < 0) continue;"),
+    "dgrad_filter_not_flipped": ("int64_t wv = w[k * ws[0] + c * ws[1] + rf * ws[2] + sf * ws[3]];\n                                acc += gv * wv;",
+                                 "int64_t wv = w[k * ws[0] + c * ws[1] + r * ws[2] + s * ws[3]];\n                                acc += gv * wv;"),
+    "dgrad_post_for_pre": ("int64_t tw = ww + pp->pre[1] - s * pp->dil[1];", "int64_t tw = ww + pp->post[1] - s * pp->dil[1];"),
+    "wgrad_output_not_flipped": ("dw[k * ws[0] + c * ws[1] + rf * ws[2] + sf * ws[3]] = (int32_t)acc;",
+                                 "dw[k * ws[0] + c * ws[1] + r * ws[2] + s * ws[3]] = (int32_t)acc;"),
+    "wgrad_loss_index_uses_image_channel": ("int64_t gv = dy[n * ys[0] + k * ys[1] + p * ys[2] + q * ys[3]];\n                                int64_t xv",
+                                            "int64_t gv = dy[n * ys[0] + (c % K) * ys[1] + p * ys[2] + q * ys[3]];\n                                int64_t xv"),
 }
 
 _PIN_FUNCS = None
@@ -436,6 +555,9 @@ def _pin_suite():
         test_flip_equivalence_between_modes,
         test_bias_then_relu,
         test_int8_output_rounding_and_saturation_closed_forms,
+        lambda: [test_grads_are_the_adjoints_of_fprop(c) for c in _small_cases()[:12]],
+        test_grads_one_by_one_are_integer_gemms,
+        test_dgrad_stride_two_leaves_unreached_pixels_zero,
     ]
     for f in funcs:
         try:
