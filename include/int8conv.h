@@ -269,6 +269,52 @@ conv_status conv_fprop_static_workspace(const conv_tensor_desc *x, const int8_t 
                                         const int32_t *bias_dev, const conv_fprop_params *p,
                                         void *stream);
 
+/*
+ * Gradients of the same convolution (cuDNN "Convolutions", sections
+ * "Convolution Dgrad" and "Convolution Wgrad": the data and weight gradients
+ * during backpropagation).  The pages name the operations and their
+ * arguments but print no formula; they are computed as the transposes of
+ * the forward sum:
+ *
+ *   dX[n,c,h,w]   = sum over k, r, s of dY[n,k,p,q] * W[k,c,r',s'],
+ *                   p = (h + pre_h - r*dil_h) / stride_h when that division
+ *                   is exact and 0 <= p < P (q likewise),
+ *   dW[k,c,r',s'] = sum over n, p, q of dY[n,k,p,q] * X[n,c,h,w],
+ *                   h = p*stride_h - pre_h + r*dil_h (w likewise), zero
+ *                   outside the image,
+ *
+ * with (r', s') = (r, s) in CROSS_CORRELATION and (R-1-r, S-1-s) in
+ * CONVOLUTION, exactly as conv_fprop pairs image and filter elements.
+ *
+ * Descriptors: dy is the loss gradient, int8 [N,K,P,Q]; w and x as in
+ * conv_fprop (int8); dx is int32 [N,C,H,W] and dw int32 [K,C,R,S], any
+ * strides.  H, W (dgrad) and R, S (wgrad) come from the output descriptor;
+ * P, Q must be the forward output size for them.  p is the forward call's
+ * parameters with no epilogue (epilogue and out_shift 0) and algo AUTO,
+ * IMPLICIT_GEMM or DIRECT_GENERIC.  Results are exact: dgrad needs
+ * K*R*S*2^14 <= 2^31-1 and wgrad N*P*Q*2^14 <= 2^31-1, else
+ * CONV_ERR_OVERFLOW_RISK.
+ *
+ * conv_dgrad with stride 1 and padding no wider than the filter's reach
+ * (pre, post <= dilation*(taps-1)) runs on the tensor cores as a forward
+ * convolution of dY and needs the workspace conv_dgrad_workspace_size
+ * reports (256-byte aligned, caller-owned); other calls run CUDA-core
+ * kernels and need none.  conv_wgrad runs a CUDA-core kernel (workspace 0;
+ * IMPLICIT_GEMM returns CONV_ERR_ALIGNMENT).  Pointers are device pointers on
+ * the current device, outputs must not overlap inputs or the workspace; the
+ * calls are asynchronous on `stream` and allocate nothing.
+ */
+conv_status conv_dgrad_workspace_size(const conv_tensor_desc *dy, const conv_tensor_desc *w,
+                                      const conv_tensor_desc *dx, const conv_fprop_params *p, size_t *bytes);
+conv_status conv_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const conv_tensor_desc *w,
+                       const int8_t *w_dev, const conv_tensor_desc *dx, int32_t *dx_dev,
+                       const conv_fprop_params *p, void *workspace, size_t workspace_bytes, void *stream);
+conv_status conv_wgrad_workspace_size(const conv_tensor_desc *x, const conv_tensor_desc *dy,
+                                      const conv_tensor_desc *dw, const conv_fprop_params *p, size_t *bytes);
+conv_status conv_wgrad(const conv_tensor_desc *x, const int8_t *x_dev, const conv_tensor_desc *dy,
+                       const int8_t *dy_dev, const conv_tensor_desc *dw, int32_t *dw_dev,
+                       const conv_fprop_params *p, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Synchronise `stream`, then read and clear the current device's status
  * word: CONV_OK, or CONV_ERR_DEVICE_TIMEOUT if a kernel gave up waiting
  * since the last call. */

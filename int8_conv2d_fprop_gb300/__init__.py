@@ -49,6 +49,7 @@ EXPORTED_SYMBOLS = (
     "conv_fprop", "conv_fprop_pack_filter", "conv_fprop_prepacked", "conv_fprop_static_workspace",
     "conv_fprop_host_buffer_size", "conv_fprop_host", "conv_device_status",
     "conv_selftest_wait_timeout", "conv_status_string", "conv_library_version",
+    "conv_dgrad_workspace_size", "conv_dgrad", "conv_wgrad_workspace_size", "conv_wgrad",
 )
 
 
@@ -160,6 +161,13 @@ def lib():
         L.conv_fprop_host_buffer_size.restype = ctypes.c_int
         L.conv_fprop_host.argtypes = list(L.conv_fprop.argtypes)
         L.conv_fprop_host.restype = ctypes.c_int
+        for name in ("conv_dgrad_workspace_size", "conv_wgrad_workspace_size"):
+            getattr(L, name).argtypes = [D, D, D, P, ctypes.POINTER(ctypes.c_size_t)]
+            getattr(L, name).restype = ctypes.c_int
+        for name in ("conv_dgrad", "conv_wgrad"):
+            getattr(L, name).argtypes = [D, ctypes.c_void_p, D, ctypes.c_void_p, D, ctypes.c_void_p, P,
+                                         ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+            getattr(L, name).restype = ctypes.c_int
         L.conv_device_status.argtypes = [ctypes.c_void_p]
         L.conv_selftest_wait_timeout.argtypes = [ctypes.c_uint32, ctypes.c_void_p]
         L.conv_status_string.argtypes = [ctypes.c_int]
@@ -326,4 +334,58 @@ def conv_fprop(x, w, bias=None, *, pre_padding=(0, 0), post_padding=(0, 0), padd
                         workspace.numel() * workspace.element_size() if ws_bytes else 0,
                         stream.cuda_stream)
     _check(st, "conv_fprop")
+    return out
+
+
+def dgrad_workspace_size(dyd: TensorDesc, wd: TensorDesc, dxd: TensorDesc, p: Params) -> int:
+    out = ctypes.c_size_t()
+    _check(lib().conv_dgrad_workspace_size(ctypes.byref(dyd), ctypes.byref(wd), ctypes.byref(dxd), ctypes.byref(p),
+                                           ctypes.byref(out)), "dgrad workspace size")
+    return int(out.value)
+
+
+def wgrad_workspace_size(xd: TensorDesc, dyd: TensorDesc, dwd: TensorDesc, p: Params) -> int:
+    out = ctypes.c_size_t()
+    _check(lib().conv_wgrad_workspace_size(ctypes.byref(xd), ctypes.byref(dyd), ctypes.byref(dwd), ctypes.byref(p),
+                                           ctypes.byref(out)), "wgrad workspace size")
+    return int(out.value)
+
+
+def _grad_params(pre_padding, post_padding, padding, stride, dilation, mode, algo):
+    return Params.make(pre_padding, post_padding, stride, dilation, mode, False, False, algo, padding)
+
+
+def conv_dgrad(dy, w, *, out, pre_padding=(0, 0), post_padding=(0, 0), padding=None, stride=(1, 1),
+               dilation=(1, 1), mode: int = CROSS_CORRELATION, algo: int = ALGO_AUTO, workspace=None, stream=None):
+    """Data gradient dX of conv_fprop: dy int8 CUDA tensor [N,K,P,Q] (the loss
+    gradient), w int8 [K,C,R,S], out int32 [N,C,H,W] (any strides; H, W are
+    the forward image size).  Parameters as for conv_fprop.  Returns ``out``."""
+    import torch
+    p = _grad_params(pre_padding, post_padding, padding, stride, dilation, mode, algo)
+    dyd, wd, dxd = TensorDesc.from_tensor(dy), TensorDesc.from_tensor(w), TensorDesc.from_tensor(out)
+    ws_bytes = dgrad_workspace_size(dyd, wd, dxd, p)
+    if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dy.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(dy.device)
+    st = lib().conv_dgrad(ctypes.byref(dyd), dy.data_ptr(), ctypes.byref(wd), w.data_ptr(), ctypes.byref(dxd),
+                          out.data_ptr(), ctypes.byref(p), workspace.data_ptr() if ws_bytes else None,
+                          ws_bytes if ws_bytes else 0, stream.cuda_stream or None)
+    _check(st, "conv_dgrad")
+    return out
+
+
+def conv_wgrad(x, dy, *, out, pre_padding=(0, 0), post_padding=(0, 0), padding=None, stride=(1, 1),
+               dilation=(1, 1), mode: int = CROSS_CORRELATION, algo: int = ALGO_AUTO, stream=None):
+    """Weight gradient dW of conv_fprop: x int8 CUDA tensor [N,C,H,W], dy int8
+    [N,K,P,Q] (the loss gradient), out int32 [K,C,R,S] (any strides; R, S are
+    the forward filter size).  Parameters as for conv_fprop.  Returns ``out``."""
+    import torch
+    p = _grad_params(pre_padding, post_padding, padding, stride, dilation, mode, algo)
+    xd, dyd, dwd = TensorDesc.from_tensor(x), TensorDesc.from_tensor(dy), TensorDesc.from_tensor(out)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    st = lib().conv_wgrad(ctypes.byref(xd), x.data_ptr(), ctypes.byref(dyd), dy.data_ptr(), ctypes.byref(dwd),
+                          out.data_ptr(), ctypes.byref(p), None, 0, stream.cuda_stream or None)
+    _check(st, "conv_wgrad")
     return out

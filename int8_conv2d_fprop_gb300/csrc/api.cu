@@ -73,13 +73,6 @@ uint64_t wait_limit_ns() {
 
 namespace {
 
-// [lo, hi) byte ranges of two buffers overlap?
-bool overlaps(const void *a, uint64_t a_bytes, const void *b, uint64_t b_bytes) {
-    if (!a || !b || a_bytes == 0 || b_bytes == 0) return false;
-    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
-    return a0 < b0 + b_bytes && b0 < a0 + a_bytes;
-}
-
 int choose_algo(const ConvGeom &g, int requested) {
     if (requested != CONV_ALGO_AUTO) return requested;
     if (g.C >= 16 && igemm_supported(g)) return CONV_ALGO_IMPLICIT_GEMM;

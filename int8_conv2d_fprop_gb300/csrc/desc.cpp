@@ -123,6 +123,70 @@ void make_geom(const conv_tensor_desc *x, const conv_tensor_desc *w, const conv_
     g->out_shift = p->out_shift;
 }
 
+// The gradients take the forward convolution's parameters without an
+// epilogue: no bias, ReLU or int8 output, and the algorithm AUTO, IMPLICIT_GEMM
+// or DIRECT_GENERIC.
+static conv_status check_grad_params(const conv_fprop_params *p) {
+    conv_status st = check_params(p);
+    if (st) return st;
+    if (p->epilogue != 0 || p->out_shift != 0) return CONV_ERR_BAD_PARAM;
+    if (p->algo != CONV_ALGO_AUTO && p->algo != CONV_ALGO_IMPLICIT_GEMM && p->algo != CONV_ALGO_DIRECT_GENERIC)
+        return CONV_ERR_BAD_PARAM;
+    return CONV_OK;
+}
+
+// Shapes of a gradient call: image [N,C,H,W], filter [K,C,R,S] and loss
+// gradient [N,K,P,Q] with P, Q the forward output size of H, W.  `terms` is
+// the largest number of products summed into one result.
+static conv_status check_grad_shapes(const conv_tensor_desc *img, const conv_tensor_desc *flt,
+                                     const conv_tensor_desc *dy, const conv_fprop_params *p, int64_t terms) {
+    if (img->dims[0] != dy->dims[0] || img->dims[1] != flt->dims[1] || flt->dims[0] != dy->dims[1])
+        return CONV_ERR_SHAPE_MISMATCH;
+    for (int i = 0; i < 2; ++i) {
+        const int64_t o = out_extent(img->dims[2 + i], p->pre_padding[i], p->post_padding[i], flt->dims[2 + i],
+                                     p->dilation[i], p->stride[i]);
+        if (o < 1) return CONV_ERR_BAD_PARAM;
+        if (dy->dims[2 + i] != o) return CONV_ERR_SHAPE_MISMATCH;
+    }
+    if (terms > (int64_t)(INT32_MAX / (128 * 128))) return CONV_ERR_OVERFLOW_RISK;
+    int64_t m;
+    if (!mul_ok(img->dims[0], img->dims[2], &m) || !mul_ok(m, img->dims[3], &m) || m > (int64_t)INT32_MAX - 256)
+        return CONV_ERR_TOO_LARGE;
+    if (!mul_ok(dy->dims[0], dy->dims[2], &m) || !mul_ok(m, dy->dims[3], &m) || m > (int64_t)INT32_MAX - 256)
+        return CONV_ERR_TOO_LARGE;
+    if (flt->dims[0] > (1 << 24) || flt->dims[1] > (1 << 24)) return CONV_ERR_TOO_LARGE;
+    return CONV_OK;
+}
+
+conv_status validate_dgrad(const conv_tensor_desc *dy, const conv_tensor_desc *w, const conv_tensor_desc *dx,
+                           const conv_fprop_params *p) {
+    if (!dy || !w || !dx || !p) return CONV_ERR_NULL_PTR;
+    conv_status st = check_grad_params(p);
+    if (st) return st;
+    const int64_t img_min[4] = {0, 1, 1, 1}, flt_min[4] = {1, 1, 1, 1}, dy_min[4] = {0, 1, 1, 1};
+    if ((st = check_desc(dy, CONV_INT8, dy_min)) || (st = check_desc(w, CONV_INT8, flt_min)) ||
+        (st = check_desc(dx, CONV_INT32, img_min)))
+        return st;
+    int64_t terms = 0;  // dX sums over k and the taps
+    if (!mul_ok(w->dims[0], w->dims[2], &terms) || !mul_ok(terms, w->dims[3], &terms)) return CONV_ERR_OVERFLOW_RISK;
+    return check_grad_shapes(dx, w, dy, p, terms);
+}
+
+conv_status validate_wgrad(const conv_tensor_desc *x, const conv_tensor_desc *dy, const conv_tensor_desc *dw,
+                           const conv_fprop_params *p) {
+    if (!x || !dy || !dw || !p) return CONV_ERR_NULL_PTR;
+    conv_status st = check_grad_params(p);
+    if (st) return st;
+    const int64_t img_min[4] = {0, 1, 1, 1}, flt_min[4] = {1, 1, 1, 1}, dy_min[4] = {0, 1, 1, 1};
+    if ((st = check_desc(x, CONV_INT8, img_min)) || (st = check_desc(dy, CONV_INT8, dy_min)) ||
+        (st = check_desc(dw, CONV_INT32, flt_min)))
+        return st;
+    int64_t terms = 0;  // dW sums over the batch and the output pixels
+    if (!mul_ok(dy->dims[0], dy->dims[2], &terms) || !mul_ok(terms, dy->dims[3], &terms))
+        return CONV_ERR_OVERFLOW_RISK;
+    return check_grad_shapes(x, dw, dy, p, terms);
+}
+
 }  // namespace i8c
 
 using namespace i8c;

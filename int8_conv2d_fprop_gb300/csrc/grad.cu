@@ -1,0 +1,263 @@
+// grad.cu -- data and weight gradients of the INT8 convolution (cuDNN
+// "Convolutions", sections "Convolution Dgrad" and "Convolution Wgrad"): the
+// transposes of the forward sum with respect to the image and to the filter.
+//
+// dgrad, dX[n,c,h,w] = sum over k, r, s of dY[n,k,p,q] * W[k,c,r',s'] with
+// p = (h + pre_h - r*dil_h) / stride_h exact and in range (q likewise):
+//  * stride 1, and padding no wider than the filter's reach (pre, post <=
+//    dil*(taps-1)): a forward convolution of dY by the filter with K and C
+//    exchanged, the taps reversed (the other convolution mode) and the
+//    padding dil*(taps-1) - pre before, dil*(taps-1) - post after.  It runs on
+//    the tensor-core kernel, with its filter repack and workspace.
+//  * otherwise: a CUDA-core kernel, one thread per dX element.
+// wgrad, dW[k,c,r',s'] = sum over n, p, q of dY[n,k,p,q] * X[n,c,h,w]: a
+// CUDA-core kernel, one warp per dW element, the lanes splitting the n, p, q
+// sum (int32 partial sums, exact by the validator's bound, added across the
+// warp with shuffles).
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace i8c {
+namespace {
+
+struct GradArgs {
+    const int8_t *a;  // dgrad: dY; wgrad: X
+    const int8_t *b;  // dgrad: W;  wgrad: dY
+    int32_t *out;     // dgrad: dX; wgrad: dW
+    int64_t N, C, H, W, K, R, S, P, Q;
+    int64_t xs[4], ws[4], ys[4];  // strides of the image (or dX), the filter (or dW), dY
+    int64_t pad_h, pad_w, str_h, str_w, dil_h, dil_w;
+    int32_t mode;
+};
+
+__global__ void __launch_bounds__(256) dgrad_direct_kernel(const GradArgs g) {
+    const int64_t total = g.N * g.C * g.H * g.W;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t w = i % g.W;
+        int64_t t = i / g.W;
+        const int64_t h = t % g.H;
+        t /= g.H;
+        const int64_t c = t % g.C;
+        const int64_t n = t / g.C;
+        int32_t acc = 0;
+        for (int64_t r = 0; r < g.R; ++r) {
+            const int64_t th = h + g.pad_h - r * g.dil_h;
+            if (th < 0 || th % g.str_h) continue;
+            const int64_t p = th / g.str_h;
+            if (p >= g.P) continue;
+            const int64_t rf = g.mode ? g.R - 1 - r : r;
+            for (int64_t s = 0; s < g.S; ++s) {
+                const int64_t tw = w + g.pad_w - s * g.dil_w;
+                if (tw < 0 || tw % g.str_w) continue;
+                const int64_t q = tw / g.str_w;
+                if (q >= g.Q) continue;
+                const int64_t sf = g.mode ? g.S - 1 - s : s;
+                const int8_t *dy = g.a + n * g.ys[0] + p * g.ys[2] + q * g.ys[3];
+                const int8_t *wk = g.b + c * g.ws[1] + rf * g.ws[2] + sf * g.ws[3];
+                for (int64_t k = 0; k < g.K; ++k)
+                    acc += (int32_t)__ldg(dy + k * g.ys[1]) * (int32_t)__ldg(wk + k * g.ws[0]);
+            }
+        }
+        g.out[n * g.xs[0] + c * g.xs[1] + h * g.xs[2] + w * g.xs[3]] = acc;
+    }
+}
+
+__global__ void __launch_bounds__(256) wgrad_direct_kernel(const GradArgs g) {
+    const int64_t total = g.K * g.C * g.R * g.S;
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t npq = g.N * g.P * g.Q;
+    for (int64_t e = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; e < total; e += warps) {
+        const int64_t sf = e % g.S;
+        int64_t t = e / g.S;
+        const int64_t rf = t % g.R;
+        t /= g.R;
+        const int64_t c = t % g.C;
+        const int64_t k = t / g.C;
+        // the spatial tap whose products land in filter element (rf, sf)
+        const int64_t r = g.mode ? g.R - 1 - rf : rf;
+        const int64_t s = g.mode ? g.S - 1 - sf : sf;
+        int32_t acc = 0;
+        for (int64_t i = lane; i < npq; i += 32) {
+            const int64_t q = i % g.Q;
+            const int64_t t2 = i / g.Q;
+            const int64_t p = t2 % g.P;
+            const int64_t n = t2 / g.P;
+            const int64_t h = p * g.str_h - g.pad_h + r * g.dil_h;
+            const int64_t w = q * g.str_w - g.pad_w + s * g.dil_w;
+            if (h < 0 || h >= g.H || w < 0 || w >= g.W) continue;
+            acc += (int32_t)__ldg(g.b + n * g.ys[0] + k * g.ys[1] + p * g.ys[2] + q * g.ys[3]) *
+                   (int32_t)__ldg(g.a + n * g.xs[0] + c * g.xs[1] + h * g.xs[2] + w * g.xs[3]);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) g.out[k * g.ws[0] + c * g.ws[1] + rf * g.ws[2] + sf * g.ws[3]] = acc;
+    }
+}
+
+// Strides of a descriptor with those of unit dims zeroed (never multiplied by
+// a non-zero index).
+void unit_strides(const conv_tensor_desc *d, int64_t out[4]) {
+    for (int i = 0; i < 4; ++i) out[i] = d->dims[i] > 1 ? d->strides[i] : 0;
+}
+
+GradArgs grad_args(const conv_tensor_desc *img, const conv_tensor_desc *flt, const conv_tensor_desc *dy,
+                   const conv_fprop_params *p) {
+    GradArgs g;
+    g.N = img->dims[0]; g.C = img->dims[1]; g.H = img->dims[2]; g.W = img->dims[3];
+    g.K = flt->dims[0]; g.R = flt->dims[2]; g.S = flt->dims[3];
+    g.P = dy->dims[2]; g.Q = dy->dims[3];
+    unit_strides(img, g.xs);
+    unit_strides(flt, g.ws);
+    unit_strides(dy, g.ys);
+    g.pad_h = p->pre_padding[0]; g.pad_w = p->pre_padding[1];
+    g.str_h = p->stride[0]; g.str_w = p->stride[1];
+    g.dil_h = p->dilation[0]; g.dil_w = p->dilation[1];
+    g.mode = p->mode;
+    return g;
+}
+
+int grid_for(int64_t items, int per_block) {
+    int64_t blocks = (items + per_block - 1) / per_block;
+    const int64_t cap = (int64_t)device_sm_count() * 16;
+    if (blocks > cap) blocks = cap;
+    return (int)(blocks < 1 ? 1 : blocks);
+}
+
+// dgrad as a forward convolution of dY (see the top of the file), when the
+// stride is 1 and the padding within the filter's reach; fills g and returns
+// true then.
+bool dgrad_as_fprop(const conv_tensor_desc *dy, const conv_tensor_desc *w, const conv_tensor_desc *dx,
+                    const conv_fprop_params *p, ConvGeom *g) {
+    if (p->stride[0] != 1 || p->stride[1] != 1) return false;
+    const int64_t reach_h = p->dilation[0] * (w->dims[2] - 1), reach_w = p->dilation[1] * (w->dims[3] - 1);
+    if (p->pre_padding[0] > reach_h || p->post_padding[0] > reach_h || p->pre_padding[1] > reach_w ||
+        p->post_padding[1] > reach_w)
+        return false;
+    g->N = dy->dims[0]; g->C = dy->dims[1]; g->H = dy->dims[2]; g->W = dy->dims[3];
+    g->K = dx->dims[1]; g->R = w->dims[2]; g->S = w->dims[3];
+    g->P = dx->dims[2]; g->Q = dx->dims[3];
+    unit_strides(dy, g->xs);
+    int64_t fs[4];
+    unit_strides(w, fs);
+    // the filter with its first two dims exchanged: [C][K][R][S]
+    g->ws[0] = w->dims[1] > 1 ? fs[1] : 0;
+    g->ws[1] = w->dims[0] > 1 ? fs[0] : 0;
+    g->ws[2] = fs[2];
+    g->ws[3] = fs[3];
+    unit_strides(dx, g->ys);
+    g->pad_h = reach_h - p->pre_padding[0];
+    g->pad_w = reach_w - p->pre_padding[1];
+    g->str_h = g->str_w = 1;
+    g->dil_h = p->dilation[0];
+    g->dil_w = p->dilation[1];
+    g->mode = p->mode ? 0 : 1;  // the taps run backwards
+    g->bias = g->relu = g->out_int8 = false;
+    g->out_shift = 0;
+    return igemm_supported(*g);
+}
+
+// Plans a dgrad call: *tensor and *pl describe the tensor-core route when it
+// is taken.
+conv_status plan_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const conv_tensor_desc *w,
+                       const conv_tensor_desc *dx, const conv_fprop_params *p, ConvGeom *g, bool *tensor,
+                       IgemmPlan *pl) {
+    conv_status st = validate_dgrad(dy, w, dx, p);
+    if (st) return st;
+    *tensor = p->algo != CONV_ALGO_DIRECT_GENERIC && dgrad_as_fprop(dy, w, dx, p, g);
+    if (p->algo == CONV_ALGO_IMPLICIT_GEMM && !*tensor) return CONV_ERR_ALIGNMENT;
+    if (*tensor) igemm_plan(*g, dy_dev, pl);
+    return CONV_OK;
+}
+
+}  // namespace
+}  // namespace i8c
+
+using namespace i8c;
+
+extern "C" {
+
+conv_status conv_dgrad_workspace_size(const conv_tensor_desc *dy, const conv_tensor_desc *w,
+                                      const conv_tensor_desc *dx, const conv_fprop_params *p, size_t *bytes) {
+    if (!bytes) return CONV_ERR_NULL_PTR;
+    ConvGeom g;
+    IgemmPlan pl;
+    bool tensor = false;
+    conv_status st = plan_dgrad(dy, nullptr, w, dx, p, &g, &tensor, &pl);
+    if (st) return st;
+    *bytes = (tensor && g.N > 0 && g.K > 0) ? pl.workspace_bytes : 0;
+    return CONV_OK;
+}
+
+conv_status conv_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const conv_tensor_desc *w,
+                       const int8_t *w_dev, const conv_tensor_desc *dx, int32_t *dx_dev,
+                       const conv_fprop_params *p, void *workspace, size_t workspace_bytes, void *stream) {
+    ConvGeom g;
+    IgemmPlan pl;
+    bool tensor = false;
+    conv_status st = plan_dgrad(dy, dy_dev, w, dx, p, &g, &tensor, &pl);
+    if (st) return st;
+    if (dx->dims[0] == 0) return CONV_OK;
+    if (!dy_dev || !w_dev || !dx_dev) return CONV_ERR_NULL_PTR;
+    const uint64_t dx_bytes = (uint64_t)desc_extent_elems(dx) * 4;
+    if (overlaps(dx_dev, dx_bytes, dy_dev, (uint64_t)desc_extent_elems(dy)) ||
+        overlaps(dx_dev, dx_bytes, w_dev, (uint64_t)desc_extent_elems(w)) ||
+        overlaps(dx_dev, dx_bytes, workspace, workspace_bytes))
+        return CONV_ERR_OVERLAP;
+    if ((st = check_device())) return st;
+    if (tensor) {
+        if (!workspace || workspace_bytes < pl.workspace_bytes || ((uintptr_t)workspace % 256) != 0)
+            return CONV_ERR_WORKSPACE;
+        if (overlaps(workspace, pl.workspace_bytes, dy_dev, (uint64_t)desc_extent_elems(dy)) ||
+            overlaps(workspace, pl.workspace_bytes, w_dev, (uint64_t)desc_extent_elems(w)))
+            return CONV_ERR_OVERLAP;
+        if ((st = igemm_pack_filter_launch(g, pl, w_dev, workspace, stream))) return st;
+        return igemm_main_launch(g, pl, dy_dev, dx_dev, nullptr, workspace, stream);
+    }
+    const GradArgs a = [&] {
+        GradArgs r = grad_args(dx, w, dy, p);
+        r.a = dy_dev;
+        r.b = w_dev;
+        r.out = dx_dev;
+        return r;
+    }();
+    dgrad_direct_kernel<<<grid_for(a.N * a.C * a.H * a.W, 256), 256, 0, (cudaStream_t)stream>>>(a);
+    return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}
+
+conv_status conv_wgrad_workspace_size(const conv_tensor_desc *x, const conv_tensor_desc *dy,
+                                      const conv_tensor_desc *dw, const conv_fprop_params *p, size_t *bytes) {
+    if (!bytes) return CONV_ERR_NULL_PTR;
+    conv_status st = validate_wgrad(x, dy, dw, p);
+    if (st) return st;
+    if (p->algo == CONV_ALGO_IMPLICIT_GEMM) return CONV_ERR_ALIGNMENT;
+    *bytes = 0;
+    return CONV_OK;
+}
+
+conv_status conv_wgrad(const conv_tensor_desc *x, const int8_t *x_dev, const conv_tensor_desc *dy,
+                       const int8_t *dy_dev, const conv_tensor_desc *dw, int32_t *dw_dev,
+                       const conv_fprop_params *p, void *workspace, size_t workspace_bytes, void *stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    conv_status st = validate_wgrad(x, dy, dw, p);
+    if (st) return st;
+    if (p->algo == CONV_ALGO_IMPLICIT_GEMM) return CONV_ERR_ALIGNMENT;
+    if (!x_dev || !dy_dev || !dw_dev) return CONV_ERR_NULL_PTR;
+    const uint64_t dw_bytes = (uint64_t)desc_extent_elems(dw) * 4;
+    if (overlaps(dw_dev, dw_bytes, x_dev, (uint64_t)desc_extent_elems(x)) ||
+        overlaps(dw_dev, dw_bytes, dy_dev, (uint64_t)desc_extent_elems(dy)))
+        return CONV_ERR_OVERLAP;
+    if ((st = check_device())) return st;
+    GradArgs a = grad_args(x, dw, dy, p);
+    a.a = x_dev;
+    a.b = dy_dev;
+    a.out = dw_dev;
+    // an empty batch gives an all-zero gradient
+    wgrad_direct_kernel<<<grid_for(a.K * a.C * a.R * a.S * 32, 256), 256, 0, (cudaStream_t)stream>>>(a);
+    return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}
+
+}  // extern "C"

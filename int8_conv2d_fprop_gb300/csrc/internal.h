@@ -40,6 +40,20 @@ __device__ __forceinline__ int8_t requant_i8(int32_t v, int32_t shift) {
 void make_geom(const conv_tensor_desc *x, const conv_tensor_desc *w, const conv_tensor_desc *y,
                const conv_fprop_params *p, ConvGeom *g);
 
+// Validation of the gradient calls (descriptors, shapes, parameters, the
+// int32 accumulator bound).
+conv_status validate_dgrad(const conv_tensor_desc *dy, const conv_tensor_desc *w, const conv_tensor_desc *dx,
+                           const conv_fprop_params *p);
+conv_status validate_wgrad(const conv_tensor_desc *x, const conv_tensor_desc *dy, const conv_tensor_desc *dw,
+                           const conv_fprop_params *p);
+
+// [lo, hi) byte ranges of two buffers overlap?
+inline bool overlaps(const void *a, uint64_t a_bytes, const void *b, uint64_t b_bytes) {
+    if (!a || !b || a_bytes == 0 || b_bytes == 0) return false;
+    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + b_bytes && b0 < a0 + a_bytes;
+}
+
 // Largest addressed element offset + 1 of a descriptor (0 if a dim is 0).
 int64_t desc_extent_elems(const conv_tensor_desc *d);
 

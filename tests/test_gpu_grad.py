@@ -1,0 +1,131 @@
+"""GPU parity of the gradients (conv_dgrad, conv_wgrad through the C ABI)
+against the CPU oracle, element by element (integer results: tolerance 0).
+Cases cover both dgrad routes (tensor cores for stride 1 and padding within
+the filter's reach; the CUDA-core kernel otherwise), both modes, strides,
+dilations, asymmetric padding, NHWC and NCHW layouts and a ragged tail."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def ic():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import int8_conv2d_fprop_gb300 as m
+    torch.cuda.set_device(0)
+    return m
+
+
+@dataclasses.dataclass
+class G:
+    name: str
+    N: int
+    C: int
+    H: int
+    W: int
+    K: int
+    R: int
+    S: int
+    pre: tuple = (0, 0)
+    post: tuple = (0, 0)
+    stride: tuple = (1, 1)
+    dil: tuple = (1, 1)
+    mode: int = 0
+    layout: str = "NHWC"
+    algo: int = 0
+    tensor: bool = False  # dgrad expected on the tensor-core route
+
+
+CASES = [
+    G("s1_3x3_pad1", 2, 64, 13, 11, 48, 3, 3, (1, 1), (1, 1), tensor=True),
+    G("s1_5x3_dil_asym_conv", 2, 32, 12, 9, 40, 5, 3, (2, 1), (3, 2), dil=(2, 1), mode=1, tensor=True),
+    G("s1_nchw_k200", 1, 24, 10, 10, 200, 3, 3, (0, 2), (2, 0), layout="NCHW", tensor=True),
+    G("s1_generic_forced", 2, 16, 9, 8, 20, 3, 3, (1, 1), (1, 1), algo=3),
+    G("s2_3x3", 2, 32, 15, 14, 24, 3, 3, (1, 1), (1, 0), stride=(2, 2)),
+    G("s21_dil_conv", 1, 8, 11, 12, 12, 3, 2, (2, 0), (0, 1), stride=(2, 1), dil=(1, 2), mode=1),
+    G("pad_wider_than_reach", 2, 16, 6, 7, 8, 1, 1, (1, 2), (1, 0)),
+    G("c3_shape_batch2", 2, 256, 56, 56, 256, 3, 3, (1, 1), (1, 1), tensor=True),
+]
+
+
+def _place(a, layout):
+    f, s = synth.place(a, layout)
+    return torch.as_strided(torch.from_numpy(np.ascontiguousarray(f)).cuda(), a.shape, s), f, s
+
+
+def _setup(c):
+    x = synth.int8_uniform(7000 + len(c.name), 1, (c.N, c.C, c.H, c.W))
+    w = synth.int8_uniform(7000 + len(c.name), 2, (c.K, c.C, c.R, c.S))
+    yd = oracle.out_dims(x.shape, w.shape, c.pre, c.post, c.stride, c.dil)
+    dy = synth.int8_uniform(7000 + len(c.name), 3, yd)
+    return x, w, dy
+
+
+def _out(shape, layout):
+    fmt = torch.channels_last if layout == "NHWC" else torch.contiguous_format
+    return torch.full(shape, -999, dtype=torch.int32, device="cuda").to(memory_format=fmt)
+
+
+@pytest.mark.parametrize("c", CASES, ids=lambda c: c.name)
+def test_dgrad_matches_oracle(ic, c):
+    x, w, dy = _setup(c)
+    wl = "KRSC" if c.layout == "NHWC" else "KCRS"
+    dyt, dyf, dys = _place(dy, c.layout)
+    wt, wf, wss = _place(w, wl)
+    dx = _out(x.shape, c.layout)
+    kw = dict(pre_padding=c.pre, post_padding=c.post, stride=c.stride, dilation=c.dil, mode=c.mode, algo=c.algo)
+    p = ic.Params.make(c.pre, c.post, c.stride, c.dil, c.mode, False, False, c.algo)
+    route = ic.dgrad_workspace_size(ic.TensorDesc.from_tensor(dyt), ic.TensorDesc.from_tensor(wt),
+                                    ic.TensorDesc.from_tensor(dx), p) > 0
+    assert route == c.tensor
+    ic.conv_dgrad(dyt, wt, out=dx, **kw)
+    torch.cuda.synchronize()
+    assert ic.device_status() == 0
+    ref = oracle.conv_dgrad(dyf, dy.shape, dys, wf, w.shape, wss, x.shape, c.pre, c.post, c.stride, c.dil, c.mode)
+    got = dx.cpu().numpy()
+    assert np.array_equal(got, ref), f"{c.name}: {(got != ref).sum()} of {ref.size} dX elements differ"
+
+
+@pytest.mark.parametrize("c", CASES, ids=lambda c: c.name)
+def test_wgrad_matches_oracle(ic, c):
+    x, w, dy = _setup(c)
+    wl = "KRSC" if c.layout == "NHWC" else "KCRS"
+    xt, xf, xs = _place(x, c.layout)
+    dyt, dyf, dys = _place(dy, c.layout)
+    dw = _out(w.shape, "NHWC" if wl == "KRSC" else "NCHW")  # KRSC is the NHWC order of [K,C,R,S]
+    algo = 3 if c.algo == 3 else 0
+    ic.conv_wgrad(xt, dyt, out=dw, pre_padding=c.pre, post_padding=c.post, stride=c.stride, dilation=c.dil,
+                  mode=c.mode, algo=algo)
+    torch.cuda.synchronize()
+    assert ic.device_status() == 0
+    ref = oracle.conv_wgrad(xf, x.shape, xs, dyf, dy.shape, dys, w.shape, c.pre, c.post, c.stride, c.dil, c.mode)
+    got = dw.cpu().numpy()
+    assert np.array_equal(got, ref), f"{c.name}: {(got != ref).sum()} of {ref.size} dW elements differ"
+
+
+def test_dgrad_extremes_exceed_f32_integer_range(ic):
+    """All -128 loss gradient and filter on the tensor-core route: interior dX
+    sums are K*R*S*2^14 = 2304*16384 > 2^24, exact only with the grouped
+    reduction."""
+    c = G("ext", 1, 64, 12, 12, 256, 3, 3, (1, 1), (1, 1), tensor=True)
+    dy = np.full((1, 256, 12, 12), -128, dtype=np.int8)
+    w = np.full((256, 64, 3, 3), -128, dtype=np.int8)
+    dyt, dyf, dys = _place(dy, "NHWC")
+    wt, wf, wss = _place(w, "KRSC")
+    dx = _out((1, 64, 12, 12), "NHWC")
+    ic.conv_dgrad(dyt, wt, out=dx, padding=(1, 1))
+    torch.cuda.synchronize()
+    ref = oracle.conv_dgrad(dyf, dy.shape, dys, wf, w.shape, wss, (1, 64, 12, 12), (1, 1), (1, 1))
+    assert int(ref.max()) == 256 * 9 * 16384
+    assert np.array_equal(dx.cpu().numpy(), ref)

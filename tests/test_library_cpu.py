@@ -304,3 +304,64 @@ def test_call_checks_before_any_device_work(ic):
     ye = ic.TensorDesc.packed(ic.CONV_INT32, (1, 64, 28, 28), "NHWC")
     ye.dims[0] = 0
     assert ic.conv_fprop_raw(xe, 0, wd, 0, ye, 0, 0, p, 0, 0, 0) == 0
+
+
+def test_gradient_validation_and_routes(ic):
+    """conv_dgrad / conv_wgrad take the forward call's descriptors and
+    parameters: shapes, types, epilogue, algorithm and the int32 bound are
+    checked; dgrad with stride 1 and padding within the filter's reach takes
+    the tensor-core route (a workspace), everything else the CUDA-core kernels."""
+    def d(dtype, dims, layout):
+        return ic.TensorDesc.packed(dtype, dims, layout)
+
+    x = d(ic.CONV_INT8, (2, 64, 14, 14), "NHWC")
+    w = d(ic.CONV_INT8, (32, 64, 3, 3), "KRSC")
+    dy = d(ic.CONV_INT8, (2, 32, 14, 14), "NHWC")
+    dx = d(ic.CONV_INT32, (2, 64, 14, 14), "NHWC")
+    dw = d(ic.CONV_INT32, (32, 64, 3, 3), "KRSC")
+    p = ic.Params.make(padding=(1, 1))
+    assert ic.dgrad_workspace_size(dy, w, dx, p) > 0          # tensor-core route
+    assert ic.wgrad_workspace_size(x, dy, dw, p) == 0
+
+    def code(fn, *a):
+        try:
+            fn(*a)
+            return 0
+        except ic.ConvError as e:
+            return e.status
+
+    S = ic.STATUS_CODE
+    assert code(ic.dgrad_workspace_size, dy, w, d(ic.CONV_INT8, (2, 64, 14, 14), "NHWC"), p) == S["CONV_ERR_DTYPE"]
+    assert code(ic.dgrad_workspace_size, dy, w, d(ic.CONV_INT32, (2, 64, 15, 14), "NHWC"), p) == \
+        S["CONV_ERR_SHAPE_MISMATCH"]
+    assert code(ic.wgrad_workspace_size, x, d(ic.CONV_INT8, (2, 31, 14, 14), "NHWC"), dw, p) == \
+        S["CONV_ERR_SHAPE_MISMATCH"]
+    pb = ic.Params.make(padding=(1, 1), relu=True)
+    assert code(ic.dgrad_workspace_size, dy, w, dx, pb) == S["CONV_ERR_BAD_PARAM"]
+    p8 = ic.Params.make(padding=(1, 1), out_shift=3)
+    assert code(ic.wgrad_workspace_size, x, dy, dw, p8) == S["CONV_ERR_BAD_PARAM"]
+    pa = ic.Params.make(padding=(1, 1), algo=ic.ALGO_DIRECT_DP4A)
+    assert code(ic.dgrad_workspace_size, dy, w, dx, pa) == S["CONV_ERR_BAD_PARAM"]
+    pg = ic.Params.make(padding=(1, 1), algo=ic.ALGO_IMPLICIT_GEMM)
+    assert code(ic.wgrad_workspace_size, x, dy, dw, pg) == S["CONV_ERR_ALIGNMENT"]
+    # stride 2: CUDA-core route, no workspace; forcing the tensor cores is refused
+    dy2 = d(ic.CONV_INT8, (2, 32, 7, 7), "NHWC")
+    p2 = ic.Params.make(pre_padding=(1, 1), post_padding=(0, 0), stride=(2, 2))
+    assert ic.dgrad_workspace_size(dy2, w, dx, p2) == 0
+    p2g = ic.Params.make(pre_padding=(1, 1), post_padding=(0, 0), stride=(2, 2), algo=ic.ALGO_IMPLICIT_GEMM)
+    assert code(ic.dgrad_workspace_size, dy2, w, dx, p2g) == S["CONV_ERR_ALIGNMENT"]
+    # padding wider than the filter's reach (3 > 2): CUDA-core route
+    dy3 = d(ic.CONV_INT8, (2, 32, 18, 18), "NHWC")
+    p3 = ic.Params.make(padding=(3, 3))
+    assert ic.dgrad_workspace_size(dy3, w, dx, p3) == 0
+    # int32 bounds: dgrad sums K*R*S terms, wgrad N*P*Q terms
+    wbig = d(ic.CONV_INT8, (14564, 64, 3, 3), "KRSC")    # 14564*9 = 131076 > 131071
+    dybig = d(ic.CONV_INT8, (2, 14564, 14, 14), "NHWC")
+    assert code(ic.dgrad_workspace_size, dybig, wbig, dx, p) == S["CONV_ERR_OVERFLOW_RISK"]
+    xl = d(ic.CONV_INT8, (1, 8, 363, 363), "NHWC")      # 363*363 = 131769 > 131071 pixels
+    dyl = d(ic.CONV_INT8, (1, 4, 363, 363), "NHWC")
+    dwl = d(ic.CONV_INT32, (4, 8, 1, 1), "KRSC")
+    assert code(ic.wgrad_workspace_size, xl, dyl, dwl, ic.Params.make()) == S["CONV_ERR_OVERFLOW_RISK"]
+    xs = d(ic.CONV_INT8, (1, 8, 362, 362), "NHWC")      # 131044 pixels fit
+    dys = d(ic.CONV_INT8, (1, 4, 362, 362), "NHWC")
+    assert ic.wgrad_workspace_size(xs, dys, dwl, ic.Params.make()) == 0
