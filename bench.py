@@ -53,6 +53,9 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="fprop", choices=["fprop", "fprop_int8", "dgrad", "wgrad", "graph"],
+                    help="fprop: the headline line; the others time the extensions on the same workload "
+                         "(int8 output, data gradient, weight gradient, CUDA-graph replay vs eager calls)")
     return ap.parse_args(argv)
 
 
@@ -417,10 +420,194 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------- extensions
+IMAD_PER_SM_CLK = 64  # 32-bit integer multiply-adds per SM per clock (CUDA cores)
+
+
+def run_extension(args):
+    """One JSON line for an extension op on the workload, single GPU: the int8
+    output epilogue, the data gradient, the weight gradient, or CUDA-graph
+    replay of conv_fprop against eager calls.  Inputs resident, rotating sets
+    larger than L2, CUDA events on the launching stream around every call."""
+    import torch
+
+    import int8_conv2d_fprop_gb300 as ic
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    cfg = synth.CONFIGS[args.workload]
+    x, w, b = synth.make_inputs(cfg)
+    xf, xs = synth.place(x, cfg.x_layout)
+    wf, ws = synth.place(w, cfg.w_layout)
+    ystr = synth.packed_strides(cfg.y_dims, cfg.y_layout)
+    ysz = int(np.prod(cfg.y_dims))
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    peaks, peak_src = load_peaks()
+    bf16 = _peak_value(peaks, ("bf16_tflops", "bf16_dense_tflops")) or FALLBACK_PEAKS["bf16_tflops"]
+    if _peak_value(peaks, ("bf16_tflops", "bf16_dense_tflops")) is None:
+        peak_src = "fallback"
+    w_dev = torch.from_numpy(wf).to(dev)
+    wd = ic.TensorDesc.make(ic.CONV_INT8, cfg.w_dims, ws, wf.size)
+    xd = ic.TensorDesc.make(ic.CONV_INT8, cfg.x_dims, xs, xf.size)
+    extra = {}
+
+    if args.op in ("fprop_int8", "fprop", "graph"):
+        int8 = args.op == "fprop_int8"
+        esz = 1 if int8 else 4
+        yd = ic.TensorDesc.make(ic.CONV_INT8 if int8 else ic.CONV_INT32, cfg.y_dims, ystr, ysz * esz)
+        p = ic.Params.make(cfg.pre, cfg.post, cfg.stride, cfg.dilation, cfg.mode, cfg.bias, cfg.relu,
+                           out_shift=10 if int8 else None)
+        set_bytes = xf.size + ysz * esz
+        nsets = max(2, int(np.ceil(3 * L2_BYTES / set_bytes)) + 1) if args.op != "graph" else 1
+        a_sets = [torch.from_numpy(xf).to(dev) for _ in range(nsets)]
+        o_sets = [torch.empty(ysz * esz, dtype=torch.uint8, device=dev) for _ in range(nsets)]
+        b_dev = torch.from_numpy(b).to(dev) if b is not None else None
+        wsb = ic.workspace_size(xd, wd, yd, p)
+        work = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+        bias_ptr = b_dev.data_ptr() if b_dev is not None else 0
+
+        def call(i, stream_handle=None):
+            k = i % nsets
+            st = ic.conv_fprop_raw(xd, a_sets[k].data_ptr(), wd, w_dev.data_ptr(), yd, o_sets[k].data_ptr(),
+                                   bias_ptr, p, work.data_ptr(), wsb, stream_handle or sh)
+            if st:
+                raise ic.ConvError(st, "conv_fprop")
+
+        ops = cfg.ops
+        alg_bytes = xf.size + wf.size + ysz * esz + (4 * cfg.K if cfg.bias else 0)
+        metric = ("INT8 conv fprop with int8 output TOPS (2NKPQCRS/s)" if int8 else
+                  "INT8 conv fprop per-call latency, CUDA-graph replay vs eager (us)")
+        bound, peak, unit = "tensor", bf16, "TFLOP/s"
+    elif args.op == "dgrad":
+        dy = synth.int8_uniform(cfg.seed, 3, cfg.y_dims)
+        dyf, dys = synth.place(dy, cfg.y_layout)
+        dyd = ic.TensorDesc.make(ic.CONV_INT8, cfg.y_dims, dys, dyf.size)
+        dxs = synth.packed_strides(cfg.x_dims, cfg.x_layout)
+        xsz = int(np.prod(cfg.x_dims))
+        dxd = ic.TensorDesc.make(ic.CONV_INT32, cfg.x_dims, dxs, xsz * 4)
+        p = ic.Params.make(cfg.pre, cfg.post, cfg.stride, cfg.dilation, cfg.mode)
+        set_bytes = dyf.size + xsz * 4
+        nsets = max(2, int(np.ceil(3 * L2_BYTES / set_bytes)) + 1)
+        a_sets = [torch.from_numpy(dyf).to(dev) for _ in range(nsets)]
+        o_sets = [torch.empty(xsz, dtype=torch.int32, device=dev) for _ in range(nsets)]
+        wsb = ic.dgrad_workspace_size(dyd, wd, dxd, p)
+        work = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+        L = ic.lib()
+        import ctypes
+
+        def call(i):
+            k = i % nsets
+            st = L.conv_dgrad(ctypes.byref(dyd), a_sets[k].data_ptr(), ctypes.byref(wd), w_dev.data_ptr(),
+                              ctypes.byref(dxd), o_sets[k].data_ptr(), ctypes.byref(p),
+                              work.data_ptr() if wsb else None, wsb, sh)
+            if st:
+                raise ic.ConvError(st, "conv_dgrad")
+
+        ops = cfg.ops
+        alg_bytes = dyf.size + wf.size + xsz * 4
+        metric = "INT8 conv dgrad TOPS (2NKPQCRS/s)"
+        tensor = wsb > 0
+        bound = "tensor" if tensor else "alu"
+        peak = bf16 if tensor else 152 * IMAD_PER_SM_CLK * 2 * 2.07e9 / 1e12
+        unit = "TFLOP/s" if tensor else "TOPS"
+        extra["route"] = "tensor cores (forward convolution of dY)" if tensor else "CUDA cores"
+    else:  # wgrad
+        dy = synth.int8_uniform(cfg.seed, 3, cfg.y_dims)
+        dyf, dys = synth.place(dy, cfg.y_layout)
+        dyd = ic.TensorDesc.make(ic.CONV_INT8, cfg.y_dims, dys, dyf.size)
+        dws = synth.packed_strides(cfg.w_dims, cfg.w_layout)
+        wsz = int(np.prod(cfg.w_dims))
+        dwd = ic.TensorDesc.make(ic.CONV_INT32, cfg.w_dims, dws, wsz * 4)
+        p = ic.Params.make(cfg.pre, cfg.post, cfg.stride, cfg.dilation, cfg.mode)
+        nsets = max(2, int(np.ceil(3 * L2_BYTES / (xf.size + dyf.size))) + 1)
+        a_sets = [torch.from_numpy(xf).to(dev) for _ in range(nsets)]
+        g_sets = [torch.from_numpy(dyf).to(dev) for _ in range(nsets)]
+        out = torch.empty(wsz, dtype=torch.int32, device=dev)
+        L = ic.lib()
+        import ctypes
+
+        def call(i):
+            k = i % nsets
+            st = L.conv_wgrad(ctypes.byref(xd), a_sets[k].data_ptr(), ctypes.byref(dyd), g_sets[k].data_ptr(),
+                              ctypes.byref(dwd), out.data_ptr(), ctypes.byref(p), None, 0, sh)
+            if st:
+                raise ic.ConvError(st, "conv_wgrad")
+
+        ops = cfg.ops
+        alg_bytes = xf.size + dyf.size + wsz * 4
+        metric = "INT8 conv wgrad TOPS (2NKPQCRS/s)"
+        bound, unit = "alu", "TOPS"
+        peak = 152 * IMAD_PER_SM_CLK * 2 * 2.07e9 / 1e12
+        extra["route"] = "CUDA cores"
+
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize(dev)
+    if ic.device_status(sh):
+        raise RuntimeError("device status after warm-up")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        call(args.warmup + i)
+        evs[i][1].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    total_ms = e0.elapsed_time(e1)
+    call_ms = statistics.mean(a.elapsed_time(bb) for a, bb in evs)
+    if ic.device_status(sh):
+        raise RuntimeError("device status after the timed region")
+    ms_per_step = total_ms / args.steps
+    if args.op == "graph":
+        # the same call captured once and replayed
+        side = torch.cuda.Stream(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            call(0, side.cuda_stream)
+        side.synchronize()
+        # the call must be queued on the capturing stream to be recorded
+        with torch.cuda.graph(graph, stream=side):
+            call(0, side.cuda_stream)
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        graph_ms = g0.elapsed_time(g1) / args.steps
+        line = {"metric": metric, "value": round(graph_ms * 1e3, 3), "unit": "us", "n_gpus": 1,
+                "steps": args.steps, "warmup": args.warmup, "higher_is_better": False,
+                "eager_us": round(ms_per_step * 1e3, 3), "graph_us": round(graph_ms * 1e3, 3),
+                "config": {"workload": cfg.name, "l2": "one resident set (latency, not bandwidth)"},
+                "data": "synthetic", "dtype": "int8 x int8 -> int32"}
+        print(json.dumps(line), flush=True)
+        return
+    achieved = ops / (call_ms * 1e-3) / 1e12
+    line = {
+        "metric": metric, "value": round(ops / (ms_per_step * 1e-3) / 1e12, 3), "unit": "TOPS", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "dtype": "int8 x int8 -> int32", "data": "synthetic (splitmix64 seeded int8 uniform[-128,127])",
+        "config": {"workload": cfg.name, "op": args.op, "ops_per_step": ops,
+                   "l2": f"rotating {nsets} resident sets (> 129 MB L2)", **extra},
+        "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 2), "unit": unit,
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src if bound == "tensor" else
+                     "152 SMs x 64 int32 multiply-adds/clk x 2 ops x 2.07 GHz",
+                     "call_ms": round(call_ms, 5), "algorithmic_bytes": int(alg_bytes)},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.op != "fprop":
+        run_extension(args)
     else:
         run_ours(args)
 

@@ -593,7 +593,51 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 ++gi;
             }
             if (!ok) break;
-            if (a.y_tma) {
+            // epilogue arithmetic, once: + bias[k] (int32 wrap-around), then ReLU
+            if (a.bias || a.relu) {
+                const int kb = nt * NT + col0;
+#pragma unroll
+                for (int i = 0; i < HALF; ++i) {
+                    int32_t val = acc[i];
+                    if (a.bias && kb + i < a.K) val = (int32_t)((uint32_t)val + (uint32_t)__ldg(a.bias + kb + i));
+                    acc[i] = a.relu ? max(val, 0) : val;
+                }
+            }
+            if (a.y_tma && a.out_int8) {
+                // int8 output: as below, with 64 one-byte columns per 64-byte
+                // staged row
+                const int k0 = nt * NT + col0;
+                const int m0w = mt * MT + quad * 32;
+                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (2u * EPI_BUF_BYTES);
+                const uint32_t sw = ((uint32_t)lane >> 1) & 3u;
+#pragma unroll
+                for (int ch = 0; ch < HALF / 64; ++ch) {
+                    const uint32_t buf = ebase + (uint32_t)(ch & 1) * EPI_BUF_BYTES;
+                    if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store that last read buf is done
+                    __syncwarp();
+                    const uint32_t rowaddr = buf + (uint32_t)lane * 64u;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t wv[4];
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            wv[q4] = 0;
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int i = ch * 64 + c * 16 + q4 * 4 + e;
+                                wv[q4] |= (uint32_t)(uint8_t)requant_i8(acc[i], a.out_shift) << (8 * e);
+                            }
+                        }
+                        ptx::st_shared_v4(rowaddr + ((((uint32_t)c) ^ sw) << 4), make_uint4(wv[0], wv[1], wv[2], wv[3]));
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_2d(&a.tmap_y, k0 + ch * 64, m0w, buf);
+                        ptx::bulk_commit_group();
+                    }
+                }
+            } else if (a.y_tma) {
                 // Rows of the tile are consecutive pixels with contiguous
                 // channels: each warp stages 32 rows x 16 columns at a time in
                 // shared memory (64-byte rows; 16-byte chunk c of row r at
@@ -609,35 +653,13 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                     const uint32_t buf = ebase + (uint32_t)(ch & 1) * EPI_BUF_BYTES;
                     if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store that last read buf is done
                     __syncwarp();
-                    int32_t o[EPI_COLS];
+                    const int i0 = ch * EPI_COLS;
+                    const uint32_t rowaddr = buf + (uint32_t)lane * 64u;
 #pragma unroll
-                    for (int e = 0; e < EPI_COLS; ++e) {
-                        const int i = ch * EPI_COLS + e;
-                        const int k = k0 + i;
-                        int32_t val = acc[i];
-                        if (a.bias && k < a.K) val = (int32_t)((uint32_t)val + (uint32_t)__ldg(a.bias + k));
-                        if (a.relu) val = max(val, 0);
-                        o[e] = val;
-                    }
-                    if (a.out_int8) {
-                        // int8 rows of 16 bytes, unswizzled: lane r's row at r * 16
-                        uint32_t wv[4];
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            wv[c] = 0;
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                wv[c] |= (uint32_t)(uint8_t)requant_i8(o[c * 4 + e], a.out_shift) << (8 * e);
-                        }
-                        ptx::st_shared_v4(buf + (uint32_t)lane * 16u, make_uint4(wv[0], wv[1], wv[2], wv[3]));
-                    } else {
-                        const uint32_t rowaddr = buf + (uint32_t)lane * 64u;
-#pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            ptx::st_shared_v4(rowaddr + ((((uint32_t)c) ^ sw) << 4),
-                                              make_uint4((uint32_t)o[c * 4], (uint32_t)o[c * 4 + 1],
-                                                         (uint32_t)o[c * 4 + 2], (uint32_t)o[c * 4 + 3]));
-                    }
+                    for (int c = 0; c < 4; ++c)
+                        ptx::st_shared_v4(rowaddr + ((((uint32_t)c) ^ sw) << 4),
+                                          make_uint4((uint32_t)acc[i0 + c * 4], (uint32_t)acc[i0 + c * 4 + 1],
+                                                     (uint32_t)acc[i0 + c * 4 + 2], (uint32_t)acc[i0 + c * 4 + 3]));
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
@@ -651,12 +673,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
 #pragma unroll
                 for (int i = 0; i < HALF; ++i) {
                     const int k = k0 + i;
-                    if (k < a.K) {
-                        int32_t val = acc[i];
-                        if (a.bias) val = (int32_t)((uint32_t)val + (uint32_t)__ldg(a.bias + k));
-                        if (a.relu) val = max(val, 0);
-                        yrow[(int64_t)k * a.ys_k] = requant_i8(val, a.out_shift);
-                    }
+                    if (k < a.K) yrow[(int64_t)k * a.ys_k] = requant_i8(acc[i], a.out_shift);
                 }
             } else if (valid) {
                 const int k0 = nt * NT + col0;
@@ -664,14 +681,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
 #pragma unroll
                 for (int c4 = 0; c4 < HALF / 4; ++c4) {
                     const int k = k0 + c4 * 4;
-                    int32_t o[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        int32_t val = acc[c4 * 4 + e];
-                        if (a.bias && k + e < a.K) val = (int32_t)((uint32_t)val + (uint32_t)__ldg(a.bias + k + e));
-                        if (a.relu) val = max(val, 0);
-                        o[e] = val;
-                    }
+                    const int32_t o[4] = {acc[c4 * 4], acc[c4 * 4 + 1], acc[c4 * 4 + 2], acc[c4 * 4 + 3]};
                     if (a.y_vec && k + 3 < a.K) {
                         ptx::st_global_v4(yrow + (int64_t)k * a.ys_k, o[0], o[1], o[2], o[3]);
                     } else {
@@ -863,9 +873,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tiled_encoder() {
 
 // 2-D map [N*P*Q pixels][K channels] of the output when its pixels follow one
 // another at a fixed stride with channels contiguous (NHWC, possibly with
-// padded pixel rows): box 32 pixels x 16 channels; int32 elements with the
-// 64-byte swizzle, int8 elements (16-byte rows) unswizzled.  Returns false for
-// any other layout.
+// padded pixel rows): box 32 pixels x 64 bytes of channels (16 int32 or 64
+// int8) with the 64-byte swizzle.  Returns false for any other layout.
 bool encode_output_map(const ConvGeom &g, const void *y, CUtensorMap *map) {
     const int64_t esz = g.out_int8 ? 1 : 4;
     if (g.ys[1] != 1 && g.K > 1) return false;
@@ -887,11 +896,11 @@ bool encode_output_map(const ConvGeom &g, const void *y, CUtensorMap *map) {
     if (!enc) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)g.K, (cuuint64_t)m_total};
     const cuuint64_t strides[1] = {(cuuint64_t)(ps * esz)};
-    const cuuint32_t box[2] = {(cuuint32_t)EPI_COLS, 32};
+    const cuuint32_t box[2] = {(cuuint32_t)(g.out_int8 ? 64 : EPI_COLS), 32};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = enc(map, g.out_int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_INT32, 2,
                            const_cast<void *>(y), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           g.out_int8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_64B,
+                           CU_TENSOR_MAP_SWIZZLE_64B,
                            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

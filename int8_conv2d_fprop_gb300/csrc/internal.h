@@ -26,11 +26,12 @@ struct ConvGeom {
 
 #ifdef __CUDACC__
 // int8 output of CONV_EPILOGUE_INT8_OUT: floor((v + 2^(shift-1)) / 2^shift)
-// (shift > 0; the arithmetic right shift of a signed value floors), then
-// clamped to [-128, 127].
+// for shift > 0, then clamped to [-128, 127].  In 32-bit arithmetic without
+// overflow: floor(v / 2^s) is the arithmetic shift v >> s, and adding half
+// before flooring adds exactly the bit just below the cut, (v >> (s-1)) & 1.
 __device__ __forceinline__ int8_t requant_i8(int32_t v, int32_t shift) {
-    int64_t t = v;
-    if (shift > 0) t = (t + ((int64_t)1 << (shift - 1))) >> shift;
+    int32_t t = v;
+    if (shift > 0) t = (v >> shift) + ((v >> (shift - 1)) & 1);
     t = t > 127 ? 127 : (t < -128 ? -128 : t);
     return (int8_t)t;
 }
