@@ -524,22 +524,28 @@ def run_extension(args):
         a_sets = [torch.from_numpy(xf).to(dev) for _ in range(nsets)]
         g_sets = [torch.from_numpy(dyf).to(dev) for _ in range(nsets)]
         out = torch.empty(wsz, dtype=torch.int32, device=dev)
+        wsb = ic.wgrad_workspace_size(xd, dyd, dwd, p)
+        work = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
         L = ic.lib()
         import ctypes
 
         def call(i):
             k = i % nsets
             st = L.conv_wgrad(ctypes.byref(xd), a_sets[k].data_ptr(), ctypes.byref(dyd), g_sets[k].data_ptr(),
-                              ctypes.byref(dwd), out.data_ptr(), ctypes.byref(p), None, 0, sh)
+                              ctypes.byref(dwd), out.data_ptr(), ctypes.byref(p), work.data_ptr() if wsb else None,
+                              wsb, sh)
             if st:
                 raise ic.ConvError(st, "conv_wgrad")
 
         ops = cfg.ops
         alg_bytes = xf.size + dyf.size + wsz * 4
         metric = "INT8 conv wgrad TOPS (2NKPQCRS/s)"
-        bound, unit = "alu", "TOPS"
-        peak = 152 * IMAD_PER_SM_CLK * 2 * 2.07e9 / 1e12
-        extra["route"] = "CUDA cores"
+        tensor = wsb > 0
+        bound = "tensor" if tensor else "alu"
+        unit = "TFLOP/s" if tensor else "TOPS"
+        peak = bf16 if tensor else 152 * IMAD_PER_SM_CLK * 2 * 2.07e9 / 1e12
+        extra["route"] = ("tensor cores (forward convolution of the image by dY, reduction split over the SMs)"
+                          if tensor else "CUDA cores")
 
     for i in range(args.warmup):
         call(i)

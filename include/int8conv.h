@@ -297,12 +297,18 @@ conv_status conv_fprop_static_workspace(const conv_tensor_desc *x, const int8_t 
  *
  * conv_dgrad with stride 1 and padding no wider than the filter's reach
  * (pre, post <= dilation*(taps-1)) runs on the tensor cores as a forward
- * convolution of dY and needs the workspace conv_dgrad_workspace_size
- * reports (256-byte aligned, caller-owned); other calls run CUDA-core
- * kernels and need none.  conv_wgrad runs a CUDA-core kernel (workspace 0;
- * IMPLICIT_GEMM returns CONV_ERR_ALIGNMENT).  Pointers are device pointers on
- * the current device, outputs must not overlap inputs or the workspace; the
- * calls are asynchronous on `stream` and allocate nothing.
+ * convolution of dY; conv_wgrad runs on the tensor cores as a forward
+ * convolution of the image (batch and channel dims exchanged) by dY (its
+ * batch as channels, its pixels as taps) when the tensor-core kernel can
+ * express it.  Those routes need the workspace the *_workspace_size call
+ * reports (256-byte aligned, caller-owned; for wgrad it holds dY repacked to
+ * f16 blocks, about 2*K*P*Q*ceil(N/64)*64 bytes, plus the int32 partial sums
+ * of the reduction split over the SMs).  Other calls, and algo
+ * DIRECT_GENERIC, run CUDA-core kernels and need none; IMPLICIT_GEMM on a
+ * call that cannot take the tensor cores returns CONV_ERR_ALIGNMENT.
+ * Pointers are device pointers on the current device, outputs must not
+ * overlap inputs or the workspace; the calls are asynchronous on `stream`
+ * and allocate nothing.
  */
 conv_status conv_dgrad_workspace_size(const conv_tensor_desc *dy, const conv_tensor_desc *w,
                                       const conv_tensor_desc *dx, const conv_fprop_params *p, size_t *bytes);

@@ -376,16 +376,20 @@ def conv_dgrad(dy, w, *, out, pre_padding=(0, 0), post_padding=(0, 0), padding=N
 
 
 def conv_wgrad(x, dy, *, out, pre_padding=(0, 0), post_padding=(0, 0), padding=None, stride=(1, 1),
-               dilation=(1, 1), mode: int = CROSS_CORRELATION, algo: int = ALGO_AUTO, stream=None):
+               dilation=(1, 1), mode: int = CROSS_CORRELATION, algo: int = ALGO_AUTO, workspace=None, stream=None):
     """Weight gradient dW of conv_fprop: x int8 CUDA tensor [N,C,H,W], dy int8
     [N,K,P,Q] (the loss gradient), out int32 [K,C,R,S] (any strides; R, S are
     the forward filter size).  Parameters as for conv_fprop.  Returns ``out``."""
     import torch
     p = _grad_params(pre_padding, post_padding, padding, stride, dilation, mode, algo)
     xd, dyd, dwd = TensorDesc.from_tensor(x), TensorDesc.from_tensor(dy), TensorDesc.from_tensor(out)
+    ws_bytes = wgrad_workspace_size(xd, dyd, dwd, p)
+    if ws_bytes and (workspace is None or workspace.numel() * workspace.element_size() < ws_bytes):
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
     if stream is None:
         stream = torch.cuda.current_stream(x.device)
     st = lib().conv_wgrad(ctypes.byref(xd), x.data_ptr(), ctypes.byref(dyd), dy.data_ptr(), ctypes.byref(dwd),
-                          out.data_ptr(), ctypes.byref(p), None, 0, stream.cuda_stream or None)
+                          out.data_ptr(), ctypes.byref(p), workspace.data_ptr() if ws_bytes else None,
+                          ws_bytes if ws_bytes else 0, stream.cuda_stream or None)
     _check(st, "conv_wgrad")
     return out

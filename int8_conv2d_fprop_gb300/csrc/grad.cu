@@ -10,10 +10,17 @@
 //    padding dil*(taps-1) - pre before, dil*(taps-1) - post after.  It runs on
 //    the tensor-core kernel, with its filter repack and workspace.
 //  * otherwise: a CUDA-core kernel, one thread per dX element.
-// wgrad, dW[k,c,r',s'] = sum over n, p, q of dY[n,k,p,q] * X[n,c,h,w]: a
-// CUDA-core kernel, one warp per dW element, the lanes splitting the n, p, q
-// sum (int32 partial sums, exact by the validator's bound, added across the
-// warp with shuffles).
+// wgrad, dW[k,c,r',s'] = sum over n, p, q of dY[n,k,p,q] * X[n,c,h,w]:
+//  * a forward convolution whose image is X with its batch and channel dims
+//    exchanged ([C][N][H][W]), whose filter is dY ([K][N][P][Q]: the batch
+//    as channels, the output pixels as taps), with the forward stride and
+//    dilation exchanged, and whose [C][K][R][S] output is dW with its first
+//    two dims exchanged (taps written backwards in CONVOLUTION mode).  Its
+//    few output tiles have long reductions (N*P*Q), which the tensor-core
+//    kernel cuts into runs over the SMs and adds back up.
+//  * otherwise (or with DIRECT_GENERIC): a CUDA-core kernel, one warp per dW
+//    element, the lanes splitting the n, p, q sum (int32 partial sums, exact
+//    by the validator's bound, added across the warp with shuffles).
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -159,6 +166,56 @@ bool dgrad_as_fprop(const conv_tensor_desc *dy, const conv_tensor_desc *w, const
     return igemm_supported(*g);
 }
 
+// wgrad as a forward convolution (see the top of the file); fills g and the
+// element offset of the output's origin (non-zero when CONVOLUTION mode runs
+// the output taps backwards) and returns true when the tensor-core kernel
+// takes it.
+bool wgrad_as_fprop(const conv_tensor_desc *x, const conv_tensor_desc *dy, const conv_tensor_desc *dw,
+                    const conv_fprop_params *p, ConvGeom *g, int64_t *y_origin) {
+    int64_t xs[4], ys[4], ds[4];
+    unit_strides(x, xs);
+    unit_strides(dy, ys);
+    unit_strides(dw, ds);
+    // image: the batch becomes the channels, the channels the batch
+    g->N = x->dims[1]; g->C = x->dims[0]; g->H = x->dims[2]; g->W = x->dims[3];
+    g->xs[0] = xs[1]; g->xs[1] = xs[0]; g->xs[2] = xs[2]; g->xs[3] = xs[3];
+    // filter: dY, its batch as channels, its P x Q pixels as taps
+    g->K = dy->dims[1]; g->R = dy->dims[2]; g->S = dy->dims[3];
+    g->ws[0] = ys[1]; g->ws[1] = ys[0]; g->ws[2] = ys[2]; g->ws[3] = ys[3];
+    // output [C][K][R][S]: dW with its first two dims exchanged
+    g->P = dw->dims[2]; g->Q = dw->dims[3];
+    g->ys[0] = ds[1]; g->ys[1] = ds[0]; g->ys[2] = ds[2]; g->ys[3] = ds[3];
+    *y_origin = 0;
+    if (p->mode == CONV_CONVOLUTION) {  // dW[k,c,R-1-r,S-1-s] holds tap (r, s)
+        *y_origin = (g->P - 1) * ds[2] + (g->Q - 1) * ds[3];
+        g->ys[2] = -ds[2];
+        g->ys[3] = -ds[3];
+    }
+    // h = r*dil - pre + p*stride: the forward stride and dilation change places
+    g->pad_h = p->pre_padding[0]; g->pad_w = p->pre_padding[1];
+    g->str_h = p->dilation[0]; g->str_w = p->dilation[1];
+    g->dil_h = p->stride[0]; g->dil_w = p->stride[1];
+    g->mode = CONV_CROSS_CORRELATION;
+    g->bias = g->relu = g->out_int8 = false;
+    g->out_shift = 0;
+    if (!igemm_supported(*g)) return false;
+    // the repacked loss gradient grows with P*Q*ceil(N/64) f16 blocks: keep it
+    // within a few GB
+    const int64_t blocks = ((g->K + 255) / 256) * g->R * g->S * ((g->C + 63) / 64);
+    return blocks * 256 * 128 <= ((int64_t)4 << 30);
+}
+
+conv_status plan_wgrad(const conv_tensor_desc *x, const void *x_dev, const conv_tensor_desc *dy,
+                       const conv_tensor_desc *dw, const conv_fprop_params *p, ConvGeom *g, int64_t *y_origin,
+                       bool *tensor, IgemmPlan *pl) {
+    conv_status st = validate_wgrad(x, dy, dw, p);
+    if (st) return st;
+    *tensor = p->algo != CONV_ALGO_DIRECT_GENERIC && wgrad_as_fprop(x, dy, dw, p, g, y_origin);
+    if (p->algo == CONV_ALGO_IMPLICIT_GEMM && !*tensor) return CONV_ERR_ALIGNMENT;
+    if (*tensor) igemm_plan(*g, x_dev, pl);
+    return CONV_OK;
+}
+
 // Plans a dgrad call: *tensor and *pl describe the tensor-core route when it
 // is taken.
 conv_status plan_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const conv_tensor_desc *w,
@@ -230,32 +287,46 @@ conv_status conv_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const c
 conv_status conv_wgrad_workspace_size(const conv_tensor_desc *x, const conv_tensor_desc *dy,
                                       const conv_tensor_desc *dw, const conv_fprop_params *p, size_t *bytes) {
     if (!bytes) return CONV_ERR_NULL_PTR;
-    conv_status st = validate_wgrad(x, dy, dw, p);
+    ConvGeom g;
+    IgemmPlan pl;
+    int64_t origin = 0;
+    bool tensor = false;
+    conv_status st = plan_wgrad(x, nullptr, dy, dw, p, &g, &origin, &tensor, &pl);
     if (st) return st;
-    if (p->algo == CONV_ALGO_IMPLICIT_GEMM) return CONV_ERR_ALIGNMENT;
-    *bytes = 0;
+    *bytes = (tensor && g.N > 0 && g.K > 0) ? pl.workspace_bytes : 0;
     return CONV_OK;
 }
 
 conv_status conv_wgrad(const conv_tensor_desc *x, const int8_t *x_dev, const conv_tensor_desc *dy,
                        const int8_t *dy_dev, const conv_tensor_desc *dw, int32_t *dw_dev,
                        const conv_fprop_params *p, void *workspace, size_t workspace_bytes, void *stream) {
-    (void)workspace;
-    (void)workspace_bytes;
-    conv_status st = validate_wgrad(x, dy, dw, p);
+    ConvGeom g;
+    IgemmPlan pl;
+    int64_t origin = 0;
+    bool tensor = false;
+    conv_status st = plan_wgrad(x, x_dev, dy, dw, p, &g, &origin, &tensor, &pl);
     if (st) return st;
-    if (p->algo == CONV_ALGO_IMPLICIT_GEMM) return CONV_ERR_ALIGNMENT;
     if (!x_dev || !dy_dev || !dw_dev) return CONV_ERR_NULL_PTR;
     const uint64_t dw_bytes = (uint64_t)desc_extent_elems(dw) * 4;
     if (overlaps(dw_dev, dw_bytes, x_dev, (uint64_t)desc_extent_elems(x)) ||
-        overlaps(dw_dev, dw_bytes, dy_dev, (uint64_t)desc_extent_elems(dy)))
+        overlaps(dw_dev, dw_bytes, dy_dev, (uint64_t)desc_extent_elems(dy)) ||
+        overlaps(dw_dev, dw_bytes, workspace, workspace_bytes))
         return CONV_ERR_OVERLAP;
     if ((st = check_device())) return st;
+    // an empty batch gives an all-zero gradient (the CUDA-core kernel writes it)
+    if (tensor && x->dims[0] > 0) {
+        if (!workspace || workspace_bytes < pl.workspace_bytes || ((uintptr_t)workspace % 256) != 0)
+            return CONV_ERR_WORKSPACE;
+        if (overlaps(workspace, pl.workspace_bytes, x_dev, (uint64_t)desc_extent_elems(x)) ||
+            overlaps(workspace, pl.workspace_bytes, dy_dev, (uint64_t)desc_extent_elems(dy)))
+            return CONV_ERR_OVERLAP;
+        if ((st = igemm_pack_filter_launch(g, pl, dy_dev, workspace, stream))) return st;
+        return igemm_main_launch(g, pl, x_dev, dw_dev + origin, nullptr, workspace, stream);
+    }
     GradArgs a = grad_args(x, dw, dy, p);
     a.a = x_dev;
     a.b = dy_dev;
     a.out = dw_dev;
-    // an empty batch gives an all-zero gradient
     wgrad_direct_kernel<<<grid_for(a.K * a.C * a.R * a.S * 32, 256), 256, 0, (cudaStream_t)stream>>>(a);
     return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }

@@ -24,7 +24,7 @@
 //    pre-swizzled f16 filter block with one bulk async copy.
 //  * global loads (fallback when an im2col map cannot express the call):
 //    warpgroup 0 threads each own one pixel row, gather 64 channels of one tap
-//    with 16-byte loads two items ahead (address formed from stride, padding
+//    with 16-byte loads one item ahead (address formed from stride, padding
 //    and dilation), convert in registers and write the row; thread 0 also
 //    issues the filter block copies.
 // In both, warp 4 allocates tensor memory and its lane 0 issues tcgen05.mma
@@ -62,7 +62,7 @@ constexpr int NUM_EPI_THREADS = 256;
 constexpr int PRODUCER_REGS = 80;
 constexpr int EPILOGUE_REGS = 176;
 static_assert(2 * 128 * PRODUCER_REGS + 2 * 128 * EPILOGUE_REGS <= 65536, "register split exceeds the launch");
-constexpr int PREFETCH = 2;  // register path: items in flight ahead of the one being stored
+constexpr int PREFETCH = 1;  // register path: items in flight ahead of the one being stored
 constexpr int STG_BYTES = MT * KS;  // one int8 im2col tile: 128 pixels x 64 channels
 constexpr int A_ISSUER_WARP = 5;    // TMA path: issues the im2col loads
 constexpr int B_ISSUER_WARP = 6;    // TMA path: issues the filter block copies
@@ -120,6 +120,33 @@ struct Ring {
     }
 };
 
+// One work unit: a tile and its run [kb, ke) of k-steps; split >= 0 for a
+// run of a tile that several CTAs share.
+struct Unit {
+    int tile, kb, ke, split;
+};
+
+__device__ __forceinline__ Unit unit_at(int u, int full_units, int splits, int k_steps) {
+    Unit w;
+    if (u < full_units) {
+        w.tile = u;
+        w.kb = 0;
+        w.ke = k_steps;
+        w.split = -1;
+    } else {
+        const int t = u - full_units;
+        w.tile = full_units + t / splits;
+        w.split = t - (t / splits) * splits;
+        w.kb = (int)(((int64_t)w.split * k_steps) / splits);
+        w.ke = (int)(((int64_t)(w.split + 1) * k_steps) / splits);
+    }
+    return w;
+}
+
+// Groups of a run of kn k-steps: the fewest runs of at most MAX_GROUP_STEPS
+// (group g covers k-steps g*kn/ng .. (g+1)*kn/ng - 1 of the run).
+__device__ __forceinline__ int groups_of(int kn) { return (kn + MAX_GROUP_STEPS - 1) / MAX_GROUP_STEPS; }
+
 struct IgemmArgs {
     CUtensorMap tmap_x;  // im2col map of the channels-last image (TMA path only)
     CUtensorMap tmap_y;  // 2-D [pixels][K] map of the output (when y_tma)
@@ -132,9 +159,16 @@ struct IgemmArgs {
     int64_t ys_n, ys_k, ys_p, ys_q;
     int32_t H, W, P, Q, K, S;
     int32_t c16;         // channel bytes per pixel that may be loaded (multiple of 16)
-    int32_t c_steps, k_steps, groups;
+    int32_t c_steps, k_steps;
     int32_t pad_h, pad_w, str_h, str_w, dil_h, dil_w;
     int32_t m_total, n_tiles, num_tiles;
+    // Work units.  Units below full_units are whole tiles (unit u = tile u).
+    // When there are fewer tiles than SMs and each has a long reduction, the
+    // tiles are cut into `splits` runs of k-steps instead: unit
+    // full_units + t covers run t % splits of tile full_units + t / splits,
+    // and writes its raw int32 sums to tail_part for the reduction kernel.
+    int32_t full_units, splits, num_units;
+    int32_t *tail_part;  // [cut tile][split][MT rows][NT columns]
     int32_t relu, y_vec;
     int32_t y_tma;       // output pixel-major with contiguous channels: TMA stores
     uint64_t wait_limit_ns;
@@ -205,21 +239,28 @@ __device__ __forceinline__ void cvt16(const uint4 in, uint4 &lo, uint4 &hi) {
     hi.z = cvt_pair(d, 0x4140); hi.w = cvt_pair(d, 0x4342);
 }
 
-// Where one producer thread is in its (tile, k-step) sequence.
+// Where one producer thread is in its (unit, k-step) sequence.
 struct LoadCursor {
-    int tile;       // tile index, >= num_tiles when done
-    int j, cb, r, s;
+    int u;          // work unit, >= num_units when done
+    int j, je;      // current and end k-step of the unit
+    int cb, r, s;   // channel block and tap of k-step j
     int64_t xoff;   // n * xs_n
     int h0, w0;
     bool valid;     // this thread's pixel row exists
 };
 
-__device__ __forceinline__ void cursor_set_tile(LoadCursor &c, const IgemmArgs &a, int tile, int row) {
-    c.tile = tile;
-    c.j = c.cb = c.r = c.s = 0;
-    const int mt = tile / a.n_tiles;
+__device__ __forceinline__ void cursor_set_unit(LoadCursor &c, const IgemmArgs &a, int u, int row) {
+    c.u = u;
+    const Unit w = unit_at(u < a.num_units ? u : 0, a.full_units, a.splits, a.k_steps);
+    c.j = w.kb;
+    c.je = w.ke;
+    const int tap = w.kb / a.c_steps;
+    c.cb = w.kb - tap * a.c_steps;
+    c.r = tap / a.S;
+    c.s = tap - c.r * a.S;
+    const int mt = w.tile / a.n_tiles;
     const int m = mt * MT + row;
-    c.valid = tile < a.num_tiles && m < a.m_total;
+    c.valid = u < a.num_units && m < a.m_total;
     const int mm = c.valid ? m : 0;
     const int pq = a.P * a.Q;
     const int n = mm / pq;
@@ -247,8 +288,8 @@ __device__ __forceinline__ void cursor_load(const LoadCursor &c, const IgemmArgs
 }
 
 __device__ __forceinline__ void cursor_advance(LoadCursor &c, const IgemmArgs &a, int row) {
-    if (++c.j == a.k_steps) {
-        cursor_set_tile(c, a, c.tile + gridDim.x, row);
+    if (++c.j == c.je) {
+        cursor_set_unit(c, a, c.u + gridDim.x, row);
         return;
     }
     if (++c.cb == a.c_steps) {
@@ -295,11 +336,15 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int my_tiles = blockIdx.x < a.num_tiles ? (a.num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-    const int total = my_tiles * a.k_steps;  // (tile, k-step) items of this CTA
-    // TMA path: each CTA walks the reduction starting at its own k-step, so
-    // the SMs do not all fetch the same filter block at the same moment (any
-    // order is exact: a group is any run of at most 1024 products)
+    int total = 0;  // k-steps of all units of this CTA
+    for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
+        const Unit w = unit_at(u, a.full_units, a.splits, a.k_steps);
+        total += w.ke - w.kb;
+    }
+    // TMA path: each CTA walks the reduction of a whole tile starting at its
+    // own k-step, so the SMs do not all fetch the same filter block at the
+    // same moment (any order is exact: a group is any run of at most 1024
+    // products)
     const int rot = kTma ? (int)(((int64_t)blockIdx.x * 7) % a.k_steps) : 0;
 
     if (threadIdx.x == 0) {
@@ -373,17 +418,20 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
         const uint32_t row_off = (uint32_t)row * 128u;
         const uint32_t swz = (uint32_t)(row & 7);
         LoadCursor cur;
-        cursor_set_tile(cur, a, blockIdx.x, row);
+        cursor_set_unit(cur, a, blockIdx.x, row);
         uint4 pf[PREFETCH][4];
 #pragma unroll
         for (int d = 0; d < PREFETCH; ++d) {
-            if (cur.tile < a.num_tiles) {
+            if (cur.u < a.num_units) {
                 cursor_load(cur, a, pf[d]);
                 cursor_advance(cur, a, row);
             }
         }
         Ring<ST> rg;
-        int b_tile = blockIdx.x, b_j = 0;  // filter block cursor (thread 0 only)
+        // filter block cursor (thread 0 only): unit b_u, k-step b_j < b_je
+        int b_u = blockIdx.x;
+        Unit bw = unit_at(b_u < a.num_units ? b_u : 0, a.full_units, a.splits, a.k_steps);
+        int b_j = bw.kb, b_je = bw.ke;
         int64_t b_issued = 0;
         bool ok = true;
         for (int it = 0; it < total && ok; it += PREFETCH) {
@@ -393,7 +441,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 uint4 v[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) v[i] = pf[d][i];
-                if (cur.tile < a.num_tiles) {  // keep PREFETCH items in flight
+                if (cur.u < a.num_units) {  // keep PREFETCH items in flight
                     cursor_load(cur, a, pf[d]);
                     cursor_advance(cur, a, row);
                 }
@@ -404,13 +452,15 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 if (threadIdx.x == 0) {
                     const uint32_t bar = ptx::smem_addr(&ctl->full[rg.idx]);
                     ptx::mbar_arrive_expect_tx(bar, B_BYTES);
-                    const int nt = b_tile % a.n_tiles;
+                    const int nt = bw.tile % a.n_tiles;
                     const uint8_t *src = a.wp + ((size_t)nt * a.k_steps + b_j) * (size_t)B_BYTES;
                     ptx::bulk_copy_g2s(b_smem + rg.idx * B_BYTES, src, B_BYTES, bar);
                     ++b_issued;
-                    if (++b_j == a.k_steps) {
-                        b_j = 0;
-                        b_tile += gridDim.x;
+                    if (++b_j == b_je) {
+                        b_u += gridDim.x;
+                        bw = unit_at(b_u < a.num_units ? b_u : 0, a.full_units, a.splits, a.k_steps);
+                        b_j = bw.kb;
+                        b_je = bw.ke;
                     }
                 }
                 const uint32_t dst = a_smem + rg.idx * A_BYTES + row_off;
@@ -439,10 +489,13 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
             Ring<ST> rg;
             uint32_t gi = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
-                for (int g = 0; g < a.groups && ok; ++g) {
-                    const int js = (int)(((int64_t)g * a.k_steps) / a.groups);
-                    const int je = (int)(((int64_t)(g + 1) * a.k_steps) / a.groups);
+            for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
+                const Unit w = unit_at(u, a.full_units, a.splits, a.k_steps);
+                const int kn = w.ke - w.kb;
+                const int ng = groups_of(kn);
+                for (int g = 0; g < ng && ok; ++g) {
+                    const int js = (int)(((int64_t)g * kn) / ng);
+                    const int je = (int)(((int64_t)(g + 1) * kn) / ng);
                     const uint32_t slot = gi % NSLOT;
                     const uint32_t aph = (gi / NSLOT) & 1u;
                     if (!wait_phase(ptx::smem_addr(&ctl->acc_empty[slot]), aph ^ 1u, abort_flag, limit, a.status)) {
@@ -488,17 +541,21 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
             int64_t issued = 0;
             bool ok = true;
             const int pq = a.P * a.Q;
-            for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
-                const int m0 = (tile / a.n_tiles) * MT;
+            for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
+                const Unit wu = unit_at(u, a.full_units, a.splits, a.k_steps);
+                const int kn = wu.ke - wu.kb;
+                const int urot = wu.split < 0 ? rot : 0;
+                const int m0 = (wu.tile / a.n_tiles) * MT;
                 const int n0 = m0 / pq;
                 const int rem = m0 - n0 * pq;
                 const int p0 = rem / a.Q;
                 const int q0 = rem - p0 * a.Q;
                 const int w0 = q0 * a.str_w - a.pad_w;
                 const int h0 = p0 * a.str_h - a.pad_h;
-                for (int j = 0; j < a.k_steps; ++j) {
-                    int jr = j + rot;
-                    if (jr >= a.k_steps) jr -= a.k_steps;
+                for (int j = 0; j < kn; ++j) {
+                    int jr = j + urot;
+                    if (jr >= kn) jr -= kn;
+                    jr += wu.kb;
                     const int tap = jr / a.c_steps;
                     const int cb = jr - tap * a.c_steps;
                     const int r = tap / a.S;
@@ -523,12 +580,16 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
             Ring<ST> rb;
             int64_t issued = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
-                const int nt = tile % a.n_tiles;
+            for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
+                const Unit wu = unit_at(u, a.full_units, a.splits, a.k_steps);
+                const int kn = wu.ke - wu.kb;
+                const int urot = wu.split < 0 ? rot : 0;
+                const int nt = wu.tile % a.n_tiles;
                 const uint8_t *blk = a.wp + (size_t)nt * a.k_steps * (size_t)B_BYTES;
-                for (int j = 0; j < a.k_steps; ++j) {
-                    int jr = j + rot;
-                    if (jr >= a.k_steps) jr -= a.k_steps;
+                for (int j = 0; j < kn; ++j) {
+                    int jr = j + urot;
+                    if (jr >= kn) jr -= kn;
+                    jr += wu.kb;
                     if (!wait_phase(ptx::smem_addr(&ctl->empty[rb.idx]), rb.phase ^ 1u, abort_flag, limit,
                                     a.status)) {
                         ok = false;
@@ -553,9 +614,12 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
         const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)col0;
         uint32_t gi = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
-            const int mt = tile / a.n_tiles;
-            const int nt = tile - mt * a.n_tiles;
+        const int wpos = warp - FIRST_EPI_WARP;  // this warp's part of the tile (0..7)
+        for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
+            const Unit wu = unit_at(u, a.full_units, a.splits, a.k_steps);
+            const int ng = groups_of(wu.ke - wu.kb);
+            const int mt = wu.tile / a.n_tiles;
+            const int nt = wu.tile - mt * a.n_tiles;
             const int m = mt * MT + row;
             const bool valid = m < a.m_total;
             int64_t yoff = 0;
@@ -570,7 +634,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
             int32_t acc[HALF];
 #pragma unroll
             for (int i = 0; i < HALF; ++i) acc[i] = 0;
-            for (int g = 0; g < a.groups; ++g) {
+            for (int g = 0; g < ng; ++g) {
                 const uint32_t slot = gi % NSLOT;
                 const uint32_t aph = (gi / NSLOT) & 1u;
                 // tcgen05.ld is warp-collective: the whole warp proceeds or stops together
@@ -593,6 +657,17 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 ++gi;
             }
             if (!ok) break;
+            if (wu.split >= 0) {
+                // one run of a cut tile: its raw int32 sums go to the
+                // workspace, [cut tile][split][row][column]; the reduction
+                // kernel adds the runs and finishes the tile
+                int4 *dst = reinterpret_cast<int4 *>(
+                    a.tail_part + (((size_t)(wu.tile - a.full_units) * a.splits + wu.split) * MT + row) * NT + col0);
+#pragma unroll
+                for (int c4 = 0; c4 < HALF / 4; ++c4)
+                    __stcg(dst + c4, make_int4(acc[4 * c4], acc[4 * c4 + 1], acc[4 * c4 + 2], acc[4 * c4 + 3]));
+                continue;
+            }
             // epilogue arithmetic, once: + bias[k] (int32 wrap-around), then ReLU
             if (a.bias || a.relu) {
                 const int kb = nt * NT + col0;
@@ -757,6 +832,60 @@ __global__ void igemm_pack_filter_kernel(const int8_t *w, int64_t ws0, int64_t w
     }
 }
 
+// ---------------------------------------------------------------- cut tiles
+// Adds the runs of every cut tile (raw int32 sums in the workspace, [tile]
+// [split][MT rows][nt_cols columns]), then applies bias, ReLU and the int8
+// requantisation like the main epilogue and stores the tile.  One thread per
+// 4 columns of a row: reads of the partial sums and channels-contiguous
+// outputs are coalesced.
+__global__ void __launch_bounds__(256) igemm_split_reduce_kernel(const int32_t *part, int32_t tiles, int32_t splits,
+                                                                 int32_t n_tiles, int32_t nt_cols, int32_t m_total,
+                                                                 int32_t K, int32_t P, int32_t Q, int64_t ys_n,
+                                                                 int64_t ys_k, int64_t ys_p, int64_t ys_q, void *y,
+                                                                 int32_t out_int8, int32_t out_shift,
+                                                                 const int32_t *bias, int32_t relu) {
+    const int q4n = nt_cols / 4;
+    const int64_t total = (int64_t)tiles * MT * q4n;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int c4 = (int)(idx % q4n);
+        const int64_t t = idx / q4n;
+        const int row = (int)(t % MT);
+        const int tile = (int)(t / MT);
+        const int mt = tile / n_tiles;
+        const int nt = tile - mt * n_tiles;
+        const int m = mt * MT + row;
+        if (m >= m_total) continue;
+        int32_t v[4] = {0, 0, 0, 0};
+        for (int sp = 0; sp < splits; ++sp) {
+            const int4 x = __ldcg(reinterpret_cast<const int4 *>(
+                part + (((size_t)tile * splits + sp) * MT + row) * nt_cols + c4 * 4));
+            v[0] += x.x;
+            v[1] += x.y;
+            v[2] += x.z;
+            v[3] += x.w;
+        }
+        const int pq = P * Q;
+        const int n = m / pq;
+        const int rem = m - n * pq;
+        const int p = rem / Q;
+        const int q = rem - p * Q;
+        const int64_t yoff = (int64_t)n * ys_n + (int64_t)p * ys_p + (int64_t)q * ys_q;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int k = nt * nt_cols + c4 * 4 + e;
+            if (k >= K) continue;
+            int32_t val = v[e];
+            if (bias) val = (int32_t)((uint32_t)val + (uint32_t)__ldg(bias + k));
+            if (relu) val = max(val, 0);
+            if (out_int8)
+                static_cast<int8_t *>(y)[yoff + (int64_t)k * ys_k] = requant_i8(val, out_shift);
+            else
+                static_cast<int32_t *>(y)[yoff + (int64_t)k * ys_k] = val;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- image repack
 // Channels-last copy of an image with arbitrary strides: xp[((n*H+h)*W+w)*c16 + c],
 // channels C..c16-1 zero.  One thread writes 16 channels of one pixel; threads
@@ -792,6 +921,10 @@ __global__ void igemm_pack_image_kernel(const int8_t *x, int64_t xs0, int64_t xs
 }
 
 inline int64_t align256(int64_t v) { return (v + 255) & ~255LL; }
+
+constexpr int64_t kSplitMinKSteps = 64;  // only reductions at least this long are cut
+constexpr int64_t kMinSplitSteps = 16;   // k-steps of the shortest run of a cut tile
+constexpr int64_t kMaxSplits = 32;
 
 template <int NT, bool kTma>
 conv_status launch_conv(const IgemmArgs &a, int grid, cudaStream_t st) {
@@ -933,7 +1066,33 @@ void igemm_plan(const ConvGeom &g, const void *x_dev, IgemmPlan *pl) {
     pl->m_tiles = (g.N * g.P * g.Q + MT - 1) / MT;
     pl->wpack_bytes = (size_t)align256(pl->n_tiles * pl->k_steps * pl->n_tile * (int64_t)(KS * 2));
     pl->xpack_bytes = pl->pack_x ? (size_t)align256(g.N * g.H * g.W * pl->c16) : 0;
-    pl->workspace_bytes = pl->wpack_bytes + pl->xpack_bytes;
+    // One CTA per SM walks the tiles.  With fewer tiles than SMs and long
+    // reductions (the weight gradient's shape: few output tiles, a reduction
+    // over every pixel of the batch) the tiles are cut along the reduction
+    // into as many runs as keep the SMs busy, each at least kMinSplitSteps
+    // long; the int32 partial sums are added by the last run to finish.
+    const int64_t tiles = pl->m_tiles * pl->n_tiles;
+    const int64_t sms = device_sm_count();
+    pl->splits = 1;
+    if (tiles > 0 && tiles < sms && pl->k_steps >= kSplitMinKSteps) {
+        int64_t sp = sms / tiles;
+        if (sp > pl->k_steps / kMinSplitSteps) sp = pl->k_steps / kMinSplitSteps;
+        if (sp > kMaxSplits) sp = kMaxSplits;
+        if (sp >= 2) pl->splits = sp;
+    }
+    pl->full_units = pl->splits > 1 ? 0 : tiles;
+    pl->num_units = pl->splits > 1 ? tiles * pl->splits : tiles;
+    pl->grid = pl->num_units < sms ? pl->num_units : sms;
+    // workspace: [filter blocks][partial sums][image copy]
+    size_t off = pl->wpack_bytes;
+    pl->tail_part_off = off;
+    pl->tail_part_bytes = 0;
+    if (pl->splits > 1) {
+        pl->tail_part_bytes = (size_t)align256(tiles * pl->splits * MT * pl->n_tile * 4);
+        off += pl->tail_part_bytes;
+    }
+    pl->xpack_off = off;
+    pl->workspace_bytes = off + pl->xpack_bytes;
 }
 
 conv_status igemm_pack_filter_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *w, void *workspace,
@@ -958,7 +1117,7 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
     uint8_t *wp = static_cast<uint8_t *>(workspace);
     IgemmArgs a;
     if (pl.pack_x) {
-        int8_t *xp = reinterpret_cast<int8_t *>(wp + pl.wpack_bytes);
+        int8_t *xp = reinterpret_cast<int8_t *>(wp + pl.xpack_off);
         const int64_t total = g.N * g.H * g.W * (pl.c16 / 16);
         int64_t blocks = (total + 255) / 256;
         if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
@@ -987,13 +1146,16 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
     a.c16 = (int32_t)pl.c16;
     a.c_steps = (int32_t)pl.c_steps;
     a.k_steps = (int32_t)pl.k_steps;
-    a.groups = (int32_t)((pl.k_steps + MAX_GROUP_STEPS - 1) / MAX_GROUP_STEPS);
     a.pad_h = (int32_t)g.pad_h; a.pad_w = (int32_t)g.pad_w;
     a.str_h = (int32_t)g.str_h; a.str_w = (int32_t)g.str_w;
     a.dil_h = (int32_t)g.dil_h; a.dil_w = (int32_t)g.dil_w;
     a.m_total = (int32_t)(g.N * g.P * g.Q);
     a.n_tiles = (int32_t)pl.n_tiles;
     a.num_tiles = (int32_t)(pl.m_tiles * pl.n_tiles);
+    a.full_units = (int32_t)pl.full_units;
+    a.splits = (int32_t)pl.splits;
+    a.num_units = (int32_t)pl.num_units;
+    a.tail_part = pl.splits > 1 ? reinterpret_cast<int32_t *>(wp + pl.tail_part_off) : nullptr;
     a.relu = g.relu ? 1 : 0;
     a.y_vec = (!g.out_int8 && g.ys[1] == 1 && (g.K % 4) == 0 && ((uintptr_t)y % 16) == 0 && (g.ys[0] % 4) == 0 &&
                (g.ys[2] % 4) == 0 && (g.ys[3] % 4) == 0)
@@ -1004,11 +1166,22 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
     a.status = device_status_word();
     if (!a.status) return CONV_ERR_CUDA;
     if (a.num_tiles == 0) return CONV_OK;
-    const int grid = a.num_tiles < sms ? a.num_tiles : sms;
+    const int grid = (int)pl.grid;
     const bool tma = !pl.register_loads && encode_im2col_map(g, a.x, a.xs_n, a.xs_h, a.xs_w,
                                                              pl.pack_x ? pl.c16 : g.C, &a.tmap_x);
-    if (tma) return pl.n_tile == 256 ? launch_conv<256, true>(a, grid, st) : launch_conv<128, true>(a, grid, st);
-    return pl.n_tile == 256 ? launch_conv<256, false>(a, grid, st) : launch_conv<128, false>(a, grid, st);
+    conv_status rc;
+    if (tma)
+        rc = pl.n_tile == 256 ? launch_conv<256, true>(a, grid, st) : launch_conv<128, true>(a, grid, st);
+    else
+        rc = pl.n_tile == 256 ? launch_conv<256, false>(a, grid, st) : launch_conv<128, false>(a, grid, st);
+    if (rc || pl.splits <= 1) return rc;
+    const int64_t items = (int64_t)a.num_tiles * MT * (pl.n_tile / 4);
+    int64_t blocks = (items + 255) / 256;
+    if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
+    igemm_split_reduce_kernel<<<(unsigned)blocks, 256, 0, st>>>(
+        a.tail_part, a.num_tiles, a.splits, a.n_tiles, (int32_t)pl.n_tile, a.m_total, a.K, a.P, a.Q, a.ys_n, a.ys_k,
+        a.ys_p, a.ys_q, a.y, a.out_int8, a.out_shift, a.bias, a.relu);
+    return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
 }  // namespace i8c

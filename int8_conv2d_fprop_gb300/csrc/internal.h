@@ -76,6 +76,12 @@ struct IgemmPlan {
     int64_t m_tiles;        // ceil(N*P*Q / kIgemmMTile)
     size_t wpack_bytes;     // repacked filter
     size_t xpack_bytes;     // channels-last image copy (0 if not needed)
+    // Work split: with few tiles and long reductions each tile is cut into
+    // `splits` runs of k-steps computed by different CTAs (splits == 1: whole
+    // tiles, full_units == num_units == tiles).
+    int64_t full_units, splits, num_units, grid;
+    size_t tail_part_off, tail_part_bytes;  // int32 partial sums of the cut tiles
+    size_t xpack_off;       // image copy, after the filter and the partial sums
     size_t workspace_bytes; // total, each part 256-byte aligned
 };
 
