@@ -833,12 +833,13 @@ __global__ void igemm_pack_filter_kernel(const int8_t *w, int64_t ws0, int64_t w
 }
 
 // ---------------------------------------------------------------- cut tiles
-// Adds the runs of every cut tile (raw int32 sums in the workspace, [tile]
-// [split][MT rows][nt_cols columns]), then applies bias, ReLU and the int8
+// Adds the runs of every cut tile (tiles tile0.. of the grid walk; raw int32
+// sums in the workspace, [cut tile][split][MT rows][nt_cols columns]), then applies bias, ReLU and the int8
 // requantisation like the main epilogue and stores the tile.  One thread per
 // 4 columns of a row: reads of the partial sums and channels-contiguous
 // outputs are coalesced.
-__global__ void __launch_bounds__(256) igemm_split_reduce_kernel(const int32_t *part, int32_t tiles, int32_t splits,
+__global__ void __launch_bounds__(256) igemm_split_reduce_kernel(const int32_t *part, int32_t tile0,
+                                                                 int32_t tiles, int32_t splits,
                                                                  int32_t n_tiles, int32_t nt_cols, int32_t m_total,
                                                                  int32_t K, int32_t P, int32_t Q, int64_t ys_n,
                                                                  int64_t ys_k, int64_t ys_p, int64_t ys_q, void *y,
@@ -851,7 +852,8 @@ __global__ void __launch_bounds__(256) igemm_split_reduce_kernel(const int32_t *
         const int c4 = (int)(idx % q4n);
         const int64_t t = idx / q4n;
         const int row = (int)(t % MT);
-        const int tile = (int)(t / MT);
+        const int ct = (int)(t / MT);   // cut tile
+        const int tile = tile0 + ct;
         const int mt = tile / n_tiles;
         const int nt = tile - mt * n_tiles;
         const int m = mt * MT + row;
@@ -859,7 +861,7 @@ __global__ void __launch_bounds__(256) igemm_split_reduce_kernel(const int32_t *
         int32_t v[4] = {0, 0, 0, 0};
         for (int sp = 0; sp < splits; ++sp) {
             const int4 x = __ldcg(reinterpret_cast<const int4 *>(
-                part + (((size_t)tile * splits + sp) * MT + row) * nt_cols + c4 * 4));
+                part + (((size_t)ct * splits + sp) * MT + row) * nt_cols + c4 * 4));
             v[0] += x.x;
             v[1] += x.y;
             v[2] += x.z;
@@ -1081,14 +1083,15 @@ void igemm_plan(const ConvGeom &g, const void *x_dev, IgemmPlan *pl) {
         if (sp >= 2) pl->splits = sp;
     }
     pl->full_units = pl->splits > 1 ? 0 : tiles;
-    pl->num_units = pl->splits > 1 ? tiles * pl->splits : tiles;
+    const int64_t cut_tiles = tiles - pl->full_units;
+    pl->num_units = pl->full_units + cut_tiles * pl->splits;
     pl->grid = pl->num_units < sms ? pl->num_units : sms;
     // workspace: [filter blocks][partial sums][image copy]
     size_t off = pl->wpack_bytes;
     pl->tail_part_off = off;
     pl->tail_part_bytes = 0;
     if (pl->splits > 1) {
-        pl->tail_part_bytes = (size_t)align256(tiles * pl->splits * MT * pl->n_tile * 4);
+        pl->tail_part_bytes = (size_t)align256(cut_tiles * pl->splits * MT * pl->n_tile * 4);
         off += pl->tail_part_bytes;
     }
     pl->xpack_off = off;
@@ -1175,12 +1178,13 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
     else
         rc = pl.n_tile == 256 ? launch_conv<256, false>(a, grid, st) : launch_conv<128, false>(a, grid, st);
     if (rc || pl.splits <= 1) return rc;
-    const int64_t items = (int64_t)a.num_tiles * MT * (pl.n_tile / 4);
+    const int32_t cut_tiles = a.num_tiles - a.full_units;
+    const int64_t items = (int64_t)cut_tiles * MT * (pl.n_tile / 4);
     int64_t blocks = (items + 255) / 256;
     if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
     igemm_split_reduce_kernel<<<(unsigned)blocks, 256, 0, st>>>(
-        a.tail_part, a.num_tiles, a.splits, a.n_tiles, (int32_t)pl.n_tile, a.m_total, a.K, a.P, a.Q, a.ys_n, a.ys_k,
-        a.ys_p, a.ys_q, a.y, a.out_int8, a.out_shift, a.bias, a.relu);
+        a.tail_part, a.full_units, cut_tiles, a.splits, a.n_tiles, (int32_t)pl.n_tile, a.m_total, a.K, a.P, a.Q,
+        a.ys_n, a.ys_k, a.ys_p, a.ys_q, a.y, a.out_int8, a.out_shift, a.bias, a.relu);
     return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
