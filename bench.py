@@ -511,7 +511,8 @@ def run_extension(args):
         bound = "tensor" if tensor else "alu"
         peak = bf16 if tensor else 152 * IMAD_PER_SM_CLK * 2 * 2.07e9 / 1e12
         unit = "TFLOP/s" if tensor else "TOPS"
-        extra["route"] = "tensor cores (forward convolution of dY)" if tensor else "CUDA cores"
+        extra["route"] = ("tensor cores (a forward convolution of dY per residue class of the stride)"
+                          if tensor else "CUDA cores")
     else:  # wgrad
         dy = synth.int8_uniform(cfg.seed, 3, cfg.y_dims)
         dyf, dys = synth.place(dy, cfg.y_layout)

@@ -295,15 +295,19 @@ conv_status conv_fprop_static_workspace(const conv_tensor_desc *x, const int8_t 
  * K*R*S*2^14 <= 2^31-1 and wgrad N*P*Q*2^14 <= 2^31-1, else
  * CONV_ERR_OVERFLOW_RISK.
  *
- * conv_dgrad with stride 1 and padding no wider than the filter's reach
- * (pre, post <= dilation*(taps-1)) runs on the tensor cores as a forward
- * convolution of dY; conv_wgrad runs on the tensor cores as a forward
- * convolution of the image (batch and channel dims exchanged) by dY (its
- * batch as channels, its pixels as taps) when the tensor-core kernel can
- * express it.  Those routes need the workspace the *_workspace_size call
- * reports (256-byte aligned, caller-owned; for wgrad it holds dY repacked to
- * f16 blocks, about 2*K*P*Q*ceil(N/64)*64 bytes, plus the int32 partial sums
- * of the reduction split over the SMs).  Other calls, and algo
+ * conv_dgrad runs on the tensor cores as stride_h*stride_w forward
+ * convolutions of dY, one per residue class (h mod stride_h, w mod
+ * stride_w) of dX's pixels, each by the filter taps that reach that class
+ * (taken backwards, K and C exchanged) with stride 1, one after the other on
+ * `stream` in one workspace; a class no tap reaches is written with zeros.
+ * More than 64 classes take the CUDA-core kernel.  conv_wgrad runs on the
+ * tensor cores as a forward convolution of the image (batch and channel
+ * dims exchanged) by dY (its batch as channels, its pixels as taps) when the
+ * tensor-core kernel can express it.  Those routes need the workspace the
+ * *_workspace_size call reports (256-byte aligned, caller-owned; for dgrad
+ * it holds the largest class's filter repacked to f16 blocks, for wgrad dY
+ * repacked to f16 blocks, about 2*K*P*Q*ceil(N/64)*64 bytes, plus the int32
+ * partial sums of the reduction split over the SMs).  Other calls, and algo
  * DIRECT_GENERIC, run CUDA-core kernels and need none; IMPLICIT_GEMM on a
  * call that cannot take the tensor cores returns CONV_ERR_ALIGNMENT.
  * Pointers are device pointers on the current device, outputs must not

@@ -4,12 +4,20 @@
 //
 // dgrad, dX[n,c,h,w] = sum over k, r, s of dY[n,k,p,q] * W[k,c,r',s'] with
 // p = (h + pre_h - r*dil_h) / stride_h exact and in range (q likewise):
-//  * stride 1, and padding no wider than the filter's reach (pre, post <=
-//    dil*(taps-1)): a forward convolution of dY by the filter with K and C
-//    exchanged, the taps reversed (the other convolution mode) and the
-//    padding dil*(taps-1) - pre before, dil*(taps-1) - post after.  It runs on
-//    the tensor-core kernel, with its filter repack and workspace.
-//  * otherwise: a CUDA-core kernel, one thread per dX element.
+//  * split by the residues (rho_h, rho_w) of h and w modulo the stride.  The
+//    pixels h = rho + i*stride of one residue are reached only by the taps
+//    with r*dil = rho + pre (mod stride), r = r0 + t*delta (delta =
+//    stride / gcd(dil, stride)), and p = i + c0 - t*e with e = dil*delta /
+//    stride and c0 = (rho + pre - r0*dil) / stride.  So each residue class is
+//    a stride-1 forward convolution of dY, dilation e, pre-padding
+//    (T-1)*e - c0, by the filter's taps r0, r0 + delta, ... taken backwards,
+//    K and C exchanged, written into dX through its strides times the stride.
+//    With stride 1 there is one class, the whole filter reversed.  Each class
+//    runs on the tensor-core kernel with its own filter repack, one after the
+//    other in one workspace; a class no tap reaches is zero-filled.
+//  * otherwise (a class the tensor-core kernel cannot express, more than
+//    kMaxDgradPhases classes, or DIRECT_GENERIC): a CUDA-core kernel, one
+//    thread per dX element.
 // wgrad, dW[k,c,r',s'] = sum over n, p, q of dY[n,k,p,q] * X[n,c,h,w]:
 //  * a forward convolution whose image is X with its batch and channel dims
 //    exchanged ([C][N][H][W]), whose filter is dY ([K][N][P][Q]: the batch
@@ -22,6 +30,9 @@
 //    element, the lanes splitting the n, p, q sum (int32 partial sums, exact
 //    by the validator's bound, added across the warp with shuffles).
 #include <cuda_runtime.h>
+
+#include <numeric>
+#include <vector>
 
 #include "internal.h"
 
@@ -133,37 +144,108 @@ int grid_for(int64_t items, int per_block) {
     return (int)(blocks < 1 ? 1 : blocks);
 }
 
-// dgrad as a forward convolution of dY (see the top of the file), when the
-// stride is 1 and the padding within the filter's reach; fills g and returns
-// true then.
-bool dgrad_as_fprop(const conv_tensor_desc *dy, const conv_tensor_desc *w, const conv_tensor_desc *dx,
-                    const conv_fprop_params *p, ConvGeom *g) {
-    if (p->stride[0] != 1 || p->stride[1] != 1) return false;
-    const int64_t reach_h = p->dilation[0] * (w->dims[2] - 1), reach_w = p->dilation[1] * (w->dims[3] - 1);
-    if (p->pre_padding[0] > reach_h || p->post_padding[0] > reach_h || p->pre_padding[1] > reach_w ||
-        p->post_padding[1] > reach_w)
-        return false;
-    g->N = dy->dims[0]; g->C = dy->dims[1]; g->H = dy->dims[2]; g->W = dy->dims[3];
-    g->K = dx->dims[1]; g->R = w->dims[2]; g->S = w->dims[3];
-    g->P = dx->dims[2]; g->Q = dx->dims[3];
-    unit_strides(dy, g->xs);
-    int64_t fs[4];
+// More residue classes than this (stride_h * stride_w) take the CUDA-core
+// kernel: each class costs a filter repack and a launch.
+constexpr int64_t kMaxDgradPhases = 64;
+
+__global__ void __launch_bounds__(256) zero_view_kernel(int32_t *y, int64_t N, int64_t C, int64_t P, int64_t Q,
+                                                        int64_t s0, int64_t s1, int64_t s2, int64_t s3) {
+    const int64_t total = N * C * P * Q;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t q = i % Q, t = i / Q, p = t % P, t2 = t / P, c = t2 % C, n = t2 / C;
+        y[n * s0 + c * s1 + p * s2 + q * s3] = 0;
+    }
+}
+
+// One residue class (rho_h, rho_w) of dX's pixels under the stride, as a
+// forward convolution of dY (see the top of the file).
+struct DgradPhase {
+    ConvGeom g;        // image dY, filter the class's taps, output the class's dX pixels
+    IgemmPlan pl;
+    int64_t w_origin;  // element offset in W of the class filter's tap (0, 0)
+    int64_t y_origin;  // element offset in dX of the class's first pixel
+    bool taps;         // false: no tap reaches the class, its pixels are zero
+};
+
+// The taps of one axis that reach residue rho: r = r0 + t*delta, t < T.
+// Returns T (0 when none), with r0, delta, the class's dilation e and its
+// pre-padding.
+int64_t phase_axis(int64_t rho, int64_t pre, int64_t str, int64_t dil, int64_t taps, int64_t *r0, int64_t *delta,
+                   int64_t *e, int64_t *pad) {
+    const int64_t gcd = std::gcd(dil, str);
+    *delta = str / gcd;
+    *e = dil / gcd;
+    // r*dil = rho + pre (mod str) has its solutions every delta taps, the
+    // first below delta when there are any
+    for (int64_t r = 0; r < *delta && r < taps; ++r) {
+        if ((r * dil - rho - pre) % str != 0) continue;
+        const int64_t T = (taps - r + *delta - 1) / *delta;
+        const int64_t c0 = (rho + pre - r * dil) / str;  // exact
+        *r0 = r;
+        *pad = (T - 1) * *e - c0;
+        return T;
+    }
+    return 0;
+}
+
+// dgrad as stride_h * stride_w forward convolutions of dY, one per residue
+// class; returns false when the tensor-core kernel cannot take one of them.
+bool dgrad_phases(const conv_tensor_desc *dy, const conv_tensor_desc *w, const conv_tensor_desc *dx,
+                  const conv_fprop_params *p, std::vector<DgradPhase> *out) {
+    const int64_t sh = p->stride[0], sw = p->stride[1];
+    if (sh * sw > kMaxDgradPhases) return false;
+    int64_t ys[4], fs[4], xs[4];
+    unit_strides(dy, ys);
     unit_strides(w, fs);
-    // the filter with its first two dims exchanged: [C][K][R][S]
-    g->ws[0] = w->dims[1] > 1 ? fs[1] : 0;
-    g->ws[1] = w->dims[0] > 1 ? fs[0] : 0;
-    g->ws[2] = fs[2];
-    g->ws[3] = fs[3];
-    unit_strides(dx, g->ys);
-    g->pad_h = reach_h - p->pre_padding[0];
-    g->pad_w = reach_w - p->pre_padding[1];
-    g->str_h = g->str_w = 1;
-    g->dil_h = p->dilation[0];
-    g->dil_w = p->dilation[1];
-    g->mode = p->mode ? 0 : 1;  // the taps run backwards
-    g->bias = g->relu = g->out_int8 = false;
-    g->out_shift = 0;
-    return igemm_supported(*g);
+    unit_strides(dx, xs);
+    const int64_t R = w->dims[2], S = w->dims[3], H = dx->dims[2], W = dx->dims[3];
+    for (int64_t rh = 0; rh < sh && rh < H; ++rh) {
+        for (int64_t rw = 0; rw < sw && rw < W; ++rw) {
+            DgradPhase ph = {};
+            ConvGeom &g = ph.g;
+            // output: the class's pixels of dX, [N][C][P'][Q']
+            g.N = dy->dims[0];
+            g.K = dx->dims[1];
+            g.P = (H - rh + sh - 1) / sh;
+            g.Q = (W - rw + sw - 1) / sw;
+            g.ys[0] = xs[0]; g.ys[1] = xs[1]; g.ys[2] = sh * xs[2]; g.ys[3] = sw * xs[3];
+            ph.y_origin = rh * xs[2] + rw * xs[3];
+            int64_t r0 = 0, dh = 1, eh = 1, padh = 0, s0 = 0, dw = 1, ew = 1, padw = 0;
+            const int64_t th = phase_axis(rh, p->pre_padding[0], sh, p->dilation[0], R, &r0, &dh, &eh, &padh);
+            const int64_t tw = phase_axis(rw, p->pre_padding[1], sw, p->dilation[1], S, &s0, &dw, &ew, &padw);
+            ph.taps = th > 0 && tw > 0 && dy->dims[1] > 0;
+            if (ph.taps) {
+                // image: dY, its K channels the reduction
+                g.C = dy->dims[1]; g.H = dy->dims[2]; g.W = dy->dims[3];
+                for (int i = 0; i < 4; ++i) g.xs[i] = ys[i];
+                // filter [C][K][T_h][T_w]: tap (u, v) is r = r0 + (T_h-1-u)*delta_h
+                // (s likewise), stored at r' = r or R-1-r by the mode
+                g.R = th; g.S = tw;
+                g.ws[0] = fs[1];
+                g.ws[1] = fs[0];
+                const int64_t rl = r0 + (th - 1) * dh, sl = s0 + (tw - 1) * dw;  // the taps of u, v = 0
+                if (p->mode == CONV_CONVOLUTION) {
+                    ph.w_origin = (R - 1 - rl) * fs[2] + (S - 1 - sl) * fs[3];
+                    g.ws[2] = dh * fs[2];
+                    g.ws[3] = dw * fs[3];
+                } else {
+                    ph.w_origin = rl * fs[2] + sl * fs[3];
+                    g.ws[2] = -dh * fs[2];
+                    g.ws[3] = -dw * fs[3];
+                }
+                g.pad_h = padh; g.pad_w = padw;
+                g.str_h = g.str_w = 1;
+                g.dil_h = eh; g.dil_w = ew;
+                g.mode = CONV_CROSS_CORRELATION;
+                g.bias = g.relu = g.out_int8 = false;
+                g.out_shift = 0;
+                if (!igemm_supported(g)) return false;
+            }
+            out->push_back(ph);
+        }
+    }
+    return true;
 }
 
 // wgrad as a forward convolution (see the top of the file); fills g and the
@@ -216,16 +298,25 @@ conv_status plan_wgrad(const conv_tensor_desc *x, const void *x_dev, const conv_
     return CONV_OK;
 }
 
-// Plans a dgrad call: *tensor and *pl describe the tensor-core route when it
-// is taken.
+// Plans a dgrad call: *tensor tells whether the residue classes in *ph run on
+// the tensor cores, *ws_bytes the workspace they share (the largest class's).
 conv_status plan_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const conv_tensor_desc *w,
-                       const conv_tensor_desc *dx, const conv_fprop_params *p, ConvGeom *g, bool *tensor,
-                       IgemmPlan *pl) {
+                       const conv_tensor_desc *dx, const conv_fprop_params *p, std::vector<DgradPhase> *ph,
+                       bool *tensor, size_t *ws_bytes) {
     conv_status st = validate_dgrad(dy, w, dx, p);
     if (st) return st;
-    *tensor = p->algo != CONV_ALGO_DIRECT_GENERIC && dgrad_as_fprop(dy, w, dx, p, g);
+    *tensor = p->algo != CONV_ALGO_DIRECT_GENERIC && dgrad_phases(dy, w, dx, p, ph);
     if (p->algo == CONV_ALGO_IMPLICIT_GEMM && !*tensor) return CONV_ERR_ALIGNMENT;
-    if (*tensor) igemm_plan(*g, dy_dev, pl);
+    *ws_bytes = 0;
+    if (!*tensor) return CONV_OK;
+    for (DgradPhase &c : *ph) {
+        if (!c.taps) continue;
+        igemm_plan(c.g, dy_dev, &c.pl);
+        // a class whose window starts inside dY (negative padding) gathers
+        // with register loads, which bounds-check every pixel
+        if (c.g.pad_h < 0 || c.g.pad_w < 0) c.pl.register_loads = true;
+        if (c.g.N > 0 && c.pl.workspace_bytes > *ws_bytes) *ws_bytes = c.pl.workspace_bytes;
+    }
     return CONV_OK;
 }
 
@@ -239,22 +330,22 @@ extern "C" {
 conv_status conv_dgrad_workspace_size(const conv_tensor_desc *dy, const conv_tensor_desc *w,
                                       const conv_tensor_desc *dx, const conv_fprop_params *p, size_t *bytes) {
     if (!bytes) return CONV_ERR_NULL_PTR;
-    ConvGeom g;
-    IgemmPlan pl;
+    std::vector<DgradPhase> ph;
     bool tensor = false;
-    conv_status st = plan_dgrad(dy, nullptr, w, dx, p, &g, &tensor, &pl);
+    size_t ws = 0;
+    conv_status st = plan_dgrad(dy, nullptr, w, dx, p, &ph, &tensor, &ws);
     if (st) return st;
-    *bytes = (tensor && g.N > 0 && g.K > 0) ? pl.workspace_bytes : 0;
+    *bytes = ws;
     return CONV_OK;
 }
 
 conv_status conv_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const conv_tensor_desc *w,
                        const int8_t *w_dev, const conv_tensor_desc *dx, int32_t *dx_dev,
                        const conv_fprop_params *p, void *workspace, size_t workspace_bytes, void *stream) {
-    ConvGeom g;
-    IgemmPlan pl;
+    std::vector<DgradPhase> ph;
     bool tensor = false;
-    conv_status st = plan_dgrad(dy, dy_dev, w, dx, p, &g, &tensor, &pl);
+    size_t ws = 0;
+    conv_status st = plan_dgrad(dy, dy_dev, w, dx, p, &ph, &tensor, &ws);
     if (st) return st;
     if (dx->dims[0] == 0) return CONV_OK;
     if (!dy_dev || !w_dev || !dx_dev) return CONV_ERR_NULL_PTR;
@@ -264,14 +355,29 @@ conv_status conv_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const c
         overlaps(dx_dev, dx_bytes, workspace, workspace_bytes))
         return CONV_ERR_OVERLAP;
     if ((st = check_device())) return st;
+    cudaStream_t s = (cudaStream_t)stream;
     if (tensor) {
-        if (!workspace || workspace_bytes < pl.workspace_bytes || ((uintptr_t)workspace % 256) != 0)
-            return CONV_ERR_WORKSPACE;
-        if (overlaps(workspace, pl.workspace_bytes, dy_dev, (uint64_t)desc_extent_elems(dy)) ||
-            overlaps(workspace, pl.workspace_bytes, w_dev, (uint64_t)desc_extent_elems(w)))
-            return CONV_ERR_OVERLAP;
-        if ((st = igemm_pack_filter_launch(g, pl, w_dev, workspace, stream))) return st;
-        return igemm_main_launch(g, pl, dy_dev, dx_dev, nullptr, workspace, stream);
+        if (ws > 0) {
+            if (!workspace || workspace_bytes < ws || ((uintptr_t)workspace % 256) != 0) return CONV_ERR_WORKSPACE;
+            if (overlaps(workspace, ws, dy_dev, (uint64_t)desc_extent_elems(dy)) ||
+                overlaps(workspace, ws, w_dev, (uint64_t)desc_extent_elems(w)))
+                return CONV_ERR_OVERLAP;
+        }
+        // the classes run one after the other on the stream, each repacking
+        // its taps into the same workspace
+        for (const DgradPhase &c : ph) {
+            int32_t *y = dx_dev + c.y_origin;
+            if (!c.taps) {
+                const ConvGeom &g = c.g;
+                zero_view_kernel<<<grid_for(g.N * g.K * g.P * g.Q, 256), 256, 0, s>>>(
+                    y, g.N, g.K, g.P, g.Q, g.ys[0], g.ys[1], g.ys[2], g.ys[3]);
+                if (cudaGetLastError() != cudaSuccess) return CONV_ERR_CUDA;
+                continue;
+            }
+            if ((st = igemm_pack_filter_launch(c.g, c.pl, w_dev + c.w_origin, workspace, stream))) return st;
+            if ((st = igemm_main_launch(c.g, c.pl, dy_dev, y, nullptr, workspace, stream))) return st;
+        }
+        return CONV_OK;
     }
     const GradArgs a = [&] {
         GradArgs r = grad_args(dx, w, dy, p);
@@ -280,7 +386,7 @@ conv_status conv_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const c
         r.out = dx_dev;
         return r;
     }();
-    dgrad_direct_kernel<<<grid_for(a.N * a.C * a.H * a.W, 256), 256, 0, (cudaStream_t)stream>>>(a);
+    dgrad_direct_kernel<<<grid_for(a.N * a.C * a.H * a.W, 256), 256, 0, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 

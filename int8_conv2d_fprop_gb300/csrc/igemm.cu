@@ -1045,11 +1045,14 @@ bool encode_output_map(const ConvGeom &g, const void *y, CUtensorMap *map) {
 bool igemm_supported(const ConvGeom &g) {
     const int64_t lim = (int64_t)1 << 30;
     if (g.H >= lim || g.W >= lim || g.P >= lim || g.Q >= lim) return false;
-    if (g.pad_h >= (1 << 20) || g.pad_w >= (1 << 20) || g.str_h >= (1 << 20) || g.str_w >= (1 << 20) ||
-        g.dil_h >= (1 << 20) || g.dil_w >= (1 << 20))
+    if (g.pad_h >= (1 << 20) || g.pad_w >= (1 << 20) || g.pad_h <= -(1 << 20) || g.pad_w <= -(1 << 20) ||
+        g.str_h >= (1 << 20) || g.str_w >= (1 << 20) || g.dil_h >= (1 << 20) || g.dil_w >= (1 << 20))
         return false;
-    // largest image coordinate formed in the gather must stay in int32
-    if ((g.P - 1) * g.str_h + (g.R - 1) * g.dil_h >= lim || (g.Q - 1) * g.str_w + (g.S - 1) * g.dil_w >= lim)
+    // largest image coordinate formed in the gather must stay in int32 (a
+    // negative pre-padding starts the windows inside the image)
+    const int64_t in_h = g.pad_h < 0 ? -g.pad_h : 0, in_w = g.pad_w < 0 ? -g.pad_w : 0;
+    if ((g.P - 1) * g.str_h + (g.R - 1) * g.dil_h + in_h >= lim ||
+        (g.Q - 1) * g.str_w + (g.S - 1) * g.dil_w + in_w >= lim)
         return false;
     if (g.R * g.S > (1 << 20)) return false;
     return true;

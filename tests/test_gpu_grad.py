@@ -1,8 +1,11 @@
 """GPU parity of the gradients (conv_dgrad, conv_wgrad through the C ABI)
 against the CPU oracle, element by element (integer results: tolerance 0).
-Cases cover both dgrad routes (tensor cores for stride 1 and padding within
-the filter's reach; the CUDA-core kernel otherwise), both modes, strides,
-dilations, asymmetric padding, NHWC and NCHW layouts and a ragged tail."""
+Cases cover both dgrad routes (tensor cores, one forward convolution per
+residue class of the stride; the CUDA-core kernel for more than 64 classes
+or when forced), classes no tap reaches (zero-filled), classes whose windows
+start inside dY (padding wider than the filter's reach), strides sharing a
+factor with the dilation, both modes, NHWC and NCHW layouts and a ragged
+tail."""
 import dataclasses
 
 import numpy as np
@@ -52,10 +55,16 @@ CASES = [
     G("s1_5x3_dil_asym_conv", 2, 32, 12, 9, 40, 5, 3, (2, 1), (3, 2), dil=(2, 1), mode=1, tensor=True),
     G("s1_nchw_k200", 1, 24, 10, 10, 200, 3, 3, (0, 2), (2, 0), layout="NCHW", tensor=True),
     G("s1_generic_forced", 2, 16, 9, 8, 20, 3, 3, (1, 1), (1, 1), algo=3),
-    G("s2_3x3", 2, 32, 15, 14, 24, 3, 3, (1, 1), (1, 0), stride=(2, 2)),
-    G("s21_dil_conv", 1, 8, 11, 12, 12, 3, 2, (2, 0), (0, 1), stride=(2, 1), dil=(1, 2), mode=1),
-    G("pad_wider_than_reach", 2, 16, 6, 7, 8, 1, 1, (1, 2), (1, 0)),
+    G("s2_3x3", 2, 32, 15, 14, 24, 3, 3, (1, 1), (1, 0), stride=(2, 2), tensor=True),
+    G("s21_dil_conv", 1, 8, 11, 12, 12, 3, 2, (2, 0), (0, 1), stride=(2, 1), dil=(1, 2), mode=1, tensor=True),
+    G("pad_wider_than_reach", 2, 16, 6, 7, 8, 1, 1, (1, 2), (1, 0), tensor=True),
+    G("s2_1x1_untouched_classes", 2, 64, 15, 16, 96, 1, 1, stride=(2, 2), tensor=True),
+    G("s23_dil23_shared_factor", 1, 40, 17, 19, 72, 3, 3, (2, 2), (1, 2), stride=(2, 3), dil=(2, 3), tensor=True),
+    G("s4_7x7_stem_nchw_conv", 2, 3, 32, 29, 64, 7, 7, (3, 3), (2, 3), stride=(4, 4), mode=1, layout="NCHW",
+      tensor=True),
+    G("s98_many_classes", 2, 16, 14, 14, 32, 3, 3, (1, 1), (0, 0), stride=(9, 8)),
     G("c3_shape_batch2", 2, 256, 56, 56, 256, 3, 3, (1, 1), (1, 1), tensor=True),
+    G("c2_shape_s2_batch1", 1, 128, 56, 56, 256, 3, 3, (1, 1), (0, 0), stride=(2, 2), tensor=True),
 ]
 
 

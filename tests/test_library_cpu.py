@@ -348,16 +348,24 @@ def test_gradient_validation_and_routes(ic):
     assert code(ic.dgrad_workspace_size, dy, w, dx, pa) == S["CONV_ERR_BAD_PARAM"]
     pg = ic.Params.make(padding=(1, 1), algo=ic.ALGO_IMPLICIT_GEMM)
     assert ic.wgrad_workspace_size(x, dy, dw, pg) > 0
-    # stride 2: CUDA-core route, no workspace; forcing the tensor cores is refused
+    # stride 2: four residue classes on the tensor cores, the workspace of the
+    # largest (2 x 2 taps of the 3 x 3 filter, one 128-channel tile, one
+    # channel step of 64 f16)
     dy2 = d(ic.CONV_INT8, (2, 32, 7, 7), "NHWC")
     p2 = ic.Params.make(pre_padding=(1, 1), post_padding=(0, 0), stride=(2, 2))
-    assert ic.dgrad_workspace_size(dy2, w, dx, p2) == 0
-    p2g = ic.Params.make(pre_padding=(1, 1), post_padding=(0, 0), stride=(2, 2), algo=ic.ALGO_IMPLICIT_GEMM)
-    assert code(ic.dgrad_workspace_size, dy2, w, dx, p2g) == S["CONV_ERR_ALIGNMENT"]
-    # padding wider than the filter's reach (3 > 2): CUDA-core route
+    assert ic.dgrad_workspace_size(dy2, w, dx, p2) == 2 * 2 * 128 * 128
+    # padding wider than the filter's reach (3 > 2): one class, windows that
+    # start inside dY
     dy3 = d(ic.CONV_INT8, (2, 32, 18, 18), "NHWC")
     p3 = ic.Params.make(padding=(3, 3))
-    assert ic.dgrad_workspace_size(dy3, w, dx, p3) == 0
+    assert ic.dgrad_workspace_size(dy3, w, dx, p3) == 3 * 3 * 128 * 128
+    # strides (9, 8): 72 classes, CUDA-core route, no workspace; forcing the
+    # tensor cores is refused
+    dy4 = d(ic.CONV_INT8, (2, 32, 2, 2), "NHWC")
+    p4 = ic.Params.make(pre_padding=(1, 1), post_padding=(0, 0), stride=(9, 8))
+    assert ic.dgrad_workspace_size(dy4, w, dx, p4) == 0
+    p4g = ic.Params.make(pre_padding=(1, 1), post_padding=(0, 0), stride=(9, 8), algo=ic.ALGO_IMPLICIT_GEMM)
+    assert code(ic.dgrad_workspace_size, dy4, w, dx, p4g) == S["CONV_ERR_ALIGNMENT"]
     # int32 bounds: dgrad sums K*R*S terms, wgrad N*P*Q terms
     wbig = d(ic.CONV_INT8, (14564, 64, 3, 3), "KRSC")    # 14564*9 = 131076 > 131071
     dybig = d(ic.CONV_INT8, (2, 14564, 14, 14), "NHWC")
