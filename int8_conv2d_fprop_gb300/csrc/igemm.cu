@@ -88,10 +88,10 @@ constexpr int EPI_SMEM_BYTES = 8 * 2 * EPI_BUF_BYTES;  // 32 KB
 #define IGEMM_STG_256 6
 #endif
 #ifndef IGEMM_ST_128
-#define IGEMM_ST_128 5
+#define IGEMM_ST_128 4
 #endif
 #ifndef IGEMM_STG_128
-#define IGEMM_STG_128 4
+#define IGEMM_STG_128 8
 #endif
 
 template <int NT, bool kTma>
@@ -149,7 +149,7 @@ __device__ __forceinline__ int groups_of(int kn) { return (kn + MAX_GROUP_STEPS 
 
 struct IgemmArgs {
     CUtensorMap tmap_x;  // im2col map of the channels-last image (TMA path only)
-    CUtensorMap tmap_y;  // 2-D [pixels][K] map of the output (when y_tma)
+    CUtensorMap tmap_y;  // output map: 2-D [pixels][K] (y_tma 1) or 3-D [N][K][P*Q] (y_tma 2)
     const int8_t *x;     // channels-last image
     const uint8_t *wp;   // repacked f16 filter blocks
     void *y;             // int32 output, or int8 when out_int8
@@ -170,7 +170,8 @@ struct IgemmArgs {
     int32_t full_units, splits, num_units;
     int32_t *tail_part;  // [cut tile][split][MT rows][NT columns]
     int32_t relu, y_vec;
-    int32_t y_tma;       // output pixel-major with contiguous channels: TMA stores
+    int32_t y_tma;       // TMA stores: 1 pixel-major with contiguous channels, 2 channel-major
+                         // (each channel's P*Q pixels contiguous, P*Q a multiple of 32)
     uint64_t wait_limit_ns;
     int *status;         // device status word
 };
@@ -376,13 +377,18 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
     ptx::tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
     const uint64_t limit = a.wait_limit_ns;
+    // launched as a programmatic dependent of the filter (or image) repack:
+    // the set-up above overlaps its tail, nothing below runs before its
+    // writes are visible
+    ptx::grid_dependency_wait();
 
     if (warp < 4 && kTma) {
         // ------------------------------------------------------------ converters
         // The im2col tile in staging holds pixel row i at i*64 bytes.  Four
         // neighbouring lanes take the four 16-byte chunks of one row, so a
         // warp reads 8 whole rows per instruction and writes them to the
-        // swizzled f16 stage without bank conflicts.
+        // swizzled f16 stage without bank conflicts.  A thread's four loads
+        // go out together before any conversion waits on one.
         ptx::setmaxnreg_dec<PRODUCER_REGS>();
         const uint32_t chunk = threadIdx.x & 3;
         const int row0 = (warp << 5) + (lane >> 2);
@@ -394,12 +400,14 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 break;
             const uint32_t src = stg_smem + rs.idx * STG_BYTES + chunk * 16u;
             const uint32_t dst = a_smem + ra.idx * A_BYTES;
+            uint4 vin[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) vin[i] = ptx::ld_shared_v4(src + (uint32_t)(row0 + 8 * i) * 64u);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint32_t row = (uint32_t)(row0 + 8 * i);
-                const uint4 v = ptx::ld_shared_v4(src + row * 64u);
                 uint4 lo, hi;
-                cvt16(v, lo, hi);
+                cvt16(vin[i], lo, hi);
                 const uint32_t rdst = dst + row * 128u;
                 const uint32_t swz = row & 7u;
                 ptx::st_shared_v4(rdst + (((2u * chunk) ^ swz) << 4), lo);
@@ -644,13 +652,21 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                     break;
                 }
                 ptx::tc_fence_after();
+                // 32-column tensor-memory loads, LD_BATCH in flight per wait
+                // (two where the registers allow: 64-column halves)
+                constexpr int LD_BATCH = HALF <= 64 ? 2 : 1;
 #pragma unroll
-                for (int cc = 0; cc < HALF / 32; ++cc) {
-                    uint32_t v[32];
-                    ptx::tmem_ld_32x32b_x32(lane_base + slot * NT + cc * 32, v);
+                for (int cc = 0; cc < HALF / 32; cc += LD_BATCH) {
+                    uint32_t v[LD_BATCH][32];
+#pragma unroll
+                    for (int b = 0; b < LD_BATCH; ++b)
+                        ptx::tmem_ld_32x32b_x32(lane_base + slot * NT + (cc + b) * 32, v[b]);
                     ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[cc * 32 + i] += __float2int_rn(__uint_as_float(v[i]));
+                    for (int b = 0; b < LD_BATCH; ++b)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            acc[(cc + b) * 32 + i] += __float2int_rn(__uint_as_float(v[b][i]));
                 }
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(ptx::smem_addr(&ctl->acc_empty[slot]));
@@ -668,17 +684,55 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                     __stcg(dst + c4, make_int4(acc[4 * c4], acc[4 * c4 + 1], acc[4 * c4 + 2], acc[4 * c4 + 3]));
                 continue;
             }
-            // epilogue arithmetic, once: + bias[k] (int32 wrap-around), then ReLU
-            if (a.bias || a.relu) {
+            // epilogue arithmetic, once: + bias[k] (int32 wrap-around), then
+            // ReLU.  All lanes of the warp hold the same HALF columns: each
+            // lane loads HALF/32 of the bias values and the warp passes them
+            // round with shuffles (one load per lane instead of HALF).
+            if (a.bias) {
                 const int kb = nt * NT + col0;
+                int32_t bv[HALF / 32];
 #pragma unroll
-                for (int i = 0; i < HALF; ++i) {
-                    int32_t val = acc[i];
-                    if (a.bias && kb + i < a.K) val = (int32_t)((uint32_t)val + (uint32_t)__ldg(a.bias + kb + i));
-                    acc[i] = a.relu ? max(val, 0) : val;
+                for (int j = 0; j < HALF / 32; ++j) {
+                    const int k = kb + j * 32 + lane;
+                    bv[j] = k < a.K ? __ldg(a.bias + k) : 0;
                 }
+#pragma unroll
+                for (int i = 0; i < HALF; ++i)
+                    acc[i] = (int32_t)((uint32_t)acc[i] + (uint32_t)__shfl_sync(0xffffffffu, bv[i / 32], i % 32));
             }
-            if (a.y_tma && a.out_int8) {
+            if (a.relu) {
+#pragma unroll
+                for (int i = 0; i < HALF; ++i) acc[i] = max(acc[i], 0);
+            }
+            if (a.y_tma == 2) {
+                // Channel-major output: the warp's 32 rows are 32 consecutive
+                // pixels of one image (P*Q is a multiple of 32).  It stages
+                // 16 channels x 32 pixels at a time as 16 rows of 128 bytes,
+                // lane i writing pixel i of each row (no bank conflicts), and
+                // one lane stores them as a {32 pixels, 16 channels, 1 image}
+                // box; the map clips channels past K and images past N.
+                const int k0 = nt * NT + col0;
+                const int m0w = mt * MT + quad * 32;
+                const int pq = a.P * a.Q;
+                const int img = m0w / pq;
+                const int pix = m0w - img * pq;
+                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (2u * EPI_BUF_BYTES);
+#pragma unroll
+                for (int ch = 0; ch < HALF / EPI_COLS; ++ch) {
+                    const uint32_t buf = ebase + (uint32_t)(ch & 1) * EPI_BUF_BYTES;
+                    if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store that last read buf is done
+                    __syncwarp();
+#pragma unroll
+                    for (int c = 0; c < EPI_COLS; ++c)
+                        ptx::st_shared_b32(buf + (uint32_t)c * 128u + (uint32_t)lane * 4u, (uint32_t)acc[ch * EPI_COLS + c]);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_3d(&a.tmap_y, pix, k0 + ch * EPI_COLS, img, buf);
+                        ptx::bulk_commit_group();
+                    }
+                }
+            } else if (a.y_tma && a.out_int8) {
                 // int8 output: as below, with 64 one-byte columns per 64-byte
                 // staged row
                 const int k0 = nt * NT + col0;
@@ -785,6 +839,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
 __global__ void igemm_pack_filter_kernel(const int8_t *w, int64_t ws0, int64_t ws1, int64_t ws2, int64_t ws3,
                                          int32_t K, int32_t C, int32_t R, int32_t S, int32_t mode, int32_t c_steps,
                                          int32_t k_steps, int32_t n_tiles, int32_t nt_rows, uint8_t *wp) {
+    ptx::launch_dependents();
     const int64_t total = (int64_t)n_tiles * k_steps * nt_rows * 8;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
@@ -894,6 +949,7 @@ __global__ void __launch_bounds__(256) igemm_split_reduce_kernel(const int32_t *
 // of a warp take neighbouring pixels so that reads along W coalesce for NCHW.
 __global__ void igemm_pack_image_kernel(const int8_t *x, int64_t xs0, int64_t xs1, int64_t xs2, int64_t xs3,
                                         int64_t N, int32_t C, int32_t H, int32_t W, int32_t c16, int8_t *xp) {
+    ptx::launch_dependents();
     const int64_t pixels = N * H * W;
     const int cblocks = c16 / 16;
     const int64_t total = pixels * cblocks;
@@ -940,7 +996,22 @@ conv_status launch_conv(const IgemmArgs &a, int grid, cudaStream_t st) {
             return CONV_ERR_CUDA;
         if (dev >= 0 && dev < 64) attr_set[dev].store(true);
     }
-    igemm_conv_kernel<NT, kTma><<<grid, THREADS, Cfg::SMEM_BYTES, st>>>(a);
+    // a programmatic dependent of the previous kernel in the stream: its CTAs
+    // may start (allocate, initialise barriers) while a repack kernel that
+    // signals launch_dependents finishes, and wait for its writes in
+    // grid_dependency_wait; behind any other kernel or copy it starts when
+    // that completes, as without the attribute
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, igemm_conv_kernel<NT, kTma>, a) != cudaSuccess) return CONV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
@@ -1037,6 +1108,34 @@ bool encode_output_map(const ConvGeom &g, const void *y, CUtensorMap *map) {
                            const_cast<void *>(y), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                            CU_TENSOR_MAP_SWIZZLE_64B,
                            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 3-D map [N][K][P*Q] of an int32 output whose channels each hold their P*Q
+// pixels contiguously (NCHW, possibly with padded channel or image strides):
+// box 32 pixels x 16 channels x 1 image, no swizzle.  Requires P*Q to be a
+// multiple of 32, so that the 32 pixels of an epilogue warp never straddle
+// two images and start 128 bytes aligned.  Returns false for any other
+// layout.
+bool encode_output_map_nchw(const ConvGeom &g, const void *y, CUtensorMap *map) {
+    if (g.out_int8) return false;
+    const int64_t pq = g.P * g.Q;
+    if (pq % 32 != 0) return false;
+    if (g.Q > 1 && g.ys[3] != 1) return false;
+    if (g.P > 1 && g.ys[2] != g.Q) return false;
+    const int64_t ks = g.K > 1 ? g.ys[1] : pq;
+    const int64_t ns = g.N > 1 ? g.ys[0] : ks * g.K;
+    if (ks < pq || ns < ks * g.K || (ks * 4) % 16 != 0 || (ns * 4) % 16 != 0 || ((uintptr_t)y % 16) != 0) return false;
+    if (pq >= ((int64_t)1 << 32) || ns * 4 >= ((int64_t)1 << 40)) return false;
+    auto enc = tiled_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)pq, (cuuint64_t)g.K, (cuuint64_t)g.N};
+    const cuuint64_t strides[2] = {(cuuint64_t)(ks * 4), (cuuint64_t)(ns * 4)};
+    const cuuint32_t box[3] = {32, (cuuint32_t)EPI_COLS, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, const_cast<void *>(y), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -1167,7 +1266,7 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
                (g.ys[2] % 4) == 0 && (g.ys[3] % 4) == 0)
                   ? 1
                   : 0;
-    a.y_tma = encode_output_map(g, y, &a.tmap_y) ? 1 : 0;
+    a.y_tma = encode_output_map(g, y, &a.tmap_y) ? 1 : (encode_output_map_nchw(g, y, &a.tmap_y) ? 2 : 0);
     a.wait_limit_ns = wait_limit_ns();
     a.status = device_status_word();
     if (!a.status) return CONV_ERR_CUDA;

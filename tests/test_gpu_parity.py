@@ -182,6 +182,48 @@ def test_padded_strides_and_output_layouts(ic, algo):
         _assert_equal(got, ref, f"padded strides algo {algo} y {yl}")
 
 
+@pytest.mark.parametrize("k_pad,n_pad", [(0, 0), (16, 0), (4, 96)])
+@pytest.mark.parametrize("case", [
+    synth.ConvConfig("pq64_k40_ragged", 3, 48, 8, 8, 40, 3, 3, pre=(1, 1), post=(1, 1), seed=51),
+    synth.ConvConfig("pq96_k256_bias_relu", 2, 64, 12, 8, 256, 1, 1, bias=True, relu=True, seed=52),
+    synth.ConvConfig("pq32_k130_s2", 5, 32, 8, 16, 130, 3, 3, stride=(2, 2), pre=(1, 1), post=(0, 0), seed=53),
+], ids=lambda c: c.name)
+def test_channel_major_output(ic, case, k_pad, n_pad):
+    """NCHW outputs whose P*Q is a multiple of 32 take the channel-major TMA
+    store; channel and image strides padded beyond P*Q and K*ks must be
+    honoured, channels past K and images past N clipped, and nothing written
+    outside the output (canaries)."""
+    cfg = case
+    x, w, b = synth.make_inputs(cfg)
+    xf, xs = synth.place(x, cfg.x_layout)
+    wf, ws = synth.place(w, cfg.w_layout)
+    xt, wt = _to_dev(xf, cfg.x_dims, xs), _to_dev(wf, cfg.w_dims, ws)
+    bt = torch.from_numpy(b).cuda() if b is not None else None
+    N, K, P, Q = cfg.y_dims
+    assert (P * Q) % 32 == 0
+    ks = P * Q + k_pad
+    ns = K * ks + n_pad
+    span = (N - 1) * ns + (K - 1) * ks + P * Q
+    fill = 0x5A5A5A5A
+    guard = torch.full((span + 128,), fill, dtype=torch.int32, device="cuda")
+    yt = torch.as_strided(guard[64:64 + span], (N, K, P, Q), (ns, ks, Q, 1))
+    y = ic.conv_fprop(xt, wt, bt, pre_padding=cfg.pre, post_padding=cfg.post, stride=cfg.stride,
+                      dilation=cfg.dilation, mode=cfg.mode, relu=cfg.relu, out=yt)
+    torch.cuda.synchronize()
+    assert ic.device_status() == 0
+    g = guard.cpu().numpy()
+    assert np.all(g[:64] == fill) and np.all(g[64 + span:] == fill), "write outside the output"
+    # the padding between channels and between images is left alone
+    inside = np.zeros(span, dtype=bool)
+    for n in range(N):
+        for k in range(K):
+            inside[n * ns + k * ks:n * ns + k * ks + P * Q] = True
+    assert np.all(g[64:64 + span][~inside] == fill), "write into the stride padding"
+    ref = oracle.conv_fprop(xf, cfg.x_dims, xs, wf, cfg.w_dims, ws, cfg.pre, cfg.post, cfg.stride,
+                            cfg.dilation, cfg.mode, b, cfg.relu)
+    _assert_equal(y.cpu().numpy(), ref, f"{cfg.name} k_pad {k_pad} n_pad {n_pad}")
+
+
 # ------------------------------------------------------------------ exactness
 def test_extreme_values_exceed_f32_integer_range(ic):
     """All -128 operands: interior sums C*R*S*2^14 = 37,748,736 > 2^24, so
