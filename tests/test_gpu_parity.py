@@ -224,6 +224,40 @@ def test_channel_major_output(ic, case, k_pad, n_pad):
     _assert_equal(y.cpu().numpy(), ref, f"{cfg.name} k_pad {k_pad} n_pad {n_pad}")
 
 
+def _partial_round_cases():
+    C = synth.ConvConfig
+    return [
+        # 196 tiles of 256 channels, 18 k-steps
+        C("rounds_3x3_nt256", 8, 128, 56, 56, 256, 3, 3, pre=(1, 1), post=(1, 1), seed=61),
+        # 196 tiles of 128 channels, 4 k-steps, bias and ReLU
+        C("rounds_1x1_bias_relu", 32, 256, 28, 28, 128, 1, 1, bias=True, relu=True, seed=62),
+        # 166 tiles over two channel tiles (K = 300), ragged pixels and channels
+        C("rounds_ragged_two_ntiles", 5, 96, 45, 47, 300, 3, 3, pre=(1, 1), post=(1, 1), seed=63),
+        # 172 tiles, 72 k-steps: five groups of at most 16 k-steps per tile
+        C("rounds_long_reduction", 7, 512, 56, 56, 128, 3, 3, pre=(1, 1), post=(1, 1), seed=64),
+        # 168 tiles, NCHW image and output (channel-major stores), convolution mode
+        C("rounds_nchw_conv_mode", 4, 64, 86, 64, 192, 7, 1, stride=(1, 1), dilation=(2, 1), pre=(6, 0),
+          post=(6, 0), mode=1, x_layout="NCHW", w_layout="KCRS", y_layout="NCHW", seed=65),
+    ]
+
+
+@pytest.mark.parametrize("case", _partial_round_cases(), ids=lambda c: c.name)
+def test_more_tiles_than_sms_matches_oracle(ic, case):
+    """More tiles than SMs, the last round partial: every CTA walks several
+    tiles and some CTAs one more than others.  Every output element is
+    compared, twice (a second call on the same workspace)."""
+    got, ref = _run_both(ic, case)
+    _assert_equal(got, ref, case.name)
+    got2, _ = _run_both(ic, case)
+    _assert_equal(got2, ref, case.name + " (second call)")
+
+
+def test_more_tiles_than_sms_int8_output(ic):
+    cfg = _partial_round_cases()[1]
+    got, ref = _run_both(ic, cfg, out_shift=14)
+    _assert_equal(got, ref, "int8 output, partial last round")
+
+
 # ------------------------------------------------------------------ exactness
 def test_extreme_values_exceed_f32_integer_range(ic):
     """All -128 operands: interior sums C*R*S*2^14 = 37,748,736 > 2^24, so
