@@ -340,8 +340,9 @@ def run_ours(args):
             with open(TRAFFIC_FILE) as f:
                 tr = json.load(f)
             src_sha = hashlib.sha256(open(DOMINANT_KERNEL_SRC, "rb").read()).hexdigest()
-            if tr.get("kernel_src_sha256") == src_sha and tr.get("workload") == args.workload:
-                traffic = tr.get("dram_bytes_per_launch")
+            entry = tr.get("workloads", {}).get(args.workload)
+            if tr.get("kernel_src_sha256") == src_sha and entry:
+                traffic = entry.get("dram_bytes_per_launch")
         except (OSError, ValueError):
             traffic = None
     hbm = _peak_value(peaks, ("hbm_gbs",))
