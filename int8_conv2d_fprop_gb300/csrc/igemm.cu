@@ -978,6 +978,80 @@ __global__ void igemm_pack_image_kernel(const int8_t *x, int64_t xs0, int64_t xs
     }
 }
 
+// The same copy for images whose channels each hold their H x W pixels in one
+// contiguous plane (NCHW-like, 16-byte aligned planes, H*W a multiple of 16):
+// a transpose through shared memory.  A block takes 64 channels x 256 pixels
+// of one image.  Loads: four threads per channel, 16-byte loads of 256
+// contiguous pixels, stored as they are in a [channel][pixel] tile.  Stores:
+// a thread takes 4 pixels x 16 channels, reads the 16 channels' 4-pixel words
+// and transposes each 4 x 4 block of bytes with byte permutes, then writes
+// each pixel's 16 channels; four neighbouring threads cover a pixel's 64
+// channels (64 contiguous bytes of the channels-last copy).  Channels from C
+// up to c16 are zero.
+constexpr int kPackPix = 256, kPackCh = 64, kPackPitch = 272;  // pitch: 16-byte rows, 2-way conflicts at most on the tile stores
+
+__device__ __forceinline__ void transpose4x4_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t (&o)[4]) {
+    // o[i] = byte i of a, b, c, d
+    const uint32_t ab_lo = __byte_perm(a, b, 0x5140), ab_hi = __byte_perm(a, b, 0x7362);
+    const uint32_t cd_lo = __byte_perm(c, d, 0x5140), cd_hi = __byte_perm(c, d, 0x7362);
+    o[0] = __byte_perm(ab_lo, cd_lo, 0x5410);
+    o[1] = __byte_perm(ab_lo, cd_lo, 0x7632);
+    o[2] = __byte_perm(ab_hi, cd_hi, 0x5410);
+    o[3] = __byte_perm(ab_hi, cd_hi, 0x7632);
+}
+
+__global__ void __launch_bounds__(256) igemm_pack_image_planes_kernel(const int8_t *x, int64_t xs0, int64_t xs1,
+                                                                      int64_t N, int32_t C, int32_t HW, int32_t c16,
+                                                                      int8_t *xp) {
+    ptx::launch_dependents();
+    __shared__ __align__(16) uint8_t tile[kPackCh * kPackPitch];
+    const int ptiles = (HW + kPackPix - 1) / kPackPix;
+    const int ctiles = (c16 + kPackCh - 1) / kPackCh;
+    const int64_t total = N * ptiles * ctiles;
+    const int cl = threadIdx.x >> 2, seg = threadIdx.x & 3;  // loads: channel row, 64-pixel segment
+    const int cb = threadIdx.x & 3, q = threadIdx.x >> 2;    // stores: 16-channel block, 4-pixel quad
+    for (int64_t b = blockIdx.x; b < total; b += gridDim.x) {
+        const int ct = (int)(b % ctiles);
+        const int64_t t = b / ctiles;
+        const int pt = (int)(t % ptiles);
+        const int64_t n = t / ptiles;
+        const int p0 = pt * kPackPix, c0 = ct * kPackCh;
+        const int c = c0 + cl;
+        const int8_t *src = x + n * xs0 + (int64_t)c * xs1 + p0 + seg * 64;
+        uint4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int p = p0 + seg * 64 + j * 16;
+            v[j] = (c < C && p < HW) ? __ldg(reinterpret_cast<const uint4 *>(src + j * 16)) : make_uint4(0, 0, 0, 0);
+        }
+        __syncthreads();  // the previous tile's stores have read the buffer
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4 *>(tile + cl * kPackPitch + seg * 64 + j * 16) = v[j];
+        __syncthreads();
+        uint32_t w[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+            w[k] = *reinterpret_cast<const uint32_t *>(tile + (cb * 16 + k) * kPackPitch + q * 4);
+        uint32_t px[4][4];  // [pixel][channel word]
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            uint32_t o[4];
+            transpose4x4_bytes(w[4 * m], w[4 * m + 1], w[4 * m + 2], w[4 * m + 3], o);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) px[i][m] = o[i];
+        }
+        const int cc = c0 + cb * 16;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int p = p0 + q * 4 + i;
+            if (p < HW && cc < c16)
+                *reinterpret_cast<uint4 *>(xp + (n * HW + p) * c16 + cc) =
+                    make_uint4(px[i][0], px[i][1], px[i][2], px[i][3]);
+        }
+    }
+}
+
 inline int64_t align256(int64_t v) { return (v + 255) & ~255LL; }
 
 constexpr int64_t kSplitMinKSteps = 64;  // only reductions at least this long are cut
@@ -1223,12 +1297,22 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
     IgemmArgs a;
     if (pl.pack_x) {
         int8_t *xp = reinterpret_cast<int8_t *>(wp + pl.xpack_off);
-        const int64_t total = g.N * g.H * g.W * (pl.c16 / 16);
-        int64_t blocks = (total + 255) / 256;
-        if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
-        igemm_pack_image_kernel<<<(unsigned)blocks, 256, 0, st>>>(x, g.xs[0], g.xs[1], g.xs[2], g.xs[3], g.N,
-                                                                  (int32_t)g.C, (int32_t)g.H, (int32_t)g.W,
-                                                                  (int32_t)pl.c16, xp);
+        const int64_t hw = g.H * g.W;
+        const bool planes = (g.W == 1 || g.xs[3] == 1) && (g.H == 1 || g.xs[2] == g.W) && g.xs[1] % 16 == 0 &&
+                            g.xs[0] % 16 == 0 && hw % 16 == 0 && ((uintptr_t)x % 16) == 0 && hw < ((int64_t)1 << 31);
+        if (planes) {
+            const int64_t total = g.N * ((hw + kPackPix - 1) / kPackPix) * ((pl.c16 + kPackCh - 1) / kPackCh);
+            int64_t blocks = total < (int64_t)sms * 8 ? total : (int64_t)sms * 8;
+            igemm_pack_image_planes_kernel<<<(unsigned)blocks, 256, 0, st>>>(x, g.xs[0], g.xs[1], g.N, (int32_t)g.C,
+                                                                             (int32_t)hw, (int32_t)pl.c16, xp);
+        } else {
+            const int64_t total = g.N * g.H * g.W * (pl.c16 / 16);
+            int64_t blocks = (total + 255) / 256;
+            if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
+            igemm_pack_image_kernel<<<(unsigned)blocks, 256, 0, st>>>(x, g.xs[0], g.xs[1], g.xs[2], g.xs[3], g.N,
+                                                                      (int32_t)g.C, (int32_t)g.H, (int32_t)g.W,
+                                                                      (int32_t)pl.c16, xp);
+        }
         if (cudaGetLastError() != cudaSuccess) return CONV_ERR_CUDA;
         a.x = xp;
         a.xs_n = g.H * g.W * pl.c16;

@@ -258,6 +258,41 @@ def test_more_tiles_than_sms_int8_output(ic):
     _assert_equal(got, ref, "int8 output, partial last round")
 
 
+@pytest.mark.parametrize("c_pad,n_pad", [(0, 0), (48, 0), (16, 256)])
+@pytest.mark.parametrize("case", [
+    synth.ConvConfig("planes_c24_hw144", 3, 24, 9, 16, 40, 3, 3, pre=(1, 1), post=(1, 1), x_layout="NCHW",
+                     w_layout="KCRS", seed=71),
+    synth.ConvConfig("planes_c80_hw400", 2, 80, 20, 20, 96, 3, 1, stride=(2, 1), pre=(1, 0), post=(1, 0),
+                     x_layout="NCHW", w_layout="KCRS", y_layout="NCHW", seed=72),
+    synth.ConvConfig("planes_c130_hw512", 2, 130, 16, 32, 64, 1, 1, x_layout="NCHW", w_layout="KCRS", seed=73),
+], ids=lambda c: c.name)
+def test_nchw_image_plane_copy(ic, case, c_pad, n_pad):
+    """Images whose channels each hold a contiguous H x W plane (H*W a
+    multiple of 16) are copied to channels-last by a shared-memory
+    transpose before the tensor-core kernel; channel and image strides padded
+    beyond the plane must be honoured."""
+    cfg = case
+    x, w, b = synth.make_inputs(cfg)
+    N, C, H, W = cfg.x_dims
+    cs = H * W + c_pad
+    ns = C * cs + n_pad
+    xflat = np.zeros((N - 1) * ns + (C - 1) * cs + H * W, dtype=np.int8)
+    for n in range(N):
+        for c in range(C):
+            xflat[n * ns + c * cs:n * ns + c * cs + H * W] = x[n, c].reshape(-1)
+    xs = (ns, cs, W, 1)
+    wf, ws = synth.place(w, cfg.w_layout)
+    xt, wt = _to_dev(xflat, cfg.x_dims, xs), _to_dev(wf, cfg.w_dims, ws)
+    bt = torch.from_numpy(b).cuda() if b is not None else None
+    y = ic.conv_fprop(xt, wt, bt, pre_padding=cfg.pre, post_padding=cfg.post, stride=cfg.stride,
+                      dilation=cfg.dilation, mode=cfg.mode, relu=cfg.relu, algo=ic.ALGO_IMPLICIT_GEMM)
+    torch.cuda.synchronize()
+    assert ic.device_status() == 0
+    ref = oracle.conv_fprop(xflat, cfg.x_dims, xs, wf, cfg.w_dims, ws, cfg.pre, cfg.post, cfg.stride,
+                            cfg.dilation, cfg.mode, b, cfg.relu)
+    _assert_equal(y.cpu().numpy(), ref, f"{cfg.name} c_pad {c_pad} n_pad {n_pad}")
+
+
 # ------------------------------------------------------------------ exactness
 def test_extreme_values_exceed_f32_integer_range(ic):
     """All -128 operands: interior sums C*R*S*2^14 = 37,748,736 > 2^24, so
