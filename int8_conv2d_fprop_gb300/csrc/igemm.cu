@@ -895,12 +895,13 @@ __global__ void igemm_pack_filter_kernel(const int8_t *w, int64_t ws0, int64_t w
 // Adds the runs of every cut tile (tiles tile0.. of the grid walk; raw int32
 // sums in the workspace as int4 quads, [cut tile][split][column quad][row]),
 // then applies bias, ReLU and the int8 requantisation like the main epilogue
-// and stores the tile.  A block takes 32 columns x 128 rows of one cut tile:
-// it adds the runs with rows fastest (512 contiguous bytes per warp and run)
-// into a shared tile, then stores with columns fastest when the output's
-// channels are contiguous (128 contiguous bytes of int32 per warp), rows
-// fastest otherwise (consecutive pixels of one channel).
-constexpr int kRedCols = 32, kRedPitch = kRedCols + 4;  // int32 per shared row, 16-byte aligned rows
+// and stores the tile.  A block (256 threads) takes 32 rows x 32 columns of
+// one cut tile, one quad per thread: each warp reads 32 consecutive rows of
+// one quad (512 contiguous bytes per run), four runs' loads in flight; the
+// sums go through a shared tile so that the stores run with columns fastest
+// when the output's channels are contiguous (128 contiguous bytes of int32
+// per warp), rows fastest otherwise (consecutive pixels of one channel).
+constexpr int kRedRows = 32, kRedCols = 32, kRedPitch = kRedCols + 4;  // int32 per shared row
 __global__ void __launch_bounds__(256) igemm_split_reduce_kernel(const int32_t *part, int32_t tile0,
                                                                  int32_t tiles, int32_t splits,
                                                                  int32_t n_tiles, int32_t nt_cols, int32_t m_total,
@@ -908,57 +909,41 @@ __global__ void __launch_bounds__(256) igemm_split_reduce_kernel(const int32_t *
                                                                  int64_t ys_k, int64_t ys_p, int64_t ys_q, void *y,
                                                                  int32_t out_int8, int32_t out_shift,
                                                                  const int32_t *bias, int32_t relu) {
-    __shared__ __align__(16) int32_t sums[MT * kRedPitch];
-    // launched as a programmatic dependent of the convolution (256 threads
-    // a block): nothing is read before its writes are visible
+    __shared__ __align__(16) int32_t sums[kRedRows * kRedPitch];
+    // launched as a programmatic dependent of the convolution: nothing is
+    // read before its writes are visible
     ptx::grid_dependency_wait();
-    const int qblocks = nt_cols / kRedCols;
-    const int64_t total = (int64_t)tiles * qblocks;
+    const int qblocks = nt_cols / kRedCols, rblocks = MT / kRedRows;
+    const int64_t total = (int64_t)tiles * qblocks * rblocks;
     const bool chan_fast = ys_k == 1;
     const int pq = P * Q;
+    const size_t run_quads = (size_t)MT * nt_cols / 4;
+    const int lr = threadIdx.x % kRedRows, lq = threadIdx.x / kRedRows;  // this thread's row and quad
     for (int64_t b = blockIdx.x; b < total; b += gridDim.x) {
-        const int qb = (int)(b % qblocks);
-        const int ct = (int)(b / qblocks);  // cut tile
+        const int rb = (int)(b % rblocks);
+        const int64_t t = b / rblocks;
+        const int qb = (int)(t % qblocks);
+        const int ct = (int)(t / qblocks);  // cut tile
         const int tile = tile0 + ct;
         const int mt = tile / n_tiles;
         const int nt = tile - mt * n_tiles;
-        // each thread adds RED_Q quads over all runs, the quads' loads of a
-        // run issued together (the runs are L2-resident: latency, not
-        // bandwidth, sets the pace)
-        constexpr int RED_Q = MT * (kRedCols / 4) / 256;
-        int4 v[RED_Q];
-        size_t off[RED_Q];
-#pragma unroll
-        for (int j = 0; j < RED_Q; ++j) {
-            const int i = threadIdx.x + j * 256;
-            off[j] = (size_t)(qb * (kRedCols / 4) + i / MT) * MT + i % MT;
-            v[j] = make_int4(0, 0, 0, 0);
-        }
-        const int4 *run0 = reinterpret_cast<const int4 *>(part + (size_t)ct * splits * MT * nt_cols);
-        const size_t run_quads = (size_t)MT * nt_cols / 4;
-#pragma unroll 2
+        const int4 *src = reinterpret_cast<const int4 *>(part + (size_t)ct * splits * MT * nt_cols) +
+                          (size_t)(qb * (kRedCols / 4) + lq) * MT + rb * kRedRows + lr;
+        int4 v = make_int4(0, 0, 0, 0);
+#pragma unroll 4
         for (int sp = 0; sp < splits; ++sp) {
-            int4 x[RED_Q];
-#pragma unroll
-            for (int j = 0; j < RED_Q; ++j) x[j] = __ldcg(run0 + sp * run_quads + off[j]);
-#pragma unroll
-            for (int j = 0; j < RED_Q; ++j) {
-                v[j].x += x[j].x;
-                v[j].y += x[j].y;
-                v[j].z += x[j].z;
-                v[j].w += x[j].w;
-            }
+            const int4 x = __ldcg(src + sp * run_quads);
+            v.x += x.x;
+            v.y += x.y;
+            v.z += x.z;
+            v.w += x.w;
         }
-#pragma unroll
-        for (int j = 0; j < RED_Q; ++j) {
-            const int i = threadIdx.x + j * 256;
-            *reinterpret_cast<int4 *>(sums + (i % MT) * kRedPitch + (i / MT) * 4) = v[j];
-        }
+        *reinterpret_cast<int4 *>(sums + lr * kRedPitch + lq * 4) = v;
         __syncthreads();
-        for (int i = threadIdx.x; i < MT * kRedCols; i += blockDim.x) {
-            const int row = chan_fast ? i / kRedCols : i % MT;
-            const int col = chan_fast ? i % kRedCols : i / MT;
-            const int m = mt * MT + row;
+        for (int i = threadIdx.x; i < kRedRows * kRedCols; i += blockDim.x) {
+            const int row = chan_fast ? i / kRedCols : i % kRedRows;
+            const int col = chan_fast ? i % kRedCols : i / kRedRows;
+            const int m = mt * MT + rb * kRedRows + row;
             const int k = nt * nt_cols + qb * kRedCols + col;
             if (m >= m_total || k >= K) continue;
             int32_t val = sums[row * kRedPitch + col];
@@ -1407,8 +1392,8 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
         rc = pl.n_tile == 256 ? launch_conv<256, false>(a, grid, st) : launch_conv<128, false>(a, grid, st);
     if (rc || pl.splits <= 1) return rc;
     const int32_t cut_tiles = a.num_tiles - a.full_units;
-    int64_t blocks = (int64_t)cut_tiles * (pl.n_tile / kRedCols);
-    if (blocks > (int64_t)sms * 6) blocks = (int64_t)sms * 6;
+    int64_t blocks = (int64_t)cut_tiles * (pl.n_tile / kRedCols) * (MT / kRedRows);
+    if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(256);
