@@ -298,14 +298,17 @@ conv_status conv_fprop_static_workspace(const conv_tensor_desc *x, const int8_t 
  * conv_dgrad runs on the tensor cores as stride_h*stride_w forward
  * convolutions of dY, one per residue class (h mod stride_h, w mod
  * stride_w) of dX's pixels, each by the filter taps that reach that class
- * (taken backwards, K and C exchanged) with stride 1, one after the other on
- * `stream` in one workspace; a class no tap reaches is written with zeros.
+ * (taken backwards, K and C exchanged) with stride 1, each in its own part of
+ * the workspace; several classes run side by side on up to four
+ * library-owned streams forked from `stream` and joined back to it (events;
+ * created on the first such call on a device, so make that call outside a
+ * stream capture); a class no tap reaches is written with zeros.
  * More than 64 classes take the CUDA-core kernel.  conv_wgrad runs on the
  * tensor cores as a forward convolution of the image (batch and channel
  * dims exchanged) by dY (its batch as channels, its pixels as taps) when the
  * tensor-core kernel can express it.  Those routes need the workspace the
  * *_workspace_size call reports (256-byte aligned, caller-owned; for dgrad
- * it holds the largest class's filter repacked to f16 blocks, for wgrad dY
+ * it holds every class's filter repacked to f16 blocks, for wgrad dY
  * repacked to f16 blocks, about 2*K*P*Q*ceil(N/64)*64 bytes, plus the int32
  * partial sums of the reduction split over the SMs).  Other calls, and algo
  * DIRECT_GENERIC, run CUDA-core kernels and need none; IMPLICIT_GEMM on a

@@ -13,8 +13,10 @@
 //    (T-1)*e - c0, by the filter's taps r0, r0 + delta, ... taken backwards,
 //    K and C exchanged, written into dX through its strides times the stride.
 //    With stride 1 there is one class, the whole filter reversed.  Each class
-//    runs on the tensor-core kernel with its own filter repack, one after the
-//    other in one workspace; a class no tap reaches is zero-filled.
+//    runs on the tensor-core kernel with its own filter repack in its own
+//    part of the workspace; several classes run side by side on streams
+//    forked from the caller's and joined back to it; a class no tap reaches
+//    is zero-filled.
 //  * otherwise (a class the tensor-core kernel cannot express, more than
 //    kMaxDgradPhases classes, or DIRECT_GENERIC): a CUDA-core kernel, one
 //    thread per dX element.
@@ -31,6 +33,7 @@
 //    by the validator's bound, added across the warp with shuffles).
 #include <cuda_runtime.h>
 
+#include <mutex>
 #include <numeric>
 #include <vector>
 
@@ -165,8 +168,26 @@ struct DgradPhase {
     IgemmPlan pl;
     int64_t w_origin;  // element offset in W of the class filter's tap (0, 0)
     int64_t y_origin;  // element offset in dX of the class's first pixel
+    size_t ws_off;     // the class's own part of the workspace
     bool taps;         // false: no tap reaches the class, its pixels are zero
 };
+
+// Streams the residue classes of one dgrad call run on side by side, forked
+// from the caller's stream and joined back to it; created on first use, one
+// set per device, kept for the life of the process.
+constexpr int kSideStreams = 4;
+constexpr int kSideDevices = 64;
+
+cudaStream_t side_stream(int i) {
+    static std::mutex mu;
+    static cudaStream_t streams[kSideDevices][kSideStreams] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kSideDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!streams[dev][i] && cudaStreamCreateWithFlags(&streams[dev][i], cudaStreamNonBlocking) != cudaSuccess)
+        streams[dev][i] = nullptr;
+    return streams[dev][i];
+}
 
 // The taps of one axis that reach residue rho: r = r0 + t*delta, t < T.
 // Returns T (0 when none), with r0, delta, the class's dilation e and its
@@ -299,7 +320,8 @@ conv_status plan_wgrad(const conv_tensor_desc *x, const void *x_dev, const conv_
 }
 
 // Plans a dgrad call: *tensor tells whether the residue classes in *ph run on
-// the tensor cores, *ws_bytes the workspace they share (the largest class's).
+// the tensor cores, *ws_bytes the workspace they need (each class its own
+// part, so that they can run at the same time).
 conv_status plan_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const conv_tensor_desc *w,
                        const conv_tensor_desc *dx, const conv_fprop_params *p, std::vector<DgradPhase> *ph,
                        bool *tensor, size_t *ws_bytes) {
@@ -315,7 +337,8 @@ conv_status plan_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const c
         // a class whose window starts inside dY (negative padding) gathers
         // with register loads, which bounds-check every pixel
         if (c.g.pad_h < 0 || c.g.pad_w < 0) c.pl.register_loads = true;
-        if (c.g.N > 0 && c.pl.workspace_bytes > *ws_bytes) *ws_bytes = c.pl.workspace_bytes;
+        c.ws_off = *ws_bytes;
+        if (c.g.N > 0) *ws_bytes += (c.pl.workspace_bytes + 255) & ~(size_t)255;
     }
     return CONV_OK;
 }
@@ -363,21 +386,49 @@ conv_status conv_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const c
                 overlaps(workspace, ws, w_dev, (uint64_t)desc_extent_elems(w)))
                 return CONV_ERR_OVERLAP;
         }
-        // the classes run one after the other on the stream, each repacking
-        // its taps into the same workspace
-        for (const DgradPhase &c : ph) {
+        // one class: on the caller's stream.  Several: each on a side
+        // stream forked from the caller's (an event), repacking its taps into
+        // its own part of the workspace and writing its own dX pixels, then
+        // joined back (an event per side stream)
+        auto run_class = [&](const DgradPhase &c, cudaStream_t cs) -> conv_status {
             int32_t *y = dx_dev + c.y_origin;
             if (!c.taps) {
                 const ConvGeom &g = c.g;
-                zero_view_kernel<<<grid_for(g.N * g.K * g.P * g.Q, 256), 256, 0, s>>>(
+                zero_view_kernel<<<grid_for(g.N * g.K * g.P * g.Q, 256), 256, 0, cs>>>(
                     y, g.N, g.K, g.P, g.Q, g.ys[0], g.ys[1], g.ys[2], g.ys[3]);
-                if (cudaGetLastError() != cudaSuccess) return CONV_ERR_CUDA;
+                return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+            }
+            void *cw = static_cast<uint8_t *>(workspace) + c.ws_off;
+            conv_status r = igemm_pack_filter_launch(c.g, c.pl, w_dev + c.w_origin, cw, cs);
+            if (r == CONV_OK) r = igemm_main_launch(c.g, c.pl, dy_dev, y, nullptr, cw, cs);
+            return r;
+        };
+        if (ph.empty()) return CONV_OK;
+        if (ph.size() == 1) return run_class(ph[0], s);
+        const int nside = (int)ph.size() < kSideStreams ? (int)ph.size() : kSideStreams;
+        cudaStream_t side[kSideStreams];
+        for (int i = 0; i < nside; ++i)
+            if (!(side[i] = side_stream(i))) return CONV_ERR_CUDA;
+        cudaEvent_t fork;
+        if (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess) return CONV_ERR_CUDA;
+        conv_status rc = cudaEventRecord(fork, s) == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+        for (int i = 0; i < nside && rc == CONV_OK; ++i)
+            if (cudaStreamWaitEvent(side[i], fork, 0) != cudaSuccess) rc = CONV_ERR_CUDA;
+        for (size_t i = 0; i < ph.size() && rc == CONV_OK; ++i) rc = run_class(ph[i], side[i % nside]);
+        // join every side stream back, whatever happened above, so that the
+        // caller's stream (or its capture) is left whole
+        for (int i = 0; i < nside; ++i) {
+            cudaEvent_t join;
+            if (cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
+                rc = CONV_ERR_CUDA;
                 continue;
             }
-            if ((st = igemm_pack_filter_launch(c.g, c.pl, w_dev + c.w_origin, workspace, stream))) return st;
-            if ((st = igemm_main_launch(c.g, c.pl, dy_dev, y, nullptr, workspace, stream))) return st;
+            if (cudaEventRecord(join, side[i]) != cudaSuccess || cudaStreamWaitEvent(s, join, 0) != cudaSuccess)
+                rc = CONV_ERR_CUDA;
+            cudaEventDestroy(join);
         }
-        return CONV_OK;
+        cudaEventDestroy(fork);
+        return rc;
     }
     const GradArgs a = [&] {
         GradArgs r = grad_args(dx, w, dy, p);

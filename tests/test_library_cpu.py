@@ -348,12 +348,12 @@ def test_gradient_validation_and_routes(ic):
     assert code(ic.dgrad_workspace_size, dy, w, dx, pa) == S["CONV_ERR_BAD_PARAM"]
     pg = ic.Params.make(padding=(1, 1), algo=ic.ALGO_IMPLICIT_GEMM)
     assert ic.wgrad_workspace_size(x, dy, dw, pg) > 0
-    # stride 2: four residue classes on the tensor cores, the workspace of the
-    # largest (2 x 2 taps of the 3 x 3 filter, one 128-channel tile, one
-    # channel step of 64 f16)
+    # stride 2: four residue classes on the tensor cores, each with its own
+    # filter blocks (1 x 1, 1 x 2, 2 x 1 and 2 x 2 taps of the 3 x 3 filter,
+    # one 128-channel tile, one channel step of 64 f16 per tap)
     dy2 = d(ic.CONV_INT8, (2, 32, 7, 7), "NHWC")
     p2 = ic.Params.make(pre_padding=(1, 1), post_padding=(0, 0), stride=(2, 2))
-    assert ic.dgrad_workspace_size(dy2, w, dx, p2) == 2 * 2 * 128 * 128
+    assert ic.dgrad_workspace_size(dy2, w, dx, p2) == (1 + 2 + 2 + 4) * 128 * 128
     # padding wider than the filter's reach (3 > 2): one class, windows that
     # start inside dY
     dy3 = d(ic.CONV_INT8, (2, 32, 18, 18), "NHWC")
