@@ -163,10 +163,11 @@ struct IgemmArgs {
     int32_t pad_h, pad_w, str_h, str_w, dil_h, dil_w;
     int32_t m_total, n_tiles, num_tiles;
     // Work units.  Units below full_units are whole tiles (unit u = tile u).
-    // When there are fewer tiles than SMs and each has a long reduction, the
-    // tiles are cut into `splits` runs of k-steps instead: unit
-    // full_units + t covers run t % splits of tile full_units + t / splits,
-    // and writes its raw int32 sums to tail_part for the reduction kernel.
+    // The tiles from full_units on (all of them when there are fewer tiles
+    // than SMs and long reductions; a short partial last round otherwise)
+    // are cut into `splits` runs of k-steps: unit full_units + t covers run
+    // t % splits of tile full_units + t / splits, and writes its raw int32
+    // sums to tail_part for the reduction kernel.
     int32_t full_units, splits, num_units;
     int32_t *tail_part;  // [cut tile][split][MT rows][NT columns]
     int32_t relu, y_vec;
@@ -1077,6 +1078,7 @@ inline int64_t align256(int64_t v) { return (v + 255) & ~255LL; }
 constexpr int64_t kSplitMinKSteps = 64;  // only reductions at least this long are cut
 constexpr int64_t kMinSplitSteps = 16;   // k-steps of the shortest run of a cut tile
 constexpr int64_t kMaxSplits = 32;
+constexpr int64_t kMinTailSteps = 4;     // k-steps of the shortest run of a last-round tile
 
 template <int NT, bool kTma>
 conv_status launch_conv(const IgemmArgs &a, int grid, cudaStream_t st) {
@@ -1270,9 +1272,12 @@ void igemm_plan(const ConvGeom &g, const void *x_dev, IgemmPlan *pl) {
     // into as many runs as keep the SMs busy, each at least kMinSplitSteps
     // long; the reduction kernel adds the runs' int32 sums and finishes the
     // tiles.
-    // (Cutting the partial last round of a many-tile call the same way was
-    // measured: the convolution gets 11% shorter on the 3x3 workload, but
-    // writing the runs' sums and the reduction kernel cost more than that.)
+    // With more tiles than SMs and a short partial last round (rem tiles, at
+    // most a quarter of the SMs), the tiles of that round are cut the same
+    // way into runs of at least kMinTailSteps k-steps: the round takes a
+    // fraction of a tile's time instead of a whole one.  (Longer last rounds
+    // were measured too: the reduction of their runs costs more than it
+    // saves.)
     const int64_t tiles = pl->m_tiles * pl->n_tiles;
     const int64_t sms = device_sm_count();
     pl->splits = 1;
@@ -1284,6 +1289,15 @@ void igemm_plan(const ConvGeom &g, const void *x_dev, IgemmPlan *pl) {
         if (sp >= 2) {
             pl->splits = sp;
             cut_tiles = tiles;
+        }
+    } else if (tiles > sms && tiles % sms != 0 && tiles % sms <= sms / 4 && pl->k_steps >= 4 * kMinTailSteps) {
+        const int64_t rem = tiles % sms;
+        int64_t sp = sms / rem;
+        if (sp > pl->k_steps / kMinTailSteps) sp = pl->k_steps / kMinTailSteps;
+        if (sp > kMaxSplits) sp = kMaxSplits;
+        if (sp >= 4) {
+            pl->splits = sp;
+            cut_tiles = rem;
         }
     }
     pl->full_units = tiles - cut_tiles;

@@ -76,7 +76,8 @@ struct IgemmPlan {
     int64_t m_tiles;        // ceil(N*P*Q / kIgemmMTile)
     size_t wpack_bytes;     // repacked filter
     size_t xpack_bytes;     // channels-last image copy (0 if not needed)
-    // Work split: with few tiles and long reductions each tile is cut into
+    // Work split: with few tiles and long reductions each tile, and with a
+    // short partial last round of tiles each tile of that round, is cut into
     // `splits` runs of k-steps computed by different CTAs (splits == 1: whole
     // tiles, full_units == num_units == tiles).
     int64_t full_units, splits, num_units, grid;
