@@ -159,9 +159,12 @@ conv_status conv_fprop_plan(const conv_tensor_desc *x, const conv_tensor_desc *w
                             int32_t *algo_out);
 
 /* Bytes of device workspace conv_fprop needs for this call (0 for the direct
- * kernels; the repacked half-precision filter, plus a channels-last copy of
- * the image when its strides do not allow direct loads, for the implicit
- * GEMM).  The caller allocates it, 256-byte aligned.  The size assumes a
+ * kernels; for the implicit GEMM the repacked half-precision filter, plus
+ * the int32 partial sums of tiles whose reduction is cut over several SMs
+ * (calls with fewer tiles than SMs and long reductions, or a short partial
+ * last round of tiles), plus a channels-last copy of the image when its
+ * strides do not allow direct loads).  The caller allocates it, 256-byte
+ * aligned.  The size assumes a
  * 16-byte-aligned image pointer (as every cudaMalloc or PyTorch allocation
  * is); with a misaligned one the image needs the copy too, and conv_fprop
  * returns CONV_ERR_WORKSPACE if the workspace cannot hold it. */
