@@ -900,8 +900,9 @@ __global__ void igemm_pack_filter_kernel(const int8_t *w, int64_t ws0, int64_t w
 // one cut tile, one quad per thread: each warp reads 32 consecutive rows of
 // one quad (512 contiguous bytes per run), four runs' loads in flight; the
 // sums go through a shared tile so that the stores run with columns fastest
-// when the output's channels are contiguous (128 contiguous bytes of int32
-// per warp), rows fastest otherwise (consecutive pixels of one channel).
+// when the output's channels are contiguous (a thread stores four channels
+// of one pixel, eight threads a pixel's 32), rows fastest otherwise
+// (consecutive pixels of one channel).
 constexpr int kRedRows = 32, kRedCols = 32, kRedPitch = kRedCols + 4;  // int32 per shared row
 __global__ void __launch_bounds__(256) igemm_split_reduce_kernel(const int32_t *part, int32_t tile0,
                                                                  int32_t tiles, int32_t splits,
@@ -941,24 +942,57 @@ __global__ void __launch_bounds__(256) igemm_split_reduce_kernel(const int32_t *
         }
         *reinterpret_cast<int4 *>(sums + lr * kRedPitch + lq * 4) = v;
         __syncthreads();
-        for (int i = threadIdx.x; i < kRedRows * kRedCols; i += blockDim.x) {
-            const int row = chan_fast ? i / kRedCols : i % kRedRows;
-            const int col = chan_fast ? i % kRedCols : i / kRedRows;
+        if (chan_fast) {
+            // thread = (row, 4 columns): one pixel decomposition, four
+            // consecutive channels (16 bytes of int32 when aligned)
+            const int row = threadIdx.x / (kRedCols / 4), c0 = (threadIdx.x % (kRedCols / 4)) * 4;
             const int m = mt * MT + rb * kRedRows + row;
-            const int k = nt * nt_cols + qb * kRedCols + col;
-            if (m >= m_total || k >= K) continue;
-            int32_t val = sums[row * kRedPitch + col];
-            if (bias) val = (int32_t)((uint32_t)val + (uint32_t)__ldg(bias + k));
-            if (relu) val = max(val, 0);
-            const int n = m / pq;
-            const int rem = m - n * pq;
-            const int p = rem / Q;
-            const int q = rem - p * Q;
-            const int64_t off = (int64_t)n * ys_n + (int64_t)p * ys_p + (int64_t)q * ys_q + (int64_t)k * ys_k;
-            if (out_int8)
-                static_cast<int8_t *>(y)[off] = requant_i8(val, out_shift);
-            else
-                static_cast<int32_t *>(y)[off] = val;
+            const int k0 = nt * nt_cols + qb * kRedCols + c0;
+            if (m < m_total && k0 < K) {
+                const int n = m / pq;
+                const int rem = m - n * pq;
+                const int p = rem / Q;
+                const int q = rem - p * Q;
+                const int64_t yoff = (int64_t)n * ys_n + (int64_t)p * ys_p + (int64_t)q * ys_q;
+                int32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    int32_t val = sums[row * kRedPitch + c0 + e];
+                    if (bias && k0 + e < K) val = (int32_t)((uint32_t)val + (uint32_t)__ldg(bias + k0 + e));
+                    o[e] = relu ? max(val, 0) : val;
+                }
+                if (!out_int8 && k0 + 3 < K && ((uintptr_t)(static_cast<int32_t *>(y) + yoff + k0) & 15) == 0) {
+                    *reinterpret_cast<int4 *>(static_cast<int32_t *>(y) + yoff + k0) = make_int4(o[0], o[1], o[2], o[3]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (k0 + e >= K) break;
+                        if (out_int8)
+                            static_cast<int8_t *>(y)[yoff + k0 + e] = requant_i8(o[e], out_shift);
+                        else
+                            static_cast<int32_t *>(y)[yoff + k0 + e] = o[e];
+                    }
+                }
+            }
+        } else {
+            for (int i = threadIdx.x; i < kRedRows * kRedCols; i += blockDim.x) {
+                const int row = i % kRedRows, col = i / kRedRows;  // consecutive pixels of one channel
+                const int m = mt * MT + rb * kRedRows + row;
+                const int k = nt * nt_cols + qb * kRedCols + col;
+                if (m >= m_total || k >= K) continue;
+                int32_t val = sums[row * kRedPitch + col];
+                if (bias) val = (int32_t)((uint32_t)val + (uint32_t)__ldg(bias + k));
+                if (relu) val = max(val, 0);
+                const int n = m / pq;
+                const int rem = m - n * pq;
+                const int p = rem / Q;
+                const int q = rem - p * Q;
+                const int64_t off = (int64_t)n * ys_n + (int64_t)p * ys_p + (int64_t)q * ys_q + (int64_t)k * ys_k;
+                if (out_int8)
+                    static_cast<int8_t *>(y)[off] = requant_i8(val, out_shift);
+                else
+                    static_cast<int32_t *>(y)[off] = val;
+            }
         }
         __syncthreads();  // the next block's sums overwrite the tile
     }
