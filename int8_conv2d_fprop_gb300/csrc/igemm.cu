@@ -18,10 +18,11 @@
 // Persistent, warp-specialised CTA (one per SM), 512 threads, tile 128 pixels
 // x NT output channels (NT = 128 or 256).  Two ways to stage the image tile:
 //  * TMA (default): warp 5 lane 0 issues one TMA im2col load per k-step (128
-//    output pixels x 64 channels of one tap, zero outside the image) into an
-//    8-deep int8 staging ring; warpgroup 0 converts each staged tile to f16
-//    into the 128-byte-swizzled A stage; warp 6 lane 0 brings the matching
-//    pre-swizzled f16 filter block with one bulk async copy.
+//    output pixels x 64 channels of one tap, zero outside the image) into a
+//    6-deep (NT = 256) or 8-deep (NT = 128) int8 staging ring; warpgroup 0
+//    converts each staged tile to f16 into the 128-byte-swizzled A stage;
+//    warp 6 lane 0 brings the matching pre-swizzled f16 filter block with
+//    one bulk async copy.
 //  * global loads (fallback when an im2col map cannot express the call):
 //    warpgroup 0 threads each own one pixel row, gather 64 channels of one tap
 //    with 16-byte loads one item ahead (address formed from stride, padding
@@ -31,7 +32,11 @@
 // (M=128, N=NT, K=16 per instruction) into one of two accumulator slots:
 //   warpgroups 2-3  epilogue, two warps per tensor-memory lane quadrant, each
 //                owning NT/2 columns: tcgen05.ld each finished slot,
-//                f32 -> int32, sum the groups, add bias, ReLU, store int32.
+//                f32 -> int32, sum the groups, add bias, ReLU, optional int8
+//                requantisation, TMA tensor stores (or plain stores).
+// Work comes in units: whole tiles round by round, or runs of k-steps of cut
+// tiles (few tiles with long reductions; a short partial last round) whose
+// int32 sums igemm_split_reduce_kernel adds.
 // Registers are moved from warpgroups 0-1 to the epilogue with setmaxnreg.
 // Every wait is bounded in time; on expiry the CTA records
 // CONV_ERR_DEVICE_TIMEOUT, stops, lets issued copies and MMAs finish and frees
