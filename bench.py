@@ -386,7 +386,7 @@ def run_ours(args):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps if algo == ic.ALGO_IMPLICIT_GEMM else args.steps,
+        "gpu_launches": ic.kernel_count(xd, wd, yd, p) * args.steps,
         "clocks": clocks,
     }
     if rank == 0:

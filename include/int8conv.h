@@ -172,6 +172,16 @@ conv_status conv_fprop_workspace_size(const conv_tensor_desc *x, const conv_tens
                                       const conv_tensor_desc *y, const conv_fprop_params *p,
                                       size_t *bytes);
 
+/* Number of kernels conv_fprop launches for this call, under the same
+ * assumption of a 16-byte aligned image pointer: 0 for an empty output, 1
+ * for the direct kernels; for the implicit GEMM the filter repack, the
+ * channels-last image copy when needed, the convolution, and the reduction
+ * of cut tiles when the call cuts them.  conv_fprop_pack_filter launches the
+ * first of these, conv_fprop_prepacked the rest.  Errors as
+ * conv_fprop_validate; CONV_ERR_NULL_PTR if count is NULL. */
+conv_status conv_fprop_kernel_count(const conv_tensor_desc *x, const conv_tensor_desc *w,
+                                    const conv_tensor_desc *y, const conv_fprop_params *p, int32_t *count);
+
 /*
  * Y = conv_fprop(X, W) on `stream` (a cudaStream_t; NULL = legacy default).
  * x_dev, w_dev, y_dev, bias_dev and workspace are device pointers on the

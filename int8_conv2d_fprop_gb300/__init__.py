@@ -46,6 +46,7 @@ STATUS_CODE = {v: k for k, v in STATUS.items()}
 EXPORTED_SYMBOLS = (
     "conv_params_init", "conv_params_set_symmetric_padding", "conv_tensor_desc_packed",
     "conv_fprop_output_dims", "conv_fprop_validate", "conv_fprop_plan", "conv_fprop_workspace_size",
+    "conv_fprop_kernel_count",
     "conv_fprop", "conv_fprop_pack_filter", "conv_fprop_prepacked", "conv_fprop_static_workspace",
     "conv_fprop_host_buffer_size", "conv_fprop_host", "conv_device_status",
     "conv_selftest_wait_timeout", "conv_status_string", "conv_library_version",
@@ -150,6 +151,7 @@ def lib():
         L.conv_fprop_validate.argtypes = [D, D, D, P, ctypes.c_int64]
         L.conv_fprop_plan.argtypes = [D, D, D, P, ctypes.POINTER(ctypes.c_int32)]
         L.conv_fprop_workspace_size.argtypes = [D, D, D, P, ctypes.POINTER(ctypes.c_size_t)]
+        L.conv_fprop_kernel_count.argtypes = [D, D, D, P, ctypes.POINTER(ctypes.c_int32)]
         L.conv_fprop.argtypes = [D, ctypes.c_void_p, D, ctypes.c_void_p, D, ctypes.c_void_p, ctypes.c_void_p,
                                  P, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
         L.conv_fprop_pack_filter.argtypes = [D, D, ctypes.c_void_p, D, P, ctypes.c_void_p, ctypes.c_size_t,
@@ -214,6 +216,14 @@ def workspace_size(xd: TensorDesc, wd: TensorDesc, yd: TensorDesc, p: Params) ->
     out = ctypes.c_size_t()
     _check(lib().conv_fprop_workspace_size(ctypes.byref(xd), ctypes.byref(wd), ctypes.byref(yd),
                                            ctypes.byref(p), ctypes.byref(out)), "workspace size")
+    return int(out.value)
+
+
+def kernel_count(xd: TensorDesc, wd: TensorDesc, yd: TensorDesc, p: Params) -> int:
+    """Kernels conv_fprop launches for this call (see the header)."""
+    out = ctypes.c_int32()
+    _check(lib().conv_fprop_kernel_count(ctypes.byref(xd), ctypes.byref(wd), ctypes.byref(yd), ctypes.byref(p),
+                                         ctypes.byref(out)), "kernel count")
     return int(out.value)
 
 

@@ -167,6 +167,24 @@ conv_status conv_fprop_workspace_size(const conv_tensor_desc *x, const conv_tens
     return CONV_OK;
 }
 
+conv_status conv_fprop_kernel_count(const conv_tensor_desc *x, const conv_tensor_desc *w,
+                                    const conv_tensor_desc *y, const conv_fprop_params *p, int32_t *count) {
+    if (!count) return CONV_ERR_NULL_PTR;
+    ConvGeom g;
+    IgemmPlan pl;
+    int algo = 0;
+    conv_status st = plan_call(x, w, y, p, nullptr, &g, &algo, &pl);
+    if (st) return st;
+    if (g.N == 0 || g.K == 0 || g.P == 0 || g.Q == 0) {
+        *count = 0;
+    } else if (algo != CONV_ALGO_IMPLICIT_GEMM) {
+        *count = 1;
+    } else {
+        *count = 2 + (pl.pack_x ? 1 : 0) + (pl.splits > 1 ? 1 : 0);
+    }
+    return CONV_OK;
+}
+
 namespace {
 
 // Validation, planning and pointer checks shared by the three entry points

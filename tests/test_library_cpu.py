@@ -195,10 +195,23 @@ def test_unit_dim_strides_are_ignored(ic):
 def test_planner_choices_and_workspace(ic):
     algo = {}
     ws = {}
+    kernels = {}
     for name, cfg in synth.CONFIGS.items():
         xd, wd, yd, p = _descs(ic, cfg)
         algo[name] = ic.plan(xd, wd, yd, p)
         ws[name] = ic.workspace_size(xd, wd, yd, p)
+        kernels[name] = ic.kernel_count(xd, wd, yd, p)
+    # kernels per call: one direct kernel; filter repack + convolution, plus
+    # the channels-last copy of C5's NCHW image (no GPU here: one SM, so no
+    # call cuts its tiles)
+    assert kernels == {"c1_tiny_nchw": 1, "p4_shape": 1, "c2_s2_nhwc": 2, "c3_3x3_large": 2,
+                       "c4_1x1_bias_relu": 2, "c5_7x1_dilated_conv": 3}
+    # an empty batch launches nothing
+    cfg = synth.CONFIGS["c3_3x3_large"]
+    xd = ic.TensorDesc.make(ic.CONV_INT8, (0, 256, 56, 56), (56 * 56 * 256, 1, 56 * 256, 256), 0)
+    yd = ic.TensorDesc.make(ic.CONV_INT32, (0, 256, 56, 56), (56 * 56 * 256, 1, 56 * 256, 256), 0)
+    _, wd, _, p = _descs(ic, cfg)
+    assert ic.kernel_count(xd, wd, yd, p) == 0
     assert algo["c1_tiny_nchw"] == ic.ALGO_DIRECT_DP4A
     assert algo["p4_shape"] == ic.ALGO_DIRECT_DP4A
     for name in ("c2_s2_nhwc", "c3_3x3_large", "c4_1x1_bias_relu", "c5_7x1_dilated_conv"):
