@@ -99,6 +99,19 @@ conv_status host_plan(const conv_tensor_desc *x, const conv_tensor_desc *w, cons
     yc.capacity_bytes = (uint64_t)(hp->y_chunk_elems * hp->y_esz);
     hp->ws_bytes = 0;
     if (hp->per_chunk > 0 && (st = conv_fprop_workspace_size(&xc, w, &yc, p, &hp->ws_bytes))) return st;
+    // the last chunk may hold fewer images, and with fewer tiles its plan may
+    // cut tiles along the reduction where the full chunks' plan does not:
+    // the workspace serves both
+    const int64_t last = N - (int64_t)(hp->chunks - 1) * hp->per_chunk;
+    if (hp->chunks > 1 && last > 0 && last != hp->per_chunk) {
+        conv_tensor_desc xl = *x, yl = *y;
+        xl.dims[0] = yl.dims[0] = last;
+        xl.capacity_bytes = (uint64_t)extent_of_images(x, last);
+        yl.capacity_bytes = (uint64_t)(extent_of_images(y, last) * hp->y_esz);
+        size_t wl = 0;
+        if ((st = conv_fprop_workspace_size(&xl, w, &yl, p, &wl))) return st;
+        if (wl > hp->ws_bytes) hp->ws_bytes = wl;
+    }
     size_t off = 0;
     hp->off_w = off;
     off = align256(off + (size_t)hp->w_elems);
