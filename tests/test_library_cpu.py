@@ -322,8 +322,9 @@ def test_call_checks_before_any_device_work(ic):
 def test_gradient_validation_and_routes(ic):
     """conv_dgrad / conv_wgrad take the forward call's descriptors and
     parameters: shapes, types, epilogue, algorithm and the int32 bound are
-    checked; dgrad with stride 1 and padding within the filter's reach takes
-    the tensor-core route (a workspace), everything else the CUDA-core kernels."""
+    checked; dgrad takes the tensor-core route (one forward convolution per
+    residue class of the stride, each with its own workspace) up to 64
+    classes, the CUDA-core kernel beyond that or when forced."""
     def d(dtype, dims, layout):
         return ic.TensorDesc.packed(dtype, dims, layout)
 
@@ -390,3 +391,41 @@ def test_gradient_validation_and_routes(ic):
     xs = d(ic.CONV_INT8, (1, 8, 362, 362), "NHWC")      # 131044 pixels fit
     dys = d(ic.CONV_INT8, (1, 4, 362, 362), "NHWC")
     assert ic.wgrad_workspace_size(xs, dys, dwl, ic.Params.make()) >= 0
+
+
+def _class_taps(rho, pre, stride, dil, taps):
+    """Taps of one axis that reach the pixels h = rho (mod stride) of dX: the
+    r with r*dil = rho + pre (mod stride), by direct enumeration."""
+    return sum(1 for r in range(taps) if (r * dil - rho - pre) % stride == 0)
+
+
+@pytest.mark.parametrize("stride,dil,pre,post,R,S", [
+    ((2, 2), (1, 1), (1, 1), (0, 0), 3, 3),
+    ((3, 2), (2, 3), (2, 1), (1, 2), 5, 4),
+    ((2, 3), (2, 3), (0, 2), (1, 0), 3, 3),   # stride and dilation share a factor
+    ((4, 4), (1, 1), (3, 3), (2, 3), 7, 7),
+    ((2, 2), (1, 1), (0, 0), (0, 0), 1, 1),   # three of four classes untouched
+    ((1, 1), (2, 1), (5, 0), (1, 2), 3, 3),   # padding wider than the reach (5 > 4)
+])
+def test_dgrad_residue_class_workspace(ic, stride, dil, pre, post, R, S):
+    """The data gradient's workspace is the sum over the residue classes of
+    the stride of each class's repacked filter: (taps of the class in H) x
+    (taps in W) k-steps of 128 filter rows x 64 f16 channels (one tile of
+    output channels, one channel step).  The tap counts come from
+    enumerating the taps, not from the library's closed form."""
+    def d(dtype, dims, layout):
+        return ic.TensorDesc.packed(dtype, dims, layout)
+    H, W = 23, 21
+    P = (H + pre[0] + post[0] - dil[0] * (R - 1) - 1) // stride[0] + 1
+    Q = (W + pre[1] + post[1] - dil[1] * (S - 1) - 1) // stride[1] + 1
+    dy = d(ic.CONV_INT8, (2, 48, P, Q), "NHWC")
+    w = d(ic.CONV_INT8, (48, 40, R, S), "KRSC")
+    dx = d(ic.CONV_INT32, (2, 40, H, W), "NHWC")
+    p = ic.Params.make(pre_padding=pre, post_padding=post, stride=stride, dilation=dil)
+    want = 0
+    for rh in range(stride[0]):
+        for rw in range(stride[1]):
+            th = _class_taps(rh, pre[0], stride[0], dil[0], R)
+            tw = _class_taps(rw, pre[1], stride[1], dil[1], S)
+            want += th * tw * 128 * 128  # zero taps: a zero-filled class, no workspace
+    assert ic.dgrad_workspace_size(dy, w, dx, p) == want
