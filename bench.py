@@ -15,6 +15,17 @@ with cold caches.  Under torchrun each rank runs its own copy of the workload
 (weak scaling, no collective on the data path); the elapsed time is the max
 over ranks.  ``--impl reference`` times the CPU oracle on the host cores
 instead (rank 0 only).
+
+The line's ``workloads`` map holds one record per workload of the
+specification (the five shapes, ``--workloads``), each over ``--launches``
+launches with a cold L2: the step and the convolution call alone, as the
+average of back-to-back launches over rotating sets (the large workloads) or
+the median of launches each timed by its own events after a 258 MiB write
+(the small ones); the isolated medians beside them; the step with a warm L2;
+and a roofline per workload.  The headline ``roofline.kernel_ms`` is the
+convolution call of the headline workload's record.  ``int8_routes`` holds
+the measured dense rates of the int8-capable instruction routes
+(conv_measure_peak_rates).
 """
 from __future__ import annotations
 
@@ -41,7 +52,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 DOMINANT_KERNEL_SRC = os.path.join(ROOT, "int8_conv2d_fprop_gb300", "csrc", "igemm.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "igemm_traffic.json")
 L2_BYTES = 129 * 1024 * 1024
-KERNEL_SAMPLE = 8  # one timed step in this many carries events around the convolution kernel
+ALL_WORKLOADS_DEFAULT = ("c1_tiny_nchw", "c2_s2_nhwc", "c3_3x3_large", "c4_1x1_bias_relu", "c5_7x1_dilated_conv")
 
 
 def parse_args(argv=None):
@@ -51,12 +62,20 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="c3_3x3_large", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--workloads", default=",".join(ALL_WORKLOADS_DEFAULT),
+                    help="comma-separated workloads timed one by one into the line's 'workloads' map "
+                         "(empty: none)")
+    ap.add_argument("--launches", type=int, default=60,
+                    help="event-timed launches behind each median of the 'workloads' map (>= 50)")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="fprop", choices=["fprop", "fprop_int8", "dgrad", "wgrad", "graph"],
+    ap.add_argument("--no-peak-probe", action="store_true",
+                    help="skip the measured instruction-route rates (conv_measure_peak_rates)")
+    ap.add_argument("--op", default="fprop", choices=["fprop", "fprop_int8", "dgrad", "wgrad", "graph", "peaks"],
                     help="fprop: the headline line; the others time the extensions on the same workload "
-                         "(int8 output, data gradient, weight gradient, CUDA-graph replay vs eager calls)")
+                         "(int8 output, data gradient, weight gradient, CUDA-graph replay vs eager calls), "
+                         "or print the measured instruction-route rates (peaks)")
     return ap.parse_args(argv)
 
 
@@ -170,10 +189,215 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ---------------------------------------------------------------------- workloads on the device
+ROTATE_MIN_BYTES = 16 << 20   # image+output sets at least this large rotate to keep L2 cold; smaller ones flush it
+FLUSH_BYTES = 2 * L2_BYTES    # written between cold launches of the small workloads
+HOST_AHEAD_CYCLES = 20_000_000  # GPU spin (~10 ms) before an event-timed loop: the host queues it meanwhile
+IMAD_PER_SM_CLK = 64          # 32-bit integer multiply-adds per SM per clock (CUDA cores)
+
+
+def workload_label(cfg) -> str:
+    """The workload's name and every size that defines it (both arms print this)."""
+    return (f"{cfg.name}: N={cfg.N} C={cfg.C} H={cfg.H} W={cfg.W} K={cfg.K} R={cfg.R} "
+            f"S={cfg.S} stride={cfg.stride} pad={cfg.pre}/{cfg.post} dil={cfg.dilation} "
+            f"mode={'conv' if cfg.mode else 'xcorr'} x={cfg.x_layout} w={cfg.w_layout} "
+            f"y={cfg.y_layout} bias={cfg.bias} relu={cfg.relu}")
+
+
+def rotating_sets(cfg) -> int:
+    """Image/output sets to rotate over so that every call starts with a cold
+    L2 (1: the set is small and the L2 is flushed instead)."""
+    set_bytes = cfg.N * cfg.C * cfg.H * cfg.W + 4 * cfg.N * cfg.K * cfg.P * cfg.Q
+    if set_bytes < ROTATE_MIN_BYTES:
+        return 1
+    return max(2, int(np.ceil(3 * L2_BYTES / set_bytes)) + 1)
+
+
+class DeviceWorkload:
+    """One workload resident on a device, called the way the benchmark times
+    it: conv_fprop_pack_filter (the filter repack) then conv_fprop_prepacked
+    (the convolution) through the C ABI, over ``nsets`` image/output sets."""
+
+    def __init__(self, ic, cfg, dev, nsets: int = 1):
+        import torch
+        self.ic, self.cfg, self.dev, self.nsets = ic, cfg, dev, nsets
+        self.x, self.w, self.b = synth.make_inputs(cfg)
+        self.xf, self.xs = synth.place(self.x, cfg.x_layout)
+        self.wf, self.ws = synth.place(self.w, cfg.w_layout)
+        self.ystr = synth.packed_strides(cfg.y_dims, cfg.y_layout)
+        self.ysz = int(np.prod(cfg.y_dims))
+        self.x_dev = [torch.from_numpy(self.xf).to(dev) for _ in range(nsets)]
+        self.y_dev = [torch.empty(self.ysz, dtype=torch.int32, device=dev) for _ in range(nsets)]
+        self.w_dev = torch.from_numpy(self.wf).to(dev)
+        self.b_dev = torch.from_numpy(self.b).to(dev) if self.b is not None else None
+        self.xd = ic.TensorDesc.make(ic.CONV_INT8, cfg.x_dims, self.xs, self.xf.size)
+        self.wd = ic.TensorDesc.make(ic.CONV_INT8, cfg.w_dims, self.ws, self.wf.size)
+        self.yd = ic.TensorDesc.make(ic.CONV_INT32, cfg.y_dims, self.ystr, self.ysz * 4)
+        self.p = ic.Params.make(cfg.pre, cfg.post, cfg.stride, cfg.dilation, cfg.mode, cfg.bias, cfg.relu)
+        self.algo = ic.plan(self.xd, self.wd, self.yd, self.p)
+        self.ws_bytes = ic.workspace_size(self.xd, self.wd, self.yd, self.p)
+        self.work = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
+        self.kernels_per_step = ic.kernel_count(self.xd, self.wd, self.yd, self.p)
+        self.bias_ptr = self.b_dev.data_ptr() if self.b_dev is not None else 0
+
+    def pack(self, sh: int) -> None:
+        st = self.ic.pack_filter_raw(self.xd, self.wd, self.w_dev.data_ptr(), self.yd, self.p, self.work.data_ptr(),
+                                     self.ws_bytes, sh)
+        if st:
+            raise self.ic.ConvError(st, "pack filter")
+
+    def conv(self, i: int, sh: int) -> None:
+        s = i % self.nsets
+        st = self.ic.conv_fprop_prepacked_raw(self.xd, self.x_dev[s].data_ptr(), self.wd, self.w_dev.data_ptr(),
+                                              self.yd, self.y_dev[s].data_ptr(), self.bias_ptr, self.p,
+                                              self.work.data_ptr(), self.ws_bytes, sh)
+        if st:
+            raise self.ic.ConvError(st, "conv")
+
+    def step(self, i: int, sh: int) -> None:
+        self.pack(sh)
+        self.conv(i, sh)
+
+    def output(self, i: int = 0) -> np.ndarray:
+        """Logical [N,K,P,Q] int32 output of set i (after a synchronize)."""
+        return synth.gather_logical(self.y_dev[i % self.nsets].cpu().numpy(), self.cfg.y_dims, self.ystr)
+
+
+def roofline_of(cfg, algo_name: str, kernel_ms: float, peaks: dict, peak_src: str) -> dict:
+    """Roofline of one convolution call: tensor floor (ops / bf16 peak) against
+    the HBM floor (algorithmic bytes / copy bandwidth) for the tensor-core
+    route, the CUDA cores' integer rate for the direct kernels."""
+    bf16 = _peak_value(peaks, ("bf16_tflops", "bf16_dense_tflops"))
+    bsrc = peak_src
+    if bf16 is None:
+        bf16, bsrc = FALLBACK_PEAKS["bf16_tflops"], "fallback"
+    hbm = _peak_value(peaks, ("hbm_gbs",))
+    hsrc = peak_src
+    if hbm is None:
+        hbm, hsrc = FALLBACK_PEAKS["hbm_gbs"], "fallback"
+    alg_bytes = cfg.algorithmic_bytes()
+    tensor_floor_ms = cfg.ops / (bf16 * 1e12) * 1e3
+    hbm_floor_ms = alg_bytes / (hbm * 1e9) * 1e3
+    r = {"kernel_ms": round(kernel_ms, 5), "algorithmic_bytes": alg_bytes,
+         "tensor_floor_ms": round(tensor_floor_ms, 5), "hbm_floor_ms": round(hbm_floor_ms, 5)}
+    if not algo_name.startswith("implicit_gemm"):
+        alu = 152 * IMAD_PER_SM_CLK * 2 * 2.07e9 / 1e12
+        ach = cfg.ops / (kernel_ms * 1e-3) / 1e12
+        r.update({"bound": "alu", "achieved": round(ach, 6), "peak": round(alu, 2), "unit": "TOPS",
+                  "frac": round(ach / alu, 6),
+                  "peak_source": "152 SMs x 64 int32 multiply-adds/clk x 2 ops x 2.07 GHz (CUDA cores)"})
+    elif hbm_floor_ms > tensor_floor_ms:
+        gbs = alg_bytes / (kernel_ms * 1e-3) / 1e9
+        r.update({"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                  "frac": round(gbs / hbm, 4), "peak_source": f"{hsrc} HBM copy bandwidth",
+                  "tensor_frac": round(cfg.ops / (kernel_ms * 1e-3) / 1e12 / bf16, 4)})
+    else:
+        ach = cfg.ops / (kernel_ms * 1e-3) / 1e12
+        r.update({"bound": "tensor", "achieved": round(ach, 2), "peak": bf16, "unit": "TFLOP/s",
+                  "frac": round(ach / bf16, 4),
+                  "peak_source": f"{bsrc} bf16 dense burst (f16 operands run at the bf16 rate; sm_103a has "
+                                 "no integer tcgen05 MMA)"})
+    return r
+
+
+def _median(v):
+    return float(statistics.median(v)) if v else None
+
+
+def time_workload(ic, cfg, dev, stream, flush, iters: int, warmup: int, peaks: dict, peak_src: str) -> dict:
+    """Per-workload record: medians over ``iters`` event-timed launches of
+    the step (repack + convolution) and of the convolution alone, each with a
+    cold L2 (rotating sets, or a flush before each launch), and of the step
+    with a warm L2 (one set, back to back)."""
+    import torch
+    nsets = rotating_sets(cfg)
+    wl = DeviceWorkload(ic, cfg, dev, nsets)
+    sh = stream.cuda_stream
+    for i in range(warmup):
+        wl.step(i, sh)
+    torch.cuda.synchronize(dev)
+    st = ic.device_status(sh)
+    if st:
+        raise ic.ConvError(st, f"{cfg.name} warm-up")
+
+    def timed(fn, cold):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        torch.cuda._sleep(HOST_AHEAD_CYCLES)
+        for i in range(iters):
+            if cold and nsets == 1:
+                flush.zero_()
+            evs[i][0].record(stream)
+            fn(i + 1 if cold else 0)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b) for a, b in evs]
+
+    def looped(fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(HOST_AHEAD_CYCLES)
+        e0.record(stream)
+        for i in range(iters):
+            fn(i + 1)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / iters
+
+    step_ms = timed(lambda i: wl.step(i, sh), True)
+    conv_ms = timed(lambda i: wl.conv(i, sh), True)
+    warm_ms = timed(lambda i: wl.step(i, sh), False)
+    if nsets > 1:
+        # launches back to back over the rotating sets (every one cold): the
+        # average duration of a step and of a convolution call in a stream of
+        # them, as in the headline's timed region
+        step_avg, conv_avg = looped(lambda i: wl.step(i, sh)), looped(lambda i: wl.conv(i, sh))
+    st = ic.device_status(sh)
+    if st:
+        raise ic.ConvError(st, f"{cfg.name} timed launches")
+    algo = ic.ALGO_NAMES.get(wl.algo, str(wl.algo))
+    if nsets > 1:
+        ms, kms, how = step_avg, conv_avg, (f"average over {iters} back-to-back launches on rotating sets "
+                                            f"(events at the ends)")
+    else:
+        ms, kms, how = _median(step_ms), _median(conv_ms), (f"median of {iters} launches, each after an L2 "
+                                                            f"flush and timed with its own events")
+    rec = {
+        "workload": workload_label(cfg), "algo": algo, "ops": cfg.ops,
+        "ms": round(ms, 5), "value": round(cfg.ops / (ms * 1e-3) / 1e12, 3), "unit": "TOPS",
+        "kernel_ms": round(kms, 5), "kernel_share": round(kms / ms, 4), "timing": how,
+        "isolated_step_ms_median": round(_median(step_ms), 5),
+        "isolated_kernel_ms_median": round(_median(conv_ms), 5),
+        "warm_ms": round(_median(warm_ms), 5),
+        "warm_value": round(cfg.ops / (_median(warm_ms) * 1e-3) / 1e12, 3),
+        "launches_timed": iters, "kernels_per_step": wl.kernels_per_step,
+        "l2": (f"cold: rotating {nsets} resident sets" if nsets > 1 else
+               f"cold: {FLUSH_BYTES >> 20} MiB written before each launch") +
+              "; warm: one set, launches back to back, median of their own events",
+        "roofline": roofline_of(cfg, algo, kms, peaks, peak_src),
+    }
+    del wl
+    torch.cuda.empty_cache()
+    return rec
+
+
+def measure_routes(ic, dev, sh) -> dict:
+    """conv_measure_peak_rates over a 1 GiB scratch buffer: the dense rates of
+    tcgen05 kind::f16 (the route taken), warp-level mma.sync s8 and f16, dp4a,
+    and the copy bandwidth, with the SM clock seen."""
+    import torch
+    scratch = torch.empty((1 << 30) + 4096, dtype=torch.uint8, device=dev)
+    r = ic.measure_peak_rates(scratch.data_ptr(), scratch.numel(), sh)
+    del scratch
+    torch.cuda.empty_cache()
+    out = {k: round(v, 2) for k, v in r.items()}
+    out["note"] = ("sm_103a has no integer tcgen05 MMA; the convolution takes tcgen05 kind::f16 (exact by "
+                   "grouping), the fastest exact route measured here")
+    return out
+
+
 # ---------------------------------------------------------------------- oracle timing
 def time_oracle_sample(cfg, seconds: float, x, w, b):
     """Time the CPU oracle on a random sample of output points sized to take
-    about ``seconds``; returns (TOPS, threads, description)."""
+    about ``seconds``; returns (TOPS, threads, description, points)."""
     import oracle
     oracle.build()
     xf, xs = synth.place(x, cfg.x_layout)
@@ -202,6 +426,33 @@ def time_oracle_sample(cfg, seconds: float, x, w, b):
     return tops, oracle.num_threads(), desc, n
 
 
+def time_oracle_single_thread(names=("c1_tiny_nchw", "c2_s2_nhwc", "p4_shape")) -> dict:
+    """The oracle on one core over the whole output of small workloads."""
+    import oracle
+    oracle.build()
+    threads = oracle.num_threads()
+    out = {}
+    try:
+        oracle.set_num_threads(1)
+        for name in names:
+            cfg = synth.CONFIGS[name]
+            x, w, b = synth.make_inputs(cfg)
+            xf, xs = synth.place(x, cfg.x_layout)
+            wf, ws = synth.place(w, cfg.w_layout)
+            reps, dt = 0, 0.0
+            t0 = time.perf_counter()
+            while reps == 0 or (dt < 0.2 and reps < 10000):
+                oracle.conv_fprop(xf, cfg.x_dims, xs, wf, cfg.w_dims, ws, cfg.pre, cfg.post, cfg.stride,
+                                  cfg.dilation, cfg.mode, b, cfg.relu)
+                reps += 1
+                dt = time.perf_counter() - t0
+            out[name] = {"ms": round(1e3 * dt / reps, 4), "tops": round(cfg.ops * reps / dt / 1e12, 8),
+                         "ops": cfg.ops, "repeats": reps}
+    finally:
+        oracle.set_num_threads(threads)
+    return out
+
+
 # ---------------------------------------------------------------------- our arm
 def run_ours(args):
     import torch
@@ -213,94 +464,105 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     init_dist(world, "nccl")
     cfg = synth.CONFIGS[args.workload]
-    x, w, b = synth.make_inputs(cfg)
-    xf, xs = synth.place(x, cfg.x_layout)
-    wf, ws = synth.place(w, cfg.w_layout)
-    ystr = synth.packed_strides(cfg.y_dims, cfg.y_layout)
-    ysz = int(np.prod(cfg.y_dims))
-    set_bytes = xf.size + ysz * 4
-    nsets = max(2, int(np.ceil(3 * L2_BYTES / set_bytes)) + 1)
-    xs_dev = [torch.from_numpy(xf).to(dev) for _ in range(nsets)]
-    ys_dev = [torch.empty(ysz, dtype=torch.int32, device=dev) for _ in range(nsets)]
-    w_dev = torch.from_numpy(wf).to(dev)
-    b_dev = torch.from_numpy(b).to(dev) if b is not None else None
-    xd = ic.TensorDesc.make(ic.CONV_INT8, cfg.x_dims, xs, xf.size)
-    wd = ic.TensorDesc.make(ic.CONV_INT8, cfg.w_dims, ws, wf.size)
-    yd = ic.TensorDesc.make(ic.CONV_INT32, cfg.y_dims, ystr, ysz * 4)
-    p = ic.Params.make(cfg.pre, cfg.post, cfg.stride, cfg.dilation, cfg.mode, cfg.bias, cfg.relu)
-    algo = ic.plan(xd, wd, yd, p)
-    ws_bytes = ic.workspace_size(xd, wd, yd, p)
-    work = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    bias_ptr = b_dev.data_ptr() if b_dev is not None else 0
-
-    def step(i, ev_a=None, ev_b=None):
-        s = i % nsets
-        st = ic.pack_filter_raw(xd, wd, w_dev.data_ptr(), yd, p, work.data_ptr(), ws_bytes, sh)
-        if st:
-            raise ic.ConvError(st, "pack filter")
-        if ev_a is not None:
-            ev_a.record(stream)
-        st = ic.conv_fprop_prepacked_raw(xd, xs_dev[s].data_ptr(), wd, w_dev.data_ptr(), yd, ys_dev[s].data_ptr(),
-                                         bias_ptr, p, work.data_ptr(), ws_bytes, sh)
-        if st:
-            raise ic.ConvError(st, "conv")
-        if ev_b is not None:
-            ev_b.record(stream)
-
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize(dev)
-    status = ic.device_status(sh)
-    if status:
-        raise ic.ConvError(status, "warm-up")
-    # the convolution kernel's own duration is taken with events around it on
-    # every KERNEL_SAMPLE-th step of the timed region: an event recorded
-    # between the filter repack and the convolution keeps the convolution
-    # from starting during the repack (programmatic dependent launch), so
-    # the other steps run without one
-    sampled = list(range(0, args.steps, KERNEL_SAMPLE))
-    evs = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for i in sampled}
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    peaks, peak_src = load_peaks()
     uuid = None
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         uuid = str(local)
     sampler = ClockSampler(uuid)
-    barrier(world)
-    torch.cuda.synchronize(dev)
     sampler.start()
     time.sleep(0.15)
+
+    # measured rates of the int8-capable instruction routes (rank 0)
+    routes = None
+    if rank == 0 and not args.no_peak_probe:
+        routes = measure_routes(ic, dev, sh)
+
+    # every workload of the specification, one record each (rank 0)
+    per_workload = {}
+    if rank == 0 and args.workloads:
+        flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        for name in args.workloads.split(","):
+            per_workload[name] = time_workload(ic, synth.CONFIGS[name], dev, stream, flush, args.launches,
+                                               max(3, args.warmup if args.warmup < 20 else 20), peaks, peak_src)
+        del flush
+        torch.cuda.empty_cache()
+
+    # the headline: exactly K steps of the workload, back to back
+    nsets = max(2, rotating_sets(cfg))
+    wl = DeviceWorkload(ic, cfg, dev, nsets)
+    for i in range(args.warmup):
+        wl.step(i, sh)
+    torch.cuda.synchronize(dev)
+    status = ic.device_status(sh)
+    if status:
+        raise ic.ConvError(status, "warm-up")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    torch.cuda._sleep(HOST_AHEAD_CYCLES)
     e0.record(stream)
     for i in range(args.steps):
-        step(args.warmup + i, *evs.get(i, (None, None)))
+        wl.step(args.warmup + i, sh)
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    clocks = sampler.stop()
     barrier(world)
     elapsed_ms = e0.elapsed_time(e1)
-    main_ms = [a.elapsed_time(bb) for a, bb in evs.values()]
     status = ic.device_status(sh)
     if status:
         raise ic.ConvError(status, "timed region")
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
-    kernel_ms = statistics.mean(main_ms)
+    clocks = sampler.stop()
+    if clocks:
+        clocks["window"] = "whole GPU measurement (every workload's launches and the headline steps)"
+    ms_per_step = elapsed_ms / args.steps
+    value = world * cfg.ops / (ms_per_step * 1e-3) / 1e12
+    algo_name = ic.ALGO_NAMES.get(wl.algo, str(wl.algo))
+    gpu_launches = wl.kernels_per_step * args.steps
+
+    # kernel time of the headline workload: the median of its own record (or
+    # of a separate run of convolution-only launches when it has none)
+    head = per_workload.get(cfg.name)
+    if head is None:
+        flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        head = time_workload(ic, cfg, dev, stream, flush, args.launches, 3, peaks, peak_src)
+        del flush
+    roofline = dict(head["roofline"])
+    roofline["kernel"] = ("igemm_conv_kernel (+ igemm_split_reduce_kernel when the call cuts tiles)"
+                          if algo_name.startswith("implicit_gemm") else algo_name)
+    roofline["kernel_launches_timed"] = head["launches_timed"]
+    roofline["kernel_ms_source"] = ("convolution-only calls (conv_fprop_prepacked) with a cold L2: " +
+                                    head["timing"])
+    traffic = None
+    if os.path.exists(TRAFFIC_FILE):
+        try:
+            with open(TRAFFIC_FILE) as f:
+                tr = json.load(f)
+            src_sha = hashlib.sha256(open(DOMINANT_KERNEL_SRC, "rb").read()).hexdigest()
+            entry = tr.get("workloads", {}).get(args.workload)
+            if tr.get("kernel_src_sha256") == src_sha and entry:
+                traffic = entry.get("dram_bytes_per_launch")
+        except (OSError, ValueError):
+            traffic = None
+    roofline["traffic"] = traffic
 
     # end to end through the C ABI with host buffers (conv_fprop_host): every
     # step copies the image, filter and bias in from page-locked host memory
     # and the int32 output back, pipelined over the batch by the library
     e2e = None
     if args.e2e_steps > 0:
-        xh = torch.from_numpy(xf).pin_memory()
-        wh = torch.from_numpy(wf).pin_memory()
-        bh = torch.from_numpy(b).pin_memory() if b is not None else None
-        yh = torch.empty(ysz, dtype=torch.int32).pin_memory()
+        xh = torch.from_numpy(wl.xf).pin_memory()
+        wh = torch.from_numpy(wl.wf).pin_memory()
+        bh = torch.from_numpy(wl.b).pin_memory() if wl.b is not None else None
+        yh = torch.empty(wl.ysz, dtype=torch.int32).pin_memory()
+        xd, wd, yd, p = wl.xd, wl.wd, wl.yd, wl.p
+        del wl
+        torch.cuda.empty_cache()
         hbytes = ic.host_buffer_size(xd, wd, yd, p)
         hbuf = torch.empty(hbytes, dtype=torch.uint8, device=dev)
-        del xs_dev[1:], ys_dev[1:]  # free the rotating sets first
-        torch.cuda.empty_cache()
 
         def e2e_step():
             st = ic.conv_fprop_host_raw(xd, xh.data_ptr(), wd, wh.data_ptr(), yd, yh.data_ptr(),
@@ -322,72 +584,35 @@ def run_ours(args):
         status = ic.device_status(sh)
         if status:
             raise ic.ConvError(status, "end-to-end")
-        h2d = xf.size + wf.size + (b.size * 4 if b is not None else 0)
+        h2d = xh.numel() + wh.numel() + (bh.numel() * 4 if bh is not None else 0)
         e2e = {"value": round(world * cfg.ops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TOPS",
-               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(ysz * 4),
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(yh.numel() * 4),
                "api": "conv_fprop_host (C ABI, page-locked host buffers, batch pipelined in chunks)"}
-
-    ms_per_step = elapsed_ms / args.steps
-    value = world * cfg.ops / (ms_per_step * 1e-3) / 1e12
-    peaks, peak_src = load_peaks()
-    bf16 = _peak_value(peaks, ("bf16_tflops", "bf16_dense_tflops"))
-    if bf16 is None:
-        bf16, peak_src = FALLBACK_PEAKS["bf16_tflops"], "fallback"
-    achieved = cfg.ops / (kernel_ms * 1e-3) / 1e12
-    traffic = None
-    if os.path.exists(TRAFFIC_FILE):
-        try:
-            with open(TRAFFIC_FILE) as f:
-                tr = json.load(f)
-            src_sha = hashlib.sha256(open(DOMINANT_KERNEL_SRC, "rb").read()).hexdigest()
-            entry = tr.get("workloads", {}).get(args.workload)
-            if tr.get("kernel_src_sha256") == src_sha and entry:
-                traffic = entry.get("dram_bytes_per_launch")
-        except (OSError, ValueError):
-            traffic = None
-    hbm = _peak_value(peaks, ("hbm_gbs",))
-    hbm_src = peak_src if hbm is not None else "fallback"
-    hbm = hbm or FALLBACK_PEAKS["hbm_gbs"]
-    tensor_floor_ms = cfg.ops / (bf16 * 1e12) * 1e3
-    hbm_floor_ms = cfg.algorithmic_bytes() / (hbm * 1e9) * 1e3
-    roofline = {
-        "kernel": "igemm_conv_kernel" if algo == ic.ALGO_IMPLICIT_GEMM else ic.ALGO_NAMES.get(algo),
-        "traffic": traffic, "kernel_ms": round(kernel_ms, 5), "kernel_launches_timed": len(main_ms),
-        "algorithmic_bytes": cfg.algorithmic_bytes(),
-        "tensor_floor_ms": round(tensor_floor_ms, 5), "hbm_floor_ms": round(hbm_floor_ms, 5),
-    }
-    if hbm_floor_ms > tensor_floor_ms:
-        # moving the algorithmic bytes once takes longer than the arithmetic
-        gbs = cfg.algorithmic_bytes() / (kernel_ms * 1e-3) / 1e9
-        roofline.update({"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
-                         "frac": round(gbs / hbm, 4), "peak_source": f"{hbm_src} HBM copy bandwidth",
-                         "tensor_frac": round(achieved / bf16, 4)})
     else:
-        roofline.update({"bound": "tensor", "achieved": round(achieved, 2), "peak": bf16, "unit": "TFLOP/s",
-                         "frac": round(achieved / bf16, 4),
-                         "peak_source": f"{peak_src} bf16 dense (f16 operands run at the bf16 rate; sm_103a has "
-                                        "no integer tensor MMA)"})
+        del wl
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        x, w, b = synth.make_inputs(cfg)
         tops, threads, desc, _ = time_oracle_sample(cfg, args.cpu_seconds, x, w, b)
-        cpu = {"value": round(tops, 6), "unit": "TOPS", "cores": threads, "kind": "oracle", "sample": desc}
+        cpu = {"value": round(tops, 6), "unit": "TOPS", "cores": threads, "kind": "oracle", "sample": desc,
+               "single_thread": time_oracle_single_thread()}
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8 x int8 -> int32 (exact, f16 tensor MMA)",
         "data": "synthetic (splitmix64 seeded int8 uniform[-128,127])",
-        "config": {"workload": f"{cfg.name}: N={cfg.N} C={cfg.C} H={cfg.H} W={cfg.W} K={cfg.K} R={cfg.R} "
-                               f"S={cfg.S} stride={cfg.stride} pad={cfg.pre}/{cfg.post} dil={cfg.dilation} "
-                               f"mode={'conv' if cfg.mode else 'xcorr'} x={cfg.x_layout} w={cfg.w_layout} "
-                               f"y={cfg.y_layout} bias={cfg.bias} relu={cfg.relu}",
-                   "ops_per_step": cfg.ops, "algo": ic.ALGO_NAMES.get(algo),
-                   "l2": f"rotating {nsets} resident input/output sets ({nsets * set_bytes / 1e6:.0f} MB > 129 MB L2)",
+        "config": {"workload": workload_label(cfg), "ops_per_step": cfg.ops, "algo": algo_name,
+                   "l2": f"rotating {nsets} resident input/output sets (> 129 MB L2)",
                    "parallelism": f"replicas x{world}, no data-path collective"},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": ic.kernel_count(xd, wd, yd, p) * args.steps,
+        "gpu_launches": gpu_launches,
         "clocks": clocks,
+        "workloads": per_workload,
+        "int8_routes": routes,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -432,7 +657,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8 x int8 -> int64 -> int32",
         "data": "synthetic (splitmix64 seeded int8 uniform[-128,127])",
-        "config": {"workload": cfg.name, "ops_per_step_sampled": int(2 * npts * red)},
+        "config": {"workload": workload_label(cfg), "ops_per_step_sampled": int(2 * npts * red)},
         "cpu_baseline": {"value": round(value, 6), "unit": "TOPS", "kind": "oracle", "cores": threads,
                          "sample": desc},
         "e2e": {"value": round(value, 6), "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -441,7 +666,6 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------- extensions
-IMAD_PER_SM_CLK = 64  # 32-bit integer multiply-adds per SM per clock (CUDA cores)
 
 
 def run_extension(args):
@@ -629,10 +853,26 @@ def run_extension(args):
     print(json.dumps(line), flush=True)
 
 
+def run_peaks(args):
+    import torch
+
+    import int8_conv2d_fprop_gb300 as ic
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    r = measure_routes(ic, dev, torch.cuda.current_stream(dev).cuda_stream)
+    peaks, src = load_peaks()
+    line = {"metric": "measured dense rates of the int8-capable instruction routes", "routes": r,
+            "driver_peaks": {k: peaks.get(k) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")},
+            "driver_peaks_source": src}
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "peaks":
+        run_peaks(args)
     elif args.op != "fprop":
         run_extension(args)
     else:

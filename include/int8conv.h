@@ -259,17 +259,22 @@ conv_status conv_fprop_host(const conv_tensor_desc *x, const int8_t *x_host,
  * call cudaMalloc, which may synchronise the device.)
  *
  * Same arguments and results as conv_fprop, minus the workspace: the scratch
- * (the repacked filter and, when the image strides need it, a channels-last
- * image copy) lives in a device array of CONV_STATIC_WORKSPACE_BYTES that is
- * part of the library, so every GPU that loads the library holds that much
- * memory until the process exits.  Calls needing more scratch than that
+ * (the repacked filter; the int32 partial sums of the tiles whose reduction
+ * a call cuts into runs for different SMs, which on a 32 x 256 x 56 x 56
+ * 3x3 call are 18.9 MB of the 20.1 MB it needs; and, when the image strides
+ * need it, a channels-last image copy) lives in a device array of
+ * CONV_STATIC_WORKSPACE_BYTES that is part of the library, so every GPU that
+ * loads the library holds that much memory until the process exits.  Calls needing more scratch than that
  * return CONV_ERR_STATIC_WORKSPACE_LIMIT and launch nothing
  * (conv_fprop_workspace_size tells the need in advance).  It allocates
  * nothing: no cudaMalloc, cudaFree or allocating library routine.
  *
  * The first call on a device looks up that device's copy of the array (one
  * cudaGetSymbolAddress with the device current), so make that first call
- * before any stream capture.  Every call shares the one array and the
+ * before any stream capture.  The address is kept per device ordinal for
+ * the life of the device's primary context (the runtime's context): after
+ * cudaDeviceReset, or with another context made current on that ordinal, it
+ * is stale; use conv_fprop with a workspace there.  Every call shares the one array and the
  * kernels overwrite all scratch they read, so nothing needs clearing between
  * calls; but calls whose work overlaps on the GPU (different streams, or
  * different host threads) race on the array: order them on one stream.
@@ -328,7 +333,9 @@ conv_status conv_fprop_static_workspace(const conv_tensor_desc *x, const int8_t 
  * call that cannot take the tensor cores returns CONV_ERR_ALIGNMENT.
  * Pointers are device pointers on the current device, outputs must not
  * overlap inputs or the workspace; the calls are asynchronous on `stream`
- * and allocate nothing.
+ * and allocate nothing.  An empty dX (N, C, H or W zero) is a no-op; an
+ * empty batch in conv_wgrad writes an all-zero dW and reads neither input,
+ * so x_dev and dy_dev may then be null.
  */
 conv_status conv_dgrad_workspace_size(const conv_tensor_desc *dy, const conv_tensor_desc *w,
                                       const conv_tensor_desc *dx, const conv_fprop_params *p, size_t *bytes);
@@ -350,6 +357,43 @@ conv_status conv_device_status(void *stream);
  * nobody signals, with a limit of `limit_us` microseconds, so that it records
  * CONV_ERR_DEVICE_TIMEOUT and exits.  Returns the launch status. */
 conv_status conv_selftest_wait_timeout(uint32_t limit_us, void *stream);
+
+/*
+ * Peak microbenchmark: the measured rates of the instruction routes an exact
+ * int8 product can take on the current device, and its copy bandwidth.  The
+ * pages quote no peak; the benchmark divides by these (or by the driver's
+ * measured bf16 rate and copy bandwidth) instead of a datasheet figure.
+ * sm_103a has no integer kind of tcgen05.mma, so the routes are:
+ *   tcgen05_f16_tflops   tcgen05.mma.cta_group::1.kind::f16, M=128 N=256
+ *                        K=16, f32 accumulators in tensor memory, one CTA
+ *                        per SM issuing back to back (the route the
+ *                        convolution kernel takes, exact by grouping);
+ *   mma_sync_s8_tops     warp-level mma.sync m16n8k32 s8 x s8 -> s32;
+ *   mma_sync_f16_tflops  warp-level mma.sync m16n8k16 f16 x f16 -> f32;
+ *   dp4a_tops            the CUDA cores' dp4a (4 products + 4 adds);
+ *   hbm_copy_gbs         read + write bytes per second of a 16-byte copy
+ *                        kernel over the two halves of `scratch` (0 when
+ *                        scratch_bytes is below 512 MiB + 4 KiB);
+ *   sm_mhz               SM clock during the tcgen05 run (clock64 cycles per
+ *                        global-timer nanosecond).
+ * Rates count 2 operations per multiply-add, dense.  Each kernel runs about
+ * a millisecond (best of three launches timed with events on `stream`).
+ * `scratch`: caller-owned device buffer, 256-byte aligned, at least 1 MiB
+ * (timing records; the copy uses the rest).  Synchronises `stream`; not
+ * for use inside a stream capture.  Errors: CONV_ERR_NULL_PTR,
+ * CONV_ERR_WORKSPACE (scratch too small or misaligned), CONV_ERR_CUDA,
+ * CONV_ERR_DEVICE_TIMEOUT (an MMA completion wait ran out).
+ */
+typedef struct {
+    double tcgen05_f16_tflops;
+    double mma_sync_s8_tops;
+    double mma_sync_f16_tflops;
+    double dp4a_tops;
+    double hbm_copy_gbs;
+    double sm_mhz;
+} conv_peak_rates;
+
+conv_status conv_measure_peak_rates(void *scratch, size_t scratch_bytes, conv_peak_rates *out, void *stream);
 
 /* Human-readable name of a status. */
 const char *conv_status_string(conv_status s);

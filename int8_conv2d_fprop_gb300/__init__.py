@@ -51,7 +51,14 @@ EXPORTED_SYMBOLS = (
     "conv_fprop_host_buffer_size", "conv_fprop_host", "conv_device_status",
     "conv_selftest_wait_timeout", "conv_status_string", "conv_library_version",
     "conv_dgrad_workspace_size", "conv_dgrad", "conv_wgrad_workspace_size", "conv_wgrad",
+    "conv_measure_peak_rates",
 )
+
+
+class PeakRates(ctypes.Structure):
+    _fields_ = [("tcgen05_f16_tflops", ctypes.c_double), ("mma_sync_s8_tops", ctypes.c_double),
+                ("mma_sync_f16_tflops", ctypes.c_double), ("dp4a_tops", ctypes.c_double),
+                ("hbm_copy_gbs", ctypes.c_double), ("sm_mhz", ctypes.c_double)]
 
 
 class ConvError(RuntimeError):
@@ -170,6 +177,9 @@ def lib():
             getattr(L, name).argtypes = [D, ctypes.c_void_p, D, ctypes.c_void_p, D, ctypes.c_void_p, P,
                                          ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
             getattr(L, name).restype = ctypes.c_int
+        L.conv_measure_peak_rates.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(PeakRates),
+                                              ctypes.c_void_p]
+        L.conv_measure_peak_rates.restype = ctypes.c_int
         L.conv_device_status.argtypes = [ctypes.c_void_p]
         L.conv_selftest_wait_timeout.argtypes = [ctypes.c_uint32, ctypes.c_void_p]
         L.conv_status_string.argtypes = [ctypes.c_int]
@@ -295,6 +305,15 @@ def conv_fprop_from_host(x, w, bias=None, *, out, device_buffer=None, stream=Non
                              device_buffer.numel() * device_buffer.element_size(), stream.cuda_stream)
     _check(st, "conv_fprop_host")
     return out
+
+
+def measure_peak_rates(scratch_ptr: int, scratch_bytes: int, stream: int = 0) -> dict:
+    """Measured rates of the int8-capable instruction routes and the copy
+    bandwidth of the current device (see conv_measure_peak_rates)."""
+    r = PeakRates()
+    _check(lib().conv_measure_peak_rates(scratch_ptr or None, int(scratch_bytes), ctypes.byref(r), stream or None),
+           "peak rates")
+    return {name: float(getattr(r, name)) for name, _ in PeakRates._fields_}
 
 
 def device_status(stream: int = 0) -> int:

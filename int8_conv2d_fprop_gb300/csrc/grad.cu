@@ -463,7 +463,9 @@ conv_status conv_wgrad(const conv_tensor_desc *x, const int8_t *x_dev, const con
     bool tensor = false;
     conv_status st = plan_wgrad(x, x_dev, dy, dw, p, &g, &origin, &tensor, &pl);
     if (st) return st;
-    if (!x_dev || !dy_dev || !dw_dev) return CONV_ERR_NULL_PTR;
+    // an empty batch reads neither input: only the gradient must be given
+    const bool empty_batch = x->dims[0] == 0;
+    if (!dw_dev || (!empty_batch && (!x_dev || !dy_dev))) return CONV_ERR_NULL_PTR;
     const uint64_t dw_bytes = (uint64_t)desc_extent_elems(dw) * 4;
     if (overlaps(dw_dev, dw_bytes, x_dev, (uint64_t)desc_extent_elems(x)) ||
         overlaps(dw_dev, dw_bytes, dy_dev, (uint64_t)desc_extent_elems(dy)) ||

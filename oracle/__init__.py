@@ -90,6 +90,8 @@ def _bind(path: str):
     lib.oracle_out_extent.restype = ctypes.c_int64
     lib.oracle_out_extent.argtypes = [ctypes.c_int64] * 6
     lib.oracle_num_threads.restype = ctypes.c_int
+    lib.oracle_set_num_threads.restype = None
+    lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
     return lib
 
 
@@ -110,6 +112,12 @@ def use_library(path: Optional[str]) -> None:
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads the OpenMP loops use from now on (timing only; results do not
+    depend on it)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def _i64(vals: Sequence[int]):

@@ -324,10 +324,13 @@ int oracle_conv_wgrad(const int8_t *x, const int64_t *xd, const int64_t *xs,
     return bad ? ORACLE_ACC_OUT_OF_INT32 : ORACLE_OK;
 }
 
-/* Number of threads the OpenMP runtime would use (1 without OpenMP). */
+/* Number of threads the OpenMP runtime would use (1 without OpenMP), and a
+ * way to change it (used to time the oracle on one core). */
 #ifdef _OPENMP
 #include <omp.h>
 int oracle_num_threads(void) { return omp_get_max_threads(); }
+void oracle_set_num_threads(int n) { omp_set_num_threads(n > 0 ? n : 1); }
 #else
 int oracle_num_threads(void) { return 1; }
+void oracle_set_num_threads(int n) { (void)n; }
 #endif

@@ -138,3 +138,24 @@ def test_dgrad_extremes_exceed_f32_integer_range(ic):
     ref = oracle.conv_dgrad(dyf, dy.shape, dys, wf, w.shape, wss, (1, 64, 12, 12), (1, 1), (1, 1))
     assert int(ref.max()) == 256 * 9 * 16384
     assert np.array_equal(dx.cpu().numpy(), ref)
+
+
+def test_wgrad_empty_batch_takes_null_inputs(ic):
+    """An empty batch: dW is all zeros and neither input is read, so both
+    input pointers may be null (only dW must be given)."""
+    import ctypes
+    x = ic.TensorDesc.make(ic.CONV_INT8, (0, 32, 9, 9), (9 * 9 * 32, 1, 9 * 32, 32), 0)
+    dy = ic.TensorDesc.make(ic.CONV_INT8, (0, 48, 9, 9), (9 * 9 * 48, 1, 9 * 48, 48), 0)
+    dwd = ic.TensorDesc.packed(ic.CONV_INT32, (48, 32, 3, 3), "NHWC")
+    p = ic.Params.make(padding=(1, 1))
+    out = torch.full((48 * 32 * 9,), 77, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    st = ic.lib().conv_wgrad(ctypes.byref(x), None, ctypes.byref(dy), None, ctypes.byref(dwd), out.data_ptr(),
+                             ctypes.byref(p), None, 0, s)
+    assert st == 0, ic.STATUS.get(st)
+    torch.cuda.synchronize()
+    assert ic.device_status() == 0
+    assert int(out.abs().max()) == 0
+    st = ic.lib().conv_wgrad(ctypes.byref(x), None, ctypes.byref(dy), None, ctypes.byref(dwd), None,
+                             ctypes.byref(p), None, 0, s)
+    assert ic.STATUS[st] == "CONV_ERR_NULL_PTR"
