@@ -75,7 +75,10 @@ constexpr int B_ISSUER_WARP = 6;    // TMA path: issues the filter block copies
 // 16 int32 columns (64-byte rows, 64-byte swizzle).
 constexpr int EPI_COLS = 16;
 constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 4;  // 2 KB
-constexpr int EPI_SMEM_BYTES = 8 * 2 * EPI_BUF_BYTES;  // 32 KB
+// Resident-filter variant: when the whole repacked filter of a call (one
+// tile of output channels) fits in this many bytes, every CTA loads it once
+// and keeps it in shared memory, so a k-step brings only its image tile.
+constexpr int RESB_MAX_BYTES = 128 * 1024;
 
 // kTma: the int8 image tile arrives by TMA (im2col mode) in a ring of
 // STG_STAGES staging buffers and the producer warps convert it shared ->
@@ -99,14 +102,22 @@ constexpr int EPI_SMEM_BYTES = 8 * 2 * EPI_BUF_BYTES;  // 32 KB
 #define IGEMM_STG_128 8
 #endif
 
-template <int NT, bool kTma>
+// kResB: the filter blocks of all k-steps stay resident (loaded once per
+// CTA); the ring then holds image tiles only, two f16 stages behind six
+// int8 staging buffers, and each epilogue warp stages its stores in one
+// buffer instead of two.
+template <int NT, bool kTma, bool kResB = false>
 struct TileCfg {
     static constexpr int B_BYTES = NT * KS * 2;
-    static constexpr int ST = kTma ? (NT == 256 ? IGEMM_ST_256 : IGEMM_ST_128) : (NT == 256 ? 4 : 6);
-    static constexpr int STG_STAGES = kTma ? (NT == 256 ? IGEMM_STG_256 : IGEMM_STG_128) : 0;
+    static constexpr int ST = kResB ? 2 : (kTma ? (NT == 256 ? IGEMM_ST_256 : IGEMM_ST_128) : (NT == 256 ? 4 : 6));
+    static constexpr int STG_STAGES = kResB ? 6 : (kTma ? (NT == 256 ? IGEMM_STG_256 : IGEMM_STG_128) : 0);
+    static constexpr int EPI_BUFS = kResB ? 1 : 2;  // output staging buffers per epilogue warp
+    static constexpr int EPI_BYTES = 8 * EPI_BUFS * EPI_BUF_BYTES;
+    static constexpr int B_AREA = kResB ? RESB_MAX_BYTES : ST * B_BYTES;
     static constexpr int TMEM_COLS = NSLOT * NT;
-    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + ST * (A_BYTES + B_BYTES) + STG_STAGES * STG_BYTES +
-                                      EPI_SMEM_BYTES + 512 /*barriers*/;
+    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + ST * A_BYTES + B_AREA + STG_STAGES * STG_BYTES +
+                                      EPI_BYTES + 512 /*barriers*/;
+    static_assert(!kResB || kTma, "the resident filter needs the TMA producers");
     static_assert(TMEM_COLS <= 512, "tensor memory has 512 columns");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     static_assert(ST <= 8 && STG_STAGES <= 8, "the control block has 8 barriers per ring");
@@ -188,6 +199,7 @@ struct SharedCtl {
     uint64_t acc_full[NSLOT];
     uint64_t acc_empty[NSLOT];
     uint64_t mma_done;
+    uint64_t b_res;                      // resident filter landed (kResB)
     uint32_t tmem_base;
     int32_t abort_flag;
 };
@@ -322,9 +334,9 @@ __device__ __forceinline__ void drain_ring(uint64_t *bars, int depth, int64_t is
     }
 }
 
-template <int NT, bool kTma>
+template <int NT, bool kTma, bool kResB>
 __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_constant__ IgemmArgs a) {
-    using Cfg = TileCfg<NT, kTma>;
+    using Cfg = TileCfg<NT, kTma, kResB>;
     constexpr int ST = Cfg::ST;
     constexpr int STG = Cfg::STG_STAGES;
     constexpr int B_BYTES = Cfg::B_BYTES;
@@ -335,10 +347,10 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
     uint8_t *const base_ptr = smem_raw + (base - raw_addr);
     const uint32_t a_smem = base;
     const uint32_t b_smem = a_smem + ST * A_BYTES;
-    const uint32_t stg_smem = b_smem + ST * B_BYTES;
+    const uint32_t stg_smem = b_smem + Cfg::B_AREA;
     const uint32_t epi_smem = stg_smem + STG * STG_BYTES;
     SharedCtl *ctl =
-        reinterpret_cast<SharedCtl *>(base_ptr + ST * (A_BYTES + B_BYTES) + STG * STG_BYTES + EPI_SMEM_BYTES);
+        reinterpret_cast<SharedCtl *>(base_ptr + ST * A_BYTES + Cfg::B_AREA + STG * STG_BYTES + Cfg::EPI_BYTES);
     volatile int32_t *abort_flag = &ctl->abort_flag;
 
     const int warp = threadIdx.x >> 5;
@@ -357,10 +369,12 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
     if (threadIdx.x == 0) {
         for (int i = 0; i < ST; ++i) {
             // 128 producer arrivals (A tile written) + 1 arrival with the
-            // filter copy's byte count
-            ptx::mbar_init(ptx::smem_addr(&ctl->full[i]), 129);
+            // filter copy's byte count (no filter copy per k-step when the
+            // filter is resident)
+            ptx::mbar_init(ptx::smem_addr(&ctl->full[i]), kResB ? 128 : 129);
             ptx::mbar_init(ptx::smem_addr(&ctl->empty[i]), 1);
         }
+        ptx::mbar_init(ptx::smem_addr(&ctl->b_res), 1);
         for (int i = 0; i < STG; ++i) {
             ptx::mbar_init(ptx::smem_addr(&ctl->stg_full[i]), 1);
             ptx::mbar_init(ptx::smem_addr(&ctl->stg_empty[i]), 128);
@@ -503,10 +517,12 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
             Ring<ST> rg;
             uint32_t gi = 0;
             bool ok = true;
+            if (kResB) ok = wait_phase(ptx::smem_addr(&ctl->b_res), 0, abort_flag, limit, a.status);
             for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
                 const Unit w = unit_at(u, a.full_units, a.splits, a.k_steps);
                 const int kn = w.ke - w.kb;
                 const int ng = groups_of(kn);
+                const int urot = w.split < 0 ? rot : 0;
                 for (int g = 0; g < ng && ok; ++g) {
                     const int js = (int)(((int64_t)g * kn) / ng);
                     const int je = (int)(((int64_t)(g + 1) * kn) / ng);
@@ -528,7 +544,12 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                             break;
                         }
                         const uint64_t adesc = adesc0 + (uint64_t)(rg.idx * (A_BYTES >> 4));
-                        const uint64_t bdesc = bdesc0 + (uint64_t)(rg.idx * (B_BYTES >> 4));
+                        // resident filter: the block of this k-step (the
+                        // producers walk the unit's k-steps from its rotation)
+                        int jr = j + urot;
+                        if (jr >= kn) jr -= kn;
+                        const uint64_t bdesc = kResB ? bdesc0 + (uint64_t)((w.kb + jr) * (B_BYTES >> 4))
+                                                     : bdesc0 + (uint64_t)(rg.idx * (B_BYTES >> 4));
 #pragma unroll
                         for (int kk = 0; kk < KS / 16; ++kk) {
                             // advance 16 f16 = 32 bytes along K inside the swizzled row
@@ -588,6 +609,15 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 }
             }
             if (*abort_flag) drain_ring(ctl->stg_full, STG, issued, limit, a.status);
+        } else if (kResB && warp == B_ISSUER_WARP && lane == 0) {
+            // every filter block of the call (one tile of output channels),
+            // once, onto one barrier; then wait for them so that no copy is
+            // in flight when the CTA ends
+            const uint32_t bar = ptx::smem_addr(&ctl->b_res);
+            ptx::mbar_arrive_expect_tx(bar, (uint32_t)(a.k_steps * B_BYTES));
+            for (int j = 0; j < a.k_steps; ++j)
+                ptx::bulk_copy_g2s(b_smem + j * B_BYTES, a.wp + (size_t)j * B_BYTES, B_BYTES, bar);
+            (void)drain_phase(bar, 0, limit, a.status);
         } else if (kTma && warp == B_ISSUER_WARP && lane == 0) {
             // pre-swizzled f16 filter blocks, one bulk copy per k-step, in the
             // same rotated k-step order as the image tiles
@@ -726,11 +756,11 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 const int pq = a.P * a.Q;
                 const int img = m0w / pq;
                 const int pix = m0w - img * pq;
-                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (2u * EPI_BUF_BYTES);
+                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (uint32_t)(Cfg::EPI_BUFS * EPI_BUF_BYTES);
 #pragma unroll
                 for (int ch = 0; ch < HALF / EPI_COLS; ++ch) {
-                    const uint32_t buf = ebase + (uint32_t)(ch & 1) * EPI_BUF_BYTES;
-                    if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store that last read buf is done
+                    const uint32_t buf = ebase + (uint32_t)(ch % Cfg::EPI_BUFS) * EPI_BUF_BYTES;
+                    if (lane == 0) ptx::bulk_wait_group_read<Cfg::EPI_BUFS - 1>();  // the store that last read buf is done
                     __syncwarp();
 #pragma unroll
                     for (int c = 0; c < EPI_COLS; ++c)
@@ -747,12 +777,12 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 // staged row
                 const int k0 = nt * NT + col0;
                 const int m0w = mt * MT + quad * 32;
-                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (2u * EPI_BUF_BYTES);
+                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (uint32_t)(Cfg::EPI_BUFS * EPI_BUF_BYTES);
                 const uint32_t sw = ((uint32_t)lane >> 1) & 3u;
 #pragma unroll
                 for (int ch = 0; ch < HALF / 64; ++ch) {
-                    const uint32_t buf = ebase + (uint32_t)(ch & 1) * EPI_BUF_BYTES;
-                    if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store that last read buf is done
+                    const uint32_t buf = ebase + (uint32_t)(ch % Cfg::EPI_BUFS) * EPI_BUF_BYTES;
+                    if (lane == 0) ptx::bulk_wait_group_read<Cfg::EPI_BUFS - 1>();  // the store that last read buf is done
                     __syncwarp();
                     const uint32_t rowaddr = buf + (uint32_t)lane * 64u;
 #pragma unroll
@@ -785,12 +815,12 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 // pixel and columns past K.  Two buffers per warp alternate.
                 const int k0 = nt * NT + col0;
                 const int m0w = mt * MT + quad * 32;
-                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (2u * EPI_BUF_BYTES);
+                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (uint32_t)(Cfg::EPI_BUFS * EPI_BUF_BYTES);
                 const uint32_t sw = ((uint32_t)lane >> 1) & 3u;
 #pragma unroll
                 for (int ch = 0; ch < HALF / EPI_COLS; ++ch) {
-                    const uint32_t buf = ebase + (uint32_t)(ch & 1) * EPI_BUF_BYTES;
-                    if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store that last read buf is done
+                    const uint32_t buf = ebase + (uint32_t)(ch % Cfg::EPI_BUFS) * EPI_BUF_BYTES;
+                    if (lane == 0) ptx::bulk_wait_group_read<Cfg::EPI_BUFS - 1>();  // the store that last read buf is done
                     __syncwarp();
                     const int i0 = ch * EPI_COLS;
                     const uint32_t rowaddr = buf + (uint32_t)lane * 64u;
@@ -1119,14 +1149,14 @@ constexpr int64_t kMinSplitSteps = 16;   // k-steps of the shortest run of a cut
 constexpr int64_t kMaxSplits = 32;
 constexpr int64_t kMinTailSteps = 4;     // k-steps of the shortest run of a last-round tile
 
-template <int NT, bool kTma>
+template <int NT, bool kTma, bool kResB = false>
 conv_status launch_conv(const IgemmArgs &a, int grid, cudaStream_t st) {
-    using Cfg = TileCfg<NT, kTma>;
+    using Cfg = TileCfg<NT, kTma, kResB>;
     static std::atomic<bool> attr_set[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !attr_set[dev].load()) {
-        if (cudaFuncSetAttribute(igemm_conv_kernel<NT, kTma>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(igemm_conv_kernel<NT, kTma, kResB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg::SMEM_BYTES) != cudaSuccess)
             return CONV_ERR_CUDA;
         if (dev >= 0 && dev < 64) attr_set[dev].store(true);
@@ -1146,7 +1176,7 @@ conv_status launch_conv(const IgemmArgs &a, int grid, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, igemm_conv_kernel<NT, kTma>, a) != cudaSuccess) return CONV_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, igemm_conv_kernel<NT, kTma, kResB>, a) != cudaSuccess) return CONV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
@@ -1304,6 +1334,9 @@ void igemm_plan(const ConvGeom &g, const void *x_dev, IgemmPlan *pl) {
     pl->n_tiles = (g.K + pl->n_tile - 1) / pl->n_tile;
     pl->m_tiles = (g.N * g.P * g.Q + MT - 1) / MT;
     pl->wpack_bytes = (size_t)align256(pl->n_tiles * pl->k_steps * pl->n_tile * (int64_t)(KS * 2));
+    // one tile of output channels whose filter blocks fit in shared memory:
+    // the filter stays resident in every CTA (taken with the TMA producers)
+    pl->resident_b = pl->n_tiles == 1 && pl->k_steps * pl->n_tile * (int64_t)(KS * 2) <= RESB_MAX_BYTES;
     pl->xpack_bytes = pl->pack_x ? (size_t)align256(g.N * g.H * g.W * pl->c16) : 0;
     // One CTA per SM walks the tiles.  With fewer tiles than SMs and long
     // reductions (the weight gradient's shape: few output tiles, a reduction
@@ -1439,7 +1472,9 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
     const bool tma = !pl.register_loads && encode_im2col_map(g, a.x, a.xs_n, a.xs_h, a.xs_w,
                                                              pl.pack_x ? pl.c16 : g.C, &a.tmap_x);
     conv_status rc;
-    if (tma)
+    if (tma && pl.resident_b)
+        rc = pl.n_tile == 256 ? launch_conv<256, true, true>(a, grid, st) : launch_conv<128, true, true>(a, grid, st);
+    else if (tma)
         rc = pl.n_tile == 256 ? launch_conv<256, true>(a, grid, st) : launch_conv<128, true>(a, grid, st);
     else
         rc = pl.n_tile == 256 ? launch_conv<256, false>(a, grid, st) : launch_conv<128, false>(a, grid, st);
