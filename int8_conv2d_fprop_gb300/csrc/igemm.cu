@@ -164,7 +164,7 @@ __device__ __forceinline__ Unit unit_at(int u, int full_units, int splits, int k
 __device__ __forceinline__ int groups_of(int kn) { return (kn + MAX_GROUP_STEPS - 1) / MAX_GROUP_STEPS; }
 
 struct IgemmArgs {
-    CUtensorMap tmap_x;  // im2col map of the channels-last image (TMA path only)
+    CUtensorMap tmap_x;  // im2col map of the channels-last image, or its 2-D pixel-row map (TMA path only)
     CUtensorMap tmap_y;  // output map: 2-D [pixels][K] (y_tma 1) or 3-D [N][K][P*Q] (y_tma 2)
     const int8_t *x;     // channels-last image
     const uint8_t *wp;   // repacked f16 filter blocks
@@ -187,6 +187,8 @@ struct IgemmArgs {
     int32_t full_units, splits, num_units;
     int32_t *tail_part;  // [cut tile][split][MT rows][NT columns]
     int32_t relu, y_vec;
+    int32_t a_rows;      // TMA path: 1x1, stride 1, no padding: the image tile is a plain 2-D box of
+                         // pixel rows (output pixel m reads image pixel m)
     int32_t y_tma;       // TMA stores: 1 pixel-major with contiguous channels, 2 channel-major
                          // (each channel's P*Q pixels contiguous, P*Q a multiple of 32)
     uint64_t wait_limit_ns;
@@ -587,14 +589,16 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 const int q0 = rem - p0 * a.Q;
                 const int w0 = q0 * a.str_w - a.pad_w;
                 const int h0 = p0 * a.str_h - a.pad_h;
+                // k-step kb + ((j + urot) mod kn), held as (tap row r, tap
+                // column s, channel block cb) and advanced without divisions
+                // (the issuing thread's loop is on every k-step's path)
+                int jr = wu.kb + urot;
+                int tap = jr / a.c_steps;
+                int cb = jr - tap * a.c_steps;
+                int r = tap / a.S;
+                int s = tap - r * a.S;
+#pragma unroll 1
                 for (int j = 0; j < kn; ++j) {
-                    int jr = j + urot;
-                    if (jr >= kn) jr -= kn;
-                    jr += wu.kb;
-                    const int tap = jr / a.c_steps;
-                    const int cb = jr - tap * a.c_steps;
-                    const int r = tap / a.S;
-                    const int s = tap - r * a.S;
                     if (!wait_phase(ptx::smem_addr(&ctl->stg_empty[rs.idx]), rs.phase ^ 1u, abort_flag, limit,
                                     a.status)) {
                         ok = false;
@@ -602,10 +606,26 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                     }
                     const uint32_t bar = ptx::smem_addr(&ctl->stg_full[rs.idx]);
                     ptx::mbar_arrive_expect_tx(bar, STG_BYTES);
-                    ptx::tma_load_im2col_4d(stg_smem + rs.idx * STG_BYTES, &a.tmap_x, cb * KS, w0, h0, n0,
-                                            (uint16_t)(s * a.dil_w), (uint16_t)(r * a.dil_h), bar);
+                    if (a.a_rows)
+                        ptx::tma_load_2d(stg_smem + rs.idx * STG_BYTES, &a.tmap_x, cb * KS, m0, bar);
+                    else
+                        ptx::tma_load_im2col_4d(stg_smem + rs.idx * STG_BYTES, &a.tmap_x, cb * KS, w0, h0, n0,
+                                                (uint16_t)(s * a.dil_w), (uint16_t)(r * a.dil_h), bar);
                     ++issued;
                     rs.next();
+                    if (++jr == wu.ke) {  // the rotated sequence wraps to the unit's first k-step
+                        jr = wu.kb;
+                        tap = jr / a.c_steps;
+                        cb = jr - tap * a.c_steps;
+                        r = tap / a.S;
+                        s = tap - r * a.S;
+                    } else if (++cb == a.c_steps) {
+                        cb = 0;
+                        if (++s == a.S) {
+                            s = 0;
+                            ++r;
+                        }
+                    }
                 }
             }
             if (*abort_flag) drain_ring(ctl->stg_full, STG, issued, limit, a.status);
@@ -1227,6 +1247,28 @@ bool encode_im2col_map(const ConvGeom &g, const void *x, int64_t xs_n, int64_t x
     return r == CUDA_SUCCESS;
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tiled_encoder();
+
+// 2-D map [pixels][channels] of a channels-last image whose pixels follow
+// one another at xs_w bytes (dense rows): for a 1x1 filter with stride 1 and
+// no padding, the image tile of output pixels m0.. is the box of rows m0..
+// (128 rows x 64 channels, unswizzled: the same staging layout as the
+// im2col load).
+bool encode_rows_map(const ConvGeom &g, const void *x, int64_t xs_w, int64_t c_dim, CUtensorMap *map) {
+    const int64_t rows = g.N * g.H * g.W;
+    if (((uintptr_t)x % 16) != 0 || xs_w % 16 || rows >= ((int64_t)1 << 32)) return false;
+    auto enc = tiled_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)c_dim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)xs_w};
+    const cuuint32_t box[2] = {(cuuint32_t)KS, (cuuint32_t)MT};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(x), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tiled_encoder() {
     static std::atomic<void *> fn{nullptr};
     static std::atomic<bool> tried{false};
@@ -1469,8 +1511,21 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
     if (!a.status) return CONV_ERR_CUDA;
     if (a.num_tiles == 0) return CONV_OK;
     const int grid = (int)pl.grid;
-    const bool tma = !pl.register_loads && encode_im2col_map(g, a.x, a.xs_n, a.xs_h, a.xs_w,
-                                                             pl.pack_x ? pl.c16 : g.C, &a.tmap_x);
+    // a 1x1 filter at stride 1 without padding over dense pixel rows reads
+    // image pixel m for output pixel m: plain 2-D boxes instead of im2col
+    const int64_t c_dim = pl.pack_x ? pl.c16 : g.C;
+    a.a_rows = (g.R == 1 && g.S == 1 && g.str_h == 1 && g.str_w == 1 && g.pad_h == 0 && g.pad_w == 0 &&
+                g.P == g.H && g.Q == g.W && a.xs_h == g.W * a.xs_w && a.xs_n == g.H * a.xs_h)
+                   ? 1
+                   : 0;
+    bool tma = false;
+    if (!pl.register_loads) {
+        if (a.a_rows) tma = encode_rows_map(g, a.x, a.xs_w, c_dim, &a.tmap_x);
+        if (!tma) {
+            a.a_rows = 0;
+            tma = encode_im2col_map(g, a.x, a.xs_n, a.xs_h, a.xs_w, c_dim, &a.tmap_x);
+        }
+    }
     conv_status rc;
     if (tma && pl.resident_b)
         rc = pl.n_tile == 256 ? launch_conv<256, true, true>(a, grid, st) : launch_conv<128, true, true>(a, grid, st);

@@ -77,6 +77,16 @@ __device__ __forceinline__ void tma_load_im2col_4d(uint32_t dst, const void *tma
         : "memory");
 }
 
+// Tensor copy global -> shared of a 2-D box (tile mode) at coordinates
+// (x, y); elements outside the tensor read as zero.  Completion counted in
+// bytes on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int32_t x, int32_t y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
 // Tensor copy shared -> global of a 2-D box at coordinates (x, y), tracked
 // in this thread's bulk async-group; elements outside the tensor are not
 // written.
