@@ -70,11 +70,12 @@ static_assert(2 * 128 * PRODUCER_REGS + 2 * 128 * EPILOGUE_REGS <= 65536, "regis
 constexpr int PREFETCH = 1;  // register path: items in flight ahead of the one being stored
 constexpr int STG_BYTES = MT * KS;  // one int8 im2col tile: 128 pixels x 64 channels
 constexpr int A_ISSUER_WARP = 5;    // TMA path: issues the im2col loads
+constexpr int A_ISSUER_WARP2 = 7;   // TMA path, image stages in tensor memory: second image-load issuer
 constexpr int B_ISSUER_WARP = 6;    // TMA path: issues the filter block copies
-// Output staging for TMA stores: per epilogue warp two buffers of 32 rows x
-// 16 int32 columns (64-byte rows, 64-byte swizzle).
-constexpr int EPI_COLS = 16;
-constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 4;  // 2 KB
+// Output staging for TMA stores: per epilogue warp one or two buffers of 32
+// rows x EPI_COLS int32 columns: 16 (64-byte rows, 64-byte swizzle) or, in
+// the tensor-memory variant, 32 (128-byte rows, 128-byte swizzle: half as
+// many store copies, which share each SM's TMA unit with the image loads).
 // Resident-filter variant: when the whole repacked filter of a call (one
 // tile of output channels) fits in this many bytes, every CTA loads it once
 // and keeps it in shared memory, so a k-step brings only its image tile.
@@ -103,24 +104,43 @@ constexpr int RESB_MAX_BYTES = 128 * 1024;
 #endif
 
 // kResB: the filter blocks of all k-steps stay resident (loaded once per
-// CTA); the ring then holds image tiles only, two f16 stages behind six
-// int8 staging buffers, and each epilogue warp stages its stores in one
-// buffer instead of two.
-template <int NT, bool kTma, bool kResB = false>
+// CTA); the ring then holds image tiles only, and each epilogue warp stages
+// its stores in one buffer instead of two.
+// kTmemA (128-column tiles, TMA path): the f16 image tile of a k-step goes
+// to tensor memory (columns 256.. next to the two 128-column accumulator
+// slots, 32 columns per stage) and the MMA reads it from there; the shared
+// memory that held it becomes int8 staging buffers, i.e. image bytes in
+// flight (10 with a resident filter, 16 without).
+template <int NT, bool kTma, bool kResB = false, bool kTmemA = false>
 struct TileCfg {
     static constexpr int B_BYTES = NT * KS * 2;
-    static constexpr int ST = kResB ? 2 : (kTma ? (NT == 256 ? IGEMM_ST_256 : IGEMM_ST_128) : (NT == 256 ? 4 : 6));
-    static constexpr int STG_STAGES = kResB ? 6 : (kTma ? (NT == 256 ? IGEMM_STG_256 : IGEMM_STG_128) : 0);
+    static constexpr int ST = kTmemA ? 4 : (kResB ? 2 : (kTma ? (NT == 256 ? IGEMM_ST_256 : IGEMM_ST_128)
+                                                                : (NT == 256 ? 4 : 6)));
+    static constexpr int STG_STAGES = kTmemA ? (kResB ? 10 : 12)
+                                             : (kResB ? 6 : (kTma ? (NT == 256 ? IGEMM_STG_256 : IGEMM_STG_128) : 0));
     static constexpr int EPI_BUFS = kResB ? 1 : 2;  // output staging buffers per epilogue warp
+    static constexpr int EPI_COLS = kTmemA ? 32 : 16;
+    static constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 4;  // 2 or 4 KB
     static constexpr int EPI_BYTES = 8 * EPI_BUFS * EPI_BUF_BYTES;
+    static constexpr int A_SMEM = kTmemA ? 0 : ST * A_BYTES;
     static constexpr int B_AREA = kResB ? RESB_MAX_BYTES : ST * B_BYTES;
-    static constexpr int TMEM_COLS = NSLOT * NT;
-    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + ST * A_BYTES + B_AREA + STG_STAGES * STG_BYTES +
+    static constexpr int TMEM_COLS = kTmemA ? 512 : NSLOT * NT;
+    static constexpr int TMEM_A_COL = NSLOT * NT;  // kTmemA: first column of the image stages
+    // Warps that issue the image loads (kTmemA: warps 5 and 7, one thread
+    // each): issuer i issues the loads into the staging slots s % A_ISSUERS
+    // == i.  Issuing a TMA load takes its thread a few hundred ns, so one
+    // issuer keeps only about four loads in flight; the 128-column tiles
+    // stream their image from HBM and need more.  (Lanes of one warp would
+    // not help: their divergent branches run one after the other.)
+    static constexpr int A_ISSUERS = kTmemA ? 2 : 1;
+    static_assert(STG_STAGES % A_ISSUERS == 0, "staging slots split evenly between the issuers");
+    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + A_SMEM + B_AREA + STG_STAGES * STG_BYTES +
                                       EPI_BYTES + 512 /*barriers*/;
     static_assert(!kResB || kTma, "the resident filter needs the TMA producers");
+    static_assert(!kTmemA || (kTma && NT == 128 && TMEM_A_COL + ST * 32 <= 512), "image stages in tensor memory");
     static_assert(TMEM_COLS <= 512, "tensor memory has 512 columns");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
-    static_assert(ST <= 8 && STG_STAGES <= 8, "the control block has 8 barriers per ring");
+    static_assert(ST <= 8 && STG_STAGES <= 16, "the control block has 8 ring and 16 staging barriers");
 };
 
 // Slot index and phase parity of a ring of N mbarrier-guarded buffers.
@@ -197,7 +217,7 @@ struct IgemmArgs {
 
 struct SharedCtl {
     uint64_t full[8], empty[8];          // A + filter ring
-    uint64_t stg_full[8], stg_empty[8];  // TMA path: im2col tile landed / converted
+    uint64_t stg_full[16], stg_empty[16];  // TMA path: im2col tile landed / converted
     uint64_t acc_full[NSLOT];
     uint64_t acc_empty[NSLOT];
     uint64_t mma_done;
@@ -209,15 +229,28 @@ static_assert(sizeof(SharedCtl) <= 512, "control block too large");
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting or
 // the time limit passed (then the CTA is marked aborting and the device status
-// word records the timeout).
+// word records the timeout).  backoff_ns > 0: sleep that long between polls,
+// for waits off the k-step critical path (an epilogue warp waiting for its
+// next tile, an issuer waiting for a free slot), so that polling does not take
+// issue slots from the converters and the MMA thread on the same scheduler.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int32_t *abort_flag,
-                                           uint64_t limit_ns, int *status) {
+                                           uint64_t limit_ns, int *status, uint32_t backoff_ns = 0) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::global_timer_ns();
     while (true) {
+        if (backoff_ns) {
 #pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (ptx::mbar_try_wait(bar, parity)) return true;
+            for (int i = 0; i < 8; ++i) {
+                __nanosleep(backoff_ns);
+                if (ptx::mbar_try_wait(bar, parity)) return true;
+            }
+        } else {
+            // on the k-step critical path: poll without suspending (a
+            // suspended try_wait resumes some time after the phase completes)
+#pragma unroll 1
+            for (int i = 0; i < 64; ++i)
+                if (ptx::mbar_test_wait(bar, parity)) return true;
+        }
         if (*abort_flag) return false;
         if (ptx::global_timer_ns() - t0 > limit_ns) {
             *abort_flag = 1;
@@ -226,6 +259,9 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
         }
     }
 }
+
+constexpr uint32_t kIssuerBackoffNs = 32;    // image / filter issuers waiting for a free slot
+constexpr uint32_t kEpilogueBackoffNs = 128; // epilogue warps waiting for a finished accumulator
 
 // Bounded wait that ignores the abort flag: used while shutting down to let
 // work already issued (bulk copies, MMAs) finish before shared or tensor
@@ -324,7 +360,9 @@ __device__ __forceinline__ void cursor_advance(LoadCursor &c, const IgemmArgs &a
 
 // Lets every copy issued into a ring of `depth` slots land: the newest copy
 // into slot s completes phase (copies into s) - 1, and phases complete in
-// order.  Used only after an abort.  A filter copy shares its "full" barrier
+// order.  Used only after an abort.  drain_ring_owned: the same for the
+// slots s % lanes == lane of a ring walked up to position `stop`, whose
+// copies that lane issued.  A filter copy shares its "full" barrier
 // with the 128 producer arrivals, which an aborting CTA may never make; the
 // wait is then cut off after DRAIN_LIMIT_NS.  Copies issued before the abort
 // (itself a wait that ran out after the full time limit) have long landed.
@@ -336,9 +374,17 @@ __device__ __forceinline__ void drain_ring(uint64_t *bars, int depth, int64_t is
     }
 }
 
-template <int NT, bool kTma, bool kResB>
+__device__ __forceinline__ void drain_ring_owned(uint64_t *bars, int depth, int64_t stop, int lane, int lanes,
+                                                 uint64_t limit, int *status) {
+    for (int s = lane; s < depth; s += lanes) {
+        const int64_t n_s = stop / depth + (s < stop % depth ? 1 : 0);
+        if (n_s > 0) (void)drain_phase(ptx::smem_addr(&bars[s]), (uint32_t)((n_s - 1) & 1), limit, status);
+    }
+}
+
+template <int NT, bool kTma, bool kResB, bool kTmemA>
 __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_constant__ IgemmArgs a) {
-    using Cfg = TileCfg<NT, kTma, kResB>;
+    using Cfg = TileCfg<NT, kTma, kResB, kTmemA>;
     constexpr int ST = Cfg::ST;
     constexpr int STG = Cfg::STG_STAGES;
     constexpr int B_BYTES = Cfg::B_BYTES;
@@ -348,11 +394,11 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t *const base_ptr = smem_raw + (base - raw_addr);
     const uint32_t a_smem = base;
-    const uint32_t b_smem = a_smem + ST * A_BYTES;
+    const uint32_t b_smem = a_smem + Cfg::A_SMEM;
     const uint32_t stg_smem = b_smem + Cfg::B_AREA;
     const uint32_t epi_smem = stg_smem + STG * STG_BYTES;
     SharedCtl *ctl =
-        reinterpret_cast<SharedCtl *>(base_ptr + ST * A_BYTES + Cfg::B_AREA + STG * STG_BYTES + Cfg::EPI_BYTES);
+        reinterpret_cast<SharedCtl *>(base_ptr + Cfg::A_SMEM + Cfg::B_AREA + STG * STG_BYTES + Cfg::EPI_BYTES);
     volatile int32_t *abort_flag = &ctl->abort_flag;
 
     const int warp = threadIdx.x >> 5;
@@ -404,7 +450,45 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
     // writes are visible
     ptx::grid_dependency_wait();
 
-    if (warp < 4 && kTma) {
+    if (warp < 4 && kTmemA) {
+        // ------------------------------------------------- converters (to tensor memory)
+        // Thread t converts pixel row t of the staged tile (its 64 channel
+        // bytes, 16-byte chunk c stored at chunk position c ^ ((t >> 1) & 3)
+        // by the TMA 64-byte swizzle: each 8 rows cover all banks) and writes
+        // the 32 f16 pairs to tensor-memory lane t (warp w owns lanes
+        // 32w..32w+31), column j holding channels 2j and 2j+1.
+        ptx::setmaxnreg_dec<PRODUCER_REGS>();
+        const int row = threadIdx.x;
+        const uint32_t sw = (uint32_t)((row >> 1) & 3);
+        const uint32_t lane_col0 = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)Cfg::TMEM_A_COL;
+        Ring<ST> ra;
+        Ring<STG> rs;
+        for (int it = 0; it < total; ++it) {
+            bool got = wait_phase(ptx::smem_addr(&ctl->stg_full[rs.idx]), rs.phase, abort_flag, limit, a.status);
+            got = got && wait_phase(ptx::smem_addr(&ctl->empty[ra.idx]), ra.phase ^ 1u, abort_flag, limit, a.status);
+            // tcgen05.st is warp-collective: the whole warp proceeds or stops together
+            if (!__all_sync(0xffffffffu, got)) break;
+            const uint32_t src = stg_smem + rs.idx * STG_BYTES + (uint32_t)row * 64u;
+            uint4 vin[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) vin[c] = ptx::ld_shared_v4(src + ((((uint32_t)c) ^ sw) << 4));
+            uint32_t w[32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint4 lo, hi;
+                cvt16(vin[c], lo, hi);
+                w[8 * c + 0] = lo.x; w[8 * c + 1] = lo.y; w[8 * c + 2] = lo.z; w[8 * c + 3] = lo.w;
+                w[8 * c + 4] = hi.x; w[8 * c + 5] = hi.y; w[8 * c + 6] = hi.z; w[8 * c + 7] = hi.w;
+            }
+            ptx::tmem_st_32x32b_x32(lane_col0 + (uint32_t)(ra.idx * 32), w);
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(ptx::smem_addr(&ctl->stg_empty[rs.idx]));
+            ptx::mbar_arrive(ptx::smem_addr(&ctl->full[ra.idx]));
+            ra.next();
+            rs.next();
+        }
+    } else if (warp < 4 && kTma) {
         // ------------------------------------------------------------ converters
         // The im2col tile in staging holds pixel row i at i*64 bytes.  Four
         // neighbouring lanes take the four 16-byte chunks of one row, so a
@@ -546,6 +630,10 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                             break;
                         }
                         const uint64_t adesc = adesc0 + (uint64_t)(rg.idx * (A_BYTES >> 4));
+                        // kTmemA: the converters' tensor-memory stores are
+                        // ordered before the MMAs by their fence, the barrier
+                        // and this fence
+                        if (kTmemA) ptx::tc_fence_after();
                         // resident filter: the block of this k-step (the
                         // producers walk the unit's k-steps from its rotation)
                         int jr = j + urot;
@@ -555,8 +643,13 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
 #pragma unroll
                         for (int kk = 0; kk < KS / 16; ++kk) {
                             // advance 16 f16 = 32 bytes along K inside the swizzled row
-                            ptx::mma_f16_ss(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
-                                            (j > js || kk > 0) ? 1u : 0u);
+                            // (8 columns in tensor memory)
+                            if (kTmemA)
+                                ptx::mma_f16_ts(d_tmem, tmem_base + (uint32_t)(Cfg::TMEM_A_COL + rg.idx * 32 + 8 * kk),
+                                                bdesc + (uint64_t)(2 * kk), idesc, (j > js || kk > 0) ? 1u : 0u);
+                            else
+                                ptx::mma_f16_ss(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
+                                                (j > js || kk > 0) ? 1u : 0u);
                         }
                         ptx::mma_commit(ptx::smem_addr(&ctl->empty[rg.idx]));
                         rg.next();
@@ -569,7 +662,8 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
             // all MMAs issued by this thread complete before tensor memory is freed
             ptx::mma_commit(ptx::smem_addr(&ctl->mma_done));
             (void)drain_phase(ptx::smem_addr(&ctl->mma_done), 0, limit, a.status);
-        } else if (kTma && warp == A_ISSUER_WARP && lane == 0) {
+        } else if (kTma && (warp == A_ISSUER_WARP || (Cfg::A_ISSUERS == 2 && warp == A_ISSUER_WARP2)) && lane == 0) {
+            const int issuer = warp == A_ISSUER_WARP ? 0 : 1;
             // im2col tiles: 128 consecutive output pixels x 64 channels of one
             // tap; the map's bounding box turns pixel order into window
             // origins (stride and pre-padding), the tap enters as the pixel
@@ -599,18 +693,23 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 int s = tap - r * a.S;
 #pragma unroll 1
                 for (int j = 0; j < kn; ++j) {
-                    if (!wait_phase(ptx::smem_addr(&ctl->stg_empty[rs.idx]), rs.phase ^ 1u, abort_flag, limit,
-                                    a.status)) {
-                        ok = false;
-                        break;
+                    // every issuer walks the sequence and issues into its own
+                    // slots (never more than one phase ahead on a slot: issuers
+                    // <= slots)
+                    if (Cfg::A_ISSUERS == 1 || rs.idx % Cfg::A_ISSUERS == issuer) {
+                        if (!wait_phase(ptx::smem_addr(&ctl->stg_empty[rs.idx]), rs.phase ^ 1u, abort_flag, limit,
+                                        a.status, kIssuerBackoffNs)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t bar = ptx::smem_addr(&ctl->stg_full[rs.idx]);
+                        ptx::mbar_arrive_expect_tx(bar, STG_BYTES);
+                        if (a.a_rows)
+                            ptx::tma_load_2d(stg_smem + rs.idx * STG_BYTES, &a.tmap_x, cb * KS, m0, bar);
+                        else
+                            ptx::tma_load_im2col_4d(stg_smem + rs.idx * STG_BYTES, &a.tmap_x, cb * KS, w0, h0, n0,
+                                                    (uint16_t)(s * a.dil_w), (uint16_t)(r * a.dil_h), bar);
                     }
-                    const uint32_t bar = ptx::smem_addr(&ctl->stg_full[rs.idx]);
-                    ptx::mbar_arrive_expect_tx(bar, STG_BYTES);
-                    if (a.a_rows)
-                        ptx::tma_load_2d(stg_smem + rs.idx * STG_BYTES, &a.tmap_x, cb * KS, m0, bar);
-                    else
-                        ptx::tma_load_im2col_4d(stg_smem + rs.idx * STG_BYTES, &a.tmap_x, cb * KS, w0, h0, n0,
-                                                (uint16_t)(s * a.dil_w), (uint16_t)(r * a.dil_h), bar);
                     ++issued;
                     rs.next();
                     if (++jr == wu.ke) {  // the rotated sequence wraps to the unit's first k-step
@@ -628,7 +727,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                     }
                 }
             }
-            if (*abort_flag) drain_ring(ctl->stg_full, STG, issued, limit, a.status);
+            if (*abort_flag) drain_ring_owned(ctl->stg_full, STG, issued, issuer, Cfg::A_ISSUERS, limit, a.status);
         } else if (kResB && warp == B_ISSUER_WARP && lane == 0) {
             // every filter block of the call (one tile of output channels),
             // once, onto one barrier; then wait for them so that no copy is
@@ -655,7 +754,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                     if (jr >= kn) jr -= kn;
                     jr += wu.kb;
                     if (!wait_phase(ptx::smem_addr(&ctl->empty[rb.idx]), rb.phase ^ 1u, abort_flag, limit,
-                                    a.status)) {
+                                    a.status, kIssuerBackoffNs)) {
                         ok = false;
                         break;
                     }
@@ -702,7 +801,8 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 const uint32_t slot = gi % NSLOT;
                 const uint32_t aph = (gi / NSLOT) & 1u;
                 // tcgen05.ld is warp-collective: the whole warp proceeds or stops together
-                const bool got = wait_phase(ptx::smem_addr(&ctl->acc_full[slot]), aph, abort_flag, limit, a.status);
+                const bool got =
+                    wait_phase(ptx::smem_addr(&ctl->acc_full[slot]), aph, abort_flag, limit, a.status, kEpilogueBackoffNs);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
@@ -767,28 +867,30 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
             if (a.y_tma == 2) {
                 // Channel-major output: the warp's 32 rows are 32 consecutive
                 // pixels of one image (P*Q is a multiple of 32).  It stages
-                // 16 channels x 32 pixels at a time as 16 rows of 128 bytes,
-                // lane i writing pixel i of each row (no bank conflicts), and
-                // one lane stores them as a {32 pixels, 16 channels, 1 image}
-                // box; the map clips channels past K and images past N.
+                // EPI_COLS channels x 32 pixels at a time as rows of 128
+                // bytes, lane i writing pixel i of each row (no bank
+                // conflicts), and one lane stores them as a {32 pixels,
+                // EPI_COLS channels, 1 image} box; the map clips channels past
+                // K and images past N.
                 const int k0 = nt * NT + col0;
                 const int m0w = mt * MT + quad * 32;
                 const int pq = a.P * a.Q;
                 const int img = m0w / pq;
                 const int pix = m0w - img * pq;
-                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (uint32_t)(Cfg::EPI_BUFS * EPI_BUF_BYTES);
+                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (uint32_t)(Cfg::EPI_BUFS * Cfg::EPI_BUF_BYTES);
 #pragma unroll
-                for (int ch = 0; ch < HALF / EPI_COLS; ++ch) {
-                    const uint32_t buf = ebase + (uint32_t)(ch % Cfg::EPI_BUFS) * EPI_BUF_BYTES;
+                for (int ch = 0; ch < HALF / Cfg::EPI_COLS; ++ch) {
+                    const uint32_t buf = ebase + (uint32_t)(ch % Cfg::EPI_BUFS) * Cfg::EPI_BUF_BYTES;
                     if (lane == 0) ptx::bulk_wait_group_read<Cfg::EPI_BUFS - 1>();  // the store that last read buf is done
                     __syncwarp();
 #pragma unroll
-                    for (int c = 0; c < EPI_COLS; ++c)
-                        ptx::st_shared_b32(buf + (uint32_t)c * 128u + (uint32_t)lane * 4u, (uint32_t)acc[ch * EPI_COLS + c]);
+                    for (int c = 0; c < Cfg::EPI_COLS; ++c)
+                        ptx::st_shared_b32(buf + (uint32_t)c * 128u + (uint32_t)lane * 4u,
+                                           (uint32_t)acc[ch * Cfg::EPI_COLS + c]);
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        ptx::tma_store_3d(&a.tmap_y, pix, k0 + ch * EPI_COLS, img, buf);
+                        ptx::tma_store_3d(&a.tmap_y, pix, k0 + ch * Cfg::EPI_COLS, img, buf);
                         ptx::bulk_commit_group();
                     }
                 }
@@ -797,11 +899,11 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 // staged row
                 const int k0 = nt * NT + col0;
                 const int m0w = mt * MT + quad * 32;
-                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (uint32_t)(Cfg::EPI_BUFS * EPI_BUF_BYTES);
+                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (uint32_t)(Cfg::EPI_BUFS * Cfg::EPI_BUF_BYTES);
                 const uint32_t sw = ((uint32_t)lane >> 1) & 3u;
 #pragma unroll
                 for (int ch = 0; ch < HALF / 64; ++ch) {
-                    const uint32_t buf = ebase + (uint32_t)(ch % Cfg::EPI_BUFS) * EPI_BUF_BYTES;
+                    const uint32_t buf = ebase + (uint32_t)(ch % Cfg::EPI_BUFS) * Cfg::EPI_BUF_BYTES;
                     if (lane == 0) ptx::bulk_wait_group_read<Cfg::EPI_BUFS - 1>();  // the store that last read buf is done
                     __syncwarp();
                     const uint32_t rowaddr = buf + (uint32_t)lane * 64u;
@@ -828,31 +930,34 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 }
             } else if (a.y_tma) {
                 // Rows of the tile are consecutive pixels with contiguous
-                // channels: each warp stages 32 rows x 16 columns at a time in
-                // shared memory (64-byte rows; 16-byte chunk c of row r at
-                // c ^ ((r >> 1) & 3), the 64-byte swizzle) and one lane writes
-                // them with a TMA store, which also clips rows past the last
-                // pixel and columns past K.  Two buffers per warp alternate.
+                // channels: each warp stages 32 rows x EPI_COLS columns at a
+                // time in shared memory (rows of EPI_COLS * 4 bytes; 16-byte
+                // chunk c of row r at c ^ ((r >> 1) & 3), the 64-byte
+                // swizzle, or at c ^ (r & 7), the 128-byte swizzle) and one
+                // lane writes them with a TMA store, which also clips rows
+                // past the last pixel and columns past K.  With two buffers
+                // per warp they alternate.
+                constexpr int CHUNKS = Cfg::EPI_COLS / 4;  // 16-byte chunks per staged row
                 const int k0 = nt * NT + col0;
                 const int m0w = mt * MT + quad * 32;
-                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (uint32_t)(Cfg::EPI_BUFS * EPI_BUF_BYTES);
-                const uint32_t sw = ((uint32_t)lane >> 1) & 3u;
+                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (uint32_t)(Cfg::EPI_BUFS * Cfg::EPI_BUF_BYTES);
+                const uint32_t sw = CHUNKS == 8 ? ((uint32_t)lane & 7u) : (((uint32_t)lane >> 1) & 3u);
 #pragma unroll
-                for (int ch = 0; ch < HALF / EPI_COLS; ++ch) {
-                    const uint32_t buf = ebase + (uint32_t)(ch % Cfg::EPI_BUFS) * EPI_BUF_BYTES;
+                for (int ch = 0; ch < HALF / Cfg::EPI_COLS; ++ch) {
+                    const uint32_t buf = ebase + (uint32_t)(ch % Cfg::EPI_BUFS) * Cfg::EPI_BUF_BYTES;
                     if (lane == 0) ptx::bulk_wait_group_read<Cfg::EPI_BUFS - 1>();  // the store that last read buf is done
                     __syncwarp();
-                    const int i0 = ch * EPI_COLS;
-                    const uint32_t rowaddr = buf + (uint32_t)lane * 64u;
+                    const int i0 = ch * Cfg::EPI_COLS;
+                    const uint32_t rowaddr = buf + (uint32_t)lane * (uint32_t)(Cfg::EPI_COLS * 4);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
+                    for (int c = 0; c < CHUNKS; ++c)
                         ptx::st_shared_v4(rowaddr + ((((uint32_t)c) ^ sw) << 4),
                                           make_uint4((uint32_t)acc[i0 + c * 4], (uint32_t)acc[i0 + c * 4 + 1],
                                                      (uint32_t)acc[i0 + c * 4 + 2], (uint32_t)acc[i0 + c * 4 + 3]));
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        ptx::tma_store_2d(&a.tmap_y, k0 + ch * EPI_COLS, m0w, buf);
+                        ptx::tma_store_2d(&a.tmap_y, k0 + ch * Cfg::EPI_COLS, m0w, buf);
                         ptx::bulk_commit_group();
                     }
                 }
@@ -881,8 +986,9 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 }
             }
         }
-        // the output stores must finish reading shared memory before the CTA exits
-        if (a.y_tma && lane == 0) ptx::bulk_wait_group_all();
+        // the output stores must finish reading shared memory before the CTA
+        // exits (their writes complete with the grid)
+        if (a.y_tma && lane == 0) ptx::bulk_wait_group_read<0>();
     }
 
     ptx::tc_fence_before();
@@ -1169,14 +1275,14 @@ constexpr int64_t kMinSplitSteps = 16;   // k-steps of the shortest run of a cut
 constexpr int64_t kMaxSplits = 32;
 constexpr int64_t kMinTailSteps = 4;     // k-steps of the shortest run of a last-round tile
 
-template <int NT, bool kTma, bool kResB = false>
+template <int NT, bool kTma, bool kResB = false, bool kTmemA = false>
 conv_status launch_conv(const IgemmArgs &a, int grid, cudaStream_t st) {
-    using Cfg = TileCfg<NT, kTma, kResB>;
+    using Cfg = TileCfg<NT, kTma, kResB, kTmemA>;
     static std::atomic<bool> attr_set[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !attr_set[dev].load()) {
-        if (cudaFuncSetAttribute(igemm_conv_kernel<NT, kTma, kResB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(igemm_conv_kernel<NT, kTma, kResB, kTmemA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg::SMEM_BYTES) != cudaSuccess)
             return CONV_ERR_CUDA;
         if (dev >= 0 && dev < 64) attr_set[dev].store(true);
@@ -1196,7 +1302,7 @@ conv_status launch_conv(const IgemmArgs &a, int grid, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, igemm_conv_kernel<NT, kTma, kResB>, a) != cudaSuccess) return CONV_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, igemm_conv_kernel<NT, kTma, kResB, kTmemA>, a) != cudaSuccess) return CONV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
@@ -1219,12 +1325,13 @@ PFN_cuTensorMapEncodeIm2col_v12000 im2col_encoder() {
 
 // im2col map of a channels-last int8 image [N][H][W][C] (byte strides
 // xs_n, xs_h, xs_w): each load brings 128 consecutive output pixels x 64
-// channels.  The bounding box runs from -pre to post - (taps-1)*dil along W
+// channels (rows 64-byte swizzled with swizzle64, for the converters that
+// write the image tile to tensor memory).  The bounding box runs from -pre to post - (taps-1)*dil along W
 // and H so that its traversal at the convolution stride visits exactly the
 // P x Q window origins.  Returns false when the map cannot express the call
 // (stride above 8, corner or offset out of range, encoder unavailable).
 bool encode_im2col_map(const ConvGeom &g, const void *x, int64_t xs_n, int64_t xs_h, int64_t xs_w, int64_t c_dim,
-                       CUtensorMap *map) {
+                       bool swizzle64, CUtensorMap *map) {
     if (g.str_h > 8 || g.str_w > 8) return false;
     const int64_t lo_w = -g.pad_w, lo_h = -g.pad_h;
     const int64_t hi_w = (g.Q - 1) * g.str_w + lo_w - (g.W - 1);  // = post_w - (S-1)*dil_w
@@ -1242,7 +1349,8 @@ bool encode_im2col_map(const ConvGeom &g, const void *x, int64_t xs_n, int64_t x
     const cuuint32_t estr[4] = {1, (cuuint32_t)g.str_w, (cuuint32_t)g.str_h, 1};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(x), dims, strides, lower, upper,
                            (cuuint32_t)KS, (cuuint32_t)MT, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                           swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -1252,9 +1360,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tiled_encoder();
 // 2-D map [pixels][channels] of a channels-last image whose pixels follow
 // one another at xs_w bytes (dense rows): for a 1x1 filter with stride 1 and
 // no padding, the image tile of output pixels m0.. is the box of rows m0..
-// (128 rows x 64 channels, unswizzled: the same staging layout as the
-// im2col load).
-bool encode_rows_map(const ConvGeom &g, const void *x, int64_t xs_w, int64_t c_dim, CUtensorMap *map) {
+// (128 rows x 64 channels: the same staging layout as the im2col load,
+// 64-byte swizzled or not).
+bool encode_rows_map(const ConvGeom &g, const void *x, int64_t xs_w, int64_t c_dim, bool swizzle64,
+                     CUtensorMap *map) {
     const int64_t rows = g.N * g.H * g.W;
     if (((uintptr_t)x % 16) != 0 || xs_w % 16 || rows >= ((int64_t)1 << 32)) return false;
     auto enc = tiled_encoder();
@@ -1264,7 +1373,8 @@ bool encode_rows_map(const ConvGeom &g, const void *x, int64_t xs_w, int64_t c_d
     const cuuint32_t box[2] = {(cuuint32_t)KS, (cuuint32_t)MT};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(x), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -1287,8 +1397,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tiled_encoder() {
 // 2-D map [N*P*Q pixels][K channels] of the output when its pixels follow one
 // another at a fixed stride with channels contiguous (NHWC, possibly with
 // padded pixel rows): box 32 pixels x 64 bytes of channels (16 int32 or 64
-// int8) with the 64-byte swizzle.  Returns false for any other layout.
-bool encode_output_map(const ConvGeom &g, const void *y, CUtensorMap *map) {
+// int8) with the 64-byte swizzle, or (wide, int32) 32 pixels x 32 int32 with
+// the 128-byte swizzle.  Returns false for any other layout.
+bool encode_output_map(const ConvGeom &g, const void *y, bool wide, CUtensorMap *map) {
     const int64_t esz = g.out_int8 ? 1 : 4;
     if (g.ys[1] != 1 && g.K > 1) return false;
     int64_t ps;  // element stride between consecutive pixels
@@ -1309,22 +1420,23 @@ bool encode_output_map(const ConvGeom &g, const void *y, CUtensorMap *map) {
     if (!enc) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)g.K, (cuuint64_t)m_total};
     const cuuint64_t strides[1] = {(cuuint64_t)(ps * esz)};
-    const cuuint32_t box[2] = {(cuuint32_t)(g.out_int8 ? 64 : EPI_COLS), 32};
+    const bool w32 = wide && !g.out_int8;
+    const cuuint32_t box[2] = {(cuuint32_t)(g.out_int8 ? 64 : (w32 ? 32 : 16)), 32};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = enc(map, g.out_int8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_INT32, 2,
                            const_cast<void *>(y), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_64B,
+                           w32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
 // 3-D map [N][K][P*Q] of an int32 output whose channels each hold their P*Q
 // pixels contiguously (NCHW, possibly with padded channel or image strides):
-// box 32 pixels x 16 channels x 1 image, no swizzle.  Requires P*Q to be a
+// box 32 pixels x 16 (or, wide, 32) channels x 1 image, no swizzle.  Requires P*Q to be a
 // multiple of 32, so that the 32 pixels of an epilogue warp never straddle
 // two images and start 128 bytes aligned.  Returns false for any other
 // layout.
-bool encode_output_map_nchw(const ConvGeom &g, const void *y, CUtensorMap *map) {
+bool encode_output_map_nchw(const ConvGeom &g, const void *y, bool wide, CUtensorMap *map) {
     if (g.out_int8) return false;
     const int64_t pq = g.P * g.Q;
     if (pq % 32 != 0) return false;
@@ -1338,7 +1450,7 @@ bool encode_output_map_nchw(const ConvGeom &g, const void *y, CUtensorMap *map) 
     if (!enc) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)pq, (cuuint64_t)g.K, (cuuint64_t)g.N};
     const cuuint64_t strides[2] = {(cuuint64_t)(ks * 4), (cuuint64_t)(ns * 4)};
-    const cuuint32_t box[3] = {32, (cuuint32_t)EPI_COLS, 1};
+    const cuuint32_t box[3] = {32, (cuuint32_t)(wide ? 32 : 16), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_INT32, 3, const_cast<void *>(y), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
@@ -1378,7 +1490,10 @@ void igemm_plan(const ConvGeom &g, const void *x_dev, IgemmPlan *pl) {
     pl->wpack_bytes = (size_t)align256(pl->n_tiles * pl->k_steps * pl->n_tile * (int64_t)(KS * 2));
     // one tile of output channels whose filter blocks fit in shared memory:
     // the filter stays resident in every CTA (taken with the TMA producers)
-    pl->resident_b = pl->n_tiles == 1 && pl->k_steps * pl->n_tile * (int64_t)(KS * 2) <= RESB_MAX_BYTES;
+    // (256-column tiles: the 128-column ones put their image tile in tensor
+    // memory and spend the shared memory on image staging instead)
+    pl->resident_b =
+        pl->n_tile == 256 && pl->n_tiles == 1 && pl->k_steps * pl->n_tile * (int64_t)(KS * 2) <= RESB_MAX_BYTES;
     pl->xpack_bytes = pl->pack_x ? (size_t)align256(g.N * g.H * g.W * pl->c16) : 0;
     // One CTA per SM walks the tiles.  With fewer tiles than SMs and long
     // reductions (the weight gradient's shape: few output tiles, a reduction
@@ -1505,7 +1620,6 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
                (g.ys[2] % 4) == 0 && (g.ys[3] % 4) == 0)
                   ? 1
                   : 0;
-    a.y_tma = encode_output_map(g, y, &a.tmap_y) ? 1 : (encode_output_map_nchw(g, y, &a.tmap_y) ? 2 : 0);
     a.wait_limit_ns = wait_limit_ns();
     a.status = device_status_word();
     if (!a.status) return CONV_ERR_CUDA;
@@ -1518,19 +1632,30 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
                 g.P == g.H && g.Q == g.W && a.xs_h == g.W * a.xs_w && a.xs_n == g.H * a.xs_h)
                    ? 1
                    : 0;
+    // 128-column tiles keep the f16 image tile in tensor memory; their
+    // staging loads are 64-byte swizzled for the converters' row reads
+    const bool tmem_a = pl.n_tile == 128;
     bool tma = false;
     if (!pl.register_loads) {
-        if (a.a_rows) tma = encode_rows_map(g, a.x, a.xs_w, c_dim, &a.tmap_x);
+        if (a.a_rows) tma = encode_rows_map(g, a.x, a.xs_w, c_dim, tmem_a, &a.tmap_x);
         if (!tma) {
             a.a_rows = 0;
-            tma = encode_im2col_map(g, a.x, a.xs_n, a.xs_h, a.xs_w, c_dim, &a.tmap_x);
+            tma = encode_im2col_map(g, a.x, a.xs_n, a.xs_h, a.xs_w, c_dim, tmem_a, &a.tmap_x);
         }
     }
     conv_status rc;
-    if (tma && pl.resident_b)
-        rc = pl.n_tile == 256 ? launch_conv<256, true, true>(a, grid, st) : launch_conv<128, true, true>(a, grid, st);
+    // the tensor-memory variant stages 32 output columns per store
+    const bool wide_out = tma && tmem_a;
+    a.y_tma = encode_output_map(g, y, wide_out, &a.tmap_y) ? 1 : (encode_output_map_nchw(g, y, wide_out, &a.tmap_y) ? 2 : 0);
+    // TMA path: 128-column tiles keep the image tile in tensor memory;
+    // 256-column tiles keep it in shared memory, with the filter resident
+    // when it fits
+    if (tma && tmem_a)
+        rc = launch_conv<128, true, false, true>(a, grid, st);
+    else if (tma && pl.resident_b)
+        rc = launch_conv<256, true, true>(a, grid, st);
     else if (tma)
-        rc = pl.n_tile == 256 ? launch_conv<256, true>(a, grid, st) : launch_conv<128, true>(a, grid, st);
+        rc = launch_conv<256, true>(a, grid, st);
     else
         rc = pl.n_tile == 256 ? launch_conv<256, false>(a, grid, st) : launch_conv<128, false>(a, grid, st);
     if (rc || pl.splits <= 1) return rc;
