@@ -16,7 +16,7 @@
 // registers.  The result is bit-identical to integer arithmetic.
 //
 // Persistent, warp-specialised CTA (one per SM), 512 threads, tile 128 pixels
-// x NT output channels (NT = 128 or 256).  Two ways to stage the image tile:
+// x NT output channels (NT = 128, 192 or 256).  Two ways to stage the image tile:
 //  * TMA (default): warp 5 lane 0 issues one TMA im2col load per k-step (128
 //    output pixels x 64 channels of one tap, zero outside the image) into a
 //    6-deep (NT = 256) or 8-deep (NT = 128) int8 staging ring; warpgroup 0
@@ -114,17 +114,19 @@ constexpr int RESB_MAX_BYTES = 128 * 1024;
 template <int NT, bool kTma, bool kResB = false, bool kTmemA = false>
 struct TileCfg {
     static constexpr int B_BYTES = NT * KS * 2;
-    static constexpr int ST = kTmemA ? 4 : (kResB ? 2 : (kTma ? (NT == 256 ? IGEMM_ST_256 : IGEMM_ST_128)
-                                                                : (NT == 256 ? 4 : 6)));
+    // (192-column tiles: 40 KB stages, four of them behind four staging buffers)
+    static constexpr int ST = kTmemA ? 4 : (kResB ? 2 : (kTma ? (NT == 256 ? IGEMM_ST_256 : (NT == 192 ? 4 : IGEMM_ST_128))
+                                                                : (NT == 128 ? 6 : 4)));
     static constexpr int STG_STAGES = kTmemA ? (kResB ? 10 : 12)
-                                             : (kResB ? 6 : (kTma ? (NT == 256 ? IGEMM_STG_256 : IGEMM_STG_128) : 0));
+                                             : (kResB ? 6 : (kTma ? (NT == 256 ? IGEMM_STG_256 : (NT == 192 ? 4 : IGEMM_STG_128)) : 0));
     static constexpr int EPI_BUFS = kResB ? 1 : 2;  // output staging buffers per epilogue warp
     static constexpr int EPI_COLS = kTmemA ? 32 : 16;
     static constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 4;  // 2 or 4 KB
     static constexpr int EPI_BYTES = 8 * EPI_BUFS * EPI_BUF_BYTES;
     static constexpr int A_SMEM = kTmemA ? 0 : ST * A_BYTES;
     static constexpr int B_AREA = kResB ? RESB_MAX_BYTES : ST * B_BYTES;
-    static constexpr int TMEM_COLS = kTmemA ? 512 : NSLOT * NT;
+    // (allocations are powers of two: two 192-column slots take 512)
+    static constexpr int TMEM_COLS = (kTmemA || NT == 192) ? 512 : NSLOT * NT;
     static constexpr int TMEM_A_COL = NSLOT * NT;  // kTmemA: first column of the image stages
     // Warps that issue the image loads (kTmemA: warps 5 and 7, one thread
     // each): issuer i issues the loads into the staging slots s % A_ISSUERS
@@ -1481,7 +1483,9 @@ void igemm_plan(const ConvGeom &g, const void *x_dev, IgemmPlan *pl) {
                         (g.xs[3] % 16) == 0 && (x_dev == nullptr || ((uintptr_t)x_dev % 16) == 0);
     pl->pack_x = !direct;
     pl->register_loads = false;
-    pl->n_tile = g.K > 128 ? 256 : 128;
+    // output channels per tile: 128, 192 or 256 (the smallest that covers
+    // K, so that no MMA column is wasted on 129..192 channels)
+    pl->n_tile = g.K > 192 ? 256 : (g.K > 128 ? 192 : 128);
     pl->c16 = (g.C + 15) / 16 * 16;
     pl->c_steps = (g.C + KS - 1) / KS;
     pl->k_steps = g.R * g.S * pl->c_steps;
@@ -1647,6 +1651,9 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
     // the tensor-memory variant stages 32 output columns per store
     const bool wide_out = tma && tmem_a;
     a.y_tma = encode_output_map(g, y, wide_out, &a.tmap_y) ? 1 : (encode_output_map_nchw(g, y, wide_out, &a.tmap_y) ? 2 : 0);
+    // int8 outputs are staged 64 columns at a time: a 192-column tile (96
+    // per epilogue warp) stores them with plain stores
+    if (g.out_int8 && pl.n_tile == 192) a.y_tma = 0;
     // TMA path: 128-column tiles keep the image tile in tensor memory;
     // 256-column tiles keep it in shared memory, with the filter resident
     // when it fits
@@ -1655,9 +1662,10 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
     else if (tma && pl.resident_b)
         rc = launch_conv<256, true, true>(a, grid, st);
     else if (tma)
-        rc = launch_conv<256, true>(a, grid, st);
+        rc = pl.n_tile == 256 ? launch_conv<256, true>(a, grid, st) : launch_conv<192, true>(a, grid, st);
     else
-        rc = pl.n_tile == 256 ? launch_conv<256, false>(a, grid, st) : launch_conv<128, false>(a, grid, st);
+        rc = pl.n_tile == 256 ? launch_conv<256, false>(a, grid, st)
+                              : (pl.n_tile == 192 ? launch_conv<192, false>(a, grid, st) : launch_conv<128, false>(a, grid, st));
     if (rc || pl.splits <= 1) return rc;
     const int32_t cut_tiles = a.num_tiles - a.full_units;
     int64_t blocks = (int64_t)cut_tiles * (pl.n_tile / kRedCols) * (MT / kRedRows);

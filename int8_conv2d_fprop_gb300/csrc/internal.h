@@ -69,7 +69,7 @@ struct IgemmPlan {
     bool pack_x;            // image must be copied to channels-last first
     bool register_loads;    // gather the image with global loads, not TMA im2col
     bool resident_b;        // the whole repacked filter stays in shared memory (TMA path)
-    int64_t n_tile;         // output channels per tile (128 or 256)
+    int64_t n_tile;         // output channels per tile (128, 192 or 256)
     int64_t c16;            // channel count rounded up to 16 (valid load width)
     int64_t c_steps;        // ceil(C / 64)
     int64_t k_steps;        // R * S * c_steps

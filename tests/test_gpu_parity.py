@@ -103,6 +103,8 @@ def _shape_cases():
         C("one_by_one_strided", 2, 128, 15, 15, 130, 1, 1, stride=(2, 2), bias=True, seed=16),
         C("tiny_c3", 1, 3, 12, 9, 10, 3, 3, pre=(1, 1), post=(1, 1), x_layout="NCHW", w_layout="KCRS",
           y_layout="NCHW", seed=17),
+        # 129..192 output channels: 192-column tiles, ragged K
+        C("k150_nt192", 2, 96, 9, 11, 150, 3, 3, stride=(1, 2), pre=(1, 1), post=(1, 0), bias=True, seed=18),
     ]
 
 
@@ -125,6 +127,8 @@ def _int8_out_cases():
         C("nchw_conv_mode", 2, 32, 11, 12, 20, 4, 2, stride=(1, 2), dilation=(2, 1), pre=(3, 0), post=(2, 1),
           mode=1, bias=True, relu=True, x_layout="NCHW", w_layout="KCRS", y_layout="NCHW", seed=43),
         C("one_by_one_k256", 2, 128, 15, 15, 256, 1, 1, stride=(2, 2), bias=True, seed=44),
+        # 192-column tiles write int8 with plain stores (96 columns per epilogue warp)
+        C("nhwc_k160_nt192", 2, 64, 10, 12, 160, 3, 3, pre=(1, 1), post=(1, 1), bias=True, relu=True, seed=45),
     ]
 
 
