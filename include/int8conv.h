@@ -395,6 +395,33 @@ typedef struct {
 
 conv_status conv_measure_peak_rates(void *scratch, size_t scratch_bytes, conv_peak_rates *out, void *stream);
 
+/*
+ * Plan caches (the cuDNN-frontend tutorial's kernel/plan cache, for repeated
+ * calls of one shape): conv_fprop, its two halves, the static-workspace and
+ * host-buffer variants and the gradients' forward convolutions keep
+ *   - the validated geometry, algorithm and tensor-core plan of a call,
+ *     keyed by the three descriptors, the parameters, the device and whether
+ *     the image pointer is 16-byte aligned (64 entries), and
+ *   - the tensor-core kernel's launch arguments with their encoded TMA
+ *     tensor maps, keyed by that plan and the 16-byte alignment of the image
+ *     and output pointers (32 entries); a call with other buffers re-targets
+ *     the cached maps to its addresses (cuTensorMapReplaceAddress) instead of
+ *     encoding them again.
+ * A call whose key is cached skips validation, planning and map encoding;
+ * its pointer checks (null, overlap, workspace) still run.  The caches are
+ * library-owned host memory, shared by all threads (a mutex guards them),
+ * least recently used entries giving way.  Cache lookups make no CUDA calls,
+ * so cached calls stay capturable in CUDA graphs.
+ *
+ * conv_shutdown empties both caches (their memory is static; nothing is
+ * freed or allocated).  Call it when no other thread is inside a library
+ * call.  conv_plan_cache_stats reads the hit and miss counts since the
+ * library was loaded.
+ */
+void conv_shutdown(void);
+conv_status conv_plan_cache_stats(uint64_t *plan_hits, uint64_t *plan_misses, uint64_t *launch_hits,
+                                  uint64_t *launch_misses);
+
 /* Human-readable name of a status. */
 const char *conv_status_string(conv_status s);
 

@@ -51,7 +51,7 @@ EXPORTED_SYMBOLS = (
     "conv_fprop_host_buffer_size", "conv_fprop_host", "conv_device_status",
     "conv_selftest_wait_timeout", "conv_status_string", "conv_library_version",
     "conv_dgrad_workspace_size", "conv_dgrad", "conv_wgrad_workspace_size", "conv_wgrad",
-    "conv_measure_peak_rates",
+    "conv_measure_peak_rates", "conv_shutdown", "conv_plan_cache_stats",
 )
 
 
@@ -180,6 +180,11 @@ def lib():
         L.conv_measure_peak_rates.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.POINTER(PeakRates),
                                               ctypes.c_void_p]
         L.conv_measure_peak_rates.restype = ctypes.c_int
+        L.conv_shutdown.argtypes = []
+        L.conv_shutdown.restype = None
+        u64p = ctypes.POINTER(ctypes.c_uint64)
+        L.conv_plan_cache_stats.argtypes = [u64p, u64p, u64p, u64p]
+        L.conv_plan_cache_stats.restype = ctypes.c_int
         L.conv_device_status.argtypes = [ctypes.c_void_p]
         L.conv_selftest_wait_timeout.argtypes = [ctypes.c_uint32, ctypes.c_void_p]
         L.conv_status_string.argtypes = [ctypes.c_int]
@@ -314,6 +319,19 @@ def measure_peak_rates(scratch_ptr: int, scratch_bytes: int, stream: int = 0) ->
     _check(lib().conv_measure_peak_rates(scratch_ptr or None, int(scratch_bytes), ctypes.byref(r), stream or None),
            "peak rates")
     return {name: float(getattr(r, name)) for name, _ in PeakRates._fields_}
+
+
+def shutdown() -> None:
+    """Empty the library's plan caches (conv_shutdown)."""
+    lib().conv_shutdown()
+
+
+def plan_cache_stats() -> dict:
+    """Hit and miss counts of the plan and launch caches since load."""
+    v = [ctypes.c_uint64() for _ in range(4)]
+    _check(lib().conv_plan_cache_stats(*[ctypes.byref(x) for x in v]), "plan cache stats")
+    return {"plan_hits": v[0].value, "plan_misses": v[1].value, "launch_hits": v[2].value,
+            "launch_misses": v[3].value}
 
 
 def device_status(stream: int = 0) -> int:

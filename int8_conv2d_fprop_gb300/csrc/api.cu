@@ -4,6 +4,8 @@
 
 #include <atomic>
 #include <cstdlib>
+#include <cstring>
+#include <mutex>
 
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -81,8 +83,107 @@ int choose_algo(const ConvGeom &g, int requested) {
     return CONV_ALGO_DIRECT_GENERIC;
 }
 
+// Plan cache: the validated geometry, algorithm and tensor-core plan of a
+// call, keyed by its descriptors, parameters, device and whether the image
+// pointer is 16-byte aligned (the only thing the plan reads of a pointer).
+// Repeated calls with the same shapes skip validation and planning.  Least
+// recently used entries give way; conv_shutdown empties it.
+struct PlanKey {
+    int64_t v[64];
+    int n;
+};
+
+void put_desc(PlanKey &k, const conv_tensor_desc *d) {
+    k.v[k.n++] = d->dtype;
+    k.v[k.n++] = d->rank;
+    for (int i = 0; i < 4; ++i) k.v[k.n++] = d->dims[i];
+    for (int i = 0; i < 4; ++i) k.v[k.n++] = d->strides[i];
+    k.v[k.n++] = (int64_t)d->capacity_bytes;
+}
+
+PlanKey make_plan_key(const conv_tensor_desc *x, const conv_tensor_desc *w, const conv_tensor_desc *y,
+                      const conv_fprop_params *p, const void *x_dev, int dev) {
+    PlanKey k;
+    std::memset(&k, 0, sizeof(k));
+    put_desc(k, x);
+    put_desc(k, w);
+    put_desc(k, y);
+    for (int i = 0; i < 2; ++i) {
+        k.v[k.n++] = p->pre_padding[i];
+        k.v[k.n++] = p->post_padding[i];
+        k.v[k.n++] = p->stride[i];
+        k.v[k.n++] = p->dilation[i];
+    }
+    k.v[k.n++] = p->mode;
+    k.v[k.n++] = p->compute_dtype;
+    k.v[k.n++] = p->epilogue;
+    k.v[k.n++] = p->algo;
+    k.v[k.n++] = p->out_shift;
+    k.v[k.n++] = dev;
+    k.v[k.n++] = (x_dev == nullptr || ((uintptr_t)x_dev % 16) == 0) ? 1 : 0;
+    return k;
+}
+
+constexpr int kPlanCacheSize = 64;
+struct PlanCacheEntry {
+    PlanKey key;
+    ConvGeom g;
+    int algo;
+    IgemmPlan pl;
+    uint64_t used;
+    bool valid;
+};
+std::mutex g_plan_mu;
+PlanCacheEntry g_plan_cache[kPlanCacheSize];
+uint64_t g_plan_clock = 0;
+std::atomic<uint64_t> g_plan_hits{0}, g_plan_misses{0};
+
+conv_status plan_call_uncached(const conv_tensor_desc *x, const conv_tensor_desc *w, const conv_tensor_desc *y,
+                               const conv_fprop_params *p, const void *x_dev, ConvGeom *g, int *algo,
+                               IgemmPlan *pl);
+
 conv_status plan_call(const conv_tensor_desc *x, const conv_tensor_desc *w, const conv_tensor_desc *y,
                       const conv_fprop_params *p, const void *x_dev, ConvGeom *g, int *algo, IgemmPlan *pl) {
+    if (!x || !w || !y || !p) return CONV_ERR_NULL_PTR;
+    int dev = 0;
+    cudaGetDevice(&dev);  // (no device: plans are keyed on ordinal 0)
+    const PlanKey key = make_plan_key(x, w, y, p, x_dev, dev);
+    {
+        std::lock_guard<std::mutex> lock(g_plan_mu);
+        for (auto &e : g_plan_cache)
+            if (e.valid && e.key.n == key.n && std::memcmp(e.key.v, key.v, sizeof(int64_t) * key.n) == 0) {
+                e.used = ++g_plan_clock;
+                *g = e.g;
+                *algo = e.algo;
+                *pl = e.pl;
+                g_plan_hits.fetch_add(1);
+                return CONV_OK;
+            }
+    }
+    g_plan_misses.fetch_add(1);
+    conv_status st = plan_call_uncached(x, w, y, p, x_dev, g, algo, pl);
+    if (st) return st;  // only valid plans are kept
+    std::lock_guard<std::mutex> lock(g_plan_mu);
+    PlanCacheEntry *victim = &g_plan_cache[0];
+    for (auto &e : g_plan_cache) {
+        if (!e.valid) {
+            victim = &e;
+            break;
+        }
+        if (e.used < victim->used) victim = &e;
+    }
+    victim->key = key;
+    victim->g = *g;
+    victim->algo = *algo;
+    victim->pl = *pl;
+    victim->used = ++g_plan_clock;
+    victim->valid = true;
+    return CONV_OK;
+}
+
+conv_status plan_call_uncached(const conv_tensor_desc *x, const conv_tensor_desc *w, const conv_tensor_desc *y,
+                               const conv_fprop_params *p, const void *x_dev, ConvGeom *g, int *algo,
+                               IgemmPlan *pl) {
     const int64_t bias_elems = (p && (p->epilogue & CONV_EPILOGUE_BIAS)) ? (w ? w->dims[0] : 0) : 0;
     conv_status st = conv_fprop_validate(x, w, y, p, bias_elems);
     if (st) return st;
@@ -284,6 +385,23 @@ conv_status conv_device_status(void *stream) {
         if (cudaMemcpyToSymbol(g_conv_device_status, &zero, sizeof(int)) != cudaSuccess) return CONV_ERR_CUDA;
     }
     return (conv_status)v;
+}
+
+void conv_shutdown(void) {
+    {
+        std::lock_guard<std::mutex> lock(g_plan_mu);
+        for (auto &e : g_plan_cache) e.valid = false;
+    }
+    igemm_cache_clear();
+}
+
+conv_status conv_plan_cache_stats(uint64_t *plan_hits, uint64_t *plan_misses, uint64_t *launch_hits,
+                                  uint64_t *launch_misses) {
+    if (!plan_hits || !plan_misses || !launch_hits || !launch_misses) return CONV_ERR_NULL_PTR;
+    *plan_hits = g_plan_hits.load();
+    *plan_misses = g_plan_misses.load();
+    igemm_cache_stats(launch_hits, launch_misses);
+    return CONV_OK;
 }
 
 conv_status conv_selftest_wait_timeout(uint32_t limit_us, void *stream) {

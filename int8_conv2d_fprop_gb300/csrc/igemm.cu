@@ -47,6 +47,8 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstring>
+#include <mutex>
 
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -1563,32 +1565,115 @@ conv_status igemm_pack_filter_launch(const ConvGeom &g, const IgemmPlan &pl, con
     return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
-conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *y,
-                              const int32_t *bias, void *workspace, void *stream) {
-    cudaStream_t st = (cudaStream_t)stream;
-    const int sms = device_sm_count();
-    uint8_t *wp = static_cast<uint8_t *>(workspace);
+namespace {
+
+PFN_cuTensorMapReplaceAddress_v12000 address_replacer() {
+    static std::atomic<void *> fn{nullptr};
+    static std::atomic<bool> tried{false};
+    if (!tried.load()) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapReplaceAddress", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn.store(p);
+        tried.store(true);
+    }
+    return reinterpret_cast<PFN_cuTensorMapReplaceAddress_v12000>(fn.load());
+}
+
+enum Variant { V_REG128, V_REG192, V_REG256, V_TMEM128, V_TMA192, V_TMA256, V_RESB256 };
+
+// Everything a launch of the convolution kernel needs that does not change
+// with the buffers' addresses: the kernel arguments (tensor maps encoded for
+// the addresses of the call that built them) and the kernel variant.
+struct LaunchPlan {
     IgemmArgs a;
-    if (pl.pack_x) {
-        int8_t *xp = reinterpret_cast<int8_t *>(wp + pl.xpack_off);
-        const int64_t hw = g.H * g.W;
-        const bool planes = (g.W == 1 || g.xs[3] == 1) && (g.H == 1 || g.xs[2] == g.W) && g.xs[1] % 16 == 0 &&
-                            g.xs[0] % 16 == 0 && hw % 16 == 0 && ((uintptr_t)x % 16) == 0 && hw < ((int64_t)1 << 31);
-        if (planes) {
-            const int64_t total = g.N * ((hw + kPackPix - 1) / kPackPix) * ((pl.c16 + kPackCh - 1) / kPackCh);
-            int64_t blocks = total < (int64_t)sms * 8 ? total : (int64_t)sms * 8;
-            igemm_pack_image_planes_kernel<<<(unsigned)blocks, 256, 0, st>>>(x, g.xs[0], g.xs[1], g.N, (int32_t)g.C,
-                                                                             (int32_t)hw, (int32_t)pl.c16, xp);
-        } else {
-            const int64_t total = g.N * g.H * g.W * (pl.c16 / 16);
-            int64_t blocks = (total + 255) / 256;
-            if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
-            igemm_pack_image_kernel<<<(unsigned)blocks, 256, 0, st>>>(x, g.xs[0], g.xs[1], g.xs[2], g.xs[3], g.N,
-                                                                      (int32_t)g.C, (int32_t)g.H, (int32_t)g.W,
-                                                                      (int32_t)pl.c16, xp);
+    int variant;
+    bool tma;
+    bool planes;          // plane-contiguous image copy (when the image is repacked)
+    const void *x_map;    // addresses the maps were encoded with
+    const void *y_map;
+};
+
+// Launch-plan cache: key = geometry, plan, device and the 16-byte alignment
+// of the image and output pointers; a hit re-targets the cached tensor maps
+// to the call's addresses with cuTensorMapReplaceAddress instead of encoding
+// them again.  Least recently used entries give way; conv_shutdown empties it.
+struct LaunchKey {
+    int64_t v[64];
+    int n;
+};
+
+// The key's fields, one int64 each (no padding bytes compared).
+LaunchKey make_key(const ConvGeom &g, const IgemmPlan &pl, int dev, int align) {
+    LaunchKey k;
+    std::memset(&k, 0, sizeof(k));
+    int n = 0;
+    auto put = [&](int64_t v) { k.v[n++] = v; };
+    put(g.N); put(g.C); put(g.H); put(g.W); put(g.K); put(g.R); put(g.S); put(g.P); put(g.Q);
+    for (int i = 0; i < 4; ++i) { put(g.xs[i]); put(g.ws[i]); put(g.ys[i]); }
+    put(g.pad_h); put(g.pad_w); put(g.str_h); put(g.str_w); put(g.dil_h); put(g.dil_w);
+    put(g.mode); put(g.bias); put(g.relu); put(g.out_int8); put(g.out_shift);
+    put(pl.pack_x); put(pl.register_loads); put(pl.resident_b); put(pl.n_tile); put(pl.c16); put(pl.c_steps);
+    put(pl.k_steps); put(pl.n_tiles); put(pl.m_tiles); put((int64_t)pl.wpack_bytes); put((int64_t)pl.xpack_bytes);
+    put(pl.full_units); put(pl.splits); put(pl.num_units); put(pl.grid); put((int64_t)pl.tail_part_off);
+    put((int64_t)pl.tail_part_bytes); put((int64_t)pl.xpack_off); put((int64_t)pl.workspace_bytes);
+    put(dev); put(align);
+    k.n = n;
+    return k;
+}
+
+constexpr int kLaunchCacheSize = 32;
+struct LaunchCacheEntry {
+    LaunchKey key;
+    LaunchPlan plan;
+    uint64_t used;
+    bool valid;
+};
+std::mutex g_launch_mu;
+LaunchCacheEntry g_launch_cache[kLaunchCacheSize];
+uint64_t g_launch_clock = 0;
+std::atomic<uint64_t> g_launch_hits{0}, g_launch_misses{0};
+
+bool launch_lookup(const LaunchKey &k, LaunchPlan *out) {
+    std::lock_guard<std::mutex> lock(g_launch_mu);
+    for (auto &e : g_launch_cache)
+        if (e.valid && std::memcmp(&e.key, &k, sizeof(k)) == 0) {
+            e.used = ++g_launch_clock;
+            *out = e.plan;
+            return true;
         }
-        if (cudaGetLastError() != cudaSuccess) return CONV_ERR_CUDA;
-        a.x = xp;
+    return false;
+}
+
+void launch_insert(const LaunchKey &k, const LaunchPlan &p) {
+    std::lock_guard<std::mutex> lock(g_launch_mu);
+    LaunchCacheEntry *victim = &g_launch_cache[0];
+    for (auto &e : g_launch_cache) {
+        if (!e.valid) {
+            victim = &e;
+            break;
+        }
+        if (e.used < victim->used) victim = &e;
+    }
+    victim->key = k;
+    victim->plan = p;
+    victim->used = ++g_launch_clock;
+    victim->valid = true;
+}
+
+// Builds the launch plan of a call (kernel arguments, tensor maps, variant).
+conv_status build_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *y, uint8_t *wp,
+                         LaunchPlan *L) {
+    IgemmArgs &a = L->a;
+    std::memset(&a, 0, sizeof(a));
+    L->planes = false;
+    if (pl.pack_x) {
+        const int64_t hw = g.H * g.W;
+        L->planes = (g.W == 1 || g.xs[3] == 1) && (g.H == 1 || g.xs[2] == g.W) && g.xs[1] % 16 == 0 &&
+                    g.xs[0] % 16 == 0 && hw % 16 == 0 && ((uintptr_t)x % 16) == 0 && hw < ((int64_t)1 << 31);
+        a.x = reinterpret_cast<int8_t *>(wp + pl.xpack_off);
         a.xs_n = g.H * g.W * pl.c16;
         a.xs_h = g.W * pl.c16;
         a.xs_w = pl.c16;
@@ -1602,7 +1687,6 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
     a.y = y;
     a.out_int8 = g.out_int8 ? 1 : 0;
     a.out_shift = g.out_shift;
-    a.bias = g.bias ? bias : nullptr;
     a.ys_n = g.ys[0]; a.ys_k = g.ys[1]; a.ys_p = g.ys[2]; a.ys_q = g.ys[3];
     a.H = (int32_t)g.H; a.W = (int32_t)g.W; a.P = (int32_t)g.P; a.Q = (int32_t)g.Q;
     a.K = (int32_t)g.K; a.S = (int32_t)g.S;
@@ -1627,8 +1711,6 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
     a.wait_limit_ns = wait_limit_ns();
     a.status = device_status_word();
     if (!a.status) return CONV_ERR_CUDA;
-    if (a.num_tiles == 0) return CONV_OK;
-    const int grid = (int)pl.grid;
     // a 1x1 filter at stride 1 without padding over dense pixel rows reads
     // image pixel m for output pixel m: plain 2-D boxes instead of im2col
     const int64_t c_dim = pl.pack_x ? pl.c16 : g.C;
@@ -1647,7 +1729,6 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
             tma = encode_im2col_map(g, a.x, a.xs_n, a.xs_h, a.xs_w, c_dim, tmem_a, &a.tmap_x);
         }
     }
-    conv_status rc;
     // the tensor-memory variant stages 32 output columns per store
     const bool wide_out = tma && tmem_a;
     a.y_tma = encode_output_map(g, y, wide_out, &a.tmap_y) ? 1 : (encode_output_map_nchw(g, y, wide_out, &a.tmap_y) ? 2 : 0);
@@ -1657,15 +1738,102 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
     // TMA path: 128-column tiles keep the image tile in tensor memory;
     // 256-column tiles keep it in shared memory, with the filter resident
     // when it fits
+    L->tma = tma;
     if (tma && tmem_a)
-        rc = launch_conv<128, true, false, true>(a, grid, st);
+        L->variant = V_TMEM128;
     else if (tma && pl.resident_b)
-        rc = launch_conv<256, true, true>(a, grid, st);
+        L->variant = V_RESB256;
     else if (tma)
-        rc = pl.n_tile == 256 ? launch_conv<256, true>(a, grid, st) : launch_conv<192, true>(a, grid, st);
+        L->variant = pl.n_tile == 256 ? V_TMA256 : V_TMA192;
     else
-        rc = pl.n_tile == 256 ? launch_conv<256, false>(a, grid, st)
-                              : (pl.n_tile == 192 ? launch_conv<192, false>(a, grid, st) : launch_conv<128, false>(a, grid, st));
+        L->variant = pl.n_tile == 256 ? V_REG256 : (pl.n_tile == 192 ? V_REG192 : V_REG128);
+    L->x_map = a.x;
+    L->y_map = y;
+    return CONV_OK;
+}
+
+}  // namespace
+
+void igemm_cache_clear() {
+    std::lock_guard<std::mutex> lock(g_launch_mu);
+    for (auto &e : g_launch_cache) e.valid = false;
+}
+
+void igemm_cache_stats(uint64_t *hits, uint64_t *misses) {
+    *hits = g_launch_hits.load();
+    *misses = g_launch_misses.load();
+}
+
+conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *y,
+                              const int32_t *bias, void *workspace, void *stream) {
+    cudaStream_t st = (cudaStream_t)stream;
+    const int sms = device_sm_count();
+    uint8_t *wp = static_cast<uint8_t *>(workspace);
+    if (pl.m_tiles * pl.n_tiles == 0) return CONV_OK;
+
+    // the launch plan: from the cache when an equal call ran before
+    int dev = 0;
+    cudaGetDevice(&dev);
+    // (every decision of build_launch that reads a pointer reads only its
+    // 16-byte alignment)
+    const LaunchKey key = make_key(g, pl, dev, (((uintptr_t)x % 16) == 0 ? 1 : 0) | (((uintptr_t)y % 16) == 0 ? 2 : 0));
+    LaunchPlan L;
+    bool hit = launch_lookup(key, &L);
+    const void *x_now = pl.pack_x ? (const void *)(wp + pl.xpack_off) : (const void *)x;
+    if (hit && (L.x_map != x_now || L.y_map != y)) {
+        // re-target the cached maps to this call's buffers
+        auto rep = address_replacer();
+        bool ok = rep != nullptr;
+        if (ok && L.tma && L.x_map != x_now) ok = rep(&L.a.tmap_x, const_cast<void *>(x_now)) == CUDA_SUCCESS;
+        if (ok && L.a.y_tma && L.y_map != y) ok = rep(&L.a.tmap_y, y) == CUDA_SUCCESS;
+        hit = ok;
+    }
+    if (hit) {
+        g_launch_hits.fetch_add(1);
+        L.a.x = static_cast<const int8_t *>(x_now);
+        L.a.y = y;
+        L.a.wp = wp;
+        L.a.tail_part = pl.splits > 1 ? reinterpret_cast<int32_t *>(wp + pl.tail_part_off) : nullptr;
+        L.x_map = x_now;
+        L.y_map = y;
+    } else {
+        g_launch_misses.fetch_add(1);
+        conv_status b = build_launch(g, pl, x, y, wp, &L);
+        if (b) return b;
+        launch_insert(key, L);
+    }
+    IgemmArgs &a = L.a;
+    a.bias = g.bias ? bias : nullptr;
+
+    if (pl.pack_x) {
+        int8_t *xp = reinterpret_cast<int8_t *>(wp + pl.xpack_off);
+        const int64_t hw = g.H * g.W;
+        if (L.planes) {
+            const int64_t total = g.N * ((hw + kPackPix - 1) / kPackPix) * ((pl.c16 + kPackCh - 1) / kPackCh);
+            int64_t blocks = total < (int64_t)sms * 8 ? total : (int64_t)sms * 8;
+            igemm_pack_image_planes_kernel<<<(unsigned)blocks, 256, 0, st>>>(x, g.xs[0], g.xs[1], g.N, (int32_t)g.C,
+                                                                             (int32_t)hw, (int32_t)pl.c16, xp);
+        } else {
+            const int64_t total = g.N * g.H * g.W * (pl.c16 / 16);
+            int64_t blocks = (total + 255) / 256;
+            if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
+            igemm_pack_image_kernel<<<(unsigned)blocks, 256, 0, st>>>(x, g.xs[0], g.xs[1], g.xs[2], g.xs[3], g.N,
+                                                                      (int32_t)g.C, (int32_t)g.H, (int32_t)g.W,
+                                                                      (int32_t)pl.c16, xp);
+        }
+        if (cudaGetLastError() != cudaSuccess) return CONV_ERR_CUDA;
+    }
+    const int grid = (int)pl.grid;
+    conv_status rc;
+    switch (L.variant) {
+        case V_TMEM128: rc = launch_conv<128, true, false, true>(a, grid, st); break;
+        case V_RESB256: rc = launch_conv<256, true, true>(a, grid, st); break;
+        case V_TMA256: rc = launch_conv<256, true>(a, grid, st); break;
+        case V_TMA192: rc = launch_conv<192, true>(a, grid, st); break;
+        case V_REG256: rc = launch_conv<256, false>(a, grid, st); break;
+        case V_REG192: rc = launch_conv<192, false>(a, grid, st); break;
+        default: rc = launch_conv<128, false>(a, grid, st); break;
+    }
     if (rc || pl.splits <= 1) return rc;
     const int32_t cut_tiles = a.num_tiles - a.full_units;
     int64_t blocks = (int64_t)cut_tiles * (pl.n_tile / kRedCols) * (MT / kRedRows);

@@ -97,6 +97,11 @@ conv_status igemm_pack_filter_launch(const ConvGeom &g, const IgemmPlan &pl, con
 conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *y,
                               const int32_t *bias, void *workspace, void *stream);
 
+// Launch-plan cache of the tensor-core kernel (tensor maps re-targeted to
+// each call's buffers): empty it; read its hit and miss counts.
+void igemm_cache_clear();
+void igemm_cache_stats(uint64_t *hits, uint64_t *misses);
+
 // ---------------------------------------------------------------- direct
 bool dp4a_supported(const ConvGeom &g);
 conv_status dp4a_launch(const ConvGeom &g, const int8_t *x, const int8_t *w, void *y,

@@ -219,9 +219,10 @@ def test_planner_choices_and_workspace(ic):
     assert ws["c1_tiny_nchw"] == 0 and ws["p4_shape"] == 0
     # C3: 2 n-tiles x 36 k-steps x 16 KB of f16 filter blocks, no image copy
     assert ws["c3_3x3_large"] == 2 * 36 * 16384
-    # C5 has an NCHW image: the channels-last copy is added
+    # C5 (K = 192: one 192-column tile, 14 k-steps of 192 rows x 128 bytes)
+    # has an NCHW image: the channels-last copy is added
     c5 = synth.CONFIGS["c5_7x1_dilated_conv"]
-    assert ws["c5_7x1_dilated_conv"] == 2 * 14 * 16384 + c5.N * c5.H * c5.W * c5.C
+    assert ws["c5_7x1_dilated_conv"] == 14 * 192 * 128 + c5.N * c5.H * c5.W * c5.C
     # forced algorithms are honoured
     xd, wd, yd, p = _descs(ic, synth.CONFIGS["c2_s2_nhwc"])
     for a in (ic.ALGO_DIRECT_GENERIC, ic.ALGO_DIRECT_DP4A, ic.ALGO_IMPLICIT_GEMM,
@@ -429,3 +430,37 @@ def test_dgrad_residue_class_workspace(ic, stride, dil, pre, post, R, S):
             tw = _class_taps(rw, pre[1], stride[1], dil[1], S)
             want += th * tw * 128 * 128  # zero taps: a zero-filled class, no workspace
     assert ic.dgrad_workspace_size(dy, w, dx, p) == want
+
+
+def test_plan_cache_hits_and_shutdown(ic):
+    """Repeated planning of one shape is served from the plan cache (no
+    validation or planning again); conv_shutdown empties it; invalid calls
+    are never cached."""
+    cfg = synth.CONFIGS["c3_3x3_large"]
+    xd, wd, yd, p = _descs(ic, cfg)
+    ic.shutdown()
+    s0 = ic.plan_cache_stats()
+    a1 = ic.plan(xd, wd, yd, p)
+    s1 = ic.plan_cache_stats()
+    assert s1["plan_misses"] == s0["plan_misses"] + 1
+    a2 = ic.plan(xd, wd, yd, p)
+    w2 = ic.workspace_size(xd, wd, yd, p)
+    s2 = ic.plan_cache_stats()
+    assert a1 == a2 and w2 > 0
+    assert s2["plan_hits"] == s1["plan_hits"] + 2 and s2["plan_misses"] == s1["plan_misses"]
+    # another parameter set is another key
+    p2 = ic.Params.make(cfg.pre, cfg.post, (2, 2), cfg.dilation, cfg.mode)
+    xd2, wd2, _, _ = _descs(ic, cfg)
+    yd2 = ic.TensorDesc.packed(ic.CONV_INT32, ic.output_dims(xd2, wd2, p2), cfg.y_layout)
+    ic.plan(xd2, wd2, yd2, p2)
+    assert ic.plan_cache_stats()["plan_misses"] == s2["plan_misses"] + 1
+    # an invalid call (int8 output without the int8 epilogue) is refused every time
+    bad = ic.TensorDesc.packed(ic.CONV_INT8, cfg.y_dims, cfg.y_layout)
+    for _ in range(2):
+        assert ic.validate(xd, wd, bad, p) != 0
+        with pytest.raises(ic.ConvError):
+            ic.plan(xd, wd, bad, p)
+    ic.shutdown()
+    s3 = ic.plan_cache_stats()
+    ic.plan(xd, wd, yd, p)
+    assert ic.plan_cache_stats()["plan_misses"] == s3["plan_misses"] + 1
