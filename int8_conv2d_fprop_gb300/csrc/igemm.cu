@@ -49,6 +49,7 @@
 #include <atomic>
 #include <cstring>
 #include <mutex>
+#include <numeric>
 
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -1164,11 +1165,13 @@ __global__ void __launch_bounds__(256) igemm_split_reduce_kernel(const int32_t *
 }
 
 // ---------------------------------------------------------------- image repack
-// Channels-last copy of an image with arbitrary strides: xp[((n*H+h)*W+w)*c16 + c],
-// channels C..c16-1 zero.  One thread writes 16 channels of one pixel; threads
-// of a warp take neighbouring pixels so that reads along W coalesce for NCHW.
+// Channels-last copy of an image with arbitrary strides: xp[((n*H+h)*W+w)*c16 + c]
+// = x[n, c, row0 + row_step*h, w] for the H copied rows, channels C..c16-1
+// zero.  One thread writes 16 channels of one pixel; threads of a warp take
+// neighbouring pixels so that reads along W coalesce for NCHW.
 __global__ void igemm_pack_image_kernel(const int8_t *x, int64_t xs0, int64_t xs1, int64_t xs2, int64_t xs3,
-                                        int64_t N, int32_t C, int32_t H, int32_t W, int32_t c16, int8_t *xp) {
+                                        int64_t N, int32_t C, int32_t H, int32_t W, int32_t row0, int32_t row_step,
+                                        int32_t c16, int8_t *xp) {
     ptx::launch_dependents();
     const int64_t pixels = N * H * W;
     const int cblocks = c16 / 16;
@@ -1181,7 +1184,7 @@ __global__ void igemm_pack_image_kernel(const int8_t *x, int64_t xs0, int64_t xs
         const int64_t t = pix / W;
         const int h = (int)(t % H);
         const int64_t n = t / H;
-        const int8_t *src = x + n * xs0 + (int64_t)h * xs2 + (int64_t)w * xs3;
+        const int8_t *src = x + n * xs0 + (int64_t)(row0 + (int64_t)row_step * h) * xs2 + (int64_t)w * xs3;
         uint32_t words[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -1220,8 +1223,12 @@ __device__ __forceinline__ void transpose4x4_bytes(uint32_t a, uint32_t b, uint3
     o[3] = __byte_perm(ab_hi, cd_hi, 0x7632);
 }
 
+// HW: pixels per copied image (copied rows x W); copied row h is image row
+// row0 + row_step*h (with row_step > 1, W is a multiple of 16 so that no
+// 16-byte load crosses a row).
 __global__ void __launch_bounds__(256) igemm_pack_image_planes_kernel(const int8_t *x, int64_t xs0, int64_t xs1,
-                                                                      int64_t N, int32_t C, int32_t HW, int32_t c16,
+                                                                      int64_t N, int32_t C, int32_t HW, int32_t W,
+                                                                      int32_t row0, int32_t row_step, int32_t c16,
                                                                       int8_t *xp) {
     ptx::launch_dependents();
     __shared__ __align__(16) uint8_t tile[kPackCh * kPackPitch];
@@ -1237,12 +1244,17 @@ __global__ void __launch_bounds__(256) igemm_pack_image_planes_kernel(const int8
         const int64_t n = t / ptiles;
         const int p0 = pt * kPackPix, c0 = ct * kPackCh;
         const int c = c0 + cl;
-        const int8_t *src = x + n * xs0 + (int64_t)c * xs1 + p0 + seg * 64;
+        const int8_t *plane = x + n * xs0 + (int64_t)c * xs1;
         uint4 v[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int p = p0 + seg * 64 + j * 16;
-            v[j] = (c < C && p < HW) ? __ldg(reinterpret_cast<const uint4 *>(src + j * 16)) : make_uint4(0, 0, 0, 0);
+            const int p = p0 + seg * 64 + j * 16;  // copied pixel: row p / W, column p % W
+            int64_t off = p;
+            if (row_step > 1) {
+                const int h = p / W;
+                off = (int64_t)(row0 + row_step * h) * W + (p - h * W);
+            }
+            v[j] = (c < C && p < HW) ? __ldg(reinterpret_cast<const uint4 *>(plane + off)) : make_uint4(0, 0, 0, 0);
         }
         __syncthreads();  // the previous tile's stores have read the buffer
 #pragma unroll
@@ -1500,7 +1512,25 @@ void igemm_plan(const ConvGeom &g, const void *x_dev, IgemmPlan *pl) {
     // memory and spend the shared memory on image staging instead)
     pl->resident_b =
         pl->n_tile == 256 && pl->n_tiles == 1 && pl->k_steps * pl->n_tile * (int64_t)(KS * 2) <= RESB_MAX_BYTES;
-    pl->xpack_bytes = pl->pack_x ? (size_t)align256(g.N * g.H * g.W * pl->c16) : 0;
+    // the image copy keeps only the rows the windows read: with
+    // g = gcd(stride_h, dilation_h) (stride_h for a one-row filter) every
+    // row read is h = p*stride_h - pre_h + r*dil_h = -pre_h (mod g)
+    pl->row0 = 0;
+    pl->row_step = 1;
+    pl->hp = g.H;
+    if (pl->pack_x) {
+        int64_t gh = g.R > 1 ? std::gcd(g.str_h, g.dil_h) : g.str_h;
+        if (gh > 1) {
+            const int64_t r0 = ((-g.pad_h) % gh + gh) % gh;
+            const int64_t hp = g.H > r0 ? (g.H - r0 + gh - 1) / gh : 0;
+            if (hp >= 1) {
+                pl->row0 = r0;
+                pl->row_step = gh;
+                pl->hp = hp;
+            }
+        }
+    }
+    pl->xpack_bytes = pl->pack_x ? (size_t)align256(g.N * pl->hp * g.W * pl->c16) : 0;
     // One CTA per SM walks the tiles.  With fewer tiles than SMs and long
     // reductions (the weight gradient's shape: few output tiles, a reduction
     // over every pixel of the batch) the tiles are cut along the reduction
@@ -1619,6 +1649,7 @@ LaunchKey make_key(const ConvGeom &g, const IgemmPlan &pl, int dev, int align) {
     put(pl.k_steps); put(pl.n_tiles); put(pl.m_tiles); put((int64_t)pl.wpack_bytes); put((int64_t)pl.xpack_bytes);
     put(pl.full_units); put(pl.splits); put(pl.num_units); put(pl.grid); put((int64_t)pl.tail_part_off);
     put((int64_t)pl.tail_part_bytes); put((int64_t)pl.xpack_off); put((int64_t)pl.workspace_bytes);
+    put(pl.row0); put(pl.row_step); put(pl.hp);
     put(dev); put(align);
     k.n = n;
     return k;
@@ -1663,16 +1694,35 @@ void launch_insert(const LaunchKey &k, const LaunchPlan &p) {
     victim->valid = true;
 }
 
+// The geometry the kernel sees: the call's, or, for an image copy that
+// keeps every row_step-th row from row0, the same convolution over the copy
+// (h = row0 + row_step*h', so stride, dilation and pre-padding along H are
+// divided by row_step: pre' = (pre + row0) / row_step, exact).
+ConvGeom kernel_geom(const ConvGeom &g, const IgemmPlan &pl) {
+    ConvGeom k = g;
+    if (pl.pack_x && pl.row_step > 1) {
+        k.H = pl.hp;
+        k.str_h = g.str_h / pl.row_step;
+        k.dil_h = g.R > 1 ? g.dil_h / pl.row_step : g.dil_h;
+        k.pad_h = (g.pad_h + pl.row0) / pl.row_step;
+    }
+    return k;
+}
+
 // Builds the launch plan of a call (kernel arguments, tensor maps, variant).
-conv_status build_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *y, uint8_t *wp,
+conv_status build_launch(const ConvGeom &g0, const IgemmPlan &pl, const int8_t *x, void *y, uint8_t *wp,
                          LaunchPlan *L) {
+    const ConvGeom g = kernel_geom(g0, pl);
     IgemmArgs &a = L->a;
     std::memset(&a, 0, sizeof(a));
     L->planes = false;
     if (pl.pack_x) {
-        const int64_t hw = g.H * g.W;
-        L->planes = (g.W == 1 || g.xs[3] == 1) && (g.H == 1 || g.xs[2] == g.W) && g.xs[1] % 16 == 0 &&
-                    g.xs[0] % 16 == 0 && hw % 16 == 0 && ((uintptr_t)x % 16) == 0 && hw < ((int64_t)1 << 31);
+        // plane copy: each channel's rows contiguous, whole 16-byte loads
+        // inside a row when rows are skipped
+        const int64_t hw = g0.H * g0.W;
+        L->planes = (g0.W == 1 || g0.xs[3] == 1) && (g0.H == 1 || g0.xs[2] == g0.W) && g0.xs[1] % 16 == 0 &&
+                    g0.xs[0] % 16 == 0 && hw % 16 == 0 && ((uintptr_t)x % 16) == 0 && hw < ((int64_t)1 << 31) &&
+                    (pl.row_step == 1 || g0.W % 16 == 0);
         a.x = reinterpret_cast<int8_t *>(wp + pl.xpack_off);
         a.xs_n = g.H * g.W * pl.c16;
         a.xs_h = g.W * pl.c16;
@@ -1807,18 +1857,20 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
 
     if (pl.pack_x) {
         int8_t *xp = reinterpret_cast<int8_t *>(wp + pl.xpack_off);
-        const int64_t hw = g.H * g.W;
+        const int64_t hwp = pl.hp * g.W;  // pixels of each copied image
         if (L.planes) {
-            const int64_t total = g.N * ((hw + kPackPix - 1) / kPackPix) * ((pl.c16 + kPackCh - 1) / kPackCh);
+            const int64_t total = g.N * ((hwp + kPackPix - 1) / kPackPix) * ((pl.c16 + kPackCh - 1) / kPackCh);
             int64_t blocks = total < (int64_t)sms * 8 ? total : (int64_t)sms * 8;
-            igemm_pack_image_planes_kernel<<<(unsigned)blocks, 256, 0, st>>>(x, g.xs[0], g.xs[1], g.N, (int32_t)g.C,
-                                                                             (int32_t)hw, (int32_t)pl.c16, xp);
+            igemm_pack_image_planes_kernel<<<(unsigned)blocks, 256, 0, st>>>(
+                x, g.xs[0], g.xs[1], g.N, (int32_t)g.C, (int32_t)hwp, (int32_t)g.W, (int32_t)pl.row0,
+                (int32_t)pl.row_step, (int32_t)pl.c16, xp);
         } else {
-            const int64_t total = g.N * g.H * g.W * (pl.c16 / 16);
+            const int64_t total = g.N * pl.hp * g.W * (pl.c16 / 16);
             int64_t blocks = (total + 255) / 256;
             if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
             igemm_pack_image_kernel<<<(unsigned)blocks, 256, 0, st>>>(x, g.xs[0], g.xs[1], g.xs[2], g.xs[3], g.N,
-                                                                      (int32_t)g.C, (int32_t)g.H, (int32_t)g.W,
+                                                                      (int32_t)g.C, (int32_t)pl.hp, (int32_t)g.W,
+                                                                      (int32_t)pl.row0, (int32_t)pl.row_step,
                                                                       (int32_t)pl.c16, xp);
         }
         if (cudaGetLastError() != cudaSuccess) return CONV_ERR_CUDA;

@@ -77,6 +77,11 @@ struct IgemmPlan {
     int64_t m_tiles;        // ceil(N*P*Q / kIgemmMTile)
     size_t wpack_bytes;     // repacked filter
     size_t xpack_bytes;     // channels-last image copy (0 if not needed)
+    // Rows of the image copy: when the stride and the dilation along H share
+    // a factor g, only the rows h = row0 (mod g) are ever read, and the copy
+    // holds those (hp of them); the convolution then runs on it with stride,
+    // dilation and pre-padding divided by g (row_step = g; 1: every row).
+    int64_t row0, row_step, hp;
     // Work split: with few tiles and long reductions each tile, and with a
     // short partial last round of tiles each tile of that round, is cut into
     // `splits` runs of k-steps computed by different CTAs (splits == 1: whole

@@ -105,6 +105,16 @@ def _shape_cases():
           y_layout="NCHW", seed=17),
         # 129..192 output channels: 192-column tiles, ragged K
         C("k150_nt192", 2, 96, 9, 11, 150, 3, 3, stride=(1, 2), pre=(1, 1), post=(1, 0), bias=True, seed=18),
+        # NCHW images whose H stride and dilation share a factor: the
+        # channels-last copy keeps only the rows the windows read (odd rows
+        # here: pre-padding 1; W = 13 takes the generic copy)
+        C("rows_odd_generic", 2, 40, 21, 13, 72, 3, 3, stride=(2, 1), dilation=(2, 1), pre=(1, 1), post=(2, 1),
+          x_layout="NCHW", w_layout="KCRS", seed=19),
+        # every third row from row 1 (gcd 3), plane copy (W = 32), convolution mode
+        C("rows_gcd3_planes", 2, 32, 30, 32, 64, 5, 3, stride=(3, 1), dilation=(3, 2), pre=(2, 1), post=(3, 1),
+          mode=1, x_layout="NCHW", w_layout="KCRS", y_layout="NCHW", seed=20),
+        # a 1x1 filter at stride 2: every other row
+        C("rows_1x1_s2", 2, 48, 15, 16, 40, 1, 1, stride=(2, 2), x_layout="NCHW", w_layout="KCRS", seed=21),
     ]
 
 

@@ -220,9 +220,10 @@ def test_planner_choices_and_workspace(ic):
     # C3: 2 n-tiles x 36 k-steps x 16 KB of f16 filter blocks, no image copy
     assert ws["c3_3x3_large"] == 2 * 36 * 16384
     # C5 (K = 192: one 192-column tile, 14 k-steps of 192 rows x 128 bytes)
-    # has an NCHW image: the channels-last copy is added
+    # has an NCHW image: a channels-last copy is added, of the even rows only
+    # (stride 2 and dilation 2 along H, pre-padding 6: every row read is even)
     c5 = synth.CONFIGS["c5_7x1_dilated_conv"]
-    assert ws["c5_7x1_dilated_conv"] == 14 * 192 * 128 + c5.N * c5.H * c5.W * c5.C
+    assert ws["c5_7x1_dilated_conv"] == 14 * 192 * 128 + c5.N * (c5.H // 2) * c5.W * c5.C
     # forced algorithms are honoured
     xd, wd, yd, p = _descs(ic, synth.CONFIGS["c2_s2_nhwc"])
     for a in (ic.ALGO_DIRECT_GENERIC, ic.ALGO_DIRECT_DP4A, ic.ALGO_IMPLICIT_GEMM,
