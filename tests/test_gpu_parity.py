@@ -115,6 +115,10 @@ def _shape_cases():
           mode=1, x_layout="NCHW", w_layout="KCRS", y_layout="NCHW", seed=20),
         # a 1x1 filter at stride 2: every other row
         C("rows_1x1_s2", 2, 48, 15, 16, 40, 1, 1, stride=(2, 2), x_layout="NCHW", w_layout="KCRS", seed=21),
+        # pointwise over dense channels-last rows (2-D pixel-row boxes): 80
+        # channels (the second k-step's box runs past a pixel's channels), a
+        # partial last tile of 61 pixels
+        C("pointwise_c80_ragged", 3, 80, 7, 9, 100, 1, 1, bias=True, relu=True, seed=22),
     ]
 
 
