@@ -28,11 +28,13 @@
  * Ownership: the caller owns every buffer and the stream.  conv_fprop never
  * allocates and never synchronises; all work is queued on `stream`.  The
  * library keeps one small device status word per device (see
- * conv_device_status) and nothing else between calls.
+ * conv_device_status) and, in static host memory, the plan caches described
+ * at conv_shutdown.
  *
  * Errors: every entry point returns a conv_status; nothing is thrown across
- * the ABI.  Descriptors are validated on every call before anything is
- * launched.  Kernel launch failures give CONV_ERR_CUDA.  A kernel whose
+ * the ABI.  Descriptors are validated before anything is launched (a call
+ * whose descriptors and parameters equal those of an earlier, validated call
+ * reuses that validation from the plan cache).  Kernel launch failures give CONV_ERR_CUDA.  A kernel whose
  * internal wait runs out of time records CONV_ERR_DEVICE_TIMEOUT in the
  * device status word and returns early; conv_device_status reports it.
  *
