@@ -16,19 +16,29 @@
 // registers.  The result is bit-identical to integer arithmetic.
 //
 // Persistent, warp-specialised CTA (one per SM), 512 threads, tile 128 pixels
-// x NT output channels (NT = 128, 192 or 256).  Two ways to stage the image tile:
-//  * TMA (default): warp 5 lane 0 issues one TMA im2col load per k-step (128
-//    output pixels x 64 channels of one tap, zero outside the image) into a
-//    6-deep (NT = 256) or 8-deep (NT = 128) int8 staging ring; warpgroup 0
-//    converts each staged tile to f16 into the 128-byte-swizzled A stage;
-//    warp 6 lane 0 brings the matching pre-swizzled f16 filter block with
-//    one bulk async copy.
-//  * global loads (fallback when an im2col map cannot express the call):
-//    warpgroup 0 threads each own one pixel row, gather 64 channels of one tap
-//    with 16-byte loads one item ahead (address formed from stride, padding
-//    and dilation), convert in registers and write the row; thread 0 also
-//    issues the filter block copies.
-// In both, warp 4 allocates tensor memory and its lane 0 issues tcgen05.mma
+// x NT output channels (NT = 128 for K <= 128, 192 for K <= 192, else 256).
+// The image tile of a k-step is 128 output pixels x 64 channels of one tap.
+// Kernel variants, chosen per call:
+//  * NT = 256 and NT = 192 (TMA): warp 5 lane 0 issues one TMA load per
+//    k-step (an im2col box: window origins from the pixel order, the tap as
+//    pixel offset, zeros outside the image; or, for an unpadded 1x1
+//    stride-1 filter, a plain 2-D box of 128 pixel rows) into an int8
+//    staging ring; warpgroup 0 converts each staged tile to f16 into the
+//    128-byte-swizzled A stage in shared memory; warp 6 lane 0 brings the
+//    matching pre-swizzled f16 filter block with one bulk async copy (or,
+//    when the whole repacked filter fits in 128 KB, once per CTA: the
+//    resident-filter variant).
+//  * NT = 128 (TMA): the same loads, issued by two warps (5 and 7) that own
+//    alternate staging slots; the converters write the f16 image tile into
+//    tensor memory (tcgen05.st) and the MMA reads A from there (the
+//    tensor-memory-A form), which leaves shared memory to a 12-deep staging
+//    ring; the epilogue stores 32 columns per TMA store.
+//  * global loads (fallback when a TMA map cannot express the call):
+//    warpgroup 0 threads each own one pixel row, gather 64 channels of one
+//    tap with 16-byte loads one item ahead (address formed from stride,
+//    padding and dilation), convert in registers and write the row; thread 0
+//    also issues the filter block copies.
+// In all, warp 4 allocates tensor memory and its lane 0 issues tcgen05.mma
 // (M=128, N=NT, K=16 per instruction) into one of two accumulator slots:
 //   warpgroups 2-3  epilogue, two warps per tensor-memory lane quadrant, each
 //                owning NT/2 columns: tcgen05.ld each finished slot,
@@ -37,10 +47,16 @@
 // Work comes in units: whole tiles round by round, or runs of k-steps of cut
 // tiles (few tiles with long reductions; a short partial last round) whose
 // int32 sums igemm_split_reduce_kernel adds.
+// Images that are not channels-last with 16-byte channel runs are copied to
+// channels-last first (igemm_pack_image_planes_kernel for NCHW planes,
+// igemm_pack_image_kernel for any strides), keeping only the rows that
+// the windows read when stride and dilation skip rows.
 // Registers are moved from warpgroups 0-1 to the epilogue with setmaxnreg.
 // Every wait is bounded in time; on expiry the CTA records
 // CONV_ERR_DEVICE_TIMEOUT, stops, lets issued copies and MMAs finish and frees
 // its tensor memory.
+// Launch plans (tensor maps, grid, variant) are cached per call shape; a
+// repeated call only re-targets the maps' addresses.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -109,21 +125,24 @@ constexpr int RESB_MAX_BYTES = 128 * 1024;
 // kResB: the filter blocks of all k-steps stay resident (loaded once per
 // CTA); the ring then holds image tiles only, and each epilogue warp stages
 // its stores in one buffer instead of two.
-// kTmemA (128-column tiles, TMA path): the f16 image tile of a k-step goes
-// to tensor memory (columns 256.. next to the two 128-column accumulator
-// slots, 32 columns per stage) and the MMA reads it from there; the shared
-// memory that held it becomes int8 staging buffers, i.e. image bytes in
-// flight (10 with a resident filter, 16 without).
+// kTmemA (128- and 192-column tiles, TMA path): the f16 image tile of a
+// k-step goes to tensor memory (columns 2*NT.. next to the two accumulator
+// slots, 32 columns per stage: 256..383 or 384..511) and the MMA reads it
+// from there; the shared memory that held it becomes int8 staging buffers,
+// i.e. image bytes in flight (12; 10 with a resident filter).
 template <int NT, bool kTma, bool kResB = false, bool kTmemA = false>
 struct TileCfg {
     static constexpr int B_BYTES = NT * KS * 2;
-    // (192-column tiles: 40 KB stages, four of them behind four staging buffers)
+    // (192-column tiles without kTmemA: 40 KB stages, four of them behind
+    // four staging buffers)
     static constexpr int ST = kTmemA ? 4 : (kResB ? 2 : (kTma ? (NT == 256 ? IGEMM_ST_256 : (NT == 192 ? 4 : IGEMM_ST_128))
                                                                 : (NT == 128 ? 6 : 4)));
     static constexpr int STG_STAGES = kTmemA ? (kResB ? 10 : 12)
                                              : (kResB ? 6 : (kTma ? (NT == 256 ? IGEMM_STG_256 : (NT == 192 ? 4 : IGEMM_STG_128)) : 0));
     static constexpr int EPI_BUFS = kResB ? 1 : 2;  // output staging buffers per epilogue warp
-    static constexpr int EPI_COLS = kTmemA ? 32 : 16;
+    // output columns per staged store: 32 for the 128-column tensor-memory
+    // variant (its shared memory has room for 4 KB buffers), else 16
+    static constexpr int EPI_COLS = (kTmemA && NT == 128) ? 32 : 16;
     static constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 4;  // 2 or 4 KB
     static constexpr int EPI_BYTES = 8 * EPI_BUFS * EPI_BUF_BYTES;
     static constexpr int A_SMEM = kTmemA ? 0 : ST * A_BYTES;
@@ -142,7 +161,7 @@ struct TileCfg {
     static constexpr int SMEM_BYTES = 1024 /*align slack*/ + A_SMEM + B_AREA + STG_STAGES * STG_BYTES +
                                       EPI_BYTES + 512 /*barriers*/;
     static_assert(!kResB || kTma, "the resident filter needs the TMA producers");
-    static_assert(!kTmemA || (kTma && NT == 128 && TMEM_A_COL + ST * 32 <= 512), "image stages in tensor memory");
+    static_assert(!kTmemA || (kTma && NT <= 192 && TMEM_A_COL + ST * 32 <= 512), "image stages in tensor memory");
     static_assert(TMEM_COLS <= 512, "tensor memory has 512 columns");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     static_assert(ST <= 8 && STG_STAGES <= 16, "the control block has 8 ring and 16 staging barriers");
@@ -1508,8 +1527,8 @@ void igemm_plan(const ConvGeom &g, const void *x_dev, IgemmPlan *pl) {
     pl->wpack_bytes = (size_t)align256(pl->n_tiles * pl->k_steps * pl->n_tile * (int64_t)(KS * 2));
     // one tile of output channels whose filter blocks fit in shared memory:
     // the filter stays resident in every CTA (taken with the TMA producers)
-    // (256-column tiles: the 128-column ones put their image tile in tensor
-    // memory and spend the shared memory on image staging instead)
+    // (256-column tiles: the 128- and 192-column ones put their image tile
+    // in tensor memory and spend the shared memory on image staging instead)
     pl->resident_b =
         pl->n_tile == 256 && pl->n_tiles == 1 && pl->k_steps * pl->n_tile * (int64_t)(KS * 2) <= RESB_MAX_BYTES;
     // the image copy keeps only the rows the windows read: with
@@ -1612,7 +1631,7 @@ PFN_cuTensorMapReplaceAddress_v12000 address_replacer() {
     return reinterpret_cast<PFN_cuTensorMapReplaceAddress_v12000>(fn.load());
 }
 
-enum Variant { V_REG128, V_REG192, V_REG256, V_TMEM128, V_TMA192, V_TMA256, V_RESB256 };
+enum Variant { V_REG128, V_REG192, V_REG256, V_TMEM128, V_TMEM192, V_TMA256, V_RESB256 };
 
 // Everything a launch of the convolution kernel needs that does not change
 // with the buffers' addresses: the kernel arguments (tensor maps encoded for
@@ -1768,9 +1787,9 @@ conv_status build_launch(const ConvGeom &g0, const IgemmPlan &pl, const int8_t *
                 g.P == g.H && g.Q == g.W && a.xs_h == g.W * a.xs_w && a.xs_n == g.H * a.xs_h)
                    ? 1
                    : 0;
-    // 128-column tiles keep the f16 image tile in tensor memory; their
-    // staging loads are 64-byte swizzled for the converters' row reads
-    const bool tmem_a = pl.n_tile == 128;
+    // 128- and 192-column tiles keep the f16 image tile in tensor memory;
+    // their staging loads are 64-byte swizzled for the converters' row reads
+    const bool tmem_a = pl.n_tile <= 192;
     bool tma = false;
     if (!pl.register_loads) {
         if (a.a_rows) tma = encode_rows_map(g, a.x, a.xs_w, c_dim, tmem_a, &a.tmap_x);
@@ -1779,22 +1798,22 @@ conv_status build_launch(const ConvGeom &g0, const IgemmPlan &pl, const int8_t *
             tma = encode_im2col_map(g, a.x, a.xs_n, a.xs_h, a.xs_w, c_dim, tmem_a, &a.tmap_x);
         }
     }
-    // the tensor-memory variant stages 32 output columns per store
-    const bool wide_out = tma && tmem_a;
+    // the 128-column tensor-memory variant stages 32 output columns per store
+    const bool wide_out = tma && pl.n_tile == 128;
     a.y_tma = encode_output_map(g, y, wide_out, &a.tmap_y) ? 1 : (encode_output_map_nchw(g, y, wide_out, &a.tmap_y) ? 2 : 0);
     // int8 outputs are staged 64 columns at a time: a 192-column tile (96
     // per epilogue warp) stores them with plain stores
     if (g.out_int8 && pl.n_tile == 192) a.y_tma = 0;
-    // TMA path: 128-column tiles keep the image tile in tensor memory;
-    // 256-column tiles keep it in shared memory, with the filter resident
-    // when it fits
+    // TMA path: 128- and 192-column tiles keep the image tile in tensor
+    // memory; 256-column tiles keep it in shared memory, with the filter
+    // resident when it fits
     L->tma = tma;
     if (tma && tmem_a)
-        L->variant = V_TMEM128;
+        L->variant = pl.n_tile == 128 ? V_TMEM128 : V_TMEM192;
     else if (tma && pl.resident_b)
         L->variant = V_RESB256;
     else if (tma)
-        L->variant = pl.n_tile == 256 ? V_TMA256 : V_TMA192;
+        L->variant = V_TMA256;
     else
         L->variant = pl.n_tile == 256 ? V_REG256 : (pl.n_tile == 192 ? V_REG192 : V_REG128);
     L->x_map = a.x;
@@ -1881,7 +1900,7 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
         case V_TMEM128: rc = launch_conv<128, true, false, true>(a, grid, st); break;
         case V_RESB256: rc = launch_conv<256, true, true>(a, grid, st); break;
         case V_TMA256: rc = launch_conv<256, true>(a, grid, st); break;
-        case V_TMA192: rc = launch_conv<192, true>(a, grid, st); break;
+        case V_TMEM192: rc = launch_conv<192, true, false, true>(a, grid, st); break;
         case V_REG256: rc = launch_conv<256, false>(a, grid, st); break;
         case V_REG192: rc = launch_conv<192, false>(a, grid, st); break;
         default: rc = launch_conv<128, false>(a, grid, st); break;

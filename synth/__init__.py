@@ -1,8 +1,10 @@
 """Seeded synthetic inputs and workload shapes.
 
-This module is shared by the oracle, the tests, the CUDA path's binding and
-``bench.py``.  It holds no convolution arithmetic: it only draws integers and
-describes shapes and memory layouts.
+This module feeds the same inputs to both sides of every parity check: the
+tests and ``bench.py`` call it, and hand its arrays to the oracle and (as
+device buffers) to the library.  Neither the library nor its binding imports
+it.  It holds no convolution arithmetic: it only draws integers and describes
+shapes and memory layouts.
 
 Random numbers come from splitmix64 (Steele, Lea and Flood, "Fast Splittable
 Pseudorandom Number Generators", OOPSLA 2014), used as a counter-based
