@@ -452,6 +452,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
             ptx::mbar_init(ptx::smem_addr(&ctl->stg_empty[i]), 128);
         }
         if (kTma) ptx::prefetch_tensormap(&a.tmap_x);
+        if (a.y_tma) ptx::prefetch_tensormap(&a.tmap_y);
         for (int i = 0; i < NSLOT; ++i) {
             ptx::mbar_init(ptx::smem_addr(&ctl->acc_full[i]), 1);
             ptx::mbar_init(ptx::smem_addr(&ctl->acc_empty[i]), NUM_EPI_THREADS);
@@ -818,6 +819,20 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 const int q = rem - p * a.Q;
                 yoff = (int64_t)n * a.ys_n + (int64_t)p * a.ys_p + (int64_t)q * a.ys_q;
             }
+            // bias[k] (int32) for this warp's HALF columns: each lane loads
+            // HALF/32 of them, and the warp passes them round with shuffles
+            // when it adds them.  Loaded before the accumulators are waited
+            // for, so that the load's latency hides behind the tile's
+            // main loop instead of lengthening the epilogue.
+            int32_t bv[HALF / 32];
+            if (a.bias && wu.split < 0) {
+                const int kb = nt * NT + col0;
+#pragma unroll
+                for (int j = 0; j < HALF / 32; ++j) {
+                    const int k = kb + j * 32 + lane;
+                    bv[j] = k < a.K ? __ldg(a.bias + k) : 0;
+                }
+            }
             int32_t acc[HALF];
 #pragma unroll
             for (int i = 0; i < HALF; ++i) acc[i] = 0;
@@ -869,17 +884,8 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 continue;
             }
             // epilogue arithmetic, once: + bias[k] (int32 wrap-around), then
-            // ReLU.  All lanes of the warp hold the same HALF columns: each
-            // lane loads HALF/32 of the bias values and the warp passes them
-            // round with shuffles (one load per lane instead of HALF).
+            // ReLU.  All lanes of the warp hold the same HALF columns.
             if (a.bias) {
-                const int kb = nt * NT + col0;
-                int32_t bv[HALF / 32];
-#pragma unroll
-                for (int j = 0; j < HALF / 32; ++j) {
-                    const int k = kb + j * 32 + lane;
-                    bv[j] = k < a.K ? __ldg(a.bias + k) : 0;
-                }
 #pragma unroll
                 for (int i = 0; i < HALF; ++i)
                     acc[i] = (int32_t)((uint32_t)acc[i] + (uint32_t)__shfl_sync(0xffffffffu, bv[i / 32], i % 32));
