@@ -802,7 +802,6 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
         const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)col0;
         uint32_t gi = 0;
         bool ok = true;
-        const int wpos = warp - FIRST_EPI_WARP;  // this warp's part of the tile (0..7)
         for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
             const Unit wu = unit_at(u, a.full_units, a.splits, a.k_steps);
             const int ng = groups_of(wu.ke - wu.kb);
