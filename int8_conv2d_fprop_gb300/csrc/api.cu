@@ -73,27 +73,7 @@ uint64_t wait_limit_ns() {
     return v;
 }
 
-namespace {
-
-int choose_algo(const ConvGeom &g, int requested) {
-    if (requested != CONV_ALGO_AUTO) return requested;
-    if (g.C >= 16 && igemm_supported(g)) return CONV_ALGO_IMPLICIT_GEMM;
-    if (dp4a_supported(g)) return CONV_ALGO_DIRECT_DP4A;
-    if (igemm_supported(g)) return CONV_ALGO_IMPLICIT_GEMM;
-    return CONV_ALGO_DIRECT_GENERIC;
-}
-
-// Plan cache: the validated geometry, algorithm and tensor-core plan of a
-// call, keyed by its descriptors, parameters, device and whether the image
-// pointer is 16-byte aligned (the only thing the plan reads of a pointer).
-// Repeated calls with the same shapes skip validation and planning.  Least
-// recently used entries give way; conv_shutdown empties it.
-struct PlanKey {
-    int64_t v[64];
-    int n;
-};
-
-void put_desc(PlanKey &k, const conv_tensor_desc *d) {
+static void put_desc(PlanKey &k, const conv_tensor_desc *d) {
     k.v[k.n++] = d->dtype;
     k.v[k.n++] = d->rank;
     for (int i = 0; i < 4; ++i) k.v[k.n++] = d->dims[i];
@@ -124,6 +104,22 @@ PlanKey make_plan_key(const conv_tensor_desc *x, const conv_tensor_desc *w, cons
     return k;
 }
 
+
+namespace {
+
+int choose_algo(const ConvGeom &g, int requested) {
+    if (requested != CONV_ALGO_AUTO) return requested;
+    if (g.C >= 16 && igemm_supported(g)) return CONV_ALGO_IMPLICIT_GEMM;
+    if (dp4a_supported(g)) return CONV_ALGO_DIRECT_DP4A;
+    if (igemm_supported(g)) return CONV_ALGO_IMPLICIT_GEMM;
+    return CONV_ALGO_DIRECT_GENERIC;
+}
+
+// Plan cache: the validated geometry, algorithm and tensor-core plan of a
+// call, keyed by its descriptors, parameters, device and whether the image
+// pointer is 16-byte aligned (the only thing the plan reads of a pointer).
+// Repeated calls with the same shapes skip validation and planning.  Least
+// recently used entries give way; conv_shutdown empties it.
 constexpr int kPlanCacheSize = 64;
 struct PlanCacheEntry {
     PlanKey key;
@@ -393,6 +389,7 @@ void conv_shutdown(void) {
         for (auto &e : g_plan_cache) e.valid = false;
     }
     igemm_cache_clear();
+    dgrad_cache_clear();
 }
 
 conv_status conv_plan_cache_stats(uint64_t *plan_hits, uint64_t *plan_misses, uint64_t *launch_hits,

@@ -33,6 +33,7 @@
 //    by the validator's bound, added across the warp with shuffles).
 #include <cuda_runtime.h>
 
+#include <cstring>
 #include <mutex>
 #include <numeric>
 #include <vector>
@@ -173,20 +174,39 @@ struct DgradPhase {
 };
 
 // Streams the residue classes of one dgrad call run on side by side, forked
-// from the caller's stream and joined back to it; created on first use, one
-// set per device, kept for the life of the process.
+// from the caller's stream and joined back to it, with the events that fork
+// and join them; created on first use, one set per device, kept for the life
+// of the process.  One call at a time uses a set (its mutex), so that two
+// host threads never record the same event between the other's record and
+// wait.
 constexpr int kSideStreams = 4;
 constexpr int kSideDevices = 64;
 
-cudaStream_t side_stream(int i) {
+struct SideSet {
+    std::mutex mu;
+    cudaStream_t streams[kSideStreams] = {};
+    cudaEvent_t fork = nullptr;
+    cudaEvent_t join[kSideStreams] = {};
+    bool ready = false;
+};
+
+SideSet *side_set() {
     static std::mutex mu;
-    static cudaStream_t streams[kSideDevices][kSideStreams] = {};
+    static SideSet sets[kSideDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kSideDevices) return nullptr;
     std::lock_guard<std::mutex> lock(mu);
-    if (!streams[dev][i] && cudaStreamCreateWithFlags(&streams[dev][i], cudaStreamNonBlocking) != cudaSuccess)
-        streams[dev][i] = nullptr;
-    return streams[dev][i];
+    SideSet &ss = sets[dev];
+    if (!ss.ready) {
+        bool ok = ss.fork || cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) == cudaSuccess;
+        for (int i = 0; i < kSideStreams && ok; ++i) {
+            ok = ss.streams[i] || cudaStreamCreateWithFlags(&ss.streams[i], cudaStreamNonBlocking) == cudaSuccess;
+            ok = ok && (ss.join[i] || cudaEventCreateWithFlags(&ss.join[i], cudaEventDisableTiming) == cudaSuccess);
+        }
+        if (!ok) return nullptr;  // what was created stays for the next try
+        ss.ready = true;
+    }
+    return &ss;
 }
 
 // The taps of one axis that reach residue rho: r = r0 + t*delta, t < T.
@@ -343,7 +363,70 @@ conv_status plan_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const c
     return CONV_OK;
 }
 
+// Plans of recent dgrad calls (residue classes with their plans), keyed like
+// forward plans on the descriptors, parameters, device and dY alignment; the
+// least recently used give way; conv_shutdown empties it.
+constexpr int kDgradCacheSize = 16;
+struct DgradCacheEntry {
+    PlanKey key;
+    std::vector<DgradPhase> ph;
+    bool tensor;
+    size_t ws;
+    uint64_t used;
+    bool valid;
+};
+std::mutex g_dgrad_mu;
+DgradCacheEntry g_dgrad_cache[kDgradCacheSize];
+uint64_t g_dgrad_clock = 0;
+
+conv_status plan_dgrad_cached(const conv_tensor_desc *dy, const int8_t *dy_dev, const conv_tensor_desc *w,
+                              const conv_tensor_desc *dx, const conv_fprop_params *p, std::vector<DgradPhase> *ph,
+                              bool *tensor, size_t *ws_bytes) {
+    if (!dy || !w || !dx || !p) return CONV_ERR_NULL_PTR;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const PlanKey key = make_plan_key(dy, w, dx, p, dy_dev, dev);
+    {
+        std::lock_guard<std::mutex> lock(g_dgrad_mu);
+        for (auto &e : g_dgrad_cache)
+            if (e.valid && e.key.n == key.n && std::memcmp(e.key.v, key.v, sizeof(int64_t) * key.n) == 0) {
+                e.used = ++g_dgrad_clock;
+                *ph = e.ph;
+                *tensor = e.tensor;
+                *ws_bytes = e.ws;
+                return CONV_OK;
+            }
+    }
+    conv_status st = plan_dgrad(dy, dy_dev, w, dx, p, ph, tensor, ws_bytes);
+    if (st) return st;  // only valid plans are kept
+    std::lock_guard<std::mutex> lock(g_dgrad_mu);
+    DgradCacheEntry *victim = &g_dgrad_cache[0];
+    for (auto &e : g_dgrad_cache) {
+        if (!e.valid) {
+            victim = &e;
+            break;
+        }
+        if (e.used < victim->used) victim = &e;
+    }
+    victim->key = key;
+    victim->ph = *ph;
+    victim->tensor = *tensor;
+    victim->ws = *ws_bytes;
+    victim->used = ++g_dgrad_clock;
+    victim->valid = true;
+    return CONV_OK;
+}
+
 }  // namespace
+
+void dgrad_cache_clear() {
+    std::lock_guard<std::mutex> lock(g_dgrad_mu);
+    for (auto &e : g_dgrad_cache) {
+        e.valid = false;
+        e.ph.clear();
+    }
+}
+
 }  // namespace i8c
 
 using namespace i8c;
@@ -356,7 +439,7 @@ conv_status conv_dgrad_workspace_size(const conv_tensor_desc *dy, const conv_ten
     std::vector<DgradPhase> ph;
     bool tensor = false;
     size_t ws = 0;
-    conv_status st = plan_dgrad(dy, nullptr, w, dx, p, &ph, &tensor, &ws);
+    conv_status st = plan_dgrad_cached(dy, nullptr, w, dx, p, &ph, &tensor, &ws);
     if (st) return st;
     *bytes = ws;
     return CONV_OK;
@@ -368,7 +451,7 @@ conv_status conv_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const c
     std::vector<DgradPhase> ph;
     bool tensor = false;
     size_t ws = 0;
-    conv_status st = plan_dgrad(dy, dy_dev, w, dx, p, &ph, &tensor, &ws);
+    conv_status st = plan_dgrad_cached(dy, dy_dev, w, dx, p, &ph, &tensor, &ws);
     if (st) return st;
     if (dx->dims[0] == 0) return CONV_OK;
     if (!dy_dev || !w_dev || !dx_dev) return CONV_ERR_NULL_PTR;
@@ -386,11 +469,13 @@ conv_status conv_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const c
                 overlaps(workspace, ws, w_dev, (uint64_t)desc_extent_elems(w)))
                 return CONV_ERR_OVERLAP;
         }
-        // one class: on the caller's stream.  Several: each on a side
-        // stream forked from the caller's (an event), repacking its taps into
-        // its own part of the workspace and writing its own dX pixels, then
-        // joined back (an event per side stream)
-        auto run_class = [&](const DgradPhase &c, cudaStream_t cs) -> conv_status {
+        // one class: on the caller's stream.  Several: the filters of all
+        // classes are repacked on the caller's stream (one launch per
+        // kMaxPackJobs classes, each into its own part of the workspace),
+        // then each class runs on a side stream forked from the caller's (an
+        // event), writing its own dX pixels, and the side streams are joined
+        // back (an event each)
+        auto run_class = [&](const DgradPhase &c, cudaStream_t cs, bool packed) -> conv_status {
             int32_t *y = dx_dev + c.y_origin;
             if (!c.taps) {
                 const ConvGeom &g = c.g;
@@ -399,35 +484,45 @@ conv_status conv_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const c
                 return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
             }
             void *cw = static_cast<uint8_t *>(workspace) + c.ws_off;
-            conv_status r = igemm_pack_filter_launch(c.g, c.pl, w_dev + c.w_origin, cw, cs);
+            conv_status r = packed ? CONV_OK : igemm_pack_filter_launch(c.g, c.pl, w_dev + c.w_origin, cw, cs);
             if (r == CONV_OK) r = igemm_main_launch(c.g, c.pl, dy_dev, y, nullptr, cw, cs);
             return r;
         };
         if (ph.empty()) return CONV_OK;
-        if (ph.size() == 1) return run_class(ph[0], s);
+        if (ph.size() == 1) return run_class(ph[0], s, false);
+        SideSet *ss = side_set();
+        if (!ss) return CONV_ERR_CUDA;
+        std::lock_guard<std::mutex> lock(ss->mu);
+        {
+            const ConvGeom *gs[kMaxPackJobs];
+            const IgemmPlan *ps[kMaxPackJobs];
+            const int8_t *ws_[kMaxPackJobs];
+            void *wk[kMaxPackJobs];
+            int n = 0;
+            for (size_t i = 0; i <= ph.size(); ++i) {
+                if (n == kMaxPackJobs || (i == ph.size() && n > 0)) {
+                    if ((st = igemm_pack_filter_group_launch(n, gs, ps, ws_, wk, s))) return st;
+                    n = 0;
+                }
+                if (i == ph.size() || !ph[i].taps) continue;
+                gs[n] = &ph[i].g;
+                ps[n] = &ph[i].pl;
+                ws_[n] = w_dev + ph[i].w_origin;
+                wk[n] = static_cast<uint8_t *>(workspace) + ph[i].ws_off;
+                ++n;
+            }
+        }
         const int nside = (int)ph.size() < kSideStreams ? (int)ph.size() : kSideStreams;
-        cudaStream_t side[kSideStreams];
-        for (int i = 0; i < nside; ++i)
-            if (!(side[i] = side_stream(i))) return CONV_ERR_CUDA;
-        cudaEvent_t fork;
-        if (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess) return CONV_ERR_CUDA;
-        conv_status rc = cudaEventRecord(fork, s) == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+        conv_status rc = cudaEventRecord(ss->fork, s) == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
         for (int i = 0; i < nside && rc == CONV_OK; ++i)
-            if (cudaStreamWaitEvent(side[i], fork, 0) != cudaSuccess) rc = CONV_ERR_CUDA;
-        for (size_t i = 0; i < ph.size() && rc == CONV_OK; ++i) rc = run_class(ph[i], side[i % nside]);
+            if (cudaStreamWaitEvent(ss->streams[i], ss->fork, 0) != cudaSuccess) rc = CONV_ERR_CUDA;
+        for (size_t i = 0; i < ph.size() && rc == CONV_OK; ++i) rc = run_class(ph[i], ss->streams[i % nside], true);
         // join every side stream back, whatever happened above, so that the
         // caller's stream (or its capture) is left whole
-        for (int i = 0; i < nside; ++i) {
-            cudaEvent_t join;
-            if (cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
+        for (int i = 0; i < nside; ++i)
+            if (cudaEventRecord(ss->join[i], ss->streams[i]) != cudaSuccess ||
+                cudaStreamWaitEvent(s, ss->join[i], 0) != cudaSuccess)
                 rc = CONV_ERR_CUDA;
-                continue;
-            }
-            if (cudaEventRecord(join, side[i]) != cudaSuccess || cudaStreamWaitEvent(s, join, 0) != cudaSuccess)
-                rc = CONV_ERR_CUDA;
-            cudaEventDestroy(join);
-        }
-        cudaEventDestroy(fork);
         return rc;
     }
     const GradArgs a = [&] {

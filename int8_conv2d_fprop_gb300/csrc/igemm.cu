@@ -1031,54 +1031,90 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
 // 64 f16 (channels cb*64.. of tap (r, s) = divmod(j / c_steps, S), flipped for
 // CONVOLUTION), each row's 16-byte chunk i stored at chunk position
 // i ^ (row % 8): the image of the shared-memory stage, copied as one block.
-__global__ void igemm_pack_filter_kernel(const int8_t *w, int64_t ws0, int64_t ws1, int64_t ws2, int64_t ws3,
-                                         int32_t K, int32_t C, int32_t R, int32_t S, int32_t mode, int32_t c_steps,
-                                         int32_t k_steps, int32_t n_tiles, int32_t nt_rows, uint8_t *wp) {
+// One filter to repack: its view (base, element strides [K][C][R][S]), the
+// convolution's sizes and mode, and the plan's block geometry.
+struct PackFilterJob {
+    const int8_t *w;
+    int64_t ws0, ws1, ws2, ws3;
+    int32_t K, C, R, S, mode, c_steps, k_steps, n_tiles, nt_rows;
+    uint8_t *wp;
+};
+
+__device__ __forceinline__ int64_t pack_filter_items(const PackFilterJob &j) {
+    return (int64_t)j.n_tiles * j.k_steps * j.nt_rows * 8;
+}
+
+// Item idx of a repack: 16-byte chunk (idx & 7) of block row idx >> 3.
+__device__ __forceinline__ void pack_filter_item(const PackFilterJob &jb, int64_t idx) {
+    const int nt_rows = jb.nt_rows, k_steps = jb.k_steps, c_steps = jb.c_steps;
+    const int chunk = (int)(idx & 7);
+    const int64_t t = idx >> 3;
+    const int nl = (int)(t % nt_rows);
+    const int64_t t2 = t / nt_rows;
+    const int j = (int)(t2 % k_steps);
+    const int nt = (int)(t2 / k_steps);
+    const int k = nt * nt_rows + nl;
+    const int tap = j / c_steps;
+    const int cb = j - tap * c_steps;
+    const int r = tap / jb.S;
+    const int s = tap - r * jb.S;
+    const int rf = jb.mode ? jb.R - 1 - r : r;
+    const int sf = jb.mode ? jb.S - 1 - s : s;
+    const int c0 = cb * KS + chunk * 8;
+    const int8_t *w = jb.w;
+    uint32_t words[4];
+    const int64_t off = (int64_t)k * jb.ws0 + (int64_t)c0 * jb.ws1 + (int64_t)rf * jb.ws2 + (int64_t)sf * jb.ws3;
+    if (k < jb.K && c0 + 8 <= jb.C && jb.ws1 == 1 && ((uintptr_t)(w + off) & 7) == 0) {
+        // eight channels contiguous in memory: one 8-byte load
+        const uint2 v = *reinterpret_cast<const uint2 *>(w + off);
+        const uint32_t lo = v.x ^ 0x80808080u, hi = v.y ^ 0x80808080u;
+        words[0] = cvt_pair(lo, 0x4140);
+        words[1] = cvt_pair(lo, 0x4342);
+        words[2] = cvt_pair(hi, 0x4140);
+        words[3] = cvt_pair(hi, 0x4342);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            unsigned short hv[2];
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const int c = c0 + 2 * e + b;
+                int v = 0;
+                if (k < jb.K && c < jb.C)
+                    v = w[(int64_t)k * jb.ws0 + (int64_t)c * jb.ws1 + (int64_t)rf * jb.ws2 + (int64_t)sf * jb.ws3];
+                hv[b] = __half_as_ushort(__int2half_rn(v));
+            }
+            words[e] = (uint32_t)hv[0] | ((uint32_t)hv[1] << 16);
+        }
+    }
+    uint8_t *dst = jb.wp + ((t2 * nt_rows + nl) * 128) + (((chunk ^ (nl & 7))) << 4);
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
+}
+
+__global__ void igemm_pack_filter_kernel(const __grid_constant__ PackFilterJob jb) {
     ptx::launch_dependents();
-    const int64_t total = (int64_t)n_tiles * k_steps * nt_rows * 8;
+    const int64_t total = pack_filter_items(jb);
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x)
+        pack_filter_item(jb, idx);
+}
+
+// Several repacks in one launch (the residue classes of a data gradient):
+// the items of job i are end[i-1] .. end[i]-1 of the grid walk.
+struct PackFilterJobs {
+    PackFilterJob job[kMaxPackJobs];
+    int64_t end[kMaxPackJobs];
+    int32_t n;
+};
+
+__global__ void igemm_pack_filter_group_kernel(const __grid_constant__ PackFilterJobs js) {
+    ptx::launch_dependents();
+    const int64_t total = js.end[js.n - 1];
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
-        const int chunk = (int)(idx & 7);
-        const int64_t t = idx >> 3;
-        const int nl = (int)(t % nt_rows);
-        const int64_t t2 = t / nt_rows;
-        const int j = (int)(t2 % k_steps);
-        const int nt = (int)(t2 / k_steps);
-        const int k = nt * nt_rows + nl;
-        const int tap = j / c_steps;
-        const int cb = j - tap * c_steps;
-        const int r = tap / S;
-        const int s = tap - r * S;
-        const int rf = mode ? R - 1 - r : r;
-        const int sf = mode ? S - 1 - s : s;
-        const int c0 = cb * KS + chunk * 8;
-        uint32_t words[4];
-        const int64_t off = (int64_t)k * ws0 + (int64_t)c0 * ws1 + (int64_t)rf * ws2 + (int64_t)sf * ws3;
-        if (k < K && c0 + 8 <= C && ws1 == 1 && ((uintptr_t)(w + off) & 7) == 0) {
-            // eight channels contiguous in memory: one 8-byte load
-            const uint2 v = *reinterpret_cast<const uint2 *>(w + off);
-            const uint32_t lo = v.x ^ 0x80808080u, hi = v.y ^ 0x80808080u;
-            words[0] = cvt_pair(lo, 0x4140);
-            words[1] = cvt_pair(lo, 0x4342);
-            words[2] = cvt_pair(hi, 0x4140);
-            words[3] = cvt_pair(hi, 0x4342);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                unsigned short hv[2];
-#pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    const int c = c0 + 2 * e + b;
-                    int v = 0;
-                    if (k < K && c < C)
-                        v = w[(int64_t)k * ws0 + (int64_t)c * ws1 + (int64_t)rf * ws2 + (int64_t)sf * ws3];
-                    hv[b] = __half_as_ushort(__int2half_rn(v));
-                }
-                words[e] = (uint32_t)hv[0] | ((uint32_t)hv[1] << 16);
-            }
-        }
-        uint8_t *dst = wp + ((t2 * nt_rows + nl) * 128) + (((chunk ^ (nl & 7))) << 4);
-        *reinterpret_cast<uint4 *>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
+        int i = 0;
+        while (idx >= js.end[i]) ++i;
+        pack_filter_item(js.job[i], idx - (i ? js.end[i - 1] : 0));
     }
 }
 
@@ -1604,6 +1640,26 @@ void igemm_plan(const ConvGeom &g, const void *x_dev, IgemmPlan *pl) {
     pl->workspace_bytes = off + pl->xpack_bytes;
 }
 
+static PackFilterJob pack_job(const ConvGeom &g, const IgemmPlan &pl, const int8_t *w, uint8_t *wp) {
+    PackFilterJob j;
+    j.w = w;
+    j.ws0 = g.ws[0];
+    j.ws1 = g.ws[1];
+    j.ws2 = g.ws[2];
+    j.ws3 = g.ws[3];
+    j.K = (int32_t)g.K;
+    j.C = (int32_t)g.C;
+    j.R = (int32_t)g.R;
+    j.S = (int32_t)g.S;
+    j.mode = g.mode;
+    j.c_steps = (int32_t)pl.c_steps;
+    j.k_steps = (int32_t)pl.k_steps;
+    j.n_tiles = (int32_t)pl.n_tiles;
+    j.nt_rows = (int32_t)pl.n_tile;
+    j.wp = wp;
+    return j;
+}
+
 conv_status igemm_pack_filter_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *w, void *workspace,
                                      void *stream) {
     cudaStream_t st = (cudaStream_t)stream;
@@ -1613,9 +1669,28 @@ conv_status igemm_pack_filter_launch(const ConvGeom &g, const IgemmPlan &pl, con
     int64_t blocks = (total + 255) / 256;
     if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
     if (blocks == 0) return CONV_OK;
-    igemm_pack_filter_kernel<<<(unsigned)blocks, 256, 0, st>>>(
-        w, g.ws[0], g.ws[1], g.ws[2], g.ws[3], (int32_t)g.K, (int32_t)g.C, (int32_t)g.R, (int32_t)g.S, g.mode,
-        (int32_t)pl.c_steps, (int32_t)pl.k_steps, (int32_t)pl.n_tiles, (int32_t)pl.n_tile, wp);
+    igemm_pack_filter_kernel<<<(unsigned)blocks, 256, 0, st>>>(pack_job(g, pl, w, wp));
+    return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}
+
+conv_status igemm_pack_filter_group_launch(int n, const ConvGeom *const *g, const IgemmPlan *const *pl,
+                                           const int8_t *const *w, void *const *workspace, void *stream) {
+    if (n < 1 || n > kMaxPackJobs) return CONV_ERR_CUDA;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int sms = device_sm_count();
+    PackFilterJobs js;
+    std::memset(&js, 0, sizeof(js));
+    int64_t total = 0;
+    for (int i = 0; i < n; ++i) {
+        js.job[i] = pack_job(*g[i], *pl[i], w[i], static_cast<uint8_t *>(workspace[i]));
+        total += pl[i]->n_tiles * pl[i]->k_steps * pl[i]->n_tile * 8;
+        js.end[i] = total;
+    }
+    js.n = n;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+    if (blocks == 0) return CONV_OK;
+    igemm_pack_filter_group_kernel<<<(unsigned)blocks, 256, 0, st>>>(js);
     return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 

@@ -92,11 +92,28 @@ struct IgemmPlan {
     size_t workspace_bytes; // total, each part 256-byte aligned
 };
 
+// Key of a call's plan: the three descriptors, the parameters, the device
+// and whether the image pointer is 16-byte aligned (nullptr counts as
+// aligned); equal keys give equal plans.
+struct PlanKey {
+    int64_t v[64];
+    int n;
+};
+PlanKey make_plan_key(const conv_tensor_desc *x, const conv_tensor_desc *w, const conv_tensor_desc *y,
+                      const conv_fprop_params *p, const void *x_dev, int dev);
+// Empties the data-gradient plan cache.
+void dgrad_cache_clear();
+
 bool igemm_supported(const ConvGeom &g);
 void igemm_plan(const ConvGeom &g, const void *x_dev, IgemmPlan *pl);
 // Repacks the filter into the first pl.wpack_bytes of the workspace.
 conv_status igemm_pack_filter_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *w, void *workspace,
                                      void *stream);
+// Repacks the filters of n (<= kMaxPackJobs) planned convolutions, each into
+// its own workspace, in one launch.
+constexpr int kMaxPackJobs = 8;
+conv_status igemm_pack_filter_group_launch(int n, const ConvGeom *const *g, const IgemmPlan *const *pl,
+                                           const int8_t *const *w, void *const *workspace, void *stream);
 // Runs the convolution from a workspace whose filter part is already packed
 // (copies the image to channels-last first when pl.pack_x).
 conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *y,

@@ -159,3 +159,63 @@ def test_wgrad_empty_batch_takes_null_inputs(ic):
     st = ic.lib().conv_wgrad(ctypes.byref(x), None, ctypes.byref(dy), None, ctypes.byref(dwd), None,
                              ctypes.byref(p), None, 0, s)
     assert ic.STATUS[st] == "CONV_ERR_NULL_PTR"
+
+
+def _dgrad_case(ic, c):
+    x, w, dy = _setup(c)
+    wl = "KRSC" if c.layout == "NHWC" else "KCRS"
+    dyt, dyf, dys = _place(dy, c.layout)
+    wt, wf, wss = _place(w, wl)
+    ref = oracle.conv_dgrad(dyf, dy.shape, dys, wf, w.shape, wss, x.shape, c.pre, c.post, c.stride, c.dil, c.mode)
+    kw = dict(pre_padding=c.pre, post_padding=c.post, stride=c.stride, dilation=c.dil, mode=c.mode)
+    return dyt, wt, x.shape, ref, kw
+
+
+def test_dgrad_strided_repeated_calls_and_graph_replay(ic):
+    """Strided data gradients called again and again with the same
+    descriptors (the call's plan comes from the cache, its fork and join
+    events are reused): fresh dY and dX buffers on every call, two shapes
+    taking turns, then one call captured in a CUDA graph (the side streams
+    fork from and join back into the capture) and replayed on new dY values.
+    Every result is compared with the oracle."""
+    cases = [c for c in CASES if c.name in ("s2_3x3", "s23_dil23_shared_factor")]
+    assert len(cases) == 2
+    for rep in range(3):
+        for c in cases:
+            dyt, wt, xshape, ref, kw = _dgrad_case(ic, c)
+            dyt = dyt.clone(memory_format=torch.preserve_format)  # a fresh allocation each call
+            dx = _out(xshape, c.layout)
+            ic.conv_dgrad(dyt, wt, out=dx, **kw)
+            torch.cuda.synchronize()
+            assert ic.device_status() == 0
+            got = dx.cpu().numpy()
+            assert np.array_equal(got, ref), f"{c.name} call {rep}: {(got != ref).sum()} dX elements differ"
+    c = cases[0]
+    dyt, wt, xshape, ref, kw = _dgrad_case(ic, c)
+    dx = _out(xshape, c.layout)
+    p = ic.Params.make(c.pre, c.post, c.stride, c.dil, c.mode, False, False, 0)
+    wsb = ic.dgrad_workspace_size(ic.TensorDesc.from_tensor(dyt), ic.TensorDesc.from_tensor(wt),
+                                  ic.TensorDesc.from_tensor(dx), p)
+    assert wsb > 0
+    work = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        ic.conv_dgrad(dyt, wt, out=dx, workspace=work, stream=side, **kw)
+    side.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        ic.conv_dgrad(dyt, wt, out=dx, workspace=work, stream=side, **kw)
+    # new loss gradient values in the captured buffer, then replay
+    dy2 = synth.int8_uniform(4242, 3, tuple(dyt.shape))
+    dyt2, dyf2, dys2 = _place(dy2, c.layout)
+    dyt.copy_(dyt2)
+    dx.fill_(-5)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert ic.device_status() == 0
+    _, w, _ = _setup(c)
+    wf, wss = synth.place(w, "KRSC" if c.layout == "NHWC" else "KCRS")
+    ref2 = oracle.conv_dgrad(dyf2, dy2.shape, dys2, wf, w.shape, wss, xshape, c.pre, c.post, c.stride, c.dil,
+                             c.mode)
+    got = dx.cpu().numpy()
+    assert np.array_equal(got, ref2), f"graph replay: {(got != ref2).sum()} dX elements differ"
