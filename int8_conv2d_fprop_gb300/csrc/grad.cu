@@ -14,9 +14,10 @@
 //    K and C exchanged, written into dX through its strides times the stride.
 //    With stride 1 there is one class, the whole filter reversed.  Each class
 //    runs on the tensor-core kernel with its own filter repack in its own
-//    part of the workspace; several classes run side by side on streams
-//    forked from the caller's and joined back to it; a class no tap reaches
-//    is zero-filled.
+//    part of the workspace (all repacks in one launch); several classes run
+//    side by side on streams forked from the caller's and joined back to it,
+//    reading one shared channels-last copy of dY when dY needs one; a class
+//    no tap reaches is zero-filled.
 //  * otherwise (a class the tensor-core kernel cannot express, more than
 //    kMaxDgradPhases classes, or DIRECT_GENERIC): a CUDA-core kernel, one
 //    thread per dX element.
@@ -351,14 +352,38 @@ conv_status plan_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const c
     if (p->algo == CONV_ALGO_IMPLICIT_GEMM && !*tensor) return CONV_ERR_ALIGNMENT;
     *ws_bytes = 0;
     if (!*tensor) return CONV_OK;
+    int tapped = 0;
+    bool pack = false;
     for (DgradPhase &c : *ph) {
         if (!c.taps) continue;
         igemm_plan(c.g, dy_dev, &c.pl);
         // a class whose window starts inside dY (negative padding) gathers
         // with register loads, which bounds-check every pixel
         if (c.g.pad_h < 0 || c.g.pad_w < 0) c.pl.register_loads = true;
+        ++tapped;
+        pack = pack || c.pl.pack_x;
+    }
+    // Every class reads the same dY at stride 1 (every row): when dY needs a
+    // channels-last copy, one copy after the classes' parts serves them all,
+    // made once before they fork (each part then ends before its own copy).
+    const bool share = tapped > 1 && pack;
+    for (DgradPhase &c : *ph) {
+        if (!c.taps) continue;
         c.ws_off = *ws_bytes;
-        if (c.g.N > 0) *ws_bytes += (c.pl.workspace_bytes + 255) & ~(size_t)255;
+        const size_t part = share ? c.pl.xpack_off : c.pl.workspace_bytes;
+        if (c.g.N > 0) *ws_bytes += (part + 255) & ~(size_t)255;
+    }
+    if (share) {
+        const size_t shared_off = *ws_bytes;
+        size_t xbytes = 0;
+        for (DgradPhase &c : *ph) {
+            if (!c.taps) continue;
+            xbytes = c.pl.xpack_bytes;
+            c.pl.xpack_off = shared_off - c.ws_off;
+            c.pl.workspace_bytes = c.pl.xpack_off + c.pl.xpack_bytes;
+            c.pl.pack_done = true;
+        }
+        *ws_bytes += (xbytes + 255) & ~(size_t)255;
     }
     return CONV_OK;
 }
@@ -493,6 +518,13 @@ conv_status conv_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const c
         SideSet *ss = side_set();
         if (!ss) return CONV_ERR_CUDA;
         std::lock_guard<std::mutex> lock(ss->mu);
+        // the shared channels-last copy of dY, once
+        for (const DgradPhase &c : ph)
+            if (c.taps && c.pl.pack_done) {
+                if ((st = igemm_pack_image_launch(c.g, c.pl, dy_dev, static_cast<uint8_t *>(workspace) + c.ws_off, s)))
+                    return st;
+                break;
+            }
         {
             const ConvGeom *gs[kMaxPackJobs];
             const IgemmPlan *ps[kMaxPackJobs];

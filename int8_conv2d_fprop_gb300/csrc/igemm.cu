@@ -1556,6 +1556,7 @@ void igemm_plan(const ConvGeom &g, const void *x_dev, IgemmPlan *pl) {
     const bool direct = g.xs[1] == 1 && (g.C % 16) == 0 && (g.xs[0] % 16) == 0 && (g.xs[2] % 16) == 0 &&
                         (g.xs[3] % 16) == 0 && (x_dev == nullptr || ((uintptr_t)x_dev % 16) == 0);
     pl->pack_x = !direct;
+    pl->pack_done = false;
     pl->register_loads = false;
     // output channels per tile: 128, 192 or 256 (the smallest that covers
     // K, so that no MMA column is wasted on 129..192 channels)
@@ -1809,6 +1810,16 @@ ConvGeom kernel_geom(const ConvGeom &g, const IgemmPlan &pl) {
 }
 
 // Builds the launch plan of a call (kernel arguments, tensor maps, variant).
+// The channels-last copy of the image takes the plane transpose: each
+// channel's rows contiguous, whole 16-byte loads inside a row when rows are
+// skipped.
+bool planes_copy(const ConvGeom &g0, const IgemmPlan &pl, const int8_t *x) {
+    const int64_t hw = g0.H * g0.W;
+    return (g0.W == 1 || g0.xs[3] == 1) && (g0.H == 1 || g0.xs[2] == g0.W) && g0.xs[1] % 16 == 0 &&
+           g0.xs[0] % 16 == 0 && hw % 16 == 0 && ((uintptr_t)x % 16) == 0 && hw < ((int64_t)1 << 31) &&
+           (pl.row_step == 1 || g0.W % 16 == 0);
+}
+
 conv_status build_launch(const ConvGeom &g0, const IgemmPlan &pl, const int8_t *x, void *y, uint8_t *wp,
                          LaunchPlan *L) {
     const ConvGeom g = kernel_geom(g0, pl);
@@ -1816,12 +1827,7 @@ conv_status build_launch(const ConvGeom &g0, const IgemmPlan &pl, const int8_t *
     std::memset(&a, 0, sizeof(a));
     L->planes = false;
     if (pl.pack_x) {
-        // plane copy: each channel's rows contiguous, whole 16-byte loads
-        // inside a row when rows are skipped
-        const int64_t hw = g0.H * g0.W;
-        L->planes = (g0.W == 1 || g0.xs[3] == 1) && (g0.H == 1 || g0.xs[2] == g0.W) && g0.xs[1] % 16 == 0 &&
-                    g0.xs[0] % 16 == 0 && hw % 16 == 0 && ((uintptr_t)x % 16) == 0 && hw < ((int64_t)1 << 31) &&
-                    (pl.row_step == 1 || g0.W % 16 == 0);
+        L->planes = planes_copy(g0, pl, x);
         a.x = reinterpret_cast<int8_t *>(wp + pl.xpack_off);
         a.xs_n = g.H * g.W * pl.c16;
         a.xs_h = g.W * pl.c16;
@@ -1913,6 +1919,32 @@ void igemm_cache_stats(uint64_t *hits, uint64_t *misses) {
     *misses = g_launch_misses.load();
 }
 
+conv_status igemm_pack_image_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *workspace,
+                                    void *stream) {
+    cudaStream_t st = (cudaStream_t)stream;
+    const int sms = device_sm_count();
+    uint8_t *wp = static_cast<uint8_t *>(workspace);
+    int8_t *xp = reinterpret_cast<int8_t *>(wp + pl.xpack_off);
+    const int64_t hwp = pl.hp * g.W;  // pixels of each copied image
+    if (g.N * hwp == 0) return CONV_OK;
+    if (planes_copy(g, pl, x)) {
+        const int64_t total = g.N * ((hwp + kPackPix - 1) / kPackPix) * ((pl.c16 + kPackCh - 1) / kPackCh);
+        int64_t blocks = total < (int64_t)sms * 8 ? total : (int64_t)sms * 8;
+        igemm_pack_image_planes_kernel<<<(unsigned)blocks, 256, 0, st>>>(
+            x, g.xs[0], g.xs[1], g.N, (int32_t)g.C, (int32_t)hwp, (int32_t)g.W, (int32_t)pl.row0,
+            (int32_t)pl.row_step, (int32_t)pl.c16, xp);
+    } else {
+        const int64_t total = g.N * pl.hp * g.W * (pl.c16 / 16);
+        int64_t blocks = (total + 255) / 256;
+        if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
+        igemm_pack_image_kernel<<<(unsigned)blocks, 256, 0, st>>>(x, g.xs[0], g.xs[1], g.xs[2], g.xs[3], g.N,
+                                                                  (int32_t)g.C, (int32_t)pl.hp, (int32_t)g.W,
+                                                                  (int32_t)pl.row0, (int32_t)pl.row_step,
+                                                                  (int32_t)pl.c16, xp);
+    }
+    return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}
+
 conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *y,
                               const int32_t *bias, void *workspace, void *stream) {
     cudaStream_t st = (cudaStream_t)stream;
@@ -1954,25 +1986,9 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
     IgemmArgs &a = L.a;
     a.bias = g.bias ? bias : nullptr;
 
-    if (pl.pack_x) {
-        int8_t *xp = reinterpret_cast<int8_t *>(wp + pl.xpack_off);
-        const int64_t hwp = pl.hp * g.W;  // pixels of each copied image
-        if (L.planes) {
-            const int64_t total = g.N * ((hwp + kPackPix - 1) / kPackPix) * ((pl.c16 + kPackCh - 1) / kPackCh);
-            int64_t blocks = total < (int64_t)sms * 8 ? total : (int64_t)sms * 8;
-            igemm_pack_image_planes_kernel<<<(unsigned)blocks, 256, 0, st>>>(
-                x, g.xs[0], g.xs[1], g.N, (int32_t)g.C, (int32_t)hwp, (int32_t)g.W, (int32_t)pl.row0,
-                (int32_t)pl.row_step, (int32_t)pl.c16, xp);
-        } else {
-            const int64_t total = g.N * pl.hp * g.W * (pl.c16 / 16);
-            int64_t blocks = (total + 255) / 256;
-            if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
-            igemm_pack_image_kernel<<<(unsigned)blocks, 256, 0, st>>>(x, g.xs[0], g.xs[1], g.xs[2], g.xs[3], g.N,
-                                                                      (int32_t)g.C, (int32_t)pl.hp, (int32_t)g.W,
-                                                                      (int32_t)pl.row0, (int32_t)pl.row_step,
-                                                                      (int32_t)pl.c16, xp);
-        }
-        if (cudaGetLastError() != cudaSuccess) return CONV_ERR_CUDA;
+    if (pl.pack_x && !pl.pack_done) {
+        const conv_status pr = igemm_pack_image_launch(g, pl, x, workspace, stream);
+        if (pr) return pr;
     }
     const int grid = (int)pl.grid;
     conv_status rc;

@@ -67,6 +67,7 @@ constexpr int kIgemmKStep = 64;
 
 struct IgemmPlan {
     bool pack_x;            // image must be copied to channels-last first
+    bool pack_done;         // ... and the copy at xpack_off is made by the caller (igemm_pack_image_launch)
     bool register_loads;    // gather the image with global loads, not TMA im2col
     bool resident_b;        // the whole repacked filter stays in shared memory (TMA path)
     int64_t n_tile;         // output channels per tile (128, 192 or 256)
@@ -114,6 +115,9 @@ conv_status igemm_pack_filter_launch(const ConvGeom &g, const IgemmPlan &pl, con
 constexpr int kMaxPackJobs = 8;
 conv_status igemm_pack_filter_group_launch(int n, const ConvGeom *const *g, const IgemmPlan *const *pl,
                                            const int8_t *const *w, void *const *workspace, void *stream);
+// Makes the channels-last copy of the image at pl.xpack_off of the workspace.
+conv_status igemm_pack_image_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *workspace,
+                                    void *stream);
 // Runs the convolution from a workspace whose filter part is already packed
 // (copies the image to channels-last first when pl.pack_x).
 conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *y,

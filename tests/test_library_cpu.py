@@ -409,27 +409,34 @@ def _class_taps(rho, pre, stride, dil, taps):
     ((2, 2), (1, 1), (0, 0), (0, 0), 1, 1),   # three of four classes untouched
     ((1, 1), (2, 1), (5, 0), (1, 2), 3, 3),   # padding wider than the reach (5 > 4)
 ])
-def test_dgrad_residue_class_workspace(ic, stride, dil, pre, post, R, S):
+@pytest.mark.parametrize("dy_layout", ["NHWC", "NCHW"])
+def test_dgrad_residue_class_workspace(ic, stride, dil, pre, post, R, S, dy_layout):
     """The data gradient's workspace is the sum over the residue classes of
     the stride of each class's repacked filter: (taps of the class in H) x
     (taps in W) k-steps of 128 filter rows x 64 f16 channels (one tile of
-    output channels, one channel step).  The tap counts come from
-    enumerating the taps, not from the library's closed form."""
+    output channels, one channel step).  A dY that is not channels-last adds
+    one channels-last copy (N x P x Q pixels x 48 channels, rounded up to 256
+    bytes) that every class reads.  The tap counts come from enumerating the
+    taps, not from the library's closed form."""
     def d(dtype, dims, layout):
         return ic.TensorDesc.packed(dtype, dims, layout)
     H, W = 23, 21
     P = (H + pre[0] + post[0] - dil[0] * (R - 1) - 1) // stride[0] + 1
     Q = (W + pre[1] + post[1] - dil[1] * (S - 1) - 1) // stride[1] + 1
-    dy = d(ic.CONV_INT8, (2, 48, P, Q), "NHWC")
+    dy = d(ic.CONV_INT8, (2, 48, P, Q), dy_layout)
     w = d(ic.CONV_INT8, (48, 40, R, S), "KRSC")
     dx = d(ic.CONV_INT32, (2, 40, H, W), "NHWC")
     p = ic.Params.make(pre_padding=pre, post_padding=post, stride=stride, dilation=dil)
     want = 0
+    tapped = 0
     for rh in range(stride[0]):
         for rw in range(stride[1]):
             th = _class_taps(rh, pre[0], stride[0], dil[0], R)
             tw = _class_taps(rw, pre[1], stride[1], dil[1], S)
             want += th * tw * 128 * 128  # zero taps: a zero-filled class, no workspace
+            tapped += th * tw > 0
+    if dy_layout == "NCHW" and tapped:
+        want += (2 * P * Q * 48 + 255) // 256 * 256
     assert ic.dgrad_workspace_size(dy, w, dx, p) == want
 
 
