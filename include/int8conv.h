@@ -34,8 +34,9 @@
  * Errors: every entry point returns a conv_status; nothing is thrown across
  * the ABI.  Descriptors are validated before anything is launched (a call
  * whose descriptors and parameters equal those of an earlier, validated call
- * reuses that validation from the plan cache).  Kernel launch failures give CONV_ERR_CUDA.  A kernel whose
- * internal wait runs out of time records CONV_ERR_DEVICE_TIMEOUT in the
+ * reuses that validation from the plan cache).  Kernel launch failures give
+ * CONV_ERR_CUDA.  A kernel whose internal wait runs out of time records
+ * CONV_ERR_DEVICE_TIMEOUT in the
  * device status word and returns early; conv_device_status reports it.
  *
  * Thread safety: all entry points are reentrant; concurrent calls on
@@ -319,10 +320,13 @@ conv_status conv_fprop_static_workspace(const conv_tensor_desc *x, const int8_t 
  * convolutions of dY, one per residue class (h mod stride_h, w mod
  * stride_w) of dX's pixels, each by the filter taps that reach that class
  * (taken backwards, K and C exchanged) with stride 1, each in its own part of
- * the workspace; several classes run side by side on up to four
- * library-owned streams forked from `stream` and joined back to it (events;
+ * the workspace; the filters of all classes are repacked by one launch on
+ * `stream`, a dY that is not channels-last is copied once for all classes,
+ * and several classes run side by side on up to four library-owned streams
+ * forked from `stream` and joined back to it (events; streams and events are
  * created on the first such call on a device, so make that call outside a
- * stream capture); a class no tap reaches is written with zeros.
+ * stream capture; one such call at a time per device forks and joins, the
+ * others wait on a host mutex); a class no tap reaches is written with zeros.
  * More than 64 classes take the CUDA-core kernel.  conv_wgrad runs on the
  * tensor cores as a forward convolution of the image (batch and channel
  * dims exchanged) by dY (its batch as channels, its pixels as taps) when the
@@ -408,15 +412,18 @@ conv_status conv_measure_peak_rates(void *scratch, size_t scratch_bytes, conv_pe
  *     tensor maps, keyed by that plan and the 16-byte alignment of the image
  *     and output pointers (32 entries); a call with other buffers re-targets
  *     the cached maps to its addresses (cuTensorMapReplaceAddress) instead of
- *     encoding them again.
+ *     encoding them again;
+ *   - for conv_dgrad, the residue classes with their tensor-core plans,
+ *     keyed like the first cache on dY, W, dX and the parameters (16
+ *     entries).
  * A call whose key is cached skips validation, planning and map encoding;
  * its pointer checks (null, overlap, workspace) still run.  The caches are
  * library-owned host memory, shared by all threads (a mutex guards them),
  * least recently used entries giving way.  Cache lookups make no CUDA calls,
  * so cached calls stay capturable in CUDA graphs.
  *
- * conv_shutdown empties both caches (their memory is static; nothing is
- * freed or allocated).  Call it when no other thread is inside a library
+ * conv_shutdown empties the three caches (their memory is static; nothing is
+ * freed or allocated; the data gradient's side streams and events stay).  Call it when no other thread is inside a library
  * call.  conv_plan_cache_stats reads the hit and miss counts since the
  * library was loaded.
  */
