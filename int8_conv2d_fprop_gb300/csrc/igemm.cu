@@ -207,6 +207,34 @@ __device__ __forceinline__ Unit unit_at(int u, int full_units, int splits, int k
 // (group g covers k-steps g*kn/ng .. (g+1)*kn/ng - 1 of the run).
 __device__ __forceinline__ int groups_of(int kn) { return (kn + MAX_GROUP_STEPS - 1) / MAX_GROUP_STEPS; }
 
+// floor(n / d) for 0 <= n < 2^31 and 1 <= d < 2^31 by one multiply-high and
+// a shift: division by an invariant integer (Granlund and Montgomery, PLDI
+// 1994).  With l = ceil(log2 d) and m = ceil(2^(31+l) / d) = (2^(31+l) + e) / d,
+// 0 <= e < d, the quotient n*m / 2^(31+l) exceeds n/d by n*e / (d*2^(31+l)),
+// which is below 1/d because n*e < 2^31 * 2^l: both have the same floor.
+// d > 2^(l-1) keeps m below 2^32, and the floor is umulhi(n, m) >> (l - 1).
+// m == 0 stands for d == 1.  The issuers set up each unit's coordinates with
+// these instead of runtime divisions, which cost them about a microsecond per
+// unit while the other warps poll.
+struct FastDiv {
+    uint32_t m, s;
+};
+
+__device__ __forceinline__ int fdiv(int n, FastDiv f) {
+    return f.m ? (int)(__umulhi((uint32_t)n, f.m) >> f.s) : n;
+}
+
+inline FastDiv make_fastdiv(int64_t d) {
+    FastDiv f = {0u, 0u};
+    if (d <= 1) return f;
+    int l = 0;
+    while ((1ll << l) < d) ++l;
+    const uint64_t two_p = 1ull << (31 + l);
+    f.m = (uint32_t)((two_p + (uint64_t)d - 1) / (uint64_t)d);
+    f.s = (uint32_t)(l - 1);
+    return f;
+}
+
 struct IgemmArgs {
     CUtensorMap tmap_x;  // im2col map of the channels-last image, or its 2-D pixel-row map (TMA path only)
     CUtensorMap tmap_y;  // output map: 2-D [pixels][K] (y_tma 1) or 3-D [N][K][P*Q] (y_tma 2)
@@ -235,6 +263,7 @@ struct IgemmArgs {
                          // pixel rows (output pixel m reads image pixel m)
     int32_t y_tma;       // TMA stores: 1 pixel-major with contiguous channels, 2 channel-major
                          // (each channel's P*Q pixels contiguous, P*Q a multiple of 32)
+    FastDiv fd_nt, fd_pq, fd_q, fd_cs, fd_s;  // by n_tiles, P*Q, Q, c_steps, S
     uint64_t wait_limit_ns;
     int *status;         // device status word
 };
@@ -701,10 +730,10 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 const Unit wu = unit_at(u, a.full_units, a.splits, a.k_steps);
                 const int kn = wu.ke - wu.kb;
                 const int urot = wu.split < 0 ? rot : 0;
-                const int m0 = (wu.tile / a.n_tiles) * MT;
-                const int n0 = m0 / pq;
+                const int m0 = fdiv(wu.tile, a.fd_nt) * MT;
+                const int n0 = fdiv(m0, a.fd_pq);
                 const int rem = m0 - n0 * pq;
-                const int p0 = rem / a.Q;
+                const int p0 = fdiv(rem, a.fd_q);
                 const int q0 = rem - p0 * a.Q;
                 const int w0 = q0 * a.str_w - a.pad_w;
                 const int h0 = p0 * a.str_h - a.pad_h;
@@ -712,9 +741,9 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 // column s, channel block cb) and advanced without divisions
                 // (the issuing thread's loop is on every k-step's path)
                 int jr = wu.kb + urot;
-                int tap = jr / a.c_steps;
+                int tap = fdiv(jr, a.fd_cs);
                 int cb = jr - tap * a.c_steps;
-                int r = tap / a.S;
+                int r = fdiv(tap, a.fd_s);
                 int s = tap - r * a.S;
 #pragma unroll 1
                 for (int j = 0; j < kn; ++j) {
@@ -739,9 +768,9 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                     rs.next();
                     if (++jr == wu.ke) {  // the rotated sequence wraps to the unit's first k-step
                         jr = wu.kb;
-                        tap = jr / a.c_steps;
+                        tap = fdiv(jr, a.fd_cs);
                         cb = jr - tap * a.c_steps;
-                        r = tap / a.S;
+                        r = fdiv(tap, a.fd_s);
                         s = tap - r * a.S;
                     } else if (++cb == a.c_steps) {
                         cb = 0;
@@ -772,7 +801,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 const Unit wu = unit_at(u, a.full_units, a.splits, a.k_steps);
                 const int kn = wu.ke - wu.kb;
                 const int urot = wu.split < 0 ? rot : 0;
-                const int nt = wu.tile % a.n_tiles;
+                const int nt = wu.tile - fdiv(wu.tile, a.fd_nt) * a.n_tiles;
                 const uint8_t *blk = a.wp + (size_t)nt * a.k_steps * (size_t)B_BYTES;
                 for (int j = 0; j < kn; ++j) {
                     int jr = j + urot;
@@ -805,16 +834,16 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
         for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
             const Unit wu = unit_at(u, a.full_units, a.splits, a.k_steps);
             const int ng = groups_of(wu.ke - wu.kb);
-            const int mt = wu.tile / a.n_tiles;
+            const int mt = fdiv(wu.tile, a.fd_nt);
             const int nt = wu.tile - mt * a.n_tiles;
             const int m = mt * MT + row;
             const bool valid = m < a.m_total;
             int64_t yoff = 0;
             if (valid) {
                 const int pq = a.P * a.Q;
-                const int n = m / pq;
+                const int n = fdiv(m, a.fd_pq);
                 const int rem = m - n * pq;
-                const int p = rem / a.Q;
+                const int p = fdiv(rem, a.fd_q);
                 const int q = rem - p * a.Q;
                 yoff = (int64_t)n * a.ys_n + (int64_t)p * a.ys_p + (int64_t)q * a.ys_q;
             }
@@ -904,7 +933,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 const int k0 = nt * NT + col0;
                 const int m0w = mt * MT + quad * 32;
                 const int pq = a.P * a.Q;
-                const int img = m0w / pq;
+                const int img = fdiv(m0w, a.fd_pq);
                 const int pix = m0w - img * pq;
                 const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (uint32_t)(Cfg::EPI_BUFS * Cfg::EPI_BUF_BYTES);
 #pragma unroll
@@ -1853,6 +1882,11 @@ conv_status build_launch(const ConvGeom &g0, const IgemmPlan &pl, const int8_t *
     a.dil_h = (int32_t)g.dil_h; a.dil_w = (int32_t)g.dil_w;
     a.m_total = (int32_t)(g.N * g.P * g.Q);
     a.n_tiles = (int32_t)pl.n_tiles;
+    a.fd_nt = make_fastdiv(pl.n_tiles);
+    a.fd_pq = make_fastdiv(g.P * g.Q);
+    a.fd_q = make_fastdiv(g.Q);
+    a.fd_cs = make_fastdiv(pl.c_steps);
+    a.fd_s = make_fastdiv(g.S);
     a.num_tiles = (int32_t)(pl.m_tiles * pl.n_tiles);
     a.full_units = (int32_t)pl.full_units;
     a.splits = (int32_t)pl.splits;
