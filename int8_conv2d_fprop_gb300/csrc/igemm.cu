@@ -115,6 +115,12 @@ constexpr int RESB_MAX_BYTES = 128 * 1024;
 #ifndef IGEMM_STG_256
 #define IGEMM_STG_256 6
 #endif
+#ifndef IGEMM_ST_TM128
+#define IGEMM_ST_TM128 6
+#endif
+#ifndef IGEMM_STG_TM128
+#define IGEMM_STG_TM128 8
+#endif
 #ifndef IGEMM_ST_128
 #define IGEMM_ST_128 4
 #endif
@@ -135,9 +141,10 @@ struct TileCfg {
     static constexpr int B_BYTES = NT * KS * 2;
     // (192-column tiles without kTmemA: 40 KB stages, four of them behind
     // four staging buffers)
-    static constexpr int ST = kTmemA ? 4 : (kResB ? 2 : (kTma ? (NT == 256 ? IGEMM_ST_256 : (NT == 192 ? 4 : IGEMM_ST_128))
-                                                                : (NT == 128 ? 6 : 4)));
-    static constexpr int STG_STAGES = kTmemA ? (kResB ? 10 : 12)
+    static constexpr int ST = kTmemA ? (NT == 128 && !kResB ? IGEMM_ST_TM128 : 4)
+                                     : (kResB ? 2 : (kTma ? (NT == 256 ? IGEMM_ST_256 : (NT == 192 ? 4 : IGEMM_ST_128))
+                                                          : (NT == 128 ? 6 : 4)));
+    static constexpr int STG_STAGES = kTmemA ? (kResB ? 10 : (NT == 128 ? IGEMM_STG_TM128 : 12))
                                              : (kResB ? 6 : (kTma ? (NT == 256 ? IGEMM_STG_256 : (NT == 192 ? 4 : IGEMM_STG_128)) : 0));
     static constexpr int EPI_BUFS = kResB ? 1 : 2;  // output staging buffers per epilogue warp
     // output columns per staged store: 32 for the 128-column tensor-memory
