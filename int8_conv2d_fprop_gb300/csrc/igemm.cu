@@ -508,8 +508,13 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
     const uint64_t limit = a.wait_limit_ns;
     // launched as a programmatic dependent of the filter (or image) repack:
     // the set-up above overlaps its tail, nothing below runs before its
-    // writes are visible
+    // writes are visible.  Without cut tiles, a programmatic dependent that
+    // follows (the next call's convolution) may be scheduled from here on; it
+    // waits for this grid before touching memory.  (With cut tiles the
+    // reduction follows, and it starts when this grid ends, so that the next
+    // convolution's CTAs cannot take SMs from it.)
     ptx::grid_dependency_wait();
+    if (a.splits <= 1) ptx::launch_dependents();
 
     if (warp < 4 && kTmemA) {
         // ------------------------------------------------- converters (to tensor memory)
