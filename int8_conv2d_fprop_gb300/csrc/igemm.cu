@@ -19,7 +19,7 @@
 // x NT output channels (NT = 128 for K <= 128, 192 for K <= 192, else 256).
 // The image tile of a k-step is 128 output pixels x 64 channels of one tap.
 // Kernel variants, chosen per call:
-//  * NT = 256 and NT = 192 (TMA): warp 5 lane 0 issues one TMA load per
+//  * NT = 256 (TMA): warp 5 lane 0 issues one TMA load per
 //    k-step (an im2col box: window origins from the pixel order, the tap as
 //    pixel offset, zeros outside the image; or, for an unpadded 1x1
 //    stride-1 filter, a plain 2-D box of 128 pixel rows) into an int8
@@ -28,11 +28,13 @@
 //    matching pre-swizzled f16 filter block with one bulk async copy (or,
 //    when the whole repacked filter fits in 128 KB, once per CTA: the
 //    resident-filter variant).
-//  * NT = 128 (TMA): the same loads, issued by two warps (5 and 7) that own
-//    alternate staging slots; the converters write the f16 image tile into
-//    tensor memory (tcgen05.st) and the MMA reads A from there (the
-//    tensor-memory-A form), which leaves shared memory to a 12-deep staging
-//    ring; the epilogue stores 32 columns per TMA store.
+//  * NT = 128 and NT = 192 (TMA): the same loads, issued by two warps (5
+//    and 7) that own alternate staging slots; the converters write the f16
+//    image tile into tensor memory (tcgen05.st) and the MMA reads A from
+//    there (the tensor-memory-A form), which leaves shared memory to the
+//    filter ring and the staging ring (NT = 128: six filter stages and eight
+//    staging buffers; NT = 192: four and twelve); the 128-column epilogue
+//    stores 32 columns per TMA store.
 //  * global loads (fallback when a TMA map cannot express the call):
 //    warpgroup 0 threads each own one pixel row, gather 64 channels of one
 //    tap with 16-byte loads one item ahead (address formed from stride,
