@@ -228,8 +228,10 @@ conv_status conv_fprop_prepacked(const conv_tensor_desc *x, const int8_t *x_dev,
  * descriptors and semantics as conv_fprop; x_host, w_host, y_host and
  * bias_host are host pointers, page-locked for the copies to overlap).
  *
- * The filter and bias are copied once; the batch is then processed in up to
- * four chunks of whole images on three library-owned streams, so that the
+ * The filter and bias are copied once; the batch is then processed in a
+ * short lead chunk (a quarter of a chunk, so that the copy back to the host
+ * starts early) and up to four chunks of whole images on three
+ * library-owned streams, so that the
  * copy of chunk c to the device, the convolution of chunk c-1 and the copy
  * of chunk c-2 back to the host run at the same time.  Chunking needs every
  * image in its own byte range of the buffers (batch outermost in memory, as

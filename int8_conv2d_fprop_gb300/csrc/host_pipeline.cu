@@ -1,6 +1,7 @@
 // host_pipeline.cu -- conv_fprop with the tensors in host memory.
 //
-// The batch is cut into up to four chunks of whole images.  The filter and
+// The batch is cut into a short lead chunk (a quarter of a chunk) and up
+// to four chunks of whole images.  The filter and
 // bias are copied once; then, on three library-owned streams, chunk c's image
 // copy (host -> device) overlaps chunk c-1's convolution and chunk c-2's
 // output copy (device -> host).  Device chunk buffers are double-buffered in
@@ -19,6 +20,7 @@ namespace i8c {
 namespace {
 
 constexpr int kMaxChunks = 4;
+constexpr int kMaxSlots = kMaxChunks + 1;  // plus the short lead chunk
 constexpr int64_t kMinChunkBytes = 8 << 20;
 constexpr int kMaxDevices = 64;
 
@@ -27,7 +29,7 @@ struct DeviceRes {
     bool ready = false;
     cudaStream_t s_in = nullptr, s_cmp = nullptr, s_out = nullptr;
     cudaEvent_t ev_start = nullptr, ev_w = nullptr;
-    cudaEvent_t ev_in[kMaxChunks] = {}, ev_cmp[kMaxChunks] = {}, ev_out[kMaxChunks] = {};
+    cudaEvent_t ev_in[kMaxSlots] = {}, ev_cmp[kMaxSlots] = {}, ev_out[kMaxSlots] = {};
 };
 DeviceRes g_res[kMaxDevices];
 
@@ -40,7 +42,7 @@ conv_status init_res(DeviceRes &r) {
         !ok(cudaEventCreateWithFlags(&r.ev_start, cudaEventDisableTiming)) ||
         !ok(cudaEventCreateWithFlags(&r.ev_w, cudaEventDisableTiming)))
         return CONV_ERR_CUDA;
-    for (int i = 0; i < kMaxChunks; ++i) {
+    for (int i = 0; i < kMaxSlots; ++i) {
         if (!ok(cudaEventCreateWithFlags(&r.ev_in[i], cudaEventDisableTiming)) ||
             !ok(cudaEventCreateWithFlags(&r.ev_cmp[i], cudaEventDisableTiming)) ||
             !ok(cudaEventCreateWithFlags(&r.ev_out[i], cudaEventDisableTiming)))
@@ -61,7 +63,8 @@ int64_t extent_of_images(const conv_tensor_desc *d, int64_t n) {
 
 struct HostPlan {
     int chunks;
-    int64_t per_chunk;       // images per chunk (the last may hold fewer)
+    int64_t per_chunk;       // images per chunk at most (the lead and the last chunk hold fewer)
+    int64_t start[kMaxSlots + 1];  // chunk c covers images start[c] .. start[c+1]-1
     int64_t x_chunk_elems;   // device bytes of one image chunk
     int64_t y_chunk_elems;   // output elements of one output chunk
     int64_t y_esz;           // bytes per output element (4 for int32, 1 for int8)
@@ -90,6 +93,25 @@ conv_status host_plan(const conv_tensor_desc *x, const conv_tensor_desc *w, cons
     // rounding the chunk size up can leave fewer non-empty chunks (N = 5 in
     // chunks of 2 needs 3, not 4)
     if (N > 0) hp->chunks = (int)((N + hp->per_chunk - 1) / hp->per_chunk);
+    // a short lead chunk (a quarter of a chunk) first: the output's copy to
+    // the host, the longest stage (the link moves about 190 GB/s to the host
+    // whatever does the copy), starts after it instead of after a full chunk
+    hp->start[0] = 0;
+    if (hp->chunks > 1 && hp->per_chunk >= 2) {
+        int c = 0;
+        hp->start[++c] = hp->per_chunk / 4 > 0 ? hp->per_chunk / 4 : 1;
+        while (hp->start[c] < N) {
+            const int64_t nxt = hp->start[c] + hp->per_chunk;
+            hp->start[c + 1] = nxt < N ? nxt : N;
+            ++c;
+        }
+        hp->chunks = c;
+    } else {
+        for (int c = 0; c < hp->chunks; ++c) {
+            const int64_t nxt = (int64_t)(c + 1) * hp->per_chunk;
+            hp->start[c + 1] = nxt < N ? nxt : N;
+        }
+    }
     hp->x_chunk_elems = hp->chunks == 1 ? desc_extent_elems(x) : extent_of_images(x, hp->per_chunk);
     hp->y_chunk_elems = hp->chunks == 1 ? desc_extent_elems(y) : extent_of_images(y, hp->per_chunk);
     hp->w_elems = desc_extent_elems(w);
@@ -99,15 +121,16 @@ conv_status host_plan(const conv_tensor_desc *x, const conv_tensor_desc *w, cons
     yc.capacity_bytes = (uint64_t)(hp->y_chunk_elems * hp->y_esz);
     hp->ws_bytes = 0;
     if (hp->per_chunk > 0 && (st = conv_fprop_workspace_size(&xc, w, &yc, p, &hp->ws_bytes))) return st;
-    // the last chunk may hold fewer images, and with fewer tiles its plan may
-    // cut tiles along the reduction where the full chunks' plan does not:
-    // the workspace serves both
-    const int64_t last = N - (int64_t)(hp->chunks - 1) * hp->per_chunk;
-    if (hp->chunks > 1 && last > 0 && last != hp->per_chunk) {
+    // the lead and the last chunk may hold fewer images, and with fewer
+    // tiles their plans may cut tiles along the reduction where the full
+    // chunks' plan does not: the workspace serves every chunk size
+    for (int c = 0; hp->chunks > 1 && c < hp->chunks; ++c) {
+        const int64_t nb = hp->start[c + 1] - hp->start[c];
+        if (nb == hp->per_chunk) continue;
         conv_tensor_desc xl = *x, yl = *y;
-        xl.dims[0] = yl.dims[0] = last;
-        xl.capacity_bytes = (uint64_t)extent_of_images(x, last);
-        yl.capacity_bytes = (uint64_t)(extent_of_images(y, last) * hp->y_esz);
+        xl.dims[0] = yl.dims[0] = nb;
+        xl.capacity_bytes = (uint64_t)extent_of_images(x, nb);
+        yl.capacity_bytes = (uint64_t)(extent_of_images(y, nb) * hp->y_esz);
         size_t wl = 0;
         if ((st = conv_fprop_workspace_size(&xl, w, &yl, p, &wl))) return st;
         if (wl > hp->ws_bytes) hp->ws_bytes = wl;
@@ -182,12 +205,11 @@ conv_status conv_fprop_host(const conv_tensor_desc *x, const int8_t *x_host, con
         return CONV_ERR_CUDA;
     if (!ok(cudaEventRecord(r.ev_w, r.s_in)) || !ok(cudaStreamWaitEvent(r.s_cmp, r.ev_w, 0))) return CONV_ERR_CUDA;
 
-    const int64_t N = x->dims[0];
     for (int c = 0; c < hp.chunks; ++c) {
         const int bsel = c & 1;
-        const int64_t n0 = c * hp.per_chunk;
-        const int64_t nb = (N - n0) < hp.per_chunk ? (N - n0) : hp.per_chunk;
-        if (nb <= 0) return CONV_ERR_BAD_PARAM;  // cannot happen: chunks = ceil(N / per_chunk)
+        const int64_t n0 = hp.start[c];
+        const int64_t nb = hp.start[c + 1] - n0;
+        if (nb <= 0) return CONV_ERR_BAD_PARAM;  // cannot happen: the starts increase
         conv_tensor_desc xc = *x, yc = *y;
         xc.dims[0] = yc.dims[0] = nb;
         const int64_t x_elems = hp.chunks == 1 ? desc_extent_elems(x) : extent_of_images(x, nb);
