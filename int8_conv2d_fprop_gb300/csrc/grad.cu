@@ -544,6 +544,36 @@ conv_status conv_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const c
                 ++n;
             }
         }
+        // the classes as one launch on the caller's stream when they share a
+        // kernel variant and cut no tiles (no fork or join then); the classes
+        // no tap reaches are zero-filled beside it
+        {
+            const ConvGeom *gs[kIgemmMaxGroup];
+            const IgemmPlan *ps[kIgemmMaxGroup];
+            void *ys[kIgemmMaxGroup];
+            void *wk[kIgemmMaxGroup];
+            int n = 0;
+            bool fits = true;
+            for (const DgradPhase &c : ph) {
+                if (!c.taps) continue;
+                if (n == kIgemmMaxGroup) {
+                    fits = false;
+                    break;
+                }
+                gs[n] = &c.g;
+                ps[n] = &c.pl;
+                ys[n] = dx_dev + c.y_origin;
+                wk[n] = static_cast<uint8_t *>(workspace) + c.ws_off;
+                ++n;
+            }
+            bool launched = false;
+            if (fits && n >= 2 && (st = igemm_group_launch(n, gs, ps, dy_dev, ys, wk, s, &launched))) return st;
+            if (launched) {
+                for (const DgradPhase &c : ph)
+                    if (!c.taps && (st = run_class(c, s, true))) return st;
+                return CONV_OK;
+            }
+        }
         const int nside = (int)ph.size() < kSideStreams ? (int)ph.size() : kSideStreams;
         conv_status rc = cudaEventRecord(ss->fork, s) == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
         for (int i = 0; i < nside && rc == CONV_OK; ++i)

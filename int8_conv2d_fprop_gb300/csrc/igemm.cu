@@ -406,9 +406,9 @@ __device__ __forceinline__ void cursor_load(const LoadCursor &c, const IgemmArgs
     }
 }
 
-__device__ __forceinline__ void cursor_advance(LoadCursor &c, const IgemmArgs &a, int row) {
+__device__ __forceinline__ void cursor_advance(LoadCursor &c, const IgemmArgs &a, int row, int gdim) {
     if (++c.j == c.je) {
-        cursor_set_unit(c, a, c.u + gridDim.x, row);
+        cursor_set_unit(c, a, c.u + gdim, row);
         return;
     }
     if (++c.cb == a.c_steps) {
@@ -444,8 +444,10 @@ __device__ __forceinline__ void drain_ring_owned(uint64_t *bars, int depth, int6
     }
 }
 
+// The kernel's body for one CTA: `a` holds the call's arguments, bid is the
+// CTA's index among the gdim CTAs that share the call's work units.
 template <int NT, bool kTma, bool kResB, bool kTmemA>
-__global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_constant__ IgemmArgs a) {
+__device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, const int gdim) {
     using Cfg = TileCfg<NT, kTma, kResB, kTmemA>;
     constexpr int ST = Cfg::ST;
     constexpr int STG = Cfg::STG_STAGES;
@@ -466,7 +468,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     int total = 0;  // k-steps of all units of this CTA
-    for (int u = blockIdx.x; u < a.num_units; u += gridDim.x) {
+    for (int u = bid; u < a.num_units; u += gdim) {
         const Unit w = unit_at(u, a.full_units, a.splits, a.k_steps);
         total += w.ke - w.kb;
     }
@@ -474,7 +476,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
     // own k-step, so the SMs do not all fetch the same filter block at the
     // same moment (any order is exact: a group is any run of at most 1024
     // products)
-    const int rot = kTma ? (int)(((int64_t)blockIdx.x * 7) % a.k_steps) : 0;
+    const int rot = kTma ? (int)(((int64_t)bid * 7) % a.k_steps) : 0;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < ST; ++i) {
@@ -600,18 +602,18 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
         const uint32_t row_off = (uint32_t)row * 128u;
         const uint32_t swz = (uint32_t)(row & 7);
         LoadCursor cur;
-        cursor_set_unit(cur, a, blockIdx.x, row);
+        cursor_set_unit(cur, a, bid, row);
         uint4 pf[PREFETCH][4];
 #pragma unroll
         for (int d = 0; d < PREFETCH; ++d) {
             if (cur.u < a.num_units) {
                 cursor_load(cur, a, pf[d]);
-                cursor_advance(cur, a, row);
+                cursor_advance(cur, a, row, gdim);
             }
         }
         Ring<ST> rg;
         // filter block cursor (thread 0 only): unit b_u, k-step b_j < b_je
-        int b_u = blockIdx.x;
+        int b_u = bid;
         Unit bw = unit_at(b_u < a.num_units ? b_u : 0, a.full_units, a.splits, a.k_steps);
         int b_j = bw.kb, b_je = bw.ke;
         int64_t b_issued = 0;
@@ -625,7 +627,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                 for (int i = 0; i < 4; ++i) v[i] = pf[d][i];
                 if (cur.u < a.num_units) {  // keep PREFETCH items in flight
                     cursor_load(cur, a, pf[d]);
-                    cursor_advance(cur, a, row);
+                    cursor_advance(cur, a, row, gdim);
                 }
                 if (!wait_phase(ptx::smem_addr(&ctl->empty[rg.idx]), rg.phase ^ 1u, abort_flag, limit, a.status)) {
                     ok = false;
@@ -639,7 +641,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
                     ptx::bulk_copy_g2s(b_smem + rg.idx * B_BYTES, src, B_BYTES, bar);
                     ++b_issued;
                     if (++b_j == b_je) {
-                        b_u += gridDim.x;
+                        b_u += gdim;
                         bw = unit_at(b_u < a.num_units ? b_u : 0, a.full_units, a.splits, a.k_steps);
                         b_j = bw.kb;
                         b_je = bw.ke;
@@ -672,7 +674,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
             uint32_t gi = 0;
             bool ok = true;
             if (kResB) ok = wait_phase(ptx::smem_addr(&ctl->b_res), 0, abort_flag, limit, a.status);
-            for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
+            for (int u = bid; u < a.num_units && ok; u += gdim) {
                 const Unit w = unit_at(u, a.full_units, a.splits, a.k_steps);
                 const int kn = w.ke - w.kb;
                 const int ng = groups_of(kn);
@@ -740,7 +742,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
             int64_t issued = 0;
             bool ok = true;
             const int pq = a.P * a.Q;
-            for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
+            for (int u = bid; u < a.num_units && ok; u += gdim) {
                 const Unit wu = unit_at(u, a.full_units, a.splits, a.k_steps);
                 const int kn = wu.ke - wu.kb;
                 const int urot = wu.split < 0 ? rot : 0;
@@ -811,7 +813,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
             Ring<ST> rb;
             int64_t issued = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
+            for (int u = bid; u < a.num_units && ok; u += gdim) {
                 const Unit wu = unit_at(u, a.full_units, a.splits, a.k_steps);
                 const int kn = wu.ke - wu.kb;
                 const int urot = wu.split < 0 ? rot : 0;
@@ -845,7 +847,7 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
         const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)col0;
         uint32_t gi = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
+        for (int u = bid; u < a.num_units && ok; u += gdim) {
             const Unit wu = unit_at(u, a.full_units, a.splits, a.k_steps);
             const int ng = groups_of(wu.ke - wu.kb);
             const int mt = fdiv(wu.tile, a.fd_nt);
@@ -1067,6 +1069,29 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_con
     __syncthreads();
     ptx::tc_fence_after();
     if (warp == MMA_WARP) ptx::tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+}
+
+template <int NT, bool kTma, bool kResB, bool kTmemA>
+__global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_constant__ IgemmArgs a) {
+    conv_cta<NT, kTma, kResB, kTmemA>(a, blockIdx.x, gridDim.x);
+}
+
+// Several convolutions of one kernel variant in one launch (the residue
+// classes of a data gradient): CTAs cta_start[c] .. cta_start[c+1]-1 work
+// on convolution c alone, each reading its own arguments.
+constexpr int kMaxGroup = kIgemmMaxGroup;
+struct IgemmGroup {
+    IgemmArgs cls[kMaxGroup];
+    int32_t cta_start[kMaxGroup + 1];
+    int32_t n;
+};
+
+template <int NT, bool kTma, bool kResB, bool kTmemA>
+__global__ void __launch_bounds__(THREADS, 1) igemm_conv_group_kernel(const __grid_constant__ IgemmGroup g) {
+    int c = 0;
+    while (c + 1 < g.n && (int)blockIdx.x >= g.cta_start[c + 1]) ++c;
+    conv_cta<NT, kTma, kResB, kTmemA>(g.cls[c], (int)blockIdx.x - g.cta_start[c],
+                                      g.cta_start[c + 1] - g.cta_start[c]);
 }
 
 // ---------------------------------------------------------------- filter repack
@@ -1993,14 +2018,13 @@ conv_status igemm_pack_image_launch(const ConvGeom &g, const IgemmPlan &pl, cons
     return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
-conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *y,
-                              const int32_t *bias, void *workspace, void *stream) {
-    cudaStream_t st = (cudaStream_t)stream;
-    const int sms = device_sm_count();
-    uint8_t *wp = static_cast<uint8_t *>(workspace);
-    if (pl.m_tiles * pl.n_tiles == 0) return CONV_OK;
+namespace {
 
-    // the launch plan: from the cache when an equal call ran before
+// The launch plan of a call (variant, grid, arguments with their tensor
+// maps): from the cache when an equal call ran before, re-targeted to this
+// call's buffers.
+conv_status prepare_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *y, const int32_t *bias,
+                           uint8_t *wp, LaunchPlan *out) {
     int dev = 0;
     cudaGetDevice(&dev);
     // (every decision of build_launch that reads a pointer reads only its
@@ -2031,8 +2055,105 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
         if (b) return b;
         launch_insert(key, L);
     }
+    L.a.bias = g.bias ? bias : nullptr;
+    *out = L;
+    return CONV_OK;
+}
+
+template <int NT, bool kTma, bool kResB = false, bool kTmemA = false>
+conv_status launch_conv_group(const IgemmGroup &grp, int grid, cudaStream_t st) {
+    using Cfg = TileCfg<NT, kTma, kResB, kTmemA>;
+    static std::atomic<bool> attr_set[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !attr_set[dev].load()) {
+        if (cudaFuncSetAttribute(igemm_conv_group_kernel<NT, kTma, kResB, kTmemA>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
+            return CONV_ERR_CUDA;
+        if (dev >= 0 && dev < 64) attr_set[dev].store(true);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, igemm_conv_group_kernel<NT, kTma, kResB, kTmemA>, grp) != cudaSuccess)
+        return CONV_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}
+
+}  // namespace
+
+conv_status igemm_group_launch(int n, const ConvGeom *const *g, const IgemmPlan *const *pl, const int8_t *x,
+                               void *const *y, void *const *workspace, void *stream, bool *launched) {
+    *launched = false;
+    if (n < 2 || n > kMaxGroup) return CONV_OK;
+    static IgemmGroup grp_zero;  // (zero-filled template: IgemmArgs has no constructor)
+    IgemmGroup grp = grp_zero;
+    int variant = -1;
+    int64_t work = 0;
+    for (int c = 0; c < n; ++c) {
+        // whole tiles only (no reduction kernel), and the image copy, if
+        // any, already made by the caller
+        if (pl[c]->splits > 1 || (pl[c]->pack_x && !pl[c]->pack_done) || pl[c]->m_tiles * pl[c]->n_tiles == 0)
+            return CONV_OK;
+        LaunchPlan L;
+        conv_status st = prepare_launch(*g[c], *pl[c], x, y[c], nullptr, static_cast<uint8_t *>(workspace[c]), &L);
+        if (st) return st;
+        if (!(L.variant == V_TMEM128 || L.variant == V_TMEM192 || L.variant == V_TMA256 || L.variant == V_RESB256) ||
+            (variant >= 0 && L.variant != variant))
+            return CONV_OK;
+        variant = L.variant;
+        grp.cls[c] = L.a;
+        work += pl[c]->num_units * pl[c]->k_steps;
+    }
+    // CTAs for each convolution in proportion to its work (tiles x k-steps;
+    // at least one CTA, at most one per tile), together at most one per SM
+    const int sms = device_sm_count();
+    int cta[kMaxGroup];
+    int used = 0;
+    for (int c = 0; c < n; ++c) {
+        int64_t share = (int64_t)sms * pl[c]->num_units * pl[c]->k_steps / work;
+        if (share < 1) share = 1;
+        if (share > pl[c]->num_units) share = pl[c]->num_units;
+        cta[c] = (int)share;
+        used += cta[c];
+    }
+    for (int c = 0; used > sms && c < n; c = (c + 1) % n)
+        if (cta[c] > 1) {
+            --cta[c];
+            --used;
+        }
+    grp.n = n;
+    grp.cta_start[0] = 0;
+    for (int c = 0; c < n; ++c) grp.cta_start[c + 1] = grp.cta_start[c] + cta[c];
+    cudaStream_t st = (cudaStream_t)stream;
+    conv_status rc;
+    switch (variant) {
+        case V_TMEM128: rc = launch_conv_group<128, true, false, true>(grp, used, st); break;
+        case V_TMEM192: rc = launch_conv_group<192, true, false, true>(grp, used, st); break;
+        case V_TMA256: rc = launch_conv_group<256, true>(grp, used, st); break;
+        default: rc = launch_conv_group<256, true, true>(grp, used, st); break;
+    }
+    if (rc == CONV_OK) *launched = true;
+    return rc;
+}
+
+conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *y,
+                              const int32_t *bias, void *workspace, void *stream) {
+    cudaStream_t st = (cudaStream_t)stream;
+    const int sms = device_sm_count();
+    uint8_t *wp = static_cast<uint8_t *>(workspace);
+    if (pl.m_tiles * pl.n_tiles == 0) return CONV_OK;
+    LaunchPlan L;
+    conv_status pst = prepare_launch(g, pl, x, y, bias, wp, &L);
+    if (pst) return pst;
     IgemmArgs &a = L.a;
-    a.bias = g.bias ? bias : nullptr;
 
     if (pl.pack_x && !pl.pack_done) {
         const conv_status pr = igemm_pack_image_launch(g, pl, x, workspace, stream);

@@ -115,6 +115,15 @@ conv_status igemm_pack_filter_launch(const ConvGeom &g, const IgemmPlan &pl, con
 constexpr int kMaxPackJobs = 8;
 conv_status igemm_pack_filter_group_launch(int n, const ConvGeom *const *g, const IgemmPlan *const *pl,
                                            const int8_t *const *w, void *const *workspace, void *stream);
+// Runs n (2..4) planned convolutions of one image x (each with its own
+// filter part of the workspace and output y[c]) as one launch of the
+// tensor-core kernel, each on its share of the SMs.  Sets *launched = false,
+// launching nothing, when the convolutions cannot share a launch (different
+// kernel variants, cut tiles, an image copy still to make, register loads);
+// the caller then runs them one by one.
+constexpr int kIgemmMaxGroup = 4;
+conv_status igemm_group_launch(int n, const ConvGeom *const *g, const IgemmPlan *const *pl, const int8_t *x,
+                               void *const *y, void *const *workspace, void *stream, bool *launched);
 // Makes the channels-last copy of the image at pl.xpack_off of the workspace.
 conv_status igemm_pack_image_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *workspace,
                                     void *stream);

@@ -65,6 +65,10 @@ CASES = [
     G("s98_many_classes", 2, 16, 14, 14, 32, 3, 3, (1, 1), (0, 0), stride=(9, 8)),
     G("c3_shape_batch2", 2, 256, 56, 56, 256, 3, 3, (1, 1), (1, 1), tensor=True),
     G("c2_shape_s2_batch1", 1, 128, 56, 56, 256, 3, 3, (1, 1), (0, 0), stride=(2, 2), tensor=True),
+    # strided classes launched together on 192- and 256-column tiles (the
+    # classes' output channels are the forward image's C)
+    G("s2_c160_group192", 2, 160, 21, 18, 48, 3, 3, (1, 1), (1, 1), stride=(2, 2), tensor=True),
+    G("s2_c256_group256_conv", 1, 256, 17, 20, 40, 3, 2, (1, 0), (0, 1), stride=(2, 2), mode=1, tensor=True),
 ]
 
 
