@@ -324,11 +324,13 @@ conv_status conv_fprop_static_workspace(const conv_tensor_desc *x, const int8_t 
  * (taken backwards, K and C exchanged) with stride 1, each in its own part of
  * the workspace; the filters of all classes are repacked by one launch on
  * `stream`, a dY that is not channels-last is copied once for all classes,
- * and several classes run side by side on up to four library-owned streams
- * forked from `stream` and joined back to it (events; streams and events are
- * created on the first such call on a device, so make that call outside a
- * stream capture; one such call at a time per device forks and joins, the
- * others wait on a host mutex); a class no tap reaches is written with zeros.
+ * and the classes run as one kernel launch on `stream` (each on its share
+ * of the SMs) when they use the same kernel variant and cut no tiles;
+ * otherwise side by side on up to four library-owned streams forked from
+ * `stream` and joined back to it (events; streams and events are created on
+ * the first such call on a device, so make that call outside a stream
+ * capture; one such call at a time per device forks and joins, the others
+ * wait on a host mutex); a class no tap reaches is written with zeros.
  * More than 64 classes take the CUDA-core kernel.  conv_wgrad runs on the
  * tensor cores as a forward convolution of the image (batch and channel
  * dims exchanged) by dY (its batch as channels, its pixels as taps) when the
