@@ -105,11 +105,12 @@ constexpr int RESB_MAX_BYTES = 128 * 1024;
 // kTma: the int8 image tile arrives by TMA (im2col mode) in a ring of
 // STG_STAGES staging buffers and the producer warps convert it shared ->
 // shared; otherwise the producer warps gather it with global loads.
-// One ring of ST stages holds the f16 A tile and the filter block of a
-// k-step side by side, guarded by one "full" barrier (128 producer arrivals
-// plus the filter copy's bytes) and one "empty" barrier (one MMA commit), so
-// the single MMA-issuing thread waits once and commits once per k-step.  The
-// int8 staging ring of the TMA path (STG stages) runs ahead of it.
+// One ring of ST stages holds the f16 A tile (or, kTmemA, guards its
+// tensor-memory stage) and the filter block of a k-step side by side,
+// guarded by one "full" barrier (128 producer arrivals plus the filter
+// copy's bytes) and one "empty" barrier (one MMA commit), so the single
+// MMA-issuing thread waits once and commits once per k-step.  The int8
+// staging ring of the TMA path (STG stages) runs ahead of it.
 // Ring depths of the TMA path (tuning knobs; shared memory is the limit).
 #ifndef IGEMM_ST_256
 #define IGEMM_ST_256 3
@@ -136,8 +137,9 @@ constexpr int RESB_MAX_BYTES = 128 * 1024;
 // kTmemA (128- and 192-column tiles, TMA path): the f16 image tile of a
 // k-step goes to tensor memory (columns 2*NT.. next to the two accumulator
 // slots, 32 columns per stage: 256..383 or 384..511) and the MMA reads it
-// from there; the shared memory that held it becomes int8 staging buffers,
-// i.e. image bytes in flight (12; 10 with a resident filter).
+// from there; the shared memory that held it goes to the filter ring and
+// the int8 staging buffers (128 columns: six filter stages, eight staging
+// buffers; 192 columns: four and twelve).
 template <int NT, bool kTma, bool kResB = false, bool kTmemA = false>
 struct TileCfg {
     static constexpr int B_BYTES = NT * KS * 2;
