@@ -189,8 +189,7 @@ conv_status plan_call_uncached(const conv_tensor_desc *x, const conv_tensor_desc
     if (*algo == CONV_ALGO_IMPLICIT_GEMM && !igemm_supported(*g)) return CONV_ERR_ALIGNMENT;
     if (*algo == CONV_ALGO_DIRECT_DP4A && !dp4a_supported(*g)) return CONV_ERR_ALIGNMENT;
     if (*algo == CONV_ALGO_IMPLICIT_GEMM) {
-        igemm_plan(*g, x_dev, pl);
-        pl->register_loads = global_loads;
+        igemm_plan(*g, x_dev, pl, global_loads);
     }
     return CONV_OK;
 }

@@ -354,15 +354,22 @@ conv_status plan_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const c
     if (!*tensor) return CONV_OK;
     int tapped = 0;
     bool pack = false;
+    // a class whose window starts inside dY (negative padding) gathers
+    // with register loads, which bounds-check every pixel
+    auto neg_pad = [](const DgradPhase &c) { return c.g.pad_h < 0 || c.g.pad_w < 0; };
+    bool in_place = false;
     for (DgradPhase &c : *ph) {
         if (!c.taps) continue;
-        igemm_plan(c.g, dy_dev, &c.pl);
-        // a class whose window starts inside dY (negative padding) gathers
-        // with register loads, which bounds-check every pixel
-        if (c.g.pad_h < 0 || c.g.pad_w < 0) c.pl.register_loads = true;
+        igemm_plan(c.g, dy_dev, &c.pl, neg_pad(c));
         ++tapped;
         pack = pack || c.pl.pack_x;
+        in_place = in_place || c.pl.nchw_rows;
     }
+    // an NCHW dY is either read in place by every class or copied once for
+    // all of them
+    if (pack && in_place)
+        for (DgradPhase &c : *ph)
+            if (c.taps && c.pl.nchw_rows) igemm_plan(c.g, dy_dev, &c.pl, neg_pad(c), false);
     // Every class reads the same dY at stride 1 (every row): when dY needs a
     // channels-last copy, one copy after the classes' parts serves them all,
     // made once before they fork (each part then ends before its own copy).

@@ -101,6 +101,10 @@ constexpr int B_ISSUER_WARP = 6;    // TMA path: issues the filter block copies
 // tile of output channels) fits in this many bytes, every CTA loads it once
 // and keeps it in shared memory, so a k-step brings only its image tile.
 constexpr int RESB_MAX_BYTES = 128 * 1024;
+// Staging slot of the NCHW-row variants: the image rows a tile's 128 pixels
+// lie on (up to 192 bytes of image row per channel), 64 channels each.
+constexpr int NCHW_STG_BYTES = 192 * KS;
+constexpr int NCHW_MAX_ROW_BYTES = NCHW_STG_BYTES / KS;
 
 // kTma: the int8 image tile arrives by TMA (im2col mode) in a ring of
 // STG_STAGES staging buffers and the producer warps convert it shared ->
@@ -140,15 +144,23 @@ constexpr int RESB_MAX_BYTES = 128 * 1024;
 // from there; the shared memory that held it goes to the filter ring and
 // the int8 staging buffers (128 columns: six filter stages, eight staging
 // buffers; 192 columns: four and twelve).
-template <int NT, bool kTma, bool kResB = false, bool kTmemA = false>
+// kNchw (with kTmemA): the image is read in place from NCHW planes, each
+// k-step's staging slot holding, for the rows its tile's pixels lie on,
+// 64 channel rows of the whole image row (one 4-D TMA box per row); the
+// converters transpose while converting (128 columns: five filter stages
+// and six 12 KB staging slots; 192 columns: four and eight).
+template <int NT, bool kTma, bool kResB = false, bool kTmemA = false, bool kNchw = false>
 struct TileCfg {
     static constexpr int B_BYTES = NT * KS * 2;
+    static constexpr int STG_SLOT = kNchw ? NCHW_STG_BYTES : STG_BYTES;  // bytes per staging slot
     // (192-column tiles without kTmemA: 40 KB stages, four of them behind
     // four staging buffers)
-    static constexpr int ST = kTmemA ? (NT == 128 && !kResB ? IGEMM_ST_TM128 : 4)
+    static constexpr int ST = kNchw ? (NT == 128 ? 5 : 4)
+                            : kTmemA ? (NT == 128 && !kResB ? IGEMM_ST_TM128 : 4)
                                      : (kResB ? 2 : (kTma ? (NT == 256 ? IGEMM_ST_256 : (NT == 192 ? 4 : IGEMM_ST_128))
                                                           : (NT == 128 ? 6 : 4)));
-    static constexpr int STG_STAGES = kTmemA ? (kResB ? 10 : (NT == 128 ? IGEMM_STG_TM128 : 12))
+    static constexpr int STG_STAGES = kNchw ? (NT == 128 ? 6 : 8)
+                                    : kTmemA ? (kResB ? 10 : (NT == 128 ? IGEMM_STG_TM128 : 12))
                                              : (kResB ? 6 : (kTma ? (NT == 256 ? IGEMM_STG_256 : (NT == 192 ? 4 : IGEMM_STG_128)) : 0));
     static constexpr int EPI_BUFS = kResB ? 1 : 2;  // output staging buffers per epilogue warp
     // output columns per staged store: 32 for the 128-column tensor-memory
@@ -169,9 +181,10 @@ struct TileCfg {
     // not help: their divergent branches run one after the other.)
     static constexpr int A_ISSUERS = kTmemA ? 2 : 1;
     static_assert(STG_STAGES % A_ISSUERS == 0, "staging slots split evenly between the issuers");
-    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + A_SMEM + B_AREA + STG_STAGES * STG_BYTES +
+    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + A_SMEM + B_AREA + STG_STAGES * STG_SLOT +
                                       EPI_BYTES + 512 /*barriers*/;
     static_assert(!kResB || kTma, "the resident filter needs the TMA producers");
+    static_assert(!kNchw || (kTmemA && !kResB), "NCHW rows feed the tensor-memory image stages");
     static_assert(!kTmemA || (kTma && NT <= 192 && TMEM_A_COL + ST * 32 <= 512), "image stages in tensor memory");
     static_assert(TMEM_COLS <= 512, "tensor memory has 512 columns");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
@@ -448,9 +461,10 @@ __device__ __forceinline__ void drain_ring_owned(uint64_t *bars, int depth, int6
 
 // The kernel's body for one CTA: `a` holds the call's arguments, bid is the
 // CTA's index among the gdim CTAs that share the call's work units.
-template <int NT, bool kTma, bool kResB, bool kTmemA>
+template <int NT, bool kTma, bool kResB, bool kTmemA, bool kNchw>
 __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, const int gdim) {
-    using Cfg = TileCfg<NT, kTma, kResB, kTmemA>;
+    using Cfg = TileCfg<NT, kTma, kResB, kTmemA, kNchw>;
+    constexpr int STG_SLOT = Cfg::STG_SLOT;
     constexpr int ST = Cfg::ST;
     constexpr int STG = Cfg::STG_STAGES;
     constexpr int B_BYTES = Cfg::B_BYTES;
@@ -462,9 +476,9 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
     const uint32_t a_smem = base;
     const uint32_t b_smem = a_smem + Cfg::A_SMEM;
     const uint32_t stg_smem = b_smem + Cfg::B_AREA;
-    const uint32_t epi_smem = stg_smem + STG * STG_BYTES;
+    const uint32_t epi_smem = stg_smem + STG * STG_SLOT;
     SharedCtl *ctl =
-        reinterpret_cast<SharedCtl *>(base_ptr + Cfg::A_SMEM + Cfg::B_AREA + STG * STG_BYTES + Cfg::EPI_BYTES);
+        reinterpret_cast<SharedCtl *>(base_ptr + Cfg::A_SMEM + Cfg::B_AREA + STG * STG_SLOT + Cfg::EPI_BYTES);
     volatile int32_t *abort_flag = &ctl->abort_flag;
 
     const int warp = threadIdx.x >> 5;
@@ -522,7 +536,121 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
     ptx::grid_dependency_wait();
     if (a.splits <= 1) ptx::launch_dependents();
 
-    if (warp < 4 && kTmemA) {
+    if (warp < 4 && kNchw) {
+        // ---------------------------------------- converters (NCHW rows to tensor memory)
+        // The staged slot holds, for each output row the tile's pixels lie
+        // on (box b), 64 channel rows of the whole image row (W bytes each).
+        // With stride 1 along W and tap offsets s*dil_w - pre_w that are
+        // multiples of 4, the tile's pixels 4t .. 4t+3 are four consecutive
+        // bytes of every channel row.  Thread (j, u) = (lane / 4, lane % 4)
+        // of warp w takes pixels 32w + 4j .. +3 and channels 16i + u + 4v
+        // (i, v = 0..3): sixteen 4-byte loads (the four u read four
+        // neighbouring channel rows).  A 4x4 byte transpose inside the
+        // conversion gives each pixel its channels, and tcgen05.st.16x256b
+        // writes them: in the warp's first 16 lanes, lane j holds pixel 4j
+        // and lane j+8 pixel 4j+1; in the second, lanes 16+j and 24+j hold
+        // pixels 4j+2 and 4j+3 (lane l of the quadrant: pixel
+        // 4*(l%8) + l/8, which the epilogue follows).  Column 8i + 2u holds
+        // channels 16i + u and 16i + u + 4, column 8i + 2u + 1 channels
+        // 16i + u + 8 and 16i + u + 12: within each 16 channels the K order
+        // swaps the two 2-bit digits of the channel index, and the filter
+        // repack writes the filter blocks in the same order.
+        ptx::setmaxnreg_dec<PRODUCER_REGS>();
+        const int jq = lane >> 2, u = lane & 3;
+        const uint32_t lanes_lo = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)Cfg::TMEM_A_COL;
+        const uint32_t lanes_hi = lanes_lo + (16u << 16);
+        const uint32_t rowb = (uint32_t)a.W;          // bytes per channel row
+        const uint32_t boxb = (uint32_t)(KS * a.W);   // bytes per image-row box
+        const int pq = a.P * a.Q;
+        Ring<ST> ra;
+        Ring<STG> rs;
+        bool ok = true;
+        for (int uu = bid; uu < a.num_units && ok; uu += gdim) {
+            const Unit wu = unit_at(uu, a.full_units, a.splits, a.k_steps);
+            const int kn = wu.ke - wu.kb;
+            const int urot = wu.split < 0 ? rot : 0;
+            const int m0 = fdiv(wu.tile, a.fd_nt) * MT;
+            const int rem = m0 - fdiv(m0, a.fd_pq) * pq;
+            const int q0 = rem - fdiv(rem, a.fd_q) * a.Q;
+            // this thread's pixels in the run of output rows that starts at
+            // the tile's first pixel: row b, column q
+            const int f = q0 + warp * 32 + jq * 4;
+            const int b = fdiv(f, a.fd_q);
+            const int q = f - b * a.Q;
+            const uint32_t pix = (uint32_t)b * boxb + (uint32_t)u * rowb;
+            // the k-steps in the issuers' order (rotated), for the tap column s
+            int jr = wu.kb + urot;
+            int tap = fdiv(jr, a.fd_cs);
+            int cb = jr - tap * a.c_steps;
+            int r = fdiv(tap, a.fd_s);
+            int s = tap - r * a.S;
+#pragma unroll 1
+            for (int j = 0; j < kn; ++j) {
+                bool got = wait_phase(ptx::smem_addr(&ctl->stg_full[rs.idx]), rs.phase, abort_flag, limit, a.status);
+                got = got && wait_phase(ptx::smem_addr(&ctl->empty[ra.idx]), ra.phase ^ 1u, abort_flag, limit, a.status);
+                // tcgen05.st is warp-collective: the whole warp proceeds or stops together
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                const int wpos = q + s * a.dil_w - a.pad_w;
+                const bool inb = (unsigned)wpos < (unsigned)a.W;  // all four pixels in or all out
+                const uint32_t src = stg_smem + rs.idx * STG_SLOT + pix + (uint32_t)wpos;
+                uint32_t xw[16];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        xw[4 * i + v] = inb ? ptx::ld_shared_b32(src + (uint32_t)(16 * i + 4 * v) * rowb) : 0u;
+                // gl[2i], gl[2i+1]: bytes [x0.b0, x1.b0, x0.b1, x1.b1] of the words
+                // of channels (16i + u, +4) and (+8, +12), i.e. those channels of
+                // pixels 4j and 4j+1; gh likewise bytes 2 and 3, pixels 4j+2, 4j+3
+                uint32_t gl[8], gh[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t x0 = xw[2 * i] ^ 0x80808080u, x1 = xw[2 * i + 1] ^ 0x80808080u;
+                    gl[i] = __byte_perm(x0, x1, 0x5140);
+                    gh[i] = __byte_perm(x0, x1, 0x7362);
+                }
+                uint32_t v[16];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    v[4 * i + 0] = cvt_pair(gl[2 * i], 0x4140);      // lane j:      pixel 4j
+                    v[4 * i + 1] = cvt_pair(gl[2 * i + 1], 0x4140);
+                    v[4 * i + 2] = cvt_pair(gl[2 * i], 0x4342);      // lane j + 8:  pixel 4j + 1
+                    v[4 * i + 3] = cvt_pair(gl[2 * i + 1], 0x4342);
+                }
+                ptx::tmem_st_16x256b_x4(lanes_lo + (uint32_t)(ra.idx * 32), v);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    v[4 * i + 0] = cvt_pair(gh[2 * i], 0x4140);      // lane 16 + j: pixel 4j + 2
+                    v[4 * i + 1] = cvt_pair(gh[2 * i + 1], 0x4140);
+                    v[4 * i + 2] = cvt_pair(gh[2 * i], 0x4342);      // lane 24 + j: pixel 4j + 3
+                    v[4 * i + 3] = cvt_pair(gh[2 * i + 1], 0x4342);
+                }
+                ptx::tmem_st_16x256b_x4(lanes_hi + (uint32_t)(ra.idx * 32), v);
+                ptx::tmem_st_wait();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(ptx::smem_addr(&ctl->stg_empty[rs.idx]));
+                ptx::mbar_arrive(ptx::smem_addr(&ctl->full[ra.idx]));
+                ra.next();
+                rs.next();
+                if (++jr == wu.ke) {
+                    jr = wu.kb;
+                    tap = fdiv(jr, a.fd_cs);
+                    cb = jr - tap * a.c_steps;
+                    r = fdiv(tap, a.fd_s);
+                    s = tap - r * a.S;
+                } else if (++cb == a.c_steps) {
+                    cb = 0;
+                    if (++s == a.S) {
+                        s = 0;
+                        ++r;
+                    }
+                }
+            }
+        }
+    } else if (warp < 4 && kTmemA) {
         // ------------------------------------------------- converters (to tensor memory)
         // Thread t converts pixel row t of the staged tile (its 64 channel
         // bytes, 16-byte chunk c stored at chunk position c ^ ((t >> 1) & 3)
@@ -540,7 +668,7 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
             got = got && wait_phase(ptx::smem_addr(&ctl->empty[ra.idx]), ra.phase ^ 1u, abort_flag, limit, a.status);
             // tcgen05.st is warp-collective: the whole warp proceeds or stops together
             if (!__all_sync(0xffffffffu, got)) break;
-            const uint32_t src = stg_smem + rs.idx * STG_BYTES + (uint32_t)row * 64u;
+            const uint32_t src = stg_smem + rs.idx * STG_SLOT + (uint32_t)row * 64u;
             uint4 vin[4];
 #pragma unroll
             for (int c = 0; c < 4; ++c) vin[c] = ptx::ld_shared_v4(src + ((((uint32_t)c) ^ sw) << 4));
@@ -576,7 +704,7 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
             if (!wait_phase(ptx::smem_addr(&ctl->stg_full[rs.idx]), rs.phase, abort_flag, limit, a.status)) break;
             if (!wait_phase(ptx::smem_addr(&ctl->empty[ra.idx]), ra.phase ^ 1u, abort_flag, limit, a.status))
                 break;
-            const uint32_t src = stg_smem + rs.idx * STG_BYTES + chunk * 16u;
+            const uint32_t src = stg_smem + rs.idx * STG_SLOT + chunk * 16u;
             const uint32_t dst = a_smem + ra.idx * A_BYTES;
             uint4 vin[4];
 #pragma unroll
@@ -755,6 +883,10 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
                 const int q0 = rem - p0 * a.Q;
                 const int w0 = q0 * a.str_w - a.pad_w;
                 const int h0 = p0 * a.str_h - a.pad_h;
+                // kNchw: the tile's pixels lie on output rows p0, p0 + 1, ...
+                // (into the next image past P - 1), one image-row box each
+                const int nrows = kNchw ? fdiv(q0 + MT - 1, a.fd_q) + 1 : 1;
+                const uint32_t box_bytes = (uint32_t)(KS * a.W);
                 // k-step kb + ((j + urot) mod kn), held as (tap row r, tap
                 // column s, channel block cb) and advanced without divisions
                 // (the issuing thread's loop is on every k-step's path)
@@ -775,12 +907,29 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
                             break;
                         }
                         const uint32_t bar = ptx::smem_addr(&ctl->stg_full[rs.idx]);
-                        ptx::mbar_arrive_expect_tx(bar, STG_BYTES);
-                        if (a.a_rows)
-                            ptx::tma_load_2d(stg_smem + rs.idx * STG_BYTES, &a.tmap_x, cb * KS, m0, bar);
-                        else
-                            ptx::tma_load_im2col_4d(stg_smem + rs.idx * STG_BYTES, &a.tmap_x, cb * KS, w0, h0, n0,
+                        if (kNchw) {
+                            // whole image rows h = p*stride_h - pre_h + r*dil_h of
+                            // channels cb*64.., boxes {W, 1, 64, 1} of the NCHW map
+                            // (rows outside the image and images past N read as zeros)
+                            ptx::mbar_arrive_expect_tx(bar, (uint32_t)nrows * box_bytes);
+                            int pb = p0, nb = n0;
+#pragma unroll 1
+                            for (int b = 0; b < nrows; ++b) {
+                                ptx::tma_load_4d(stg_smem + rs.idx * STG_SLOT + (uint32_t)b * box_bytes, &a.tmap_x, 0,
+                                                 pb * a.str_h - a.pad_h + r * a.dil_h, cb * KS, nb, bar);
+                                if (++pb == a.P) {
+                                    pb = 0;
+                                    ++nb;
+                                }
+                            }
+                        } else if (a.a_rows) {
+                            ptx::mbar_arrive_expect_tx(bar, STG_BYTES);
+                            ptx::tma_load_2d(stg_smem + rs.idx * STG_SLOT, &a.tmap_x, cb * KS, m0, bar);
+                        } else {
+                            ptx::mbar_arrive_expect_tx(bar, STG_BYTES);
+                            ptx::tma_load_im2col_4d(stg_smem + rs.idx * STG_SLOT, &a.tmap_x, cb * KS, w0, h0, n0,
                                                     (uint16_t)(s * a.dil_w), (uint16_t)(r * a.dil_h), bar);
+                        }
                     }
                     ++issued;
                     rs.next();
@@ -845,7 +994,10 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
         ptx::setmaxnreg_inc<EPILOGUE_REGS>();
         const int quad = warp & 3;                      // tensor-memory lanes this warp may access
         const int col0 = ((warp - FIRST_EPI_WARP) >> 2) * HALF;  // this warp's half of the columns
-        const int row = quad * 32 + lane;
+        // the tile row (pixel) in this thread's tensor-memory lane: the lane
+        // itself, or, for NCHW-row image stages, 4*(lane%8) + lane/8
+        const int prow = kNchw ? (((lane & 7) << 2) | (lane >> 3)) : lane;
+        const int row = quad * 32 + prow;
         const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)col0;
         uint32_t gi = 0;
         bool ok = true;
@@ -944,8 +1096,8 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
                 // Channel-major output: the warp's 32 rows are 32 consecutive
                 // pixels of one image (P*Q is a multiple of 32).  It stages
                 // EPI_COLS channels x 32 pixels at a time as rows of 128
-                // bytes, lane i writing pixel i of each row (no bank
-                // conflicts), and one lane stores them as a {32 pixels,
+                // bytes, the lane holding pixel i writing position i of each
+                // row (no bank conflicts), and one lane stores them as a {32 pixels,
                 // EPI_COLS channels, 1 image} box; the map clips channels past
                 // K and images past N.
                 const int k0 = nt * NT + col0;
@@ -961,7 +1113,7 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
                     __syncwarp();
 #pragma unroll
                     for (int c = 0; c < Cfg::EPI_COLS; ++c)
-                        ptx::st_shared_b32(buf + (uint32_t)c * 128u + (uint32_t)lane * 4u,
+                        ptx::st_shared_b32(buf + (uint32_t)c * 128u + (uint32_t)prow * 4u,
                                            (uint32_t)acc[ch * Cfg::EPI_COLS + c]);
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
@@ -976,13 +1128,13 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
                 const int k0 = nt * NT + col0;
                 const int m0w = mt * MT + quad * 32;
                 const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (uint32_t)(Cfg::EPI_BUFS * Cfg::EPI_BUF_BYTES);
-                const uint32_t sw = ((uint32_t)lane >> 1) & 3u;
+                const uint32_t sw = ((uint32_t)prow >> 1) & 3u;
 #pragma unroll
                 for (int ch = 0; ch < HALF / 64; ++ch) {
                     const uint32_t buf = ebase + (uint32_t)(ch % Cfg::EPI_BUFS) * Cfg::EPI_BUF_BYTES;
                     if (lane == 0) ptx::bulk_wait_group_read<Cfg::EPI_BUFS - 1>();  // the store that last read buf is done
                     __syncwarp();
-                    const uint32_t rowaddr = buf + (uint32_t)lane * 64u;
+                    const uint32_t rowaddr = buf + (uint32_t)prow * 64u;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t wv[4];
@@ -1017,14 +1169,14 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
                 const int k0 = nt * NT + col0;
                 const int m0w = mt * MT + quad * 32;
                 const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (uint32_t)(Cfg::EPI_BUFS * Cfg::EPI_BUF_BYTES);
-                const uint32_t sw = CHUNKS == 8 ? ((uint32_t)lane & 7u) : (((uint32_t)lane >> 1) & 3u);
+                const uint32_t sw = CHUNKS == 8 ? ((uint32_t)prow & 7u) : (((uint32_t)prow >> 1) & 3u);
 #pragma unroll
                 for (int ch = 0; ch < HALF / Cfg::EPI_COLS; ++ch) {
                     const uint32_t buf = ebase + (uint32_t)(ch % Cfg::EPI_BUFS) * Cfg::EPI_BUF_BYTES;
                     if (lane == 0) ptx::bulk_wait_group_read<Cfg::EPI_BUFS - 1>();  // the store that last read buf is done
                     __syncwarp();
                     const int i0 = ch * Cfg::EPI_COLS;
-                    const uint32_t rowaddr = buf + (uint32_t)lane * (uint32_t)(Cfg::EPI_COLS * 4);
+                    const uint32_t rowaddr = buf + (uint32_t)prow * (uint32_t)(Cfg::EPI_COLS * 4);
 #pragma unroll
                     for (int c = 0; c < CHUNKS; ++c)
                         ptx::st_shared_v4(rowaddr + ((((uint32_t)c) ^ sw) << 4),
@@ -1073,9 +1225,9 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
     if (warp == MMA_WARP) ptx::tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
-template <int NT, bool kTma, bool kResB, bool kTmemA>
+template <int NT, bool kTma, bool kResB, bool kTmemA, bool kNchw>
 __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_constant__ IgemmArgs a) {
-    conv_cta<NT, kTma, kResB, kTmemA>(a, blockIdx.x, gridDim.x);
+    conv_cta<NT, kTma, kResB, kTmemA, kNchw>(a, blockIdx.x, gridDim.x);
 }
 
 // Several convolutions of one kernel variant in one launch (the residue
@@ -1088,11 +1240,11 @@ struct IgemmGroup {
     int32_t n;
 };
 
-template <int NT, bool kTma, bool kResB, bool kTmemA>
+template <int NT, bool kTma, bool kResB, bool kTmemA, bool kNchw>
 __global__ void __launch_bounds__(THREADS, 1) igemm_conv_group_kernel(const __grid_constant__ IgemmGroup g) {
     int c = 0;
     while (c + 1 < g.n && (int)blockIdx.x >= g.cta_start[c + 1]) ++c;
-    conv_cta<NT, kTma, kResB, kTmemA>(g.cls[c], (int)blockIdx.x - g.cta_start[c],
+    conv_cta<NT, kTma, kResB, kTmemA, kNchw>(g.cls[c], (int)blockIdx.x - g.cta_start[c],
                                       g.cta_start[c + 1] - g.cta_start[c]);
 }
 
@@ -1103,10 +1255,12 @@ __global__ void __launch_bounds__(THREADS, 1) igemm_conv_group_kernel(const __gr
 // i ^ (row % 8): the image of the shared-memory stage, copied as one block.
 // One filter to repack: its view (base, element strides [K][C][R][S]), the
 // convolution's sizes and mode, and the plan's block geometry.
+// kperm: the K order of the NCHW-row variants, which within every 16
+// channels puts channel 4a + b at position 4b + a.
 struct PackFilterJob {
     const int8_t *w;
     int64_t ws0, ws1, ws2, ws3;
-    int32_t K, C, R, S, mode, c_steps, k_steps, n_tiles, nt_rows;
+    int32_t K, C, R, S, mode, c_steps, k_steps, n_tiles, nt_rows, kperm;
     uint8_t *wp;
 };
 
@@ -1134,7 +1288,7 @@ __device__ __forceinline__ void pack_filter_item(const PackFilterJob &jb, int64_
     const int8_t *w = jb.w;
     uint32_t words[4];
     const int64_t off = (int64_t)k * jb.ws0 + (int64_t)c0 * jb.ws1 + (int64_t)rf * jb.ws2 + (int64_t)sf * jb.ws3;
-    if (k < jb.K && c0 + 8 <= jb.C && jb.ws1 == 1 && ((uintptr_t)(w + off) & 7) == 0) {
+    if (!jb.kperm && k < jb.K && c0 + 8 <= jb.C && jb.ws1 == 1 && ((uintptr_t)(w + off) & 7) == 0) {
         // eight channels contiguous in memory: one 8-byte load
         const uint2 v = *reinterpret_cast<const uint2 *>(w + off);
         const uint32_t lo = v.x ^ 0x80808080u, hi = v.y ^ 0x80808080u;
@@ -1148,7 +1302,8 @@ __device__ __forceinline__ void pack_filter_item(const PackFilterJob &jb, int64_
             unsigned short hv[2];
 #pragma unroll
             for (int b = 0; b < 2; ++b) {
-                const int c = c0 + 2 * e + b;
+                const int kpos = chunk * 8 + 2 * e + b;  // position in the block's 64
+                const int c = jb.kperm ? cb * KS + ((kpos & ~15) | ((kpos & 3) << 2) | ((kpos >> 2) & 3)) : c0 + 2 * e + b;
                 int v = 0;
                 if (k < jb.K && c < jb.C)
                     v = w[(int64_t)k * jb.ws0 + (int64_t)c * jb.ws1 + (int64_t)rf * jb.ws2 + (int64_t)sf * jb.ws3];
@@ -1421,14 +1576,14 @@ constexpr int64_t kMinSplitSteps = 16;   // k-steps of the shortest run of a cut
 constexpr int64_t kMaxSplits = 32;
 constexpr int64_t kMinTailSteps = 4;     // k-steps of the shortest run of a last-round tile
 
-template <int NT, bool kTma, bool kResB = false, bool kTmemA = false>
+template <int NT, bool kTma, bool kResB = false, bool kTmemA = false, bool kNchw = false>
 conv_status launch_conv(const IgemmArgs &a, int grid, cudaStream_t st) {
-    using Cfg = TileCfg<NT, kTma, kResB, kTmemA>;
+    using Cfg = TileCfg<NT, kTma, kResB, kTmemA, kNchw>;
     static std::atomic<bool> attr_set[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !attr_set[dev].load()) {
-        if (cudaFuncSetAttribute(igemm_conv_kernel<NT, kTma, kResB, kTmemA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(igemm_conv_kernel<NT, kTma, kResB, kTmemA, kNchw>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg::SMEM_BYTES) != cudaSuccess)
             return CONV_ERR_CUDA;
         if (dev >= 0 && dev < 64) attr_set[dev].store(true);
@@ -1448,7 +1603,7 @@ conv_status launch_conv(const IgemmArgs &a, int grid, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, igemm_conv_kernel<NT, kTma, kResB, kTmemA>, a) != cudaSuccess) return CONV_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, igemm_conv_kernel<NT, kTma, kResB, kTmemA, kNchw>, a) != cudaSuccess) return CONV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
@@ -1521,6 +1676,22 @@ bool encode_rows_map(const ConvGeom &g, const void *x, int64_t xs_w, int64_t c_d
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(x), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE,
                            swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 4-D map {W, H, C, N} of an int8 image whose channels hold contiguous rows
+// (byte strides xs[2], xs[1], xs[0]): box {W, 1, 64, 1}, one image row of
+// 64 channels, no swizzle (the NCHW-row variants).
+bool encode_nchw_rows_map(const ConvGeom &g, const void *x, CUtensorMap *map) {
+    auto enc = tiled_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)g.W, (cuuint64_t)g.H, (cuuint64_t)g.C, (cuuint64_t)g.N};
+    const cuuint64_t strides[3] = {(cuuint64_t)g.xs[2], (cuuint64_t)g.xs[1], (cuuint64_t)g.xs[0]};
+    const cuuint32_t box[4] = {(cuuint32_t)g.W, 1, (cuuint32_t)KS, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(x), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -1622,15 +1793,39 @@ bool igemm_supported(const ConvGeom &g) {
     return true;
 }
 
-void igemm_plan(const ConvGeom &g, const void *x_dev, IgemmPlan *pl) {
+// Whether the NCHW-row variants can read the image in place: each channel's
+// rows contiguous with 16-byte aligned strides (the 4-D TMA map), rows of W
+// bytes with W a multiple of 16 and at most 192, and every k-step's pixels
+// whole 4-byte runs of image rows: stride 1 along W, Q, pre-padding along W
+// and the tap offsets s*dil_w all multiples of 4.  The image rows one
+// 128-pixel tile lies on must fit one staging slot: a tile starts at column
+// q0 = 128t mod Q, a multiple of gcd(128, Q), so it spans at most
+// (Q - gcd(128, Q) + 127) / Q + 1 rows.
+static bool nchw_rows_fit(const ConvGeom &g, const void *x_dev) {
+    if (g.W % 16 != 0 || g.W > NCHW_MAX_ROW_BYTES) return false;
+    if (g.xs[3] != 1 || g.xs[2] % 16 != 0 || g.xs[1] % 16 != 0 || g.xs[0] % 16 != 0) return false;
+    if (x_dev != nullptr && ((uintptr_t)x_dev % 16) != 0) return false;
+    if (g.xs[0] >= ((int64_t)1 << 40) || g.xs[1] >= ((int64_t)1 << 40) || g.xs[2] >= ((int64_t)1 << 40)) return false;
+    if (g.H >= ((int64_t)1 << 31) || g.N >= ((int64_t)1 << 31) || g.C >= ((int64_t)1 << 31)) return false;
+    if (g.str_w != 1 || g.Q % 4 != 0 || g.pad_w % 4 != 0 || (g.S > 1 && g.dil_w % 4 != 0)) return false;
+    const int64_t gq = std::gcd((int64_t)MT, g.Q);
+    const int64_t rows = (g.Q - gq + MT - 1) / g.Q + 1;
+    return rows * g.W <= NCHW_MAX_ROW_BYTES;
+}
+
+void igemm_plan(const ConvGeom &g, const void *x_dev, IgemmPlan *pl, bool register_loads, bool nchw_rows_ok) {
     const bool direct = g.xs[1] == 1 && (g.C % 16) == 0 && (g.xs[0] % 16) == 0 && (g.xs[2] % 16) == 0 &&
                         (g.xs[3] % 16) == 0 && (x_dev == nullptr || ((uintptr_t)x_dev % 16) == 0);
-    pl->pack_x = !direct;
-    pl->pack_done = false;
-    pl->register_loads = false;
     // output channels per tile: 128, 192 or 256 (the smallest that covers
     // K, so that no MMA column is wasted on 129..192 channels)
     pl->n_tile = g.K > 192 ? 256 : (g.K > 128 ? 192 : 128);
+    // an image that is not channels-last is read in place by the NCHW-row
+    // variants (128- and 192-column tiles) where they fit, else copied to
+    // channels-last first
+    pl->nchw_rows = !direct && !register_loads && nchw_rows_ok && pl->n_tile <= 192 && nchw_rows_fit(g, x_dev);
+    pl->pack_x = !direct && !pl->nchw_rows;
+    pl->pack_done = false;
+    pl->register_loads = register_loads;
     pl->c16 = (g.C + 15) / 16 * 16;
     pl->c_steps = (g.C + KS - 1) / KS;
     pl->k_steps = g.R * g.S * pl->c_steps;
@@ -1727,6 +1922,7 @@ static PackFilterJob pack_job(const ConvGeom &g, const IgemmPlan &pl, const int8
     j.k_steps = (int32_t)pl.k_steps;
     j.n_tiles = (int32_t)pl.n_tiles;
     j.nt_rows = (int32_t)pl.n_tile;
+    j.kperm = pl.nchw_rows ? 1 : 0;
     j.wp = wp;
     return j;
 }
@@ -1782,7 +1978,7 @@ PFN_cuTensorMapReplaceAddress_v12000 address_replacer() {
     return reinterpret_cast<PFN_cuTensorMapReplaceAddress_v12000>(fn.load());
 }
 
-enum Variant { V_REG128, V_REG192, V_REG256, V_TMEM128, V_TMEM192, V_TMA256, V_RESB256 };
+enum Variant { V_REG128, V_REG192, V_REG256, V_TMEM128, V_TMEM192, V_TMA256, V_RESB256, V_NCHW128, V_NCHW192 };
 
 // Everything a launch of the convolution kernel needs that does not change
 // with the buffers' addresses: the kernel arguments (tensor maps encoded for
@@ -1815,7 +2011,7 @@ LaunchKey make_key(const ConvGeom &g, const IgemmPlan &pl, int dev, int align) {
     for (int i = 0; i < 4; ++i) { put(g.xs[i]); put(g.ws[i]); put(g.ys[i]); }
     put(g.pad_h); put(g.pad_w); put(g.str_h); put(g.str_w); put(g.dil_h); put(g.dil_w);
     put(g.mode); put(g.bias); put(g.relu); put(g.out_int8); put(g.out_shift);
-    put(pl.pack_x); put(pl.register_loads); put(pl.resident_b); put(pl.n_tile); put(pl.c16); put(pl.c_steps);
+    put(pl.pack_x); put(pl.nchw_rows); put(pl.register_loads); put(pl.resident_b); put(pl.n_tile); put(pl.c16); put(pl.c_steps);
     put(pl.k_steps); put(pl.n_tiles); put(pl.m_tiles); put((int64_t)pl.wpack_bytes); put((int64_t)pl.xpack_bytes);
     put(pl.full_units); put(pl.splits); put(pl.num_units); put(pl.grid); put((int64_t)pl.tail_part_off);
     put((int64_t)pl.tail_part_bytes); put((int64_t)pl.xpack_off); put((int64_t)pl.workspace_bytes);
@@ -1944,7 +2140,7 @@ conv_status build_launch(const ConvGeom &g0, const IgemmPlan &pl, const int8_t *
     // a 1x1 filter at stride 1 without padding over dense pixel rows reads
     // image pixel m for output pixel m: plain 2-D boxes instead of im2col
     const int64_t c_dim = pl.pack_x ? pl.c16 : g.C;
-    a.a_rows = (g.R == 1 && g.S == 1 && g.str_h == 1 && g.str_w == 1 && g.pad_h == 0 && g.pad_w == 0 &&
+    a.a_rows = (!pl.nchw_rows && g.R == 1 && g.S == 1 && g.str_h == 1 && g.str_w == 1 && g.pad_h == 0 && g.pad_w == 0 &&
                 g.P == g.H && g.Q == g.W && a.xs_h == g.W * a.xs_w && a.xs_n == g.H * a.xs_h)
                    ? 1
                    : 0;
@@ -1952,7 +2148,11 @@ conv_status build_launch(const ConvGeom &g0, const IgemmPlan &pl, const int8_t *
     // their staging loads are 64-byte swizzled for the converters' row reads
     const bool tmem_a = pl.n_tile <= 192;
     bool tma = false;
-    if (!pl.register_loads) {
+    if (pl.nchw_rows) {
+        // the planner checked everything the map needs
+        if (!encode_nchw_rows_map(g, x, &a.tmap_x)) return CONV_ERR_CUDA;
+        tma = true;
+    } else if (!pl.register_loads) {
         if (a.a_rows) tma = encode_rows_map(g, a.x, a.xs_w, c_dim, tmem_a, &a.tmap_x);
         if (!tma) {
             a.a_rows = 0;
@@ -1969,7 +2169,9 @@ conv_status build_launch(const ConvGeom &g0, const IgemmPlan &pl, const int8_t *
     // memory; 256-column tiles keep it in shared memory, with the filter
     // resident when it fits
     L->tma = tma;
-    if (tma && tmem_a)
+    if (pl.nchw_rows)
+        L->variant = pl.n_tile == 128 ? V_NCHW128 : V_NCHW192;
+    else if (tma && tmem_a)
         L->variant = pl.n_tile == 128 ? V_TMEM128 : V_TMEM192;
     else if (tma && pl.resident_b)
         L->variant = V_RESB256;
@@ -2062,14 +2264,14 @@ conv_status prepare_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t 
     return CONV_OK;
 }
 
-template <int NT, bool kTma, bool kResB = false, bool kTmemA = false>
+template <int NT, bool kTma, bool kResB = false, bool kTmemA = false, bool kNchw = false>
 conv_status launch_conv_group(const IgemmGroup &grp, int grid, cudaStream_t st) {
-    using Cfg = TileCfg<NT, kTma, kResB, kTmemA>;
+    using Cfg = TileCfg<NT, kTma, kResB, kTmemA, kNchw>;
     static std::atomic<bool> attr_set[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !attr_set[dev].load()) {
-        if (cudaFuncSetAttribute(igemm_conv_group_kernel<NT, kTma, kResB, kTmemA>,
+        if (cudaFuncSetAttribute(igemm_conv_group_kernel<NT, kTma, kResB, kTmemA, kNchw>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
             return CONV_ERR_CUDA;
         if (dev >= 0 && dev < 64) attr_set[dev].store(true);
@@ -2084,7 +2286,7 @@ conv_status launch_conv_group(const IgemmGroup &grp, int grid, cudaStream_t st) 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, igemm_conv_group_kernel<NT, kTma, kResB, kTmemA>, grp) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, igemm_conv_group_kernel<NT, kTma, kResB, kTmemA, kNchw>, grp) != cudaSuccess)
         return CONV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
@@ -2107,7 +2309,8 @@ conv_status igemm_group_launch(int n, const ConvGeom *const *g, const IgemmPlan 
         LaunchPlan L;
         conv_status st = prepare_launch(*g[c], *pl[c], x, y[c], nullptr, static_cast<uint8_t *>(workspace[c]), &L);
         if (st) return st;
-        if (!(L.variant == V_TMEM128 || L.variant == V_TMEM192 || L.variant == V_TMA256 || L.variant == V_RESB256) ||
+        if (!(L.variant == V_TMEM128 || L.variant == V_TMEM192 || L.variant == V_TMA256 || L.variant == V_RESB256 ||
+              L.variant == V_NCHW128 || L.variant == V_NCHW192) ||
             (variant >= 0 && L.variant != variant))
             return CONV_OK;
         variant = L.variant;
@@ -2140,6 +2343,8 @@ conv_status igemm_group_launch(int n, const ConvGeom *const *g, const IgemmPlan 
         case V_TMEM128: rc = launch_conv_group<128, true, false, true>(grp, used, st); break;
         case V_TMEM192: rc = launch_conv_group<192, true, false, true>(grp, used, st); break;
         case V_TMA256: rc = launch_conv_group<256, true>(grp, used, st); break;
+        case V_NCHW128: rc = launch_conv_group<128, true, false, true, true>(grp, used, st); break;
+        case V_NCHW192: rc = launch_conv_group<192, true, false, true, true>(grp, used, st); break;
         default: rc = launch_conv_group<256, true, true>(grp, used, st); break;
     }
     if (rc == CONV_OK) *launched = true;
@@ -2168,6 +2373,8 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
         case V_RESB256: rc = launch_conv<256, true, true>(a, grid, st); break;
         case V_TMA256: rc = launch_conv<256, true>(a, grid, st); break;
         case V_TMEM192: rc = launch_conv<192, true, false, true>(a, grid, st); break;
+        case V_NCHW128: rc = launch_conv<128, true, false, true, true>(a, grid, st); break;
+        case V_NCHW192: rc = launch_conv<192, true, false, true, true>(a, grid, st); break;
         case V_REG256: rc = launch_conv<256, false>(a, grid, st); break;
         case V_REG192: rc = launch_conv<192, false>(a, grid, st); break;
         default: rc = launch_conv<128, false>(a, grid, st); break;

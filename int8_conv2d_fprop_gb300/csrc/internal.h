@@ -67,6 +67,7 @@ constexpr int kIgemmKStep = 64;
 
 struct IgemmPlan {
     bool pack_x;            // image must be copied to channels-last first
+    bool nchw_rows;         // image read in place from its NCHW rows (128- and 192-column tiles)
     bool pack_done;         // ... and the copy at xpack_off is made by the caller (igemm_pack_image_launch)
     bool register_loads;    // gather the image with global loads, not TMA im2col
     bool resident_b;        // the whole repacked filter stays in shared memory (TMA path)
@@ -106,7 +107,10 @@ PlanKey make_plan_key(const conv_tensor_desc *x, const conv_tensor_desc *w, cons
 void dgrad_cache_clear();
 
 bool igemm_supported(const ConvGeom &g);
-void igemm_plan(const ConvGeom &g, const void *x_dev, IgemmPlan *pl);
+// register_loads: gather the image with global loads; nchw_rows_ok: the
+// NCHW-row variants may be chosen.
+void igemm_plan(const ConvGeom &g, const void *x_dev, IgemmPlan *pl, bool register_loads = false,
+                bool nchw_rows_ok = true);
 // Repacks the filter into the first pl.wpack_bytes of the workspace.
 conv_status igemm_pack_filter_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *w, void *workspace,
                                      void *stream);

@@ -28,8 +28,12 @@ def ic():
 @pytest.mark.parametrize("cfg", [
     synth.ConvConfig("cache_3x3_nt256", 2, 64, 20, 18, 256, 3, 3, pre=(1, 1), post=(1, 1), bias=True, seed=81),
     synth.ConvConfig("cache_1x1_tmem", 4, 128, 14, 14, 96, 1, 1, relu=True, seed=82),
-    synth.ConvConfig("cache_nchw_packed", 2, 48, 16, 16, 150, 3, 1, stride=(2, 1), pre=(1, 0), post=(1, 0),
+    # NCHW image read in place (16-byte rows): the cached 4-D row map is re-targeted
+    synth.ConvConfig("cache_nchw_rows", 2, 48, 16, 16, 150, 3, 1, stride=(2, 1), pre=(1, 0), post=(1, 0),
                      x_layout="NCHW", w_layout="KCRS", y_layout="NCHW", seed=83),
+    # NCHW image copied to channels-last (20-byte rows): the map of the copy
+    synth.ConvConfig("cache_nchw_packed", 2, 48, 16, 20, 150, 3, 1, stride=(2, 1), pre=(1, 0), post=(1, 0),
+                     x_layout="NCHW", w_layout="KCRS", y_layout="NCHW", seed=84),
 ], ids=lambda c: c.name)
 def test_cached_calls_on_other_buffers(ic, cfg):
     x, w, b = synth.make_inputs(cfg)
@@ -75,13 +79,12 @@ def test_cached_calls_on_other_buffers(ic, cfg):
     assert after["launch_misses"] - before["launch_misses"] == 1
     assert after["launch_hits"] - before["launch_hits"] == calls - 1
     # an image pointer that is not 16-byte aligned is another key (and, for a
-    # channels-last image, the repacked path): still exact
+    # channels-last image or an NCHW image read in place, the path that
+    # copies the image to channels-last first): still exact
     xb = torch.zeros(xf.size + 64, dtype=torch.int8, device="cuda")
     xb[8:8 + xf.size].copy_(torch.from_numpy(xf))
-    need2 = need
-    if cfg.x_layout == "NHWC":
-        # the aligned-pointer workspace size does not cover the image copy
-        need2 = max(need, xf.size + need + 4096)
+    # the aligned-pointer workspace size need not cover the image copy
+    need2 = need + cfg.N * cfg.H * cfg.W * ((cfg.C + 15) // 16 * 16) + 4096
     wsb = torch.empty(need2 + 256, dtype=torch.uint8, device="cuda")
     yb = torch.full((ysz,), -1, dtype=torch.int32, device="cuda")
     st = ic.conv_fprop_raw(xd, xb.data_ptr() + 8, wd, wt.data_ptr(), yd, yb.data_ptr(),

@@ -69,6 +69,15 @@ CASES = [
     # classes' output channels are the forward image's C)
     G("s2_c160_group192", 2, 160, 21, 18, 48, 3, 3, (1, 1), (1, 1), stride=(2, 2), tensor=True),
     G("s2_c256_group256_conv", 1, 256, 17, 20, 40, 3, 2, (1, 0), (0, 1), stride=(2, 2), mode=1, tensor=True),
+    # NCHW dY read in place (rows of 32 bytes, class windows at offsets that
+    # are multiples of 4): one class; and a stride-2 1x1 filter whose one
+    # tapped class writes every other dX pixel
+    G("s1_nchw_rows_dy", 2, 48, 12, 32, 64, 3, 1, (1, 0), (1, 0), layout="NCHW", tensor=True),
+    G("s2_1x1_nchw_rows_dy", 1, 64, 32, 64, 32, 1, 1, stride=(2, 2), layout="NCHW", tensor=True),
+    # stride 2, 3x3, NCHW: some classes could read dY in place and some not;
+    # all of them then read one shared channels-last copy
+    G("s2_nchw_mixed_classes", 2, 32, 16, 32, 48, 3, 3, (1, 1), (1, 1), stride=(2, 2), layout="NCHW",
+      tensor=True),
 ]
 
 

@@ -262,9 +262,11 @@ def test_more_tiles_than_sms_int8_output(ic):
 ], ids=lambda c: c.name)
 def test_nchw_image_plane_copy(ic, case, c_pad, n_pad):
     """Images whose channels each hold a contiguous H x W plane (H*W a
-    multiple of 16) are copied to channels-last by a shared-memory
-    transpose before the tensor-core kernel; channel and image strides padded
-    beyond the plane must be honoured."""
+    multiple of 16) are either read in place (whole image rows by TMA, when
+    the rows and the windows allow it: the 1x1 case here) or copied to
+    channels-last by a shared-memory transpose before the tensor-core
+    kernel; channel and image strides padded beyond the plane must be
+    honoured."""
     cfg = case
     x, w, b = synth.make_inputs(cfg)
     N, C, H, W = cfg.x_dims
@@ -285,6 +287,58 @@ def test_nchw_image_plane_copy(ic, case, c_pad, n_pad):
     ref = oracle.conv_fprop(xflat, cfg.x_dims, xs, wf, cfg.w_dims, ws, cfg.pre, cfg.post, cfg.stride,
                             cfg.dilation, cfg.mode, b, cfg.relu)
     _assert_equal(y.cpu().numpy(), ref, f"{cfg.name} c_pad {c_pad} n_pad {n_pad}")
+
+
+def _nchw_rows_cases():
+    C = synth.ConvConfig
+    return [
+        # the 7x1 dilated workload's shape at batch 3: a 128-pixel tile spans
+        # two output rows (Q = 96), ragged pixel tail, convolution mode,
+        # 192-column tiles, channel-major output
+        C("rows_7x1_dilated_conv", 3, 128, 28, 96, 192, 7, 1, stride=(2, 1), dilation=(2, 1), pre=(6, 0),
+          post=(5, 0), mode=1, x_layout="NCHW", w_layout="KCRS", y_layout="NCHW", seed=81),
+        # 3x3, dilation 4 along W (tap offsets 0, 4, 8 around pre-padding 4),
+        # 80 channels (the second channel step half past C), 128-column
+        # tiles, pixel-major output, bias and ReLU
+        C("rows_3x3_dilw4_c80", 2, 80, 20, 32, 96, 3, 3, dilation=(1, 4), pre=(1, 4), post=(1, 4), bias=True,
+          relu=True, x_layout="NCHW", w_layout="KCRS", y_layout="NHWC", seed=82),
+        # 16-byte image rows: a tile spans eight output rows
+        C("rows_w16_1x3", 4, 64, 12, 16, 128, 1, 3, dilation=(1, 4), pre=(0, 4), post=(0, 4), x_layout="NCHW",
+          w_layout="KRSC", y_layout="NCHW", seed=83),
+        # five tiles, 70 k-steps: each tile cut into runs whose int32 sums the
+        # reduction kernel adds
+        C("rows_cut_tiles", 1, 640, 20, 32, 64, 7, 1, pre=(3, 0), post=(3, 0), x_layout="NCHW", w_layout="KCRS",
+          y_layout="NHWC", seed=84),
+    ]
+
+
+@pytest.mark.parametrize("case", _nchw_rows_cases(), ids=lambda c: c.name)
+def test_nchw_rows_read_in_place(ic, case):
+    """NCHW images with rows of at most 192 bytes (a multiple of 16), stride 1
+    along W and tap offsets that are multiples of 4 are read in place: each
+    k-step loads whole image rows of 64 channels, and the converters
+    transpose them into the tensor-memory image stage (pixels permuted within
+    each 32-lane quadrant, channels within each 16) with the filter repacked
+    in the same channel order.  The call launches no image copy."""
+    xd = ic.TensorDesc.make(ic.CONV_INT8, case.x_dims, synth.packed_strides(case.x_dims, case.x_layout),
+                            int(np.prod(case.x_dims)))
+    wd = ic.TensorDesc.make(ic.CONV_INT8, case.w_dims, synth.packed_strides(case.w_dims, case.w_layout),
+                            int(np.prod(case.w_dims)))
+    yd = ic.TensorDesc.make(ic.CONV_INT32, case.y_dims, synth.packed_strides(case.y_dims, case.y_layout),
+                            int(np.prod(case.y_dims)) * 4)
+    p = ic.Params.make(case.pre, case.post, case.stride, case.dilation, case.mode, case.bias, case.relu)
+    # filter repack and convolution (plus the reduction of the cut tiles)
+    assert ic.kernel_count(xd, wd, yd, p) == (3 if case.name == "rows_cut_tiles" else 2)
+    got, ref = _run_both(ic, case)
+    _assert_equal(got, ref, case.name)
+
+
+def test_nchw_rows_int8_output(ic):
+    """The in-place NCHW path with the int8 requantising epilogue, on 128-
+    and 192-column tiles."""
+    for case in _nchw_rows_cases()[:2]:
+        got, ref = _run_both(ic, case, out_shift=10)
+        _assert_equal(got, ref, case.name + " int8 out")
 
 
 # ------------------------------------------------------------------ exactness

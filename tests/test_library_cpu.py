@@ -201,11 +201,11 @@ def test_planner_choices_and_workspace(ic):
         algo[name] = ic.plan(xd, wd, yd, p)
         ws[name] = ic.workspace_size(xd, wd, yd, p)
         kernels[name] = ic.kernel_count(xd, wd, yd, p)
-    # kernels per call: one direct kernel; filter repack + convolution, plus
-    # the channels-last copy of C5's NCHW image (no GPU here: one SM, so no
-    # call cuts its tiles)
+    # kernels per call: one direct kernel; filter repack + convolution (C5's
+    # NCHW image is read in place, whole rows per k-step; no GPU here: one
+    # SM, so no call cuts its tiles)
     assert kernels == {"c1_tiny_nchw": 1, "p4_shape": 1, "c2_s2_nhwc": 2, "c3_3x3_large": 2,
-                       "c4_1x1_bias_relu": 2, "c5_7x1_dilated_conv": 3}
+                       "c4_1x1_bias_relu": 2, "c5_7x1_dilated_conv": 2}
     # an empty batch launches nothing
     cfg = synth.CONFIGS["c3_3x3_large"]
     xd = ic.TensorDesc.make(ic.CONV_INT8, (0, 256, 56, 56), (56 * 56 * 256, 1, 56 * 256, 256), 0)
@@ -220,10 +220,8 @@ def test_planner_choices_and_workspace(ic):
     # C3: 2 n-tiles x 36 k-steps x 16 KB of f16 filter blocks, no image copy
     assert ws["c3_3x3_large"] == 2 * 36 * 16384
     # C5 (K = 192: one 192-column tile, 14 k-steps of 192 rows x 128 bytes)
-    # has an NCHW image: a channels-last copy is added, of the even rows only
-    # (stride 2 and dilation 2 along H, pre-padding 6: every row read is even)
-    c5 = synth.CONFIGS["c5_7x1_dilated_conv"]
-    assert ws["c5_7x1_dilated_conv"] == 14 * 192 * 128 + c5.N * (c5.H // 2) * c5.W * c5.C
+    # reads its NCHW image in place: the workspace holds the filter only
+    assert ws["c5_7x1_dilated_conv"] == 14 * 192 * 128
     # forced algorithms are honoured
     xd, wd, yd, p = _descs(ic, synth.CONFIGS["c2_s2_nhwc"])
     for a in (ic.ALGO_DIRECT_GENERIC, ic.ALGO_DIRECT_DP4A, ic.ALGO_IMPLICIT_GEMM,
@@ -234,6 +232,42 @@ def test_planner_choices_and_workspace(ic):
         assert (ic.workspace_size(xd, wd, yd, p) > 0) == tensor_core
     p.algo = 5
     assert ic.validate(xd, wd, yd, p) == _code(ic, "CONV_ERR_BAD_PARAM")
+
+
+@pytest.mark.parametrize("W,pre_w,dil_w,S,K,stride_w,in_place", [
+    (96, 0, 1, 1, 192, 1, True),     # the 7x1 workload's rows: two output rows per tile
+    (64, 0, 1, 1, 128, 1, True),
+    (32, 4, 4, 3, 96, 1, True),      # tap offsets 0, 4, 8 around pre-padding 4
+    (16, 0, 1, 1, 128, 1, True),     # 16-byte rows, eight per tile
+    (20, 0, 1, 1, 128, 1, False),    # rows not a multiple of 16 bytes
+    (208, 0, 1, 1, 128, 1, False),   # rows longer than 192 bytes
+    (112, 0, 1, 1, 128, 1, False),   # a tile's two rows exceed the 192-byte slot row
+    (96, 1, 1, 3, 128, 1, False),    # tap offsets not multiples of 4
+    (96, 0, 2, 3, 128, 1, False),    # dilation 2 along W with three taps
+    (96, 0, 1, 1, 256, 1, False),    # 256-column tiles keep the channels-last copy
+    (96, 0, 1, 1, 128, 2, False),    # stride 2 along W
+])
+def test_nchw_rows_planner_rules(ic, W, pre_w, dil_w, S, K, stride_w, in_place):
+    """An NCHW image is read in place (no channels-last copy: two kernels,
+    the workspace holds only the filter blocks) exactly when its rows are a
+    multiple of 16 bytes and at most 192, the rows of one 128-pixel tile fit
+    192 bytes per channel, the stride along W is 1, Q and every tap offset
+    s*dil_w - pre_w are multiples of 4, and the tile has at most 192
+    columns; otherwise the image is copied to channels-last first."""
+    N, C, H = 2, 64, 10
+    Q = (W + 2 * pre_w - dil_w * (S - 1) - 1) // stride_w + 1
+    xd = ic.TensorDesc.packed(ic.CONV_INT8, (N, C, H, W), "NCHW")
+    wd = ic.TensorDesc.packed(ic.CONV_INT8, (K, C, 1, S), "KCRS")
+    yd = ic.TensorDesc.packed(ic.CONV_INT32, (N, K, H, Q), "NHWC")
+    p = ic.Params.make((0, pre_w), (0, pre_w), (1, stride_w), (1, dil_w))
+    n_tile = 128 if K <= 128 else (192 if K <= 192 else 256)
+    filt = S * n_tile * 128  # S k-steps (one channel step) of n_tile rows x 64 f16
+    copy = (N * H * W * 64 + 255) // 256 * 256
+    assert ic.kernel_count(xd, wd, yd, p) == (2 if in_place else 3)
+    assert ic.workspace_size(xd, wd, yd, p) == filt + (0 if in_place else copy)
+    # gathering with global loads always takes the copy
+    pg = ic.Params.make((0, pre_w), (0, pre_w), (1, stride_w), (1, dil_w), algo=ic.ALGO_IMPLICIT_GEMM_GLOBAL_LOADS)
+    assert ic.workspace_size(xd, wd, yd, pg) == filt + copy
 
 
 def test_host_buffer_size_covers_chunks(ic):
