@@ -35,6 +35,14 @@
 //    filter ring and the staging ring (NT = 128: six filter stages and eight
 //    staging buffers; NT = 192: four and twelve); the 128-column epilogue
 //    stores 32 columns per TMA store.
+//  * NT = 128 and NT = 192 over an NCHW image (rows of at most 192 bytes,
+//    stride 1 along W, tap offsets along W multiples of 4): the image is
+//    read in place.  Each k-step loads, for every output row its tile's
+//    pixels lie on, the whole image row of 64 channels (a 4-D TMA box
+//    {W, 1, 64, 1}); the converters transpose while converting and write
+//    tensor memory with tcgen05.st.16x256b, which permutes the tile's pixels
+//    within each 32-lane quadrant (the epilogue follows) and the channels
+//    within each 16 (the filter repack follows).
 //  * global loads (fallback when a TMA map cannot express the call):
 //    warpgroup 0 threads each own one pixel row, gather 64 channels of one
 //    tap with 16-byte loads one item ahead (address formed from stride,
@@ -49,11 +57,12 @@
 // Work comes in units: whole tiles round by round, or runs of k-steps of cut
 // tiles (few tiles with long reductions; a short partial last round) whose
 // int32 sums igemm_split_reduce_kernel adds.
-// Images that are not channels-last with 16-byte channel runs are copied to
+// Other images that are not channels-last with 16-byte channel runs are copied to
 // channels-last first (igemm_pack_image_planes_kernel for NCHW planes,
 // igemm_pack_image_kernel for any strides), keeping only the rows that
 // the windows read when stride and dilation skip rows.
-// Registers are moved from warpgroups 0-1 to the epilogue with setmaxnreg.
+// Registers are moved from warpgroups 0-1 to the epilogue with setmaxnreg
+// (the tensor-memory variants' converters keep 96, their issuers 64).
 // Every wait is bounded in time; on expiry the CTA records
 // CONV_ERR_DEVICE_TIMEOUT, stops, lets issued copies and MMAs finish and frees
 // its tensor memory.
@@ -88,6 +97,13 @@ constexpr int NUM_EPI_THREADS = 256;
 constexpr int PRODUCER_REGS = 80;
 constexpr int EPILOGUE_REGS = 176;
 static_assert(2 * 128 * PRODUCER_REGS + 2 * 128 * EPILOGUE_REGS <= 65536, "register split exceeds the launch");
+// Tensor-memory variants: the converters (warpgroup 0) keep more registers,
+// so that all of a k-step's shared loads are in flight at once, and the
+// single-thread issuers of warpgroup 1 fewer.
+constexpr int TMEM_CONV_REGS = 96;
+constexpr int TMEM_ISSUE_REGS = 64;
+static_assert(128 * TMEM_CONV_REGS + 128 * TMEM_ISSUE_REGS + 2 * 128 * EPILOGUE_REGS <= 65536,
+              "register split exceeds the launch");
 constexpr int PREFETCH = 1;  // register path: items in flight ahead of the one being stored
 constexpr int STG_BYTES = MT * KS;  // one int8 im2col tile: 128 pixels x 64 channels
 constexpr int A_ISSUER_WARP = 5;    // TMA path: issues the im2col loads
@@ -555,7 +571,7 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
         // 16i + u + 8 and 16i + u + 12: within each 16 channels the K order
         // swaps the two 2-bit digits of the channel index, and the filter
         // repack writes the filter blocks in the same order.
-        ptx::setmaxnreg_dec<PRODUCER_REGS>();
+        ptx::setmaxnreg_dec<TMEM_CONV_REGS>();
         const int jq = lane >> 2, u = lane & 3;
         const uint32_t lanes_lo = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)Cfg::TMEM_A_COL;
         const uint32_t lanes_hi = lanes_lo + (16u << 16);
@@ -657,7 +673,7 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
         // by the TMA 64-byte swizzle: each 8 rows cover all banks) and writes
         // the 32 f16 pairs to tensor-memory lane t (warp w owns lanes
         // 32w..32w+31), column j holding channels 2j and 2j+1.
-        ptx::setmaxnreg_dec<PRODUCER_REGS>();
+        ptx::setmaxnreg_dec<TMEM_CONV_REGS>();
         const int row = threadIdx.x;
         const uint32_t sw = (uint32_t)((row >> 1) & 3);
         const uint32_t lane_col0 = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)Cfg::TMEM_A_COL;
@@ -794,7 +810,7 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
         if (threadIdx.x == 0 && *abort_flag) drain_ring(ctl->full, ST, b_issued, DRAIN_LIMIT_NS, a.status);
     } else if (warp < FIRST_EPI_WARP) {
         // ------------------------------------------------------------ MMA issuer
-        ptx::setmaxnreg_dec<PRODUCER_REGS>();
+        ptx::setmaxnreg_dec<kTmemA ? TMEM_ISSUE_REGS : PRODUCER_REGS>();
         if (warp == MMA_WARP && lane == 0) {
             constexpr uint32_t idesc = ptx::idesc_f16_f32(MT, NT);
             // stage s descriptors = stage 0 descriptors + s * (stage bytes >> 4)
