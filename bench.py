@@ -216,8 +216,10 @@ def rotating_sets(cfg) -> int:
 
 class DeviceWorkload:
     """One workload resident on a device, called the way the benchmark times
-    it: conv_fprop_pack_filter (the filter repack) then conv_fprop_prepacked
-    (the convolution) through the C ABI, over ``nsets`` image/output sets."""
+    it, through the C ABI over ``nsets`` image/output sets: a step is one
+    conv_fprop call (filter repack and convolution); pack() and conv() are
+    its two halves as separate calls (conv_fprop_pack_filter,
+    conv_fprop_prepacked), used to time the convolution alone."""
 
     def __init__(self, ic, cfg, dev, nsets: int = 1):
         import torch
@@ -256,8 +258,12 @@ class DeviceWorkload:
             raise self.ic.ConvError(st, "conv")
 
     def step(self, i: int, sh: int) -> None:
-        self.pack(sh)
-        self.conv(i, sh)
+        s = i % self.nsets
+        st = self.ic.conv_fprop_raw(self.xd, self.x_dev[s].data_ptr(), self.wd, self.w_dev.data_ptr(), self.yd,
+                                    self.y_dev[s].data_ptr(), self.bias_ptr, self.p, self.work.data_ptr(),
+                                    self.ws_bytes, sh)
+        if st:
+            raise self.ic.ConvError(st, "conv_fprop")
 
     def output(self, i: int = 0) -> np.ndarray:
         """Logical [N,K,P,Q] int32 output of set i (after a synchronize)."""

@@ -312,10 +312,11 @@ conv_status prepare_call(const conv_tensor_desc *x, const int8_t *x_dev, const c
 }
 
 conv_status run_main(const ConvGeom &g, int algo, const IgemmPlan &pl, const int8_t *x_dev, const int8_t *w_dev,
-                     void *y_dev, const int32_t *bias_dev, void *workspace, void *stream) {
+                     void *y_dev, const int32_t *bias_dev, void *workspace, void *stream,
+                     bool after_own_repack = false) {
     switch (algo) {
         case CONV_ALGO_IMPLICIT_GEMM:
-            return igemm_main_launch(g, pl, x_dev, y_dev, bias_dev, workspace, stream);
+            return igemm_main_launch(g, pl, x_dev, y_dev, bias_dev, workspace, stream, after_own_repack);
         case CONV_ALGO_DIRECT_DP4A:
             return dp4a_launch(g, x_dev, w_dev, y_dev, bias_dev, stream);
         default:
@@ -337,7 +338,7 @@ conv_status conv_fprop(const conv_tensor_desc *x, const int8_t *x_dev, const con
     if (st || none) return st;
     if (algo == CONV_ALGO_IMPLICIT_GEMM && (st = igemm_pack_filter_launch(g, pl, w_dev, workspace, stream)))
         return st;
-    return run_main(g, algo, pl, x_dev, w_dev, y_dev, bias_dev, workspace, stream);
+    return run_main(g, algo, pl, x_dev, w_dev, y_dev, bias_dev, workspace, stream, true);
 }
 
 conv_status conv_fprop_pack_filter(const conv_tensor_desc *x, const conv_tensor_desc *w, const int8_t *w_dev,

@@ -517,7 +517,7 @@ conv_status conv_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const c
             }
             void *cw = static_cast<uint8_t *>(workspace) + c.ws_off;
             conv_status r = packed ? CONV_OK : igemm_pack_filter_launch(c.g, c.pl, w_dev + c.w_origin, cw, cs);
-            if (r == CONV_OK) r = igemm_main_launch(c.g, c.pl, dy_dev, y, nullptr, cw, cs);
+            if (r == CONV_OK) r = igemm_main_launch(c.g, c.pl, dy_dev, y, nullptr, cw, cs, !packed);
             return r;
         };
         if (ph.empty()) return CONV_OK;
@@ -574,7 +574,8 @@ conv_status conv_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const c
                 ++n;
             }
             bool launched = false;
-            if (fits && n >= 2 && (st = igemm_group_launch(n, gs, ps, dy_dev, ys, wk, s, &launched))) return st;
+            // (right behind the repack launch above on the caller's stream)
+            if (fits && n >= 2 && (st = igemm_group_launch(n, gs, ps, dy_dev, ys, wk, s, &launched, true))) return st;
             if (launched) {
                 for (const DgradPhase &c : ph)
                     if (!c.taps && (st = run_class(c, s, true))) return st;
@@ -644,7 +645,7 @@ conv_status conv_wgrad(const conv_tensor_desc *x, const int8_t *x_dev, const con
             overlaps(workspace, pl.workspace_bytes, dy_dev, (uint64_t)desc_extent_elems(dy)))
             return CONV_ERR_OVERLAP;
         if ((st = igemm_pack_filter_launch(g, pl, dy_dev, workspace, stream))) return st;
-        return igemm_main_launch(g, pl, x_dev, dw_dev + origin, nullptr, workspace, stream);
+        return igemm_main_launch(g, pl, x_dev, dw_dev + origin, nullptr, workspace, stream, true);
     }
     GradArgs a = grad_args(x, dw, dy, p);
     a.a = x_dev;

@@ -304,6 +304,11 @@ struct IgemmArgs {
     int32_t y_tma;       // TMA stores: 1 pixel-major with contiguous channels, 2 channel-major
                          // (each channel's P*Q pixels contiguous, P*Q a multiple of 32)
     FastDiv fd_nt, fd_pq, fd_q, fd_cs, fd_s;  // by n_tiles, P*Q, Q, c_steps, S
+    // 1: launched right behind this call's own filter repack (an ordinary
+    // launch, so every earlier kernel of the stream had completed when it
+    // started): the image is final, and the TMA image loads need not wait
+    // for the repack to finish (only the filter copies do)
+    int32_t early_image;
     uint64_t wait_limit_ns;
     int *status;         // device status word
 };
@@ -549,7 +554,10 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
     // waits for this grid before touching memory.  (With cut tiles the
     // reduction follows, and it starts when this grid ends, so that the next
     // convolution's CTAs cannot take SMs from it.)
-    ptx::grid_dependency_wait();
+    // (behind this call's own filter repack, the image-load issuers and the
+    // converters, which touch no global memory, start at once)
+    const bool image_role = warp < 4 || warp == A_ISSUER_WARP || warp == A_ISSUER_WARP2;
+    if (!(kTma && a.early_image && image_role)) ptx::grid_dependency_wait();
     if (a.splits <= 1) ptx::launch_dependents();
 
     if (warp < 4 && kNchw) {
@@ -2310,7 +2318,8 @@ conv_status launch_conv_group(const IgemmGroup &grp, int grid, cudaStream_t st) 
 }  // namespace
 
 conv_status igemm_group_launch(int n, const ConvGeom *const *g, const IgemmPlan *const *pl, const int8_t *x,
-                               void *const *y, void *const *workspace, void *stream, bool *launched) {
+                               void *const *y, void *const *workspace, void *stream, bool *launched,
+                               bool after_own_repack) {
     *launched = false;
     if (n < 2 || n > kMaxGroup) return CONV_OK;
     static IgemmGroup grp_zero;  // (zero-filled template: IgemmArgs has no constructor)
@@ -2331,6 +2340,7 @@ conv_status igemm_group_launch(int n, const ConvGeom *const *g, const IgemmPlan 
             return CONV_OK;
         variant = L.variant;
         grp.cls[c] = L.a;
+        grp.cls[c].early_image = after_own_repack && L.tma ? 1 : 0;
         work += pl[c]->num_units * pl[c]->k_steps;
     }
     // CTAs for each convolution in proportion to its work (tiles x k-steps;
@@ -2368,7 +2378,7 @@ conv_status igemm_group_launch(int n, const ConvGeom *const *g, const IgemmPlan 
 }
 
 conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *y,
-                              const int32_t *bias, void *workspace, void *stream) {
+                              const int32_t *bias, void *workspace, void *stream, bool after_own_repack) {
     cudaStream_t st = (cudaStream_t)stream;
     const int sms = device_sm_count();
     uint8_t *wp = static_cast<uint8_t *>(workspace);
@@ -2378,6 +2388,10 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
     if (pst) return pst;
     IgemmArgs &a = L.a;
 
+    // the image loads may start before the filter repack ends only when the
+    // repack is the kernel right before (not an image copy, whose output
+    // they read)
+    a.early_image = after_own_repack && L.tma && !(pl.pack_x && !pl.pack_done) ? 1 : 0;
     if (pl.pack_x && !pl.pack_done) {
         const conv_status pr = igemm_pack_image_launch(g, pl, x, workspace, stream);
         if (pr) return pr;

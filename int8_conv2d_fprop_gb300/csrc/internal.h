@@ -124,17 +124,25 @@ conv_status igemm_pack_filter_group_launch(int n, const ConvGeom *const *g, cons
 // tensor-core kernel, each on its share of the SMs.  Sets *launched = false,
 // launching nothing, when the convolutions cannot share a launch (different
 // kernel variants, cut tiles, an image copy still to make, register loads);
-// the caller then runs them one by one.
+// the caller then runs them one by one.  after_own_repack: the launch
+// directly follows the caller's own filter repack on the stream (see
+// igemm_main_launch).
 constexpr int kIgemmMaxGroup = 4;
 conv_status igemm_group_launch(int n, const ConvGeom *const *g, const IgemmPlan *const *pl, const int8_t *x,
-                               void *const *y, void *const *workspace, void *stream, bool *launched);
+                               void *const *y, void *const *workspace, void *stream, bool *launched,
+                               bool after_own_repack = false);
 // Makes the channels-last copy of the image at pl.xpack_off of the workspace.
 conv_status igemm_pack_image_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *workspace,
                                     void *stream);
 // Runs the convolution from a workspace whose filter part is already packed
 // (copies the image to channels-last first when pl.pack_x).
+// after_own_repack: the caller launched its own filter repack (an ordinary
+// launch, which starts once every earlier kernel of the stream has
+// completed) directly before on the same stream, so the image is final and
+// the kernel's image loads need not wait for the repack to end.
 conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *y,
-                              const int32_t *bias, void *workspace, void *stream);
+                              const int32_t *bias, void *workspace, void *stream,
+                              bool after_own_repack = false);
 
 // Launch-plan cache of the tensor-core kernel (tensor maps re-targeted to
 // each call's buffers): empty it; read its hit and miss counts.
