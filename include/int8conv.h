@@ -166,7 +166,11 @@ conv_status conv_fprop_plan(const conv_tensor_desc *x, const conv_tensor_desc *w
  * the int32 partial sums of tiles whose reduction is cut over several SMs
  * (calls with fewer tiles than SMs and long reductions, or a short partial
  * last round of tiles), plus a channels-last copy of the image when its
- * strides do not allow direct loads).  The caller allocates it, 256-byte
+ * strides allow neither direct channels-last loads nor whole-row loads: an
+ * NCHW-like image, each channel's rows contiguous, is read in place when its
+ * rows are at most 192 bytes (a multiple of 16), the stride along W is 1 and
+ * Q, the pre-padding along W and every tap offset s*dilation_w are multiples
+ * of 4, for K <= 192).  The caller allocates it, 256-byte
  * aligned.  The size assumes a
  * 16-byte-aligned image pointer (as every cudaMalloc or PyTorch allocation
  * is); with a misaligned one the image needs the copy too, and conv_fprop
@@ -323,7 +327,8 @@ conv_status conv_fprop_static_workspace(const conv_tensor_desc *x, const int8_t 
  * stride_w) of dX's pixels, each by the filter taps that reach that class
  * (taken backwards, K and C exchanged) with stride 1, each in its own part of
  * the workspace; the filters of all classes are repacked by one launch on
- * `stream`, a dY that is not channels-last is copied once for all classes,
+ * `stream`, a dY that is neither channels-last nor read in place by rows
+ * (as for conv_fprop's image) is copied once for all classes,
  * and the classes run as one kernel launch on `stream` (each on its share
  * of the SMs) when they use the same kernel variant and cut no tiles;
  * otherwise side by side on up to four library-owned streams forked from
