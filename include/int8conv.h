@@ -180,12 +180,15 @@ conv_status conv_fprop_workspace_size(const conv_tensor_desc *x, const conv_tens
                                       size_t *bytes);
 
 /* Number of kernels conv_fprop launches for this call, under the same
- * assumption of a 16-byte aligned image pointer: 0 for an empty output, 1
- * for the direct kernels; for the implicit GEMM the filter repack, the
- * channels-last image copy when needed, the convolution, and the reduction
- * of cut tiles when the call cuts them.  conv_fprop_pack_filter launches the
- * first of these, conv_fprop_prepacked the rest.  Errors as
- * conv_fprop_validate; CONV_ERR_NULL_PTR if count is NULL. */
+ * assumption of 16-byte aligned image and filter pointers: 0 for an empty
+ * output, 1 for the direct kernels; for the implicit GEMM the filter repack
+ * (none when the 128- or 192-column kernel converts the filter itself: K <=
+ * 192, a channels-last (or copied) image, a filter with contiguous channels
+ * and 16-byte aligned strides), the channels-last image copy when needed,
+ * the convolution, and the reduction of cut tiles when the call cuts them.
+ * (conv_fprop_pack_filter launches the repack, conv_fprop_prepacked the
+ * others, the convolution then reading the repacked filter.)
+ * Errors as conv_fprop_validate; CONV_ERR_NULL_PTR if count is NULL. */
 conv_status conv_fprop_kernel_count(const conv_tensor_desc *x, const conv_tensor_desc *w,
                                     const conv_tensor_desc *y, const conv_fprop_params *p, int32_t *count);
 
@@ -212,7 +215,9 @@ conv_status conv_fprop(const conv_tensor_desc *x, const int8_t *x_dev,
  *   conv_fprop_prepacked runs the convolution from that workspace.
  * Both take the same descriptors and params as conv_fprop and validate them
  * the same way; conv_fprop_prepacked still needs w_dev (the direct kernels
- * read the filter itself).  The workspace contents must come from a
+ * read the filter itself), and its tensor-core kernels always read the
+ * repacked filter, also where conv_fprop would have them convert the filter
+ * themselves.  The workspace contents must come from a
  * conv_fprop_pack_filter call with the same filter, descriptors and params;
  * the library cannot check that.  Calling the two in order on one stream is
  * conv_fprop.

@@ -276,7 +276,7 @@ conv_status conv_fprop_kernel_count(const conv_tensor_desc *x, const conv_tensor
     } else if (algo != CONV_ALGO_IMPLICIT_GEMM) {
         *count = 1;
     } else {
-        *count = 2 + (pl.pack_x ? 1 : 0) + (pl.splits > 1 ? 1 : 0);
+        *count = (igemm_filter_in_kernel(g, pl, nullptr) ? 1 : 2) + (pl.pack_x ? 1 : 0) + (pl.splits > 1 ? 1 : 0);
     }
     return CONV_OK;
 }
@@ -312,11 +312,10 @@ conv_status prepare_call(const conv_tensor_desc *x, const int8_t *x_dev, const c
 }
 
 conv_status run_main(const ConvGeom &g, int algo, const IgemmPlan &pl, const int8_t *x_dev, const int8_t *w_dev,
-                     void *y_dev, const int32_t *bias_dev, void *workspace, void *stream,
-                     bool after_own_repack = false) {
+                     void *y_dev, const int32_t *bias_dev, void *workspace, void *stream, bool repack) {
     switch (algo) {
         case CONV_ALGO_IMPLICIT_GEMM:
-            return igemm_main_launch(g, pl, x_dev, y_dev, bias_dev, workspace, stream, after_own_repack);
+            return igemm_main_launch(g, pl, x_dev, w_dev, y_dev, bias_dev, workspace, stream, repack);
         case CONV_ALGO_DIRECT_DP4A:
             return dp4a_launch(g, x_dev, w_dev, y_dev, bias_dev, stream);
         default:
@@ -336,8 +335,7 @@ conv_status conv_fprop(const conv_tensor_desc *x, const int8_t *x_dev, const con
     conv_status st = prepare_call(x, x_dev, w, w_dev, y, y_dev, bias_dev, p, workspace, workspace_bytes, &g,
                                   &algo, &pl, &none);
     if (st || none) return st;
-    if (algo == CONV_ALGO_IMPLICIT_GEMM && (st = igemm_pack_filter_launch(g, pl, w_dev, workspace, stream)))
-        return st;
+    // (the filter is repacked first unless the kernel converts it itself)
     return run_main(g, algo, pl, x_dev, w_dev, y_dev, bias_dev, workspace, stream, true);
 }
 
@@ -369,7 +367,7 @@ conv_status conv_fprop_prepacked(const conv_tensor_desc *x, const int8_t *x_dev,
     conv_status st = prepare_call(x, x_dev, w, w_dev, y, y_dev, bias_dev, p, workspace, workspace_bytes, &g,
                                   &algo, &pl, &none);
     if (st || none) return st;
-    return run_main(g, algo, pl, x_dev, w_dev, y_dev, bias_dev, workspace, stream);
+    return run_main(g, algo, pl, x_dev, w_dev, y_dev, bias_dev, workspace, stream, false);
 }
 
 conv_status conv_device_status(void *stream) {

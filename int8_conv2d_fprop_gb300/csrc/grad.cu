@@ -516,9 +516,7 @@ conv_status conv_dgrad(const conv_tensor_desc *dy, const int8_t *dy_dev, const c
                 return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
             }
             void *cw = static_cast<uint8_t *>(workspace) + c.ws_off;
-            conv_status r = packed ? CONV_OK : igemm_pack_filter_launch(c.g, c.pl, w_dev + c.w_origin, cw, cs);
-            if (r == CONV_OK) r = igemm_main_launch(c.g, c.pl, dy_dev, y, nullptr, cw, cs, !packed);
-            return r;
+            return igemm_main_launch(c.g, c.pl, dy_dev, w_dev + c.w_origin, y, nullptr, cw, cs, !packed);
         };
         if (ph.empty()) return CONV_OK;
         if (ph.size() == 1) return run_class(ph[0], s, false);
@@ -644,8 +642,7 @@ conv_status conv_wgrad(const conv_tensor_desc *x, const int8_t *x_dev, const con
         if (overlaps(workspace, pl.workspace_bytes, x_dev, (uint64_t)desc_extent_elems(x)) ||
             overlaps(workspace, pl.workspace_bytes, dy_dev, (uint64_t)desc_extent_elems(dy)))
             return CONV_ERR_OVERLAP;
-        if ((st = igemm_pack_filter_launch(g, pl, dy_dev, workspace, stream))) return st;
-        return igemm_main_launch(g, pl, x_dev, dw_dev + origin, nullptr, workspace, stream, true);
+        return igemm_main_launch(g, pl, x_dev, dy_dev, dw_dev + origin, nullptr, workspace, stream, true);
     }
     GradArgs a = grad_args(x, dw, dy, p);
     a.a = x_dev;

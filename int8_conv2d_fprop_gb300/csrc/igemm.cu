@@ -165,23 +165,34 @@ constexpr int NCHW_MAX_ROW_BYTES = NCHW_STG_BYTES / KS;
 // 64 channel rows of the whole image row (one 4-D TMA box per row); the
 // converters transpose while converting (128 columns: five filter stages
 // and six 12 KB staging slots; 192 columns: four and eight).
-template <int NT, bool kTma, bool kResB = false, bool kTmemA = false, bool kNchw = false>
+// kSelfB (with kTmemA, channels-last image): the kernel converts the filter
+// itself.  Per k-step the filter issuer loads the int8 filter tile (NT
+// output channels x 64 channels of one tap, a 4-D TMA box of the KRSC-like
+// filter) into a staging ring, and the converters turn it into the f16
+// filter stage beside the image tile: no repack launch (128 columns: six
+// stages, eight image and four filter staging slots; 192 columns: four,
+// six and four; 16 output columns per store).
+template <int NT, bool kTma, bool kResB = false, bool kTmemA = false, bool kNchw = false, bool kSelfB = false>
 struct TileCfg {
     static constexpr int B_BYTES = NT * KS * 2;
     static constexpr int STG_SLOT = kNchw ? NCHW_STG_BYTES : STG_BYTES;  // bytes per staging slot
+    static constexpr int BSTG = kSelfB ? 4 : 0;                          // filter staging slots
+    static constexpr int BSTG_SLOT = NT * KS;                            // int8 filter tile
     // (192-column tiles without kTmemA: 40 KB stages, four of them behind
     // four staging buffers)
-    static constexpr int ST = kNchw ? (NT == 128 ? 5 : 4)
+    static constexpr int ST = kSelfB ? (NT == 128 ? 6 : 4)
+                            : kNchw ? (NT == 128 ? 5 : 4)
                             : kTmemA ? (NT == 128 && !kResB ? IGEMM_ST_TM128 : 4)
                                      : (kResB ? 2 : (kTma ? (NT == 256 ? IGEMM_ST_256 : (NT == 192 ? 4 : IGEMM_ST_128))
                                                           : (NT == 128 ? 6 : 4)));
-    static constexpr int STG_STAGES = kNchw ? (NT == 128 ? 6 : 8)
+    static constexpr int STG_STAGES = kSelfB ? (NT == 128 ? 8 : 6)
+                                    : kNchw ? (NT == 128 ? 6 : 8)
                                     : kTmemA ? (kResB ? 10 : (NT == 128 ? IGEMM_STG_TM128 : 12))
                                              : (kResB ? 6 : (kTma ? (NT == 256 ? IGEMM_STG_256 : (NT == 192 ? 4 : IGEMM_STG_128)) : 0));
     static constexpr int EPI_BUFS = kResB ? 1 : 2;  // output staging buffers per epilogue warp
     // output columns per staged store: 32 for the 128-column tensor-memory
     // variant (its shared memory has room for 4 KB buffers), else 16
-    static constexpr int EPI_COLS = (kTmemA && NT == 128) ? 32 : 16;
+    static constexpr int EPI_COLS = (kTmemA && NT == 128 && !kSelfB) ? 32 : 16;
     static constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 4;  // 2 or 4 KB
     static constexpr int EPI_BYTES = 8 * EPI_BUFS * EPI_BUF_BYTES;
     static constexpr int A_SMEM = kTmemA ? 0 : ST * A_BYTES;
@@ -198,9 +209,10 @@ struct TileCfg {
     static constexpr int A_ISSUERS = kTmemA ? 2 : 1;
     static_assert(STG_STAGES % A_ISSUERS == 0, "staging slots split evenly between the issuers");
     static constexpr int SMEM_BYTES = 1024 /*align slack*/ + A_SMEM + B_AREA + STG_STAGES * STG_SLOT +
-                                      EPI_BYTES + 512 /*barriers*/;
+                                      BSTG * BSTG_SLOT + EPI_BYTES + 1024 /*barriers*/;
     static_assert(!kResB || kTma, "the resident filter needs the TMA producers");
     static_assert(!kNchw || (kTmemA && !kResB), "NCHW rows feed the tensor-memory image stages");
+    static_assert(!kSelfB || (kTmemA && !kResB && !kNchw), "in-kernel filter conversion: tensor-memory variants");
     static_assert(!kTmemA || (kTma && NT <= 192 && TMEM_A_COL + ST * 32 <= 512), "image stages in tensor memory");
     static_assert(TMEM_COLS <= 512, "tensor memory has 512 columns");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
@@ -278,6 +290,7 @@ inline FastDiv make_fastdiv(int64_t d) {
 struct IgemmArgs {
     CUtensorMap tmap_x;  // im2col map of the channels-last image, or its 2-D pixel-row map (TMA path only)
     CUtensorMap tmap_y;  // output map: 2-D [pixels][K] (y_tma 1) or 3-D [N][K][P*Q] (y_tma 2)
+    CUtensorMap tmap_w;  // kSelfB: 4-D {C, S, R, K} map of the int8 filter
     const int8_t *x;     // channels-last image
     const uint8_t *wp;   // repacked f16 filter blocks
     void *y;             // int32 output, or int8 when out_int8
@@ -285,7 +298,8 @@ struct IgemmArgs {
     const int32_t *bias;
     int64_t xs_n, xs_h, xs_w;  // element (= byte) strides of the channels-last image
     int64_t ys_n, ys_k, ys_p, ys_q;
-    int32_t H, W, P, Q, K, S;
+    int32_t H, W, P, Q, K, R, S;
+    int32_t mode;        // CONVOLUTION: filter taps flipped (kSelfB reads the filter itself)
     int32_t c16;         // channel bytes per pixel that may be loaded (multiple of 16)
     int32_t c_steps, k_steps;
     int32_t pad_h, pad_w, str_h, str_w, dil_h, dil_w;
@@ -316,6 +330,7 @@ struct IgemmArgs {
 struct SharedCtl {
     uint64_t full[8], empty[8];          // A + filter ring
     uint64_t stg_full[16], stg_empty[16];  // TMA path: im2col tile landed / converted
+    uint64_t bstg_full[8], bstg_empty[8];  // kSelfB: int8 filter tile landed / converted
     uint64_t acc_full[NSLOT];
     uint64_t acc_empty[NSLOT];
     uint64_t mma_done;
@@ -323,7 +338,7 @@ struct SharedCtl {
     uint32_t tmem_base;
     int32_t abort_flag;
 };
-static_assert(sizeof(SharedCtl) <= 512, "control block too large");
+static_assert(sizeof(SharedCtl) <= 1024, "control block too large");
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting or
 // the time limit passed (then the CTA is marked aborting and the device status
@@ -482,9 +497,9 @@ __device__ __forceinline__ void drain_ring_owned(uint64_t *bars, int depth, int6
 
 // The kernel's body for one CTA: `a` holds the call's arguments, bid is the
 // CTA's index among the gdim CTAs that share the call's work units.
-template <int NT, bool kTma, bool kResB, bool kTmemA, bool kNchw>
+template <int NT, bool kTma, bool kResB, bool kTmemA, bool kNchw, bool kSelfB>
 __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, const int gdim) {
-    using Cfg = TileCfg<NT, kTma, kResB, kTmemA, kNchw>;
+    using Cfg = TileCfg<NT, kTma, kResB, kTmemA, kNchw, kSelfB>;
     constexpr int STG_SLOT = Cfg::STG_SLOT;
     constexpr int ST = Cfg::ST;
     constexpr int STG = Cfg::STG_STAGES;
@@ -497,9 +512,10 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
     const uint32_t a_smem = base;
     const uint32_t b_smem = a_smem + Cfg::A_SMEM;
     const uint32_t stg_smem = b_smem + Cfg::B_AREA;
-    const uint32_t epi_smem = stg_smem + STG * STG_SLOT;
-    SharedCtl *ctl =
-        reinterpret_cast<SharedCtl *>(base_ptr + Cfg::A_SMEM + Cfg::B_AREA + STG * STG_SLOT + Cfg::EPI_BYTES);
+    const uint32_t bstg_smem = stg_smem + STG * STG_SLOT;
+    const uint32_t epi_smem = bstg_smem + Cfg::BSTG * Cfg::BSTG_SLOT;
+    SharedCtl *ctl = reinterpret_cast<SharedCtl *>(base_ptr + Cfg::A_SMEM + Cfg::B_AREA + STG * STG_SLOT +
+                                                   Cfg::BSTG * Cfg::BSTG_SLOT + Cfg::EPI_BYTES);
     volatile int32_t *abort_flag = &ctl->abort_flag;
 
     const int warp = threadIdx.x >> 5;
@@ -519,8 +535,8 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
         for (int i = 0; i < ST; ++i) {
             // 128 producer arrivals (A tile written) + 1 arrival with the
             // filter copy's byte count (no filter copy per k-step when the
-            // filter is resident)
-            ptx::mbar_init(ptx::smem_addr(&ctl->full[i]), kResB ? 128 : 129);
+            // filter is resident or the converters write the filter stage)
+            ptx::mbar_init(ptx::smem_addr(&ctl->full[i]), (kResB || kSelfB) ? 128 : 129);
             ptx::mbar_init(ptx::smem_addr(&ctl->empty[i]), 1);
         }
         ptx::mbar_init(ptx::smem_addr(&ctl->b_res), 1);
@@ -528,7 +544,12 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
             ptx::mbar_init(ptx::smem_addr(&ctl->stg_full[i]), 1);
             ptx::mbar_init(ptx::smem_addr(&ctl->stg_empty[i]), 128);
         }
+        for (int i = 0; i < Cfg::BSTG; ++i) {
+            ptx::mbar_init(ptx::smem_addr(&ctl->bstg_full[i]), 1);
+            ptx::mbar_init(ptx::smem_addr(&ctl->bstg_empty[i]), 128);
+        }
         if (kTma) ptx::prefetch_tensormap(&a.tmap_x);
+        if (kSelfB) ptx::prefetch_tensormap(&a.tmap_w);
         if (a.y_tma) ptx::prefetch_tensormap(&a.tmap_y);
         for (int i = 0; i < NSLOT; ++i) {
             ptx::mbar_init(ptx::smem_addr(&ctl->acc_full[i]), 1);
@@ -681,15 +702,24 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
         // by the TMA 64-byte swizzle: each 8 rows cover all banks) and writes
         // the 32 f16 pairs to tensor-memory lane t (warp w owns lanes
         // 32w..32w+31), column j holding channels 2j and 2j+1.
+        // kSelfB: the same threads also convert the k-step's int8 filter
+        // tile (NT rows of 64 bytes in its staging slot) into the f16 filter
+        // stage of the ring, four neighbouring lanes per row and 128-byte
+        // swizzled rows (the layout of a repacked block), while the tensor
+        // memory store of the image tile completes.
         ptx::setmaxnreg_dec<TMEM_CONV_REGS>();
         const int row = threadIdx.x;
         const uint32_t sw = (uint32_t)((row >> 1) & 3);
         const uint32_t lane_col0 = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)Cfg::TMEM_A_COL;
+        const uint32_t bchunk = threadIdx.x & 3u;
         Ring<ST> ra;
         Ring<STG> rs;
+        Ring<(Cfg::BSTG > 0 ? Cfg::BSTG : 1)> rb;
         for (int it = 0; it < total; ++it) {
             bool got = wait_phase(ptx::smem_addr(&ctl->stg_full[rs.idx]), rs.phase, abort_flag, limit, a.status);
             got = got && wait_phase(ptx::smem_addr(&ctl->empty[ra.idx]), ra.phase ^ 1u, abort_flag, limit, a.status);
+            if (kSelfB)
+                got = got && wait_phase(ptx::smem_addr(&ctl->bstg_full[rb.idx]), rb.phase, abort_flag, limit, a.status);
             // tcgen05.st is warp-collective: the whole warp proceeds or stops together
             if (!__all_sync(0xffffffffu, got)) break;
             const uint32_t src = stg_smem + rs.idx * STG_SLOT + (uint32_t)row * 64u;
@@ -705,6 +735,28 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
                 w[8 * c + 4] = hi.x; w[8 * c + 5] = hi.y; w[8 * c + 6] = hi.z; w[8 * c + 7] = hi.w;
             }
             ptx::tmem_st_32x32b_x32(lane_col0 + (uint32_t)(ra.idx * 32), w);
+            if (kSelfB) {
+                const uint32_t bsrc = bstg_smem + rb.idx * Cfg::BSTG_SLOT + bchunk * 16u;
+                const uint32_t bdst = b_smem + ra.idx * B_BYTES;
+                uint4 vb[NT / 32];
+#pragma unroll
+                for (int i = 0; i < NT / 32; ++i)
+                    vb[i] = ptx::ld_shared_v4(bsrc + (uint32_t)((threadIdx.x >> 2) + 32 * i) * 64u);
+#pragma unroll
+                for (int i = 0; i < NT / 32; ++i) {
+                    const uint32_t brow = (uint32_t)((threadIdx.x >> 2) + 32 * i);
+                    uint4 lo, hi;
+                    cvt16(vb[i], lo, hi);
+                    const uint32_t rdst = bdst + brow * 128u;
+                    const uint32_t swz = brow & 7u;
+                    ptx::st_shared_v4(rdst + (((2u * bchunk) ^ swz) << 4), lo);
+                    ptx::st_shared_v4(rdst + (((2u * bchunk + 1u) ^ swz) << 4), hi);
+                }
+                // the filter stage is read by the tensor core (async proxy)
+                ptx::fence_proxy_async_smem();
+                ptx::mbar_arrive(ptx::smem_addr(&ctl->bstg_empty[rb.idx]));
+                rb.next();
+            }
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
             ptx::mbar_arrive(ptx::smem_addr(&ctl->stg_empty[rs.idx]));
@@ -982,6 +1034,42 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
             for (int j = 0; j < a.k_steps; ++j)
                 ptx::bulk_copy_g2s(b_smem + j * B_BYTES, a.wp + (size_t)j * B_BYTES, B_BYTES, bar);
             (void)drain_phase(bar, 0, limit, a.status);
+        } else if (kSelfB && warp == B_ISSUER_WARP && lane == 0) {
+            // int8 filter tiles by TMA, in the rotated k-step order of the
+            // image tiles: for tap (r, s) and channel block cb the box
+            // {64 channels, 1, 1, NT rows} of the {C, S, R, K} map at
+            // (cb*64, s, r, nt*NT), the taps flipped (S-1-s, R-1-r) for
+            // CONVOLUTION; channels past C and rows past K read as zeros
+            Ring<(Cfg::BSTG > 0 ? Cfg::BSTG : 1)> rb;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int u = bid; u < a.num_units && ok; u += gdim) {
+                const Unit wu = unit_at(u, a.full_units, a.splits, a.k_steps);
+                const int kn = wu.ke - wu.kb;
+                const int urot = wu.split < 0 ? rot : 0;
+                const int nt = wu.tile - fdiv(wu.tile, a.fd_nt) * a.n_tiles;
+                for (int j = 0; j < kn; ++j) {
+                    int jr = j + urot;
+                    if (jr >= kn) jr -= kn;
+                    jr += wu.kb;
+                    const int tap = fdiv(jr, a.fd_cs);
+                    const int cb = jr - tap * a.c_steps;
+                    const int r = fdiv(tap, a.fd_s);
+                    const int s = tap - r * a.S;
+                    if (!wait_phase(ptx::smem_addr(&ctl->bstg_empty[rb.idx]), rb.phase ^ 1u, abort_flag, limit,
+                                    a.status, kIssuerBackoffNs)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bar = ptx::smem_addr(&ctl->bstg_full[rb.idx]);
+                    ptx::mbar_arrive_expect_tx(bar, (uint32_t)Cfg::BSTG_SLOT);
+                    ptx::tma_load_4d(bstg_smem + rb.idx * Cfg::BSTG_SLOT, &a.tmap_w, cb * KS, a.mode ? a.S - 1 - s : s,
+                                     a.mode ? a.R - 1 - r : r, nt * NT, bar);
+                    ++issued;
+                    rb.next();
+                }
+            }
+            if (*abort_flag) drain_ring(ctl->bstg_full, Cfg::BSTG, issued, limit, a.status);
         } else if (kTma && warp == B_ISSUER_WARP && lane == 0) {
             // pre-swizzled f16 filter blocks, one bulk copy per k-step, in the
             // same rotated k-step order as the image tiles
@@ -1249,9 +1337,9 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
     if (warp == MMA_WARP) ptx::tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
-template <int NT, bool kTma, bool kResB, bool kTmemA, bool kNchw>
+template <int NT, bool kTma, bool kResB, bool kTmemA, bool kNchw, bool kSelfB>
 __global__ void __launch_bounds__(THREADS, 1) igemm_conv_kernel(const __grid_constant__ IgemmArgs a) {
-    conv_cta<NT, kTma, kResB, kTmemA, kNchw>(a, blockIdx.x, gridDim.x);
+    conv_cta<NT, kTma, kResB, kTmemA, kNchw, kSelfB>(a, blockIdx.x, gridDim.x);
 }
 
 // Several convolutions of one kernel variant in one launch (the residue
@@ -1264,11 +1352,11 @@ struct IgemmGroup {
     int32_t n;
 };
 
-template <int NT, bool kTma, bool kResB, bool kTmemA, bool kNchw>
+template <int NT, bool kTma, bool kResB, bool kTmemA, bool kNchw, bool kSelfB>
 __global__ void __launch_bounds__(THREADS, 1) igemm_conv_group_kernel(const __grid_constant__ IgemmGroup g) {
     int c = 0;
     while (c + 1 < g.n && (int)blockIdx.x >= g.cta_start[c + 1]) ++c;
-    conv_cta<NT, kTma, kResB, kTmemA, kNchw>(g.cls[c], (int)blockIdx.x - g.cta_start[c],
+    conv_cta<NT, kTma, kResB, kTmemA, kNchw, kSelfB>(g.cls[c], (int)blockIdx.x - g.cta_start[c],
                                       g.cta_start[c + 1] - g.cta_start[c]);
 }
 
@@ -1600,14 +1688,14 @@ constexpr int64_t kMinSplitSteps = 16;   // k-steps of the shortest run of a cut
 constexpr int64_t kMaxSplits = 32;
 constexpr int64_t kMinTailSteps = 4;     // k-steps of the shortest run of a last-round tile
 
-template <int NT, bool kTma, bool kResB = false, bool kTmemA = false, bool kNchw = false>
+template <int NT, bool kTma, bool kResB = false, bool kTmemA = false, bool kNchw = false, bool kSelfB = false>
 conv_status launch_conv(const IgemmArgs &a, int grid, cudaStream_t st) {
-    using Cfg = TileCfg<NT, kTma, kResB, kTmemA, kNchw>;
+    using Cfg = TileCfg<NT, kTma, kResB, kTmemA, kNchw, kSelfB>;
     static std::atomic<bool> attr_set[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !attr_set[dev].load()) {
-        if (cudaFuncSetAttribute(igemm_conv_kernel<NT, kTma, kResB, kTmemA, kNchw>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(igemm_conv_kernel<NT, kTma, kResB, kTmemA, kNchw, kSelfB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg::SMEM_BYTES) != cudaSuccess)
             return CONV_ERR_CUDA;
         if (dev >= 0 && dev < 64) attr_set[dev].store(true);
@@ -1627,7 +1715,7 @@ conv_status launch_conv(const IgemmArgs &a, int grid, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, igemm_conv_kernel<NT, kTma, kResB, kTmemA, kNchw>, a) != cudaSuccess) return CONV_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, igemm_conv_kernel<NT, kTma, kResB, kTmemA, kNchw, kSelfB>, a) != cudaSuccess) return CONV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
@@ -1655,15 +1743,40 @@ PFN_cuTensorMapEncodeIm2col_v12000 im2col_encoder() {
 // and H so that its traversal at the convolution stride visits exactly the
 // P x Q window origins.  Returns false when the map cannot express the call
 // (stride above 8, corner or offset out of range, encoder unavailable).
-bool encode_im2col_map(const ConvGeom &g, const void *x, int64_t xs_n, int64_t xs_h, int64_t xs_w, int64_t c_dim,
-                       bool swizzle64, CUtensorMap *map) {
+// The geometry the kernel sees: the call's, or, for an image copy that
+// keeps every row_step-th row from row0, the same convolution over the copy
+// (h = row0 + row_step*h', so stride, dilation and pre-padding along H are
+// divided by row_step: pre' = (pre + row0) / row_step, exact).
+ConvGeom kernel_geom(const ConvGeom &g, const IgemmPlan &pl) {
+    ConvGeom k = g;
+    if (pl.pack_x && pl.row_step > 1) {
+        k.H = pl.hp;
+        k.str_h = g.str_h / pl.row_step;
+        k.dil_h = g.R > 1 ? g.dil_h / pl.row_step : g.dil_h;
+        k.pad_h = (g.pad_h + pl.row0) / pl.row_step;
+    }
+    return k;
+}
+
+// The limits of an im2col map that do not depend on the image's address:
+// stride at most 8, bounding-box corners within [-128, 127], tap offsets
+// within 16 bits.
+bool im2col_geometry_ok(const ConvGeom &g) {
     if (g.str_h > 8 || g.str_w > 8) return false;
     const int64_t lo_w = -g.pad_w, lo_h = -g.pad_h;
     const int64_t hi_w = (g.Q - 1) * g.str_w + lo_w - (g.W - 1);  // = post_w - (S-1)*dil_w
     const int64_t hi_h = (g.P - 1) * g.str_h + lo_h - (g.H - 1);
     for (int64_t v : {lo_w, lo_h, hi_w, hi_h})
         if (v < -128 || v > 127) return false;
-    if ((g.R - 1) * g.dil_h > 65535 || (g.S - 1) * g.dil_w > 65535) return false;
+    return (g.R - 1) * g.dil_h <= 65535 && (g.S - 1) * g.dil_w <= 65535;
+}
+
+bool encode_im2col_map(const ConvGeom &g, const void *x, int64_t xs_n, int64_t xs_h, int64_t xs_w, int64_t c_dim,
+                       bool swizzle64, CUtensorMap *map) {
+    if (!im2col_geometry_ok(g)) return false;
+    const int64_t lo_w = -g.pad_w, lo_h = -g.pad_h;
+    const int64_t hi_w = (g.Q - 1) * g.str_w + lo_w - (g.W - 1);  // = post_w - (S-1)*dil_w
+    const int64_t hi_h = (g.P - 1) * g.str_h + lo_h - (g.H - 1);
     if (((uintptr_t)x % 16) != 0 || xs_w % 16 || xs_h % 16 || xs_n % 16) return false;
     auto enc = im2col_encoder();
     if (!enc) return false;
@@ -1930,6 +2043,16 @@ void igemm_plan(const ConvGeom &g, const void *x_dev, IgemmPlan *pl, bool regist
     pl->workspace_bytes = off + pl->xpack_bytes;
 }
 
+bool igemm_filter_in_kernel(const ConvGeom &g, const IgemmPlan &pl, const void *w) {
+    const int64_t lim40 = (int64_t)1 << 40, lim32 = (int64_t)1 << 32;
+    // (the image taken by TMA: the im2col limits; a pixel-row map, where a
+    // 1x1 call takes one, has none of its own)
+    return pl.n_tile <= 192 && !pl.register_loads && !pl.nchw_rows && im2col_geometry_ok(kernel_geom(g, pl)) &&
+           g.ws[1] == 1 && g.ws[3] % 16 == 0 &&
+           g.ws[2] % 16 == 0 && g.ws[0] % 16 == 0 && g.ws[0] < lim40 && g.ws[2] < lim40 && g.ws[3] < lim40 &&
+           g.C < lim32 && g.K < lim32 && (w == nullptr || ((uintptr_t)w % 16) == 0);
+}
+
 static PackFilterJob pack_job(const ConvGeom &g, const IgemmPlan &pl, const int8_t *w, uint8_t *wp) {
     PackFilterJob j;
     j.w = w;
@@ -2002,7 +2125,9 @@ PFN_cuTensorMapReplaceAddress_v12000 address_replacer() {
     return reinterpret_cast<PFN_cuTensorMapReplaceAddress_v12000>(fn.load());
 }
 
-enum Variant { V_REG128, V_REG192, V_REG256, V_TMEM128, V_TMEM192, V_TMA256, V_RESB256, V_NCHW128, V_NCHW192 };
+enum Variant {
+    V_REG128, V_REG192, V_REG256, V_TMEM128, V_TMEM192, V_TMA256, V_RESB256, V_NCHW128, V_NCHW192, V_SELF128, V_SELF192
+};
 
 // Everything a launch of the convolution kernel needs that does not change
 // with the buffers' addresses: the kernel arguments (tensor maps encoded for
@@ -2014,6 +2139,7 @@ struct LaunchPlan {
     bool planes;          // plane-contiguous image copy (when the image is repacked)
     const void *x_map;    // addresses the maps were encoded with
     const void *y_map;
+    const void *w_map;    // (filter map: in-kernel filter conversion only)
 };
 
 // Launch-plan cache: key = geometry, plan, device and the 16-byte alignment
@@ -2084,20 +2210,6 @@ void launch_insert(const LaunchKey &k, const LaunchPlan &p) {
     victim->valid = true;
 }
 
-// The geometry the kernel sees: the call's, or, for an image copy that
-// keeps every row_step-th row from row0, the same convolution over the copy
-// (h = row0 + row_step*h', so stride, dilation and pre-padding along H are
-// divided by row_step: pre' = (pre + row0) / row_step, exact).
-ConvGeom kernel_geom(const ConvGeom &g, const IgemmPlan &pl) {
-    ConvGeom k = g;
-    if (pl.pack_x && pl.row_step > 1) {
-        k.H = pl.hp;
-        k.str_h = g.str_h / pl.row_step;
-        k.dil_h = g.R > 1 ? g.dil_h / pl.row_step : g.dil_h;
-        k.pad_h = (g.pad_h + pl.row0) / pl.row_step;
-    }
-    return k;
-}
 
 // Builds the launch plan of a call (kernel arguments, tensor maps, variant).
 // The channels-last copy of the image takes the plane transpose: each
@@ -2110,8 +2222,24 @@ bool planes_copy(const ConvGeom &g0, const IgemmPlan &pl, const int8_t *x) {
            (pl.row_step == 1 || g0.W % 16 == 0);
 }
 
-conv_status build_launch(const ConvGeom &g0, const IgemmPlan &pl, const int8_t *x, void *y, uint8_t *wp,
-                         LaunchPlan *L) {
+// 4-D map {C, S, R, K} of an int8 filter with contiguous channels (byte
+// strides ws[3], ws[2], ws[0]): box {64, 1, 1, NT}, the k-step's int8 tile,
+// no swizzle (the converters read 64-byte rows).
+bool encode_filter_map(const ConvGeom &g, const void *w, int64_t nt, CUtensorMap *map) {
+    auto enc = tiled_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)g.C, (cuuint64_t)g.S, (cuuint64_t)g.R, (cuuint64_t)g.K};
+    const cuuint64_t strides[3] = {(cuuint64_t)g.ws[3], (cuuint64_t)g.ws[2], (cuuint64_t)g.ws[0]};
+    const cuuint32_t box[4] = {(cuuint32_t)KS, 1, 1, (cuuint32_t)nt};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(w), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+conv_status build_launch(const ConvGeom &g0, const IgemmPlan &pl, const int8_t *x, const int8_t *w, void *y,
+                         uint8_t *wp, LaunchPlan *L) {
     const ConvGeom g = kernel_geom(g0, pl);
     IgemmArgs &a = L->a;
     std::memset(&a, 0, sizeof(a));
@@ -2183,8 +2311,16 @@ conv_status build_launch(const ConvGeom &g0, const IgemmPlan &pl, const int8_t *
             tma = encode_im2col_map(g, a.x, a.xs_n, a.xs_h, a.xs_w, c_dim, tmem_a, &a.tmap_x);
         }
     }
+    // tensor-memory tiles over a channels-last image convert a channel-
+    // contiguous filter themselves (no repack launch)
+    a.R = (int32_t)g.R;
+    a.mode = g.mode;
+    const bool self_b = w != nullptr && tma && tmem_a && !pl.nchw_rows && igemm_filter_in_kernel(g0, pl, w) &&
+                        encode_filter_map(g0, w, pl.n_tile, &a.tmap_w);
+    L->w_map = self_b ? w : nullptr;
     // the 128-column tensor-memory variant stages 32 output columns per store
-    const bool wide_out = tma && pl.n_tile == 128;
+    // (16 when the kernel also converts the filter)
+    const bool wide_out = tma && pl.n_tile == 128 && !self_b;
     a.y_tma = encode_output_map(g, y, wide_out, &a.tmap_y) ? 1 : (encode_output_map_nchw(g, y, wide_out, &a.tmap_y) ? 2 : 0);
     // int8 outputs are staged 64 columns at a time: a 192-column tile (96
     // per epilogue warp) stores them with plain stores
@@ -2195,6 +2331,8 @@ conv_status build_launch(const ConvGeom &g0, const IgemmPlan &pl, const int8_t *
     L->tma = tma;
     if (pl.nchw_rows)
         L->variant = pl.n_tile == 128 ? V_NCHW128 : V_NCHW192;
+    else if (self_b)
+        L->variant = pl.n_tile == 128 ? V_SELF128 : V_SELF192;
     else if (tma && tmem_a)
         L->variant = pl.n_tile == 128 ? V_TMEM128 : V_TMEM192;
     else if (tma && pl.resident_b)
@@ -2251,22 +2389,25 @@ namespace {
 // The launch plan of a call (variant, grid, arguments with their tensor
 // maps): from the cache when an equal call ran before, re-targeted to this
 // call's buffers.
-conv_status prepare_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *y, const int32_t *bias,
-                           uint8_t *wp, LaunchPlan *out) {
+conv_status prepare_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, const int8_t *w, void *y,
+                           const int32_t *bias, uint8_t *wp, LaunchPlan *out) {
     int dev = 0;
     cudaGetDevice(&dev);
     // (every decision of build_launch that reads a pointer reads only its
-    // 16-byte alignment)
-    const LaunchKey key = make_key(g, pl, dev, (((uintptr_t)x % 16) == 0 ? 1 : 0) | (((uintptr_t)y % 16) == 0 ? 2 : 0));
+    // 16-byte alignment, or, for the filter, whether it is given)
+    const int walign = w == nullptr ? 0 : (((uintptr_t)w % 16) == 0 ? 4 : 8);
+    const LaunchKey key =
+        make_key(g, pl, dev, (((uintptr_t)x % 16) == 0 ? 1 : 0) | (((uintptr_t)y % 16) == 0 ? 2 : 0) | walign);
     LaunchPlan L;
     bool hit = launch_lookup(key, &L);
     const void *x_now = pl.pack_x ? (const void *)(wp + pl.xpack_off) : (const void *)x;
-    if (hit && (L.x_map != x_now || L.y_map != y)) {
+    if (hit && (L.x_map != x_now || L.y_map != y || (L.w_map && L.w_map != w))) {
         // re-target the cached maps to this call's buffers
         auto rep = address_replacer();
         bool ok = rep != nullptr;
         if (ok && L.tma && L.x_map != x_now) ok = rep(&L.a.tmap_x, const_cast<void *>(x_now)) == CUDA_SUCCESS;
         if (ok && L.a.y_tma && L.y_map != y) ok = rep(&L.a.tmap_y, y) == CUDA_SUCCESS;
+        if (ok && L.w_map && L.w_map != w) ok = rep(&L.a.tmap_w, const_cast<int8_t *>(w)) == CUDA_SUCCESS;
         hit = ok;
     }
     if (hit) {
@@ -2277,9 +2418,10 @@ conv_status prepare_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t 
         L.a.tail_part = pl.splits > 1 ? reinterpret_cast<int32_t *>(wp + pl.tail_part_off) : nullptr;
         L.x_map = x_now;
         L.y_map = y;
+        if (L.w_map) L.w_map = w;
     } else {
         g_launch_misses.fetch_add(1);
-        conv_status b = build_launch(g, pl, x, y, wp, &L);
+        conv_status b = build_launch(g, pl, x, w, y, wp, &L);
         if (b) return b;
         launch_insert(key, L);
     }
@@ -2290,12 +2432,12 @@ conv_status prepare_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t 
 
 template <int NT, bool kTma, bool kResB = false, bool kTmemA = false, bool kNchw = false>
 conv_status launch_conv_group(const IgemmGroup &grp, int grid, cudaStream_t st) {
-    using Cfg = TileCfg<NT, kTma, kResB, kTmemA, kNchw>;
+    using Cfg = TileCfg<NT, kTma, kResB, kTmemA, kNchw, false>;
     static std::atomic<bool> attr_set[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !attr_set[dev].load()) {
-        if (cudaFuncSetAttribute(igemm_conv_group_kernel<NT, kTma, kResB, kTmemA, kNchw>,
+        if (cudaFuncSetAttribute(igemm_conv_group_kernel<NT, kTma, kResB, kTmemA, kNchw, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess)
             return CONV_ERR_CUDA;
         if (dev >= 0 && dev < 64) attr_set[dev].store(true);
@@ -2310,7 +2452,7 @@ conv_status launch_conv_group(const IgemmGroup &grp, int grid, cudaStream_t st) 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, igemm_conv_group_kernel<NT, kTma, kResB, kTmemA, kNchw>, grp) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, igemm_conv_group_kernel<NT, kTma, kResB, kTmemA, kNchw, false>, grp) != cudaSuccess)
         return CONV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
@@ -2332,7 +2474,7 @@ conv_status igemm_group_launch(int n, const ConvGeom *const *g, const IgemmPlan 
         if (pl[c]->splits > 1 || (pl[c]->pack_x && !pl[c]->pack_done) || pl[c]->m_tiles * pl[c]->n_tiles == 0)
             return CONV_OK;
         LaunchPlan L;
-        conv_status st = prepare_launch(*g[c], *pl[c], x, y[c], nullptr, static_cast<uint8_t *>(workspace[c]), &L);
+        conv_status st = prepare_launch(*g[c], *pl[c], x, nullptr, y[c], nullptr, static_cast<uint8_t *>(workspace[c]), &L);
         if (st) return st;
         if (!(L.variant == V_TMEM128 || L.variant == V_TMEM192 || L.variant == V_TMA256 || L.variant == V_RESB256 ||
               L.variant == V_NCHW128 || L.variant == V_NCHW192) ||
@@ -2377,21 +2519,26 @@ conv_status igemm_group_launch(int n, const ConvGeom *const *g, const IgemmPlan 
     return rc;
 }
 
-conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *y,
-                              const int32_t *bias, void *workspace, void *stream, bool after_own_repack) {
+conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, const int8_t *w, void *y,
+                              const int32_t *bias, void *workspace, void *stream, bool repack) {
     cudaStream_t st = (cudaStream_t)stream;
     const int sms = device_sm_count();
     uint8_t *wp = static_cast<uint8_t *>(workspace);
     if (pl.m_tiles * pl.n_tiles == 0) return CONV_OK;
     LaunchPlan L;
-    conv_status pst = prepare_launch(g, pl, x, y, bias, wp, &L);
+    // a call that brings its filter (repack) may have the kernel convert it
+    // itself; a call on a repacked workspace reads the repacked blocks
+    conv_status pst = prepare_launch(g, pl, x, repack ? w : nullptr, y, bias, wp, &L);
     if (pst) return pst;
     IgemmArgs &a = L.a;
-
+    const bool self_b = L.variant == V_SELF128 || L.variant == V_SELF192;
+    // the filter repack, unless the kernel converts the filter itself
+    const bool repacked = repack && !self_b;
+    if (repacked && (pst = igemm_pack_filter_launch(g, pl, w, workspace, stream))) return pst;
     // the image loads may start before the filter repack ends only when the
     // repack is the kernel right before (not an image copy, whose output
     // they read)
-    a.early_image = after_own_repack && L.tma && !(pl.pack_x && !pl.pack_done) ? 1 : 0;
+    a.early_image = repacked && L.tma && !(pl.pack_x && !pl.pack_done) ? 1 : 0;
     if (pl.pack_x && !pl.pack_done) {
         const conv_status pr = igemm_pack_image_launch(g, pl, x, workspace, stream);
         if (pr) return pr;
@@ -2405,6 +2552,8 @@ conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8
         case V_TMEM192: rc = launch_conv<192, true, false, true>(a, grid, st); break;
         case V_NCHW128: rc = launch_conv<128, true, false, true, true>(a, grid, st); break;
         case V_NCHW192: rc = launch_conv<192, true, false, true, true>(a, grid, st); break;
+        case V_SELF128: rc = launch_conv<128, true, false, true, false, true>(a, grid, st); break;
+        case V_SELF192: rc = launch_conv<192, true, false, true, false, true>(a, grid, st); break;
         case V_REG256: rc = launch_conv<256, false>(a, grid, st); break;
         case V_REG192: rc = launch_conv<192, false>(a, grid, st); break;
         default: rc = launch_conv<128, false>(a, grid, st); break;

@@ -134,15 +134,22 @@ conv_status igemm_group_launch(int n, const ConvGeom *const *g, const IgemmPlan 
 // Makes the channels-last copy of the image at pl.xpack_off of the workspace.
 conv_status igemm_pack_image_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *workspace,
                                     void *stream);
-// Runs the convolution from a workspace whose filter part is already packed
-// (copies the image to channels-last first when pl.pack_x).
-// after_own_repack: the caller launched its own filter repack (an ordinary
-// launch, which starts once every earlier kernel of the stream has
-// completed) directly before on the same stream, so the image is final and
-// the kernel's image loads need not wait for the repack to end.
-conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, void *y,
-                              const int32_t *bias, void *workspace, void *stream,
-                              bool after_own_repack = false);
+// Runs the convolution (copying the image to channels-last first when
+// pl.pack_x).  repack: launch the filter repack into the workspace first,
+// unless the kernel variant converts the filter itself
+// (igemm_filter_in_kernel); without it the workspace's filter part must
+// already be packed, and the kernel reads it.  When
+// the repack is launched it directly precedes the convolution on the stream
+// (an ordinary launch, which starts once every earlier kernel of the stream
+// has completed), so the image is final and the kernel's image loads need
+// not wait for the repack to end.
+conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, const int8_t *w, void *y,
+                              const int32_t *bias, void *workspace, void *stream, bool repack);
+// Whether the 128- and 192-column tensor-memory kernels convert this
+// call's filter themselves (channels contiguous, 16-byte aligned strides and
+// pointer; w == nullptr: a 16-byte aligned pointer assumed) instead of
+// reading repacked blocks.
+bool igemm_filter_in_kernel(const ConvGeom &g, const IgemmPlan &pl, const void *w);
 
 // Launch-plan cache of the tensor-core kernel (tensor maps re-targeted to
 // each call's buffers): empty it; read its hit and miss counts.

@@ -1,8 +1,9 @@
 """Every output of every workload at full size, in the launch configuration
-the benchmark times: the benchmark's own DeviceWorkload (filter repack by
-conv_fprop_pack_filter, then conv_fprop_prepacked on resident inputs, with the
-cut last round and its reduction kernel wherever the planner cuts one),
-compared element by element with the CPU oracle (tolerance 0).
+the benchmark times: the benchmark's own DeviceWorkload (a step is one
+conv_fprop call on resident inputs, with the cut last round and its
+reduction kernel wherever the planner cuts one; the convolution-only timing
+calls conv_fprop_pack_filter, then conv_fprop_prepacked), compared element
+by element with the CPU oracle (tolerance 0).
 
 The two large workloads take the oracle about 10 s (3x3, 118 G ops) and
 3 s (7x1 dilated) on 16 host cores."""
@@ -46,10 +47,20 @@ def test_every_output_at_full_size_as_benchmarked(ic, name):
     assert ic.device_status(sh) == 0
     ref = oracle.conv_fprop(wl.xf, cfg.x_dims, wl.xs, wl.wf, cfg.w_dims, wl.ws, cfg.pre, cfg.post, cfg.stride,
                             cfg.dilation, cfg.mode, wl.b, cfg.relu)
-    for s in (0, 1):
+    def check(s, what):
         got = wl.output(s)
         if not np.array_equal(got, ref):
             idx = np.argwhere(got != ref)
             first = tuple(idx[0])
-            raise AssertionError(f"{name} set {s}: {len(idx)} of {ref.size} outputs differ; first at {first}: "
-                                 f"got {got[first]} expected {ref[first]}")
+            raise AssertionError(f"{name} {what} set {s}: {len(idx)} of {ref.size} outputs differ; first at "
+                                 f"{first}: got {got[first]} expected {ref[first]}")
+
+    for s in (0, 1):
+        check(s, "conv_fprop")
+    # the two halves the convolution-only timing calls
+    wl.y_dev[0].fill_(0x5A5A5A5A)
+    wl.pack(sh)
+    wl.conv(0, sh)
+    torch.cuda.synchronize(dev)
+    assert ic.device_status(sh) == 0
+    check(0, "pack_filter + prepacked")

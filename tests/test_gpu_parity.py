@@ -341,6 +341,85 @@ def test_nchw_rows_int8_output(ic):
         _assert_equal(got, ref, case.name + " int8 out")
 
 
+def _filter_in_kernel_cases():
+    C = synth.ConvConfig
+    return [
+        # K = 100 (filter rows past K read as zeros), C = 80 (the second
+        # channel step half past C), 3x3 pad 1, convolution mode, bias + ReLU,
+        # 128-column tiles
+        C("selfw_k100_c80_conv", 2, 80, 14, 13, 100, 3, 3, pre=(1, 1), post=(1, 1), mode=1, bias=True, relu=True,
+          seed=91),
+        # 192-column tiles, stride 2, dilation 2
+        C("selfw_k160_s2_dil2", 3, 64, 19, 17, 160, 3, 3, stride=(2, 2), dilation=(2, 2), pre=(2, 2), post=(2, 1),
+          seed=92),
+        # 1x1 over pixel rows, channel-major output
+        C("selfw_1x1_nchw_out", 4, 128, 12, 16, 64, 1, 1, y_layout="NCHW", seed=93),
+    ]
+
+
+@pytest.mark.parametrize("w_pad", [0, 16, 3])
+@pytest.mark.parametrize("case", _filter_in_kernel_cases(), ids=lambda c: c.name)
+def test_filter_converted_in_kernel(ic, case, w_pad):
+    """128- and 192-column tiles over a channels-last image convert a filter
+    whose channels are contiguous themselves (TMA loads of int8 filter tiles,
+    converted beside the image tile): conv_fprop launches the convolution
+    alone.  Filter rows padded to a 16-byte multiple keep that path; padded
+    to an odd stride they take the repack instead.  Exact either way."""
+    if w_pad == 0:
+        xd = ic.TensorDesc.packed(ic.CONV_INT8, case.x_dims, case.x_layout)
+        wd = ic.TensorDesc.packed(ic.CONV_INT8, case.w_dims, case.w_layout)
+        yd = ic.TensorDesc.packed(ic.CONV_INT32, case.y_dims, case.y_layout)
+        p = ic.Params.make(case.pre, case.post, case.stride, case.dilation, case.mode, case.bias, case.relu)
+        assert ic.kernel_count(xd, wd, yd, p) == 1
+    got, ref = _run_both(ic, case, w_pad=w_pad)
+    _assert_equal(got, ref, f"{case.name} w_pad {w_pad}")
+    got, ref = _run_both(ic, case, w_pad=w_pad, out_shift=9)
+    _assert_equal(got, ref, f"{case.name} w_pad {w_pad} int8 out")
+
+
+def test_filter_in_kernel_unaligned_pointer_and_prepacked(ic):
+    """A filter pointer off the 16-byte grid makes conv_fprop repack the
+    filter (another launch-cache key); conv_fprop_pack_filter followed by
+    conv_fprop_prepacked reads the repacked blocks, with either pointer.
+    All exact."""
+    cfg = _filter_in_kernel_cases()[0]
+    x, w, b = synth.make_inputs(cfg)
+    xf, xs = synth.place(x, cfg.x_layout)
+    wf, ws = synth.place(w, cfg.w_layout)
+    ref = oracle.conv_fprop(xf, cfg.x_dims, xs, wf, cfg.w_dims, ws, cfg.pre, cfg.post, cfg.stride, cfg.dilation,
+                            cfg.mode, b, cfg.relu)
+    xd = ic.TensorDesc.make(ic.CONV_INT8, cfg.x_dims, xs, xf.size)
+    wd = ic.TensorDesc.make(ic.CONV_INT8, cfg.w_dims, ws, wf.size)
+    ystr = synth.packed_strides(cfg.y_dims, cfg.y_layout)
+    ysz = int(np.prod(cfg.y_dims))
+    yd = ic.TensorDesc.make(ic.CONV_INT32, cfg.y_dims, ystr, ysz * 4)
+    p = ic.Params.make(cfg.pre, cfg.post, cfg.stride, cfg.dilation, cfg.mode, cfg.bias, cfg.relu)
+    need = ic.workspace_size(xd, wd, yd, p)
+    s = torch.cuda.current_stream().cuda_stream
+    xt = torch.from_numpy(xf).cuda()
+    bt = torch.from_numpy(b).cuda()
+    wsb = torch.empty(need + 256, dtype=torch.uint8, device="cuda")
+    for off in (0, 8):
+        wb = torch.zeros(wf.size + 64, dtype=torch.int8, device="cuda")
+        wb[16 + off:16 + off + wf.size].copy_(torch.from_numpy(wf))
+        wptr = wb.data_ptr() + 16 + off
+        for how in ("conv_fprop", "prepacked"):
+            yb = torch.full((ysz,), -1, dtype=torch.int32, device="cuda")
+            if how == "conv_fprop":
+                st = ic.conv_fprop_raw(xd, xt.data_ptr(), wd, wptr, yd, yb.data_ptr(), bt.data_ptr(), p,
+                                       wsb.data_ptr(), need, s)
+            else:
+                st = ic.pack_filter_raw(xd, wd, wptr, yd, p, wsb.data_ptr(), need, s)
+                assert st == 0, ic.STATUS.get(st)
+                st = ic.conv_fprop_prepacked_raw(xd, xt.data_ptr(), wd, wptr, yd, yb.data_ptr(), bt.data_ptr(), p,
+                                                 wsb.data_ptr(), need, s)
+            assert st == 0, ic.STATUS.get(st)
+            torch.cuda.synchronize()
+            assert ic.device_status() == 0
+            got = synth.gather_logical(yb.cpu().numpy(), cfg.y_dims, ystr)
+            _assert_equal(got, ref, f"filter offset {off} {how}")
+
+
 # ------------------------------------------------------------------ exactness
 def test_extreme_values_exceed_f32_integer_range(ic):
     """All -128 operands: interior sums C*R*S*2^14 = 37,748,736 > 2^24, so
