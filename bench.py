@@ -350,6 +350,9 @@ def time_workload(ic, cfg, dev, stream, flush, iters: int, warmup: int, peaks: d
         return e0.elapsed_time(e1) / iters
 
     step_ms = timed(lambda i: wl.step(i, sh), True)
+    # the convolution-only calls read the repacked filter (conv_fprop may
+    # have converted the filter in its kernel, leaving the workspace unpacked)
+    wl.pack(sh)
     conv_ms = timed(lambda i: wl.conv(i, sh), True)
     warm_ms = timed(lambda i: wl.step(i, sh), False)
     if nsets > 1:
