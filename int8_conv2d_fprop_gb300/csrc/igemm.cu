@@ -2467,7 +2467,6 @@ conv_status igemm_group_launch(int n, const ConvGeom *const *g, const IgemmPlan 
     static IgemmGroup grp_zero;  // (zero-filled template: IgemmArgs has no constructor)
     IgemmGroup grp = grp_zero;
     int variant = -1;
-    int64_t work = 0;
     for (int c = 0; c < n; ++c) {
         // whole tiles only (no reduction kernel), and the image copy, if
         // any, already made by the caller
@@ -2483,25 +2482,29 @@ conv_status igemm_group_launch(int n, const ConvGeom *const *g, const IgemmPlan 
         variant = L.variant;
         grp.cls[c] = L.a;
         grp.cls[c].early_image = after_own_repack && L.tma ? 1 : 0;
-        work += pl[c]->num_units * pl[c]->k_steps;
     }
-    // CTAs for each convolution in proportion to its work (tiles x k-steps;
-    // at least one CTA, at most one per tile), together at most one per SM
+    // CTAs per convolution, together at most one per SM: each CTA walks its
+    // convolution's tiles, a tile costing its k-steps plus about kEpiSteps
+    // k-steps of set-up and epilogue (which dominate the one- and two-tap
+    // classes of a strided data gradient).  Starting from one CTA each, every
+    // further SM goes to the convolution whose CTAs finish last
+    // (ceil(tiles / CTAs) x cost per tile) while it has a tile without a CTA.
+    constexpr int64_t kEpiSteps = 5;
     const int sms = device_sm_count();
     int cta[kMaxGroup];
-    int used = 0;
-    for (int c = 0; c < n; ++c) {
-        int64_t share = (int64_t)sms * pl[c]->num_units * pl[c]->k_steps / work;
-        if (share < 1) share = 1;
-        if (share > pl[c]->num_units) share = pl[c]->num_units;
-        cta[c] = (int)share;
-        used += cta[c];
+    int used = n;
+    for (int c = 0; c < n; ++c) cta[c] = 1;
+    auto span = [&](int c) {
+        return (pl[c]->num_units + cta[c] - 1) / cta[c] * (pl[c]->k_steps + kEpiSteps);
+    };
+    while (used < sms) {
+        int best = -1;
+        for (int c = 0; c < n; ++c)
+            if (cta[c] < pl[c]->num_units && (best < 0 || span(c) > span(best))) best = c;
+        if (best < 0) break;
+        ++cta[best];
+        ++used;
     }
-    for (int c = 0; used > sms && c < n; c = (c + 1) % n)
-        if (cta[c] > 1) {
-            --cta[c];
-            --used;
-        }
     grp.n = n;
     grp.cta_start[0] = 0;
     for (int c = 0; c < n; ++c) grp.cta_start[c + 1] = grp.cta_start[c] + cta[c];
