@@ -1373,6 +1373,7 @@ struct PackFilterJob {
     const int8_t *w;
     int64_t ws0, ws1, ws2, ws3;
     int32_t K, C, R, S, mode, c_steps, k_steps, n_tiles, nt_rows, kperm;
+    FastDiv fd_rows, fd_ksteps, fd_csteps, fd_s;  // by nt_rows, k_steps, c_steps, S
     uint8_t *wp;
 };
 
@@ -1381,18 +1382,34 @@ __device__ __forceinline__ int64_t pack_filter_items(const PackFilterJob &j) {
 }
 
 // Item idx of a repack: 16-byte chunk (idx & 7) of block row idx >> 3.
+// kWide: a repack of 2^31 items or more (64-bit index arithmetic); otherwise
+// the row, k-step, tap and channel block come from multiply-high divisions.
+template <bool kWide>
 __device__ __forceinline__ void pack_filter_item(const PackFilterJob &jb, int64_t idx) {
     const int nt_rows = jb.nt_rows, k_steps = jb.k_steps, c_steps = jb.c_steps;
     const int chunk = (int)(idx & 7);
-    const int64_t t = idx >> 3;
-    const int nl = (int)(t % nt_rows);
-    const int64_t t2 = t / nt_rows;
-    const int j = (int)(t2 % k_steps);
-    const int nt = (int)(t2 / k_steps);
+    int64_t t2;
+    int nl, j, nt, tap, r;
+    if (kWide) {
+        const int64_t t = idx >> 3;
+        nl = (int)(t % nt_rows);
+        t2 = t / nt_rows;
+        j = (int)(t2 % k_steps);
+        nt = (int)(t2 / k_steps);
+        tap = j / c_steps;
+        r = tap / jb.S;
+    } else {
+        const int t = (int)(idx >> 3);
+        const int q = fdiv(t, jb.fd_rows);
+        nl = t - q * nt_rows;
+        t2 = q;
+        nt = fdiv(q, jb.fd_ksteps);
+        j = q - nt * k_steps;
+        tap = fdiv(j, jb.fd_csteps);
+        r = fdiv(tap, jb.fd_s);
+    }
     const int k = nt * nt_rows + nl;
-    const int tap = j / c_steps;
     const int cb = j - tap * c_steps;
-    const int r = tap / jb.S;
     const int s = tap - r * jb.S;
     const int rf = jb.mode ? jb.R - 1 - r : r;
     const int sf = jb.mode ? jb.S - 1 - s : s;
@@ -1428,12 +1445,13 @@ __device__ __forceinline__ void pack_filter_item(const PackFilterJob &jb, int64_
     *reinterpret_cast<uint4 *>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
 }
 
+template <bool kWide>
 __global__ void igemm_pack_filter_kernel(const __grid_constant__ PackFilterJob jb) {
     ptx::launch_dependents();
     const int64_t total = pack_filter_items(jb);
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x)
-        pack_filter_item(jb, idx);
+        pack_filter_item<kWide>(jb, idx);
 }
 
 // Several repacks in one launch (the residue classes of a data gradient):
@@ -1444,6 +1462,7 @@ struct PackFilterJobs {
     int32_t n;
 };
 
+template <bool kWide>
 __global__ void igemm_pack_filter_group_kernel(const __grid_constant__ PackFilterJobs js) {
     ptx::launch_dependents();
     const int64_t total = js.end[js.n - 1];
@@ -1451,7 +1470,7 @@ __global__ void igemm_pack_filter_group_kernel(const __grid_constant__ PackFilte
          idx += (int64_t)gridDim.x * blockDim.x) {
         int i = 0;
         while (idx >= js.end[i]) ++i;
-        pack_filter_item(js.job[i], idx - (i ? js.end[i - 1] : 0));
+        pack_filter_item<kWide>(js.job[i], idx - (i ? js.end[i - 1] : 0));
     }
 }
 
@@ -2070,6 +2089,10 @@ static PackFilterJob pack_job(const ConvGeom &g, const IgemmPlan &pl, const int8
     j.n_tiles = (int32_t)pl.n_tiles;
     j.nt_rows = (int32_t)pl.n_tile;
     j.kperm = pl.nchw_rows ? 1 : 0;
+    j.fd_rows = make_fastdiv(pl.n_tile);
+    j.fd_ksteps = make_fastdiv(pl.k_steps);
+    j.fd_csteps = make_fastdiv(pl.c_steps);
+    j.fd_s = make_fastdiv(g.S);
     j.wp = wp;
     return j;
 }
@@ -2083,7 +2106,10 @@ conv_status igemm_pack_filter_launch(const ConvGeom &g, const IgemmPlan &pl, con
     int64_t blocks = (total + 255) / 256;
     if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
     if (blocks == 0) return CONV_OK;
-    igemm_pack_filter_kernel<<<(unsigned)blocks, 256, 0, st>>>(pack_job(g, pl, w, wp));
+    if (total >= ((int64_t)1 << 31))
+        igemm_pack_filter_kernel<true><<<(unsigned)blocks, 256, 0, st>>>(pack_job(g, pl, w, wp));
+    else
+        igemm_pack_filter_kernel<false><<<(unsigned)blocks, 256, 0, st>>>(pack_job(g, pl, w, wp));
     return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
@@ -2104,7 +2130,10 @@ conv_status igemm_pack_filter_group_launch(int n, const ConvGeom *const *g, cons
     int64_t blocks = (total + 255) / 256;
     if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
     if (blocks == 0) return CONV_OK;
-    igemm_pack_filter_group_kernel<<<(unsigned)blocks, 256, 0, st>>>(js);
+    if (total >= ((int64_t)1 << 31))
+        igemm_pack_filter_group_kernel<true><<<(unsigned)blocks, 256, 0, st>>>(js);
+    else
+        igemm_pack_filter_group_kernel<false><<<(unsigned)blocks, 256, 0, st>>>(js);
     return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 
