@@ -43,6 +43,11 @@
 //    tensor memory with tcgen05.st.16x256b, which permutes the tile's pixels
 //    within each 32-lane quadrant (the epilogue follows) and the channels
 //    within each 16 (the filter repack follows).
+//  * NT = 128 and NT = 192 converting the filter (conv_fprop over a
+//    channels-last image with a channel-contiguous filter): warp 6 lane 0
+//    loads each k-step's int8 filter tile by TMA (a 4-D box {64, 1, 1, NT}
+//    of the caller's filter) into a staging ring, and the converters write
+//    it to the f16 filter stage next to their image tile: no repack launch.
 //  * global loads (fallback when a TMA map cannot express the call):
 //    warpgroup 0 threads each own one pixel row, gather 64 channels of one
 //    tap with 16-byte loads one item ahead (address formed from stride,
@@ -67,7 +72,10 @@
 // CONV_ERR_DEVICE_TIMEOUT, stops, lets issued copies and MMAs finish and frees
 // its tensor memory.
 // Launch plans (tensor maps, grid, variant) are cached per call shape; a
-// repeated call only re-targets the maps' addresses.
+// repeated call only re-targets the maps' addresses.  Behind the call's own
+// filter repack the image issuers and converters start without waiting for
+// it (griddepcontrol.wait only where the filter, the output or the workspace
+// is touched).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>

@@ -354,6 +354,9 @@ def _filter_in_kernel_cases():
           seed=92),
         # 1x1 over pixel rows, channel-major output
         C("selfw_1x1_nchw_out", 4, 128, 12, 16, 64, 1, 1, y_layout="NCHW", seed=93),
+        # two tiles, 144 k-steps: each tile cut into runs (the reduction
+        # kernel adds their int32 sums)
+        C("selfw_cut_tiles", 1, 1024, 12, 12, 128, 3, 3, pre=(1, 1), post=(1, 1), seed=94),
     ]
 
 
@@ -370,7 +373,8 @@ def test_filter_converted_in_kernel(ic, case, w_pad):
         wd = ic.TensorDesc.packed(ic.CONV_INT8, case.w_dims, case.w_layout)
         yd = ic.TensorDesc.packed(ic.CONV_INT32, case.y_dims, case.y_layout)
         p = ic.Params.make(case.pre, case.post, case.stride, case.dilation, case.mode, case.bias, case.relu)
-        assert ic.kernel_count(xd, wd, yd, p) == 1
+        # the convolution (and the reduction of cut tiles), no repack
+        assert ic.kernel_count(xd, wd, yd, p) == (2 if case.name == "selfw_cut_tiles" else 1)
     got, ref = _run_both(ic, case, w_pad=w_pad)
     _assert_equal(got, ref, f"{case.name} w_pad {w_pad}")
     got, ref = _run_both(ic, case, w_pad=w_pad, out_shift=9)
