@@ -121,11 +121,13 @@ __global__ void __launch_bounds__(kDp4aThreads) conv_direct_dp4a_kernel(const Di
     __shared__ long long s_off[kDp4aMaxRed];  // image offset of element e relative to (n, h0, w0)
     __shared__ int s_dh[kDp4aMaxRed];         // r*dil_h (or -1<<30 for padding elements)
     __shared__ int s_dw[kDp4aMaxRed];
-    const int64_t red = a.C * a.R * a.S;
+    // (C*R*S <= kDp4aMaxRed: the reduction index and its tap fit 32 bits)
+    const int red = (int)(a.C * a.R * a.S);
+    const int S = (int)a.S, R = (int)a.R;
     const int64_t k0 = (int64_t)blockIdx.y * kDp4aKB;
     for (int e = threadIdx.x; e < red4 * 4; e += blockDim.x) {
         if (e < red) {
-            const int64_t s = e % a.S, r = (e / a.S) % a.R, c = e / (a.S * a.R);
+            const int s = e % S, r = (e / S) % R, c = e / (S * R);
             s_off[e] = c * a.xs1 + r * a.dil_h * a.xs2 + s * a.dil_w * a.xs3;
             s_dh[e] = (int)(r * a.dil_h);
             s_dw[e] = (int)(s * a.dil_w);
@@ -138,18 +140,21 @@ __global__ void __launch_bounds__(kDp4aThreads) conv_direct_dp4a_kernel(const Di
     for (int i = threadIdx.x; i < kDp4aKB * red4; i += blockDim.x) {
         const int kk = i / red4, u = i % red4;
         const int64_t k = k0 + kk;
-        uint32_t word = 0;
+        int8_t v[4];
+#pragma unroll
         for (int b = 0; b < 4; ++b) {
-            const int64_t e = (int64_t)u * 4 + b;
-            int8_t v = 0;
+            const int e = u * 4 + b;
+            v[b] = 0;
             if (k < a.K && e < red) {
-                const int64_t s = e % a.S, r = (e / a.S) % a.R, c = e / (a.S * a.R);
-                const int64_t rf = a.mode ? a.R - 1 - r : r;
-                const int64_t sf = a.mode ? a.S - 1 - s : s;
-                v = a.w[k * a.ws0 + c * a.ws1 + rf * a.ws2 + sf * a.ws3];
+                const int s = e % S, r = (e / S) % R, c = e / (S * R);
+                const int rf = a.mode ? R - 1 - r : r;
+                const int sf = a.mode ? S - 1 - s : s;
+                v[b] = __ldg(a.w + (k * a.ws0 + c * a.ws1 + rf * a.ws2 + sf * a.ws3));
             }
-            word |= (uint32_t)(uint8_t)v << (8 * b);
         }
+        uint32_t word = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) word |= (uint32_t)(uint8_t)v[b] << (8 * b);
         s_w[kk][u] = (int32_t)word;
     }
     __syncthreads();
@@ -168,19 +173,27 @@ __global__ void __launch_bounds__(kDp4aThreads) conv_direct_dp4a_kernel(const Di
         int32_t acc[kDp4aKB];
 #pragma unroll
         for (int kk = 0; kk < kDp4aKB; ++kk) acc[kk] = 0;
-        for (int u = 0; u < red4; ++u) {
-            uint32_t word = 0;
+        // four reduction words (16 image bytes) per round, all their loads
+        // in flight together
+        for (int u0 = 0; u0 < red4; u0 += 4) {
+            int8_t v[16];
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                const int e = u * 4 + b;
-                const int64_t h = h0 + s_dh[e];
-                const int64_t w = w0 + s_dw[e];
-                int8_t v = 0;
-                if (h >= 0 && h < a.H && w >= 0 && w < a.W) v = __ldg(a.x + (base + s_off[e]));
-                word |= (uint32_t)(uint8_t)v << (8 * b);
+            for (int i = 0; i < 16; ++i) {
+                const int e = u0 * 4 + i;
+                const int64_t h = h0 + s_dh[e < red4 * 4 ? e : 0];
+                const int64_t w = w0 + s_dw[e < red4 * 4 ? e : 0];
+                v[i] = 0;
+                if (e < red4 * 4 && h >= 0 && h < a.H && w >= 0 && w < a.W) v[i] = __ldg(a.x + (base + s_off[e]));
             }
 #pragma unroll
-            for (int kk = 0; kk < kDp4aKB; ++kk) acc[kk] = __dp4a((int)word, s_w[kk][u], acc[kk]);
+            for (int uu = 0; uu < 4; ++uu) {
+                if (u0 + uu >= red4) break;
+                const uint32_t word = (uint32_t)(uint8_t)v[4 * uu] | ((uint32_t)(uint8_t)v[4 * uu + 1] << 8) |
+                                      ((uint32_t)(uint8_t)v[4 * uu + 2] << 16) |
+                                      ((uint32_t)(uint8_t)v[4 * uu + 3] << 24);
+#pragma unroll
+                for (int kk = 0; kk < kDp4aKB; ++kk) acc[kk] = __dp4a((int)word, s_w[kk][u0 + uu], acc[kk]);
+            }
         }
 #pragma unroll
         for (int kk = 0; kk < kDp4aKB; ++kk) {
