@@ -533,11 +533,9 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
         const Unit w = unit_at(u, a.full_units, a.splits, a.k_steps);
         total += w.ke - w.kb;
     }
-    // TMA path: each CTA walks the reduction of a whole tile starting at its
-    // own k-step, so the SMs do not all fetch the same filter block at the
-    // same moment (any order is exact: a group is any run of at most 1024
-    // products)
-    const int rot = kTma ? (int)(((int64_t)bid * 7) % a.k_steps) : 0;
+    // (every CTA walks a tile's reduction in k-step order, so at any moment
+    // most SMs read the same filter block: faster, from L2, than spreading
+    // them over the blocks by starting each CTA at its own k-step)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < ST; ++i) {
@@ -621,7 +619,6 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
         for (int uu = bid; uu < a.num_units && ok; uu += gdim) {
             const Unit wu = unit_at(uu, a.full_units, a.splits, a.k_steps);
             const int kn = wu.ke - wu.kb;
-            const int urot = wu.split < 0 ? rot : 0;
             const int m0 = fdiv(wu.tile, a.fd_nt) * MT;
             const int rem = m0 - fdiv(m0, a.fd_pq) * pq;
             const int q0 = rem - fdiv(rem, a.fd_q) * a.Q;
@@ -631,10 +628,9 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
             const int b = fdiv(f, a.fd_q);
             const int q = f - b * a.Q;
             const uint32_t pix = (uint32_t)b * boxb + (uint32_t)u * rowb;
-            // the k-steps in the issuers' order (rotated), for the tap column s
-            int jr = wu.kb + urot;
-            int tap = fdiv(jr, a.fd_cs);
-            int cb = jr - tap * a.c_steps;
+            // the unit's k-steps in order, for the tap column s
+            const int tap = fdiv(wu.kb, a.fd_cs);
+            int cb = wu.kb - tap * a.c_steps;
             int r = fdiv(tap, a.fd_s);
             int s = tap - r * a.S;
 #pragma unroll 1
@@ -688,13 +684,7 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
                 ptx::mbar_arrive(ptx::smem_addr(&ctl->full[ra.idx]));
                 ra.next();
                 rs.next();
-                if (++jr == wu.ke) {
-                    jr = wu.kb;
-                    tap = fdiv(jr, a.fd_cs);
-                    cb = jr - tap * a.c_steps;
-                    r = fdiv(tap, a.fd_s);
-                    s = tap - r * a.S;
-                } else if (++cb == a.c_steps) {
+                if (++cb == a.c_steps) {
                     cb = 0;
                     if (++s == a.S) {
                         s = 0;
@@ -892,7 +882,6 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
                 const Unit w = unit_at(u, a.full_units, a.splits, a.k_steps);
                 const int kn = w.ke - w.kb;
                 const int ng = groups_of(kn);
-                const int urot = w.split < 0 ? rot : 0;
                 for (int g = 0; g < ng && ok; ++g) {
                     const int js = (int)(((int64_t)g * kn) / ng);
                     const int je = (int)(((int64_t)(g + 1) * kn) / ng);
@@ -918,11 +907,8 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
                         // ordered before the MMAs by their fence, the barrier
                         // and this fence
                         if (kTmemA) ptx::tc_fence_after();
-                        // resident filter: the block of this k-step (the
-                        // producers walk the unit's k-steps from its rotation)
-                        int jr = j + urot;
-                        if (jr >= kn) jr -= kn;
-                        const uint64_t bdesc = kResB ? bdesc0 + (uint64_t)((w.kb + jr) * (B_BYTES >> 4))
+                        // resident filter: the block of this k-step
+                        const uint64_t bdesc = kResB ? bdesc0 + (uint64_t)((w.kb + j) * (B_BYTES >> 4))
                                                      : bdesc0 + (uint64_t)(rg.idx * (B_BYTES >> 4));
 #pragma unroll
                         for (int kk = 0; kk < KS / 16; ++kk) {
@@ -959,7 +945,6 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
             for (int u = bid; u < a.num_units && ok; u += gdim) {
                 const Unit wu = unit_at(u, a.full_units, a.splits, a.k_steps);
                 const int kn = wu.ke - wu.kb;
-                const int urot = wu.split < 0 ? rot : 0;
                 const int m0 = fdiv(wu.tile, a.fd_nt) * MT;
                 const int n0 = fdiv(m0, a.fd_pq);
                 const int rem = m0 - n0 * pq;
@@ -971,12 +956,11 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
                 // (into the next image past P - 1), one image-row box each
                 const int nrows = kNchw ? fdiv(q0 + MT - 1, a.fd_q) + 1 : 1;
                 const uint32_t box_bytes = (uint32_t)(KS * a.W);
-                // k-step kb + ((j + urot) mod kn), held as (tap row r, tap
-                // column s, channel block cb) and advanced without divisions
-                // (the issuing thread's loop is on every k-step's path)
-                int jr = wu.kb + urot;
-                int tap = fdiv(jr, a.fd_cs);
-                int cb = jr - tap * a.c_steps;
+                // k-step kb + j, held as (tap row r, tap column s, channel
+                // block cb) and advanced without divisions (the issuing
+                // thread's loop is on every k-step's path)
+                const int tap = fdiv(wu.kb, a.fd_cs);
+                int cb = wu.kb - tap * a.c_steps;
                 int r = fdiv(tap, a.fd_s);
                 int s = tap - r * a.S;
 #pragma unroll 1
@@ -1017,13 +1001,7 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
                     }
                     ++issued;
                     rs.next();
-                    if (++jr == wu.ke) {  // the rotated sequence wraps to the unit's first k-step
-                        jr = wu.kb;
-                        tap = fdiv(jr, a.fd_cs);
-                        cb = jr - tap * a.c_steps;
-                        r = fdiv(tap, a.fd_s);
-                        s = tap - r * a.S;
-                    } else if (++cb == a.c_steps) {
+                    if (++cb == a.c_steps) {
                         cb = 0;
                         if (++s == a.S) {
                             s = 0;
@@ -1043,8 +1021,8 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
                 ptx::bulk_copy_g2s(b_smem + j * B_BYTES, a.wp + (size_t)j * B_BYTES, B_BYTES, bar);
             (void)drain_phase(bar, 0, limit, a.status);
         } else if (kSelfB && warp == B_ISSUER_WARP && lane == 0) {
-            // int8 filter tiles by TMA, in the rotated k-step order of the
-            // image tiles: for tap (r, s) and channel block cb the box
+            // int8 filter tiles by TMA, in the k-step order of the image
+            // tiles: for tap (r, s) and channel block cb the box
             // {64 channels, 1, 1, NT rows} of the {C, S, R, K} map at
             // (cb*64, s, r, nt*NT), the taps flipped (S-1-s, R-1-r) for
             // CONVOLUTION; channels past C and rows past K read as zeros
@@ -1053,13 +1031,8 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
             bool ok = true;
             for (int u = bid; u < a.num_units && ok; u += gdim) {
                 const Unit wu = unit_at(u, a.full_units, a.splits, a.k_steps);
-                const int kn = wu.ke - wu.kb;
-                const int urot = wu.split < 0 ? rot : 0;
                 const int nt = wu.tile - fdiv(wu.tile, a.fd_nt) * a.n_tiles;
-                for (int j = 0; j < kn; ++j) {
-                    int jr = j + urot;
-                    if (jr >= kn) jr -= kn;
-                    jr += wu.kb;
+                for (int jr = wu.kb; jr < wu.ke; ++jr) {
                     const int tap = fdiv(jr, a.fd_cs);
                     const int cb = jr - tap * a.c_steps;
                     const int r = fdiv(tap, a.fd_s);
@@ -1080,20 +1053,15 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
             if (*abort_flag) drain_ring(ctl->bstg_full, Cfg::BSTG, issued, limit, a.status);
         } else if (kTma && warp == B_ISSUER_WARP && lane == 0) {
             // pre-swizzled f16 filter blocks, one bulk copy per k-step, in the
-            // same rotated k-step order as the image tiles
+            // k-step order of the image tiles
             Ring<ST> rb;
             int64_t issued = 0;
             bool ok = true;
             for (int u = bid; u < a.num_units && ok; u += gdim) {
                 const Unit wu = unit_at(u, a.full_units, a.splits, a.k_steps);
-                const int kn = wu.ke - wu.kb;
-                const int urot = wu.split < 0 ? rot : 0;
                 const int nt = wu.tile - fdiv(wu.tile, a.fd_nt) * a.n_tiles;
                 const uint8_t *blk = a.wp + (size_t)nt * a.k_steps * (size_t)B_BYTES;
-                for (int j = 0; j < kn; ++j) {
-                    int jr = j + urot;
-                    if (jr >= kn) jr -= kn;
-                    jr += wu.kb;
+                for (int jr = wu.kb; jr < wu.ke; ++jr) {
                     if (!wait_phase(ptx::smem_addr(&ctl->empty[rb.idx]), rb.phase ^ 1u, abort_flag, limit,
                                     a.status, kIssuerBackoffNs)) {
                         ok = false;
