@@ -357,6 +357,10 @@ def _filter_in_kernel_cases():
         # two tiles, 144 k-steps: each tile cut into runs (the reduction
         # kernel adds their int32 sums)
         C("selfw_cut_tiles", 1, 1024, 12, 12, 128, 3, 3, pre=(1, 1), post=(1, 1), seed=94),
+        # an NCHW image of 20-byte rows (copied to channels-last first) with a
+        # KRSC filter (converted in the kernel)
+        C("selfw_nchw_copy", 2, 48, 11, 20, 80, 3, 3, pre=(1, 1), post=(1, 1), x_layout="NCHW", y_layout="NCHW",
+          seed=95),
     ]
 
 
@@ -373,8 +377,9 @@ def test_filter_converted_in_kernel(ic, case, w_pad):
         wd = ic.TensorDesc.packed(ic.CONV_INT8, case.w_dims, case.w_layout)
         yd = ic.TensorDesc.packed(ic.CONV_INT32, case.y_dims, case.y_layout)
         p = ic.Params.make(case.pre, case.post, case.stride, case.dilation, case.mode, case.bias, case.relu)
-        # the convolution (and the reduction of cut tiles), no repack
-        assert ic.kernel_count(xd, wd, yd, p) == (2 if case.name == "selfw_cut_tiles" else 1)
+        # the convolution (and the reduction of cut tiles, or the image
+        # copy before it), no repack
+        assert ic.kernel_count(xd, wd, yd, p) == (2 if case.name in ("selfw_cut_tiles", "selfw_nchw_copy") else 1)
     got, ref = _run_both(ic, case, w_pad=w_pad)
     _assert_equal(got, ref, f"{case.name} w_pad {w_pad}")
     got, ref = _run_both(ic, case, w_pad=w_pad, out_shift=9)
