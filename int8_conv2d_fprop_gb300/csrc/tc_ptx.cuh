@@ -112,6 +112,26 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int3
         : "memory");
 }
 
+// L2 prefetches of the boxes the loads above would bring (no shared memory,
+// no barrier; the data only moves from DRAM into L2).
+__device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tmap), "r"(x), "r"(y)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_4d(const void *tmap, int32_t x, int32_t y, int32_t z, int32_t w) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(tmap), "r"(x),
+                 "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_im2col_4d(const void *tmap, int32_t c, int32_t w, int32_t h, int32_t n,
+                                                       uint16_t off_w, uint16_t off_h) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.im2col [%0, {%1, %2, %3, %4}], {%5, %6};" ::"l"(tmap),
+                 "r"(c), "r"(w), "r"(h), "r"(n), "h"(off_w), "h"(off_h)
+                 : "memory");
+}
+
 // Tensor copy shared -> global of a 2-D box at coordinates (x, y), tracked
 // in this thread's bulk async-group; elements outside the tensor are not
 // written.
