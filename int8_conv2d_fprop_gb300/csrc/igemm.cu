@@ -636,12 +636,10 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
     // (otherwise, in the 128- and 192-column variants, the first image tiles
     // are brought into L2 while the wait lasts, by an epilogue warp, which
     // has nothing to do until then, so that the image issuers' loads do not
-    // queue behind the prefetches: 1x1 and 7x1 workloads 1.0 and 1.2 us
-    // faster.  Not in calls that cut tiles: one like them follows its
-    // reduction kernel, which lets nothing start early, so there is no wait
-    // to fill.  The 256-column kernel does without: with the prefetch
-    // compiled in, the 3x3 workload ran 1 us slower even where it was not
-    // executed.)
+    // queue behind the prefetches.  Not in calls that cut tiles: a call like
+    // them follows its reduction kernel, which lets nothing start early, so
+    // there is no wait to fill.  The 256-column kernel, measured slower with
+    // the prefetch compiled in, does without.)
     if (kTma && kTmemA && !a.early_image && a.splits <= 1 && warp == FIRST_EPI_WARP && lane == 0)
         prefetch_first_image_tiles<kNchw>(a, bid, STG);
     if (!(kTma && a.early_image && image_role)) ptx::grid_dependency_wait();
