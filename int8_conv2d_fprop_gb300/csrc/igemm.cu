@@ -121,6 +121,10 @@ constexpr int B_ISSUER_WARP = 6;    // TMA path: issues the filter block copies
 // rows x EPI_COLS int32 columns: 16 (64-byte rows, 64-byte swizzle) or, in
 // the tensor-memory variant, 32 (128-byte rows, 128-byte swizzle: half as
 // many store copies, which share each SM's TMA unit with the image loads).
+// One buffer for 192- and 256-column tiles: a warp's next store then waits
+// until its last one has read the buffer, which spaces the stores out
+// between the main loop's loads (measured faster for those tiles; the
+// 128-column tiles' short last epilogue wants two).
 // Resident-filter variant: when the whole repacked filter of a call (one
 // tile of output channels) fits in this many bytes, every CTA loads it once
 // and keeps it in shared memory, so a k-step brings only its image tile.
@@ -160,8 +164,7 @@ constexpr int NCHW_MAX_ROW_BYTES = NCHW_STG_BYTES / KS;
 #endif
 
 // kResB: the filter blocks of all k-steps stay resident (loaded once per
-// CTA); the ring then holds image tiles only, and each epilogue warp stages
-// its stores in one buffer instead of two.
+// CTA); the ring then holds image tiles only.
 // kTmemA (128- and 192-column tiles, TMA path): the f16 image tile of a
 // k-step goes to tensor memory (columns 2*NT.. next to the two accumulator
 // slots, 32 columns per stage: 256..383 or 384..511) and the MMA reads it
@@ -197,7 +200,7 @@ struct TileCfg {
                                     : kNchw ? (NT == 128 ? 6 : 8)
                                     : kTmemA ? (kResB ? 10 : (NT == 128 ? IGEMM_STG_TM128 : 12))
                                              : (kResB ? 6 : (kTma ? (NT == 256 ? IGEMM_STG_256 : (NT == 192 ? 4 : IGEMM_STG_128)) : 0));
-    static constexpr int EPI_BUFS = kResB ? 1 : 2;  // output staging buffers per epilogue warp
+    static constexpr int EPI_BUFS = (kResB || NT >= 192) ? 1 : 2;  // output staging buffers per epilogue warp
     // output columns per staged store: 32 for the 128-column tensor-memory
     // variant (its shared memory has room for 4 KB buffers), else 16
     static constexpr int EPI_COLS = (kTmemA && NT == 128 && !kSelfB) ? 32 : 16;
@@ -1310,7 +1313,8 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
                 // swizzle, or at c ^ (r & 7), the 128-byte swizzle) and one
                 // lane writes them with a TMA store, which also clips rows
                 // past the last pixel and columns past K.  With two buffers
-                // per warp they alternate.
+                // per warp they alternate; with one, each store waits for
+                // the last to have read it.
                 constexpr int CHUNKS = Cfg::EPI_COLS / 4;  // 16-byte chunks per staged row
                 const int k0 = nt * NT + col0;
                 const int m0w = mt * MT + quad * 32;
