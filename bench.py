@@ -374,6 +374,9 @@ def time_workload(ic, cfg, dev, stream, flush, iters: int, warmup: int, peaks: d
         "workload": workload_label(cfg), "algo": algo, "ops": cfg.ops,
         "ms": round(ms, 5), "value": round(cfg.ops / (ms * 1e-3) / 1e12, 3), "unit": "TOPS",
         "kernel_ms": round(kms, 5), "kernel_share": round(kms / ms, 4), "timing": how,
+        "kernel_ms_source": ("convolution-only calls (conv_fprop_prepacked, repacked filter); where the step's "
+                             "one kernel converts the filter itself it is another kernel variant, and the "
+                             "share can exceed 1"),
         "isolated_step_ms_median": round(_median(step_ms), 5),
         "isolated_kernel_ms_median": round(_median(conv_ms), 5),
         "warm_ms": round(_median(warm_ms), 5),
