@@ -192,6 +192,18 @@ conv_status conv_fprop_workspace_size(const conv_tensor_desc *x, const conv_tens
 conv_status conv_fprop_kernel_count(const conv_tensor_desc *x, const conv_tensor_desc *w,
                                     const conv_tensor_desc *y, const conv_fprop_params *p, int32_t *count);
 
+/* Tile shape of the implicit-GEMM convolution for this call, under the same
+ * alignment assumption: shape[0] output pixels per tile (128), shape[1]
+ * output channels per tile (128, 192 or 256: the smallest that covers K),
+ * shape[2] the number of tiles, shape[3] the number of work units (whole
+ * tiles, plus the runs of the tiles cut along the reduction: calls with
+ * fewer tiles than SMs and long reductions, or a short partial last round,
+ * on the current device).  All four are 0 for the direct kernels and for
+ * an empty output.  Errors as conv_fprop_validate; CONV_ERR_NULL_PTR if
+ * shape is NULL.  Host-only; no device work. */
+conv_status conv_fprop_tile_shape(const conv_tensor_desc *x, const conv_tensor_desc *w,
+                                  const conv_tensor_desc *y, const conv_fprop_params *p, int64_t shape[4]);
+
 /*
  * Y = conv_fprop(X, W) on `stream` (a cudaStream_t; NULL = legacy default).
  * x_dev, w_dev, y_dev, bias_dev and workspace are device pointers on the

@@ -46,7 +46,7 @@ STATUS_CODE = {v: k for k, v in STATUS.items()}
 EXPORTED_SYMBOLS = (
     "conv_params_init", "conv_params_set_symmetric_padding", "conv_tensor_desc_packed",
     "conv_fprop_output_dims", "conv_fprop_validate", "conv_fprop_plan", "conv_fprop_workspace_size",
-    "conv_fprop_kernel_count",
+    "conv_fprop_kernel_count", "conv_fprop_tile_shape",
     "conv_fprop", "conv_fprop_pack_filter", "conv_fprop_prepacked", "conv_fprop_static_workspace",
     "conv_fprop_host_buffer_size", "conv_fprop_host", "conv_device_status",
     "conv_selftest_wait_timeout", "conv_status_string", "conv_library_version",
@@ -159,6 +159,7 @@ def lib():
         L.conv_fprop_plan.argtypes = [D, D, D, P, ctypes.POINTER(ctypes.c_int32)]
         L.conv_fprop_workspace_size.argtypes = [D, D, D, P, ctypes.POINTER(ctypes.c_size_t)]
         L.conv_fprop_kernel_count.argtypes = [D, D, D, P, ctypes.POINTER(ctypes.c_int32)]
+        L.conv_fprop_tile_shape.argtypes = [D, D, D, P, i64p]
         L.conv_fprop.argtypes = [D, ctypes.c_void_p, D, ctypes.c_void_p, D, ctypes.c_void_p, ctypes.c_void_p,
                                  P, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
         L.conv_fprop_pack_filter.argtypes = [D, D, ctypes.c_void_p, D, P, ctypes.c_void_p, ctypes.c_size_t,
@@ -240,6 +241,15 @@ def kernel_count(xd: TensorDesc, wd: TensorDesc, yd: TensorDesc, p: Params) -> i
     _check(lib().conv_fprop_kernel_count(ctypes.byref(xd), ctypes.byref(wd), ctypes.byref(yd), ctypes.byref(p),
                                          ctypes.byref(out)), "kernel count")
     return int(out.value)
+
+
+def tile_shape(xd: TensorDesc, wd: TensorDesc, yd: TensorDesc, p: Params) -> tuple:
+    """(pixels per tile, channels per tile, tiles, work units) of the
+    implicit-GEMM convolution for this call (see the header)."""
+    out = (ctypes.c_int64 * 4)()
+    _check(lib().conv_fprop_tile_shape(ctypes.byref(xd), ctypes.byref(wd), ctypes.byref(yd), ctypes.byref(p), out),
+           "tile shape")
+    return tuple(int(v) for v in out)
 
 
 def conv_fprop_raw(xd: TensorDesc, x_ptr: int, wd: TensorDesc, w_ptr: int, yd: TensorDesc, y_ptr: int,

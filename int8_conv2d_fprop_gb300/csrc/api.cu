@@ -281,6 +281,23 @@ conv_status conv_fprop_kernel_count(const conv_tensor_desc *x, const conv_tensor
     return CONV_OK;
 }
 
+conv_status conv_fprop_tile_shape(const conv_tensor_desc *x, const conv_tensor_desc *w,
+                                  const conv_tensor_desc *y, const conv_fprop_params *p, int64_t shape[4]) {
+    if (!shape) return CONV_ERR_NULL_PTR;
+    ConvGeom g;
+    IgemmPlan pl;
+    int algo = 0;
+    conv_status st = plan_call(x, w, y, p, nullptr, &g, &algo, &pl);
+    if (st) return st;
+    for (int i = 0; i < 4; ++i) shape[i] = 0;
+    if (g.N == 0 || g.K == 0 || g.P == 0 || g.Q == 0 || algo != CONV_ALGO_IMPLICIT_GEMM) return CONV_OK;
+    shape[0] = kIgemmMTile;
+    shape[1] = pl.n_tile;
+    shape[2] = pl.m_tiles * pl.n_tiles;
+    shape[3] = pl.num_units;
+    return CONV_OK;
+}
+
 namespace {
 
 // Validation, planning and pointer checks shared by the three entry points

@@ -246,6 +246,27 @@ def test_more_tiles_than_sms_matches_oracle(ic, case):
     _assert_equal(got2, ref, case.name + " (second call)")
 
 
+def test_tile_shape_on_the_device(ic):
+    """The planner's tiles and work units on this GPU: with 152 SMs the 3x3
+    workload's 784 tiles leave a partial sixth round of 24 tiles, each cut
+    into 6 runs of its 36 k-steps (760 whole tiles + 144 runs); the other
+    workloads run whole tiles."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    shapes = {}
+    for name in ("c2_s2_nhwc", "c3_3x3_large", "c4_1x1_bias_relu", "c5_7x1_dilated_conv"):
+        cfg = synth.CONFIGS[name]
+        shapes[name] = ic.tile_shape(ic.TensorDesc.packed(ic.CONV_INT8, cfg.x_dims, cfg.x_layout),
+                                     ic.TensorDesc.packed(ic.CONV_INT8, cfg.w_dims, cfg.w_layout),
+                                     ic.TensorDesc.packed(ic.CONV_INT32, cfg.y_dims, cfg.y_layout),
+                                     ic.Params.make(cfg.pre, cfg.post, cfg.stride, cfg.dilation, cfg.mode,
+                                                    cfg.bias, cfg.relu))
+    assert shapes["c2_s2_nhwc"] == (128, 128, 49, 49)
+    assert shapes["c4_1x1_bias_relu"] == (128, 128, 392, 392)
+    assert shapes["c5_7x1_dilated_conv"] == (128, 192, 672, 672)
+    if sms == 152:
+        assert shapes["c3_3x3_large"] == (128, 256, 784, 760 + 24 * 6)
+
+
 def test_more_tiles_than_sms_int8_output(ic):
     cfg = _partial_round_cases()[1]
     got, ref = _run_both(ic, cfg, out_shift=14)

@@ -236,6 +236,21 @@ def test_planner_choices_and_workspace(ic):
     assert ic.validate(xd, wd, yd, p) == _code(ic, "CONV_ERR_BAD_PARAM")
 
 
+def test_tile_shape_query(ic):
+    """conv_fprop_tile_shape: pixels and channels per tile, tiles and work
+    units of the implicit GEMM; zeros for the direct kernels.  Without a GPU
+    the planner assumes one SM, so no call cuts its tiles."""
+    shapes = {name: ic.tile_shape(*_descs(ic, cfg)) for name, cfg in synth.CONFIGS.items()}
+    assert shapes["c1_tiny_nchw"] == (0, 0, 0, 0) and shapes["p4_shape"] == (0, 0, 0, 0)
+    assert shapes["c2_s2_nhwc"] == (128, 128, 49, 49)
+    assert shapes["c3_3x3_large"] == (128, 256, 784, 784)
+    assert shapes["c4_1x1_bias_relu"] == (128, 128, 392, 392)
+    assert shapes["c5_7x1_dilated_conv"] == (128, 192, 672, 672)
+    xd, wd, yd, p = _descs(ic, synth.CONFIGS["c4_1x1_bias_relu"])
+    st = ic.lib().conv_fprop_tile_shape(ctypes.byref(xd), ctypes.byref(wd), ctypes.byref(yd), ctypes.byref(p), None)
+    assert st == _code(ic, "CONV_ERR_NULL_PTR")
+
+
 @pytest.mark.parametrize("W,pre_w,dil_w,S,K,stride_w,in_place", [
     (96, 0, 1, 1, 192, 1, True),     # the 7x1 workload's rows: two output rows per tile
     (64, 0, 1, 1, 128, 1, True),
