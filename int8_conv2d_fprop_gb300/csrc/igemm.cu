@@ -200,14 +200,22 @@ struct TileCfg {
                                     : kNchw ? (NT == 128 ? 6 : 8)
                                     : kTmemA ? (kResB ? 10 : (NT == 128 ? IGEMM_STG_TM128 : 12))
                                              : (kResB ? 6 : (kTma ? (NT == 256 ? IGEMM_STG_256 : (NT == 192 ? 4 : IGEMM_STG_128)) : 0));
-    static constexpr int EPI_BUFS = (kResB || NT >= 192) ? 1 : 2;  // output staging buffers per epilogue warp
+    // output staging buffers per epilogue warp while the CTA has tiles to
+    // come (one: each store waits for the last to have read it, which
+    // spaces the stores out between the main loop's loads)
+    static constexpr int EPI_BUFS = (kResB || NT >= 192) ? 1 : 2;
     // output columns per staged store: 32 for the 128-column tensor-memory
     // variant (its shared memory has room for 4 KB buffers), else 16
     static constexpr int EPI_COLS = (kTmemA && NT == 128 && !kSelfB) ? 32 : 16;
     static constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 4;  // 2 or 4 KB
-    static constexpr int EPI_BYTES = 8 * EPI_BUFS * EPI_BUF_BYTES;
     static constexpr int A_SMEM = kTmemA ? 0 : ST * A_BYTES;
     static constexpr int B_AREA = kResB ? RESB_MAX_BYTES : ST * B_BYTES;
+    static constexpr int SMEM_NO_EPI = 1024 /*align slack*/ + A_SMEM + B_AREA + STG_STAGES * STG_SLOT +
+                                       BSTG * BSTG_SLOT + 1024 /*barriers*/;
+    // buffers allocated: two where they fit, so that the CTA's last tile
+    // (nothing left to overlap its stores with) alternates between them
+    static constexpr int EPI_ALLOC = SMEM_NO_EPI + 8 * 2 * EPI_BUF_BYTES <= 227 * 1024 ? 2 : EPI_BUFS;
+    static constexpr int EPI_BYTES = 8 * EPI_ALLOC * EPI_BUF_BYTES;
     // (allocations are powers of two: two 192-column slots take 512)
     static constexpr int TMEM_COLS = (kTmemA || NT == 192) ? 512 : NSLOT * NT;
     static constexpr int TMEM_A_COL = NSLOT * NT;  // kTmemA: first column of the image stages
@@ -219,8 +227,7 @@ struct TileCfg {
     // not help: their divergent branches run one after the other.)
     static constexpr int A_ISSUERS = kTmemA ? 2 : 1;
     static_assert(STG_STAGES % A_ISSUERS == 0, "staging slots split evenly between the issuers");
-    static constexpr int SMEM_BYTES = 1024 /*align slack*/ + A_SMEM + B_AREA + STG_STAGES * STG_SLOT +
-                                      BSTG * BSTG_SLOT + EPI_BYTES + 1024 /*barriers*/;
+    static constexpr int SMEM_BYTES = SMEM_NO_EPI + EPI_BYTES;
     static_assert(!kResB || kTma, "the resident filter needs the TMA producers");
     static_assert(!kNchw || (kTmemA && !kResB), "NCHW rows feed the tensor-memory image stages");
     static_assert(!kSelfB || (kTmemA && !kResB && !kNchw), "in-kernel filter conversion: tensor-memory variants");
@@ -1148,6 +1155,19 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
         const int prow = kNchw ? (((lane & 7) << 2) | (lane >> 3)) : lane;
         const int row = quad * 32 + prow;
         const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)col0;
+        // output staging buffer of store ch: alternating between two (the
+        // last tile of a one-buffer variant starts on the second, which no
+        // store has read yet), or the one; and the wait for the store that
+        // last read it
+        auto epi_buf_index = [](int ch, bool two) -> uint32_t {
+            return Cfg::EPI_BUFS == 2 ? (uint32_t)(ch & 1) : (two ? (uint32_t)((ch + 1) & 1) : 0u);
+        };
+        auto epi_wait_buffer = [](bool two) {
+            if (two)
+                ptx::bulk_wait_group_read<1>();
+            else
+                ptx::bulk_wait_group_read<0>();
+        };
         uint32_t gi = 0;
         bool ok = true;
         for (int u = bid; u < a.num_units && ok; u += gdim) {
@@ -1215,6 +1235,7 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
                 ++gi;
             }
             if (!ok) break;
+            const bool two_bufs = Cfg::EPI_BUFS == 2 || (Cfg::EPI_ALLOC == 2 && u + gdim >= a.num_units);
             if (wu.split >= 0) {
                 // one run of a cut tile: its raw int32 sums go to the
                 // workspace as int4 quads, [cut tile][split][column quad][row]
@@ -1254,11 +1275,11 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
                 const int pq = a.P * a.Q;
                 const int img = fdiv(m0w, a.fd_pq);
                 const int pix = m0w - img * pq;
-                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (uint32_t)(Cfg::EPI_BUFS * Cfg::EPI_BUF_BYTES);
+                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (uint32_t)(Cfg::EPI_ALLOC * Cfg::EPI_BUF_BYTES);
 #pragma unroll
                 for (int ch = 0; ch < HALF / Cfg::EPI_COLS; ++ch) {
-                    const uint32_t buf = ebase + (uint32_t)(ch % Cfg::EPI_BUFS) * Cfg::EPI_BUF_BYTES;
-                    if (lane == 0) ptx::bulk_wait_group_read<Cfg::EPI_BUFS - 1>();  // the store that last read buf is done
+                    const uint32_t buf = ebase + epi_buf_index(ch, two_bufs) * Cfg::EPI_BUF_BYTES;
+                    if (lane == 0) epi_wait_buffer(two_bufs);
                     __syncwarp();
 #pragma unroll
                     for (int c = 0; c < Cfg::EPI_COLS; ++c)
@@ -1276,12 +1297,12 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
                 // staged row
                 const int k0 = nt * NT + col0;
                 const int m0w = mt * MT + quad * 32;
-                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (uint32_t)(Cfg::EPI_BUFS * Cfg::EPI_BUF_BYTES);
+                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (uint32_t)(Cfg::EPI_ALLOC * Cfg::EPI_BUF_BYTES);
                 const uint32_t sw = ((uint32_t)prow >> 1) & 3u;
 #pragma unroll
                 for (int ch = 0; ch < HALF / 64; ++ch) {
-                    const uint32_t buf = ebase + (uint32_t)(ch % Cfg::EPI_BUFS) * Cfg::EPI_BUF_BYTES;
-                    if (lane == 0) ptx::bulk_wait_group_read<Cfg::EPI_BUFS - 1>();  // the store that last read buf is done
+                    const uint32_t buf = ebase + epi_buf_index(ch, two_bufs) * Cfg::EPI_BUF_BYTES;
+                    if (lane == 0) epi_wait_buffer(two_bufs);
                     __syncwarp();
                     const uint32_t rowaddr = buf + (uint32_t)prow * 64u;
 #pragma unroll
@@ -1318,12 +1339,12 @@ __device__ __forceinline__ void conv_cta(const IgemmArgs &a, const int bid, cons
                 constexpr int CHUNKS = Cfg::EPI_COLS / 4;  // 16-byte chunks per staged row
                 const int k0 = nt * NT + col0;
                 const int m0w = mt * MT + quad * 32;
-                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (uint32_t)(Cfg::EPI_BUFS * Cfg::EPI_BUF_BYTES);
+                const uint32_t ebase = epi_smem + (uint32_t)(warp - FIRST_EPI_WARP) * (uint32_t)(Cfg::EPI_ALLOC * Cfg::EPI_BUF_BYTES);
                 const uint32_t sw = CHUNKS == 8 ? ((uint32_t)prow & 7u) : (((uint32_t)prow >> 1) & 3u);
 #pragma unroll
                 for (int ch = 0; ch < HALF / Cfg::EPI_COLS; ++ch) {
-                    const uint32_t buf = ebase + (uint32_t)(ch % Cfg::EPI_BUFS) * Cfg::EPI_BUF_BYTES;
-                    if (lane == 0) ptx::bulk_wait_group_read<Cfg::EPI_BUFS - 1>();  // the store that last read buf is done
+                    const uint32_t buf = ebase + epi_buf_index(ch, two_bufs) * Cfg::EPI_BUF_BYTES;
+                    if (lane == 0) epi_wait_buffer(two_bufs);
                     __syncwarp();
                     const int i0 = ch * Cfg::EPI_COLS;
                     const uint32_t rowaddr = buf + (uint32_t)prow * (uint32_t)(Cfg::EPI_COLS * 4);
