@@ -1676,6 +1676,74 @@ __global__ void igemm_pack_image_kernel(const int8_t *x, int64_t xs0, int64_t xs
     }
 }
 
+// The same copy for an image whose images (the batch index) are adjacent
+// bytes, stride 1: the weight gradient's image, a channels-last image with
+// its batch and channels exchanged.  A block takes 64 images x 64 channels
+// of one pixel: 16-byte loads of 64 consecutive images per channel (four
+// threads per channel), a transpose through shared memory, and 16-byte
+// stores of 16 channels per image (four threads per image's 64 channels).
+// Needs 16-byte aligned channel and pixel strides and base; channels from C
+// up to c16 are zero.
+constexpr int kBmPitch = 68;  // bytes per shared channel row (64 images + 4)
+
+__global__ void __launch_bounds__(256) igemm_pack_image_batch_minor_kernel(
+    const int8_t *x, int64_t xs1, int64_t xs2, int64_t xs3, int64_t N, int32_t C, int32_t H, int32_t W,
+    int32_t row0, int32_t row_step, int32_t c16, int8_t *xp) {
+    ptx::launch_dependents();
+    __shared__ __align__(16) uint8_t tile[64 * kBmPitch];
+    const int t = threadIdx.x;
+    const int64_t nblocks = (N + 63) / 64;
+    const int cblocks = (c16 + 63) / 64;
+    const int64_t pixels = (int64_t)H * W;
+    const int64_t total = nblocks * pixels * cblocks;
+    for (int64_t b = blockIdx.x; b < total; b += gridDim.x) {
+        const int cb = (int)(b % cblocks);
+        const int64_t pb = b / cblocks;
+        const int64_t pix = pb % pixels;
+        const int64_t n0 = (pb / pixels) * 64;
+        const int h = (int)(pix / W), w = (int)(pix - (int64_t)(pix / W) * W);
+        // load: channel cl = t / 4, images n0 + 16q .. +15
+        {
+            const int cl = t >> 2, q = t & 3;
+            const int c = cb * 64 + cl;
+            const int64_t n = n0 + 16 * q;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (c < C) {
+                const int8_t *src = x + (int64_t)c * xs1 + (int64_t)(row0 + (int64_t)row_step * h) * xs2 +
+                                    (int64_t)w * xs3 + n;
+                if (n + 16 <= N) {
+                    v = __ldg(reinterpret_cast<const uint4 *>(src));
+                } else {
+                    uint32_t wd[4] = {0, 0, 0, 0};
+                    for (int e = 0; e < 16 && n + e < N; ++e) wd[e >> 2] |= (uint32_t)(uint8_t)src[e] << (8 * (e & 3));
+                    v = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+                }
+            }
+            uint32_t *row = reinterpret_cast<uint32_t *>(tile + cl * kBmPitch + 16 * q);
+            row[0] = v.x; row[1] = v.y; row[2] = v.z; row[3] = v.w;
+        }
+        __syncthreads();
+        // store: image nl = t / 4, channels cb*64 + 16cq .. +15
+        {
+            const int nl = t >> 2, cq = t & 3;
+            const int64_t n = n0 + nl;
+            const int c0 = cb * 64 + 16 * cq;
+            if (n < N && c0 < c16) {
+                uint32_t wd[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    uint32_t word = 0;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) word |= (uint32_t)tile[(16 * cq + 4 * e + k) * kBmPitch + nl] << (8 * k);
+                    wd[e] = word;
+                }
+                *reinterpret_cast<uint4 *>(xp + (n * pixels + pix) * c16 + c0) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+            }
+        }
+        __syncthreads();
+    }
+}
+
 // The same copy for images whose channels each hold their H x W pixels in one
 // contiguous plane (NCHW-like, 16-byte aligned planes, H*W a multiple of 16):
 // a transpose through shared memory.  A block takes 64 channels x 256 pixels
@@ -2310,6 +2378,14 @@ bool planes_copy(const ConvGeom &g0, const IgemmPlan &pl, const int8_t *x) {
            (pl.row_step == 1 || g0.W % 16 == 0);
 }
 
+// Whether the image's images are adjacent bytes (batch stride 1, as in the
+// weight gradient's exchanged view of a channels-last image) with 16-byte
+// aligned channel and pixel strides and base: igemm_pack_image_batch_minor_kernel.
+bool batch_minor_copy(const ConvGeom &g0, const int8_t *x) {
+    return (g0.N == 1 || g0.xs[0] == 1) && g0.xs[1] % 16 == 0 && g0.xs[2] % 16 == 0 && g0.xs[3] % 16 == 0 &&
+           ((uintptr_t)x % 16) == 0 && g0.H * g0.W < ((int64_t)1 << 31);
+}
+
 // 4-D map {C, S, R, K} of an int8 filter with contiguous channels (byte
 // strides ws[3], ws[2], ws[0]): box {64, 1, 1, NT}, the k-step's int8 tile,
 // no swizzle (the converters read 64-byte rows).
@@ -2459,6 +2535,12 @@ conv_status igemm_pack_image_launch(const ConvGeom &g, const IgemmPlan &pl, cons
         int64_t blocks = total < (int64_t)sms * 8 ? total : (int64_t)sms * 8;
         igemm_pack_image_planes_kernel<<<(unsigned)blocks, 256, 0, st>>>(
             x, g.xs[0], g.xs[1], g.N, (int32_t)g.C, (int32_t)hwp, (int32_t)g.W, (int32_t)pl.row0,
+            (int32_t)pl.row_step, (int32_t)pl.c16, xp);
+    } else if (batch_minor_copy(g, x)) {
+        const int64_t total = ((g.N + 63) / 64) * hwp * ((pl.c16 + 63) / 64);
+        const int64_t blocks = total < (int64_t)sms * 16 ? total : (int64_t)sms * 16;
+        igemm_pack_image_batch_minor_kernel<<<(unsigned)blocks, 256, 0, st>>>(
+            x, g.xs[1], g.xs[2], g.xs[3], g.N, (int32_t)g.C, (int32_t)pl.hp, (int32_t)g.W, (int32_t)pl.row0,
             (int32_t)pl.row_step, (int32_t)pl.c16, xp);
     } else {
         const int64_t total = g.N * pl.hp * g.W * (pl.c16 / 16);
