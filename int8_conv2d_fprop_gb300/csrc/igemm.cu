@@ -1513,6 +1513,76 @@ __global__ void igemm_pack_filter_kernel(const __grid_constant__ PackFilterJob j
         pack_filter_item<kWide>(jb, idx);
 }
 
+// Shared tiles of the transposing copies below: 64 rows of 64 bytes, 4 bytes
+// of padding per row.
+constexpr int kBmPitch = 68;
+
+// The same repack for a filter whose output channels are adjacent bytes (K
+// stride 1: the weight gradient's loss gradient as its filter, a data
+// gradient's exchanged filter): a block takes 64 rows (output channels) x
+// the 64 channels of one k-step, by 16-byte loads of 64 consecutive rows per
+// channel (four threads per channel), a transpose through shared memory,
+// and 16-byte stores of 8 f16 channels per row into the pre-swizzled block.
+// Needs 16-byte aligned channel, tap-row and tap strides and base; rows past
+// K and channels past C are zeros.
+__global__ void __launch_bounds__(256) igemm_pack_filter_k_minor_kernel(const __grid_constant__ PackFilterJob jb) {
+    ptx::launch_dependents();
+    __shared__ __align__(16) uint8_t tile[64 * kBmPitch];
+    const int t = threadIdx.x;
+    const int row_blocks = jb.nt_rows / 64;
+    const int64_t total = (int64_t)jb.n_tiles * jb.k_steps * row_blocks;
+    for (int64_t b = blockIdx.x; b < total; b += gridDim.x) {
+        const int rb = (int)(b % row_blocks);
+        const int64_t t2 = b / row_blocks;  // block index nt * k_steps + j
+        const int nt = (int)(t2 / jb.k_steps);
+        const int j = (int)(t2 - (int64_t)nt * jb.k_steps);
+        const int tap = j / jb.c_steps;
+        const int cb = j - tap * jb.c_steps;
+        const int r = tap / jb.S, s = tap - (tap / jb.S) * jb.S;
+        const int rf = jb.mode ? jb.R - 1 - r : r;
+        const int sf = jb.mode ? jb.S - 1 - s : s;
+        const int k0 = nt * jb.nt_rows + rb * 64;
+        {
+            const int cl = t >> 2, q = t & 3;
+            const int c = cb * KS + cl;
+            const int k = k0 + 16 * q;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (c < jb.C) {
+                const int8_t *src = jb.w + (int64_t)c * jb.ws1 + (int64_t)rf * jb.ws2 + (int64_t)sf * jb.ws3 + k;
+                if (k + 16 <= jb.K) {
+                    v = __ldg(reinterpret_cast<const uint4 *>(src));
+                } else {
+                    uint32_t wd[4] = {0, 0, 0, 0};
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        if (k + e < jb.K) wd[e >> 2] |= (uint32_t)(uint8_t)src[e] << (8 * (e & 3));
+                    v = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+                }
+            }
+            uint32_t *row = reinterpret_cast<uint32_t *>(tile + cl * kBmPitch + 16 * q);
+            row[0] = v.x; row[1] = v.y; row[2] = v.z; row[3] = v.w;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int item = t + 256 * i;
+            const int nl = rb * 64 + (item >> 3), chunk = item & 7;
+            uint32_t words[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int c0 = chunk * 8 + 2 * e;
+                const int v0 = (int8_t)tile[c0 * kBmPitch + (item >> 3)];
+                const int v1 = (int8_t)tile[(c0 + 1) * kBmPitch + (item >> 3)];
+                words[e] = (uint32_t)__half_as_ushort(__int2half_rn(v0)) |
+                           ((uint32_t)__half_as_ushort(__int2half_rn(v1)) << 16);
+            }
+            uint8_t *dst = jb.wp + ((t2 * jb.nt_rows + nl) * 128) + ((chunk ^ (nl & 7)) << 4);
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
+        }
+        __syncthreads();
+    }
+}
+
 // Several repacks in one launch (the residue classes of a data gradient):
 // the items of job i are end[i-1] .. end[i]-1 of the grid walk.
 struct PackFilterJobs {
@@ -1684,7 +1754,6 @@ __global__ void igemm_pack_image_kernel(const int8_t *x, int64_t xs0, int64_t xs
 // stores of 16 channels per image (four threads per image's 64 channels).
 // Needs 16-byte aligned channel and pixel strides and base; channels from C
 // up to c16 are zero.
-constexpr int kBmPitch = 68;  // bytes per shared channel row (64 images + 4)
 
 __global__ void __launch_bounds__(256) igemm_pack_image_batch_minor_kernel(
     const int8_t *x, int64_t xs1, int64_t xs2, int64_t xs3, int64_t N, int32_t C, int32_t H, int32_t W,
@@ -1715,7 +1784,9 @@ __global__ void __launch_bounds__(256) igemm_pack_image_batch_minor_kernel(
                     v = __ldg(reinterpret_cast<const uint4 *>(src));
                 } else {
                     uint32_t wd[4] = {0, 0, 0, 0};
-                    for (int e = 0; e < 16 && n + e < N; ++e) wd[e >> 2] |= (uint32_t)(uint8_t)src[e] << (8 * (e & 3));
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        if (n + e < N) wd[e >> 2] |= (uint32_t)(uint8_t)src[e] << (8 * (e & 3));
                     v = make_uint4(wd[0], wd[1], wd[2], wd[3]);
                 }
             }
@@ -2233,7 +2304,13 @@ conv_status igemm_pack_filter_launch(const ConvGeom &g, const IgemmPlan &pl, con
     int64_t blocks = (total + 255) / 256;
     if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
     if (blocks == 0) return CONV_OK;
-    if (total >= ((int64_t)1 << 31))
+    if (!pl.nchw_rows && (g.K == 1 || g.ws[0] == 1) && g.ws[1] % 16 == 0 && g.ws[2] % 16 == 0 && g.ws[3] % 16 == 0 &&
+        ((uintptr_t)w % 16) == 0) {
+        // output channels adjacent: the transposing repack
+        const int64_t tb = pl.n_tiles * pl.k_steps * (pl.n_tile / 64);
+        igemm_pack_filter_k_minor_kernel<<<(unsigned)(tb < (int64_t)sms * 16 ? tb : (int64_t)sms * 16), 256, 0, st>>>(
+            pack_job(g, pl, w, wp));
+    } else if (total >= ((int64_t)1 << 31))
         igemm_pack_filter_kernel<true><<<(unsigned)blocks, 256, 0, st>>>(pack_job(g, pl, w, wp));
     else
         igemm_pack_filter_kernel<false><<<(unsigned)blocks, 256, 0, st>>>(pack_job(g, pl, w, wp));
