@@ -78,6 +78,10 @@ CASES = [
     # all of them then read one shared channels-last copy
     G("s2_nchw_mixed_classes", 2, 32, 16, 32, 48, 3, 3, (1, 1), (1, 1), stride=(2, 2), layout="NCHW",
       tensor=True),
+    # a batch of 70 (the weight gradient's channels: two channel steps, 80
+    # bytes per pixel of its image copy, images (C = 80) in a full and a
+    # ragged block of 64) and K = 48 rows of the repacked loss gradient
+    G("batch70_c80_k48", 70, 80, 6, 7, 48, 3, 3, (1, 1), (1, 1), tensor=True),
 ]
 
 
