@@ -356,11 +356,15 @@ conv_status conv_fprop_static_workspace(const conv_tensor_desc *x, const int8_t 
  * More than 64 classes take the CUDA-core kernel.  conv_wgrad runs on the
  * tensor cores as a forward convolution of the image (batch and channel
  * dims exchanged) by dY (its batch as channels, its pixels as taps) when the
- * tensor-core kernel can express it.  Those routes need the workspace the
+ * tensor-core kernel can express it; with a batch of at most 32 it folds T
+ * = min(64 / N, Q, 8) columns of dY into the channels, reading a copy of
+ * the image T times its size.  Those routes need the workspace the
  * *_workspace_size call reports (256-byte aligned, caller-owned; for dgrad
  * it holds every class's filter repacked to f16 blocks, for wgrad dY
- * repacked to f16 blocks, about 2*K*P*Q*ceil(N/64)*64 bytes, plus the int32
- * partial sums of the reduction split over the SMs).  Other calls, and algo
+ * repacked to f16 blocks, about 2*K*P*ceil(Q/T)*64 bytes (T = 1 unfolded,
+ * times ceil(N/64)), plus the int32 partial sums of the reduction split over
+ * the SMs, plus the folded image copy, C*H*U*ceil(T*N/16)*16 bytes with U
+ * about T*stride_w*ceil(Q/T) + dilation_w*(S-1)).  Other calls, and algo
  * DIRECT_GENERIC, run CUDA-core kernels and need none; IMPLICIT_GEMM on a
  * call that cannot take the tensor cores returns CONV_ERR_ALIGNMENT.
  * Pointers are device pointers on the current device, outputs must not

@@ -28,7 +28,10 @@
 //    dilation exchanged, and whose [C][K][R][S] output is dW with its first
 //    two dims exchanged (taps written backwards in CONVOLUTION mode).  Its
 //    few output tiles have long reductions (N*P*Q), which the tensor-core
-//    kernel cuts into runs over the SMs and adds back up.
+//    kernel cuts into runs over the SMs and adds back up.  With a batch of
+//    N <= 32 (N of each k-step's 64 channels), T columns of dY are folded
+//    into the channels (channel t*N + n) against a copy of the image T
+//    times its size: the same products in T times fewer k-steps.
 //  * otherwise (or with DIRECT_GENERIC): a CUDA-core kernel, one warp per dW
 //    element, the lanes splitting the n, p, q sum (int32 partial sums, exact
 //    by the validator's bound, added across the warp with shuffles).
@@ -329,14 +332,77 @@ bool wgrad_as_fprop(const conv_tensor_desc *x, const conv_tensor_desc *dy, const
     return blocks * 256 * 128 <= ((int64_t)4 << 30);
 }
 
+// The folded weight gradient (see WgradFold): with a batch of N <= 32 the
+// forward convolution above fills only N of each k-step's 64 channels.
+// Folding T = min(64 / N, Q, 8) output columns of dY into the channels
+// (channel t*N + n) turns the Q taps along W into Q2 = ceil(Q / T), read
+// from a copy X'' of the image in which channel t*N + n of column u is
+// X[n, c, h, u - pre_w + t*stride_w]: the same products, T times fewer
+// k-steps, for a copy T times the image.  Along W the folded convolution has
+// no padding (X'' starts at the padded origin), the tap q2 at dilation
+// T*stride_w and the output column s at stride dilation_w; along H it is
+// the convolution above.  Returns false (no folding) where it does not
+// apply or does not fit.
+bool wgrad_fold(const conv_tensor_desc *x, const conv_tensor_desc *dy, const conv_fprop_params *p,
+                const ConvGeom &g, ConvGeom *g2, WgradFold *f) {
+    const int64_t N = x->dims[0], Q = dy->dims[3];
+    if (N < 1 || N > 32) return false;
+    int64_t T = 64 / N;
+    if (T > Q) T = Q;
+    if (T > 8) T = 8;
+    if (T < 2) return false;
+    std::memset(f, 0, sizeof(*f));
+    unit_strides(x, f->xs);
+    unit_strides(dy, f->ys);
+    f->N = N; f->C = x->dims[1]; f->H = x->dims[2]; f->W = x->dims[3];
+    f->K = dy->dims[1]; f->P = dy->dims[2]; f->Q = Q;
+    f->T = T;
+    f->Q2 = (Q + T - 1) / T;
+    f->c16 = (T * N + 15) / 16 * 16;
+    f->pre_w = p->pre_padding[1];
+    f->stride_w = p->stride[1];
+    const int64_t S = g.Q;  // dW's columns: the forward convolution's output columns
+    f->U = T * f->stride_w * (f->Q2 - 1) + p->dilation[1] * (S - 1) + 1;
+    if (f->U >= ((int64_t)1 << 30) || f->C * f->H * f->U * f->c16 > ((int64_t)4 << 30)) return false;
+    *g2 = g;
+    g2->C = f->c16;
+    g2->W = f->U;
+    g2->xs[0] = f->H * f->U * f->c16; g2->xs[1] = 1; g2->xs[2] = f->U * f->c16; g2->xs[3] = f->c16;
+    g2->S = f->Q2;
+    g2->ws[0] = f->P * f->Q2 * f->c16; g2->ws[1] = 1; g2->ws[2] = f->Q2 * f->c16; g2->ws[3] = f->c16;
+    g2->pad_w = 0;
+    g2->dil_w = T * f->stride_w;
+    return igemm_supported(*g2);
+}
+
 conv_status plan_wgrad(const conv_tensor_desc *x, const void *x_dev, const conv_tensor_desc *dy,
                        const conv_tensor_desc *dw, const conv_fprop_params *p, ConvGeom *g, int64_t *y_origin,
-                       bool *tensor, IgemmPlan *pl) {
+                       bool *tensor, IgemmPlan *pl, WgradFold *fold, size_t *ws_bytes) {
     conv_status st = validate_wgrad(x, dy, dw, p);
     if (st) return st;
     *tensor = p->algo != CONV_ALGO_DIRECT_GENERIC && wgrad_as_fprop(x, dy, dw, p, g, y_origin);
     if (p->algo == CONV_ALGO_IMPLICIT_GEMM && !*tensor) return CONV_ERR_ALIGNMENT;
-    if (*tensor) igemm_plan(*g, x_dev, pl);
+    fold->T = 1;
+    *ws_bytes = 0;
+    if (!*tensor) return CONV_OK;
+    ConvGeom g2;
+    WgradFold f;
+    if (wgrad_fold(x, dy, p, *g, &g2, &f)) {
+        IgemmPlan pl2;
+        igemm_plan(g2, nullptr, &pl2);
+        // the copy is read in place (channels-last, 16-byte aligned) with one
+        // channel step per tap
+        if (!pl2.pack_x && !pl2.nchw_rows && !pl2.register_loads && pl2.c_steps == 1) {
+            *g = g2;
+            *pl = pl2;
+            *fold = f;
+            *ws_bytes = ((pl2.workspace_bytes + 255) & ~(size_t)255) +
+                        (size_t)(f.C * f.H * f.U * f.c16);
+            return CONV_OK;
+        }
+    }
+    igemm_plan(*g, x_dev, pl);
+    *ws_bytes = pl->workspace_bytes;
     return CONV_OK;
 }
 
@@ -609,11 +675,13 @@ conv_status conv_wgrad_workspace_size(const conv_tensor_desc *x, const conv_tens
     if (!bytes) return CONV_ERR_NULL_PTR;
     ConvGeom g;
     IgemmPlan pl;
+    WgradFold fold;
+    size_t need = 0;
     int64_t origin = 0;
     bool tensor = false;
-    conv_status st = plan_wgrad(x, nullptr, dy, dw, p, &g, &origin, &tensor, &pl);
+    conv_status st = plan_wgrad(x, nullptr, dy, dw, p, &g, &origin, &tensor, &pl, &fold, &need);
     if (st) return st;
-    *bytes = (tensor && g.N > 0 && g.K > 0) ? pl.workspace_bytes : 0;
+    *bytes = (tensor && g.N > 0 && g.K > 0) ? need : 0;
     return CONV_OK;
 }
 
@@ -622,9 +690,11 @@ conv_status conv_wgrad(const conv_tensor_desc *x, const int8_t *x_dev, const con
                        const conv_fprop_params *p, void *workspace, size_t workspace_bytes, void *stream) {
     ConvGeom g;
     IgemmPlan pl;
+    WgradFold fold;
+    size_t need = 0;
     int64_t origin = 0;
     bool tensor = false;
-    conv_status st = plan_wgrad(x, x_dev, dy, dw, p, &g, &origin, &tensor, &pl);
+    conv_status st = plan_wgrad(x, x_dev, dy, dw, p, &g, &origin, &tensor, &pl, &fold, &need);
     if (st) return st;
     // an empty batch reads neither input: only the gradient must be given
     const bool empty_batch = x->dims[0] == 0;
@@ -637,11 +707,19 @@ conv_status conv_wgrad(const conv_tensor_desc *x, const int8_t *x_dev, const con
     if ((st = check_device())) return st;
     // an empty batch gives an all-zero gradient (the CUDA-core kernel writes it)
     if (tensor && x->dims[0] > 0) {
-        if (!workspace || workspace_bytes < pl.workspace_bytes || ((uintptr_t)workspace % 256) != 0)
-            return CONV_ERR_WORKSPACE;
-        if (overlaps(workspace, pl.workspace_bytes, x_dev, (uint64_t)desc_extent_elems(x)) ||
-            overlaps(workspace, pl.workspace_bytes, dy_dev, (uint64_t)desc_extent_elems(dy)))
+        if (!workspace || workspace_bytes < need || ((uintptr_t)workspace % 256) != 0) return CONV_ERR_WORKSPACE;
+        if (overlaps(workspace, need, x_dev, (uint64_t)desc_extent_elems(x)) ||
+            overlaps(workspace, need, dy_dev, (uint64_t)desc_extent_elems(dy)))
             return CONV_ERR_OVERLAP;
+        if (fold.T > 1) {
+            // the copy X'' after the folded convolution's own workspace; the
+            // convolution reads the filter blocks the fold repacked
+            int8_t *x2 = static_cast<int8_t *>(workspace) + ((pl.workspace_bytes + 255) & ~(size_t)255);
+            fold.x = x_dev;
+            fold.dy = dy_dev;
+            if ((st = igemm_wgrad_fold_launch(fold, pl, x2, workspace, stream))) return st;
+            return igemm_main_launch(g, pl, x2, nullptr, dw_dev + origin, nullptr, workspace, stream, false);
+        }
         return igemm_main_launch(g, pl, x_dev, dy_dev, dw_dev + origin, nullptr, workspace, stream, true);
     }
     GradArgs a = grad_args(x, dw, dy, p);

@@ -1583,6 +1583,140 @@ __global__ void __launch_bounds__(256) igemm_pack_filter_k_minor_kernel(const __
     }
 }
 
+// The weight gradient folded over T output columns (see WgradFold): the
+// image copy X'' and the folded loss-gradient repack, each a transpose
+// through a shared tile of 64 x 64 bytes like the two kernels above.
+struct WgradFoldArgs {
+    const int8_t *x;
+    int64_t xs0, xs1, xs2, xs3;
+    const int8_t *dy;
+    int64_t ys0, ys1, ys2, ys3;
+    int64_t N, C, H, W, K, P, Q, T, Q2, U, c16, pre_w, stride_w;
+    int32_t x_vec, dy_vec;  // 16-byte loads allowed (unit stride along the loaded run, aligned)
+    int32_t nt_rows, n_tiles, k_steps;
+    int8_t *x2;
+    uint8_t *wp;
+};
+
+// Block (image block cb of 64 images c, row h, column u): tile[ch][c] holds
+// X''[c][h][u][ch] for the block's images.
+__global__ void __launch_bounds__(256) igemm_wgrad_fold_image_kernel(const __grid_constant__ WgradFoldArgs f) {
+    ptx::launch_dependents();
+    __shared__ __align__(16) uint8_t tile[64 * kBmPitch];
+    const int t = threadIdx.x;
+    const int64_t cblocks = (f.C + 63) / 64;
+    const int64_t total = cblocks * f.H * f.U;
+    const int64_t tn = f.T * f.N;
+    for (int64_t b = blockIdx.x; b < total; b += gridDim.x) {
+        const int64_t u = b % f.U;
+        const int64_t t2 = b / f.U;
+        const int64_t h = t2 % f.H;
+        const int64_t c0 = (t2 / f.H) * 64;
+        {
+            const int ch = t >> 2, q = t & 3;
+            const int64_t c = c0 + 16 * q;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (ch < tn && ch < f.c16) {
+                const int64_t n = ch % f.N, tt = ch / f.N;
+                const int64_t w = u - f.pre_w + tt * f.stride_w;
+                if (w >= 0 && w < f.W && c < f.C) {
+                    const int8_t *src = f.x + n * f.xs0 + c * f.xs1 + h * f.xs2 + w * f.xs3;
+                    if (f.x_vec && c + 16 <= f.C) {
+                        v = __ldg(reinterpret_cast<const uint4 *>(src));
+                    } else {
+                        uint32_t wd[4] = {0, 0, 0, 0};
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            if (c + e < f.C) wd[e >> 2] |= (uint32_t)(uint8_t)src[e * f.xs1] << (8 * (e & 3));
+                        v = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+                    }
+                }
+            }
+            uint32_t *row = reinterpret_cast<uint32_t *>(tile + ch * kBmPitch + 16 * q);
+            row[0] = v.x; row[1] = v.y; row[2] = v.z; row[3] = v.w;
+        }
+        __syncthreads();
+        {
+            const int cl = t >> 2, cq = t & 3;
+            const int64_t c = c0 + cl;
+            if (c < f.C && 16 * cq < f.c16) {
+                uint32_t wd[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    uint32_t word = 0;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) word |= (uint32_t)tile[(16 * cq + 4 * e + k) * kBmPitch + cl] << (8 * k);
+                    wd[e] = word;
+                }
+                *reinterpret_cast<uint4 *>(f.x2 + ((c * f.H + h) * f.U + u) * f.c16 + 16 * cq) =
+                    make_uint4(wd[0], wd[1], wd[2], wd[3]);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// Block (n-tile nt, k-step j = tap (p, q2), row block rb of 64 output
+// channels k): tile[ch][k] holds the folded loss gradient's channel ch, and
+// the block's 64 pre-swizzled f16 rows are written from it.
+__global__ void __launch_bounds__(256) igemm_wgrad_fold_filter_kernel(const __grid_constant__ WgradFoldArgs f) {
+    ptx::launch_dependents();
+    __shared__ __align__(16) uint8_t tile[64 * kBmPitch];
+    const int t = threadIdx.x;
+    const int row_blocks = f.nt_rows / 64;
+    const int64_t total = (int64_t)f.n_tiles * f.k_steps * row_blocks;
+    const int64_t tn = f.T * f.N;
+    for (int64_t b = blockIdx.x; b < total; b += gridDim.x) {
+        const int rb = (int)(b % row_blocks);
+        const int64_t t2 = b / row_blocks;  // block index nt * k_steps + j
+        const int64_t nt = t2 / f.k_steps;
+        const int64_t j = t2 - nt * f.k_steps;
+        const int64_t p = j / f.Q2, q2 = j - (j / f.Q2) * f.Q2;
+        const int64_t k0 = nt * f.nt_rows + rb * 64;
+        {
+            const int ch = t >> 2, q = t & 3;
+            const int64_t k = k0 + 16 * q;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (ch < tn && ch < f.c16) {
+                const int64_t n = ch % f.N, qq = f.T * q2 + ch / f.N;
+                if (qq < f.Q && k < f.K) {
+                    const int8_t *src = f.dy + n * f.ys0 + k * f.ys1 + p * f.ys2 + qq * f.ys3;
+                    if (f.dy_vec && k + 16 <= f.K) {
+                        v = __ldg(reinterpret_cast<const uint4 *>(src));
+                    } else {
+                        uint32_t wd[4] = {0, 0, 0, 0};
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            if (k + e < f.K) wd[e >> 2] |= (uint32_t)(uint8_t)src[e * f.ys1] << (8 * (e & 3));
+                        v = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+                    }
+                }
+            }
+            uint32_t *row = reinterpret_cast<uint32_t *>(tile + ch * kBmPitch + 16 * q);
+            row[0] = v.x; row[1] = v.y; row[2] = v.z; row[3] = v.w;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int item = t + 256 * i;
+            const int64_t nl = rb * 64 + (item >> 3);
+            const int chunk = item & 7;
+            uint32_t words[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int c0 = chunk * 8 + 2 * e;
+                const int v0 = (int8_t)tile[c0 * kBmPitch + (item >> 3)];
+                const int v1 = (int8_t)tile[(c0 + 1) * kBmPitch + (item >> 3)];
+                words[e] = (uint32_t)__half_as_ushort(__int2half_rn(v0)) |
+                           ((uint32_t)__half_as_ushort(__int2half_rn(v1)) << 16);
+            }
+            uint8_t *dst = f.wp + ((t2 * f.nt_rows + nl) * 128) + ((chunk ^ (int)(nl & 7)) << 4);
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(words[0], words[1], words[2], words[3]);
+        }
+        __syncthreads();
+    }
+}
+
 // Several repacks in one launch (the residue classes of a data gradient):
 // the items of job i are end[i-1] .. end[i]-1 of the grid walk.
 struct PackFilterJobs {
@@ -2314,6 +2448,40 @@ conv_status igemm_pack_filter_launch(const ConvGeom &g, const IgemmPlan &pl, con
         igemm_pack_filter_kernel<true><<<(unsigned)blocks, 256, 0, st>>>(pack_job(g, pl, w, wp));
     else
         igemm_pack_filter_kernel<false><<<(unsigned)blocks, 256, 0, st>>>(pack_job(g, pl, w, wp));
+    return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
+}
+
+conv_status igemm_wgrad_fold_launch(const WgradFold &fd, const IgemmPlan &pl, int8_t *x2, void *workspace,
+                                    void *stream) {
+    cudaStream_t st = (cudaStream_t)stream;
+    const int sms = device_sm_count();
+    WgradFoldArgs f;
+    std::memset(&f, 0, sizeof(f));
+    f.x = fd.x; f.xs0 = fd.xs[0]; f.xs1 = fd.xs[1]; f.xs2 = fd.xs[2]; f.xs3 = fd.xs[3];
+    f.dy = fd.dy; f.ys0 = fd.ys[0]; f.ys1 = fd.ys[1]; f.ys2 = fd.ys[2]; f.ys3 = fd.ys[3];
+    f.N = fd.N; f.C = fd.C; f.H = fd.H; f.W = fd.W; f.K = fd.K; f.P = fd.P; f.Q = fd.Q;
+    f.T = fd.T; f.Q2 = fd.Q2; f.U = fd.U; f.c16 = fd.c16; f.pre_w = fd.pre_w; f.stride_w = fd.stride_w;
+    // 16-byte loads of 16 consecutive images (channels of X) or rows (K of dY)
+    f.x_vec = (fd.C == 1 || fd.xs[1] == 1) && fd.xs[0] % 16 == 0 && fd.xs[2] % 16 == 0 && fd.xs[3] % 16 == 0 &&
+                      ((uintptr_t)fd.x % 16) == 0
+                  ? 1
+                  : 0;
+    f.dy_vec = (fd.K == 1 || fd.ys[1] == 1) && fd.ys[0] % 16 == 0 && fd.ys[2] % 16 == 0 && fd.ys[3] % 16 == 0 &&
+                       ((uintptr_t)fd.dy % 16) == 0
+                   ? 1
+                   : 0;
+    f.nt_rows = (int32_t)pl.n_tile;
+    f.n_tiles = (int32_t)pl.n_tiles;
+    f.k_steps = (int32_t)pl.k_steps;
+    f.x2 = x2;
+    f.wp = static_cast<uint8_t *>(workspace);
+    const int64_t xb = ((fd.C + 63) / 64) * fd.H * fd.U;
+    const int64_t wb = pl.n_tiles * pl.k_steps * (pl.n_tile / 64);
+    if (xb > 0)
+        igemm_wgrad_fold_image_kernel<<<(unsigned)(xb < (int64_t)sms * 16 ? xb : (int64_t)sms * 16), 256, 0, st>>>(f);
+    if (wb > 0)
+        igemm_wgrad_fold_filter_kernel<<<(unsigned)(wb < (int64_t)sms * 16 ? wb : (int64_t)sms * 16), 256, 0, st>>>(
+            f);
     return cudaGetLastError() == cudaSuccess ? CONV_OK : CONV_ERR_CUDA;
 }
 

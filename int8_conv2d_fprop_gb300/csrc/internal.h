@@ -145,6 +145,28 @@ conv_status igemm_pack_image_launch(const ConvGeom &g, const IgemmPlan &pl, cons
 // not wait for the repack to end.
 conv_status igemm_main_launch(const ConvGeom &g, const IgemmPlan &pl, const int8_t *x, const int8_t *w, void *y,
                               const int32_t *bias, void *workspace, void *stream, bool repack);
+// The weight gradient folded over T output columns of dY (grad.cu): X'' is
+// the image copy [C][H][U][c16] with X''[c][h][u][t*N + n] =
+// X[n, c, h, u - pre_w + t*stride_w] (zero outside X and for channels from
+// T*N on), and the folded loss gradient the filter [K][P][Q2][c16] with
+// channel t*N + n of tap (p, q2) = dY[n, k, p, T*q2 + t] (zero for columns
+// from Q on), repacked into the filter blocks of pl (the plan of the folded
+// forward convolution: one channel step per tap).  Strides in elements
+// (bytes).
+struct WgradFold {
+    const int8_t *x;
+    int64_t xs[4];  // X [N][C][H][W]
+    const int8_t *dy;
+    int64_t ys[4];  // dY [N][K][P][Q]
+    int64_t N, C, H, W, K, P, Q;
+    int64_t T, Q2, U, c16;
+    int64_t pre_w, stride_w;
+};
+// Launches the copy into x2 (c16 * C * H * U bytes) and the repack into the
+// workspace's filter part.
+conv_status igemm_wgrad_fold_launch(const WgradFold &f, const IgemmPlan &pl, int8_t *x2, void *workspace,
+                                    void *stream);
+
 // Whether the 128- and 192-column tensor-memory kernels convert this
 // call's filter themselves (channels contiguous, 16-byte aligned strides and
 // pointer; w == nullptr: a 16-byte aligned pointer assumed) instead of

@@ -394,9 +394,11 @@ def test_gradient_validation_and_routes(ic):
     p = ic.Params.make(padding=(1, 1))
     assert ic.dgrad_workspace_size(dy, w, dx, p) > 0          # tensor-core route
     # wgrad on the tensor cores: dY repacked as the filter of a forward
-    # convolution, one 128-channel tile (K = 32) x 14*14 taps x one channel
-    # step of 64 f16 (128 bytes)
-    assert ic.wgrad_workspace_size(x, dy, dw, p) >= 14 * 14 * 128 * 128
+    # convolution, its batch of 2 folded with T = 8 of its 14 columns into 16
+    # channels: one 128-channel tile (K = 32) x 14 x 2 taps x one channel
+    # step of 64 f16 (128 bytes), then the image copy X'' of 64 images x 14
+    # rows x 11 columns (8 * 1 * (2 - 1) + 1 * (3 - 1) + 1) x 16 channels
+    assert ic.wgrad_workspace_size(x, dy, dw, p) == 14 * 2 * 128 * 128 + 64 * 14 * 11 * 16
     assert ic.wgrad_workspace_size(x, dy, dw, ic.Params.make(padding=(1, 1), algo=ic.ALGO_DIRECT_GENERIC)) == 0
 
     def code(fn, *a):
