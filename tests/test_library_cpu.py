@@ -251,6 +251,33 @@ def test_tile_shape_query(ic):
     assert st == _code(ic, "CONV_ERR_NULL_PTR")
 
 
+def test_wgrad_fold_rule(ic):
+    """The weight gradient folds T = min(64 / N, Q, 8) columns of dY into the
+    channels for a batch N <= 32: its workspace is the folded filter blocks
+    (K rows per tile x P * ceil(Q / T) taps x 128 bytes) plus the image copy
+    X'' (C images x H rows x U columns x ceil(T*N / 16)*16 channels, U =
+    T*stride_w*(ceil(Q/T) - 1) + dilation_w*(S - 1) + 1); larger batches
+    keep one tap per k-step (their image copied channels-last with
+    ceil(N / 16)*16 channels).  One SM here: no split partial sums."""
+    def d(dtype, dims, layout):
+        return ic.TensorDesc.packed(dtype, dims, layout)
+
+    def ws(N, C, H, W, K):
+        x = d(ic.CONV_INT8, (N, C, H, W), "NHWC")
+        dy = d(ic.CONV_INT8, (N, K, H, W), "NHWC")
+        dw = d(ic.CONV_INT32, (K, C, 3, 3), "KRSC")
+        return ic.wgrad_workspace_size(x, dy, dw, ic.Params.make(padding=(1, 1)))
+
+    # the 3x3 workload: T = 2, 28 folded columns, 256-row tiles, U = 57
+    assert ws(32, 256, 56, 56, 256) == 56 * 28 * 256 * 128 + 256 * 56 * 57 * 64
+    # batch 33 and 40: unfolded, 14 x 14 taps of one 128-row tile
+    for n in (33, 40):
+        c16 = (n + 15) // 16 * 16
+        assert ws(n, 64, 14, 14, 32) == 14 * 14 * 128 * 128 + 64 * 14 * 14 * c16
+    # batch 5: T = 8 (not 12), two folded columns, 48 channels
+    assert ws(5, 64, 14, 14, 32) == 14 * 2 * 128 * 128 + 64 * 14 * 11 * 48
+
+
 @pytest.mark.parametrize("W,pre_w,dil_w,S,K,stride_w,in_place", [
     (96, 0, 1, 1, 192, 1, True),     # the 7x1 workload's rows: two output rows per tile
     (64, 0, 1, 1, 128, 1, True),
