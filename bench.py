@@ -800,8 +800,11 @@ def run_extension(args):
         bound = "tensor" if tensor else "alu"
         unit = "TFLOP/s" if tensor else "TOPS"
         peak = bf16 if tensor else 152 * IMAD_PER_SM_CLK * 2 * 2.07e9 / 1e12
-        extra["route"] = ("tensor cores (forward convolution of the image by dY, reduction split over the SMs)"
-                          if tensor else "CUDA cores")
+        n_batch, q_cols = cfg.y_dims[0], cfg.y_dims[3]
+        fold = min(64 // n_batch, q_cols, 8) if n_batch <= 32 else 1
+        extra["route"] = (("tensor cores (forward convolution of the image by dY, reduction split over the SMs"
+                           + (f"; {fold} columns of dY folded into the channels per k-step" if fold > 1 else "")
+                           + ")") if tensor else "CUDA cores")
 
     for i in range(args.warmup):
         call(i)
