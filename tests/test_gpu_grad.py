@@ -82,6 +82,10 @@ CASES = [
     # bytes per pixel of its image copy, images (C = 80) in a full and a
     # ragged block of 64) and K = 48 rows of the repacked loss gradient
     G("batch70_c80_k48", 70, 80, 6, 7, 48, 3, 3, (1, 1), (1, 1), tensor=True),
+    # a batch of 16 at stride 2: the weight gradient folds T = 4 of dY's 15
+    # columns per k-step (four folded columns, the last one short), tap
+    # dilation 8 along W over the image copy
+    G("batch16_s2_fold4", 16, 24, 12, 30, 40, 3, 3, (1, 1), (1, 1), stride=(2, 2), tensor=True),
 ]
 
 
